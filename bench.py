@@ -1,0 +1,366 @@
+"""KDA hot-path benchmark: chunked prefill + pooled decode on GB300.
+
+One step = one kda_chunk_fwd over the prefill workload (B=1, H=32, T=8192,
+dk=dv=128, bf16 q/k/v, fp32 g/beta, h0=0, C=64, out + final fp32 state) followed by
+one kda_decode_step over the decode workload (N=256, H=32, dk=dv=128, fp32 state
+pool of 1024 slots, fused RMSNorm + sigmoid gate).  `value` is prefill tokens/s
+(the metric's first half, timed on the prefill calls of the timed steps); decode
+steps/s is reported beside it.  Inputs are synthetic (seeded), resident in HBM and
+larger than L2 (prefill 404 MB, decode 1.07 GB of touched state), so no L2 flush
+is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference implementation this
+method has here) on the host cores, on the same workload and metric.
+Under torchrun (N > 1) every rank runs the same per-GPU workload (independent
+problems: weak scaling, no collective on the data path); timing is the max over
+ranks and value aggregates all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (bf16, H=32, dk=dv=128) + decode steps/s, % of roofline"
+PREFILL_BYTES_PER_TOKEN_HEAD = 3 * 2 * 128 + 4 * 128 + 4 + 2 * 128        # q,k,v bf16 + g fp32 + beta + out bf16
+PREFILL_FLOPS_PER_TOKEN_HEAD = 2 * (5 * 64 * 128 + 3 * 128 * 128)          # method's flop count at C=64, d=128
+DECODE_STATE_BYTES = 2 * 128 * 128 * 4                                    # read + write of one fp32 state
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    return world, rank, local
+
+
+def dist_max(value: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from gated_delta_rule_08_gb300 import binding, inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hbm_gbs, bf16_tflops, _, peak_kind = _peaks()
+
+    pcfg, dcfg = inputs.PREFILL, inputs.DECODE
+    P = inputs.prefill_inputs(pcfg, device=dev)
+    D = inputs.decode_inputs(dcfg, device=dev)
+    T, H = P["T_tot"], pcfg.H
+    out = torch.empty(T, H, pcfg.dv, device=dev, dtype=torch.bfloat16)
+    hT = torch.empty(1, H, pcfg.dk, pcfg.dv, device=dev, dtype=torch.float32)
+    ws = torch.empty(binding.kda_chunk_fwd_workspace_size(1, T, H, pcfg.dk, pcfg.dv), device=dev, dtype=torch.uint8)
+    dout = torch.empty(dcfg.N, dcfg.H, dcfg.dv, device=dev, dtype=torch.bfloat16)
+
+    def prefill():
+        binding.kda_chunk_fwd(P["q"], P["k"], P["v"], P["g"], P["beta"], out=out, hT=hT, workspace=ws)
+
+    def decode():
+        binding.kda_decode_step(D["q"], D["k"], D["v"], D["g"], D["beta"], D["state_pool"], D["slot_idx"], out=dout,
+                                gate=D["gate"], norm_weight=D["norm_weight"])
+
+    for _ in range(args.warmup):
+        prefill()
+        decode()
+    torch.cuda.synchronize()
+    assert binding.kda_get_device_error(dev) == 0
+
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    binding.kda_trace_enable(True)
+    binding.kda_trace_collect()  # drop anything recorded before the timed region
+    _barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            prefill()
+            ev[i][1].record(stream)
+            decode()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    _barrier(world)
+    trace = binding.kda_trace_collect()
+    binding.kda_trace_enable(False)
+    pre_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    pre_s = dist_max(sum(pre_ms) / 1e3, world)
+    dec_s = dist_max(sum(dec_ms) / 1e3, world)
+    step_s = dist_max(sum(a.elapsed_time(c) for a, _, c in ev) / 1e3, world)
+
+    value = aggregate(T * args.steps, world, pre_s)
+    dec_steps_per_s = aggregate(args.steps, world, dec_s)
+
+    # dominant prefill kernel: largest summed time among the prefill-side kernels
+    pre_k = {k: v for k, v in trace.items() if k != "kda_decode"}
+    dom = max(pre_k.items(), key=lambda kv: kv[1][1])
+    dom_ms = dom[1][1] / dom[1][0]
+    alg_bytes = PREFILL_BYTES_PER_TOKEN_HEAD * T * H
+    achieved = alg_bytes / (dom_ms * 1e-3) / 1e9
+    dec_launch = trace.get("kda_decode", (1, float("nan")))
+    dec_ms_k = dec_launch[1] / dec_launch[0]
+    dec_bytes = DECODE_STATE_BYTES * dcfg.N * dcfg.H + dcfg.N * dcfg.H * (3 * 2 * 128 + 4 * 128 + 4 + 2 * 128 + 2 * 128)
+    dec_achieved = dec_bytes / (dec_ms_k * 1e-3) / 1e9
+    pre_flops = PREFILL_FLOPS_PER_TOKEN_HEAD * T * H
+    launches = sum(v[0] for v in trace.values())
+
+    # end to end through the public API with host buffers: pinned H2D of this step's inputs,
+    # the call, D2H of the outputs, every step
+    host = {k: P[k].to("cpu").pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    dev_in = {k: torch.empty_like(P[k]) for k in host}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hT_h = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + hT_h.numel() * hT_h.element_size()
+
+    def e2e_step():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        binding.kda_chunk_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], out=out, hT=hT,
+                              workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        hT_h.copy_(hT, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    _barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = dist_max(e0.elapsed_time(e1) / 1e3, world)
+    e2e_value = aggregate(T * args.steps, world, e2e_s)
+    assert binding.kda_get_device_error(dev) == 0
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3 / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), beta=sigmoid(N), g=-5*sigmoid(N))",
+        "config": {"workload": "prefill B=1 H=32 T=8192 dk=dv=128 C=64 bf16, h0=0, out+hT; then decode N=256 "
+                               "H=32 dk=dv=128 pool=1024 fp32 slots, RMSNorm+gate",
+                   "prefill_ms_per_step": round(pre_s * 1e3 / args.steps, 4),
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "decode": {"steps_per_s": round(dec_steps_per_s, 1),
+                   "tokens_per_s": round(dec_steps_per_s * dcfg.N, 1),
+                   "ms_per_step": round(dec_s * 1e3 / args.steps, 4),
+                   "roofline": {"bound": "hbm", "achieved": round(dec_achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
+                                "frac": round(dec_achieved / hbm_gbs, 4), "traffic": None,
+                                "kernel": "kda_decode", "peak_kind": peak_kind}},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": round(achieved / hbm_gbs, 4), "traffic": None, "kernel": dom[0],
+                     "kernel_ms": round(dom_ms, 4), "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "prefill_tensor": {"flops_per_step": pre_flops,
+                           "achieved_tflops": round(pre_flops / (pre_s / args.steps) / 1e12, 2),
+                           "peak_tflops": bf16_tflops,
+                           "frac": round(pre_flops / (pre_s / args.steps) / 1e12 / bf16_tflops, 4)},
+        "kernels": {k: {"launches": v[0], "total_ms": round(v[1], 4)} for k, v in trace.items()},
+        "gpu_launches": launches,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clocks.summary(),
+        "wall_s": round(t_wall, 3),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    return line
+
+
+def _oracle_prefill_sample(tokens: int):
+    """The oracle on the first `tokens` tokens of the prefill workload (all 32 heads)."""
+    import dataclasses
+
+    from gated_delta_rule_08_gb300 import inputs
+    from oracle import oracle_kda_prefill, oracle_threads
+
+    cfg = dataclasses.replace(inputs.PREFILL, T=tokens)
+    P = inputs.prefill_inputs(cfg, device="cpu")
+    t0 = time.perf_counter()
+    oracle_kda_prefill(P["q"], P["k"], P["v"], P["g"], P["beta"])
+    return time.perf_counter() - t0, oracle_threads()
+
+
+def cpu_baseline(args):
+    tokens = args.cpu_tokens
+    secs, cores = _oracle_prefill_sample(tokens)
+    return {"value": round(tokens / secs, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 token-by-token oracle on the first {tokens} of the 8192 prefill tokens, all 32 heads "
+                      f"(OpenMP over heads; {secs:.2f} s wall)"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    tokens = args.cpu_tokens
+    times = []
+    cores = 1
+    for i in range(args.warmup + args.steps):
+        s, cores = _oracle_prefill_sample(tokens)
+        if i >= args.warmup:
+            times.append(s)
+    total = sum(times)
+    value = tokens * len(times) / total
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total * 1e3 / len(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": "prefill B=1 H=32 T=8192 dk=dv=128 (oracle sample: first "
+                               f"{tokens} tokens, all heads)"},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {tokens} of 8192 tokens, all 32 heads, per step"},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-tokens", type=int, default=8192)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    line = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

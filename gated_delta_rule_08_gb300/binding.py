@@ -1,0 +1,247 @@
+"""Thin Python binding of libkda (ctypes): argument marshalling only.
+
+Every function here checks shapes/dtypes/devices of torch tensors, passes their
+device pointers and the current CUDA stream to the C-ABI entry point of the same
+name (include/kda.h), and raises on a non-OK status.  No arithmetic of the method
+happens in Python.  There is no fallback: without a built libkda.so or a CUDA
+device the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkda.so")
+
+KDA_DTYPE_BF16 = 0
+KDA_DTYPE_FP32 = 1
+STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
+          4: "KDA_ERR_DEVICE", 5: "KDA_ERR_WORKSPACE"}
+DEVERR_BAD_SLOT = 0x1
+DEVERR_BAD_SEQLENS = 0x2
+DEVERR_WAIT_TIMEOUT = 0x4
+
+# Exported symbols, as declared in include/kda.h.
+EXPORTS = ("kda_chunk_fwd_workspace_size", "kda_chunk_fwd", "kda_decode_step", "kda_get_device_error",
+           "kda_status_string", "kda_trace_enable", "kda_trace_collect")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class _Epilogue(ctypes.Structure):
+    _fields_ = [("gate_logits", ctypes.c_void_p), ("norm_weight", ctypes.c_void_p), ("eps", ctypes.c_float)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: Optional[str] = None):
+    """Load libkda.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libkda.so not built ({p}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(p)
+        P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        lib.kda_chunk_fwd_workspace_size.argtypes = [I, I64, I, I, I, I, I]
+        lib.kda_chunk_fwd_workspace_size.restype = SZ
+        lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, I, I, P, P, SZ, P]
+        lib.kda_chunk_fwd.restype = I
+        lib.kda_decode_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
+        lib.kda_decode_step.restype = I
+        lib.kda_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+        lib.kda_get_device_error.restype = I
+        lib.kda_trace_enable.argtypes = [I]
+        lib.kda_trace_enable.restype = I
+        lib.kda_trace_collect.argtypes = [I, ctypes.c_char_p, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(I)]
+        lib.kda_trace_collect.restype = I
+        lib.kda_status_string.argtypes = [I]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return KDA_DTYPE_FP32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t: Optional[torch.Tensor], name: str, dtype=None, shape=None, device=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def kda_chunk_fwd_workspace_size(B: int, T: int, H: int, dk: int, dv: int, C: int = 64,
+                                 dtype: torch.dtype = torch.bfloat16) -> int:
+    code = KDA_DTYPE_BF16 if dtype == torch.bfloat16 else KDA_DTYPE_FP32
+    return int(load_library().kda_chunk_fwd_workspace_size(B, T, H, dk, dv, C, code))
+
+
+def kda_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, out=None, hT=None, *, B: Optional[int] = None,
+                  C: int = 64, gate=None, norm_weight=None, eps: float = 1e-6, workspace=None,
+                  output_final_state: bool = True, out_dtype: Optional[torch.dtype] = None):
+    """Chunked KDA prefill.  q, k: [T_tot, H, dk]; v: [T_tot, H, dv]; g: [T_tot, H, dk] fp32;
+    beta: [T_tot, H] fp32; h0: [B, H, dk, dv] fp32 or None; cu_seqlens: int32 [B+1] on the device
+    or None (then B sequences of T_tot/B tokens).  gate/norm_weight enable the fused epilogue.
+    out_dtype: element type of out (default: the dtype of q; bf16 or fp32).
+    Returns (out [T_tot, H, dv], hT [B, H, dk, dv] or None)."""
+    lib = load_library()
+    dev = q.device
+    T_tot, H, dk = q.shape
+    dv = v.shape[2]
+    dt = q.dtype
+    code = _dtype_code(q)
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, device=dev)
+        nB = cu_seqlens.numel() - 1
+        if B is not None and B != nB:
+            raise ValueError("B does not match cu_seqlens")
+        B = nB
+        T_arg = T_tot
+    else:
+        B = 1 if B is None else B
+        if T_tot % B:
+            raise ValueError("without cu_seqlens, T_tot must be a multiple of B")
+        T_arg = T_tot // B
+    _check(q, "q", dt, (T_tot, H, dk), dev)
+    _check(k, "k", dt, (T_tot, H, dk), dev)
+    _check(v, "v", dt, (T_tot, H, dv), dev)
+    _check(g, "g", torch.float32, (T_tot, H, dk), dev)
+    _check(beta, "beta", torch.float32, (T_tot, H), dev)
+    _check(h0, "h0", torch.float32, (B, H, dk, dv), dev)
+    _check(gate, "gate", dt, (T_tot, H, dv), dev)
+    _check(norm_weight, "norm_weight", torch.float32, (dv,), dev)
+    odt = out.dtype if out is not None else (out_dtype or dt)
+    if out is None:
+        out = torch.empty(T_tot, H, dv, device=dev, dtype=odt)
+    _check(out, "out", odt, (T_tot, H, dv), dev)
+    ocode = _dtype_code(out)
+    if hT is None and output_final_state:
+        hT = torch.empty(B, H, dk, dv, device=dev, dtype=torch.float32)
+    _check(hT, "hT", torch.float32, (B, H, dk, dv), dev)
+    need = int(lib.kda_chunk_fwd_workspace_size(B, T_arg, H, dk, dv, C, code))
+    if need == 0:
+        raise KdaError("kda_chunk_fwd_workspace_size", 2)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    _check(workspace, "workspace", torch.uint8, None, dev)
+    epi = None
+    if gate is not None:
+        epi = _Epilogue(gate.data_ptr(), norm_weight.data_ptr() if norm_weight is not None else None, float(eps))
+    st = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
+                           _ptr(out), _ptr(hT), B, T_arg, H, dk, dv, C, code, ocode,
+                           ctypes.byref(epi) if epi is not None else None, _ptr(workspace),
+                           workspace.numel(), _stream(dev))
+    if st != 0:
+        raise KdaError("kda_chunk_fwd", st)
+    return out, hT
+
+
+def kda_decode_step(q, k, v, g, beta, state_pool, slot_idx, out=None, *, gate=None, norm_weight=None,
+                    eps: float = 1e-6, out_dtype: Optional[torch.dtype] = None):
+    """One decode step.  q, k: [N, H, dk]; v: [N, H, dv]; g: [N, H, dk] fp32; beta: [N, H] fp32;
+    state_pool: [num_slots, H, dk, dv] fp32 (updated in place); slot_idx: int32 [N].
+    Returns out [N, H, dv]."""
+    lib = load_library()
+    dev = q.device
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    dt = q.dtype
+    code = _dtype_code(q)
+    num_slots = state_pool.shape[0]
+    _check(q, "q", dt, (N, H, dk), dev)
+    _check(k, "k", dt, (N, H, dk), dev)
+    _check(v, "v", dt, (N, H, dv), dev)
+    _check(g, "g", torch.float32, (N, H, dk), dev)
+    _check(beta, "beta", torch.float32, (N, H), dev)
+    _check(state_pool, "state_pool", torch.float32, (num_slots, H, dk, dv), dev)
+    _check(slot_idx, "slot_idx", torch.int32, (N,), dev)
+    _check(gate, "gate", dt, (N, H, dv), dev)
+    _check(norm_weight, "norm_weight", torch.float32, (dv,), dev)
+    odt = out.dtype if out is not None else (out_dtype or dt)
+    if out is None:
+        out = torch.empty(N, H, dv, device=dev, dtype=odt)
+    _check(out, "out", odt, (N, H, dv), dev)
+    ocode = _dtype_code(out)
+    epi = None
+    if gate is not None:
+        epi = _Epilogue(gate.data_ptr(), norm_weight.data_ptr() if norm_weight is not None else None, float(eps))
+    st = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_pool), _ptr(slot_idx),
+                             _ptr(out), N, H, dk, dv, num_slots, code, ocode,
+                             ctypes.byref(epi) if epi is not None else None, _stream(dev))
+    if st != 0:
+        raise KdaError("kda_decode_step", st)
+    return out
+
+
+def kda_get_device_error(device=None) -> int:
+    """Synchronise the current stream and read + clear the device error word."""
+    lib = load_library()
+    flags = ctypes.c_uint32(0)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    st = lib.kda_get_device_error(_stream(dev), ctypes.byref(flags))
+    if st != 0:
+        raise KdaError("kda_get_device_error", st)
+    return int(flags.value)
+
+
+def kda_status_string(status: int) -> str:
+    return load_library().kda_status_string(status).decode()
+
+
+def kda_trace_enable(enable: bool = True) -> None:
+    """Bracket every internal kernel launch with CUDA events (profiling aid)."""
+    st = load_library().kda_trace_enable(1 if enable else 0)
+    if st != 0:
+        raise KdaError("kda_trace_enable", st)
+
+
+def kda_trace_collect(max_entries: int = 32) -> dict:
+    """{kernel name: (launches, total ms)} since the previous collect (synchronises)."""
+    lib = load_library()
+    names = ctypes.create_string_buffer(64 * max_entries)
+    launches = (ctypes.c_int * max_entries)()
+    total = (ctypes.c_double * max_entries)()
+    n = ctypes.c_int(0)
+    st = lib.kda_trace_collect(max_entries, names, launches, total, ctypes.byref(n))
+    if st != 0:
+        raise KdaError("kda_trace_collect", st)
+    raw = names.raw
+    return {raw[64 * i:64 * i + 64].split(b"\0", 1)[0].decode(): (int(launches[i]), float(total[i]))
+            for i in range(n.value)}

@@ -1,0 +1,102 @@
+// Internal declarations shared by the host-side translation units of libkda.
+// Not part of the public ABI (include/kda.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kChunk = 64;  // tokens per chunk (C)
+
+// Epilogue arguments as the kernels see them (gate == nullptr: no epilogue).
+struct Epilogue {
+  const void* gate;
+  const float* norm_weight;
+  float eps;
+};
+
+struct PrefillArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  const float* h0;            // may be null
+  const int32_t* cu_seqlens;  // may be null (equal lengths)
+  void* out;
+  float* hT;                  // may be null
+  int B;
+  int64_t T;                  // per-sequence length if cu_seqlens == null, else T_tot
+  int64_t T_tot;
+  int H, dk, dv;
+  bool bf16;       // q, k, v, gate are bf16 (else fp32)
+  bool out_bf16;   // out is bf16 (else fp32)
+  Epilogue epi;
+  void* workspace;
+  size_t workspace_bytes;
+  unsigned int* err;          // device error word
+};
+
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  float* state_pool;
+  const int32_t* slot_idx;
+  void* out;
+  int N, H, dk, dv, num_slots;
+  bool bf16;
+  bool out_bf16;
+  Epilogue epi;
+  unsigned int* err;
+};
+
+// Upper bound on the number of 64-token chunks of a packed batch:
+// sum_b ceil(len_b / 64) <= ceil(T_tot / 64) + B.
+inline int64_t max_chunks(int B, int64_t T, bool has_cu) {
+  if (!has_cu) return (int64_t)B * ((T + kChunk - 1) / kChunk);
+  return (T + kChunk - 1) / kChunk + B;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Plan region at the start of the workspace: int32 chunk offsets [B+1] + one valid flag.
+inline size_t plan_bytes(int B) { return align_up((size_t)(B + 2) * sizeof(int32_t), 256); }
+
+// fp32 CUDA-core path (kda_prefill_cc.cu)
+size_t prefill_cc_blob_bytes(int dk, int dv);
+cudaError_t prefill_cc_launch(const PrefillArgs& a, cudaStream_t stream);
+
+// bf16 tensor-core path (kda_prefill_tc.cu)
+size_t prefill_tc_blob_bytes(int dk, int dv);
+bool prefill_tc_supported(int dk, int dv);
+cudaError_t prefill_tc_launch(const PrefillArgs& a, cudaStream_t stream);
+
+// plan kernel (kda_prefill_cc.cu): chunk offsets per sequence + cu_seqlens validation
+cudaError_t plan_launch(const int32_t* cu_seqlens, int B, int64_t T_tot, int32_t* plan,
+                        unsigned int* err, cudaStream_t stream);
+
+// decode (kda_decode.cu)
+cudaError_t decode_launch(const DecodeArgs& a, cudaStream_t stream);
+
+// Kernel tracing (kda_trace_enable): brackets internal launches with CUDA events.
+bool trace_enabled();
+void trace_begin(const char* name, cudaStream_t s);
+void trace_end(cudaStream_t s);
+
+struct TraceScope {
+  cudaStream_t s;
+  bool on;
+  TraceScope(const char* name, cudaStream_t st) : s(st), on(trace_enabled()) {
+    if (on) trace_begin(name, s);
+  }
+  ~TraceScope() {
+    if (on) trace_end(s);
+  }
+};
+
+}  // namespace kda

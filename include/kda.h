@@ -1,0 +1,142 @@
+/*
+ * libkda — Kimi Delta Attention (KDA) hot path for GB300 (sm_103a).
+ *
+ * The operation (Kimi K3 technical-report walk-through, kimi-k3-paper.pages.dev):
+ *   per (sequence, head), tokens t = 1..T, state S in R^{dk x dv} (rows = key channels)
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T      (section 2.2, Eq. 1)
+ *     o_t = S_t^T q_t                                                        (section 2.4, Eq. 3)
+ *   with a channel-wise decay exp(g_t), g_t in (-5, 0] (sections 2.3 and 3.2, Eq. 5), and
+ *   an optional epilogue y_t = o_t / sqrt(mean(o_t^2) + eps) * w * sigmoid(gate_t)
+ *   (section 3.3, Eq. 6: head-wise RMSNorm, then the sigmoid output gate).
+ *
+ * General conventions for every entry point:
+ *   - All tensor pointers are caller-owned DEVICE memory, dense, row-major, in the
+ *     layouts stated per argument.  The library never allocates device memory and
+ *     never frees anything it is given.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL means
+ *     the legacy default stream).  The call returns after validation and launch.
+ *   - Argument errors are detected synchronously on the host: nothing is launched and
+ *     the corresponding status is returned.  Conditions that only the device can see
+ *     (an out-of-range slot index, inconsistent cu_seqlens, a device wait that ran out)
+ *     are recorded in a per-device error word read by kda_get_device_error(); the
+ *     affected rows are skipped, never trapped on.
+ *   - dk, dv must each be 64 or 128 and C must be 64 (KDA_ERR_UNSUPPORTED otherwise).
+ *   - `dtype` is the element type of q, k, v and the gate logits; `out_dtype` that of out
+ *     (either may be bf16 or fp32).  bf16 inputs run on the tensor-core path; fp32 inputs
+ *     run on an fp32 CUDA-core path (slower, ~1e-6 relative error).  The read-out is
+ *     computed in fp32 and rounded once when stored in out_dtype.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent sizes          */
+  KDA_ERR_UNSUPPORTED = 2,   /* dk/dv not in {64,128}, C != 64, unknown dtype, no sm_103a */
+  KDA_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, attribute, sync)      */
+  KDA_ERR_DEVICE = 4,        /* the device error word is non-zero (kda_get_device_error)  */
+  KDA_ERR_WORKSPACE = 5      /* workspace pointer NULL or smaller than required           */
+} kda_status;
+
+typedef enum {
+  KDA_DTYPE_BF16 = 0,
+  KDA_DTYPE_FP32 = 1
+} kda_dtype;
+
+/* Bits of the device error word. */
+#define KDA_DEVERR_BAD_SLOT     0x1u  /* decode: slot_idx[n] outside [0, num_slots)        */
+#define KDA_DEVERR_BAD_SEQLENS  0x2u  /* prefill: cu_seqlens not non-decreasing in [0, T]  */
+#define KDA_DEVERR_WAIT_TIMEOUT 0x4u  /* a bounded device-side wait gave up                */
+
+/* Optional fused epilogue (section 3.3, Eq. 6): RMSNorm over dv per (token, head), then
+ * the sigmoid output gate.  The norm is taken on the fp32 read-out before rounding.
+ *   gate_logits : [rows, H, dv] in the call's dtype (rows = T_tot or N)   — required
+ *   norm_weight : [dv] fp32, shared by all heads; NULL means weight 1
+ *   eps         : added to mean(o^2) before the square root (typical 1e-6) */
+typedef struct {
+  const void* gate_logits;
+  const float* norm_weight;
+  float eps;
+} kda_epilogue;
+
+/* Bytes of device scratch kda_chunk_fwd needs for this problem (0 on bad arguments).
+ * T has the same meaning as in kda_chunk_fwd.  The scratch holds per-chunk operands
+ * of the chunkwise form (~72.5 KB per 64-token chunk and head for bf16 at dk=dv=128)
+ * plus a small plan. */
+size_t kda_chunk_fwd_workspace_size(int B, int64_t T, int H, int dk, int dv, int C,
+                                    kda_dtype dtype);
+
+/* Chunked prefill over a packed batch of B variable-length sequences
+ * (section 2.5, Eq. 4: serial inter-chunk state pass + parallel intra-chunk term).
+ *   q, k      : [T_tot, H, dk]  (dtype)      L2-normalised upstream; not re-normalised
+ *   v         : [T_tot, H, dv]  (dtype)
+ *   g         : [T_tot, H, dk]  fp32         log-decay; precondition g in (-5, 0]
+ *   beta      : [T_tot, H]      fp32         write strength, precondition in [0, 1]
+ *   h0        : [B, H, dk, dv]  fp32 or NULL (zero initial states)
+ *   cu_seqlens: [B+1] int32 device token offsets (cu[0] = 0, cu[B] = T_tot, non-decreasing),
+ *               or NULL meaning B sequences of exactly T tokens each
+ *   out       : [T_tot, H, dv]  (out_dtype)  must not alias any input
+ *   hT        : [B, H, dk, dv]  fp32 or NULL (final states not written); may alias h0
+ *   T         : tokens per sequence if cu_seqlens == NULL, else T_tot
+ *   C         : chunk size, must be 64.  Chunks start at each sequence's first token.
+ *   epi       : NULL or the fused epilogue
+ *   workspace : device scratch of at least kda_chunk_fwd_workspace_size(...) bytes,
+ *               256-byte aligned; contents on entry are ignored, on exit undefined.
+ * Errors: KDA_ERR_INVALID_ARG / _UNSUPPORTED / _WORKSPACE before any launch; KDA_ERR_CUDA
+ * if a launch fails.  Bad cu_seqlens set KDA_DEVERR_BAD_SEQLENS and the affected
+ * sequences are skipped. */
+kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* h0, const int32_t* cu_seqlens,
+                         void* out, float* hT, int B, int64_t T, int H, int dk, int dv, int C,
+                         kda_dtype dtype, kda_dtype out_dtype, const kda_epilogue* epi,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* One recurrent decode step for N requests, one token each, on a pool of fp32 states
+ * updated in place (section 13.9 prefix cache: one fixed-size state per request in a
+ * pooled layout; section 13.10: state update and read-out in a single fused kernel).
+ *   q, k       : [N, H, dk] (dtype);  v : [N, H, dv] (dtype)
+ *   g          : [N, H, dk] fp32;     beta : [N, H] fp32
+ *   state_pool : [num_slots, H, dk, dv] fp32, read and written in place
+ *   slot_idx   : [N] int32 device; request n uses state_pool[slot_idx[n]].  Slots must be
+ *                distinct (duplicates race; not checked).  An index outside
+ *                [0, num_slots) sets KDA_DEVERR_BAD_SLOT and leaves that request's out rows
+ *                and every slot untouched.
+ *   out        : [N, H, dv] (out_dtype)
+ * Slots not named in slot_idx are never read or written. */
+kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, float* state_pool, const int32_t* slot_idx,
+                           void* out, int N, int H, int dk, int dv, int num_slots,
+                           kda_dtype dtype, kda_dtype out_dtype, const kda_epilogue* epi,
+                           void* stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error word into
+ * *flags (KDA_DEVERR_* bits).  Returns KDA_OK, or KDA_ERR_CUDA if the sync failed. */
+kda_status kda_get_device_error(void* stream, uint32_t* flags);
+
+/* Kernel-level timing for profilers; not needed for normal use.  While enabled, each
+ * internal kernel launch made by kda_chunk_fwd / kda_decode_step is bracketed by two CUDA
+ * events recorded on the call's stream (a few microseconds of host overhead per launch).
+ * kda_trace_collect synchronises on those events and reports, per kernel name, the number
+ * of launches and their summed device time in milliseconds since the previous collect:
+ *   names    : caller buffer of max_entries * 64 bytes (NUL-terminated names)
+ *   launches : [max_entries];  total_ms : [max_entries];  *n_entries : entries written
+ * Both return KDA_ERR_CUDA if an event call fails.  Not thread-safe against concurrent
+ * enable/disable; recording itself is serialised internally. */
+kda_status kda_trace_enable(int enable);
+kda_status kda_trace_collect(int max_entries, char* names, int* launches, double* total_ms,
+                             int* n_entries);
+
+/* Static, human-readable name of a status code. */
+const char* kda_status_string(kda_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_H_ */

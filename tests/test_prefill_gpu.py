@@ -1,0 +1,191 @@
+"""Chunked prefill on the GPU vs the fp64 oracle (through the C-ABI binding)."""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_08_gb300 import binding, inputs
+from gpu_util import TOL, assert_no_device_error, oracle_prefill, parity_err, rel_err, run_prefill
+from oracle import oracle_kda_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(cfg, *, epilogue=None, device_gen=False, out_dtypes=(torch.float32, torch.bfloat16)):
+    """GPU vs oracle on the same inputs.  The tolerance is the one for the input dtype
+    (1e-3 fp32, 2e-2 bf16) on max|err|/RMS, per output tensor; a bf16-stored output is
+    allowed its own storage rounding on top (see gpu_util.parity_err)."""
+    inp = inputs.prefill_inputs(cfg, device="cuda" if device_gen else "cpu")
+    inp_d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    ref_out, ref_hT = oracle_prefill(inp_d, epilogue=epilogue)
+    tol = TOL[inputs.torch_dtype(cfg.dtype)]
+    res = None
+    for odt in out_dtypes:
+        out, hT = run_prefill(inp_d, epilogue=epilogue, out_dtype=odt)
+        assert_no_device_error()
+        e_o, e_h = parity_err(out, ref_out), rel_err(hT, ref_hT)
+        assert e_o <= tol and e_h <= tol, (cfg.name, odt, e_o, e_h)
+        res = res or (inp_d, out, hT)
+    return res
+
+
+# ------------------------------------------------------------------ the named workloads
+def test_tiny_fp32_h2_t256_d64():
+    _check(inputs.TINY)
+
+
+def test_prefill_bf16_h32_t8192_d128():
+    _check(inputs.PREFILL, device_gen=True)
+
+
+def test_varlen_bf16_8seqs_h32_d128_h0():
+    _check(inputs.VARLEN, device_gen=True)
+
+
+# ------------------------------------------------------------------ sweeps: lengths, dims, states, epilogue
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 200])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_single_sequence_lengths(T, dtype):
+    cfg = inputs.PrefillConfig("len sweep", H=3, dk=128, dv=128, dtype=dtype, B=1, T=T, h0_std=0.1, seed=100 + T)
+    _check(cfg)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 64), (64, 128), (128, 128)])
+@pytest.mark.parametrize("epilogue", [False, True])
+def test_dims_and_epilogue(dk, dv, epilogue):
+    cfg = inputs.PrefillConfig("dims", H=2, dk=dk, dv=dv, dtype="bf16", lengths=(130, 64, 1, 77), B=4,
+                               h0_std=0.1, epilogue=epilogue, seed=200 + dk + dv)
+    _check(cfg, epilogue=epilogue)
+
+
+def test_varlen_with_empty_and_short_sequences():
+    cfg = inputs.PrefillConfig("varlen edge", H=4, dk=128, dv=128, dtype="bf16",
+                               lengths=(0, 1, 63, 64, 65, 0, 129, 3), B=8, h0_std=0.1, epilogue=True, seed=300)
+    inp, out, hT = _check(cfg, epilogue=True)
+    # empty sequences: final state equals initial state, bit for bit
+    assert torch.equal(hT[0], inp["h0"][0]) and torch.equal(hT[5], inp["h0"][5])
+
+
+def test_equal_lengths_without_cu_seqlens():
+    cfg = inputs.PrefillConfig("equal", H=2, dk=128, dv=128, dtype="bf16", B=3, T=100, h0_std=0.1, seed=301)
+    inp = inputs.prefill_inputs(cfg, device="cuda")
+    out_a, h_a = binding.kda_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], h0=inp["h0"], B=3)
+    out_b, h_b = binding.kda_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], h0=inp["h0"],
+                                       cu_seqlens=inp["cu_seqlens"])
+    assert torch.equal(out_a, out_b) and torch.equal(h_a, h_b)
+
+
+# ------------------------------------------------------------------ bit-exact properties
+def test_packed_equals_each_sequence_alone():
+    cfg = inputs.PrefillConfig("pack", H=2, dk=128, dv=128, dtype="bf16", lengths=(70, 5, 128, 200), B=4,
+                               h0_std=0.1, seed=302)
+    inp = inputs.prefill_inputs(cfg, device="cuda")
+    out, hT = run_prefill(inp)
+    cu = inp["cu_seqlens"].tolist()
+    for b in range(4):
+        a, e = cu[b], cu[b + 1]
+        o1, h1 = binding.kda_chunk_fwd(inp["q"][a:e].contiguous(), inp["k"][a:e].contiguous(),
+                                       inp["v"][a:e].contiguous(), inp["g"][a:e].contiguous(),
+                                       inp["beta"][a:e].contiguous(), h0=inp["h0"][b:b + 1].contiguous())
+        assert torch.equal(o1, out[a:e]), b
+        assert torch.equal(h1[0], hT[b]), b
+
+
+def test_run_to_run_deterministic():
+    cfg = inputs.PrefillConfig("det", H=4, dk=128, dv=128, dtype="bf16", lengths=(300, 17), B=2, h0_std=0.1,
+                               epilogue=True, seed=303)
+    inp = inputs.prefill_inputs(cfg, device="cuda")
+    o1, h1 = run_prefill(inp)
+    o2, h2 = run_prefill(inp)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_final_state_may_alias_initial_state():
+    cfg = inputs.PrefillConfig("alias", H=2, dk=128, dv=128, dtype="bf16", lengths=(90, 33), B=2, h0_std=0.1,
+                               seed=304)
+    inp = inputs.prefill_inputs(cfg, device="cuda")
+    out, hT = run_prefill(inp)
+    state = inp["h0"].clone()
+    out2, _ = binding.kda_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], h0=state,
+                                    cu_seqlens=inp["cu_seqlens"], hT=state)
+    assert torch.equal(out, out2) and torch.equal(state, hT)
+
+
+def test_split_run_resumes_from_final_state():
+    """Prefill of a prefix, then of the rest from its final state == one prefill (checkpoint/resume)."""
+    cfg = inputs.PrefillConfig("resume", H=2, dk=128, dv=128, dtype="bf16", B=1, T=256, h0_std=0.1, seed=305)
+    inp = inputs.prefill_inputs(cfg, device="cuda")
+    out, hT = run_prefill(inp)
+    o1, h1 = binding.kda_chunk_fwd(*(inp[x][:128].contiguous() for x in ("q", "k", "v", "g", "beta")),
+                                   h0=inp["h0"])
+    o2, h2 = binding.kda_chunk_fwd(*(inp[x][128:].contiguous() for x in ("q", "k", "v", "g", "beta")), h0=h1)
+    assert torch.equal(torch.cat([o1, o2]), out) and torch.equal(h2, hT)
+
+
+def test_decode_steps_match_prefill():
+    cfg = inputs.PrefillConfig("dec", H=2, dk=128, dv=128, dtype="bf16", B=1, T=20, h0_std=0.1, seed=306)
+    inp = inputs.prefill_inputs(cfg, device="cuda")
+    out, hT = run_prefill(inp)
+    pool = torch.zeros(3, 2, 128, 128, device="cuda")
+    pool[1] = inp["h0"][0]
+    slot = torch.tensor([1], dtype=torch.int32, device="cuda")
+    outs = []
+    for t in range(20):
+        outs.append(binding.kda_decode_step(*(inp[x][t:t + 1].contiguous() for x in ("q", "k", "v", "g", "beta")),
+                                            pool, slot))
+    dec = torch.cat(outs)
+    assert parity_err(dec, out.double().cpu().numpy()) <= 2e-2
+    assert rel_err(pool[1], hT[0].double().cpu().numpy()) <= 2e-2
+
+
+def test_bad_cu_seqlens_sets_flag():
+    cfg = inputs.PrefillConfig("bad", H=2, dk=128, dv=128, dtype="bf16", lengths=(10, 20), B=2, seed=307)
+    inp = inputs.prefill_inputs(cfg, device="cuda")
+    bad = torch.tensor([0, 25, 20], dtype=torch.int32, device="cuda")  # decreasing
+    hT = torch.full((2, 2, 128, 128), 3.0, device="cuda")
+    binding.kda_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], cu_seqlens=bad, hT=hT)
+    assert binding.kda_get_device_error() & binding.DEVERR_BAD_SEQLENS
+    assert torch.all(hT == 3.0)  # skipped, untouched
+
+
+# ------------------------------------------------------------------ long context: 1M tokens, H=16
+def _window_start(g_host_f64, p, eps_log=math.log(1e-12), max_w=8192):
+    """Smallest window start a such that prod_{t=a..p} max_c alpha_t < 1e-12 (all heads).
+    For |k| = 1 and beta in [0, 1] each token's transition has operator norm <= max_c alpha_t,
+    so restarting the recurrence from zero at a changes S_p by < 1e-12 * |S_{a-1}|."""
+    acc = np.zeros(g_host_f64.shape[1])
+    a = p
+    while a >= 0 and p - a < max_w:
+        acc += g_host_f64[a].max(axis=-1)
+        if acc.max() < eps_log:
+            return a
+        a -= 1
+    return max(a, 0)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("cfg", [inputs.LONG, inputs.LONG_SLOW], ids=["z_mean+2", "z_mean-2"])
+def test_long_context_1m_tokens(cfg):
+    inp = inputs.prefill_inputs(cfg, device="cuda")
+    T = inp["T_tot"]
+    # (i) the first 65,536 tokens against the full oracle
+    P = 65536
+    pre = {x: inp[x][:P].contiguous() for x in ("q", "k", "v", "g", "beta")}
+    o_p, h_p = binding.kda_chunk_fwd(pre["q"], pre["k"], pre["v"], pre["g"], pre["beta"])
+    assert_no_device_error()
+    ref_o, ref_h = oracle_kda_prefill(pre["q"], pre["k"], pre["v"], pre["g"], pre["beta"])
+    assert parity_err(o_p, ref_o) <= 2e-2 and rel_err(h_p, ref_h) <= 2e-2
+    del pre, o_p, h_p, ref_o, ref_h
+    # (ii) the full sequence; spot rows against the oracle restarted on a provably sufficient window
+    out, hT = binding.kda_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"])
+    assert_no_device_error()
+    for p in [70000, 262143, 500001, 777777, T - 1]:
+        gw = inp["g"][max(0, p - 8192):p + 1].double().cpu().numpy()
+        a = max(0, p - 8192) + _window_start(gw, gw.shape[0] - 1)
+        sl = slice(a, p + 1)
+        ro, rh = oracle_kda_prefill(*(inp[x][sl] for x in ("q", "k", "v", "g", "beta")))
+        assert parity_err(out[p], ro[-1]) <= 2e-2, p
+        if p == T - 1:
+            assert rel_err(hT[0], rh[0]) <= 2e-2
