@@ -28,7 +28,8 @@ DEVERR_WAIT_TIMEOUT = 0x4
 
 # Exported symbols, as declared in include/kda.h.
 EXPORTS = ("kda_chunk_fwd_workspace_size", "kda_chunk_fwd", "kda_decode_step", "kda_get_device_error",
-           "kda_status_string", "kda_trace_enable", "kda_trace_collect")
+           "kda_status_string", "kda_trace_enable", "kda_trace_collect", "kda_chunk_fwd_noalloc",
+           "kda_noalloc_scratch_bytes")
 
 
 class KdaError(RuntimeError):
@@ -64,6 +65,10 @@ def load_library(path: Optional[str] = None):
         lib.kda_decode_step.restype = I
         lib.kda_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
         lib.kda_get_device_error.restype = I
+        lib.kda_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, I, I, P, P]
+        lib.kda_chunk_fwd_noalloc.restype = I
+        lib.kda_noalloc_scratch_bytes.argtypes = []
+        lib.kda_noalloc_scratch_bytes.restype = SZ
         lib.kda_trace_enable.argtypes = [I]
         lib.kda_trace_enable.restype = I
         lib.kda_trace_collect.argtypes = [I, ctypes.c_char_p, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double),
@@ -245,3 +250,49 @@ def kda_trace_collect(max_entries: int = 32) -> dict:
     raw = names.raw
     return {raw[64 * i:64 * i + 64].split(b"\0", 1)[0].decode(): (int(launches[i]), float(total[i]))
             for i in range(n.value)}
+
+
+def kda_chunk_fwd_noalloc(q, k, v, g, beta, h0=None, cu_seqlens=None, out=None, hT=None, *,
+                          B: Optional[int] = None, C: int = 64, gate=None, norm_weight=None, eps: float = 1e-6,
+                          out_dtype: Optional[torch.dtype] = None):
+    """kda_chunk_fwd without a caller workspace: the library's fixed device scratch is used
+    instead, so the C call itself allocates nothing (out/hT are allocated here only when the
+    caller passes None).  For callers that cannot allocate at call time; problems needing more
+    than kda_noalloc_scratch_bytes() of scratch are rejected.  Same arguments and results as
+    kda_chunk_fwd."""
+    lib = load_library()
+    dev = q.device
+    T_tot, H, dk = q.shape
+    dv = v.shape[2]
+    code = _dtype_code(q)
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, device=dev)
+        B = cu_seqlens.numel() - 1
+        T_arg = T_tot
+    else:
+        B = 1 if B is None else B
+        if T_tot % B:
+            raise ValueError("without cu_seqlens, T_tot must be a multiple of B")
+        T_arg = T_tot // B
+    for t, name, dt_, shp in ((q, "q", q.dtype, (T_tot, H, dk)), (k, "k", q.dtype, (T_tot, H, dk)),
+                              (v, "v", q.dtype, (T_tot, H, dv)), (g, "g", torch.float32, (T_tot, H, dk)),
+                              (beta, "beta", torch.float32, (T_tot, H)), (h0, "h0", torch.float32, (B, H, dk, dv)),
+                              (gate, "gate", q.dtype, (T_tot, H, dv)),
+                              (norm_weight, "norm_weight", torch.float32, (dv,))):
+        _check(t, name, dt_, shp, dev)
+    odt = out.dtype if out is not None else (out_dtype or q.dtype)
+    if out is None:
+        out = torch.empty(T_tot, H, dv, device=dev, dtype=odt)
+    _check(out, "out", odt, (T_tot, H, dv), dev)
+    if hT is None:
+        hT = torch.empty(B, H, dk, dv, device=dev, dtype=torch.float32)
+    _check(hT, "hT", torch.float32, (B, H, dk, dv), dev)
+    epi = None
+    if gate is not None:
+        epi = _Epilogue(gate.data_ptr(), norm_weight.data_ptr() if norm_weight is not None else None, float(eps))
+    st = lib.kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
+                                   _ptr(out), _ptr(hT), B, T_arg, H, dk, dv, C, code, _dtype_code(out),
+                                   ctypes.byref(epi) if epi is not None else None, _stream(dev))
+    if st != 0:
+        raise KdaError("kda_chunk_fwd_noalloc", st)
+    return out, hT

@@ -133,6 +133,31 @@ kda_status kda_trace_enable(int enable);
 kda_status kda_trace_collect(int max_entries, char* names, int* launches, double* total_ms,
                              int* n_entries);
 
+/* kda_chunk_fwd for callers that cannot allocate device memory.  The method itself has
+ * no counterpart to this: it is an interface variant for deployment.  Callers such as
+ * code running under an allocator that owns all device memory, or hosts whose execution
+ * path forbids cudaMalloc, cannot provide kda_chunk_fwd's workspace; this entry point
+ * takes no workspace and allocates nothing (no cudaMalloc/cudaFree, no allocating
+ * library call).  Its scratch is a fixed library-owned device array of
+ * kda_noalloc_scratch_bytes() bytes (64 MiB), reserved on every device that loads the
+ * library until the process exits.
+ *   - Arguments, layouts, results and errors are those of kda_chunk_fwd.
+ *   - Problems with kda_chunk_fwd_workspace_size(...) above the scratch size return
+ *     KDA_ERR_WORKSPACE before any launch.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
+ *     make that first call outside any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls whose GPU work overlaps in time, e.g.
+ *     on two unordered streams, race on it: order them. */
+kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, const float* h0, const int32_t* cu_seqlens,
+                                 void* out, float* hT, int B, int64_t T, int H, int dk, int dv,
+                                 int C, kda_dtype dtype, kda_dtype out_dtype,
+                                 const kda_epilogue* epi, void* stream);
+
+/* Size in bytes of the library-owned scratch used by kda_chunk_fwd_noalloc. */
+size_t kda_noalloc_scratch_bytes(void);
+
 /* Static, human-readable name of a status code. */
 const char* kda_status_string(kda_status status);
 
