@@ -43,6 +43,8 @@ kda_status device_state(unsigned int** err, int* major, int* minor) {
 
 bool dims_ok(int dk, int dv) { return (dk == 64 || dk == 128) && (dv == 64 || dv == 128); }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 size_t blob_bytes(kda_dtype dtype, int dk, int dv) {
   if (dtype == KDA_DTYPE_BF16 && prefill_tc_supported(dk, dv)) return prefill_tc_blob_bytes(dk, dv);
   return prefill_cc_blob_bytes(dk, dv);
@@ -90,6 +92,9 @@ KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, co
   if (T_tot > ((int64_t)1 << 31) * 64 / H) return KDA_ERR_UNSUPPORTED;  // chunk index fits int32
   if (out && (out == q || out == k || out == v || out == (const void*)g || out == (const void*)beta))
     return KDA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(out) ||
+      !aligned16(h0) || !aligned16(hT) || (epi && (!aligned16(epi->gate_logits) || !aligned16(epi->norm_weight))))
+    return KDA_ERR_INVALID_ARG;
   const size_t need = kda_chunk_fwd_workspace_size(B, T, H, dk, dv, C, dtype);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return KDA_ERR_WORKSPACE;
@@ -126,6 +131,7 @@ KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, 
   if (epi && N > 0 && !epi->gate_logits) return KDA_ERR_INVALID_ARG;
   if (epi && !(epi->eps >= 0.f)) return KDA_ERR_INVALID_ARG;
   if ((int64_t)N * H > 0x7fffffff) return KDA_ERR_UNSUPPORTED;
+  if (!aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
   unsigned int* err = nullptr;
   int major = 0, minor = 0;
   kda_status st = device_state(&err, &major, &minor);

@@ -8,32 +8,32 @@
 //   U = U_hat - W S0,  O = Q_hat S0 + M U,  S_C = Diag(e^{G_C}) S0 + K_bar^T U
 // Section 3.2 / Eq. 5 (g > -5) bounds every reference-scaled factor used below by e^{+-80}.
 //
-// Two kernels, both written with tcgen05 MMAs, TMEM accumulators and bulk (TMA-engine) copies:
-//
-//  kda_tc_chunk_prep  (grid = chunks x heads, fully parallel)
-//    - cumulative log-decay G (fp32), reference-scaled operands (two centred references per
-//      chunk, 15 and 47, and 47 for the off-diagonal block);
-//    - one split-tf32 product (three tf32 MMAs per K step, fp32 accumulation), M=128 (64 key rows
-//      + 64 query rows) x N=96 x K=128, yields both A and M: N columns 0..63 are the two diagonal
-//      32x32 blocks, 64..95 the off-diagonal block;
-//    - the unit-lower solve T = (I + A)^-1 Diag(beta) in fp32 on the CUDA cores;
+//  kda_tc_chunk_prep  (persistent, one CTA per SM, loops over (chunk, head) tasks)
+//    - TMA (128-byte swizzle) brings the raw q, k, v, g tiles of the NEXT task into a second
+//      buffer while the current task computes;
+//    - cumulative log-decay G in fp32 (in place), per-channel decay constants;
+//    - A and M as one split-tf32 product (x = x_hi + x_lo, three tf32 MMAs per K step, fp32
+//      accumulation), M=128 (64 key rows + 64 query rows) x N=96 (two diagonal 32x32 blocks with
+//      centred references 15 and 47, plus the off-diagonal block with reference 47), in four
+//      32-channel passes; the same passes emit Q_hat and K_bar (to the record) and K_hat;
+//    - T = (I + A)^-1 Diag(beta) by blocked (16 x 16) forward substitution in fp32;
 //    - fp16 MMAs W^T = K_hat^T T^T and U_hat^T = V^T T^T (M=128, N=64, K=64);
-//    - writes one 74 KB record per (chunk, head) laid out exactly as the scan kernel's shared
-//      memory operands want them (W^T, Q_hat, K_bar, M, U_hat^T in fp16, e^{G_C} in fp32).
+//    - one 74 KB record per (chunk, head), laid out as the scan kernel's shared-memory operands.
 //
 //  kda_tc_chunk_scan  (grid = sequences x heads; serial over the chunks of a sequence)
-//    - S^T (dv x dk, fp32) lives in TMEM for the whole sequence; an fp16 copy in shared memory
-//      is the A operand of the two state products;
-//    - per chunk: D_U = S^T W^T, D_O = S^T Q_hat^T (MMA), U^T = U_hat^T - D_U (CUDA cores, fp16),
-//      S^T = S^T Diag(e^{G_C}) (TMEM ld/st) + U^T K_bar (MMA), D_O += U^T M^T (MMA);
-//    - records are double-buffered with bulk copies so the next chunk's operands arrive while
-//      the current chunk runs; the optional RMSNorm + sigmoid-gate epilogue is fused in.
+//    - warps 0-3 run the state chain: S^T (dv x dk, fp32) lives in TMEM for the whole sequence,
+//      an fp16 copy in shared memory is the A operand of D_U = S^T W^T and D_O = S^T Q_hat^T;
+//      U^T = U_hat^T - D_U; S^T = S^T Diag(e^{G_C}) + U^T K_bar; D_O += U^T M^T;
+//    - warps 4-7 drain the read-out accumulator (double-buffered in TMEM) through a staging
+//      buffer and run the optional RMSNorm + sigmoid-gate epilogue, off the serial path;
+//    - record operands are double-buffered with bulk copies.
 //
 // Precision: bf16 operands cannot meet the parity bound on these workloads (see the design
 // notes); fp16 has the bf16 MMA rate with 3 more significand bits, and every fp16 operand here is
 // bounded (decayed keys/queries <= 1, values and states well inside the fp16 range).  The
 // reference-scaled A/M operands need fp32 range; plain tf32 is enough for A but not for M (it
 // feeds the read-out directly), so the A/M product is split-tf32.  Accumulation is fp32.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -47,28 +47,32 @@ namespace {
 using namespace tc;
 
 // ----------------------------------------------------------------- record layout (bytes)
-constexpr uint32_t kRecWT = 0;        // W^T   [128 dk][64 r] fp16, row format (MN-major B of D_U)
-constexpr uint32_t kRecQH = 16384;    // Q_hat [64 r][128 dk] fp16, token-row blocks (K-major B of D_O)
-constexpr uint32_t kRecKB = 32768;    // K_bar [64 r][128 dk] fp16, token-row blocks (MN-major B of D_S)
-constexpr uint32_t kRecMM = 49152;    // M     [64 r][64 s]   fp16, row format (K-major B of D_O)
-constexpr uint32_t kRecUT = 57344;    // U_hat^T [128 dv][64 r] fp16, row format (read by threads)
-constexpr uint32_t kRecGC = 73728;    // e^{G_C} [128] fp32
-constexpr uint32_t kRecBytes = 75776; // 74 KB, multiple of 1024
+constexpr uint32_t kRecWT = 0;          // W^T   [128 dk][64 r] fp16, row format (MN-major B of D_U)
+constexpr uint32_t kRecQH = 16384;      // Q_hat [64 r][128 dk] fp16, token-row blocks (K-major B of D_O)
+constexpr uint32_t kRecKB = 32768;      // K_bar [64 r][128 dk] fp16, token-row blocks (MN-major B of D_S)
+constexpr uint32_t kRecMM = 49152;      // M     [64 r][64 s]   fp16, row format (K-major B of D_O)
+constexpr uint32_t kRecGC = 57344;      // e^{G_C} [128] fp32
+constexpr uint32_t kRecStage = 57856;   // bytes the scan kernel stages in shared memory
+constexpr uint32_t kRecUT = 59392;      // U_hat^T [128 dv][64 r] fp16, row format (read from global)
+constexpr uint32_t kRecBytes = 75776;   // 74 KB
 
 // ----------------------------------------------------------------- swizzled addressing
-// fp16 [64 rows][128 channels] as two 64-channel blocks of 64 x 128 B, 128-byte swizzle.
-__device__ __forceinline__ uint32_t trow_f16(int r, int c) {
-  return (uint32_t)(c >> 6) * 8192u + (uint32_t)r * 128u + ((((uint32_t)(c >> 3) & 7u) ^ ((uint32_t)r & 7u)) << 4) +
-         ((uint32_t)(c & 7) << 1);
+// fp16/bf16 [64 rows][128 channels] as two 64-channel blocks of 64 x 128 B (128-byte swizzle):
+// byte offset of the 16-byte chunk holding channels 8j..8j+7 of row r.
+__device__ __forceinline__ uint32_t trow_chunk(int r, int c8) {
+  return (uint32_t)(c8 >> 3) * 8192u + (uint32_t)r * 128u + ((((uint32_t)c8 & 7u) ^ ((uint32_t)r & 7u)) << 4);
 }
-// fp16 [R rows][64 cols], one 128-byte row each, 128-byte swizzle.
-__device__ __forceinline__ uint32_t row64_f16(int r, int j) {
-  return (uint32_t)r * 128u + ((((uint32_t)(j >> 3) ^ (uint32_t)r) & 7u) << 4) + ((uint32_t)(j & 7) << 1);
+// fp32 [64 rows][128 channels] as four 32-channel blocks of 64 x 128 B: chunk of channels 4j..4j+3.
+__device__ __forceinline__ uint32_t g_chunk(int r, int c4) {
+  return (uint32_t)(c4 >> 3) * 8192u + (uint32_t)r * 128u + ((((uint32_t)c4 & 7u) ^ ((uint32_t)r & 7u)) << 4);
 }
-// tf32 (fp32 container) [R rows][128 channels] K-major: four 32-channel blocks of R x 128 B.
-__device__ __forceinline__ uint32_t kmaj_tf32(int r, int c, int R) {
-  return (uint32_t)(c >> 5) * (uint32_t)(R * 128) + (uint32_t)r * 128u +
-         ((((uint32_t)(c >> 2) & 7u) ^ ((uint32_t)r & 7u)) << 4) + ((uint32_t)(c & 3) << 2);
+// tf32 [R rows][32 channels] (one 128-byte K block): chunk of channels 4j..4j+3 of row r.
+__device__ __forceinline__ uint32_t op_chunk(int r, int c4) {
+  return (uint32_t)r * 128u + ((((uint32_t)c4 & 7u) ^ ((uint32_t)r & 7u)) << 4);
+}
+// fp16 [R rows][64 cols] row format: chunk j (cols 8j..8j+7) of row r.
+__device__ __forceinline__ uint32_t row_chunk(int r, int j) {
+  return (uint32_t)r * 128u + ((((uint32_t)j ^ (uint32_t)r) & 7u) << 4);
 }
 
 __device__ __forceinline__ float to_tf32(float x) {
@@ -84,20 +88,24 @@ __device__ __forceinline__ float2 unpack_h2(uint32_t u) {
   __half2 h = *reinterpret_cast<__half2*>(&u);
   return __half22float2(h);
 }
-// Write one 64-element fp16 row (row format) from 64 floats.
-__device__ __forceinline__ void store_row64(uint8_t* base, int r, const float* v) {
+__device__ __forceinline__ float2 unpack_bf2(uint32_t u) {
+  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
+  return __bfloat1622float2(h);
+}
+__device__ __forceinline__ uint4 pack8_h(const float* v) {
+  uint4 w;
+  w.x = pack_h2(v[0], v[1]);
+  w.y = pack_h2(v[2], v[3]);
+  w.z = pack_h2(v[4], v[5]);
+  w.w = pack_h2(v[6], v[7]);
+  return w;
+}
+// 64 floats -> one fp16 row (row format) at `dst` (shared or global memory).
+__device__ __forceinline__ void store_row64(uint8_t* dst, int r, const float* v) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint4 w;
-    w.x = pack_h2(v[8 * j + 0], v[8 * j + 1]);
-    w.y = pack_h2(v[8 * j + 2], v[8 * j + 3]);
-    w.z = pack_h2(v[8 * j + 4], v[8 * j + 5]);
-    w.w = pack_h2(v[8 * j + 6], v[8 * j + 7]);
-    *reinterpret_cast<uint4*>(base + (uint32_t)r * 128u + ((((uint32_t)j ^ (uint32_t)r) & 7u) << 4)) = w;
-  }
+  for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(dst + row_chunk(r, j)) = pack8_h(v + 8 * j);
 }
 
-// Instruction descriptors.
 constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | (0u << 7) | (0u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -115,12 +123,9 @@ __device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uin
       "l"(a), "l"(b), "r"(idesc), "r"(acc ? 1u : 0u)
       : "memory");
 }
-
 __device__ __forceinline__ uint32_t tmem_lane(uint32_t base, int warp) {
   return base + ((uint32_t)((warp & 3) * 32) << 16);
 }
-
-// Load 64 consecutive TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -131,291 +136,417 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
   }
   tmem_wait_ld();
 }
+// Named barrier over `n` threads returning the AND of `v` across them.
+__device__ __forceinline__ bool group_and(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void group_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 // =================================================================== prep kernel
 constexpr int kPrepThreads = 256;
-// shared-memory map (offsets from a 1024-aligned base)
-// A/M pass operands (one 64-channel pass at a time), tf32 K-major, 112 KB in total:
-constexpr uint32_t P_XH = 0;          // X hi [128 rows][64 ch] 32 KB
-constexpr uint32_t P_XL = 32768;      // X lo 32 KB
-constexpr uint32_t P_YH = 65536;      // Y hi [96 rows][64 ch] 24 KB
-constexpr uint32_t P_YL = 90112;      // Y lo 24 KB
-// ... reused after the A/M product:
-constexpr uint32_t P_WT = 0;          // fp16 W^T [128][64] 16 KB
-constexpr uint32_t P_UT = 16384;      // fp16 U_hat^T [128][64] 16 KB
-constexpr uint32_t P_SA = 65536;      // fp32 A [64][65] for the solve
-constexpr uint32_t P_KH = 114688;     // fp16 K_hat token-row blocks 16 KB
-constexpr uint32_t P_VV = 131072;     // fp16 V token-row blocks 16 KB
-constexpr uint32_t P_QH = 147456;     // fp16 Q_hat 16 KB
-constexpr uint32_t P_KB = 163840;     // fp16 K_bar 16 KB
-constexpr uint32_t P_TT = 180224;     // fp16 T [64 r][64 s] 8 KB
-constexpr uint32_t P_MM = 188416;     // fp16 M [64 r][64 s] 8 KB
-constexpr uint32_t P_GC = 196608;     // fp32 [128]
-constexpr uint32_t P_BETA = 197120;   // fp32 [64]
-constexpr uint32_t P_REF = 197376;    // fp32 [4][128]: G_15, G_31, G_47, G_63
-constexpr uint32_t P_BAR = 199424;    // 2 mbarriers + TMEM address
-constexpr uint32_t P_END = 199488;
-constexpr uint32_t kPrepSmem = P_END + 1024;
+// raw stage: k | q | v (bf16 token-row blocks) | g (fp32, four 32-channel blocks)
+constexpr uint32_t R_K = 0, R_Q = 16384, R_V = 32768, R_G = 49152, R_BYTES = 81920;
+constexpr uint32_t P_RAW0 = 0;
+constexpr uint32_t P_RAW1 = R_BYTES;
+constexpr uint32_t P_OPS = 2 * R_BYTES;  // 56 KB: one 32-channel pass of split-tf32 operands
+constexpr uint32_t O_XH = 0, O_XL = 16384, O_YH = 32768, O_YL = 45056, O_BYTES = 57344;
+// after the A/M product the operand region holds the solve:
+constexpr uint32_t O_SA = 0;             // fp32 A [64][65]
+constexpr uint32_t O_SX = 16640;         // fp32 X = (I + A)^-1 [64][65]
+constexpr uint32_t O_SY = 33280;         // fp32 scratch, three 16 x 16 blocks
+constexpr uint32_t O_TT = 37888;         // fp16 T [64 r][64 s] row format (1024-aligned)
+constexpr uint32_t P_MISC = P_OPS + O_BYTES;
+constexpr uint32_t M_BETA = 0;           // fp32 [64]
+constexpr uint32_t M_CON = 256;          // fp32 [5][128]: e^{G15}, e^{G47}, e^{G63-G15}, e^{G63-G47}, e^{G47-G15}
+constexpr uint32_t M_BAR = 2816;         // full[2], bar_am, bar_wu, bar_fin; tmem slot
+constexpr uint32_t M_END = 2880;
+constexpr uint32_t kPrepSmem = P_MISC + M_END + 1024;
 
-constexpr uint32_t T_AM = 0;     // TMEM columns: A/M accumulator [128 x 96]
-constexpr uint32_t T_W = 96;     // W^T accumulator [128 x 64]
-constexpr uint32_t T_U = 160;    // U_hat^T accumulator [128 x 64]
+constexpr uint32_t T_AM = 0;   // TMEM: A/M accumulator [128 x 96]
+constexpr uint32_t T_W = 96;   // W^T [128 x 64]
+constexpr uint32_t T_U = 160;  // U_hat^T [128 x 64]
+
+struct PrepMaps {
+  CUtensorMap k, q, v, g;
+};
+
+__device__ __forceinline__ void issue_raw_loads(const PrepMaps& m, uint8_t* raw, uint64_t* bar, int h, int64_t t0) {
+  mbar_arrive_expect_tx(bar, R_BYTES);
+  const int y = (int)t0;
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    tma_load_2d(raw + R_K + 8192 * b, &m.k, h * 128 + 64 * b, y, bar);
+    tma_load_2d(raw + R_Q + 8192 * b, &m.q, h * 128 + 64 * b, y, bar);
+    tma_load_2d(raw + R_V + 8192 * b, &m.v, h * 128 + 64 * b, y, bar);
+  }
+#pragma unroll
+  for (int b = 0; b < 4; ++b) tma_load_2d(raw + R_G + 8192 * b, &m.g, h * 128 + 32 * b, y, bar);
+}
+
+// Next valid task index >= t (tasks: chunk-major, head-minor), or -1.
+__device__ __forceinline__ int64_t next_task(int64_t t, int64_t ntask, int64_t stride, const int32_t* plan,
+                                             const int32_t* cu, int B, int64_t T, int H, int& h, int64_t& t0,
+                                             int& n, int64_t& chunk) {
+  for (; t < ntask; t += stride) {
+    chunk = t / H;
+    h = (int)(t - chunk * H);
+    int b;
+    int64_t cseq;
+    if (resolve_chunk(chunk, plan, cu, B, T, b, t0, n, cseq)) return t;
+  }
+  return -1;
+}
 
 __global__ void __launch_bounds__(kPrepThreads, 1)
-kda_tc_chunk_prep(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                  const __nv_bfloat16* __restrict__ v, const float* __restrict__ g, const float* __restrict__ beta,
+kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict__ beta,
                   const int32_t* __restrict__ plan, const int32_t* __restrict__ cu, int B, int64_t T, int H,
-                  uint8_t* __restrict__ records, unsigned int* __restrict__ err) {
+                  int64_t ntask, uint8_t* __restrict__ records, unsigned int* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar_am = reinterpret_cast<uint64_t*>(sm + P_BAR);
-  uint64_t* bar_wu = bar_am + 1;
-  uint64_t* bar_fin = bar_am + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P_BAR + 32);
-  float* sGC = reinterpret_cast<float*>(sm + P_GC);
-  float* sBeta = reinterpret_cast<float*>(sm + P_BETA);
-  float* sRef = reinterpret_cast<float*>(sm + P_REF);
+  uint8_t* ops = sm + P_OPS;
+  uint8_t* misc = sm + P_MISC;
+  float* sBeta = reinterpret_cast<float*>(misc + M_BETA);
+  float* sCon = reinterpret_cast<float*>(misc + M_CON);
+  uint64_t* full = reinterpret_cast<uint64_t*>(misc + M_BAR);  // [2]
+  uint64_t* bar_am = full + 2;
+  uint64_t* bar_wu = full + 3;
+  uint64_t* bar_fin = full + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + M_BAR + 48);
 
-  const int64_t chunk = blockIdx.x;
-  const int h = blockIdx.y;
-  int b, n;
-  int64_t t0, cseq;
-  if (!resolve_chunk(chunk, plan, cu, B, T, b, t0, n, cseq)) return;
-  uint8_t* rec = records + ((size_t)chunk * H + h) * kRecBytes;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t stride = gridDim.x;
+  int h, n;
+  int64_t t0, chunk;
+  int64_t task = next_task(blockIdx.x, ntask, stride, plan, cu, B, T, H, h, t0, n, chunk);
+  if (task < 0) return;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
     tmem_alloc(tmem_slot, 256);
     tmem_relinquish();
   }
   if (tid == 32) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
     mbar_init(bar_am, 1);
     mbar_init(bar_wu, 1);
     mbar_init(bar_fin, 1);
     mbar_fence_init();
   }
-
-  // ---- 1. cumulative log-decay: thread (channel c, half) owns rows 32*half .. 32*half+31
-  const int c = tid & 127, half = tid >> 7, r0 = 32 * half;
-  float G[32];
-  {
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int r = r0 + i;
-      const float gv = (r < n) ? g[((size_t)(t0 + r) * H + h) * 128 + c] : 0.f;
-      acc += gv;
-      G[i] = acc;
-    }
-  }
-  if (tid < 64) sBeta[tid] = (tid < n) ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
-  if (half == 0) {
-    sRef[0 * 128 + c] = G[15];
-    sRef[1 * 128 + c] = G[31];
-  }
-  __syncthreads();
-  if (half == 1) {
-    const float base = sRef[1 * 128 + c];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) G[i] += base;
-    sRef[2 * 128 + c] = G[15];
-    sRef[3 * 128 + c] = G[31];
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (tid == 0) issue_raw_loads(maps, sm + P_RAW0, &full[0], h, t0);
 
-  // ---- 2. operands
-  {
-    const float G63 = sRef[3 * 128 + c];
-    if (half == 0) sGC[c] = __expf(G63);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int r = r0 + i;
-      const size_t gi = ((size_t)(t0 + r) * H + h) * 128 + c;
-      float kv = 0.f, qv = 0.f, vv = 0.f;
-      if (r < n) {
-        kv = __bfloat162float(k[gi]);
-        qv = __bfloat162float(q[gi]);
-        vv = __bfloat162float(v[gi]);
-      }
-      const float Gr = G[i];
-      const float eG = __expf(Gr);
-      *reinterpret_cast<__half*>(sm + P_KH + trow_f16(r, c)) = __float2half_rn(kv * eG);
-      *reinterpret_cast<__half*>(sm + P_QH + trow_f16(r, c)) = __float2half_rn(qv * eG);
-      *reinterpret_cast<__half*>(sm + P_KB + trow_f16(r, c)) = __float2half_rn(kv * __expf(G63 - Gr));
-      *reinterpret_cast<__half*>(sm + P_VV + trow_f16(r, c)) = __float2half_rn(vv);
-    }
-  }
-  // ---- 3. A and M: D[128 x 96] = X[128 x 128] Y[96 x 128]^T with X = [k e^{G-R}; q e^{G-R}],
-  // Y = [k e^{R-G}; k e^{G_47-G} (s < 32)], as split-tf32 products (x = x_hi + x_lo, three MMAs:
-  // hi*hi + hi*lo + lo*hi, fp32 accumulation; ~fp32 accuracy, which M needs for the read-out).
-  // The operands of both splits do not fit at once, so the 128 channels go in two passes of 64.
   bool ok = true;
-#pragma unroll 1
-  for (int pass = 0; pass < 2; ++pass) {
-    if (pass == 1) ok = __syncthreads_and(ok && mbar_wait(bar_am, 0)) != 0;  // pass 0 MMAs done
-    if ((c >> 6) == pass) {
-      const int cc = c & 63;
-      const float R = sRef[(half == 0 ? 0 : 2) * 128 + c];
-      const float G47 = sRef[2 * 128 + c];
+  uint32_t it = 0;
+  while (task >= 0 && ok) {
+    const int st = (int)(it & 1);
+    uint8_t* raw = sm + (st ? P_RAW1 : P_RAW0);
+    uint8_t* rec = records + ((size_t)chunk * H + h) * kRecBytes;
+    // next task: resolve and prefetch its raw tiles into the other stage
+    int nh = 0, nn = 0;
+    int64_t nt0 = 0, nchunk = 0;
+    const int64_t ntask_idx = next_task(task + stride, ntask, stride, plan, cu, B, T, H, nh, nt0, nn, nchunk);
+    if (tid == 0 && ntask_idx >= 0) issue_raw_loads(maps, sm + (st ? P_RAW0 : P_RAW1), &full[st ^ 1], nh, nt0);
+    float bval = 0.f;
+    if (tid < 64 && tid < n) bval = beta[(size_t)(t0 + tid) * H + h];
+    ok = __syncthreads_and(mbar_wait(&full[st], (it >> 1) & 1)) != 0;
+    if (!ok) break;
+
+    // ---- cumulative log-decay (threads 0..127, one channel each, in place), V -> fp16 (128..255)
+    if (tid < 128) {
+      const int c = tid;
+      float acc = 0.f;
+      float* gcol = reinterpret_cast<float*>(raw + R_G);
+      const uint32_t cb = (uint32_t)(c >> 5) * 2048u, cw = (uint32_t)(c & 3), cc4 = (uint32_t)((c >> 2) & 7);
+#pragma unroll 8
+      for (int r = 0; r < 64; ++r) {
+        float* p = gcol + cb + (uint32_t)r * 32u + (((cc4 ^ ((uint32_t)r & 7u)) << 2) | cw);
+        acc += (r < n) ? *p : 0.f;
+        *p = acc;
+      }
+    } else {
+      const int t = tid - 128;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int r = r0 + i;
-        const size_t gi = ((size_t)(t0 + r) * H + h) * 128 + c;
-        float kv = 0.f, qv = 0.f;
-        if (r < n) {
-          kv = __bfloat162float(k[gi]);
-          qv = __bfloat162float(q[gi]);
+      for (int i = 0; i < 8; ++i) {  // 1024 chunks of 8 values / 128 threads
+        const int idx = t + 128 * i, r = idx >> 4, c8 = idx & 15;
+        uint4* p = reinterpret_cast<uint4*>(raw + R_V + trow_chunk(r, c8));
+        uint4 w = *p;
+        float f[8];
+        const float2 a0 = unpack_bf2(w.x), a1 = unpack_bf2(w.y), a2 = unpack_bf2(w.z), a3 = unpack_bf2(w.w);
+        f[0] = a0.x; f[1] = a0.y; f[2] = a1.x; f[3] = a1.y; f[4] = a2.x; f[5] = a2.y; f[6] = a3.x; f[7] = a3.y;
+        if (r >= n)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] = 0.f;
+        *p = pack8_h(f);
+      }
+    }
+    if (tid < 64) sBeta[tid] = bval;
+    __syncthreads();
+    // per-channel decay constants and e^{G_C} for the record
+    if (tid < 128) {
+      const int c = tid;
+      const float* gb = reinterpret_cast<const float*>(raw + R_G);
+      auto G = [&](int r) {
+        return gb[(uint32_t)(c >> 5) * 2048u + (uint32_t)r * 32u + (((((uint32_t)c >> 2) & 7u) ^ ((uint32_t)r & 7u)) << 2) +
+                  ((uint32_t)c & 3u)];
+      };
+      const float g15 = G(15), g47 = G(47), g63 = G(63);
+      // Only factors that cannot underflow while the product they help form is still
+      // significant are precomputed: e^{G15} >= e^{-80} and e^{G63-G47} >= e^{-80} always;
+      // e^{G47} may underflow, but then every q/k e^{G_r} it scales (r >= 32) is below e^{-12}.
+      sCon[0 * 128 + c] = __expf(g15);
+      sCon[1 * 128 + c] = __expf(g47);
+      sCon[2 * 128 + c] = g47;
+      sCon[3 * 128 + c] = __expf(g63 - g47);
+      sCon[4 * 128 + c] = g63;
+      reinterpret_cast<float*>(rec + kRecGC)[c] = __expf(g63);
+    }
+    __syncthreads();
+
+    // ---- A and M: four 32-channel passes of split-tf32 operands, three MMAs per K step
+    {
+      const int r = tid >> 2;            // row 0..63
+      const int cq = (tid & 3) * 8;      // 8 channels within the pass
+      const bool valid = r < n;
+      const int rref = r < 32 ? 15 : 47;
+      const int hsel = r < 32 ? 0 : 1;
+#pragma unroll 1
+      for (int pass = 0; pass < 4; ++pass) {
+        if (pass > 0) {
+          ok = __syncthreads_and(ok && mbar_wait(bar_am, (pass - 1) & 1)) != 0;
+          if (!ok) break;
         }
-        const float Gr = G[i];
-        const float e1 = __expf(Gr - R), e2 = __expf(R - Gr);
-        float x, hi;
-        x = kv * e1; hi = to_tf32(x);
-        *reinterpret_cast<float*>(sm + P_XH + kmaj_tf32(r, cc, 128)) = hi;
-        *reinterpret_cast<float*>(sm + P_XL + kmaj_tf32(r, cc, 128)) = to_tf32(x - hi);
-        x = qv * e1; hi = to_tf32(x);
-        *reinterpret_cast<float*>(sm + P_XH + kmaj_tf32(64 + r, cc, 128)) = hi;
-        *reinterpret_cast<float*>(sm + P_XL + kmaj_tf32(64 + r, cc, 128)) = to_tf32(x - hi);
-        x = kv * e2; hi = to_tf32(x);
-        *reinterpret_cast<float*>(sm + P_YH + kmaj_tf32(r, cc, 96)) = hi;
-        *reinterpret_cast<float*>(sm + P_YL + kmaj_tf32(r, cc, 96)) = to_tf32(x - hi);
-        if (half == 0) {
-          x = kv * __expf(G47 - Gr); hi = to_tf32(x);
-          *reinterpret_cast<float*>(sm + P_YH + kmaj_tf32(64 + r, cc, 96)) = hi;
-          *reinterpret_cast<float*>(sm + P_YL + kmaj_tf32(64 + r, cc, 96)) = to_tf32(x - hi);
+        const int c0 = 32 * pass + cq;   // first of this thread's 8 channels
+        float kv[8], qv[8], G[8], R[8];
+        {
+          const uint4 wk = *reinterpret_cast<const uint4*>(raw + R_K + trow_chunk(r, c0 >> 3));
+          const uint4 wq = *reinterpret_cast<const uint4*>(raw + R_Q + trow_chunk(r, c0 >> 3));
+          const uint32_t ku[4] = {wk.x, wk.y, wk.z, wk.w}, qu[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 a = unpack_bf2(ku[j]), b = unpack_bf2(qu[j]);
+            kv[2 * j] = valid ? a.x : 0.f; kv[2 * j + 1] = valid ? a.y : 0.f;
+            qv[2 * j] = valid ? b.x : 0.f; qv[2 * j + 1] = valid ? b.y : 0.f;
+          }
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float4 g4 = *reinterpret_cast<const float4*>(raw + R_G + g_chunk(r, (c0 >> 2) + hh));
+            const float4 r4 = *reinterpret_cast<const float4*>(raw + R_G + g_chunk(rref, (c0 >> 2) + hh));
+            G[4 * hh + 0] = g4.x; G[4 * hh + 1] = g4.y; G[4 * hh + 2] = g4.z; G[4 * hh + 3] = g4.w;
+            R[4 * hh + 0] = r4.x; R[4 * hh + 1] = r4.y; R[4 * hh + 2] = r4.z; R[4 * hh + 3] = r4.w;
+          }
+        }
+        float xkh[8], xkl[8], xqh[8], xql[8], yh[8], yl[8], zh[8], zl[8], qh[8], kb[8], kh[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = c0 + j;
+          const float e1 = __expf(G[j] - R[j]);
+          const float e2 = __expf(R[j] - G[j]);
+          float x = kv[j] * e1;
+          xkh[j] = to_tf32(x); xkl[j] = to_tf32(x - xkh[j]);
+          x = qv[j] * e1;
+          xqh[j] = to_tf32(x); xql[j] = to_tf32(x - xqh[j]);
+          x = kv[j] * e2;
+          yh[j] = to_tf32(x); yl[j] = to_tf32(x - yh[j]);
+          const float eR = sCon[hsel * 128 + c];
+          qh[j] = qv[j] * e1 * eR;  // q e^{G}
+          kh[j] = kv[j] * e1 * eR;  // k e^{G}
+          if (hsel == 0) {
+            // rows < 32: k e^{G_47 - G} (off-diagonal block operand) and k e^{G_C - G}, each from
+            // one exponential: the factored forms can underflow while the product is O(1)
+            x = kv[j] * __expf(sCon[2 * 128 + c] - G[j]);
+            zh[j] = to_tf32(x); zl[j] = to_tf32(x - zh[j]);
+            kb[j] = kv[j] * __expf(sCon[4 * 128 + c] - G[j]);
+          } else {
+            zh[j] = 0.f; zl[j] = 0.f;
+            kb[j] = kv[j] * e2 * sCon[3 * 128 + c];  // e^{G_C - G_47} >= e^{-80}: no underflow
+          }
+        }
+        const int c4 = (c0 & 31) >> 2;   // first tf32 chunk within the pass's 128-byte rows
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int o = 4 * hh;
+          *reinterpret_cast<float4*>(ops + O_XH + op_chunk(r, c4 + hh)) = make_float4(xkh[o], xkh[o + 1], xkh[o + 2], xkh[o + 3]);
+          *reinterpret_cast<float4*>(ops + O_XL + op_chunk(r, c4 + hh)) = make_float4(xkl[o], xkl[o + 1], xkl[o + 2], xkl[o + 3]);
+          *reinterpret_cast<float4*>(ops + O_XH + op_chunk(64 + r, c4 + hh)) = make_float4(xqh[o], xqh[o + 1], xqh[o + 2], xqh[o + 3]);
+          *reinterpret_cast<float4*>(ops + O_XL + op_chunk(64 + r, c4 + hh)) = make_float4(xql[o], xql[o + 1], xql[o + 2], xql[o + 3]);
+          *reinterpret_cast<float4*>(ops + O_YH + op_chunk(r, c4 + hh)) = make_float4(yh[o], yh[o + 1], yh[o + 2], yh[o + 3]);
+          *reinterpret_cast<float4*>(ops + O_YL + op_chunk(r, c4 + hh)) = make_float4(yl[o], yl[o + 1], yl[o + 2], yl[o + 3]);
+          if (r < 32) {
+            *reinterpret_cast<float4*>(ops + O_YH + op_chunk(64 + r, c4 + hh)) = make_float4(zh[o], zh[o + 1], zh[o + 2], zh[o + 3]);
+            *reinterpret_cast<float4*>(ops + O_YL + op_chunk(64 + r, c4 + hh)) = make_float4(zl[o], zl[o + 1], zl[o + 2], zl[o + 3]);
+          }
+        }
+        *reinterpret_cast<uint4*>(rec + kRecQH + trow_chunk(r, c0 >> 3)) = pack8_h(qh);
+        *reinterpret_cast<uint4*>(rec + kRecKB + trow_chunk(r, c0 >> 3)) = pack8_h(kb);
+        *reinterpret_cast<uint4*>(raw + R_K + trow_chunk(r, c0 >> 3)) = pack8_h(kh);  // K_hat in place
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+          tc_fence_after();
+          const uint32_t idesc = idesc_tf32(128, 96);
+#pragma unroll
+          for (int k0 = 0; k0 < 32; k0 += 8) {
+            const uint32_t kk = (uint32_t)k0 * 4u;
+            const uint64_t xh = smem_desc_sw128(smem_u32(ops + O_XH) + kk, 16, 1024);
+            const uint64_t xl = smem_desc_sw128(smem_u32(ops + O_XL) + kk, 16, 1024);
+            const uint64_t yhd = smem_desc_sw128(smem_u32(ops + O_YH) + kk, 16, 1024);
+            const uint64_t yld = smem_desc_sw128(smem_u32(ops + O_YL) + kk, 16, 1024);
+            mma_tf32(tmem + T_AM, xh, yhd, idesc, pass > 0 || k0 > 0);
+            mma_tf32(tmem + T_AM, xh, yld, idesc, true);
+            mma_tf32(tmem + T_AM, xl, yhd, idesc, true);
+          }
+          mma_commit(bar_am);
+        }
+      }
+    }
+    if (!ok) break;
+    ok = __syncthreads_and(mbar_wait(bar_am, 1)) != 0;  // 4th completion of this task: parity 1
+    if (!ok) break;
+    tc_fence_after();
+
+    // ---- TMEM -> A (fp32, beta-scaled strict lower) and M (fp16, straight into the record)
+    float* sA = reinterpret_cast<float*>(ops + O_SA);
+    if (warp < 4) {
+      const int lrow = warp * 32 + lane;  // 0..63 key rows (A), 64..127 query rows (M)
+      const int r = lrow & 63;
+      float d[96];
+#pragma unroll
+      for (int q4 = 0; q4 < 6; ++q4) {
+        float t[16];
+        tmem_ld16(tmem_lane(tmem + T_AM, warp) + 16 * q4, t);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) d[16 * q4 + j] = t[j];
+      }
+      tmem_wait_ld();
+      float row[64];
+#pragma unroll
+      for (int s = 0; s < 64; ++s) {
+        const bool same = (s >> 5) == (r >> 5);
+        const float raw_v = same ? d[s] : ((r >= 32 && s < 32) ? d[64 + (s & 31)] : 0.f);
+        row[s] = raw_v;
+      }
+      if (lrow < 64) {
+        const float br = sBeta[r];
+#pragma unroll
+        for (int s = 0; s < 64; ++s) sA[r * 65 + s] = (s < r) ? br * row[s] : 0.f;  // select, not mask-multiply
+      } else {
+#pragma unroll
+        for (int s = 0; s < 64; ++s) row[s] = (s <= r) ? row[s] : 0.f;
+        store_row64(rec + kRecMM, r, row);
+      }
+    }
+    __syncthreads();
+
+    // ---- T = (I + A)^-1 Diag(beta), blocked 16 x 16 forward substitution (fp32)
+    {
+      float* sX = reinterpret_cast<float*>(ops + O_SX);
+      float* sY = reinterpret_cast<float*>(ops + O_SY);
+      // diagonal blocks: one thread per column, substitution inside its 16 x 16 block
+      if (tid < 64) {
+        const int s = tid, r0 = s & ~15;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = r0 + i;
+          float acc = 0.f;
+#pragma unroll
+          for (int j = 0; j < i; ++j) acc = fmaf(sA[r * 65 + r0 + j], x[j], acc);
+          x[i] = (r == s) ? 1.f : ((r < s) ? 0.f : -acc);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sX[(r0 + i) * 65 + s] = x[i];
+      }
+      __syncthreads();
+      // block rows 1..3: X_ij = -X_ii * sum_{m=j}^{i-1} A_im X_mj
+      const int rr = tid >> 4, cc = tid & 15;
+#pragma unroll 1
+      for (int i = 1; i < 4; ++i) {
+        for (int j = 0; j < i; ++j) {
+          float acc = 0.f;
+          for (int m = j; m < i; ++m) {
+#pragma unroll
+            for (int k2 = 0; k2 < 16; ++k2)
+              acc = fmaf(sA[(16 * i + rr) * 65 + 16 * m + k2], sX[(16 * m + k2) * 65 + 16 * j + cc], acc);
+          }
+          sY[j * 256 + rr * 16 + cc] = acc;
+        }
+        __syncthreads();
+        for (int j = 0; j < i; ++j) {
+          float acc = 0.f;
+#pragma unroll
+          for (int k2 = 0; k2 < 16; ++k2)
+            acc = fmaf(sX[(16 * i + rr) * 65 + 16 * i + k2], sY[j * 256 + k2 * 16 + cc], acc);
+          sX[(16 * i + rr) * 65 + 16 * j + cc] = -acc;
+        }
+        __syncthreads();
+      }
+      // T = X Diag(beta) -> fp16 row format [r][s] (zero above the diagonal)
+      {
+        const int r = tid >> 2, j0 = (tid & 3) * 2;  // two 8-column chunks per thread
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = j0 + jj;
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int s = 8 * j + e;
+            v[e] = (s <= r) ? sX[r * 65 + s] * sBeta[s] : 0.f;
+          }
+          *reinterpret_cast<uint4*>(ops + O_TT + row_chunk(r, j)) = pack8_h(v);
         }
       }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && ok) {
+
+    // ---- W^T = K_hat^T T^T, U_hat^T = V^T T^T (fp16 MMAs, M=128, N=64, K=64)
+    if (tid == 0) {
       tc_fence_after();
-      const uint32_t idesc = idesc_tf32(128, 96);
+      const uint32_t idesc = idesc_f16(128, 64, /*a_mn=*/true, /*b_mn=*/false);
 #pragma unroll
-      for (int k0 = 0; k0 < 64; k0 += 8) {
-        const uint32_t kb = k0 >> 5, kk = (k0 & 31) * 4;
-        const uint64_t xh = smem_desc_sw128(smem_u32(sm + P_XH) + kb * 128 * 128 + kk, 16, 1024);
-        const uint64_t xl = smem_desc_sw128(smem_u32(sm + P_XL) + kb * 128 * 128 + kk, 16, 1024);
-        const uint64_t yh = smem_desc_sw128(smem_u32(sm + P_YH) + kb * 96 * 128 + kk, 16, 1024);
-        const uint64_t yl = smem_desc_sw128(smem_u32(sm + P_YL) + kb * 96 * 128 + kk, 16, 1024);
-        mma_tf32(tmem + T_AM, xh, yh, idesc, pass > 0 || k0 > 0);
-        mma_tf32(tmem + T_AM, xh, yl, idesc, true);
-        mma_tf32(tmem + T_AM, xl, yh, idesc, true);
+      for (int k0 = 0; k0 < 64; k0 += 16) {
+        const uint64_t bd = smem_desc_sw128(smem_u32(ops + O_TT) + k0 * 2, 16, 1024);
+        const uint64_t ak = smem_desc_sw128(smem_u32(raw + R_K) + (k0 >> 3) * 1024, 8192, 1024);
+        const uint64_t av = smem_desc_sw128(smem_u32(raw + R_V) + (k0 >> 3) * 1024, 8192, 1024);
+        mma_f16(tmem + T_W, ak, bd, idesc, k0 > 0);
+        mma_f16(tmem + T_U, av, bd, idesc, k0 > 0);
       }
-      mma_commit(bar_am);
+      mma_commit(bar_wu);
     }
-  }
-  ok = __syncthreads_and(ok && mbar_wait(bar_am, 1)) != 0;
-  tc_fence_after();
-
-  // ---- 4. TMEM -> A (fp32, smem, beta-scaled strict lower) and M (fp16 record operand)
-  float* sA = reinterpret_cast<float*>(sm + P_SA);  // [64][65]
-  if (ok && warp < 4) {
-    const int lane_row = warp * 32 + (tid & 31);  // 0..63: key rows (A); 64..127: query rows (M)
-    const int r = lane_row & 63;
-    float d[96];
-#pragma unroll
-    for (int q4 = 0; q4 < 6; ++q4) {
-      float t[16];
-      tmem_ld16(tmem_lane(tmem + T_AM, warp) + 16 * q4, t);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) d[16 * q4 + j] = t[j];
-    }
-    tmem_wait_ld();
-    if (lane_row < 64) {
-      const float br = sBeta[r];
-#pragma unroll
-      for (int s = 0; s < 64; ++s) {
-        const bool same = (s >> 5) == (r >> 5);
-        const float raw = same ? d[s] : ((r >= 32 && s < 32) ? d[64 + (s & 31)] : 0.f);
-        sA[r * 65 + s] = (s < r) ? br * raw : 0.f;  // select, never multiply a mask
-      }
-    } else {
-      float m[64];
-#pragma unroll
-      for (int s = 0; s < 64; ++s) {
-        const bool same = (s >> 5) == (r >> 5);
-        const float raw = same ? d[s] : ((r >= 32 && s < 32) ? d[64 + (s & 31)] : 0.f);
-        m[s] = (s <= r) ? raw : 0.f;
-      }
-      store_row64(sm + P_MM, r, m);
-    }
-  }
-  __syncthreads();
-
-  // ---- 5. T = (I + A)^-1 Diag(beta): forward substitution, 4 threads per column
-  if (ok) {
-    const int s = tid >> 2, part = tid & 3;
-    float x[16];
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj) x[jj] = 0.f;
-#pragma unroll
-    for (int r = 0; r < 64; ++r) {
-      float acc = 0.f;
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int j = 4 * jj + part;
-        if (j < r) acc = fmaf(sA[r * 65 + j], x[jj], acc);
-      }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      const float xv = (r == s) ? 1.f : ((r < s) ? 0.f : -acc);
-      if (part == (r & 3)) x[r >> 2] = xv;
-    }
-    const float bs = sBeta[s];
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj)
-      *reinterpret_cast<__half*>(sm + P_TT + row64_f16(4 * jj + part, s)) = __float2half_rn(x[jj] * bs);
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- 6. W^T = K_hat^T T^T, U_hat^T = V^T T^T (fp16, M=128, N=64, K=64)
-  if (tid == 0 && ok) {
+    ok = __syncthreads_and(mbar_wait(bar_wu, it & 1)) != 0;
+    if (!ok) break;
     tc_fence_after();
-    const uint32_t idesc = idesc_f16(128, 64, /*a_mn=*/true, /*b_mn=*/false);
-#pragma unroll
-    for (int k0 = 0; k0 < 64; k0 += 16) {
-      const uint64_t bd = smem_desc_sw128(smem_u32(sm + P_TT) + k0 * 2, 16, 1024);
-      const uint64_t ak = smem_desc_sw128(smem_u32(sm + P_KH) + (k0 >> 3) * 1024, 8192, 1024);
-      const uint64_t av = smem_desc_sw128(smem_u32(sm + P_VV) + (k0 >> 3) * 1024, 8192, 1024);
-      mma_f16(tmem + T_W, ak, bd, idesc, k0 > 0);
-      mma_f16(tmem + T_U, av, bd, idesc, k0 > 0);
+    {
+      const int row = (warp & 3) * 32 + lane;  // dk row (W^T, warps 0-3) or dv row (U_hat^T, warps 4-7)
+      float vrow[64];
+      tmem_ld64(tmem_lane(tmem + (warp < 4 ? T_W : T_U), warp), vrow);
+      store_row64(rec + (warp < 4 ? kRecWT : kRecUT), row, vrow);
     }
-    mma_commit(bar_wu);
+    fence_proxy_async_smem();  // generic writes of this stage happen before the next TMA into it
+    tc_fence_before();
+    __syncthreads();
+    task = ntask_idx;
+    h = nh; n = nn; t0 = nt0; chunk = nchunk;
+    ++it;
   }
-  ok = __syncthreads_and(ok && mbar_wait(bar_wu, 0)) != 0;
-  tc_fence_after();
 
-  // ---- 7. TMEM -> fp16 W^T (warps 0-3) and U_hat^T (warps 4-7) rows, into the old XA region
-  if (ok) {
-    const int row = (warp & 3) * 32 + (tid & 31);  // dk row (W^T) or dv row (U_hat^T)
-    float vrow[64];
-    tmem_ld64(tmem_lane(tmem + (warp < 4 ? T_W : T_U), warp), vrow);
-    store_row64(sm + (warp < 4 ? P_WT : P_UT), row, vrow);
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- 8. record -> global (bulk copies), then release TMEM
-  if (tid == 0 && ok) {
-    bulk_s2g(rec + kRecWT, sm + P_WT, 16384);
-    bulk_s2g(rec + kRecQH, sm + P_QH, 16384);
-    bulk_s2g(rec + kRecKB, sm + P_KB, 16384);
-    bulk_s2g(rec + kRecMM, sm + P_MM, 8192);
-    bulk_s2g(rec + kRecUT, sm + P_UT, 16384);
-    bulk_s2g(rec + kRecGC, sm + P_GC, 512);
-    bulk_commit();
-    bulk_wait_all();
-  }
-  if (tid == 0 && !ok) {
-    // a wait ran out: record it, let this thread's issued MMAs drain (bounded), then free TMEM
+  if (!ok && tid == 0) {
+    // a wait ran out: record it; let in-flight TMA loads and MMAs drain (bounded), free TMEM
     atomicOr(err, KDA_DEVERR_WAIT_TIMEOUT);
+    mbar_wait(&full[(it + 1) & 1], ((it + 1) >> 1) & 1);
     mma_commit(bar_fin);
     mbar_wait(bar_fin, 0);
   }
@@ -426,33 +557,27 @@ kda_tc_chunk_prep(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
 }
 
 // =================================================================== scan kernel
-constexpr int kScanThreads = 128;
+constexpr int kScanThreads = 256;
+constexpr uint32_t kStage = 59392;               // staged record bytes, 1024-aligned
 constexpr uint32_t S_STAGE0 = 0;
-constexpr uint32_t S_STAGE1 = kRecBytes;
-constexpr uint32_t S_SA = 2 * kRecBytes;          // fp16 S^T [128 dv][128 dk], two 16 KB K-blocks
-constexpr uint32_t S_UA = S_SA + 32768;           // fp16 U^T [128 dv][64 r]
-constexpr uint32_t S_BAR = S_UA + 16384;          // full[2], bar_u, bar_s, bar_o, bar_fin, tmem slot
-constexpr uint32_t S_END = S_BAR + 64;
+constexpr uint32_t S_STAGE1 = kStage;
+constexpr uint32_t S_SA = 2 * kStage;            // fp16 S^T [128 dv][128 dk], two 16 KB K-blocks
+constexpr uint32_t S_UA = S_SA + 32768;          // fp16 U^T [128 dv][64 r]
+constexpr uint32_t S_OUT = S_UA + 16384;         // fp32 read-out staging [64 r][128 dv]
+constexpr uint32_t S_BAR = S_OUT + 32768;        // barriers + tmem slot
+constexpr uint32_t S_END = S_BAR + 128;
 constexpr uint32_t kScanSmem = S_END + 1024;
 
 constexpr uint32_t T_S = 0;      // TMEM: S^T fp32 [128 x 128]
 constexpr uint32_t T_DU = 128;   // D_U [128 x 64]
-constexpr uint32_t T_DO = 192;   // D_O [128 x 64]
+constexpr uint32_t T_DO = 192;   // D_O, two buffers [128 x 64] at 192 and 256
 
-// fp16 S^T element address: two K-blocks (dk 0..63, 64..127) of [128 rows][128 B]
 __device__ __forceinline__ void store_srow(uint8_t* sa, int row, const float* s) {
 #pragma unroll
   for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float* p = s + 64 * kb + 8 * j;
-      uint4 w;
-      w.x = pack_h2(p[0], p[1]);
-      w.y = pack_h2(p[2], p[3]);
-      w.z = pack_h2(p[4], p[5]);
-      w.w = pack_h2(p[6], p[7]);
-      *reinterpret_cast<uint4*>(sa + kb * 16384 + (uint32_t)row * 128u + ((((uint32_t)j ^ (uint32_t)row) & 7u) << 4)) = w;
-    }
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint4*>(sa + kb * 16384 + row_chunk(row, j)) = pack8_h(s + 64 * kb + 8 * j);
 }
 
 template <typename Tout>
@@ -463,14 +588,16 @@ kda_tc_chunk_scan(const uint8_t* __restrict__ records, const int32_t* __restrict
                   const float* __restrict__ norm_w, float eps, unsigned int* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [2]
-  uint64_t* bar_u = full + 2;
-  uint64_t* bar_s = full + 3;
-  uint64_t* bar_o = full + 4;
-  uint64_t* bar_fin = full + 5;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 48);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [2] record staged
+  uint64_t* bar_u = full + 2;                                // D_U ready
+  uint64_t* bar_s = full + 3;                                // S^T updated
+  uint64_t* bar_o = full + 4;                                // [2] D_O[b] complete
+  uint64_t* do_free = full + 6;                              // [2] D_O[b] read by the output warps
+  uint64_t* bar_fin = full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 80);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S_BAR + 84);
 
-  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (cu != nullptr && plan[B + 1] == 0) return;  // invalid cu_seqlens: sequence skipped
   int64_t first_chunk, t_begin, len;
   const int64_t nchunks = sequence_chunks(b, plan, cu, B, T, first_chunk, t_begin, len);
@@ -480,212 +607,227 @@ kda_tc_chunk_scan(const uint8_t* __restrict__ records, const int32_t* __restrict
     tmem_relinquish();
   }
   if (tid == 32) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
-    mbar_init(bar_u, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
-    mbar_init(bar_fin, 1);
+    for (int i = 0; i < 9; ++i) mbar_init(&full[i], 1);
+    *abort_flag = 0;
     mbar_fence_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tl = tmem_lane(tmem, warp);  // this warp's lane quadrant
-  const int row = tid;                         // dv row owned by this thread (TMEM lane)
-
-  // initial state: S^T[row][dk] = h0[dk][row]
-  {
-    const size_t soff = ((size_t)b * H + h) * 128 * 128;
-    float s[128];
-#pragma unroll
-    for (int c = 0; c < 128; ++c) s[c] = h0 ? h0[soff + (size_t)c * 128 + row] : 0.f;
-#pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) {
-      float t[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) t[j] = s[16 * q4 + j];
-      tmem_st16(tl + T_S + 16 * q4, t);
-    }
-    tmem_wait_st();
-    store_srow(sm + S_SA, row, s);
-  }
-  if (tid == 0 && nchunks > 0) {
-    mbar_arrive_expect_tx(&full[0], kRecBytes);
-    bulk_g2s(sm + S_STAGE0, records + ((size_t)first_chunk * H + h) * kRecBytes, kRecBytes, &full[0]);
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
+  const uint32_t tl = tmem_lane(tmem, warp);
+  const int row = (warp & 3) * 32 + lane;  // TMEM lane = dv row
+  const size_t soff = ((size_t)b * H + h) * 128 * 128;
+  const uint8_t* rec0 = records + ((size_t)first_chunk * H + h) * kRecBytes;
+  const size_t rec_stride = (size_t)H * kRecBytes;
 
   bool ok = true;
-  int64_t pending = nchunks > 0 ? 0 : -1;  // chunk whose record load is in flight / unconsumed
-  for (int64_t c = 0; c < nchunks && ok; ++c) {
-    const int st = (int)(c & 1);
-    uint8_t* stage = sm + (st ? S_STAGE1 : S_STAGE0);
-    const uint32_t ph = (uint32_t)(c & 1);
-    // prefetch the next record into the other stage (freed at the end of chunk c-1)
-    if (tid == 0 && c + 1 < nchunks) {
-      uint8_t* nst = sm + (st ? S_STAGE0 : S_STAGE1);
-      mbar_arrive_expect_tx(&full[st ^ 1], kRecBytes);
-      bulk_g2s(nst, records + ((size_t)(first_chunk + c + 1) * H + h) * kRecBytes, kRecBytes, &full[st ^ 1]);
-    }
-    if (!__syncthreads_and(mbar_wait(&full[st], (uint32_t)((c >> 1) & 1)))) { ok = false; break; }
-    pending = c + 1 < nchunks ? c + 1 : -1;
-    tc_fence_after();
-
-    // MMA: D_U = S^T W^T ; D_O = S^T Q_hat^T
-    if (tid == 0) {
-      const uint32_t id_u = idesc_f16(128, 64, false, true);
-      const uint32_t id_o = idesc_f16(128, 64, false, false);
-#pragma unroll
-      for (int k0 = 0; k0 < 128; k0 += 16) {
-        const uint32_t kb = k0 >> 6, kk = (k0 & 63) * 2;
-        const uint64_t ad = smem_desc_sw128(smem_u32(sm + S_SA) + kb * 16384 + kk, 16, 1024);
-        const uint64_t bw = smem_desc_sw128(smem_u32(stage + kRecWT) + (k0 >> 3) * 1024, 8192, 1024);
-        mma_f16(tmem + T_DU, ad, bw, id_u, k0 > 0);
-      }
-      mma_commit(bar_u);
-#pragma unroll
-      for (int k0 = 0; k0 < 128; k0 += 16) {
-        const uint32_t kb = k0 >> 6, kk = (k0 & 63) * 2;
-        const uint64_t ad = smem_desc_sw128(smem_u32(sm + S_SA) + kb * 16384 + kk, 16, 1024);
-        const uint64_t bq = smem_desc_sw128(smem_u32(stage + kRecQH) + kb * 8192 + kk, 16, 1024);
-        mma_f16(tmem + T_DO, ad, bq, id_o, k0 > 0);
-      }
-    }
-    __syncwarp();
-
-    // while the MMAs run: S^T <- S^T Diag(e^{G_C}) in TMEM (the MMAs read the fp16 copy)
+  if (warp < 4) {
+    // ======================== state warps
     {
-      const float* gc = reinterpret_cast<const float*>(stage + kRecGC);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = h0 ? h0[soff + (size_t)c * 128 + row] : 0.f;
 #pragma unroll
       for (int q4 = 0; q4 < 8; ++q4) {
         float t[16];
-        tmem_ld16(tl + T_S + 16 * q4, t);
-        tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) t[j] *= gc[16 * q4 + j];
+        for (int j = 0; j < 16; ++j) t[j] = s[16 * q4 + j];
         tmem_st16(tl + T_S + 16 * q4, t);
       }
       tmem_wait_st();
+      store_srow(sm + S_SA, row, s);
     }
-
-    // U^T = U_hat^T - D_U  -> fp16 A operand
-    if (!__syncthreads_and(mbar_wait(bar_u, ph))) { ok = false; break; }
-    tc_fence_after();
-    {
-      float u[64];
-      tmem_ld64(tl + T_DU, u);
-      const uint8_t* ut = stage + kRecUT + (uint32_t)row * 128u;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint4 w = *reinterpret_cast<const uint4*>(ut + ((((uint32_t)j ^ (uint32_t)row) & 7u) << 4));
-        const float2 a0 = unpack_h2(w.x), a1 = unpack_h2(w.y), a2 = unpack_h2(w.z), a3 = unpack_h2(w.w);
-        u[8 * j + 0] = a0.x - u[8 * j + 0]; u[8 * j + 1] = a0.y - u[8 * j + 1];
-        u[8 * j + 2] = a1.x - u[8 * j + 2]; u[8 * j + 3] = a1.y - u[8 * j + 3];
-        u[8 * j + 4] = a2.x - u[8 * j + 4]; u[8 * j + 5] = a2.y - u[8 * j + 5];
-        u[8 * j + 6] = a3.x - u[8 * j + 6]; u[8 * j + 7] = a3.y - u[8 * j + 7];
-      }
-      store_row64(sm + S_UA, row, u);
+    if (tid == 0 && nchunks > 0) {
+      mbar_arrive_expect_tx(&full[0], kRecStage);
+      bulk_g2s(sm + S_STAGE0, rec0, kRecStage, &full[0]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    group_sync(1, 128);
 
-    // MMA: S^T += U^T K_bar ; D_O += U^T M^T
-    if (tid == 0) {
+    for (int64_t c = 0; c < nchunks; ++c) {
+      const int st = (int)(c & 1);
+      uint8_t* stage = sm + (st ? S_STAGE1 : S_STAGE0);
+      const uint32_t ph = (uint32_t)(c & 1);
+      // U_hat^T row of this chunk (global / L2), consumed after D_U is ready
+      uint4 uh[8];
+      {
+        const uint8_t* ut = rec0 + (size_t)c * rec_stride + kRecUT;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) uh[j] = *reinterpret_cast<const uint4*>(ut + row_chunk(row, j));
+      }
+      if (tid == 0) {
+        bool w = true;
+        // stage st^1 is free once chunk c-1's MMAs are done: prefetch chunk c+1 into it
+        if (c >= 1) w = mbar_wait(&bar_o[st ^ 1], (uint32_t)(((c - 1) >> 1) & 1));
+        if (w && c + 1 < nchunks) {
+          mbar_arrive_expect_tx(&full[st ^ 1], kRecStage);
+          bulk_g2s(sm + (st ? S_STAGE0 : S_STAGE1), rec0 + (size_t)(c + 1) * rec_stride, kRecStage, &full[st ^ 1]);
+        }
+        w = w && mbar_wait(&full[st], (uint32_t)((c >> 1) & 1));
+        // D_O[st] is free once the output warps have read chunk c-2
+        if (w && c >= 2) w = mbar_wait(&do_free[st], (uint32_t)(((c - 2) >> 1) & 1));
+        if (w) {
+          tc_fence_after();
+          const uint32_t id_u = idesc_f16(128, 64, false, true);
+          const uint32_t id_o = idesc_f16(128, 64, false, false);
+#pragma unroll
+          for (int k0 = 0; k0 < 128; k0 += 16) {
+            const uint32_t kb = k0 >> 6, kk = (k0 & 63) * 2;
+            const uint64_t ad = smem_desc_sw128(smem_u32(sm + S_SA) + kb * 16384 + kk, 16, 1024);
+            const uint64_t bw = smem_desc_sw128(smem_u32(stage + kRecWT) + (k0 >> 3) * 1024, 8192, 1024);
+            mma_f16(tmem + T_DU, ad, bw, id_u, k0 > 0);
+          }
+          mma_commit(bar_u);
+#pragma unroll
+          for (int k0 = 0; k0 < 128; k0 += 16) {
+            const uint32_t kb = k0 >> 6, kk = (k0 & 63) * 2;
+            const uint64_t ad = smem_desc_sw128(smem_u32(sm + S_SA) + kb * 16384 + kk, 16, 1024);
+            const uint64_t bq = smem_desc_sw128(smem_u32(stage + kRecQH) + kb * 8192 + kk, 16, 1024);
+            mma_f16(tmem + T_DO + 64 * st, ad, bq, id_o, k0 > 0);
+          }
+        } else {
+          *abort_flag = 1;
+        }
+      }
+      ok = group_and(1, 128, !*abort_flag);
+      if (!ok) break;
+      // while the MMAs run: S^T <- S^T Diag(e^{G_C}) in TMEM (the MMAs read the fp16 copy)
+      {
+        const float* gc = reinterpret_cast<const float*>(stage + kRecGC);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          float t[16];
+          tmem_ld16(tl + T_S + 16 * q4, t);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) t[j] *= gc[16 * q4 + j];
+          tmem_st16(tl + T_S + 16 * q4, t);
+        }
+        tmem_wait_st();
+      }
+      ok = group_and(1, 128, mbar_wait(bar_u, ph));
+      if (!ok) { if (tid == 0) *abort_flag = 1; break; }
       tc_fence_after();
-      const uint32_t id_s = idesc_f16(128, 128, false, true);
-      const uint32_t id_o = idesc_f16(128, 64, false, false);
+      {
+        float u[64];
+        tmem_ld64(tl + T_DU, u);
 #pragma unroll
-      for (int k0 = 0; k0 < 64; k0 += 16) {
-        const uint64_t au = smem_desc_sw128(smem_u32(sm + S_UA) + k0 * 2, 16, 1024);
-        const uint64_t bk = smem_desc_sw128(smem_u32(stage + kRecKB) + (k0 >> 3) * 1024, 8192, 1024);
-        mma_f16(tmem + T_S, au, bk, id_s, true);
-      }
-      mma_commit(bar_s);
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t w4[4] = {uh[j].x, uh[j].y, uh[j].z, uh[j].w};
 #pragma unroll
-      for (int k0 = 0; k0 < 64; k0 += 16) {
-        const uint64_t au = smem_desc_sw128(smem_u32(sm + S_UA) + k0 * 2, 16, 1024);
-        const uint64_t bm = smem_desc_sw128(smem_u32(stage + kRecMM) + k0 * 2, 16, 1024);
-        mma_f16(tmem + T_DO, au, bm, id_o, true);
+          for (int e = 0; e < 4; ++e) {
+            const float2 a = unpack_h2(w4[e]);
+            u[8 * j + 2 * e] = a.x - u[8 * j + 2 * e];
+            u[8 * j + 2 * e + 1] = a.y - u[8 * j + 2 * e + 1];
+          }
+        }
+        store_row64(sm + S_UA, row, u);
       }
-      mma_commit(bar_o);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      group_sync(1, 128);
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t id_s = idesc_f16(128, 128, false, true);
+        const uint32_t id_o = idesc_f16(128, 64, false, false);
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16) {
+          const uint64_t au = smem_desc_sw128(smem_u32(sm + S_UA) + k0 * 2, 16, 1024);
+          const uint64_t bk = smem_desc_sw128(smem_u32(stage + kRecKB) + (k0 >> 3) * 1024, 8192, 1024);
+          mma_f16(tmem + T_S, au, bk, id_s, true);
+        }
+        mma_commit(bar_s);
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16) {
+          const uint64_t au = smem_desc_sw128(smem_u32(sm + S_UA) + k0 * 2, 16, 1024);
+          const uint64_t bm = smem_desc_sw128(smem_u32(stage + kRecMM) + k0 * 2, 16, 1024);
+          mma_f16(tmem + T_DO + 64 * st, au, bm, id_o, true);
+        }
+        mma_commit(&bar_o[st]);
+      }
+      ok = group_and(1, 128, mbar_wait(bar_s, ph));
+      if (!ok) { if (tid == 0) *abort_flag = 1; break; }
+      tc_fence_after();
+      {
+        float s[128];
+        tmem_ld64(tl + T_S, s);
+        tmem_ld64(tl + T_S + 64, s + 64);
+        store_srow(sm + S_SA, row, s);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      group_sync(1, 128);
     }
-    __syncwarp();
-
-    // new state -> fp16 A operand for the next chunk
-    if (!__syncthreads_and(mbar_wait(bar_s, ph))) { ok = false; break; }
-    tc_fence_after();
-    {
+    if (ok && hT != nullptr) {
+      tc_fence_after();
       float s[128];
       tmem_ld64(tl + T_S, s);
       tmem_ld64(tl + T_S + 64, s + 64);
-      store_srow(sm + S_SA, row, s);
+#pragma unroll
+      for (int c = 0; c < 128; ++c) hT[soff + (size_t)c * 128 + row] = s[c];
     }
-
-    // outputs: D_O -> fp32 [r][dv] in this stage (its operands are consumed) -> epilogue -> global
-    if (!__syncthreads_and(mbar_wait(bar_o, ph))) { ok = false; break; }
-    tc_fence_after();
-    {
+  } else {
+    // ======================== output warps: D_O -> staging -> epilogue -> global
+    float* ost = reinterpret_cast<float*>(sm + S_OUT);
+    for (int64_t c = 0; c < nchunks; ++c) {
+      const int st = (int)(c & 1);
+      bool w = false;
+      for (int spin = 0; spin < 64 && !w; ++spin) {
+        if (*abort_flag) break;
+        w = mbar_wait(&bar_o[st], (uint32_t)((c >> 1) & 1), 1u << 20);
+      }
+      ok = group_and(2, 128, w);
+      if (!ok) break;
+      tc_fence_after();
       float o[64];
-      tmem_ld64(tl + T_DO, o);
-      float* ost = reinterpret_cast<float*>(stage);
+      tmem_ld64(tl + T_DO + 64 * st, o);
+      tc_fence_before();
+      group_sync(2, 128);
+      if (tid == 128) mbar_arrive(&do_free[st]);
 #pragma unroll
       for (int r = 0; r < 64; ++r) ost[r * 128 + row] = o[r];
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    {
+      group_sync(2, 128);
       const int64_t rem = len - 64 * c;
       const int n = (int)(rem < 64 ? rem : 64);
       const int64_t t0 = t_begin + 64 * c;
-      const float* ost = reinterpret_cast<const float*>(stage);
-      const int lane = tid & 31;
-      for (int r = warp; r < n; r += 4) {
+      for (int r = warp - 4; r < n; r += 4) {
         float4 y = *reinterpret_cast<const float4*>(ost + r * 128 + 4 * lane);
         const size_t orow = ((size_t)(t0 + r) * H + h) * 128 + 4 * lane;
         if (gate != nullptr) {
           float ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
           ss = warp_sum(ss);
           const float inv = rsqrtf(ss * (1.f / 128.f) + eps);
-          float w0 = 1.f, w1 = 1.f, w2 = 1.f, w3 = 1.f;
-          if (norm_w) { w0 = norm_w[4 * lane]; w1 = norm_w[4 * lane + 1]; w2 = norm_w[4 * lane + 2]; w3 = norm_w[4 * lane + 3]; }
-          y.x = y.x * inv * w0 * sigmoidf_(__bfloat162float(gate[orow + 0]));
-          y.y = y.y * inv * w1 * sigmoidf_(__bfloat162float(gate[orow + 1]));
-          y.z = y.z * inv * w2 * sigmoidf_(__bfloat162float(gate[orow + 2]));
-          y.w = y.w * inv * w3 * sigmoidf_(__bfloat162float(gate[orow + 3]));
+          const uint2 gw = *reinterpret_cast<const uint2*>(gate + orow);
+          const float2 g01 = unpack_bf2(gw.x), g23 = unpack_bf2(gw.y);
+          float4 wv = make_float4(1.f, 1.f, 1.f, 1.f);
+          if (norm_w) wv = make_float4(norm_w[4 * lane], norm_w[4 * lane + 1], norm_w[4 * lane + 2], norm_w[4 * lane + 3]);
+          y.x = y.x * inv * wv.x * sigmoidf_(g01.x);
+          y.y = y.y * inv * wv.y * sigmoidf_(g01.y);
+          y.z = y.z * inv * wv.z * sigmoidf_(g23.x);
+          y.w = y.w * inv * wv.w * sigmoidf_(g23.y);
         }
-        out[orow + 0] = from_f32<Tout>(y.x);
-        out[orow + 1] = from_f32<Tout>(y.y);
-        out[orow + 2] = from_f32<Tout>(y.z);
-        out[orow + 3] = from_f32<Tout>(y.w);
+        if constexpr (sizeof(Tout) == 4) {
+          *reinterpret_cast<float4*>(out + orow) = y;
+        } else {
+          __nv_bfloat162 a = __floats2bfloat162_rn(y.x, y.y), b2 = __floats2bfloat162_rn(y.z, y.w);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&a);
+          pk.y = *reinterpret_cast<uint32_t*>(&b2);
+          *reinterpret_cast<uint2*>(out + orow) = pk;
+        }
       }
+      group_sync(2, 128);  // staging buffer free for the next chunk
     }
-    tc_fence_before();
-    __syncthreads();  // stage free for the prefetch issued at the start of chunk c+1
+    if (!ok) *abort_flag = 1;
   }
 
-  if (!ok) {
-    // a wait ran out: record it, let the in-flight record load and this thread's MMAs drain
-    // (each wait bounded), then free TMEM and return
-    if (tid == 0) {
-      atomicOr(err, KDA_DEVERR_WAIT_TIMEOUT);
-      if (pending >= 0) mbar_wait(&full[pending & 1], (uint32_t)((pending >> 1) & 1));
-      mma_commit(bar_fin);
-      mbar_wait(bar_fin, 0);
-    }
-  } else if (hT != nullptr) {
-    tc_fence_after();
-    float s[128];
-    tmem_ld64(tl + T_S, s);
-    tmem_ld64(tl + T_S + 64, s + 64);
-    const size_t soff = ((size_t)b * H + h) * 128 * 128;
-#pragma unroll
-    for (int c = 0; c < 128; ++c) hT[soff + (size_t)c * 128 + row] = s[c];
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    atomicOr(err, KDA_DEVERR_WAIT_TIMEOUT);
+    mma_commit(bar_fin);  // let this thread's MMAs drain (bounded) before TMEM is released
+    mbar_wait(bar_fin, 0);
   }
   tc_fence_before();
   __syncthreads();
@@ -693,9 +835,41 @@ kda_tc_chunk_scan(const uint8_t* __restrict__ records, const int32_t* __restrict
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// ----------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D map over [rows = T_tot][cols = H * 128] with a {box_x, 64} box and 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int64_t rows, int H, int box_x) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)H * 128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)H * 128 * esize};
+  cuuint32_t box[2] = {(cuuint32_t)box_x, 64};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 template <typename Tout>
 cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
   static bool attr_done[64] = {};
+  static int sm_count[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev]) {
@@ -703,6 +877,8 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
                                          (int)kPrepSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
@@ -715,11 +891,18 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
     cudaError_t e = plan_launch(a.cu_seqlens, a.B, a.T_tot, plan, a.err, st);
     if (e != cudaSuccess) return e;
   }
-  if (nchunks > 0) {
+  if (nchunks > 0 && a.T_tot > 0) {
+    PrepMaps maps;
+    if (!make_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T_tot, a.H, 64) ||
+        !make_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T_tot, a.H, 64) ||
+        !make_map(&maps.v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T_tot, a.H, 64) ||
+        !make_map(&maps.g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T_tot, a.H, 32))
+      return cudaErrorInvalidValue;
+    const int64_t ntask = nchunks * a.H;
+    const int grid = (int)(ntask < sm_count[dev] ? ntask : sm_count[dev]);
     TraceScope ts("kda_tc_chunk_prep", st);
-    kda_tc_chunk_prep<<<dim3((unsigned)nchunks, (unsigned)a.H), kPrepThreads, kPrepSmem, st>>>(
-        static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
-        static_cast<const __nv_bfloat16*>(a.v), a.g, a.beta, plan, a.cu_seqlens, a.B, a.T, a.H, records, a.err);
+    kda_tc_chunk_prep<<<grid, kPrepThreads, kPrepSmem, st>>>(maps, a.beta, plan, a.cu_seqlens, a.B, a.T, a.H, ntask,
+                                                            records, a.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

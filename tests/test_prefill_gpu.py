@@ -189,3 +189,22 @@ def test_long_context_1m_tokens(cfg):
         assert parity_err(out[p], ro[-1]) <= 2e-2, p
         if p == T - 1:
             assert rel_err(hT[0], rh[0]) <= 2e-2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_strong_decay_inside_chunk_with_weak_decay_across_the_half_boundary(dtype):
+    """g near the bound over tokens 16..30 and 33..47 of every chunk but ~0 at 31..32: the
+    off-diagonal-block entry for (r, s) = (32, 31) is O(1) while the cumulative decay between the
+    two centred references (e^{G_47 - G_15} ~ e^{-142}) underflows fp32."""
+    cfg = inputs.PrefillConfig("decay edge", H=2, dk=128, dv=128, dtype=dtype, B=1, T=256, h0_std=0.1, seed=308)
+    inp = inputs.prefill_inputs(cfg, device="cpu")
+    pos = torch.arange(256) % 64
+    strong = ((pos >= 16) & (pos <= 30)) | ((pos >= 33) & (pos <= 47))
+    g = torch.where(strong[:, None, None], torch.full_like(inp["g"], -4.9), torch.full_like(inp["g"], -0.01))
+    inp["g"] = (g + 0.05 * inp["g"] / 5.0).contiguous()  # keep a little per-channel variation, g in (-5, 0)
+    inp = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    ref_out, ref_hT = oracle_prefill(inp)
+    out, hT = run_prefill(inp, out_dtype=torch.float32)
+    assert_no_device_error()
+    tol = TOL[inputs.torch_dtype(dtype)]
+    assert rel_err(out, ref_out) <= tol and rel_err(hT, ref_hT) <= tol
