@@ -73,7 +73,9 @@ KDA_API size_t kda_chunk_fwd_workspace_size(int B, int64_t T, int H, int dk, int
   // Sized for the cu_seqlens case (the larger bound), so one size serves both.
   const int64_t chunks = max_chunks(B, T, true) > max_chunks(B, T, false) ? max_chunks(B, T, true)
                                                                            : max_chunks(B, T, false);
-  return plan_bytes(B) + (size_t)chunks * (size_t)H * blob_bytes(dtype, dk, dv);
+  size_t bytes = plan_bytes(B) + align_up((size_t)chunks * (size_t)H * blob_bytes(dtype, dk, dv), 256);
+  if (dtype == KDA_DTYPE_BF16 && prefill_tc_supported(dk, dv)) bytes += prefill_tc_cp_bytes(B, T, H);
+  return bytes;
 }
 
 KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,

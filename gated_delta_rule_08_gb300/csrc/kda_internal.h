@@ -71,10 +71,18 @@ inline size_t plan_bytes(int B) { return align_up((size_t)(B + 2) * sizeof(int32
 size_t prefill_cc_blob_bytes(int dk, int dv);
 cudaError_t prefill_cc_launch(const PrefillArgs& a, cudaStream_t stream);
 
-// bf16 tensor-core path (kda_prefill_tc.cu)
+// bf16 tensor-core path (kda_prefill_tc.cu, kda_scan_tc.cu)
 size_t prefill_tc_blob_bytes(int dk, int dv);
 bool prefill_tc_supported(int dk, int dv);
 cudaError_t prefill_tc_launch(const PrefillArgs& a, cudaStream_t stream);
+// Intra-device context parallelism: sequence segments of the state pass (1 = none), chosen
+// from the problem shape and the current device's SM count, and the scratch it needs.
+constexpr int64_t kCpMinChunks = 256;      // sequences shorter than this are never split
+constexpr int64_t kCpMinSegChunks = 64;    // smallest segment
+int prefill_tc_cp_segments(int B, int64_t T, int H);
+size_t prefill_tc_cp_bytes(int B, int64_t T, int H);
+cudaError_t scan_tc_launch(const PrefillArgs& a, const uint8_t* records, const int32_t* plan, float* cp, int nseg,
+                           int64_t seg_len, cudaStream_t stream);
 
 // plan kernel (kda_prefill_cc.cu): chunk offsets per sequence + cu_seqlens validation
 cudaError_t plan_launch(const int32_t* cu_seqlens, int B, int64_t T_tot, int32_t* plan,

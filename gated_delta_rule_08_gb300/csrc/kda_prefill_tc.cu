@@ -37,118 +37,13 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include "kda_device.cuh"
 #include "kda_internal.h"
-#include "tc_ptx.cuh"
+#include "kda_tc_common.cuh"
 
 namespace kda {
 namespace {
 
-using namespace tc;
-
-// ----------------------------------------------------------------- record layout (bytes)
-constexpr uint32_t kRecWT = 0;          // W^T   [128 dk][64 r] fp16, row format (MN-major B of D_U)
-constexpr uint32_t kRecQH = 16384;      // Q_hat [64 r][128 dk] fp16, token-row blocks (K-major B of D_O)
-constexpr uint32_t kRecKB = 32768;      // K_bar [64 r][128 dk] fp16, token-row blocks (MN-major B of D_S)
-constexpr uint32_t kRecMM = 49152;      // M     [64 r][64 s]   fp16, row format (K-major B of D_O)
-constexpr uint32_t kRecGC = 57344;      // e^{G_C} [128] fp32
-constexpr uint32_t kRecStage = 57856;   // bytes the scan kernel stages in shared memory
-constexpr uint32_t kRecUT = 59392;      // U_hat^T [128 dv][64 r] fp16, row format (read from global)
-constexpr uint32_t kRecBytes = 75776;   // 74 KB
-
-// ----------------------------------------------------------------- swizzled addressing
-// fp16/bf16 [64 rows][128 channels] as two 64-channel blocks of 64 x 128 B (128-byte swizzle):
-// byte offset of the 16-byte chunk holding channels 8j..8j+7 of row r.
-__device__ __forceinline__ uint32_t trow_chunk(int r, int c8) {
-  return (uint32_t)(c8 >> 3) * 8192u + (uint32_t)r * 128u + ((((uint32_t)c8 & 7u) ^ ((uint32_t)r & 7u)) << 4);
-}
-// fp32 [64 rows][128 channels] as four 32-channel blocks of 64 x 128 B: chunk of channels 4j..4j+3.
-__device__ __forceinline__ uint32_t g_chunk(int r, int c4) {
-  return (uint32_t)(c4 >> 3) * 8192u + (uint32_t)r * 128u + ((((uint32_t)c4 & 7u) ^ ((uint32_t)r & 7u)) << 4);
-}
-// tf32 [R rows][32 channels] (one 128-byte K block): chunk of channels 4j..4j+3 of row r.
-__device__ __forceinline__ uint32_t op_chunk(int r, int c4) {
-  return (uint32_t)r * 128u + ((((uint32_t)c4 & 7u) ^ ((uint32_t)r & 7u)) << 4);
-}
-// fp16 [R rows][64 cols] row format: chunk j (cols 8j..8j+7) of row r.
-__device__ __forceinline__ uint32_t row_chunk(int r, int j) {
-  return (uint32_t)r * 128u + ((((uint32_t)j ^ (uint32_t)r) & 7u) << 4);
-}
-
-__device__ __forceinline__ float to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
-}
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-__device__ __forceinline__ float2 unpack_h2(uint32_t u) {
-  __half2 h = *reinterpret_cast<__half2*>(&u);
-  return __half22float2(h);
-}
-__device__ __forceinline__ float2 unpack_bf2(uint32_t u) {
-  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
-  return __bfloat1622float2(h);
-}
-__device__ __forceinline__ uint4 pack8_h(const float* v) {
-  uint4 w;
-  w.x = pack_h2(v[0], v[1]);
-  w.y = pack_h2(v[2], v[3]);
-  w.z = pack_h2(v[4], v[5]);
-  w.w = pack_h2(v[6], v[7]);
-  return w;
-}
-// 64 floats -> one fp16 row (row format) at `dst` (shared or global memory).
-__device__ __forceinline__ void store_row64(uint8_t* dst, int r, const float* v) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(dst + row_chunk(r, j)) = pack8_h(v + 8 * j);
-}
-
-constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-constexpr uint32_t idesc_tf32(int M, int N) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
-  mma_bf16_ss(d, a, b, idesc, acc);  // same instruction form; the descriptor selects f16
-}
-__device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc ? 1u : 0u)
-      : "memory");
-}
-__device__ __forceinline__ uint32_t tmem_lane(uint32_t base, int warp) {
-  return base + ((uint32_t)((warp & 3) * 32) << 16);
-}
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    float t[16];
-    tmem_ld16(taddr + 16 * q, t);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[16 * q + j] = t[j];
-  }
-  tmem_wait_ld();
-}
-// Named barrier over `n` threads returning the AND of `v` across them.
-__device__ __forceinline__ bool group_and(int id, int n, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void group_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
+using namespace tcx;
 
 // =================================================================== prep kernel
 constexpr int kPrepThreads = 256;
@@ -156,7 +51,7 @@ constexpr int kPrepThreads = 256;
 constexpr uint32_t R_K = 0, R_Q = 16384, R_V = 32768, R_G = 49152, R_BYTES = 81920;
 constexpr uint32_t P_RAW0 = 0;
 constexpr uint32_t P_RAW1 = R_BYTES;
-constexpr uint32_t P_OPS = 2 * R_BYTES;  // 56 KB: one 32-channel pass of split-tf32 operands
+constexpr uint32_t P_OPS = 2 * R_BYTES;  // 56 KB: one 64-channel pass of split-bf16 operands
 constexpr uint32_t O_XH = 0, O_XL = 16384, O_YH = 32768, O_YL = 45056, O_BYTES = 57344;
 // after the A/M product the operand region holds the solve:
 constexpr uint32_t O_SA = 0;             // fp32 A [64][65]
@@ -173,6 +68,21 @@ constexpr uint32_t kPrepSmem = P_MISC + M_END + 1024;
 constexpr uint32_t T_AM = 0;   // TMEM: A/M accumulator [128 x 96]
 constexpr uint32_t T_W = 96;   // W^T [128 x 64]
 constexpr uint32_t T_U = 160;  // U_hat^T [128 x 64]
+
+// x (8 floats) -> bf16 hi (x with its low 16 bits cleared, exact in bf16) and lo = x - hi
+// rounded to bf16, each packed as 8 bf16 values.
+__device__ __forceinline__ void split_bf16x8(const float* x, uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t a = __float_as_uint(x[2 * j]) & 0xFFFF0000u, b = __float_as_uint(x[2 * j + 1]) & 0xFFFF0000u;
+    h[j] = (a >> 16) | b;
+    const __nv_bfloat162 t = __floats2bfloat162_rn(x[2 * j] - __uint_as_float(a), x[2 * j + 1] - __uint_as_float(b));
+    l[j] = *reinterpret_cast<const uint32_t*>(&t);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
 
 struct PrepMaps {
   CUtensorMap k, q, v, g;
@@ -262,25 +172,36 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
     ok = __syncthreads_and(mbar_wait(&full[st], (it >> 1) & 1)) != 0;
     if (!ok) break;
 
-    // ---- cumulative log-decay (threads 0..127, one channel each, in place), V -> fp16 (128..255)
-    if (tid < 128) {
-      const int c = tid;
-      float acc = 0.f;
-      float* gcol = reinterpret_cast<float*>(raw + R_G);
-      const uint32_t cb = (uint32_t)(c >> 5) * 2048u, cw = (uint32_t)(c & 3), cc4 = (uint32_t)((c >> 2) & 7);
-#pragma unroll 8
-      for (int r = 0; r < 64; ++r) {
-        float* p = gcol + cb + (uint32_t)r * 32u + (((cc4 ^ ((uint32_t)r & 7u)) << 2) | cw);
-        acc += (r < n) ? *p : 0.f;
-        *p = acc;
-      }
-    } else {
-      const int t = tid - 128;
+    // ---- cumulative log-decay in place: warp w scans channel quads w, w+8, w+16, w+24; lane l
+    // holds rows 2l and 2l+1 (a pair sum, then a warp-wide inclusive scan of the pair sums)
+    {
+#pragma unroll 1
+      for (int qd = warp; qd < 32; qd += 8) {
+        const int r0 = 2 * lane, r1 = r0 + 1;
+        float4* p0 = reinterpret_cast<float4*>(raw + R_G + g_chunk(r0, qd));
+        float4* p1 = reinterpret_cast<float4*>(raw + R_G + g_chunk(r1, qd));
+        float4 a = (r0 < n) ? *p0 : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 b = (r1 < n) ? *p1 : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 x = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+        const float4 pair = x;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {  // 1024 chunks of 8 values / 128 threads
-        const int idx = t + 128 * i, r = idx >> 4, c8 = idx & 15;
+        for (int o = 1; o < 32; o <<= 1) {
+          float4 y;
+          y.x = __shfl_up_sync(0xffffffffu, x.x, o);
+          y.y = __shfl_up_sync(0xffffffffu, x.y, o);
+          y.z = __shfl_up_sync(0xffffffffu, x.z, o);
+          y.w = __shfl_up_sync(0xffffffffu, x.w, o);
+          if (lane >= o) { x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w; }
+        }
+        *p0 = make_float4(x.x - pair.x + a.x, x.y - pair.y + a.y, x.z - pair.z + a.z, x.w - pair.w + a.w);
+        *p1 = x;
+      }
+      // V -> fp16 in place (rows past the sequence end zeroed)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int idx = tid + 256 * i, r = idx >> 4, c8 = idx & 15;
         uint4* p = reinterpret_cast<uint4*>(raw + R_V + trow_chunk(r, c8));
-        uint4 w = *p;
+        const uint4 w = *p;
         float f[8];
         const float2 a0 = unpack_bf2(w.x), a1 = unpack_bf2(w.y), a2 = unpack_bf2(w.z), a3 = unpack_bf2(w.w);
         f[0] = a0.x; f[1] = a0.y; f[2] = a1.x; f[3] = a1.y; f[4] = a2.x; f[5] = a2.y; f[6] = a3.x; f[7] = a3.y;
@@ -292,7 +213,10 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
     }
     if (tid < 64) sBeta[tid] = bval;
     __syncthreads();
-    // per-channel decay constants and e^{G_C} for the record
+    // per-channel constants and e^{G_C} for the record.  Only factors that cannot underflow while
+    // the product they help form is still significant are precomputed: e^{G15} >= e^{-80} and
+    // e^{G63-G47} >= e^{-80} always; e^{G47} may underflow, but then every q/k e^{G_r} it scales
+    // (r >= 32) is below e^{-12}.
     if (tid < 128) {
       const int c = tid;
       const float* gb = reinterpret_cast<const float*>(raw + R_G);
@@ -301,9 +225,6 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
                   ((uint32_t)c & 3u)];
       };
       const float g15 = G(15), g47 = G(47), g63 = G(63);
-      // Only factors that cannot underflow while the product they help form is still
-      // significant are precomputed: e^{G15} >= e^{-80} and e^{G63-G47} >= e^{-80} always;
-      // e^{G47} may underflow, but then every q/k e^{G_r} it scales (r >= 32) is below e^{-12}.
       sCon[0 * 128 + c] = __expf(g15);
       sCon[1 * 128 + c] = __expf(g47);
       sCon[2 * 128 + c] = g47;
@@ -313,106 +234,116 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
     }
     __syncthreads();
 
-    // ---- A and M: four 32-channel passes of split-tf32 operands, three MMAs per K step
+    // ---- A and M: D[128 x 96] = X Y^T, X = [k e^{G-R}; q e^{G-R}], Y = [k e^{R-G}; k e^{G_47-G} (s < 32)],
+    // as a three-way bf16 split (x = hi + lo, hi = x with its low 16 bits cleared, lo = x - hi;
+    // products hi*hi + hi*lo + lo*hi accumulate in fp32, ~2^-16 relative), in two 64-channel passes.
+    // The same passes emit Q_hat and K_bar into the record and K_hat in place of k.
     {
       const int r = tid >> 2;            // row 0..63
-      const int cq = (tid & 3) * 8;      // 8 channels within the pass
+      const int cq = (tid & 3) * 16;     // 16 channels within the pass
       const bool valid = r < n;
       const int rref = r < 32 ? 15 : 47;
       const int hsel = r < 32 ? 0 : 1;
+      const uint32_t id_am = idesc_bf16_f32(128, 96, false, false);
+      const uint64_t dxh = smem_desc_sw128(smem_u32(ops + O_XH), 16, 1024);
+      const uint64_t dxl = smem_desc_sw128(smem_u32(ops + O_XL), 16, 1024);
+      const uint64_t dyh = smem_desc_sw128(smem_u32(ops + O_YH), 16, 1024);
+      const uint64_t dyl = smem_desc_sw128(smem_u32(ops + O_YL), 16, 1024);
 #pragma unroll 1
-      for (int pass = 0; pass < 4; ++pass) {
+      for (int pass = 0; pass < 2; ++pass) {
         if (pass > 0) {
-          ok = __syncthreads_and(ok && mbar_wait(bar_am, (pass - 1) & 1)) != 0;
+          ok = __syncthreads_and(ok && mbar_wait(bar_am, 0)) != 0;
           if (!ok) break;
         }
-        const int c0 = 32 * pass + cq;   // first of this thread's 8 channels
-        float kv[8], qv[8], G[8], R[8];
-        {
-          const uint4 wk = *reinterpret_cast<const uint4*>(raw + R_K + trow_chunk(r, c0 >> 3));
-          const uint4 wq = *reinterpret_cast<const uint4*>(raw + R_Q + trow_chunk(r, c0 >> 3));
-          const uint32_t ku[4] = {wk.x, wk.y, wk.z, wk.w}, qu[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 a = unpack_bf2(ku[j]), b = unpack_bf2(qu[j]);
-            kv[2 * j] = valid ? a.x : 0.f; kv[2 * j + 1] = valid ? a.y : 0.f;
-            qv[2 * j] = valid ? b.x : 0.f; qv[2 * j + 1] = valid ? b.y : 0.f;
+        for (int half8 = 0; half8 < 2; ++half8) {
+          const int c0 = 64 * pass + cq + 8 * half8;  // first of 8 channels
+          float kv[8], qv[8], G[8], R[8], eR[8], g47[8], c3[8], g63[8];
+          {
+            const uint4 wk = *reinterpret_cast<const uint4*>(raw + R_K + trow_chunk(r, c0 >> 3));
+            const uint4 wq = *reinterpret_cast<const uint4*>(raw + R_Q + trow_chunk(r, c0 >> 3));
+            const uint32_t ku[4] = {wk.x, wk.y, wk.z, wk.w}, qu[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 a = unpack_bf2(ku[j]), bq = unpack_bf2(qu[j]);
+              kv[2 * j] = valid ? a.x : 0.f; kv[2 * j + 1] = valid ? a.y : 0.f;
+              qv[2 * j] = valid ? bq.x : 0.f; qv[2 * j + 1] = valid ? bq.y : 0.f;
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const float4 g4 = *reinterpret_cast<const float4*>(raw + R_G + g_chunk(r, (c0 >> 2) + hh));
+              const float4 r4 = *reinterpret_cast<const float4*>(raw + R_G + g_chunk(rref, (c0 >> 2) + hh));
+              const float4 e4 = *reinterpret_cast<const float4*>(sCon + hsel * 128 + c0 + 4 * hh);
+              const float4 a4 = *reinterpret_cast<const float4*>(sCon + 2 * 128 + c0 + 4 * hh);
+              const float4 b4 = *reinterpret_cast<const float4*>(sCon + 3 * 128 + c0 + 4 * hh);
+              const float4 d4 = *reinterpret_cast<const float4*>(sCon + 4 * 128 + c0 + 4 * hh);
+              const int o = 4 * hh;
+              G[o] = g4.x; G[o + 1] = g4.y; G[o + 2] = g4.z; G[o + 3] = g4.w;
+              R[o] = r4.x; R[o + 1] = r4.y; R[o + 2] = r4.z; R[o + 3] = r4.w;
+              eR[o] = e4.x; eR[o + 1] = e4.y; eR[o + 2] = e4.z; eR[o + 3] = e4.w;
+              g47[o] = a4.x; g47[o + 1] = a4.y; g47[o + 2] = a4.z; g47[o + 3] = a4.w;
+              c3[o] = b4.x; c3[o + 1] = b4.y; c3[o + 2] = b4.z; c3[o + 3] = b4.w;
+              g63[o] = d4.x; g63[o + 1] = d4.y; g63[o + 2] = d4.z; g63[o + 3] = d4.w;
+            }
           }
+          float xk[8], xq[8], yy[8], zz[8], qh[8], kb[8], kh[8];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const float4 g4 = *reinterpret_cast<const float4*>(raw + R_G + g_chunk(r, (c0 >> 2) + hh));
-            const float4 r4 = *reinterpret_cast<const float4*>(raw + R_G + g_chunk(rref, (c0 >> 2) + hh));
-            G[4 * hh + 0] = g4.x; G[4 * hh + 1] = g4.y; G[4 * hh + 2] = g4.z; G[4 * hh + 3] = g4.w;
-            R[4 * hh + 0] = r4.x; R[4 * hh + 1] = r4.y; R[4 * hh + 2] = r4.z; R[4 * hh + 3] = r4.w;
+          for (int j = 0; j < 8; ++j) {
+            const float e1 = __expf(G[j] - R[j]);
+            const float e2 = __expf(R[j] - G[j]);
+            xk[j] = kv[j] * e1;
+            xq[j] = qv[j] * e1;
+            yy[j] = kv[j] * e2;
+            qh[j] = qv[j] * e1 * eR[j];  // q e^{G}
+            kh[j] = kv[j] * e1 * eR[j];  // k e^{G}
+            if (hsel == 0) {
+              // rows < 32: k e^{G_47 - G} and k e^{G_C - G} from one exponential each (a factored
+              // form can underflow while the product it feeds is O(1))
+              zz[j] = kv[j] * __expf(g47[j] - G[j]);
+              kb[j] = kv[j] * __expf(g63[j] - G[j]);
+            } else {
+              zz[j] = 0.f;
+              kb[j] = kv[j] * e2 * c3[j];  // e^{G_C - G_47} >= e^{-80}: no underflow
+            }
           }
-        }
-        float xkh[8], xkl[8], xqh[8], xql[8], yh[8], yl[8], zh[8], zl[8], qh[8], kb[8], kh[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int c = c0 + j;
-          const float e1 = __expf(G[j] - R[j]);
-          const float e2 = __expf(R[j] - G[j]);
-          float x = kv[j] * e1;
-          xkh[j] = to_tf32(x); xkl[j] = to_tf32(x - xkh[j]);
-          x = qv[j] * e1;
-          xqh[j] = to_tf32(x); xql[j] = to_tf32(x - xqh[j]);
-          x = kv[j] * e2;
-          yh[j] = to_tf32(x); yl[j] = to_tf32(x - yh[j]);
-          const float eR = sCon[hsel * 128 + c];
-          qh[j] = qv[j] * e1 * eR;  // q e^{G}
-          kh[j] = kv[j] * e1 * eR;  // k e^{G}
+          uint4 hi, lo;
+          const uint32_t ck = (uint32_t)((c0 & 63) >> 3);  // 16-byte chunk within the 128-byte row
+          split_bf16x8(xk, hi, lo);
+          *reinterpret_cast<uint4*>(ops + O_XH + row_chunk(r, ck)) = hi;
+          *reinterpret_cast<uint4*>(ops + O_XL + row_chunk(r, ck)) = lo;
+          split_bf16x8(xq, hi, lo);
+          *reinterpret_cast<uint4*>(ops + O_XH + row_chunk(64 + r, ck)) = hi;
+          *reinterpret_cast<uint4*>(ops + O_XL + row_chunk(64 + r, ck)) = lo;
+          split_bf16x8(yy, hi, lo);
+          *reinterpret_cast<uint4*>(ops + O_YH + row_chunk(r, ck)) = hi;
+          *reinterpret_cast<uint4*>(ops + O_YL + row_chunk(r, ck)) = lo;
           if (hsel == 0) {
-            // rows < 32: k e^{G_47 - G} (off-diagonal block operand) and k e^{G_C - G}, each from
-            // one exponential: the factored forms can underflow while the product is O(1)
-            x = kv[j] * __expf(sCon[2 * 128 + c] - G[j]);
-            zh[j] = to_tf32(x); zl[j] = to_tf32(x - zh[j]);
-            kb[j] = kv[j] * __expf(sCon[4 * 128 + c] - G[j]);
-          } else {
-            zh[j] = 0.f; zl[j] = 0.f;
-            kb[j] = kv[j] * e2 * sCon[3 * 128 + c];  // e^{G_C - G_47} >= e^{-80}: no underflow
+            split_bf16x8(zz, hi, lo);
+            *reinterpret_cast<uint4*>(ops + O_YH + row_chunk(64 + r, ck)) = hi;
+            *reinterpret_cast<uint4*>(ops + O_YL + row_chunk(64 + r, ck)) = lo;
           }
+          *reinterpret_cast<uint4*>(rec + kRecQH + trow_chunk(r, c0 >> 3)) = pack8_h(qh);
+          *reinterpret_cast<uint4*>(rec + kRecKB + trow_chunk(r, c0 >> 3)) = pack8_h(kb);
+          *reinterpret_cast<uint4*>(raw + R_K + trow_chunk(r, c0 >> 3)) = pack8_h(kh);  // K_hat in place
         }
-        const int c4 = (c0 & 31) >> 2;   // first tf32 chunk within the pass's 128-byte rows
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int o = 4 * hh;
-          *reinterpret_cast<float4*>(ops + O_XH + op_chunk(r, c4 + hh)) = make_float4(xkh[o], xkh[o + 1], xkh[o + 2], xkh[o + 3]);
-          *reinterpret_cast<float4*>(ops + O_XL + op_chunk(r, c4 + hh)) = make_float4(xkl[o], xkl[o + 1], xkl[o + 2], xkl[o + 3]);
-          *reinterpret_cast<float4*>(ops + O_XH + op_chunk(64 + r, c4 + hh)) = make_float4(xqh[o], xqh[o + 1], xqh[o + 2], xqh[o + 3]);
-          *reinterpret_cast<float4*>(ops + O_XL + op_chunk(64 + r, c4 + hh)) = make_float4(xql[o], xql[o + 1], xql[o + 2], xql[o + 3]);
-          *reinterpret_cast<float4*>(ops + O_YH + op_chunk(r, c4 + hh)) = make_float4(yh[o], yh[o + 1], yh[o + 2], yh[o + 3]);
-          *reinterpret_cast<float4*>(ops + O_YL + op_chunk(r, c4 + hh)) = make_float4(yl[o], yl[o + 1], yl[o + 2], yl[o + 3]);
-          if (r < 32) {
-            *reinterpret_cast<float4*>(ops + O_YH + op_chunk(64 + r, c4 + hh)) = make_float4(zh[o], zh[o + 1], zh[o + 2], zh[o + 3]);
-            *reinterpret_cast<float4*>(ops + O_YL + op_chunk(64 + r, c4 + hh)) = make_float4(zl[o], zl[o + 1], zl[o + 2], zl[o + 3]);
-          }
-        }
-        *reinterpret_cast<uint4*>(rec + kRecQH + trow_chunk(r, c0 >> 3)) = pack8_h(qh);
-        *reinterpret_cast<uint4*>(rec + kRecKB + trow_chunk(r, c0 >> 3)) = pack8_h(kb);
-        *reinterpret_cast<uint4*>(raw + R_K + trow_chunk(r, c0 >> 3)) = pack8_h(kh);  // K_hat in place
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
           tc_fence_after();
-          const uint32_t idesc = idesc_tf32(128, 96);
 #pragma unroll
-          for (int k0 = 0; k0 < 32; k0 += 8) {
-            const uint32_t kk = (uint32_t)k0 * 4u;
-            const uint64_t xh = smem_desc_sw128(smem_u32(ops + O_XH) + kk, 16, 1024);
-            const uint64_t xl = smem_desc_sw128(smem_u32(ops + O_XL) + kk, 16, 1024);
-            const uint64_t yhd = smem_desc_sw128(smem_u32(ops + O_YH) + kk, 16, 1024);
-            const uint64_t yld = smem_desc_sw128(smem_u32(ops + O_YL) + kk, 16, 1024);
-            mma_tf32(tmem + T_AM, xh, yhd, idesc, pass > 0 || k0 > 0);
-            mma_tf32(tmem + T_AM, xh, yld, idesc, true);
-            mma_tf32(tmem + T_AM, xl, yhd, idesc, true);
+          for (int k0 = 0; k0 < 64; k0 += 16) {
+            const uint32_t off = (uint32_t)k0 * 2u;
+            mma_bf16_ss(tmem + T_AM, desc_add(dxh, off), desc_add(dyh, off), id_am, pass > 0 || k0 > 0);
+            mma_bf16_ss(tmem + T_AM, desc_add(dxh, off), desc_add(dyl, off), id_am, true);
+            mma_bf16_ss(tmem + T_AM, desc_add(dxl, off), desc_add(dyh, off), id_am, true);
           }
           mma_commit(bar_am);
         }
       }
     }
     if (!ok) break;
-    ok = __syncthreads_and(mbar_wait(bar_am, 1)) != 0;  // 4th completion of this task: parity 1
+    ok = __syncthreads_and(mbar_wait(bar_am, 1)) != 0;  // 2nd completion of this task: parity 1
     if (!ok) break;
     tc_fence_after();
 
@@ -460,35 +391,41 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int r = r0 + i;
-          float acc = 0.f;
+          float acc0 = 0.f, acc1 = 0.f;  // two independent chains
 #pragma unroll
-          for (int j = 0; j < i; ++j) acc = fmaf(sA[r * 65 + r0 + j], x[j], acc);
-          x[i] = (r == s) ? 1.f : ((r < s) ? 0.f : -acc);
+          for (int j = 0; j < i; j += 2) {
+            acc0 = fmaf(sA[r * 65 + r0 + j], x[j], acc0);
+            if (j + 1 < i) acc1 = fmaf(sA[r * 65 + r0 + j + 1], x[j + 1], acc1);
+          }
+          x[i] = (r == s) ? 1.f : ((r < s) ? 0.f : -(acc0 + acc1));
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) sX[(r0 + i) * 65 + s] = x[i];
       }
       __syncthreads();
-      // block rows 1..3: X_ij = -X_ii * sum_{m=j}^{i-1} A_im X_mj
+      // block rows 1..3: X_ij = -X_ii * sum_{m=j}^{i-1} A_im X_mj (16 x 16 blocks, one entry per thread)
       const int rr = tid >> 4, cc = tid & 15;
-#pragma unroll 1
+#pragma unroll
       for (int i = 1; i < 4; ++i) {
+#pragma unroll
         for (int j = 0; j < i; ++j) {
-          float acc = 0.f;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
           for (int m = j; m < i; ++m) {
 #pragma unroll
             for (int k2 = 0; k2 < 16; ++k2)
-              acc = fmaf(sA[(16 * i + rr) * 65 + 16 * m + k2], sX[(16 * m + k2) * 65 + 16 * j + cc], acc);
+              acc[k2 & 3] = fmaf(sA[(16 * i + rr) * 65 + 16 * m + k2], sX[(16 * m + k2) * 65 + 16 * j + cc], acc[k2 & 3]);
           }
-          sY[j * 256 + rr * 16 + cc] = acc;
+          sY[j * 256 + rr * 16 + cc] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         }
         __syncthreads();
+#pragma unroll
         for (int j = 0; j < i; ++j) {
-          float acc = 0.f;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int k2 = 0; k2 < 16; ++k2)
-            acc = fmaf(sX[(16 * i + rr) * 65 + 16 * i + k2], sY[j * 256 + k2 * 16 + cc], acc);
-          sX[(16 * i + rr) * 65 + 16 * j + cc] = -acc;
+            acc[k2 & 3] = fmaf(sX[(16 * i + rr) * 65 + 16 * i + k2], sY[j * 256 + k2 * 16 + cc], acc[k2 & 3]);
+          sX[(16 * i + rr) * 65 + 16 * j + cc] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
         }
         __syncthreads();
       }
@@ -516,13 +453,13 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
     if (tid == 0) {
       tc_fence_after();
       const uint32_t idesc = idesc_f16(128, 64, /*a_mn=*/true, /*b_mn=*/false);
+      const uint64_t dtt = smem_desc_sw128(smem_u32(ops + O_TT), 16, 1024);
+      const uint64_t dkh = smem_desc_sw128(smem_u32(raw + R_K), 8192, 1024);
+      const uint64_t dvv = smem_desc_sw128(smem_u32(raw + R_V), 8192, 1024);
 #pragma unroll
       for (int k0 = 0; k0 < 64; k0 += 16) {
-        const uint64_t bd = smem_desc_sw128(smem_u32(ops + O_TT) + k0 * 2, 16, 1024);
-        const uint64_t ak = smem_desc_sw128(smem_u32(raw + R_K) + (k0 >> 3) * 1024, 8192, 1024);
-        const uint64_t av = smem_desc_sw128(smem_u32(raw + R_V) + (k0 >> 3) * 1024, 8192, 1024);
-        mma_f16(tmem + T_W, ak, bd, idesc, k0 > 0);
-        mma_f16(tmem + T_U, av, bd, idesc, k0 > 0);
+        mma_f16(tmem + T_W, desc_add(dkh, (k0 >> 3) * 1024), desc_add(dtt, k0 * 2), idesc, k0 > 0);
+        mma_f16(tmem + T_U, desc_add(dvv, (k0 >> 3) * 1024), desc_add(dtt, k0 * 2), idesc, k0 > 0);
       }
       mma_commit(bar_wu);
     }
@@ -554,285 +491,6 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, 256);
-}
-
-// =================================================================== scan kernel
-constexpr int kScanThreads = 256;
-constexpr uint32_t kStage = 59392;               // staged record bytes, 1024-aligned
-constexpr uint32_t S_STAGE0 = 0;
-constexpr uint32_t S_STAGE1 = kStage;
-constexpr uint32_t S_SA = 2 * kStage;            // fp16 S^T [128 dv][128 dk], two 16 KB K-blocks
-constexpr uint32_t S_UA = S_SA + 32768;          // fp16 U^T [128 dv][64 r]
-constexpr uint32_t S_OUT = S_UA + 16384;         // fp32 read-out staging [64 r][128 dv]
-constexpr uint32_t S_BAR = S_OUT + 32768;        // barriers + tmem slot
-constexpr uint32_t S_END = S_BAR + 128;
-constexpr uint32_t kScanSmem = S_END + 1024;
-
-constexpr uint32_t T_S = 0;      // TMEM: S^T fp32 [128 x 128]
-constexpr uint32_t T_DU = 128;   // D_U [128 x 64]
-constexpr uint32_t T_DO = 192;   // D_O, two buffers [128 x 64] at 192 and 256
-
-__device__ __forceinline__ void store_srow(uint8_t* sa, int row, const float* s) {
-#pragma unroll
-  for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<uint4*>(sa + kb * 16384 + row_chunk(row, j)) = pack8_h(s + 64 * kb + 8 * j);
-}
-
-template <typename Tout>
-__global__ void __launch_bounds__(kScanThreads, 1)
-kda_tc_chunk_scan(const uint8_t* __restrict__ records, const int32_t* __restrict__ plan,
-                  const int32_t* __restrict__ cu, int B, int64_t T, int H, const float* __restrict__ h0,
-                  float* __restrict__ hT, Tout* __restrict__ out, const __nv_bfloat16* __restrict__ gate,
-                  const float* __restrict__ norm_w, float eps, unsigned int* __restrict__ err) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [2] record staged
-  uint64_t* bar_u = full + 2;                                // D_U ready
-  uint64_t* bar_s = full + 3;                                // S^T updated
-  uint64_t* bar_o = full + 4;                                // [2] D_O[b] complete
-  uint64_t* do_free = full + 6;                              // [2] D_O[b] read by the output warps
-  uint64_t* bar_fin = full + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 80);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S_BAR + 84);
-
-  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (cu != nullptr && plan[B + 1] == 0) return;  // invalid cu_seqlens: sequence skipped
-  int64_t first_chunk, t_begin, len;
-  const int64_t nchunks = sequence_chunks(b, plan, cu, B, T, first_chunk, t_begin, len);
-
-  if (warp == 0) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  if (tid == 32) {
-    for (int i = 0; i < 9; ++i) mbar_init(&full[i], 1);
-    *abort_flag = 0;
-    mbar_fence_init();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tl = tmem_lane(tmem, warp);
-  const int row = (warp & 3) * 32 + lane;  // TMEM lane = dv row
-  const size_t soff = ((size_t)b * H + h) * 128 * 128;
-  const uint8_t* rec0 = records + ((size_t)first_chunk * H + h) * kRecBytes;
-  const size_t rec_stride = (size_t)H * kRecBytes;
-
-  bool ok = true;
-  if (warp < 4) {
-    // ======================== state warps
-    {
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 128; ++c) s[c] = h0 ? h0[soff + (size_t)c * 128 + row] : 0.f;
-#pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
-        float t[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) t[j] = s[16 * q4 + j];
-        tmem_st16(tl + T_S + 16 * q4, t);
-      }
-      tmem_wait_st();
-      store_srow(sm + S_SA, row, s);
-    }
-    if (tid == 0 && nchunks > 0) {
-      mbar_arrive_expect_tx(&full[0], kRecStage);
-      bulk_g2s(sm + S_STAGE0, rec0, kRecStage, &full[0]);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    group_sync(1, 128);
-
-    for (int64_t c = 0; c < nchunks; ++c) {
-      const int st = (int)(c & 1);
-      uint8_t* stage = sm + (st ? S_STAGE1 : S_STAGE0);
-      const uint32_t ph = (uint32_t)(c & 1);
-      // U_hat^T row of this chunk (global / L2), consumed after D_U is ready
-      uint4 uh[8];
-      {
-        const uint8_t* ut = rec0 + (size_t)c * rec_stride + kRecUT;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) uh[j] = *reinterpret_cast<const uint4*>(ut + row_chunk(row, j));
-      }
-      if (tid == 0) {
-        bool w = true;
-        // stage st^1 is free once chunk c-1's MMAs are done: prefetch chunk c+1 into it
-        if (c >= 1) w = mbar_wait(&bar_o[st ^ 1], (uint32_t)(((c - 1) >> 1) & 1));
-        if (w && c + 1 < nchunks) {
-          mbar_arrive_expect_tx(&full[st ^ 1], kRecStage);
-          bulk_g2s(sm + (st ? S_STAGE0 : S_STAGE1), rec0 + (size_t)(c + 1) * rec_stride, kRecStage, &full[st ^ 1]);
-        }
-        w = w && mbar_wait(&full[st], (uint32_t)((c >> 1) & 1));
-        // D_O[st] is free once the output warps have read chunk c-2
-        if (w && c >= 2) w = mbar_wait(&do_free[st], (uint32_t)(((c - 2) >> 1) & 1));
-        if (w) {
-          tc_fence_after();
-          const uint32_t id_u = idesc_f16(128, 64, false, true);
-          const uint32_t id_o = idesc_f16(128, 64, false, false);
-#pragma unroll
-          for (int k0 = 0; k0 < 128; k0 += 16) {
-            const uint32_t kb = k0 >> 6, kk = (k0 & 63) * 2;
-            const uint64_t ad = smem_desc_sw128(smem_u32(sm + S_SA) + kb * 16384 + kk, 16, 1024);
-            const uint64_t bw = smem_desc_sw128(smem_u32(stage + kRecWT) + (k0 >> 3) * 1024, 8192, 1024);
-            mma_f16(tmem + T_DU, ad, bw, id_u, k0 > 0);
-          }
-          mma_commit(bar_u);
-#pragma unroll
-          for (int k0 = 0; k0 < 128; k0 += 16) {
-            const uint32_t kb = k0 >> 6, kk = (k0 & 63) * 2;
-            const uint64_t ad = smem_desc_sw128(smem_u32(sm + S_SA) + kb * 16384 + kk, 16, 1024);
-            const uint64_t bq = smem_desc_sw128(smem_u32(stage + kRecQH) + kb * 8192 + kk, 16, 1024);
-            mma_f16(tmem + T_DO + 64 * st, ad, bq, id_o, k0 > 0);
-          }
-        } else {
-          *abort_flag = 1;
-        }
-      }
-      ok = group_and(1, 128, !*abort_flag);
-      if (!ok) break;
-      // while the MMAs run: S^T <- S^T Diag(e^{G_C}) in TMEM (the MMAs read the fp16 copy)
-      {
-        const float* gc = reinterpret_cast<const float*>(stage + kRecGC);
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          float t[16];
-          tmem_ld16(tl + T_S + 16 * q4, t);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) t[j] *= gc[16 * q4 + j];
-          tmem_st16(tl + T_S + 16 * q4, t);
-        }
-        tmem_wait_st();
-      }
-      ok = group_and(1, 128, mbar_wait(bar_u, ph));
-      if (!ok) { if (tid == 0) *abort_flag = 1; break; }
-      tc_fence_after();
-      {
-        float u[64];
-        tmem_ld64(tl + T_DU, u);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t w4[4] = {uh[j].x, uh[j].y, uh[j].z, uh[j].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 a = unpack_h2(w4[e]);
-            u[8 * j + 2 * e] = a.x - u[8 * j + 2 * e];
-            u[8 * j + 2 * e + 1] = a.y - u[8 * j + 2 * e + 1];
-          }
-        }
-        store_row64(sm + S_UA, row, u);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      group_sync(1, 128);
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t id_s = idesc_f16(128, 128, false, true);
-        const uint32_t id_o = idesc_f16(128, 64, false, false);
-#pragma unroll
-        for (int k0 = 0; k0 < 64; k0 += 16) {
-          const uint64_t au = smem_desc_sw128(smem_u32(sm + S_UA) + k0 * 2, 16, 1024);
-          const uint64_t bk = smem_desc_sw128(smem_u32(stage + kRecKB) + (k0 >> 3) * 1024, 8192, 1024);
-          mma_f16(tmem + T_S, au, bk, id_s, true);
-        }
-        mma_commit(bar_s);
-#pragma unroll
-        for (int k0 = 0; k0 < 64; k0 += 16) {
-          const uint64_t au = smem_desc_sw128(smem_u32(sm + S_UA) + k0 * 2, 16, 1024);
-          const uint64_t bm = smem_desc_sw128(smem_u32(stage + kRecMM) + k0 * 2, 16, 1024);
-          mma_f16(tmem + T_DO + 64 * st, au, bm, id_o, true);
-        }
-        mma_commit(&bar_o[st]);
-      }
-      ok = group_and(1, 128, mbar_wait(bar_s, ph));
-      if (!ok) { if (tid == 0) *abort_flag = 1; break; }
-      tc_fence_after();
-      {
-        float s[128];
-        tmem_ld64(tl + T_S, s);
-        tmem_ld64(tl + T_S + 64, s + 64);
-        store_srow(sm + S_SA, row, s);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      group_sync(1, 128);
-    }
-    if (ok && hT != nullptr) {
-      tc_fence_after();
-      float s[128];
-      tmem_ld64(tl + T_S, s);
-      tmem_ld64(tl + T_S + 64, s + 64);
-#pragma unroll
-      for (int c = 0; c < 128; ++c) hT[soff + (size_t)c * 128 + row] = s[c];
-    }
-  } else {
-    // ======================== output warps: D_O -> staging -> epilogue -> global
-    float* ost = reinterpret_cast<float*>(sm + S_OUT);
-    for (int64_t c = 0; c < nchunks; ++c) {
-      const int st = (int)(c & 1);
-      bool w = false;
-      for (int spin = 0; spin < 64 && !w; ++spin) {
-        if (*abort_flag) break;
-        w = mbar_wait(&bar_o[st], (uint32_t)((c >> 1) & 1), 1u << 20);
-      }
-      ok = group_and(2, 128, w);
-      if (!ok) break;
-      tc_fence_after();
-      float o[64];
-      tmem_ld64(tl + T_DO + 64 * st, o);
-      tc_fence_before();
-      group_sync(2, 128);
-      if (tid == 128) mbar_arrive(&do_free[st]);
-#pragma unroll
-      for (int r = 0; r < 64; ++r) ost[r * 128 + row] = o[r];
-      group_sync(2, 128);
-      const int64_t rem = len - 64 * c;
-      const int n = (int)(rem < 64 ? rem : 64);
-      const int64_t t0 = t_begin + 64 * c;
-      for (int r = warp - 4; r < n; r += 4) {
-        float4 y = *reinterpret_cast<const float4*>(ost + r * 128 + 4 * lane);
-        const size_t orow = ((size_t)(t0 + r) * H + h) * 128 + 4 * lane;
-        if (gate != nullptr) {
-          float ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
-          ss = warp_sum(ss);
-          const float inv = rsqrtf(ss * (1.f / 128.f) + eps);
-          const uint2 gw = *reinterpret_cast<const uint2*>(gate + orow);
-          const float2 g01 = unpack_bf2(gw.x), g23 = unpack_bf2(gw.y);
-          float4 wv = make_float4(1.f, 1.f, 1.f, 1.f);
-          if (norm_w) wv = make_float4(norm_w[4 * lane], norm_w[4 * lane + 1], norm_w[4 * lane + 2], norm_w[4 * lane + 3]);
-          y.x = y.x * inv * wv.x * sigmoidf_(g01.x);
-          y.y = y.y * inv * wv.y * sigmoidf_(g01.y);
-          y.z = y.z * inv * wv.z * sigmoidf_(g23.x);
-          y.w = y.w * inv * wv.w * sigmoidf_(g23.y);
-        }
-        if constexpr (sizeof(Tout) == 4) {
-          *reinterpret_cast<float4*>(out + orow) = y;
-        } else {
-          __nv_bfloat162 a = __floats2bfloat162_rn(y.x, y.y), b2 = __floats2bfloat162_rn(y.z, y.w);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t*>(&a);
-          pk.y = *reinterpret_cast<uint32_t*>(&b2);
-          *reinterpret_cast<uint2*>(out + orow) = pk;
-        }
-      }
-      group_sync(2, 128);  // staging buffer free for the next chunk
-    }
-    if (!ok) *abort_flag = 1;
-  }
-
-  __syncthreads();
-  if (*abort_flag && tid == 0) {
-    atomicOr(err, KDA_DEVERR_WAIT_TIMEOUT);
-    mma_commit(bar_fin);  // let this thread's MMAs drain (bounded) before TMEM is released
-    mbar_wait(bar_fin, 0);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // ----------------------------------------------------------------- host side
@@ -876,8 +534,6 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(kda_tc_chunk_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kPrepSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
-    if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
@@ -906,14 +562,34 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  TraceScope ts("kda_tc_chunk_scan", st);
-  kda_tc_chunk_scan<Tout><<<dim3((unsigned)a.B, (unsigned)a.H), kScanThreads, kScanSmem, st>>>(
-      records, plan, a.cu_seqlens, a.B, a.T, a.H, a.h0, a.hT, static_cast<Tout*>(a.out),
-      static_cast<const __nv_bfloat16*>(a.epi.gate), a.epi.norm_weight, a.epi.eps, a.err);
-  return cudaGetLastError();
+  // state pass, split into sequence segments when there are too few (sequence, head) chains
+  const int nseg = prefill_tc_cp_segments(a.B, a.T, a.H);
+  const int64_t maxc = (a.T + kChunk - 1) / kChunk;  // chunks of the longest possible sequence
+  const int64_t seg_len = (maxc + nseg - 1) / nseg;
+  float* cp = reinterpret_cast<float*>(records + align_up((size_t)nchunks * a.H * kRecBytes, 256));
+  return scan_tc_launch(a, records, plan, cp, nseg, seg_len > 0 ? seg_len : 1, st);
 }
 
 }  // namespace
+
+int prefill_tc_cp_segments(int B, int64_t T, int H) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  const int64_t maxc = (T + kChunk - 1) / kChunk;
+  const int64_t chains = (int64_t)B * H;
+  // Worth it only for long sequences and when the chains leave at least half of the SMs idle;
+  // segments hold at least kCpMinSegChunks chunks.
+  if (maxc < kCpMinChunks || chains * 2 > sms) return 1;
+  int64_t n = sms / chains;
+  if (n > maxc / kCpMinSegChunks) n = maxc / kCpMinSegChunks;
+  return n < 1 ? 1 : (int)n;
+}
+
+size_t prefill_tc_cp_bytes(int B, int64_t T, int H) {
+  const int nseg = prefill_tc_cp_segments(B, T, H);
+  return nseg > 1 ? (size_t)B * H * nseg * 3 * 128 * 128 * sizeof(float) : 0;
+}
 
 size_t prefill_tc_blob_bytes(int, int) { return kRecBytes; }
 bool prefill_tc_supported(int dk, int dv) { return dk == 128 && dv == 128; }

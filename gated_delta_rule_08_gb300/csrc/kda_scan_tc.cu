@@ -1,0 +1,478 @@
+// KDA prefill: the serial inter-chunk state pass on the tcgen05 tensor cores, and the
+// intra-device context parallelism that splits it into sequence segments.
+//
+// Kimi K3: Open Frontier Intelligence (kimi-k3-paper.pages.dev), section 2.5 / Eq. 4: per
+// chunk, with chunk-start state S0 and the chunk record (W, U_hat, Q_hat, K_bar, M, e^{G_C}):
+//   U = U_hat - W S0,  O = Q_hat S0 + M U,  S_C = Diag(e^{G_C}) S0 + K_bar^T U.
+// Section 13.3.1 (intra-device CP): the SMs of one device each take a segment of a sequence,
+// evaluate the segment's transition independently, then merge to recover every segment's
+// initial state.  A chunk maps S0 affinely, S_C = (Diag(e^{G_C}) - K_bar^T W) S0 + K_bar^T U_hat,
+// so a segment of chunks maps S_in to S_out = P S_in + b with
+//   b = the segment's final state from S_in = 0,
+//   P = the segment's final state from S_in = I with U_hat = 0 (a dk x dk state);
+// both are ordinary runs of the same state pass.  The merge then walks the segments,
+// S_in(p+1) = P_p S_in(p) + b_p, and a last pass re-runs every segment from its S_in with outputs.
+//
+//  kda_tc_chunk_scan<Tout, MODE> (grid = sequences x heads x segments, 12 warps):
+//    warps 0-7 run the state chain: state^T (fp32) resident in TMEM, an fp16 copy in shared
+//      memory as the MMA A operand; two warps per TMEM lane quadrant, each owning half of
+//      the columns, so every TMEM <-> register <-> shared conversion is split in two;
+//    MODE 0 (read-out): warps 8-11 drain the double-buffered read-out accumulator through a
+//      staging buffer and run the optional RMSNorm + gate epilogue, off the serial path;
+//    MODE 1 (transition): z = 2 p + kind; kind 0 runs b_p, kind 1 runs P_p; no read-out.
+//  kda_cp_merge (grid = sequences x heads x 8 column slices): the sequential segment merge in fp32.
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+#include "kda_tc_common.cuh"
+
+namespace kda {
+namespace {
+
+using namespace tcx;
+
+constexpr int kScanThreads = 384;
+constexpr int kStateThreads = 256;               // warps 0-7
+constexpr uint32_t kStage = 59392;               // staged record bytes, 1024-aligned
+constexpr uint32_t S_STAGE0 = 0;
+constexpr uint32_t S_STAGE1 = kStage;
+constexpr uint32_t S_SA = 2 * kStage;            // fp16 state^T [128 rows][128], two 16 KB K-blocks
+constexpr uint32_t S_UA = S_SA + 32768;          // fp16 U^T [128 rows][64 r]
+constexpr uint32_t S_OUT = S_UA + 16384;         // fp32 read-out staging [64 r][128 dv]
+constexpr uint32_t S_BAR = S_OUT + 32768;        // barriers + tmem slot + abort flag
+constexpr uint32_t S_END = S_BAR + 128;
+constexpr uint32_t kScanSmem = S_END + 1024;
+
+constexpr uint32_t T_S = 0;      // TMEM: state^T fp32 [128 x 128]
+constexpr uint32_t T_DU = 128;   // D_U [128 x 64]
+constexpr uint32_t T_DO = 192;   // D_O, two buffers [128 x 64] at 192 and 256
+
+constexpr size_t kCpMat = 128 * 128;  // floats per CP matrix
+
+struct ScanParams {
+  const uint8_t* records;
+  const int32_t* plan;
+  const int32_t* cu;
+  int B;
+  int64_t T;
+  int H;
+  const float* h0;
+  float* hT;
+  void* out;
+  const __nv_bfloat16* gate;
+  const float* norm_w;
+  float eps;
+  unsigned int* err;
+  int nseg;
+  int64_t seg_len;  // chunks per segment
+  float* cp;        // [B][H][nseg][3][128][128]: P_p, b_p, S_in(p)
+};
+
+// 64 state columns (one 64-column K block of the fp16 copy) -> shared memory.
+__device__ __forceinline__ void store_shalf(uint8_t* sa, int row, int hc, const float* s) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<uint4*>(sa + hc * 16384 + row_chunk(row, j)) = pack8_h(s + 8 * j);
+}
+__device__ __forceinline__ void tmem_ld64b(uint32_t taddr, float* v) {
+  float a[32], b[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = a[i];
+    v[32 + i] = b[i];
+  }
+}
+
+template <typename Tout, int MODE>
+__global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [2] record staged
+  uint64_t* bar_u = full + 2;                                // D_U ready
+  uint64_t* bar_s = full + 3;                                // state updated
+  uint64_t* bar_o = full + 4;                                // [2] D_O[b] complete
+  uint64_t* do_free = full + 6;                              // [2] D_O[b] read by the output warps
+  uint64_t* bar_fin = full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 80);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S_BAR + 84);
+
+  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.H;
+  if (p.cu != nullptr && p.plan[p.B + 1] == 0) return;  // invalid cu_seqlens: sequence skipped
+  int64_t first_chunk, t_begin, len;
+  const int64_t nchunks = sequence_chunks(b, p.plan, p.cu, p.B, p.T, first_chunk, t_begin, len);
+  const int64_t p_last = nchunks > 0 ? (nchunks - 1) / p.seg_len : 0;
+  const int seg = MODE == 0 ? (int)blockIdx.z : (int)(blockIdx.z >> 1);
+  const int kind = MODE == 0 ? 0 : (int)(blockIdx.z & 1);  // MODE 1: 0 = offset b, 1 = transition P
+  if (MODE == 0 && seg > p_last) return;
+  if (MODE == 1 && seg >= p_last) return;
+  const int64_t c_begin = (int64_t)seg * p.seg_len;
+  const int64_t c_end = nchunks < c_begin + p.seg_len ? nchunks : c_begin + p.seg_len;
+  const int64_t ncs = c_end > c_begin ? c_end - c_begin : 0;
+  float* cpb = p.cp + ((size_t)(b * H + h) * p.nseg + seg) * 3 * kCpMat;
+
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int i = 0; i < 9; ++i) mbar_init(&full[i], 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tl = tmem_lane(tmem, warp);
+  const int row = (warp & 3) * 32 + lane;  // TMEM lane = state column (dv for S, dk for P)
+  const size_t soff = ((size_t)b * H + h) * kCpMat;
+  const uint8_t* rec0 = p.records + ((size_t)(first_chunk + c_begin) * H + h) * kRecBytes;
+  const size_t rec_stride = (size_t)H * kRecBytes;
+
+  bool ok = true;
+  if (warp < 8) {
+    // ======================== state warps: quadrant warp & 3, column half hc
+    const int hc = warp >> 2;
+    {
+      const float* init = nullptr;
+      if (MODE == 0) init = seg == 0 ? (p.h0 ? p.h0 + soff : nullptr) : cpb + 2 * kCpMat;
+      float s[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const int col = 64 * hc + c;
+        if (MODE == 0) s[c] = init ? init[(size_t)col * 128 + row] : 0.f;
+        else s[c] = (kind == 1 && col == row) ? 1.f : 0.f;
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float t[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) t[j] = s[16 * q4 + j];
+        tmem_st16(tl + T_S + 64 * hc + 16 * q4, t);
+      }
+      tmem_wait_st();
+      store_shalf(sm + S_SA, row, hc, s);
+    }
+    if (tid == 0 && ncs > 0) {
+      mbar_arrive_expect_tx(&full[0], kRecStage);
+      bulk_g2s(sm + S_STAGE0, rec0, kRecStage, &full[0]);
+    }
+    // this thread's half of the U_hat^T row (chunks 4 hc .. 4 hc + 3), fetched one chunk ahead
+    uint4 uh[4];
+    const bool use_uh = MODE == 0 || kind == 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) uh[j] = make_uint4(0u, 0u, 0u, 0u);
+    if (use_uh && ncs > 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) uh[j] = *reinterpret_cast<const uint4*>(rec0 + kRecUT + row_chunk(row, 4 * hc + j));
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    group_sync(1, kStateThreads);
+
+    for (int64_t c = 0; c < ncs; ++c) {
+      const int st = (int)(c & 1);
+      uint8_t* stage = sm + (st ? S_STAGE1 : S_STAGE0);
+      const uint32_t ph = (uint32_t)(c & 1);
+      uint4 uh_next[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) uh_next[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (use_uh && c + 1 < ncs) {
+        const uint8_t* ut = rec0 + (size_t)(c + 1) * rec_stride + kRecUT;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) uh_next[j] = *reinterpret_cast<const uint4*>(ut + row_chunk(row, 4 * hc + j));
+      }
+      if (tid == 0) {
+        bool w = true;
+        // stage st^1 is free once chunk c-1's MMAs are done: prefetch chunk c+1 into it
+        if (c >= 1)
+          w = mbar_wait(MODE == 0 ? &bar_o[st ^ 1] : bar_s,
+                        MODE == 0 ? (uint32_t)(((c - 1) >> 1) & 1) : (uint32_t)((c - 1) & 1));
+        if (w && c + 1 < ncs) {
+          mbar_arrive_expect_tx(&full[st ^ 1], kRecStage);
+          bulk_g2s(sm + (st ? S_STAGE0 : S_STAGE1), rec0 + (size_t)(c + 1) * rec_stride, kRecStage, &full[st ^ 1]);
+        }
+        w = w && mbar_wait(&full[st], (uint32_t)((c >> 1) & 1));
+        // D_O[st] is free once the output warps have read chunk c-2
+        if (MODE == 0 && w && c >= 2) w = mbar_wait(&do_free[st], (uint32_t)(((c - 2) >> 1) & 1));
+        if (w) {
+          tc_fence_after();
+          const uint32_t id_u = idesc_f16(128, 64, false, true);
+          const uint64_t dsa = smem_desc_sw128(smem_u32(sm + S_SA), 16, 1024);
+          const uint64_t dwt = smem_desc_sw128(smem_u32(stage + kRecWT), 8192, 1024);
+#pragma unroll
+          for (int k0 = 0; k0 < 128; k0 += 16)
+            mma_f16(tmem + T_DU, desc_add(dsa, (k0 >> 6) * 16384 + (k0 & 63) * 2), desc_add(dwt, (k0 >> 3) * 1024),
+                    id_u, k0 > 0);
+          mma_commit(bar_u);
+          if (MODE == 0) {
+            const uint32_t id_o = idesc_f16(128, 64, false, false);
+            const uint64_t dqh = smem_desc_sw128(smem_u32(stage + kRecQH), 16, 1024);
+#pragma unroll
+            for (int k0 = 0; k0 < 128; k0 += 16) {
+              const uint32_t off = (k0 & 63) * 2;
+              mma_f16(tmem + T_DO + 64 * st, desc_add(dsa, (k0 >> 6) * 16384 + off), desc_add(dqh, (k0 >> 6) * 8192 + off),
+                      id_o, k0 > 0);
+            }
+          }
+        } else {
+          *abort_flag = 1;
+        }
+      }
+      ok = group_and(1, kStateThreads, !*abort_flag);
+      if (!ok) break;
+      // while the MMAs run: this thread's 64 state columns <- Diag(e^{G_C}) scaling, in TMEM
+      {
+        const float* gc = reinterpret_cast<const float*>(stage + kRecGC) + 64 * hc;
+        float t[64];
+        tmem_ld64b(tl + T_S + 64 * hc, t);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float u[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) u[j] = t[16 * q4 + j] * gc[16 * q4 + j];
+          tmem_st16(tl + T_S + 64 * hc + 16 * q4, u);
+        }
+        tmem_wait_st();
+      }
+      ok = group_and(1, kStateThreads, mbar_wait(bar_u, ph));
+      if (!ok) { if (tid == 0) *abort_flag = 1; break; }
+      tc_fence_after();
+      {
+        float u[32];
+        tmem_ld32(tl + T_DU + 32 * hc, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t w4[4] = {uh[j].x, uh[j].y, uh[j].z, uh[j].w};
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 a = unpack_h2(w4[e]);
+            v[2 * e] = a.x - u[8 * j + 2 * e];
+            v[2 * e + 1] = a.y - u[8 * j + 2 * e + 1];
+          }
+          *reinterpret_cast<uint4*>(sm + S_UA + row_chunk(row, 4 * hc + j)) = pack8_h(v);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      group_sync(1, kStateThreads);
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t id_s = idesc_f16(128, 128, false, true);
+        const uint64_t dua = smem_desc_sw128(smem_u32(sm + S_UA), 16, 1024);
+        const uint64_t dkb = smem_desc_sw128(smem_u32(stage + kRecKB), 8192, 1024);
+#pragma unroll
+        for (int k0 = 0; k0 < 64; k0 += 16)
+          mma_f16(tmem + T_S, desc_add(dua, k0 * 2), desc_add(dkb, (k0 >> 3) * 1024), id_s, true);
+        mma_commit(bar_s);
+        if (MODE == 0) {
+          const uint32_t id_o = idesc_f16(128, 64, false, false);
+          const uint64_t dmm = smem_desc_sw128(smem_u32(stage + kRecMM), 16, 1024);
+#pragma unroll
+          for (int k0 = 0; k0 < 64; k0 += 16)
+            mma_f16(tmem + T_DO + 64 * st, desc_add(dua, k0 * 2), desc_add(dmm, k0 * 2), id_o, true);
+          mma_commit(&bar_o[st]);
+        }
+      }
+      ok = group_and(1, kStateThreads, mbar_wait(bar_s, ph));
+      if (!ok) { if (tid == 0) *abort_flag = 1; break; }
+      tc_fence_after();
+      {
+        float s[64];
+        tmem_ld64b(tl + T_S + 64 * hc, s);
+        store_shalf(sm + S_SA, row, hc, s);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) uh[j] = uh_next[j];
+      fence_proxy_async_smem();
+      tc_fence_before();
+      group_sync(1, kStateThreads);
+    }
+    // final state of this (sequence, head, segment)
+    float* dst = nullptr;
+    if (MODE == 0 && seg == p_last) dst = p.hT ? p.hT + soff : nullptr;
+    if (MODE == 1) dst = cpb + (kind == 1 ? 0 : kCpMat);
+    if (ok && dst != nullptr) {
+      tc_fence_after();
+      float s[64];
+      tmem_ld64b(tl + T_S + 64 * hc, s);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) dst[(size_t)(64 * hc + c) * 128 + row] = s[c];
+    }
+  } else if (MODE == 0) {
+    // ======================== output warps: D_O -> staging -> epilogue -> global
+    float* ost = reinterpret_cast<float*>(sm + S_OUT);
+    Tout* out = static_cast<Tout*>(p.out);
+    const int ow = warp - 8;
+    for (int64_t c = 0; c < ncs; ++c) {
+      const int st = (int)(c & 1);
+      bool w = false;
+      for (int spin = 0; spin < 64 && !w; ++spin) {
+        if (*abort_flag) break;
+        w = mbar_wait(&bar_o[st], (uint32_t)((c >> 1) & 1), 1u << 20);
+      }
+      ok = group_and(2, 128, w);
+      if (!ok) break;
+      tc_fence_after();
+      float o[64];
+      tmem_ld64b(tl + T_DO + 64 * st, o);
+      tc_fence_before();
+      group_sync(2, 128);
+      if (ow == 0 && lane == 0) mbar_arrive(&do_free[st]);
+#pragma unroll
+      for (int r = 0; r < 64; ++r) ost[r * 128 + row] = o[r];
+      group_sync(2, 128);
+      const int64_t cg = c_begin + c;
+      const int64_t rem = len - 64 * cg;
+      const int n = (int)(rem < 64 ? rem : 64);
+      const int64_t t0 = t_begin + 64 * cg;
+      for (int r = ow; r < n; r += 4) {
+        float4 y = *reinterpret_cast<const float4*>(ost + r * 128 + 4 * lane);
+        const size_t orow = ((size_t)(t0 + r) * H + h) * 128 + 4 * lane;
+        if (p.gate != nullptr) {
+          float ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+          ss = warp_sum(ss);
+          const float inv = rsqrtf(ss * (1.f / 128.f) + p.eps);
+          const uint2 gw = *reinterpret_cast<const uint2*>(p.gate + orow);
+          const float2 g01 = unpack_bf2(gw.x), g23 = unpack_bf2(gw.y);
+          float4 wv = make_float4(1.f, 1.f, 1.f, 1.f);
+          if (p.norm_w)
+            wv = make_float4(p.norm_w[4 * lane], p.norm_w[4 * lane + 1], p.norm_w[4 * lane + 2], p.norm_w[4 * lane + 3]);
+          y.x = y.x * inv * wv.x * sigmoidf_(g01.x);
+          y.y = y.y * inv * wv.y * sigmoidf_(g01.y);
+          y.z = y.z * inv * wv.z * sigmoidf_(g23.x);
+          y.w = y.w * inv * wv.w * sigmoidf_(g23.y);
+        }
+        if constexpr (sizeof(Tout) == 4) {
+          *reinterpret_cast<float4*>(out + orow) = y;
+        } else {
+          __nv_bfloat162 a = __floats2bfloat162_rn(y.x, y.y), b2 = __floats2bfloat162_rn(y.z, y.w);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&a);
+          pk.y = *reinterpret_cast<uint32_t*>(&b2);
+          *reinterpret_cast<uint2*>(out + orow) = pk;
+        }
+      }
+      group_sync(2, 128);  // staging buffer free for the next chunk
+    }
+    if (!ok) *abort_flag = 1;
+  }
+
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    atomicOr(p.err, KDA_DEVERR_WAIT_TIMEOUT);
+    mma_commit(bar_fin);  // let this thread's MMAs drain (bounded) before TMEM is released
+    mbar_wait(bar_fin, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// Segment merge: S_in(p+1) = P_p S_in(p) + b_p for p < p_last, fp32, on a 16-column slice.
+constexpr int kMergeThreads = 256;
+__global__ void __launch_bounds__(kMergeThreads) kda_cp_merge(const ScanParams p) {
+  __shared__ __align__(16) float sS[128][16];
+  const int b = blockIdx.x, h = blockIdx.y, j0 = 16 * blockIdx.z, tid = threadIdx.x;
+  if (p.cu != nullptr && p.plan[p.B + 1] == 0) return;
+  int64_t first_chunk, t_begin, len;
+  const int64_t nchunks = sequence_chunks(b, p.plan, p.cu, p.B, p.T, first_chunk, t_begin, len);
+  const int64_t p_last = nchunks > 0 ? (nchunks - 1) / p.seg_len : 0;
+  const size_t soff = ((size_t)b * p.H + h) * kCpMat;
+  float* cp = p.cp + (size_t)(b * p.H + h) * p.nseg * 3 * kCpMat;
+  for (int i = tid; i < 128 * 16; i += kMergeThreads) {
+    const int r = i >> 4, c = i & 15;
+    sS[r][c] = p.h0 ? p.h0[soff + (size_t)r * 128 + j0 + c] : 0.f;
+  }
+  __syncthreads();
+  const int r = tid >> 1, cb = (tid & 1) * 8;  // this thread: row r, columns cb..cb+7 of the slice
+  for (int64_t s = 0; s < p_last; ++s) {
+    const float* P = cp + (size_t)s * 3 * kCpMat;
+    const float* bo = P + kCpMat;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = bo[(size_t)r * 128 + j0 + cb + e];
+    for (int k0 = 0; k0 < 128; k0 += 32) {
+      // P row r, columns k0..k0+31 (each row is read by the two threads of that row)
+      float prow[32];
+#pragma unroll
+      for (int kk = 0; kk < 32; kk += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(P + (size_t)r * 128 + k0 + kk);
+        prow[kk] = v.x; prow[kk + 1] = v.y; prow[kk + 2] = v.z; prow[kk + 3] = v.w;
+      }
+#pragma unroll
+      for (int kk = 0; kk < 32; ++kk) {
+        const float4 s0 = *reinterpret_cast<const float4*>(&sS[k0 + kk][cb]);
+        const float4 s1 = *reinterpret_cast<const float4*>(&sS[k0 + kk][cb + 4]);
+        acc[0] = fmaf(prow[kk], s0.x, acc[0]); acc[1] = fmaf(prow[kk], s0.y, acc[1]);
+        acc[2] = fmaf(prow[kk], s0.z, acc[2]); acc[3] = fmaf(prow[kk], s0.w, acc[3]);
+        acc[4] = fmaf(prow[kk], s1.x, acc[4]); acc[5] = fmaf(prow[kk], s1.y, acc[5]);
+        acc[6] = fmaf(prow[kk], s1.z, acc[6]); acc[7] = fmaf(prow[kk], s1.w, acc[7]);
+      }
+    }
+    __syncthreads();
+    float* sin_next = cp + ((size_t)(s + 1) * 3 + 2) * kCpMat;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      sS[r][cb + e] = acc[e];
+      sin_next[(size_t)r * 128 + j0 + cb + e] = acc[e];
+    }
+    __syncthreads();
+  }
+}
+
+template <typename Tout>
+cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int32_t* plan, float* cp, int nseg,
+                        int64_t seg_len, cudaStream_t st) {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kScanSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  ScanParams p;
+  p.records = records; p.plan = plan; p.cu = a.cu_seqlens; p.B = a.B; p.T = a.T; p.H = a.H;
+  p.h0 = a.h0; p.hT = a.hT; p.out = a.out; p.gate = static_cast<const __nv_bfloat16*>(a.epi.gate);
+  p.norm_w = a.epi.norm_weight; p.eps = a.epi.eps; p.err = a.err;
+  p.nseg = nseg; p.seg_len = seg_len; p.cp = cp;
+  if (nseg > 1) {
+    {
+      TraceScope ts("kda_tc_chunk_scan_transition", st);
+      kda_tc_chunk_scan<Tout, 1><<<dim3((unsigned)a.B, (unsigned)a.H, (unsigned)(2 * (nseg - 1))), kScanThreads,
+                                   kScanSmem, st>>>(p);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    {
+      TraceScope ts("kda_cp_merge", st);
+      kda_cp_merge<<<dim3((unsigned)a.B, (unsigned)a.H, 8), kMergeThreads, 0, st>>>(p);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+  }
+  TraceScope ts("kda_tc_chunk_scan", st);
+  kda_tc_chunk_scan<Tout, 0><<<dim3((unsigned)a.B, (unsigned)a.H, (unsigned)nseg), kScanThreads, kScanSmem, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t scan_tc_launch(const PrefillArgs& a, const uint8_t* records, const int32_t* plan, float* cp, int nseg,
+                           int64_t seg_len, cudaStream_t st) {
+  return a.out_bf16 ? launch_scan<__nv_bfloat16>(a, records, plan, cp, nseg, seg_len, st)
+                    : launch_scan<float>(a, records, plan, cp, nseg, seg_len, st);
+}
+
+}  // namespace kda

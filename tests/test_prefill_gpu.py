@@ -208,3 +208,12 @@ def test_strong_decay_inside_chunk_with_weak_decay_across_the_half_boundary(dtyp
     assert_no_device_error()
     tol = TOL[inputs.torch_dtype(dtype)]
     assert rel_err(out, ref_out) <= tol and rel_err(hT, ref_hT) <= tol
+
+
+@pytest.mark.parametrize("lengths,H,epilogue", [((16384,), 4, False), ((20000, 300), 2, True)])
+def test_sequence_split_across_sms_matches_oracle(lengths, H, epilogue):
+    """Few (sequence, head) chains with long sequences: the state pass is split into segments
+    whose transitions are merged (intra-device context parallelism); results must not change."""
+    cfg = inputs.PrefillConfig("cp", H=H, dk=128, dv=128, dtype="bf16", lengths=lengths, B=len(lengths),
+                               h0_std=0.1, epilogue=epilogue, seed=309)
+    _check(cfg, epilogue=epilogue, device_gen=True)
