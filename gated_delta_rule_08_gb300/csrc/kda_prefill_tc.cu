@@ -46,12 +46,14 @@ namespace {
 using namespace tcx;
 
 // =================================================================== prep kernel
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 288;   // warps 0-7 compute, warp 8 stages inputs and issues the MMAs
+constexpr int kCompute = 256;
+constexpr int kIssuer = 8;
 // raw stage: k | q | v (bf16 token-row blocks) | g (fp32, four 32-channel blocks)
 constexpr uint32_t R_K = 0, R_Q = 16384, R_V = 32768, R_G = 49152, R_BYTES = 81920;
 constexpr uint32_t P_RAW0 = 0;
 constexpr uint32_t P_RAW1 = R_BYTES;
-constexpr uint32_t P_OPS = 2 * R_BYTES;  // 56 KB: one 64-channel pass of split-bf16 operands
+constexpr uint32_t P_OPS = 2 * R_BYTES;  // 56 KB: one 64-channel K block of split-bf16 operands
 constexpr uint32_t O_XH = 0, O_XL = 16384, O_YH = 32768, O_YL = 45056, O_BYTES = 57344;
 // after the A/M product the operand region holds the solve:
 constexpr uint32_t O_SA = 0;             // fp32 A [64][65]
@@ -59,47 +61,28 @@ constexpr uint32_t O_SX = 16640;         // fp32 X = (I + A)^-1 [64][65]
 constexpr uint32_t O_SY = 33280;         // fp32 scratch, three 16 x 16 blocks
 constexpr uint32_t O_TT = 37888;         // fp16 T [64 r][64 s] row format (1024-aligned)
 constexpr uint32_t P_MISC = P_OPS + O_BYTES;
-constexpr uint32_t M_BETA = 0;           // fp32 [64]
-constexpr uint32_t M_CON = 256;          // fp32 [5][128]: e^{G15}, e^{G47}, e^{G63-G15}, e^{G63-G47}, e^{G47-G15}
-constexpr uint32_t M_BAR = 2816;         // full[2], bar_am, bar_wu, bar_fin; tmem slot
-constexpr uint32_t M_END = 2880;
+constexpr uint32_t M_BETA = 0;           // fp32 [2 stages][64]
+constexpr uint32_t M_TOT = 512;          // fp32 [2][16 row groups][32 channels]: per-group decay sums
+constexpr uint32_t M_BAR = 4608;         // barriers, tmem slot, abort flag
+constexpr uint32_t M_END = 4736;
 constexpr uint32_t kPrepSmem = P_MISC + M_END + 1024;
 
-constexpr uint32_t T_AM = 0;   // TMEM: A/M accumulator [128 x 96]
-constexpr uint32_t T_W = 96;   // W^T [128 x 64]
-constexpr uint32_t T_U = 160;  // U_hat^T [128 x 64]
+constexpr uint32_t T_AM = 0;    // TMEM: [X_h Y_h + X_l Y_h | X_h Y_l] [128 x 192]
+constexpr uint32_t T_W = 192;   // W^T [128 x 64]
+constexpr uint32_t T_U = 256;   // U_hat^T [128 x 64]
 
-// x (8 floats) -> bf16 hi (x with its low 16 bits cleared, exact in bf16) and lo = x - hi
-// rounded to bf16, each packed as 8 bf16 values.
-__device__ __forceinline__ void split_bf16x8(const float* x, uint4& hi, uint4& lo) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t a = __float_as_uint(x[2 * j]) & 0xFFFF0000u, b = __float_as_uint(x[2 * j + 1]) & 0xFFFF0000u;
-    h[j] = (a >> 16) | b;
-    const __nv_bfloat162 t = __floats2bfloat162_rn(x[2 * j] - __uint_as_float(a), x[2 * j + 1] - __uint_as_float(b));
-    l[j] = *reinterpret_cast<const uint32_t*>(&t);
-  }
-  hi = make_uint4(h[0], h[1], h[2], h[3]);
-  lo = make_uint4(l[0], l[1], l[2], l[3]);
+// x (2 floats) -> bf16 hi (x with its low 16 bits cleared, exact in bf16) and lo = x - hi
+// rounded to bf16, each as a packed pair.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const uint32_t a = __float_as_uint(x0) & 0xFFFF0000u, b = __float_as_uint(x1) & 0xFFFF0000u;
+  hi = (a >> 16) | b;
+  const __nv_bfloat162 t = __floats2bfloat162_rn(x0 - __uint_as_float(a), x1 - __uint_as_float(b));
+  lo = *reinterpret_cast<const uint32_t*>(&t);
 }
 
 struct PrepMaps {
   CUtensorMap k, q, v, g;
 };
-
-__device__ __forceinline__ void issue_raw_loads(const PrepMaps& m, uint8_t* raw, uint64_t* bar, int h, int64_t t0) {
-  mbar_arrive_expect_tx(bar, R_BYTES);
-  const int y = (int)t0;
-#pragma unroll
-  for (int b = 0; b < 2; ++b) {
-    tma_load_2d(raw + R_K + 8192 * b, &m.k, h * 128 + 64 * b, y, bar);
-    tma_load_2d(raw + R_Q + 8192 * b, &m.q, h * 128 + 64 * b, y, bar);
-    tma_load_2d(raw + R_V + 8192 * b, &m.v, h * 128 + 64 * b, y, bar);
-  }
-#pragma unroll
-  for (int b = 0; b < 4; ++b) tma_load_2d(raw + R_G + 8192 * b, &m.g, h * 128 + 32 * b, y, bar);
-}
 
 // Next valid task index >= t (tasks: chunk-major, head-minor), or -1.
 __device__ __forceinline__ int64_t next_task(int64_t t, int64_t ntask, int64_t stride, const int32_t* plan,
@@ -115,6 +98,30 @@ __device__ __forceinline__ int64_t next_task(int64_t t, int64_t ntask, int64_t s
   return -1;
 }
 
+// Issuer warp: raw q/k/v/g tiles of a task by TMA, beta by plain loads into shared memory.
+// full[] expects two arrivals: the transaction-counted one and the beta one.
+__device__ __forceinline__ void stage_task(const PrepMaps& m, const float* beta, uint8_t* raw, float* sbeta,
+                                           uint64_t* bar, int h, int64_t t0, int n, int H, int lane) {
+  if (lane == 0) {
+    mbar_arrive_expect_tx(bar, R_BYTES);
+    const int y = (int)t0;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      tma_load_2d(raw + R_K + 8192 * b, &m.k, h * 128 + 64 * b, y, bar);
+      tma_load_2d(raw + R_Q + 8192 * b, &m.q, h * 128 + 64 * b, y, bar);
+      tma_load_2d(raw + R_V + 8192 * b, &m.v, h * 128 + 64 * b, y, bar);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) tma_load_2d(raw + R_G + 8192 * b, &m.g, h * 128 + 32 * b, y, bar);
+  }
+  const float b0 = lane < n ? beta[(size_t)(t0 + lane) * H + h] : 0.f;
+  const float b1 = lane + 32 < n ? beta[(size_t)(t0 + lane + 32) * H + h] : 0.f;
+  sbeta[lane] = b0;
+  sbeta[lane + 32] = b1;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
 __global__ void __launch_bounds__(kPrepThreads, 1)
 kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict__ beta,
                   const int32_t* __restrict__ plan, const int32_t* __restrict__ cu, int B, int64_t T, int H,
@@ -123,13 +130,16 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ops = sm + P_OPS;
   uint8_t* misc = sm + P_MISC;
-  float* sBeta = reinterpret_cast<float*>(misc + M_BETA);
-  float* sCon = reinterpret_cast<float*>(misc + M_CON);
-  uint64_t* full = reinterpret_cast<uint64_t*>(misc + M_BAR);  // [2]
-  uint64_t* bar_am = full + 2;
-  uint64_t* bar_wu = full + 3;
-  uint64_t* bar_fin = full + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + M_BAR + 48);
+  float* sBetaAll = reinterpret_cast<float*>(misc + M_BETA);
+  float2* sTot = reinterpret_cast<float2*>(misc + M_TOT);      // [2][16][16] channel pairs
+  uint64_t* full = reinterpret_cast<uint64_t*>(misc + M_BAR);  // [2] raw stage landed (+ beta)
+  uint64_t* ops_ready = full + 2;                              // [2] pass operands written (256 arrivals)
+  uint64_t* bar_ops = full + 4;                                // [2] pass MMAs done
+  uint64_t* tt_ready = full + 6;                               // T written (256 arrivals)
+  uint64_t* bar_wu = full + 7;                                 // W / U_hat MMAs done
+  uint64_t* bar_fin = full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + M_BAR + 80);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + M_BAR + 84);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t stride = gridDim.x;
@@ -139,358 +149,364 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
   if (task < 0) return;
 
   if (warp == 0) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   if (tid == 32) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
-    mbar_init(bar_am, 1);
+    mbar_init(&full[0], 2);
+    mbar_init(&full[1], 2);
+    mbar_init(&ops_ready[0], kCompute);
+    mbar_init(&ops_ready[1], kCompute);
+    mbar_init(&bar_ops[0], 1);
+    mbar_init(&bar_ops[1], 1);
+    mbar_init(tt_ready, kCompute);
     mbar_init(bar_wu, 1);
     mbar_init(bar_fin, 1);
+    *abort_flag = 0;
     mbar_fence_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (tid == 0) issue_raw_loads(maps, sm + P_RAW0, &full[0], h, t0);
 
-  bool ok = true;
-  uint32_t it = 0;
-  while (task >= 0 && ok) {
-    const int st = (int)(it & 1);
-    uint8_t* raw = sm + (st ? P_RAW1 : P_RAW0);
-    uint8_t* rec = records + ((size_t)chunk * H + h) * kRecBytes;
-    // next task: resolve and prefetch its raw tiles into the other stage
-    int nh = 0, nn = 0;
-    int64_t nt0 = 0, nchunk = 0;
-    const int64_t ntask_idx = next_task(task + stride, ntask, stride, plan, cu, B, T, H, nh, nt0, nn, nchunk);
-    if (tid == 0 && ntask_idx >= 0) issue_raw_loads(maps, sm + (st ? P_RAW0 : P_RAW1), &full[st ^ 1], nh, nt0);
-    float bval = 0.f;
-    if (tid < 64 && tid < n) bval = beta[(size_t)(t0 + tid) * H + h];
-    ok = __syncthreads_and(mbar_wait(&full[st], (it >> 1) & 1)) != 0;
-    if (!ok) break;
-
-    // ---- cumulative log-decay in place: warp w scans channel quads w, w+8, w+16, w+24; lane l
-    // holds rows 2l and 2l+1 (a pair sum, then a warp-wide inclusive scan of the pair sums)
-    {
-#pragma unroll 1
-      for (int qd = warp; qd < 32; qd += 8) {
-        const int r0 = 2 * lane, r1 = r0 + 1;
-        float4* p0 = reinterpret_cast<float4*>(raw + R_G + g_chunk(r0, qd));
-        float4* p1 = reinterpret_cast<float4*>(raw + R_G + g_chunk(r1, qd));
-        float4 a = (r0 < n) ? *p0 : make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 b = (r1 < n) ? *p1 : make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 x = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-        const float4 pair = x;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          float4 y;
-          y.x = __shfl_up_sync(0xffffffffu, x.x, o);
-          y.y = __shfl_up_sync(0xffffffffu, x.y, o);
-          y.z = __shfl_up_sync(0xffffffffu, x.z, o);
-          y.w = __shfl_up_sync(0xffffffffu, x.w, o);
-          if (lane >= o) { x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w; }
-        }
-        *p0 = make_float4(x.x - pair.x + a.x, x.y - pair.y + a.y, x.z - pair.z + a.z, x.w - pair.w + a.w);
-        *p1 = x;
-      }
-      // V -> fp16 in place (rows past the sequence end zeroed)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int idx = tid + 256 * i, r = idx >> 4, c8 = idx & 15;
-        uint4* p = reinterpret_cast<uint4*>(raw + R_V + trow_chunk(r, c8));
-        const uint4 w = *p;
-        float f[8];
-        const float2 a0 = unpack_bf2(w.x), a1 = unpack_bf2(w.y), a2 = unpack_bf2(w.z), a3 = unpack_bf2(w.w);
-        f[0] = a0.x; f[1] = a0.y; f[2] = a1.x; f[3] = a1.y; f[4] = a2.x; f[5] = a2.y; f[6] = a3.x; f[7] = a3.y;
-        if (r >= n)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) f[j] = 0.f;
-        *p = pack8_h(f);
-      }
-    }
-    if (tid < 64) sBeta[tid] = bval;
-    __syncthreads();
-    // per-channel constants and e^{G_C} for the record.  Only factors that cannot underflow while
-    // the product they help form is still significant are precomputed: e^{G15} >= e^{-80} and
-    // e^{G63-G47} >= e^{-80} always; e^{G47} may underflow, but then every q/k e^{G_r} it scales
-    // (r >= 32) is below e^{-12}.
-    if (tid < 128) {
-      const int c = tid;
-      const float* gb = reinterpret_cast<const float*>(raw + R_G);
-      auto G = [&](int r) {
-        return gb[(uint32_t)(c >> 5) * 2048u + (uint32_t)r * 32u + (((((uint32_t)c >> 2) & 7u) ^ ((uint32_t)r & 7u)) << 2) +
-                  ((uint32_t)c & 3u)];
-      };
-      const float g15 = G(15), g47 = G(47), g63 = G(63);
-      sCon[0 * 128 + c] = __expf(g15);
-      sCon[1 * 128 + c] = __expf(g47);
-      sCon[2 * 128 + c] = g47;
-      sCon[3 * 128 + c] = __expf(g63 - g47);
-      sCon[4 * 128 + c] = g63;
-      reinterpret_cast<float*>(rec + kRecGC)[c] = __expf(g63);
-    }
-    __syncthreads();
-
-    // ---- A and M: D[128 x 96] = X Y^T, X = [k e^{G-R}; q e^{G-R}], Y = [k e^{R-G}; k e^{G_47-G} (s < 32)],
-    // as a three-way bf16 split (x = hi + lo, hi = x with its low 16 bits cleared, lo = x - hi;
-    // products hi*hi + hi*lo + lo*hi accumulate in fp32, ~2^-16 relative), in two 64-channel passes.
-    // The same passes emit Q_hat and K_bar into the record and K_hat in place of k.
-    {
-      const int r = tid >> 2;            // row 0..63
-      const int cq = (tid & 3) * 16;     // 16 channels within the pass
-      const bool valid = r < n;
-      const int rref = r < 32 ? 15 : 47;
-      const int hsel = r < 32 ? 0 : 1;
-      const uint32_t id_am = idesc_bf16_f32(128, 96, false, false);
-      const uint64_t dxh = smem_desc_sw128(smem_u32(ops + O_XH), 16, 1024);
-      const uint64_t dxl = smem_desc_sw128(smem_u32(ops + O_XL), 16, 1024);
-      const uint64_t dyh = smem_desc_sw128(smem_u32(ops + O_YH), 16, 1024);
-      const uint64_t dyl = smem_desc_sw128(smem_u32(ops + O_YL), 16, 1024);
-#pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
-        if (pass > 0) {
-          ok = __syncthreads_and(ok && mbar_wait(bar_am, 0)) != 0;
+  if (warp == kIssuer) {
+    // ======================== issuer warp
+    int64_t last_stage_task = 0;  // tasks staged so far (for the drain on abort)
+    stage_task(maps, beta, sm + P_RAW0, sBetaAll, &full[0], h, t0, n, H, lane);
+    last_stage_task = 1;
+    bool ok = true;
+    const uint32_t id_hh = idesc_bf16_f32(128, 192, false, false);  // X_h [Y_h ; Y_l]^T
+    const uint32_t id_lh = idesc_bf16_f32(128, 96, false, false);   // X_l Y_h^T
+    const uint32_t id_wu = idesc_f16(128, 64, /*a_mn=*/true, /*b_mn=*/false);
+    const uint64_t dxh = smem_desc_sw128(smem_u32(ops + O_XH), 16, 1024);
+    const uint64_t dxl = smem_desc_sw128(smem_u32(ops + O_XL), 16, 1024);
+    const uint64_t dyh = smem_desc_sw128(smem_u32(ops + O_YH), 16, 1024);
+    const uint64_t dtt = smem_desc_sw128(smem_u32(ops + O_TT), 16, 1024);
+    uint32_t it = 0;
+    while (task >= 0 && ok) {
+      const int st = (int)(it & 1);
+      uint8_t* raw = sm + (st ? P_RAW1 : P_RAW0);
+      int nh = 0, nn = 0;
+      int64_t nt0 = 0, nchunk = 0;
+      const int64_t ntask_idx = next_task(task + stride, ntask, stride, plan, cu, B, T, H, nh, nt0, nn, nchunk);
+      if (ntask_idx >= 0) {
+        // the other raw stage is free once the previous task's W / U_hat MMAs are done
+        if (it >= 1) {
+          bool w = true;
+          if (lane == 0) w = wait_or_abort(bar_wu, (it - 1) & 1, abort_flag);
+          ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
           if (!ok) break;
         }
-#pragma unroll
-        for (int half8 = 0; half8 < 2; ++half8) {
-          const int c0 = 64 * pass + cq + 8 * half8;  // first of 8 channels
-          float kv[8], qv[8], G[8], R[8], eR[8], g47[8], c3[8], g63[8];
-          {
-            const uint4 wk = *reinterpret_cast<const uint4*>(raw + R_K + trow_chunk(r, c0 >> 3));
-            const uint4 wq = *reinterpret_cast<const uint4*>(raw + R_Q + trow_chunk(r, c0 >> 3));
-            const uint32_t ku[4] = {wk.x, wk.y, wk.z, wk.w}, qu[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float2 a = unpack_bf2(ku[j]), bq = unpack_bf2(qu[j]);
-              kv[2 * j] = valid ? a.x : 0.f; kv[2 * j + 1] = valid ? a.y : 0.f;
-              qv[2 * j] = valid ? bq.x : 0.f; qv[2 * j + 1] = valid ? bq.y : 0.f;
-            }
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const float4 g4 = *reinterpret_cast<const float4*>(raw + R_G + g_chunk(r, (c0 >> 2) + hh));
-              const float4 r4 = *reinterpret_cast<const float4*>(raw + R_G + g_chunk(rref, (c0 >> 2) + hh));
-              const float4 e4 = *reinterpret_cast<const float4*>(sCon + hsel * 128 + c0 + 4 * hh);
-              const float4 a4 = *reinterpret_cast<const float4*>(sCon + 2 * 128 + c0 + 4 * hh);
-              const float4 b4 = *reinterpret_cast<const float4*>(sCon + 3 * 128 + c0 + 4 * hh);
-              const float4 d4 = *reinterpret_cast<const float4*>(sCon + 4 * 128 + c0 + 4 * hh);
-              const int o = 4 * hh;
-              G[o] = g4.x; G[o + 1] = g4.y; G[o + 2] = g4.z; G[o + 3] = g4.w;
-              R[o] = r4.x; R[o + 1] = r4.y; R[o + 2] = r4.z; R[o + 3] = r4.w;
-              eR[o] = e4.x; eR[o + 1] = e4.y; eR[o + 2] = e4.z; eR[o + 3] = e4.w;
-              g47[o] = a4.x; g47[o + 1] = a4.y; g47[o + 2] = a4.z; g47[o + 3] = a4.w;
-              c3[o] = b4.x; c3[o + 1] = b4.y; c3[o + 2] = b4.z; c3[o + 3] = b4.w;
-              g63[o] = d4.x; g63[o + 1] = d4.y; g63[o + 2] = d4.z; g63[o + 3] = d4.w;
-            }
-          }
-          float xk[8], xq[8], yy[8], zz[8], qh[8], kb[8], kh[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float e1 = __expf(G[j] - R[j]);
-            const float e2 = __expf(R[j] - G[j]);
-            xk[j] = kv[j] * e1;
-            xq[j] = qv[j] * e1;
-            yy[j] = kv[j] * e2;
-            qh[j] = qv[j] * e1 * eR[j];  // q e^{G}
-            kh[j] = kv[j] * e1 * eR[j];  // k e^{G}
-            if (hsel == 0) {
-              // rows < 32: k e^{G_47 - G} and k e^{G_C - G} from one exponential each (a factored
-              // form can underflow while the product it feeds is O(1))
-              zz[j] = kv[j] * __expf(g47[j] - G[j]);
-              kb[j] = kv[j] * __expf(g63[j] - G[j]);
-            } else {
-              zz[j] = 0.f;
-              kb[j] = kv[j] * e2 * c3[j];  // e^{G_C - G_47} >= e^{-80}: no underflow
-            }
-          }
-          uint4 hi, lo;
-          const uint32_t ck = (uint32_t)((c0 & 63) >> 3);  // 16-byte chunk within the 128-byte row
-          split_bf16x8(xk, hi, lo);
-          *reinterpret_cast<uint4*>(ops + O_XH + row_chunk(r, ck)) = hi;
-          *reinterpret_cast<uint4*>(ops + O_XL + row_chunk(r, ck)) = lo;
-          split_bf16x8(xq, hi, lo);
-          *reinterpret_cast<uint4*>(ops + O_XH + row_chunk(64 + r, ck)) = hi;
-          *reinterpret_cast<uint4*>(ops + O_XL + row_chunk(64 + r, ck)) = lo;
-          split_bf16x8(yy, hi, lo);
-          *reinterpret_cast<uint4*>(ops + O_YH + row_chunk(r, ck)) = hi;
-          *reinterpret_cast<uint4*>(ops + O_YL + row_chunk(r, ck)) = lo;
-          if (hsel == 0) {
-            split_bf16x8(zz, hi, lo);
-            *reinterpret_cast<uint4*>(ops + O_YH + row_chunk(64 + r, ck)) = hi;
-            *reinterpret_cast<uint4*>(ops + O_YL + row_chunk(64 + r, ck)) = lo;
-          }
-          *reinterpret_cast<uint4*>(rec + kRecQH + trow_chunk(r, c0 >> 3)) = pack8_h(qh);
-          *reinterpret_cast<uint4*>(rec + kRecKB + trow_chunk(r, c0 >> 3)) = pack8_h(kb);
-          *reinterpret_cast<uint4*>(raw + R_K + trow_chunk(r, c0 >> 3)) = pack8_h(kh);  // K_hat in place
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
+        stage_task(maps, beta, sm + (st ? P_RAW0 : P_RAW1), sBetaAll + 64 * (st ^ 1), &full[st ^ 1], nh, nt0, nn, H,
+                   lane);
+        ++last_stage_task;
+      }
+      if (lane == 0) {
+        for (int pass = 0; pass < 4 && ok; ++pass) {
+          ok = wait_or_abort(&ops_ready[pass & 1], (uint32_t)((pass >> 1) & 1), abort_flag);
+          if (!ok) break;
           tc_fence_after();
 #pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint32_t off = (uint32_t)(32 * (pass & 1) + 16 * kk) * 2u;
+            mma_bf16_ss(tmem + T_AM, desc_add(dxh, off), desc_add(dyh, off), id_hh, pass > 0 || kk > 0);
+            mma_bf16_ss(tmem + T_AM, desc_add(dxl, off), desc_add(dyh, off), id_lh, true);
+          }
+          mma_commit(&bar_ops[pass & 1]);
+        }
+        if (ok) ok = wait_or_abort(tt_ready, it & 1, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          const uint64_t dkh = smem_desc_sw128(smem_u32(raw + R_K), 8192, 1024);
+          const uint64_t dvv = smem_desc_sw128(smem_u32(raw + R_V), 8192, 1024);
+#pragma unroll
           for (int k0 = 0; k0 < 64; k0 += 16) {
-            const uint32_t off = (uint32_t)k0 * 2u;
-            mma_bf16_ss(tmem + T_AM, desc_add(dxh, off), desc_add(dyh, off), id_am, pass > 0 || k0 > 0);
-            mma_bf16_ss(tmem + T_AM, desc_add(dxh, off), desc_add(dyl, off), id_am, true);
-            mma_bf16_ss(tmem + T_AM, desc_add(dxl, off), desc_add(dyh, off), id_am, true);
+            mma_f16(tmem + T_W, desc_add(dkh, (k0 >> 3) * 1024), desc_add(dtt, k0 * 2), id_wu, k0 > 0);
+            mma_f16(tmem + T_U, desc_add(dvv, (k0 >> 3) * 1024), desc_add(dtt, k0 * 2), id_wu, k0 > 0);
           }
-          mma_commit(bar_am);
+          mma_commit(bar_wu);
         }
       }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      task = ntask_idx;
+      h = nh; n = nn; t0 = nt0; chunk = nchunk;
+      ++it;
     }
-    if (!ok) break;
-    ok = __syncthreads_and(mbar_wait(bar_am, 1)) != 0;  // 2nd completion of this task: parity 1
-    if (!ok) break;
-    tc_fence_after();
-
-    // ---- TMEM -> A (fp32, beta-scaled strict lower) and M (fp16, straight into the record)
-    float* sA = reinterpret_cast<float*>(ops + O_SA);
-    if (warp < 4) {
-      const int lrow = warp * 32 + lane;  // 0..63 key rows (A), 64..127 query rows (M)
-      const int r = lrow & 63;
-      float d[96];
-#pragma unroll
-      for (int q4 = 0; q4 < 6; ++q4) {
-        float t[16];
-        tmem_ld16(tmem_lane(tmem + T_AM, warp) + 16 * q4, t);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) d[16 * q4 + j] = t[j];
-      }
-      tmem_wait_ld();
-      float row[64];
-#pragma unroll
-      for (int s = 0; s < 64; ++s) {
-        const bool same = (s >> 5) == (r >> 5);
-        const float raw_v = same ? d[s] : ((r >= 32 && s < 32) ? d[64 + (s & 31)] : 0.f);
-        row[s] = raw_v;
-      }
-      if (lrow < 64) {
-        const float br = sBeta[r];
-#pragma unroll
-        for (int s = 0; s < 64; ++s) sA[r * 65 + s] = (s < r) ? br * row[s] : 0.f;  // select, not mask-multiply
-      } else {
-#pragma unroll
-        for (int s = 0; s < 64; ++s) row[s] = (s <= r) ? row[s] : 0.f;
-        store_row64(rec + kRecMM, r, row);
-      }
+    if (lane == 0 && (!ok || *abort_flag)) {
+      *abort_flag = 1;
+      // let staged copies and issued MMAs drain (bounded) before TMEM is released
+      const int64_t lt = last_stage_task - 1;
+      mbar_wait(&full[lt & 1], (uint32_t)((lt >> 1) & 1));
+      mma_commit(bar_fin);
+      mbar_wait(bar_fin, 0);
     }
-    __syncthreads();
+  } else {
+    // ======================== compute warps
+    const int cp = tid & 15, rg = tid >> 4;  // channel pair within a 32-channel pass, row group (4 rows)
+    const int cl = 2 * cp;
+    bool ok = true;
+    uint32_t it = 0;
+    while (task >= 0 && ok) {
+      const int st = (int)(it & 1);
+      uint8_t* raw = sm + (st ? P_RAW1 : P_RAW0);
+      const float* sBeta = sBetaAll + 64 * st;
+      uint8_t* rec = records + ((size_t)chunk * H + h) * kRecBytes;
+      int nh = 0, nn = 0;
+      int64_t nt0 = 0, nchunk = 0;
+      const int64_t ntask_idx = next_task(task + stride, ntask, stride, plan, cu, B, T, H, nh, nt0, nn, nchunk);
+      // every break decision of the compute warps is made together (named barriers follow)
+      ok = group_and(1, kCompute, wait_or_abort(&full[st], (it >> 1) & 1, abort_flag));
+      if (!ok) break;
 
-    // ---- T = (I + A)^-1 Diag(beta), blocked 16 x 16 forward substitution (fp32)
-    {
-      float* sX = reinterpret_cast<float*>(ops + O_SX);
-      float* sY = reinterpret_cast<float*>(ops + O_SY);
-      // diagonal blocks: one thread per column, substitution inside its 16 x 16 block
-      if (tid < 64) {
-        const int s = tid, r0 = s & ~15;
-        float x[16];
+      // ---- four 32-channel passes.  Pass p fills half (p & 1) of every 128-byte operand row, so
+      // it only has to wait for the MMAs of pass p - 2.  Per pass: cumulative log-decay of this
+      // thread's 4 rows x 2 channels, the group sums exchanged through shared memory, then the
+      // reference-scaled operands, the record's Q_hat^T / K_bar^T, K_hat (in place of k) and V (fp16).
+#pragma unroll 1
+      for (int pass = 0; pass < 4; ++pass) {
+        const int c = 32 * pass + cl;  // first of this thread's two channels
+        float2 L[4];
+        {
+          float2 run = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int r = r0 + i;
-          float acc0 = 0.f, acc1 = 0.f;  // two independent chains
-#pragma unroll
-          for (int j = 0; j < i; j += 2) {
-            acc0 = fmaf(sA[r * 65 + r0 + j], x[j], acc0);
-            if (j + 1 < i) acc1 = fmaf(sA[r * 65 + r0 + j + 1], x[j + 1], acc1);
+          for (int i = 0; i < 4; ++i) {
+            const int r = 4 * rg + i;
+            float2 gv = make_float2(0.f, 0.f);
+            if (r < n)
+              gv = *reinterpret_cast<const float2*>(raw + R_G + 8192u * pass + r * 128 +
+                                                    ((((uint32_t)cl >> 2) ^ ((uint32_t)r & 7u)) << 4) + (cl & 3) * 4);
+            run.x += gv.x;
+            run.y += gv.y;
+            L[i] = run;
           }
-          x[i] = (r == s) ? 1.f : ((r < s) ? 0.f : -(acc0 + acc1));
+          sTot[(pass & 1) * 256 + rg * 16 + cp] = run;
         }
+        if (pass >= 2) ok = wait_or_abort(&bar_ops[pass & 1], 0, abort_flag);
+        ok = group_and(1, kCompute, ok);
+        if (!ok) break;
+        float2 off = make_float2(0.f, 0.f), cum = make_float2(0.f, 0.f), G15, G47, G63;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sX[(r0 + i) * 65 + s] = x[i];
+        for (int g = 0; g < 16; ++g) {
+          const float2 t = sTot[(pass & 1) * 256 + g * 16 + cp];
+          if (g == rg) off = cum;
+          cum.x += t.x;
+          cum.y += t.y;
+          if (g == 3) G15 = cum;
+          if (g == 11) G47 = cum;
+        }
+        G63 = cum;
+        const bool first = rg < 8;  // rows < 32: reference row 15, else 47
+        const float2 R = first ? G15 : G47;
+        const float eR0 = __expf(R.x), eR1 = __expf(R.y);
+        const float c30 = __expf(G63.x - G47.x), c31 = __expf(G63.y - G47.y);
+        if (rg == 0)
+          *reinterpret_cast<float2*>(rec + kRecGC + c * 4) = make_float2(__expf(G63.x), __expf(G63.y));
+        uint32_t qh2[4], kb2[4];
+        const uint32_t kbyte = (uint32_t)(c & 63) * 2u;  // byte of channel c within its 128-byte row
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 4 * rg + i;
+          const bool valid = r < n;
+          const float G0 = off.x + L[i].x, G1 = off.y + L[i].y;
+          const uint32_t toff = (uint32_t)(c >> 6) * 8192u + (uint32_t)r * 128u +
+                                ((((kbyte >> 4) ^ (uint32_t)r) & 7u) << 4) + (kbyte & 15u);
+          uint32_t* pk = reinterpret_cast<uint32_t*>(raw + R_K + toff);
+          uint32_t* pq = reinterpret_cast<uint32_t*>(raw + R_Q + toff);
+          uint32_t* pv = reinterpret_cast<uint32_t*>(raw + R_V + toff);
+          float2 k2 = unpack_bf2(*pk), q2 = unpack_bf2(*pq), v2 = unpack_bf2(*pv);
+          if (!valid) {
+            k2 = make_float2(0.f, 0.f);
+            q2 = k2;
+            v2 = k2;
+          }
+          const float e10 = __expf(G0 - R.x), e11 = __expf(G1 - R.y);
+          const float e20 = __expf(R.x - G0), e21 = __expf(R.y - G1);
+          uint32_t hi, lo;
+          const uint32_t ob = (uint32_t)r * 128u + ((((kbyte >> 4) ^ (uint32_t)r) & 7u) << 4) + (kbyte & 15u);
+          const uint32_t ob64 = ob + 64u * 128u;  // row 64 + r (same swizzle phase)
+          split_bf16x2(k2.x * e10, k2.y * e11, hi, lo);
+          *reinterpret_cast<uint32_t*>(ops + O_XH + ob) = hi;
+          *reinterpret_cast<uint32_t*>(ops + O_XL + ob) = lo;
+          split_bf16x2(q2.x * e10, q2.y * e11, hi, lo);
+          *reinterpret_cast<uint32_t*>(ops + O_XH + ob64) = hi;
+          *reinterpret_cast<uint32_t*>(ops + O_XL + ob64) = lo;
+          split_bf16x2(k2.x * e20, k2.y * e21, hi, lo);
+          *reinterpret_cast<uint32_t*>(ops + O_YH + ob) = hi;
+          *reinterpret_cast<uint32_t*>(ops + O_YL + ob) = lo;
+          float kb0, kb1;
+          if (first) {
+            // rows < 32: k e^{G_47 - G} and k e^{G_C - G} from one exponential each (a factored
+            // form can underflow while the product it feeds is O(1))
+            split_bf16x2(k2.x * __expf(G47.x - G0), k2.y * __expf(G47.y - G1), hi, lo);
+            *reinterpret_cast<uint32_t*>(ops + O_YH + ob64) = hi;
+            *reinterpret_cast<uint32_t*>(ops + O_YL + ob64) = lo;
+            kb0 = k2.x * __expf(G63.x - G0);
+            kb1 = k2.y * __expf(G63.y - G1);
+          } else {
+            kb0 = k2.x * e20 * c30;  // e^{G_C - G_47} >= e^{-80}: no underflow
+            kb1 = k2.y * e21 * c31;
+          }
+          qh2[i] = pack_h2(q2.x * e10 * eR0, q2.y * e11 * eR1);  // q e^{G}
+          kb2[i] = pack_h2(kb0, kb1);
+          *pk = pack_h2(k2.x * e10 * eR0, k2.y * e11 * eR1);     // K_hat = k e^{G}, in place
+          *pv = pack_h2(v2.x, v2.y);                              // V as fp16, in place
+        }
+        // Q_hat^T / K_bar^T rows (channel-major): lanes l and l ^ 16 hold rows 8w..8w+3 and
+        // 8w+4..8w+7 of the same two channels; after one exchange each writes a full 16-byte
+        // chunk (8 rows) of one channel.
+        {
+          const bool lower = lane < 16;
+          const int ch = lower ? c : c + 1;
+          const uint32_t chunk_off = row_chunk(ch, rg >> 1);
+#pragma unroll
+          for (int a = 0; a < 2; ++a) {
+            const uint32_t* x = a == 0 ? qh2 : kb2;
+            const uint32_t c0a = __byte_perm(x[0], x[1], 0x5410), c0b = __byte_perm(x[2], x[3], 0x5410);  // channel c
+            const uint32_t c1a = __byte_perm(x[0], x[1], 0x7632), c1b = __byte_perm(x[2], x[3], 0x7632);  // channel c+1
+            const uint32_t s0 = lower ? c1a : c0a, s1 = lower ? c1b : c0b;
+            const uint32_t r0 = __shfl_xor_sync(0xffffffffu, s0, 16), r1 = __shfl_xor_sync(0xffffffffu, s1, 16);
+            const uint4 v = lower ? make_uint4(c0a, c0b, r0, r1) : make_uint4(r0, r1, c1a, c1b);
+            *reinterpret_cast<uint4*>(rec + (a == 0 ? kRecQT : kRecKT) + chunk_off) = v;
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&ops_ready[pass & 1]);
       }
-      __syncthreads();
-      // block rows 1..3: X_ij = -X_ii * sum_{m=j}^{i-1} A_im X_mj (16 x 16 blocks, one entry per thread)
-      const int rr = tid >> 4, cc = tid & 15;
+      if (!ok) break;
+      ok = group_and(1, kCompute, wait_or_abort(&bar_ops[1], 1, abort_flag));  // pass 3 (and all before) done
+      if (!ok) break;
+      tc_fence_after();
+
+      // ---- TMEM -> A (fp32, beta-scaled strict lower) and M (fp16, into the record).
+      // D[:, 0..95] + D[:, 96..191]; columns 0..63 hold the two diagonal 32 x 32 blocks, 64..95 the
+      // off-diagonal block (rows >= 32, columns < 32).  Warp w: TMEM lane quadrant w & 3, s-half w >> 2.
+      float* sA = reinterpret_cast<float*>(ops + O_SA);
+      {
+        const int q = warp & 3, hh = warp >> 2;
+        const int lrow = 32 * q + lane;
+        const int r = lrow & 63;
+        float val[32];
+        if ((q & 1) == 0 && hh == 1) {
 #pragma unroll
-      for (int i = 1; i < 4; ++i) {
+          for (int j = 0; j < 32; ++j) val[j] = 0.f;  // upper off-diagonal block
+        } else {
+          const uint32_t c1 = (q & 1) == 0 ? 0u : (hh == 0 ? 64u : 32u);
+          float a1[32], a2[32];
+          tmem_ld32(tmem_lane(tmem + T_AM, warp) + c1, a1);
+          tmem_ld32(tmem_lane(tmem + T_AM, warp) + c1 + 96u, a2);
+          tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < i; ++j) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int j = 0; j < 32; ++j) val[j] = a1[j] + a2[j];
+        }
+        if (lrow < 64) {
+          const float br = sBeta[r];
 #pragma unroll
-          for (int m = j; m < i; ++m) {
+          for (int j = 0; j < 32; ++j) {
+            const int s_ = 32 * hh + j;
+            sA[r * 65 + s_] = (s_ < r) ? br * val[j] : 0.f;  // select, not mask-multiply
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) val[j] = (32 * hh + j <= r) ? val[j] : 0.f;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            *reinterpret_cast<uint4*>(rec + kRecMM + row_chunk(r, 4 * hh + jj)) = pack8_h(val + 8 * jj);
+        }
+      }
+      group_sync(1, kCompute);
+
+      // ---- T = (I + A)^-1 Diag(beta), blocked 16 x 16 forward substitution (fp32)
+      {
+        float* sX = reinterpret_cast<float*>(ops + O_SX);
+        float* sY = reinterpret_cast<float*>(ops + O_SY);
+        // diagonal blocks: one thread per column, substitution inside its 16 x 16 block
+        if (tid < 64) {
+          const int s_ = tid, r0 = s_ & ~15;
+          float x[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int r = r0 + i;
+            float acc0 = 0.f, acc1 = 0.f;  // two independent chains
+#pragma unroll
+            for (int j = 0; j < i; j += 2) {
+              acc0 = fmaf(sA[r * 65 + r0 + j], x[j], acc0);
+              if (j + 1 < i) acc1 = fmaf(sA[r * 65 + r0 + j + 1], x[j + 1], acc1);
+            }
+            x[i] = (r == s_) ? 1.f : ((r < s_) ? 0.f : -(acc0 + acc1));
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sX[(r0 + i) * 65 + s_] = x[i];
+        }
+        group_sync(1, kCompute);
+        // block rows 1..3: X_ij = -X_ii * sum_{m=j}^{i-1} A_im X_mj (16 x 16 blocks, one entry per thread)
+        const int rr = tid >> 4, cc = tid & 15;
+#pragma unroll
+        for (int i = 1; i < 4; ++i) {
+#pragma unroll
+          for (int j = 0; j < i; ++j) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m = j; m < i; ++m) {
+#pragma unroll
+              for (int k2 = 0; k2 < 16; ++k2)
+                acc[k2 & 3] = fmaf(sA[(16 * i + rr) * 65 + 16 * m + k2], sX[(16 * m + k2) * 65 + 16 * j + cc], acc[k2 & 3]);
+            }
+            sY[j * 256 + rr * 16 + cc] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+          }
+          group_sync(1, kCompute);
+#pragma unroll
+          for (int j = 0; j < i; ++j) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k2 = 0; k2 < 16; ++k2)
-              acc[k2 & 3] = fmaf(sA[(16 * i + rr) * 65 + 16 * m + k2], sX[(16 * m + k2) * 65 + 16 * j + cc], acc[k2 & 3]);
+              acc[k2 & 3] = fmaf(sX[(16 * i + rr) * 65 + 16 * i + k2], sY[j * 256 + k2 * 16 + cc], acc[k2 & 3]);
+            sX[(16 * i + rr) * 65 + 16 * j + cc] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
           }
-          sY[j * 256 + rr * 16 + cc] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+          group_sync(1, kCompute);
         }
-        __syncthreads();
+        // T = X Diag(beta) -> fp16 row format [r][s] (zero above the diagonal)
+        {
+          const int r = tid >> 2, j0 = (tid & 3) * 2;  // two 8-column chunks per thread
 #pragma unroll
-        for (int j = 0; j < i; ++j) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int jj = 0; jj < 2; ++jj) {
+            const int j = j0 + jj;
+            float v[8];
 #pragma unroll
-          for (int k2 = 0; k2 < 16; ++k2)
-            acc[k2 & 3] = fmaf(sX[(16 * i + rr) * 65 + 16 * i + k2], sY[j * 256 + k2 * 16 + cc], acc[k2 & 3]);
-          sX[(16 * i + rr) * 65 + 16 * j + cc] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
-        }
-        __syncthreads();
-      }
-      // T = X Diag(beta) -> fp16 row format [r][s] (zero above the diagonal)
-      {
-        const int r = tid >> 2, j0 = (tid & 3) * 2;  // two 8-column chunks per thread
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = j0 + jj;
-          float v[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int s = 8 * j + e;
-            v[e] = (s <= r) ? sX[r * 65 + s] * sBeta[s] : 0.f;
+            for (int e = 0; e < 8; ++e) {
+              const int s_ = 8 * j + e;
+              v[e] = (s_ <= r) ? sX[r * 65 + s_] * sBeta[s_] : 0.f;
+            }
+            *reinterpret_cast<uint4*>(ops + O_TT + row_chunk(r, j)) = pack8_h(v);
           }
-          *reinterpret_cast<uint4*>(ops + O_TT + row_chunk(r, j)) = pack8_h(v);
         }
       }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
+      fence_proxy_async_smem();
+      mbar_arrive(tt_ready);
 
-    // ---- W^T = K_hat^T T^T, U_hat^T = V^T T^T (fp16 MMAs, M=128, N=64, K=64)
-    if (tid == 0) {
+      // ---- W^T = K_hat^T T^T, U_hat^T = V^T T^T (issued by the issuer warp) -> the record
+      ok = group_and(1, kCompute, wait_or_abort(bar_wu, it & 1, abort_flag));
+      if (!ok) break;
       tc_fence_after();
-      const uint32_t idesc = idesc_f16(128, 64, /*a_mn=*/true, /*b_mn=*/false);
-      const uint64_t dtt = smem_desc_sw128(smem_u32(ops + O_TT), 16, 1024);
-      const uint64_t dkh = smem_desc_sw128(smem_u32(raw + R_K), 8192, 1024);
-      const uint64_t dvv = smem_desc_sw128(smem_u32(raw + R_V), 8192, 1024);
-#pragma unroll
-      for (int k0 = 0; k0 < 64; k0 += 16) {
-        mma_f16(tmem + T_W, desc_add(dkh, (k0 >> 3) * 1024), desc_add(dtt, k0 * 2), idesc, k0 > 0);
-        mma_f16(tmem + T_U, desc_add(dvv, (k0 >> 3) * 1024), desc_add(dtt, k0 * 2), idesc, k0 > 0);
+      {
+        const int row = (warp & 3) * 32 + lane;  // dk row (W^T, warps 0-3) or dv row (U_hat^T, warps 4-7)
+        float vrow[64];
+        tmem_ld64(tmem_lane(tmem + (warp < 4 ? T_W : T_U), warp), vrow);
+        store_row64(rec + (warp < 4 ? kRecWT : kRecUT), row, vrow);
       }
-      mma_commit(bar_wu);
+      tc_fence_before();
+      task = ntask_idx;
+      h = nh; n = nn; t0 = nt0; chunk = nchunk;
+      ++it;
     }
-    ok = __syncthreads_and(mbar_wait(bar_wu, it & 1)) != 0;
-    if (!ok) break;
-    tc_fence_after();
-    {
-      const int row = (warp & 3) * 32 + lane;  // dk row (W^T, warps 0-3) or dv row (U_hat^T, warps 4-7)
-      float vrow[64];
-      tmem_ld64(tmem_lane(tmem + (warp < 4 ? T_W : T_U), warp), vrow);
-      store_row64(rec + (warp < 4 ? kRecWT : kRecUT), row, vrow);
-    }
-    fence_proxy_async_smem();  // generic writes of this stage happen before the next TMA into it
-    tc_fence_before();
-    __syncthreads();
-    task = ntask_idx;
-    h = nh; n = nn; t0 = nt0; chunk = nchunk;
-    ++it;
+    if (!ok) *abort_flag = 1;
   }
 
-  if (!ok && tid == 0) {
-    // a wait ran out: record it; let in-flight TMA loads and MMAs drain (bounded), free TMEM
-    atomicOr(err, KDA_DEVERR_WAIT_TIMEOUT);
-    mbar_wait(&full[(it + 1) & 1], ((it + 1) >> 1) & 1);
-    mma_commit(bar_fin);
-    mbar_wait(bar_fin, 0);
-  }
   tc_fence_before();
   __syncthreads();
+  if (tid == 0 && *abort_flag) atomicOr(err, KDA_DEVERR_WAIT_TIMEOUT);
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // ----------------------------------------------------------------- host side

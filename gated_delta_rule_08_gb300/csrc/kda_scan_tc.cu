@@ -13,12 +13,18 @@
 // both are ordinary runs of the same state pass.  The merge then walks the segments,
 // S_in(p+1) = P_p S_in(p) + b_p, and a last pass re-runs every segment from its S_in with outputs.
 //
-//  kda_tc_chunk_scan<Tout, MODE> (grid = sequences x heads x segments, 12 warps):
-//    warps 0-7 run the state chain: state^T (fp32) resident in TMEM, an fp16 copy in shared
-//      memory as the MMA A operand; two warps per TMEM lane quadrant, each owning half of
-//      the columns, so every TMEM <-> register <-> shared conversion is split in two;
-//    MODE 0 (read-out): warps 8-11 drain the double-buffered read-out accumulator through a
-//      staging buffer and run the optional RMSNorm + gate epilogue, off the serial path;
+//  kda_tc_chunk_scan<Tout, MODE> (grid = sequences x heads x segments, 13 warps):
+//    the state^T (dv x dk, fp32) lives in TMEM for the whole segment, next to an fp16 copy that
+//    is the A operand (read from TMEM) of the first fused product
+//      [D_U | D_O] = S^T [W^T | Q_hat^T]                      (8 MMAs, N = 128)
+//    and U^T (fp16, also in TMEM) is the A operand of the second
+//      [D_O | S^T] += U^T [M ; K_bar^T]^T                     (4 MMAs, N = 192),
+//    with S^T already scaled by Diag(e^{G_C}) in place.
+//    warp 12 (one lane) stages the records with bulk copies and issues every MMA;
+//    warps 0-7 (two per TMEM lane quadrant, each owning half of the columns) convert
+//      D_U -> U^T and the updated state -> its fp16 copy, and apply the decay;
+//    MODE 0 (read-out): warps 8-11 drain D_O through a staging buffer and run the optional
+//      RMSNorm + gate epilogue, off the serial path;
 //    MODE 1 (transition): z = 2 p + kind; kind 0 runs b_p, kind 1 runs P_p; no read-out.
 //  kda_cp_merge (grid = sequences x heads x 8 column slices): the sequential segment merge in fp32.
 #include <cuda_bf16.h>
@@ -31,21 +37,22 @@ namespace {
 
 using namespace tcx;
 
-constexpr int kScanThreads = 384;
+constexpr int kScanThreads = 416;
 constexpr int kStateThreads = 256;               // warps 0-7
+constexpr int kIssuerWarp = 12;
 constexpr uint32_t kStage = 59392;               // staged record bytes, 1024-aligned
 constexpr uint32_t S_STAGE0 = 0;
 constexpr uint32_t S_STAGE1 = kStage;
-constexpr uint32_t S_SA = 2 * kStage;            // fp16 state^T [128 rows][128], two 16 KB K-blocks
-constexpr uint32_t S_UA = S_SA + 32768;          // fp16 U^T [128 rows][64 r]
-constexpr uint32_t S_OUT = S_UA + 16384;         // fp32 read-out staging [64 r][128 dv]
+constexpr uint32_t S_OUT = 2 * kStage;           // fp32 read-out staging [64 r][128 dv]
 constexpr uint32_t S_BAR = S_OUT + 32768;        // barriers + tmem slot + abort flag
 constexpr uint32_t S_END = S_BAR + 128;
 constexpr uint32_t kScanSmem = S_END + 1024;
 
-constexpr uint32_t T_S = 0;      // TMEM: state^T fp32 [128 x 128]
-constexpr uint32_t T_DU = 128;   // D_U [128 x 64]
-constexpr uint32_t T_DO = 192;   // D_O, two buffers [128 x 64] at 192 and 256
+constexpr uint32_t T_DU = 0;     // TMEM: D_U [128 x 64]
+constexpr uint32_t T_DO = 64;    // D_O [128 x 64]   (directly after D_U and directly before S)
+constexpr uint32_t T_S = 128;    // state^T fp32 [128 x 128]
+constexpr uint32_t T_S16 = 256;  // state^T fp16 pairs [128 x 64 columns]
+constexpr uint32_t T_U16 = 320;  // U^T fp16 pairs [128 x 32 columns]
 
 constexpr size_t kCpMat = 128 * 128;  // floats per CP matrix
 
@@ -68,12 +75,6 @@ struct ScanParams {
   float* cp;        // [B][H][nseg][3][128][128]: P_p, b_p, S_in(p)
 };
 
-// 64 state columns (one 64-column K block of the fp16 copy) -> shared memory.
-__device__ __forceinline__ void store_shalf(uint8_t* sa, int row, int hc, const float* s) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    *reinterpret_cast<uint4*>(sa + hc * 16384 + row_chunk(row, j)) = pack8_h(s + 8 * j);
-}
 __device__ __forceinline__ void tmem_ld64b(uint32_t taddr, float* v) {
   float a[32], b[32];
   tmem_ld32(taddr, a);
@@ -85,19 +86,38 @@ __device__ __forceinline__ void tmem_ld64b(uint32_t taddr, float* v) {
     v[32 + i] = b[i];
   }
 }
+// 64 fp32 columns -> TMEM (as raw bits)
+__device__ __forceinline__ void tmem_st64f(uint32_t taddr, const float* v) {
+  uint32_t a[32], b[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    a[i] = __float_as_uint(v[i]);
+    b[i] = __float_as_uint(v[32 + i]);
+  }
+  tmem_st32u(taddr, a);
+  tmem_st32u(taddr + 32, b);
+}
+// 64 fp32 values -> 32 fp16 pairs -> TMEM
+__device__ __forceinline__ void tmem_st64h(uint32_t taddr, const float* v) {
+  uint32_t a[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) a[i] = pack_h2(v[2 * i], v[2 * i + 1]);
+  tmem_st32u(taddr, a);
+}
 
 template <typename Tout, int MODE>
 __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [2] record staged
-  uint64_t* bar_u = full + 2;                                // D_U ready
-  uint64_t* bar_s = full + 3;                                // state updated
-  uint64_t* bar_o = full + 4;                                // [2] D_O[b] complete
-  uint64_t* do_free = full + 6;                              // [2] D_O[b] read by the output warps
-  uint64_t* bar_fin = full + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 80);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S_BAR + 84);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [2] record staged (bulk copy)
+  uint64_t* bar_u = full + 2;                                // [D_U | D_O] product done
+  uint64_t* bar_s = full + 3;                                // [D_O | S] product done
+  uint64_t* s16_ready = full + 4;                            // fp16 state copy written (256 arrivals)
+  uint64_t* u16_ready = full + 5;                            // U^T written, decay applied (256 arrivals)
+  uint64_t* do_free = full + 6;                              // D_O read by the output warps
+  uint64_t* bar_fin = full + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S_BAR + 68);
 
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
@@ -119,7 +139,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
     tmem_relinquish();
   }
   if (tid == 32) {
-    for (int i = 0; i < 9; ++i) mbar_init(&full[i], 1);
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(bar_u, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(s16_ready, kStateThreads);
+    mbar_init(u16_ready, kStateThreads);
+    mbar_init(do_free, 1);
+    mbar_init(bar_fin, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -133,10 +160,64 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
   const uint8_t* rec0 = p.records + ((size_t)(first_chunk + c_begin) * H + h) * kRecBytes;
   const size_t rec_stride = (size_t)H * kRecBytes;
 
-  bool ok = true;
-  if (warp < 8) {
-    // ======================== state warps: quadrant warp & 3, column half hc
+  if (warp == kIssuerWarp) {
+    // ======================== issuer: record staging + all MMAs (one lane)
+    if (lane == 0) {
+      int64_t last_load = -1;
+      bool ok = true;
+      if (ncs > 0) {
+        mbar_arrive_expect_tx(&full[0], kRecStage);
+        bulk_g2s(sm + S_STAGE0, rec0, kRecStage, &full[0]);
+        last_load = 0;
+      }
+      const uint32_t id1 = MODE == 0 ? idesc_f16(128, 128, false, true) : idesc_f16(128, 64, false, true);
+      const uint32_t id2 = MODE == 0 ? idesc_f16(128, 192, false, false) : idesc_f16(128, 128, false, false);
+      for (int64_t c = 0; c < ncs && ok; ++c) {
+        const int st = (int)(c & 1);
+        uint8_t* stage = sm + (st ? S_STAGE1 : S_STAGE0);
+        if (c + 1 < ncs) {
+          // stage st^1 held chunk c-1: free once that chunk's products are done
+          if (c >= 1) ok = wait_or_abort(bar_s, (uint32_t)((c - 1) & 1), abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&full[st ^ 1], kRecStage);
+          bulk_g2s(sm + (st ? S_STAGE0 : S_STAGE1), rec0 + (size_t)(c + 1) * rec_stride, kRecStage, &full[st ^ 1]);
+          last_load = c + 1;
+        }
+        ok = wait_or_abort(&full[st], (uint32_t)((c >> 1) & 1), abort_flag) &&
+             wait_or_abort(s16_ready, (uint32_t)(c & 1), abort_flag);
+        if (MODE == 0 && ok && c >= 1) ok = wait_or_abort(do_free, (uint32_t)((c - 1) & 1), abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint64_t db = smem_desc_sw128(smem_u32(stage + kRecWT), kRecQT - kRecWT, 1024);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ts(tmem + T_DU, tmem + T_S16 + 8 * ks, desc_add(db, ks * 2048), id1, ks > 0);
+          mma_commit(bar_u);
+        }
+        ok = wait_or_abort(u16_ready, (uint32_t)(c & 1), abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint64_t db = smem_desc_sw128(smem_u32(stage + (MODE == 0 ? kRecMM : kRecKT)), 16, 1024);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_f16_ts(tmem + (MODE == 0 ? T_DO : T_S), tmem + T_U16 + 8 * ks, desc_add(db, ks * 32), id2, true);
+          mma_commit(bar_s);
+        }
+      }
+      if (!ok || *abort_flag) {
+        *abort_flag = 1;
+        // let this thread's copies and MMAs drain (bounded) before TMEM is released
+        if (last_load >= 0) mbar_wait(&full[last_load & 1], (uint32_t)((last_load >> 1) & 1));
+        mma_commit(bar_fin);
+        mbar_wait(bar_fin, 0);
+      }
+    }
+  } else if (warp < 8) {
+    // ======================== state warps: TMEM lane quadrant warp & 3, column half hc
     const int hc = warp >> 2;
+    bool ok = true;
     {
       const float* init = nullptr;
       if (MODE == 0) init = seg == 0 ? (p.h0 ? p.h0 + soff : nullptr) : cpb + 2 * kCpMat;
@@ -147,37 +228,31 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
         if (MODE == 0) s[c] = init ? init[(size_t)col * 128 + row] : 0.f;
         else s[c] = (kind == 1 && col == row) ? 1.f : 0.f;
       }
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float t[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) t[j] = s[16 * q4 + j];
-        tmem_st16(tl + T_S + 64 * hc + 16 * q4, t);
-      }
+      tmem_st64h(tl + T_S16 + 32 * hc, s);
       tmem_wait_st();
-      store_shalf(sm + S_SA, row, hc, s);
+      tc_fence_before();
+      mbar_arrive(s16_ready);
+      if (ncs > 0) {
+        ok = wait_or_abort(&full[0], 0, abort_flag);
+        if (ok) {
+          const float* gc = reinterpret_cast<const float*>(sm + S_STAGE0 + kRecGC) + 64 * hc;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) s[c] *= gc[c];
+        }
+      }
+      tmem_st64f(tl + T_S + 64 * hc, s);
+      tmem_wait_st();
     }
-    if (tid == 0 && ncs > 0) {
-      mbar_arrive_expect_tx(&full[0], kRecStage);
-      bulk_g2s(sm + S_STAGE0, rec0, kRecStage, &full[0]);
-    }
-    // this thread's half of the U_hat^T row (chunks 4 hc .. 4 hc + 3), fetched one chunk ahead
-    uint4 uh[4];
+    // this thread's half of the U_hat^T row (r = 32 hc .. 32 hc + 31), fetched one chunk ahead
     const bool use_uh = MODE == 0 || kind == 0;
+    uint4 uh[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) uh[j] = make_uint4(0u, 0u, 0u, 0u);
     if (use_uh && ncs > 0) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) uh[j] = *reinterpret_cast<const uint4*>(rec0 + kRecUT + row_chunk(row, 4 * hc + j));
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    group_sync(1, kStateThreads);
-
-    for (int64_t c = 0; c < ncs; ++c) {
-      const int st = (int)(c & 1);
-      uint8_t* stage = sm + (st ? S_STAGE1 : S_STAGE0);
-      const uint32_t ph = (uint32_t)(c & 1);
+    for (int64_t c = 0; c < ncs && ok; ++c) {
       uint4 uh_next[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) uh_next[j] = make_uint4(0u, 0u, 0u, 0u);
@@ -186,145 +261,79 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
 #pragma unroll
         for (int j = 0; j < 4; ++j) uh_next[j] = *reinterpret_cast<const uint4*>(ut + row_chunk(row, 4 * hc + j));
       }
-      if (tid == 0) {
-        bool w = true;
-        // stage st^1 is free once chunk c-1's MMAs are done: prefetch chunk c+1 into it
-        if (c >= 1)
-          w = mbar_wait(MODE == 0 ? &bar_o[st ^ 1] : bar_s,
-                        MODE == 0 ? (uint32_t)(((c - 1) >> 1) & 1) : (uint32_t)((c - 1) & 1));
-        if (w && c + 1 < ncs) {
-          mbar_arrive_expect_tx(&full[st ^ 1], kRecStage);
-          bulk_g2s(sm + (st ? S_STAGE0 : S_STAGE1), rec0 + (size_t)(c + 1) * rec_stride, kRecStage, &full[st ^ 1]);
-        }
-        w = w && mbar_wait(&full[st], (uint32_t)((c >> 1) & 1));
-        // D_O[st] is free once the output warps have read chunk c-2
-        if (MODE == 0 && w && c >= 2) w = mbar_wait(&do_free[st], (uint32_t)(((c - 2) >> 1) & 1));
-        if (w) {
-          tc_fence_after();
-          const uint32_t id_u = idesc_f16(128, 64, false, true);
-          const uint64_t dsa = smem_desc_sw128(smem_u32(sm + S_SA), 16, 1024);
-          const uint64_t dwt = smem_desc_sw128(smem_u32(stage + kRecWT), 8192, 1024);
-#pragma unroll
-          for (int k0 = 0; k0 < 128; k0 += 16)
-            mma_f16(tmem + T_DU, desc_add(dsa, (k0 >> 6) * 16384 + (k0 & 63) * 2), desc_add(dwt, (k0 >> 3) * 1024),
-                    id_u, k0 > 0);
-          mma_commit(bar_u);
-          if (MODE == 0) {
-            const uint32_t id_o = idesc_f16(128, 64, false, false);
-            const uint64_t dqh = smem_desc_sw128(smem_u32(stage + kRecQH), 16, 1024);
-#pragma unroll
-            for (int k0 = 0; k0 < 128; k0 += 16) {
-              const uint32_t off = (k0 & 63) * 2;
-              mma_f16(tmem + T_DO + 64 * st, desc_add(dsa, (k0 >> 6) * 16384 + off), desc_add(dqh, (k0 >> 6) * 8192 + off),
-                      id_o, k0 > 0);
-            }
-          }
-        } else {
-          *abort_flag = 1;
-        }
-      }
-      ok = group_and(1, kStateThreads, !*abort_flag);
+      // U^T = U_hat^T - D_U on this thread's 32 columns
+      ok = wait_or_abort(bar_u, (uint32_t)(c & 1), abort_flag);
       if (!ok) break;
-      // while the MMAs run: this thread's 64 state columns <- Diag(e^{G_C}) scaling, in TMEM
-      {
-        const float* gc = reinterpret_cast<const float*>(stage + kRecGC) + 64 * hc;
-        float t[64];
-        tmem_ld64b(tl + T_S + 64 * hc, t);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float u[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) u[j] = t[16 * q4 + j] * gc[16 * q4 + j];
-          tmem_st16(tl + T_S + 64 * hc + 16 * q4, u);
-        }
-        tmem_wait_st();
-      }
-      ok = group_and(1, kStateThreads, mbar_wait(bar_u, ph));
-      if (!ok) { if (tid == 0) *abort_flag = 1; break; }
       tc_fence_after();
       {
         float u[32];
         tmem_ld32(tl + T_DU + 32 * hc, u);
         tmem_wait_ld();
+        uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t w4[4] = {uh[j].x, uh[j].y, uh[j].z, uh[j].w};
-          float v[8];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 a = unpack_h2(w4[e]);
-            v[2 * e] = a.x - u[8 * j + 2 * e];
-            v[2 * e + 1] = a.y - u[8 * j + 2 * e + 1];
+            pk[4 * j + e] = pack_h2(a.x - u[8 * j + 2 * e], a.y - u[8 * j + 2 * e + 1]);
           }
-          *reinterpret_cast<uint4*>(sm + S_UA + row_chunk(row, 4 * hc + j)) = pack8_h(v);
         }
+        tmem_st16u(tl + T_U16 + 16 * hc, pk);
+        tmem_wait_st();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      group_sync(1, kStateThreads);
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t id_s = idesc_f16(128, 128, false, true);
-        const uint64_t dua = smem_desc_sw128(smem_u32(sm + S_UA), 16, 1024);
-        const uint64_t dkb = smem_desc_sw128(smem_u32(stage + kRecKB), 8192, 1024);
-#pragma unroll
-        for (int k0 = 0; k0 < 64; k0 += 16)
-          mma_f16(tmem + T_S, desc_add(dua, k0 * 2), desc_add(dkb, (k0 >> 3) * 1024), id_s, true);
-        mma_commit(bar_s);
-        if (MODE == 0) {
-          const uint32_t id_o = idesc_f16(128, 64, false, false);
-          const uint64_t dmm = smem_desc_sw128(smem_u32(stage + kRecMM), 16, 1024);
-#pragma unroll
-          for (int k0 = 0; k0 < 64; k0 += 16)
-            mma_f16(tmem + T_DO + 64 * st, desc_add(dua, k0 * 2), desc_add(dmm, k0 * 2), id_o, true);
-          mma_commit(&bar_o[st]);
-        }
-      }
-      ok = group_and(1, kStateThreads, mbar_wait(bar_s, ph));
-      if (!ok) { if (tid == 0) *abort_flag = 1; break; }
+      mbar_arrive(u16_ready);
+      // updated state -> fp16 copy (next chunk's A operand), then the next chunk's decay in place
+      ok = wait_or_abort(bar_s, (uint32_t)(c & 1), abort_flag);
+      if (!ok) break;
       tc_fence_after();
-      {
+      if (c + 1 < ncs) {
         float s[64];
         tmem_ld64b(tl + T_S + 64 * hc, s);
-        store_shalf(sm + S_SA, row, hc, s);
+        tmem_st64h(tl + T_S16 + 32 * hc, s);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(s16_ready);
+        const int st1 = (int)((c + 1) & 1);
+        ok = wait_or_abort(&full[st1], (uint32_t)(((c + 1) >> 1) & 1), abort_flag);
+        if (!ok) break;
+        const float* gc = reinterpret_cast<const float*>(sm + (st1 ? S_STAGE1 : S_STAGE0) + kRecGC) + 64 * hc;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) s[j] *= gc[j];
+        tmem_st64f(tl + T_S + 64 * hc, s);
+        tmem_wait_st();
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) uh[j] = uh_next[j];
-      fence_proxy_async_smem();
-      tc_fence_before();
-      group_sync(1, kStateThreads);
     }
     // final state of this (sequence, head, segment)
     float* dst = nullptr;
     if (MODE == 0 && seg == p_last) dst = p.hT ? p.hT + soff : nullptr;
     if (MODE == 1) dst = cpb + (kind == 1 ? 0 : kCpMat);
-    if (ok && dst != nullptr) {
+    if (ok && !*abort_flag && dst != nullptr) {
       tc_fence_after();
       float s[64];
       tmem_ld64b(tl + T_S + 64 * hc, s);
 #pragma unroll
       for (int c = 0; c < 64; ++c) dst[(size_t)(64 * hc + c) * 128 + row] = s[c];
     }
+    if (!ok) *abort_flag = 1;
   } else if (MODE == 0) {
     // ======================== output warps: D_O -> staging -> epilogue -> global
     float* ost = reinterpret_cast<float*>(sm + S_OUT);
     Tout* out = static_cast<Tout*>(p.out);
     const int ow = warp - 8;
+    bool ok = true;
     for (int64_t c = 0; c < ncs; ++c) {
-      const int st = (int)(c & 1);
-      bool w = false;
-      for (int spin = 0; spin < 64 && !w; ++spin) {
-        if (*abort_flag) break;
-        w = mbar_wait(&bar_o[st], (uint32_t)((c >> 1) & 1), 1u << 20);
-      }
-      ok = group_and(2, 128, w);
+      ok = group_and(2, 128, wait_or_abort(bar_s, (uint32_t)(c & 1), abort_flag));
       if (!ok) break;
       tc_fence_after();
       float o[64];
-      tmem_ld64b(tl + T_DO + 64 * st, o);
+      tmem_ld64b(tl + T_DO, o);
       tc_fence_before();
       group_sync(2, 128);
-      if (ow == 0 && lane == 0) mbar_arrive(&do_free[st]);
+      if (ow == 0 && lane == 0) mbar_arrive(do_free);
 #pragma unroll
       for (int r = 0; r < 64; ++r) ost[r * 128 + row] = o[r];
       group_sync(2, 128);
@@ -364,14 +373,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
     if (!ok) *abort_flag = 1;
   }
 
-  __syncthreads();
-  if (*abort_flag && tid == 0) {
-    atomicOr(p.err, KDA_DEVERR_WAIT_TIMEOUT);
-    mma_commit(bar_fin);  // let this thread's MMAs drain (bounded) before TMEM is released
-    mbar_wait(bar_fin, 0);
-  }
   tc_fence_before();
   __syncthreads();
+  if (tid == 0 && *abort_flag) atomicOr(p.err, KDA_DEVERR_WAIT_TIMEOUT);
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
