@@ -1,4 +1,5 @@
-// KDA chunked prefill on the tcgen05 tensor cores (bf16 inputs, dk = dv = 128).
+// KDA chunked prefill on the tcgen05 tensor cores (bf16 inputs, dk = dv = 128): the
+// chunk-parallel part.
 //
 // Kimi K3: Open Frontier Intelligence (kimi-k3-paper.pages.dev), section 2.5 / Eq. 4:
 // per 64-token chunk a parallel intra-chunk part and a serial inter-chunk state pass.
@@ -8,31 +9,30 @@
 //   U = U_hat - W S0,  O = Q_hat S0 + M U,  S_C = Diag(e^{G_C}) S0 + K_bar^T U
 // Section 3.2 / Eq. 5 (g > -5) bounds every reference-scaled factor used below by e^{+-80}.
 //
-//  kda_tc_chunk_prep  (persistent, one CTA per SM, loops over (chunk, head) tasks)
-//    - TMA (128-byte swizzle) brings the raw q, k, v, g tiles of the NEXT task into a second
-//      buffer while the current task computes;
-//    - cumulative log-decay G in fp32 (in place), per-channel decay constants;
-//    - A and M as one split-tf32 product (x = x_hi + x_lo, three tf32 MMAs per K step, fp32
-//      accumulation), M=128 (64 key rows + 64 query rows) x N=96 (two diagonal 32x32 blocks with
-//      centred references 15 and 47, plus the off-diagonal block with reference 47), in four
-//      32-channel passes; the same passes emit Q_hat and K_bar (to the record) and K_hat;
+//  kda_tc_chunk_prep (persistent, two CTAs per SM, each looping over (chunk, head) tasks)
+//    warp 8 stages the raw q, k, v tiles by TMA (128-byte swizzle; q of the next task as soon as
+//      the current one has been read, k and v once its last MMAs are done) and beta by plain
+//      loads, and issues every MMA;
+//    warps 0-7, per task:
+//    - four 32-channel passes; thread = (channel pair, 4 rows): the cumulative log-decay is a
+//      running sum over the thread's rows plus the sums of the row groups above it (exchanged in
+//      shared memory); g is read straight from global memory one pass ahead;
+//    - each pass writes the reference-scaled keys/queries as a three-way bf16 split
+//      (x = hi + lo, hi = x with its low 16 bits cleared, lo = x - hi rounded): A and M come from
+//      X_h [Y_h ; Y_l]^T (N = 192) + X_l Y_h^T (N = 96), fp32 accumulation, M = 128 rows (64 key
+//      rows for A, 64 query rows for M) x 96 columns (two diagonal 32 x 32 blocks with centred
+//      references 15 and 47, plus the off-diagonal block with reference 47).  Pass p fills half
+//      (p & 1) of every 128-byte operand row, so it only waits for the MMAs of pass p - 2;
+//    - the passes also emit Q_hat^T and K_bar^T (channel-major) and e^{G_C} into the record, and
+//      K_hat and V (fp16) in place of the raw tiles;
 //    - T = (I + A)^-1 Diag(beta) by blocked (16 x 16) forward substitution in fp32;
-//    - fp16 MMAs W^T = K_hat^T T^T and U_hat^T = V^T T^T (M=128, N=64, K=64);
-//    - one 74 KB record per (chunk, head), laid out as the scan kernel's shared-memory operands.
+//    - fp16 MMAs W^T = K_hat^T T^T and U_hat^T = V^T T^T (M = 128, N = 64, K = 64), then W^T, M
+//      and U_hat^T into the record.
 //
-//  kda_tc_chunk_scan  (grid = sequences x heads; serial over the chunks of a sequence)
-//    - warps 0-3 run the state chain: S^T (dv x dk, fp32) lives in TMEM for the whole sequence,
-//      an fp16 copy in shared memory is the A operand of D_U = S^T W^T and D_O = S^T Q_hat^T;
-//      U^T = U_hat^T - D_U; S^T = S^T Diag(e^{G_C}) + U^T K_bar; D_O += U^T M^T;
-//    - warps 4-7 drain the read-out accumulator (double-buffered in TMEM) through a staging
-//      buffer and run the optional RMSNorm + sigmoid-gate epilogue, off the serial path;
-//    - record operands are double-buffered with bulk copies.
-//
-// Precision: bf16 operands cannot meet the parity bound on these workloads (see the design
-// notes); fp16 has the bf16 MMA rate with 3 more significand bits, and every fp16 operand here is
-// bounded (decayed keys/queries <= 1, values and states well inside the fp16 range).  The
-// reference-scaled A/M operands need fp32 range; plain tf32 is enough for A but not for M (it
-// feeds the read-out directly), so the A/M product is split-tf32.  Accumulation is fp32.
+// Precision: bf16 operands cannot meet the parity bound on these workloads; fp16 has the bf16
+// MMA rate with 3 more significand bits, and every fp16 operand here is bounded (decayed
+// keys/queries <= 1, values well inside the fp16 range).  The reference-scaled A/M operands
+// need fp32 range and ~16 significant bits (M feeds the read-out directly): hence the split.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -49,11 +49,9 @@ using namespace tcx;
 constexpr int kPrepThreads = 288;   // warps 0-7 compute, warp 8 stages inputs and issues the MMAs
 constexpr int kCompute = 256;
 constexpr int kIssuer = 8;
-// raw stage: k | q | v (bf16 token-row blocks) | g (fp32, four 32-channel blocks)
-constexpr uint32_t R_K = 0, R_Q = 16384, R_V = 32768, R_G = 49152, R_BYTES = 81920;
-constexpr uint32_t P_RAW0 = 0;
-constexpr uint32_t P_RAW1 = R_BYTES;
-constexpr uint32_t P_OPS = 2 * R_BYTES;  // 56 KB: one 64-channel K block of split-bf16 operands
+// raw tiles: k | q | v (bf16 token-row blocks, two 64-channel blocks each)
+constexpr uint32_t R_K = 0, R_Q = 16384, R_V = 32768, R_BYTES = 49152;
+constexpr uint32_t P_OPS = R_BYTES;      // 56 KB: one 64-channel K block of split-bf16 operands
 constexpr uint32_t O_XH = 0, O_XL = 16384, O_YH = 32768, O_YL = 45056, O_BYTES = 57344;
 // after the A/M product the operand region holds the solve:
 constexpr uint32_t O_SA = 0;             // fp32 A [64][65]
@@ -61,15 +59,16 @@ constexpr uint32_t O_SX = 16640;         // fp32 X = (I + A)^-1 [64][65]
 constexpr uint32_t O_SY = 33280;         // fp32 scratch, three 16 x 16 blocks
 constexpr uint32_t O_TT = 37888;         // fp16 T [64 r][64 s] row format (1024-aligned)
 constexpr uint32_t P_MISC = P_OPS + O_BYTES;
-constexpr uint32_t M_BETA = 0;           // fp32 [2 stages][64]
-constexpr uint32_t M_TOT = 512;          // fp32 [2][16 row groups][32 channels]: per-group decay sums
+constexpr uint32_t M_BETA = 0;           // fp32 [2 tasks][64]
+constexpr uint32_t M_TOT = 512;          // float2 [2][16 row groups][16 channel pairs]: group decay sums
 constexpr uint32_t M_BAR = 4608;         // barriers, tmem slot, abort flag
 constexpr uint32_t M_END = 4736;
 constexpr uint32_t kPrepSmem = P_MISC + M_END + 1024;
+constexpr uint32_t kPrepTmemCols = 256;
 
 constexpr uint32_t T_AM = 0;    // TMEM: [X_h Y_h + X_l Y_h | X_h Y_l] [128 x 192]
-constexpr uint32_t T_W = 192;   // W^T [128 x 64]
-constexpr uint32_t T_U = 256;   // U_hat^T [128 x 64]
+constexpr uint32_t T_W = 0;     // W^T [128 x 64]      } reuse the A/M columns once they are read
+constexpr uint32_t T_U = 64;    // U_hat^T [128 x 64]  }
 
 // x (2 floats) -> bf16 hi (x with its low 16 bits cleared, exact in bf16) and lo = x - hi
 // rounded to bf16, each as a packed pair.
@@ -81,7 +80,7 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
 }
 
 struct PrepMaps {
-  CUtensorMap k, q, v, g;
+  CUtensorMap k, q, v;
 };
 
 // Next valid task index >= t (tasks: chunk-major, head-minor), or -1.
@@ -98,22 +97,30 @@ __device__ __forceinline__ int64_t next_task(int64_t t, int64_t ntask, int64_t s
   return -1;
 }
 
-// Issuer warp: raw q/k/v/g tiles of a task by TMA, beta by plain loads into shared memory.
-// full[] expects two arrivals: the transaction-counted one and the beta one.
-__device__ __forceinline__ void stage_task(const PrepMaps& m, const float* beta, uint8_t* raw, float* sbeta,
-                                           uint64_t* bar, int h, int64_t t0, int n, int H, int lane) {
-  if (lane == 0) {
-    mbar_arrive_expect_tx(bar, R_BYTES);
-    const int y = (int)t0;
+// g of this thread's 4 rows x 2 channels for one pass (rows past the sequence end read as 0).
+__device__ __forceinline__ void load_g(float2 (&gv)[4], const float* __restrict__ g, int64_t t0, int n, int H, int h,
+                                       int c, int rg) {
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      tma_load_2d(raw + R_K + 8192 * b, &m.k, h * 128 + 64 * b, y, bar);
-      tma_load_2d(raw + R_Q + 8192 * b, &m.q, h * 128 + 64 * b, y, bar);
-      tma_load_2d(raw + R_V + 8192 * b, &m.v, h * 128 + 64 * b, y, bar);
-    }
-#pragma unroll
-    for (int b = 0; b < 4; ++b) tma_load_2d(raw + R_G + 8192 * b, &m.g, h * 128 + 32 * b, y, bar);
+  for (int i = 0; i < 4; ++i) {
+    const int r = 4 * rg + i;
+    gv[i] = r < n ? __ldg(reinterpret_cast<const float2*>(g + ((size_t)(t0 + r) * H + h) * 128 + c))
+                  : make_float2(0.f, 0.f);
   }
+}
+
+// Raw q, k, v tiles of a task (one transaction-counted arrival on `bar`).
+__device__ __forceinline__ void tma_qkv(const PrepMaps& m, uint8_t* raw, uint64_t* bar, int h, int64_t t0) {
+  mbar_arrive_expect_tx(bar, R_BYTES);
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    tma_load_2d(raw + R_K + 8192 * b, &m.k, h * 128 + 64 * b, (int)t0, bar);
+    tma_load_2d(raw + R_Q + 8192 * b, &m.q, h * 128 + 64 * b, (int)t0, bar);
+    tma_load_2d(raw + R_V + 8192 * b, &m.v, h * 128 + 64 * b, (int)t0, bar);
+  }
+}
+// beta of a task into shared memory (whole issuer warp), then one arrival on `bar`.
+__device__ __forceinline__ void stage_beta(const float* beta, float* sbeta, uint64_t* bar, int h, int64_t t0, int n,
+                                           int H, int lane) {
   const float b0 = lane < n ? beta[(size_t)(t0 + lane) * H + h] : 0.f;
   const float b1 = lane + 32 < n ? beta[(size_t)(t0 + lane + 32) * H + h] : 0.f;
   sbeta[lane] = b0;
@@ -122,22 +129,23 @@ __device__ __forceinline__ void stage_task(const PrepMaps& m, const float* beta,
   if (lane == 0) mbar_arrive(bar);
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 1)
-kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict__ beta,
+__global__ void __launch_bounds__(kPrepThreads, 2)
+kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict__ g, const float* __restrict__ beta,
                   const int32_t* __restrict__ plan, const int32_t* __restrict__ cu, int B, int64_t T, int H,
                   int64_t ntask, uint8_t* __restrict__ records, unsigned int* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* raw = sm;
   uint8_t* ops = sm + P_OPS;
   uint8_t* misc = sm + P_MISC;
   float* sBetaAll = reinterpret_cast<float*>(misc + M_BETA);
-  float2* sTot = reinterpret_cast<float2*>(misc + M_TOT);      // [2][16][16] channel pairs
-  uint64_t* full = reinterpret_cast<uint64_t*>(misc + M_BAR);  // [2] raw stage landed (+ beta)
-  uint64_t* ops_ready = full + 2;                              // [2] pass operands written (256 arrivals)
-  uint64_t* bar_ops = full + 4;                                // [2] pass MMAs done
-  uint64_t* tt_ready = full + 6;                               // T written (256 arrivals)
-  uint64_t* bar_wu = full + 7;                                 // W / U_hat MMAs done
-  uint64_t* bar_fin = full + 8;
+  float2* sTot = reinterpret_cast<float2*>(misc + M_TOT);      // [2][16][16]
+  uint64_t* full = reinterpret_cast<uint64_t*>(misc + M_BAR);  // raw tiles landed + beta staged
+  uint64_t* ops_ready = full + 1;                              // [2] pass operands written (256 arrivals)
+  uint64_t* bar_ops = full + 3;                                // [2] pass MMAs done
+  uint64_t* tt_ready = full + 5;                               // T written, A/M read (256 arrivals)
+  uint64_t* bar_wu = full + 6;                                 // W / U_hat MMAs done
+  uint64_t* bar_fin = full + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + M_BAR + 80);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + M_BAR + 84);
 
@@ -149,12 +157,11 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
   if (task < 0) return;
 
   if (warp == 0) {
-    tmem_alloc(tmem_slot, 512);
+    tmem_alloc(tmem_slot, kPrepTmemCols);
     tmem_relinquish();
   }
   if (tid == 32) {
-    mbar_init(&full[0], 2);
-    mbar_init(&full[1], 2);
+    mbar_init(full, 2);
     mbar_init(&ops_ready[0], kCompute);
     mbar_init(&ops_ready[1], kCompute);
     mbar_init(&bar_ops[0], 1);
@@ -172,9 +179,13 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
 
   if (warp == kIssuer) {
     // ======================== issuer warp
-    int64_t last_stage_task = 0;  // tasks staged so far (for the drain on abort)
-    stage_task(maps, beta, sm + P_RAW0, sBetaAll, &full[0], h, t0, n, H, lane);
-    last_stage_task = 1;
+    // full: the raw tiles of a task (one transaction-counted arrival) and its beta (one arrival).
+    // The tiles of the next task are loaded once the current task's last MMAs have read them;
+    // the other CTA on the SM covers that latency.
+    bool load_pending = false;  // a tile load has been issued and not yet waited for by the compute warps
+    if (lane == 0) tma_qkv(maps, raw, full, h, t0);
+    stage_beta(beta, sBetaAll, full, h, t0, n, H, lane);
+    load_pending = true;
     bool ok = true;
     const uint32_t id_hh = idesc_bf16_f32(128, 192, false, false);  // X_h [Y_h ; Y_l]^T
     const uint32_t id_lh = idesc_bf16_f32(128, 96, false, false);   // X_l Y_h^T
@@ -183,29 +194,18 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
     const uint64_t dxl = smem_desc_sw128(smem_u32(ops + O_XL), 16, 1024);
     const uint64_t dyh = smem_desc_sw128(smem_u32(ops + O_YH), 16, 1024);
     const uint64_t dtt = smem_desc_sw128(smem_u32(ops + O_TT), 16, 1024);
+    const uint64_t dkh = smem_desc_sw128(smem_u32(raw + R_K), 8192, 1024);
+    const uint64_t dvv = smem_desc_sw128(smem_u32(raw + R_V), 8192, 1024);
     uint32_t it = 0;
     while (task >= 0 && ok) {
-      const int st = (int)(it & 1);
-      uint8_t* raw = sm + (st ? P_RAW1 : P_RAW0);
       int nh = 0, nn = 0;
       int64_t nt0 = 0, nchunk = 0;
       const int64_t ntask_idx = next_task(task + stride, ntask, stride, plan, cu, B, T, H, nh, nt0, nn, nchunk);
-      if (ntask_idx >= 0) {
-        // the other raw stage is free once the previous task's W / U_hat MMAs are done
-        if (it >= 1) {
-          bool w = true;
-          if (lane == 0) w = wait_or_abort(bar_wu, (it - 1) & 1, abort_flag);
-          ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-          if (!ok) break;
-        }
-        stage_task(maps, beta, sm + (st ? P_RAW0 : P_RAW1), sBetaAll + 64 * (st ^ 1), &full[st ^ 1], nh, nt0, nn, H,
-                   lane);
-        ++last_stage_task;
-      }
       if (lane == 0) {
         for (int pass = 0; pass < 4 && ok; ++pass) {
           ok = wait_or_abort(&ops_ready[pass & 1], (uint32_t)((pass >> 1) & 1), abort_flag);
           if (!ok) break;
+          if (pass == 0) load_pending = false;  // the compute warps have consumed this task's tiles
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
@@ -215,17 +215,28 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
           }
           mma_commit(&bar_ops[pass & 1]);
         }
-        if (ok) ok = wait_or_abort(tt_ready, it & 1, abort_flag);
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      if (ntask_idx >= 0) stage_beta(beta, sBetaAll + 64 * ((it + 1) & 1), full, nh, nt0, nn, H, lane);
+      if (lane == 0) {
+        ok = wait_or_abort(tt_ready, it & 1, abort_flag);
         if (ok) {
           tc_fence_after();
-          const uint64_t dkh = smem_desc_sw128(smem_u32(raw + R_K), 8192, 1024);
-          const uint64_t dvv = smem_desc_sw128(smem_u32(raw + R_V), 8192, 1024);
 #pragma unroll
           for (int k0 = 0; k0 < 64; k0 += 16) {
             mma_f16(tmem + T_W, desc_add(dkh, (k0 >> 3) * 1024), desc_add(dtt, k0 * 2), id_wu, k0 > 0);
             mma_f16(tmem + T_U, desc_add(dvv, (k0 >> 3) * 1024), desc_add(dtt, k0 * 2), id_wu, k0 > 0);
           }
           mma_commit(bar_wu);
+          if (ntask_idx >= 0) {
+            // the next task's tiles once these MMAs have read the current k and v
+            ok = wait_or_abort(bar_wu, it & 1, abort_flag);
+            if (ok) {
+              tma_qkv(maps, raw, full, nh, nt0);
+              load_pending = true;
+            }
+          }
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -236,8 +247,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
     if (lane == 0 && (!ok || *abort_flag)) {
       *abort_flag = 1;
       // let staged copies and issued MMAs drain (bounded) before TMEM is released
-      const int64_t lt = last_stage_task - 1;
-      mbar_wait(&full[lt & 1], (uint32_t)((lt >> 1) & 1));
+      if (load_pending) mbar_wait(full, it & 1);
       mma_commit(bar_fin);
       mbar_wait(bar_fin, 0);
     }
@@ -247,37 +257,32 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
     const int cl = 2 * cp;
     bool ok = true;
     uint32_t it = 0;
+    float2 gcur[4];
+    load_g(gcur, g, t0, n, H, h, cl, rg);
     while (task >= 0 && ok) {
-      const int st = (int)(it & 1);
-      uint8_t* raw = sm + (st ? P_RAW1 : P_RAW0);
-      const float* sBeta = sBetaAll + 64 * st;
+      const float* sBeta = sBetaAll + 64 * (it & 1);
       uint8_t* rec = records + ((size_t)chunk * H + h) * kRecBytes;
       int nh = 0, nn = 0;
       int64_t nt0 = 0, nchunk = 0;
       const int64_t ntask_idx = next_task(task + stride, ntask, stride, plan, cu, B, T, H, nh, nt0, nn, nchunk);
       // every break decision of the compute warps is made together (named barriers follow)
-      ok = group_and(1, kCompute, wait_or_abort(&full[st], (it >> 1) & 1, abort_flag));
+      ok = group_and(1, kCompute, wait_or_abort(full, it & 1, abort_flag));
       if (!ok) break;
 
-      // ---- four 32-channel passes.  Pass p fills half (p & 1) of every 128-byte operand row, so
-      // it only has to wait for the MMAs of pass p - 2.  Per pass: cumulative log-decay of this
-      // thread's 4 rows x 2 channels, the group sums exchanged through shared memory, then the
-      // reference-scaled operands, the record's Q_hat^T / K_bar^T, K_hat (in place of k) and V (fp16).
+      // ---- four 32-channel passes
 #pragma unroll 1
       for (int pass = 0; pass < 4; ++pass) {
         const int c = 32 * pass + cl;  // first of this thread's two channels
+        float2 gnext[4];
+        if (pass < 3) load_g(gnext, g, t0, n, H, h, c + 32, rg);
+        else if (ntask_idx >= 0) load_g(gnext, g, nt0, nn, H, nh, cl, rg);
         float2 L[4];
         {
           float2 run = make_float2(0.f, 0.f);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int r = 4 * rg + i;
-            float2 gv = make_float2(0.f, 0.f);
-            if (r < n)
-              gv = *reinterpret_cast<const float2*>(raw + R_G + 8192u * pass + r * 128 +
-                                                    ((((uint32_t)cl >> 2) ^ ((uint32_t)r & 7u)) << 4) + (cl & 3) * 4);
-            run.x += gv.x;
-            run.y += gv.y;
+            run.x += gcur[i].x;
+            run.y += gcur[i].y;
             L[i] = run;
           }
           sTot[(pass & 1) * 256 + rg * 16 + cp] = run;
@@ -287,13 +292,13 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
         if (!ok) break;
         float2 off = make_float2(0.f, 0.f), cum = make_float2(0.f, 0.f), G15, G47, G63;
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
-          const float2 t = sTot[(pass & 1) * 256 + g * 16 + cp];
-          if (g == rg) off = cum;
+        for (int gi = 0; gi < 16; ++gi) {
+          const float2 t = sTot[(pass & 1) * 256 + gi * 16 + cp];
+          if (gi == rg) off = cum;
           cum.x += t.x;
           cum.y += t.y;
-          if (g == 3) G15 = cum;
-          if (g == 11) G47 = cum;
+          if (gi == 3) G15 = cum;
+          if (gi == 11) G47 = cum;
         }
         G63 = cum;
         const bool first = rg < 8;  // rows < 32: reference row 15, else 47
@@ -309,8 +314,8 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
           const int r = 4 * rg + i;
           const bool valid = r < n;
           const float G0 = off.x + L[i].x, G1 = off.y + L[i].y;
-          const uint32_t toff = (uint32_t)(c >> 6) * 8192u + (uint32_t)r * 128u +
-                                ((((kbyte >> 4) ^ (uint32_t)r) & 7u) << 4) + (kbyte & 15u);
+          const uint32_t ob = (uint32_t)r * 128u + ((((kbyte >> 4) ^ (uint32_t)r) & 7u) << 4) + (kbyte & 15u);
+          const uint32_t toff = (uint32_t)(c >> 6) * 8192u + ob;
           uint32_t* pk = reinterpret_cast<uint32_t*>(raw + R_K + toff);
           uint32_t* pq = reinterpret_cast<uint32_t*>(raw + R_Q + toff);
           uint32_t* pv = reinterpret_cast<uint32_t*>(raw + R_V + toff);
@@ -323,7 +328,6 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
           const float e10 = __expf(G0 - R.x), e11 = __expf(G1 - R.y);
           const float e20 = __expf(R.x - G0), e21 = __expf(R.y - G1);
           uint32_t hi, lo;
-          const uint32_t ob = (uint32_t)r * 128u + ((((kbyte >> 4) ^ (uint32_t)r) & 7u) << 4) + (kbyte & 15u);
           const uint32_t ob64 = ob + 64u * 128u;  // row 64 + r (same swizzle phase)
           split_bf16x2(k2.x * e10, k2.y * e11, hi, lo);
           *reinterpret_cast<uint32_t*>(ops + O_XH + ob) = hi;
@@ -372,6 +376,8 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
         }
         fence_proxy_async_smem();
         mbar_arrive(&ops_ready[pass & 1]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) gcur[i] = gnext[i];
       }
       if (!ok) break;
       ok = group_and(1, kCompute, wait_or_abort(&bar_ops[1], 1, abort_flag));  // pass 3 (and all before) done
@@ -386,34 +392,36 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
         const int q = warp & 3, hh = warp >> 2;
         const int lrow = 32 * q + lane;
         const int r = lrow & 63;
-        float val[32];
-        if ((q & 1) == 0 && hh == 1) {
+        const bool zero_half = (q & 1) == 0 && hh == 1;  // upper off-diagonal block
+        const uint32_t c1 = (q & 1) == 0 ? 0u : (hh == 0 ? 64u : 32u);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) val[j] = 0.f;  // upper off-diagonal block
-        } else {
-          const uint32_t c1 = (q & 1) == 0 ? 0u : (hh == 0 ? 64u : 32u);
-          float a1[32], a2[32];
-          tmem_ld32(tmem_lane(tmem + T_AM, warp) + c1, a1);
-          tmem_ld32(tmem_lane(tmem + T_AM, warp) + c1 + 96u, a2);
-          tmem_wait_ld();
+        for (int part = 0; part < 2; ++part) {
+          float val[16];
+          if (zero_half) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) val[j] = a1[j] + a2[j];
-        }
-        if (lrow < 64) {
-          const float br = sBeta[r];
+            for (int j = 0; j < 16; ++j) val[j] = 0.f;
+          } else {
+            float a1[16], a2[16];
+            tmem_ld16(tmem_lane(tmem + T_AM, warp) + c1 + 16 * part, a1);
+            tmem_ld16(tmem_lane(tmem + T_AM, warp) + c1 + 96u + 16 * part, a2);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int s_ = 32 * hh + j;
-            sA[r * 65 + s_] = (s_ < r) ? br * val[j] : 0.f;  // select, not mask-multiply
+            for (int j = 0; j < 16; ++j) val[j] = a1[j] + a2[j];
           }
-        } else {
+          const int s0 = 32 * hh + 16 * part;
+          if (lrow < 64) {
+            const float br = sBeta[r];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) val[j] = (32 * hh + j <= r) ? val[j] : 0.f;
+            for (int j = 0; j < 16; ++j) sA[r * 65 + s0 + j] = (s0 + j < r) ? br * val[j] : 0.f;  // select, not mask-multiply
+          } else {
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-            *reinterpret_cast<uint4*>(rec + kRecMM + row_chunk(r, 4 * hh + jj)) = pack8_h(val + 8 * jj);
+            for (int j = 0; j < 16; ++j) val[j] = (s0 + j <= r) ? val[j] : 0.f;
+            *reinterpret_cast<uint4*>(rec + kRecMM + row_chunk(r, s0 >> 3)) = pack8_h(val);
+            *reinterpret_cast<uint4*>(rec + kRecMM + row_chunk(r, (s0 >> 3) + 1)) = pack8_h(val + 8);
+          }
         }
       }
+      tc_fence_before();
       group_sync(1, kCompute);
 
       // ---- T = (I + A)^-1 Diag(beta), blocked 16 x 16 forward substitution (fp32)
@@ -490,9 +498,17 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
       tc_fence_after();
       {
         const int row = (warp & 3) * 32 + lane;  // dk row (W^T, warps 0-3) or dv row (U_hat^T, warps 4-7)
-        float vrow[64];
-        tmem_ld64(tmem_lane(tmem + (warp < 4 ? T_W : T_U), warp), vrow);
-        store_row64(rec + (warp < 4 ? kRecWT : kRecUT), row, vrow);
+        const uint32_t ta = tmem_lane(tmem + (warp < 4 ? T_W : T_U), warp);
+        uint8_t* dst = rec + (warp < 4 ? kRecWT : kRecUT);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          float v[32];
+          tmem_ld32(ta + 32 * part, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(dst + row_chunk(row, 4 * part + j)) = pack8_h(v + 8 * j);
+        }
       }
       tc_fence_before();
       task = ntask_idx;
@@ -506,7 +522,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
   __syncthreads();
   if (tid == 0 && *abort_flag) atomicOr(err, KDA_DEVERR_WAIT_TIMEOUT);
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, 512);
+  if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
 // ----------------------------------------------------------------- host side
@@ -567,14 +583,14 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
     PrepMaps maps;
     if (!make_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T_tot, a.H, 64) ||
         !make_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T_tot, a.H, 64) ||
-        !make_map(&maps.v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T_tot, a.H, 64) ||
-        !make_map(&maps.g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T_tot, a.H, 32))
+        !make_map(&maps.v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T_tot, a.H, 64))
       return cudaErrorInvalidValue;
     const int64_t ntask = nchunks * a.H;
-    const int grid = (int)(ntask < sm_count[dev] ? ntask : sm_count[dev]);
+    const int64_t slots = 2 * (int64_t)sm_count[dev];  // two CTAs per SM
+    const int grid = (int)(ntask < slots ? ntask : slots);
     TraceScope ts("kda_tc_chunk_prep", st);
-    kda_tc_chunk_prep<<<grid, kPrepThreads, kPrepSmem, st>>>(maps, a.beta, plan, a.cu_seqlens, a.B, a.T, a.H, ntask,
-                                                            records, a.err);
+    kda_tc_chunk_prep<<<grid, kPrepThreads, kPrepSmem, st>>>(maps, a.g, a.beta, plan, a.cu_seqlens, a.B, a.T, a.H,
+                                                            ntask, records, a.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

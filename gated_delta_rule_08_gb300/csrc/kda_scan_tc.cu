@@ -40,10 +40,9 @@ using namespace tcx;
 constexpr int kScanThreads = 416;
 constexpr int kStateThreads = 256;               // warps 0-7
 constexpr int kIssuerWarp = 12;
+constexpr int kStages = 3;                       // records staged up to two chunks ahead
 constexpr uint32_t kStage = 59392;               // staged record bytes, 1024-aligned
-constexpr uint32_t S_STAGE0 = 0;
-constexpr uint32_t S_STAGE1 = kStage;
-constexpr uint32_t S_OUT = 2 * kStage;           // fp32 read-out staging [64 r][128 dv]
+constexpr uint32_t S_OUT = kStages * kStage;     // fp32 read-out staging [64 r][128 dv]
 constexpr uint32_t S_BAR = S_OUT + 32768;        // barriers + tmem slot + abort flag
 constexpr uint32_t S_END = S_BAR + 128;
 constexpr uint32_t kScanSmem = S_END + 1024;
@@ -109,15 +108,15 @@ template <typename Tout, int MODE>
 __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [2] record staged (bulk copy)
-  uint64_t* bar_u = full + 2;                                // [D_U | D_O] product done
-  uint64_t* bar_s = full + 3;                                // [D_O | S] product done
-  uint64_t* s16_ready = full + 4;                            // fp16 state copy written (256 arrivals)
-  uint64_t* u16_ready = full + 5;                            // U^T written, decay applied (256 arrivals)
-  uint64_t* do_free = full + 6;                              // D_O read by the output warps
-  uint64_t* bar_fin = full + 7;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 64);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S_BAR + 68);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [3] record staged (bulk copy)
+  uint64_t* bar_u = full + 3;                                // [D_U | D_O] product done
+  uint64_t* bar_s = full + 4;                                // [D_O | S] product done
+  uint64_t* s16_ready = full + 5;                            // fp16 state copy written (256 arrivals)
+  uint64_t* u16_ready = full + 6;                            // U^T written, decay applied (256 arrivals)
+  uint64_t* do_free = full + 7;                              // D_O read by the output warps
+  uint64_t* bar_fin = full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 80);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S_BAR + 84);
 
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
@@ -139,8 +138,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
     tmem_relinquish();
   }
   if (tid == 32) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    for (int i = 0; i < kStages; ++i) mbar_init(&full[i], 1);
     mbar_init(bar_u, 1);
     mbar_init(bar_s, 1);
     mbar_init(s16_ready, kStateThreads);
@@ -163,28 +161,30 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
   if (warp == kIssuerWarp) {
     // ======================== issuer: record staging + all MMAs (one lane)
     if (lane == 0) {
-      int64_t last_load = -1;
+      int64_t last_load = -1, consumed = -1;
       bool ok = true;
-      if (ncs > 0) {
-        mbar_arrive_expect_tx(&full[0], kRecStage);
-        bulk_g2s(sm + S_STAGE0, rec0, kRecStage, &full[0]);
-        last_load = 0;
+      for (int64_t c = 0; c < 2 && c < ncs; ++c) {
+        mbar_arrive_expect_tx(&full[c], kRecStage);
+        bulk_g2s(sm + c * kStage, rec0 + (size_t)c * rec_stride, kRecStage, &full[c]);
+        last_load = c;
       }
       const uint32_t id1 = MODE == 0 ? idesc_f16(128, 128, false, true) : idesc_f16(128, 64, false, true);
       const uint32_t id2 = MODE == 0 ? idesc_f16(128, 192, false, false) : idesc_f16(128, 128, false, false);
       for (int64_t c = 0; c < ncs && ok; ++c) {
-        const int st = (int)(c & 1);
-        uint8_t* stage = sm + (st ? S_STAGE1 : S_STAGE0);
-        if (c + 1 < ncs) {
-          // stage st^1 held chunk c-1: free once that chunk's products are done
+        const int st = (int)(c % kStages);
+        uint8_t* stage = sm + st * kStage;
+        if (c + 2 < ncs) {
+          // chunk c+2 goes where chunk c-1 was: free once that chunk's products are done
           if (c >= 1) ok = wait_or_abort(bar_s, (uint32_t)((c - 1) & 1), abort_flag);
           if (!ok) break;
-          mbar_arrive_expect_tx(&full[st ^ 1], kRecStage);
-          bulk_g2s(sm + (st ? S_STAGE0 : S_STAGE1), rec0 + (size_t)(c + 1) * rec_stride, kRecStage, &full[st ^ 1]);
-          last_load = c + 1;
+          const int s2 = (int)((c + 2) % kStages);
+          mbar_arrive_expect_tx(&full[s2], kRecStage);
+          bulk_g2s(sm + s2 * kStage, rec0 + (size_t)(c + 2) * rec_stride, kRecStage, &full[s2]);
+          last_load = c + 2;
         }
-        ok = wait_or_abort(&full[st], (uint32_t)((c >> 1) & 1), abort_flag) &&
-             wait_or_abort(s16_ready, (uint32_t)(c & 1), abort_flag);
+        ok = wait_or_abort(&full[st], (uint32_t)((c / kStages) & 1), abort_flag);
+        if (ok) consumed = c;
+        ok = ok && wait_or_abort(s16_ready, (uint32_t)(c & 1), abort_flag);
         if (MODE == 0 && ok && c >= 1) ok = wait_or_abort(do_free, (uint32_t)((c - 1) & 1), abort_flag);
         if (!ok) break;
         tc_fence_after();
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
       if (!ok || *abort_flag) {
         *abort_flag = 1;
         // let this thread's copies and MMAs drain (bounded) before TMEM is released
-        if (last_load >= 0) mbar_wait(&full[last_load & 1], (uint32_t)((last_load >> 1) & 1));
+        for (int64_t l = consumed + 1; l <= last_load; ++l) mbar_wait(&full[l % kStages], (uint32_t)((l / kStages) & 1));
         mma_commit(bar_fin);
         mbar_wait(bar_fin, 0);
       }
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
       if (ncs > 0) {
         ok = wait_or_abort(&full[0], 0, abort_flag);
         if (ok) {
-          const float* gc = reinterpret_cast<const float*>(sm + S_STAGE0 + kRecGC) + 64 * hc;
+          const float* gc = reinterpret_cast<const float*>(sm + kRecGC) + 64 * hc;
 #pragma unroll
           for (int c = 0; c < 64; ++c) s[c] *= gc[c];
         }
@@ -295,10 +295,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(s16_ready);
-        const int st1 = (int)((c + 1) & 1);
-        ok = wait_or_abort(&full[st1], (uint32_t)(((c + 1) >> 1) & 1), abort_flag);
+        const int st1 = (int)((c + 1) % kStages);
+        ok = wait_or_abort(&full[st1], (uint32_t)(((c + 1) / kStages) & 1), abort_flag);
         if (!ok) break;
-        const float* gc = reinterpret_cast<const float*>(sm + (st1 ? S_STAGE1 : S_STAGE0) + kRecGC) + 64 * hc;
+        const float* gc = reinterpret_cast<const float*>(sm + st1 * kStage + kRecGC) + 64 * hc;
 #pragma unroll
         for (int j = 0; j < 64; ++j) s[j] *= gc[j];
         tmem_st64f(tl + T_S + 64 * hc, s);
