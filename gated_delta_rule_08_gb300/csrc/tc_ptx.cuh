@@ -184,6 +184,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst_smem, const void* tmap, in
       : "memory");
 }
 
+// 2-D tiled TMA store from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* src_smem, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap), "r"(x),
+               "r"(y), "r"(smem_u32(src_smem))
+               : "memory");
+}
+
 // ------------------------------------------------------------------ swizzled smem addressing
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a 128-byte-swizzled
 // region whose base is 1024-byte aligned (rows of 128 bytes, 8-row atoms of 1024 bytes).
