@@ -25,7 +25,8 @@
 //      (p & 1) of every 128-byte operand row, so it only waits for the MMAs of pass p - 2;
 //    - the passes also emit Q_hat^T and K_bar^T (channel-major) and e^{G_C} into the record, and
 //      K_hat and V (fp16) in place of the raw tiles;
-//    - T = (I + A)^-1 Diag(beta) by blocked (16 x 16) forward substitution in fp32;
+//    - T = (I + A)^-1 Diag(beta): 16 x 16 diagonal blocks by forward substitution (fp32), the
+//      off-diagonal blocks by warp-level tf32 MMAs with a three-term split (~fp32), one block per warp;
 //    - fp16 MMAs W^T = K_hat^T T^T and U_hat^T = V^T T^T (M = 128, N = 64, K = 64), then W^T, M
 //      and U_hat^T into the record.
 //
@@ -56,7 +57,7 @@ constexpr uint32_t O_XH = 0, O_XL = 16384, O_YH = 32768, O_YL = 45056, O_BYTES =
 // after the A/M product the operand region holds the solve:
 constexpr uint32_t O_SA = 0;             // fp32 A [64][65]
 constexpr uint32_t O_SX = 16640;         // fp32 X = (I + A)^-1 [64][65]
-constexpr uint32_t O_SY = 33280;         // fp32 scratch, three 16 x 16 blocks
+constexpr uint32_t O_SY = 33280;         // fp32 scratch: three warps x [16][17]
 constexpr uint32_t O_TT = 37888;         // fp16 T [64 r][64 s] row format (1024-aligned)
 constexpr uint32_t P_MISC = P_OPS + O_BYTES;
 constexpr uint32_t M_BETA = 0;           // fp32 [2 tasks][64]
@@ -77,6 +78,52 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
   hi = (a >> 16) | b;
   const __nv_bfloat162 t = __floats2bfloat162_rn(x0 - __uint_as_float(a), x1 - __uint_as_float(b));
   lo = *reinterpret_cast<const uint32_t*>(&t);
+}
+
+// ---- warp-level tf32 MMA (mma.sync m16n8k8) for the 16 x 16 blocks of the triangular solve.
+// Fragments: A (16 x 8) a0 (g, t), a1 (g+8, t), a2 (g, t+4), a3 (g+8, t+4); B (8 x 8, k x n) b0 (t, g),
+// b1 (t+4, g); C (16 x 8) c0 (g, 2t), c1 (g, 2t+1), c2 (g+8, 2t), c3 (g+8, 2t+1); g = lane / 4, t = lane % 4.
+__device__ __forceinline__ uint32_t tf32_bits(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32_m16n8k8(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// acc[term][n-tile] += M1 (16 x 16, row-major, stride ld1) * M2 (16 x 16 as k rows x n columns, stride
+// ld2), with each operand split as x = hi + lo (both tf32): the terms hi*hi, hi*lo, lo*hi accumulate
+// separately (independent MMA chains) and sum to ~fp32 accuracy with fp32 range.
+__device__ __forceinline__ void warp_gemm16_acc(float (&acc)[3][2][4], const float* M1, int ld1, const float* M2,
+                                                int ld2, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    const float af[4] = {M1[g * ld1 + 8 * ks + t], M1[(g + 8) * ld1 + 8 * ks + t], M1[g * ld1 + 8 * ks + t + 4],
+                         M1[(g + 8) * ld1 + 8 * ks + t + 4]};
+    uint32_t ah[4], al[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ah[i] = tf32_bits(af[i]);
+      al[i] = tf32_bits(af[i] - __uint_as_float(ah[i]));
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const float b0 = M2[(8 * ks + t) * ld2 + 8 * nt + g], b1 = M2[(8 * ks + t + 4) * ld2 + 8 * nt + g];
+      const uint32_t bh0 = tf32_bits(b0), bh1 = tf32_bits(b1);
+      const uint32_t bl0 = tf32_bits(b0 - __uint_as_float(bh0)), bl1 = tf32_bits(b1 - __uint_as_float(bh1));
+      mma_tf32_m16n8k8(acc[0][nt], ah, bh0, bh1);
+      mma_tf32_m16n8k8(acc[1][nt], ah, bl0, bl1);
+      mma_tf32_m16n8k8(acc[2][nt], al, bh0, bh1);
+    }
+  }
+}
+// (acc[0] + (acc[1] + acc[2])) of one n-tile element
+__device__ __forceinline__ float acc_sum(const float (&acc)[3][2][4], int nt, int e) {
+  return acc[0][nt][e] + (acc[1][nt][e] + acc[2][nt][e]);
 }
 
 struct PrepMaps {
@@ -424,7 +471,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
       tc_fence_before();
       group_sync(1, kCompute);
 
-      // ---- T = (I + A)^-1 Diag(beta), blocked 16 x 16 forward substitution (fp32)
+      // ---- T = (I + A)^-1 Diag(beta), blocked 16 x 16
       {
         float* sX = reinterpret_cast<float*>(ops + O_SX);
         float* sY = reinterpret_cast<float*>(ops + O_SY);
@@ -447,31 +494,41 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
           for (int i = 0; i < 16; ++i) sX[(r0 + i) * 65 + s_] = x[i];
         }
         group_sync(1, kCompute);
-        // block rows 1..3: X_ij = -X_ii * sum_{m=j}^{i-1} A_im X_mj (16 x 16 blocks, one entry per thread)
-        const int rr = tid >> 4, cc = tid & 15;
+        // off-diagonal blocks by their distance d from the diagonal, one block per warp:
+        // X_ij = -X_ii * sum_{m=j}^{i-1} A_im X_mj  (i = j + d), warp-level tf32 MMAs
+        {
+          const int g = lane >> 2, t = lane & 3;
+          float* sYw = sY + warp * (16 * 17);  // per-warp 16 x 16 scratch (stride 17)
+#pragma unroll 1
+          for (int d = 1; d < 4; ++d) {
+            if (warp < 4 - d) {
+              const int j = warp, i = j + d;
+              float acc[3][2][4] = {};
+#pragma unroll 1
+              for (int m = j; m < i; ++m)
+                warp_gemm16_acc(acc, sA + (16 * i) * 65 + 16 * m, 65, sX + (16 * m) * 65 + 16 * j, 65, lane);
 #pragma unroll
-        for (int i = 1; i < 4; ++i) {
+              for (int nt = 0; nt < 2; ++nt) {
+                sYw[g * 17 + 8 * nt + 2 * t] = acc_sum(acc, nt, 0);
+                sYw[g * 17 + 8 * nt + 2 * t + 1] = acc_sum(acc, nt, 1);
+                sYw[(g + 8) * 17 + 8 * nt + 2 * t] = acc_sum(acc, nt, 2);
+                sYw[(g + 8) * 17 + 8 * nt + 2 * t + 1] = acc_sum(acc, nt, 3);
+              }
+              __syncwarp();
+              float z[3][2][4] = {};
+              warp_gemm16_acc(z, sX + (16 * i) * 65 + 16 * i, 65, sYw, 17, lane);
+              float* xo = sX + (16 * i) * 65 + 16 * j;
 #pragma unroll
-          for (int j = 0; j < i; ++j) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int m = j; m < i; ++m) {
-#pragma unroll
-              for (int k2 = 0; k2 < 16; ++k2)
-                acc[k2 & 3] = fmaf(sA[(16 * i + rr) * 65 + 16 * m + k2], sX[(16 * m + k2) * 65 + 16 * j + cc], acc[k2 & 3]);
+              for (int nt = 0; nt < 2; ++nt) {
+                xo[g * 65 + 8 * nt + 2 * t] = -acc_sum(z, nt, 0);
+                xo[g * 65 + 8 * nt + 2 * t + 1] = -acc_sum(z, nt, 1);
+                xo[(g + 8) * 65 + 8 * nt + 2 * t] = -acc_sum(z, nt, 2);
+                xo[(g + 8) * 65 + 8 * nt + 2 * t + 1] = -acc_sum(z, nt, 3);
+              }
+              __syncwarp();
             }
-            sY[j * 256 + rr * 16 + cc] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            group_sync(1, kCompute);
           }
-          group_sync(1, kCompute);
-#pragma unroll
-          for (int j = 0; j < i; ++j) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int k2 = 0; k2 < 16; ++k2)
-              acc[k2 & 3] = fmaf(sX[(16 * i + rr) * 65 + 16 * i + k2], sY[j * 256 + k2 * 16 + cc], acc[k2 & 3]);
-            sX[(16 * i + rr) * 65 + 16 * j + cc] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
-          }
-          group_sync(1, kCompute);
         }
         // T = X Diag(beta) -> fp16 row format [r][s] (zero above the diagonal)
         {
