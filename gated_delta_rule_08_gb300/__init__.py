@@ -7,7 +7,9 @@ the same entry-point names, and the seeded synthetic-input generators.
 from .binding import (  # noqa: F401
     KdaError,
     kda_chunk_fwd,
+    kda_chunk_fwd_checkpoints,
     kda_chunk_fwd_workspace_size,
+    kda_decode_multi,
     kda_decode_step,
     kda_get_device_error,
     kda_status_string,

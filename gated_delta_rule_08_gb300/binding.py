@@ -25,9 +25,11 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "K
 DEVERR_BAD_SLOT = 0x1
 DEVERR_BAD_SEQLENS = 0x2
 DEVERR_WAIT_TIMEOUT = 0x4
+DEVERR_BAD_COUNT = 0x8
 
 # Exported symbols, as declared in include/kda.h.
-EXPORTS = ("kda_chunk_fwd_workspace_size", "kda_chunk_fwd", "kda_decode_step", "kda_get_device_error",
+EXPORTS = ("kda_chunk_fwd_workspace_size", "kda_chunk_fwd", "kda_decode_step", "kda_decode_multi",
+           "kda_chunk_fwd_checkpoints", "kda_get_device_error",
            "kda_status_string", "kda_trace_enable", "kda_trace_collect", "kda_chunk_fwd_noalloc",
            "kda_noalloc_scratch_bytes")
 
@@ -63,6 +65,11 @@ def load_library(path: Optional[str] = None):
         lib.kda_chunk_fwd.restype = I
         lib.kda_decode_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
         lib.kda_decode_step.restype = I
+        lib.kda_decode_multi.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P]
+        lib.kda_decode_multi.restype = I
+        lib.kda_chunk_fwd_checkpoints.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I, I64, I, I, I, I, I, I, P, P,
+                                                  SZ, P]
+        lib.kda_chunk_fwd_checkpoints.restype = I
         lib.kda_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
         lib.kda_get_device_error.restype = I
         lib.kda_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, I, I, P, P]
@@ -120,7 +127,7 @@ def kda_chunk_fwd_workspace_size(B: int, T: int, H: int, dk: int, dv: int, C: in
 
 def kda_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, out=None, hT=None, *, B: Optional[int] = None,
                   C: int = 64, gate=None, norm_weight=None, eps: float = 1e-6, workspace=None,
-                  output_final_state: bool = True, out_dtype: Optional[torch.dtype] = None):
+                  output_final_state: bool = True, out_dtype: Optional[torch.dtype] = None, _ckpt=None):
     """Chunked KDA prefill.  q, k: [T_tot, H, dk]; v: [T_tot, H, dv]; g: [T_tot, H, dk] fp32;
     beta: [T_tot, H] fp32; h0: [B, H, dk, dv] fp32 or None; cu_seqlens: int32 [B+1] on the device
     or None (then B sequences of T_tot/B tokens).  gate/norm_weight enable the fused epilogue.
@@ -169,13 +176,42 @@ def kda_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, out=None, hT=None,
     epi = None
     if gate is not None:
         epi = _Epilogue(gate.data_ptr(), norm_weight.data_ptr() if norm_weight is not None else None, float(eps))
-    st = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
-                           _ptr(out), _ptr(hT), B, T_arg, H, dk, dv, C, code, ocode,
-                           ctypes.byref(epi) if epi is not None else None, _ptr(workspace),
-                           workspace.numel(), _stream(dev))
+    if _ckpt is None:
+        st = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
+                               _ptr(out), _ptr(hT), B, T_arg, H, dk, dv, C, code, ocode,
+                               ctypes.byref(epi) if epi is not None else None, _ptr(workspace),
+                               workspace.numel(), _stream(dev))
+        if st != 0:
+            raise KdaError("kda_chunk_fwd", st)
+        return out, hT
+    states, ckpt_chunks = _ckpt
+    span = 64 * ckpt_chunks
+    if cu_seqlens is not None:
+        lens = (cu_seqlens[1:] - cu_seqlens[:-1]).to("cpu").to(torch.int64)
+        n_ckpt = int((lens // span).sum())
+    else:
+        n_ckpt = B * (T_arg // span)
+    if states is None:
+        states = torch.empty(n_ckpt, H, dk, dv, device=dev, dtype=torch.float32)
+    _check(states, "states", torch.float32, (n_ckpt, H, dk, dv), dev)
+    st = lib.kda_chunk_fwd_checkpoints(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
+                                       _ptr(out), _ptr(hT), ctypes.c_void_p(states.data_ptr()), int(ckpt_chunks), B,
+                                       T_arg, H, dk, dv, C, code, ocode,
+                                       ctypes.byref(epi) if epi is not None else None, _ptr(workspace),
+                                       workspace.numel(), _stream(dev))
     if st != 0:
-        raise KdaError("kda_chunk_fwd", st)
-    return out, hT
+        raise KdaError("kda_chunk_fwd_checkpoints", st)
+    return out, hT, states
+
+
+def kda_chunk_fwd_checkpoints(q, k, v, g, beta, h0=None, cu_seqlens=None, out=None, hT=None, *, ckpt_chunks: int,
+                              states=None, **kw):
+    """kda_chunk_fwd that also returns the fp32 state of every sequence after each 64 * ckpt_chunks
+    of its tokens: states [n_ckpt, H, dk, dv], sequences in order, each in token order.
+    Returns (out, hT, states)."""
+    if ckpt_chunks < 1:
+        raise ValueError("ckpt_chunks must be >= 1")
+    return kda_chunk_fwd(q, k, v, g, beta, h0, cu_seqlens, out, hT, _ckpt=(states, int(ckpt_chunks)), **kw)
 
 
 def kda_decode_step(q, k, v, g, beta, state_pool, slot_idx, out=None, *, gate=None, norm_weight=None,
@@ -212,6 +248,47 @@ def kda_decode_step(q, k, v, g, beta, state_pool, slot_idx, out=None, *, gate=No
                              ctypes.byref(epi) if epi is not None else None, _stream(dev))
     if st != 0:
         raise KdaError("kda_decode_step", st)
+    return out
+
+
+def kda_decode_multi(q, k, v, g, beta, state_pool, slot_idx, ntok_per_req=None, out=None, *, commit: bool,
+                     gate=None, norm_weight=None, eps: float = 1e-6, out_dtype: Optional[torch.dtype] = None):
+    """Several tokens per request (speculative-decode verify / accept).  q, k: [N, n_tok, H, dk];
+    v: [N, n_tok, H, dv]; g: [N, n_tok, H, dk] fp32; beta: [N, n_tok, H] fp32; state_pool:
+    [num_slots, H, dk, dv] fp32; slot_idx: int32 [N]; ntok_per_req: int32 [N] (tokens applied per
+    request) or None (all n_tok).  commit=False leaves the pool untouched (verify); commit=True
+    writes each request's state after its applied tokens back (accept).
+    Returns out [N, n_tok, H, dv]; rows of tokens not applied are left as they were in `out`."""
+    lib = load_library()
+    dev = q.device
+    N, n_tok, H, dk = q.shape
+    dv = v.shape[3]
+    dt = q.dtype
+    code = _dtype_code(q)
+    num_slots = state_pool.shape[0]
+    _check(q, "q", dt, (N, n_tok, H, dk), dev)
+    _check(k, "k", dt, (N, n_tok, H, dk), dev)
+    _check(v, "v", dt, (N, n_tok, H, dv), dev)
+    _check(g, "g", torch.float32, (N, n_tok, H, dk), dev)
+    _check(beta, "beta", torch.float32, (N, n_tok, H), dev)
+    _check(state_pool, "state_pool", torch.float32, (num_slots, H, dk, dv), dev)
+    _check(slot_idx, "slot_idx", torch.int32, (N,), dev)
+    _check(ntok_per_req, "ntok_per_req", torch.int32, (N,), dev)
+    _check(gate, "gate", dt, (N, n_tok, H, dv), dev)
+    _check(norm_weight, "norm_weight", torch.float32, (dv,), dev)
+    odt = out.dtype if out is not None else (out_dtype or dt)
+    if out is None:
+        out = torch.empty(N, n_tok, H, dv, device=dev, dtype=odt)
+    _check(out, "out", odt, (N, n_tok, H, dv), dev)
+    ocode = _dtype_code(out)
+    epi = None
+    if gate is not None:
+        epi = _Epilogue(gate.data_ptr(), norm_weight.data_ptr() if norm_weight is not None else None, float(eps))
+    st = lib.kda_decode_multi(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_pool), _ptr(slot_idx),
+                              _ptr(ntok_per_req), _ptr(out), N, n_tok, H, dk, dv, num_slots, 1 if commit else 0,
+                              code, ocode, ctypes.byref(epi) if epi is not None else None, _stream(dev))
+    if st != 0:
+        raise KdaError("kda_decode_multi", st)
     return out
 
 

@@ -78,12 +78,14 @@ KDA_API size_t kda_chunk_fwd_workspace_size(int B, int64_t T, int H, int dk, int
   return bytes;
 }
 
-KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
-                                 const float* beta, const float* h0, const int32_t* cu_seqlens, void* out,
-                                 float* hT, int B, int64_t T, int H, int dk, int dv, int C, kda_dtype dtype,
-                                 kda_dtype out_dtype, const kda_epilogue* epi, void* workspace,
-                                 size_t workspace_bytes, void* stream) {
+namespace {
+kda_status chunk_fwd_common(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                            const float* h0, const int32_t* cu_seqlens, void* out, float* hT, float* states,
+                            int64_t ckpt_chunks, int B, int64_t T, int H, int dk, int dv, int C, kda_dtype dtype,
+                            kda_dtype out_dtype, const kda_epilogue* epi, void* workspace, size_t workspace_bytes,
+                            void* stream) {
   if (B <= 0 || T < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  if (states && (ckpt_chunks <= 0 || !aligned16(states))) return KDA_ERR_INVALID_ARG;
   if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_FP32) return KDA_ERR_UNSUPPORTED;
   if (out_dtype != KDA_DTYPE_BF16 && out_dtype != KDA_DTYPE_FP32) return KDA_ERR_UNSUPPORTED;
   if (C != kChunk || !dims_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
@@ -116,32 +118,58 @@ KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, co
   a.epi.norm_weight = epi ? epi->norm_weight : nullptr;
   a.epi.eps = epi ? epi->eps : 0.f;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.err = err;
+  a.ckpt = states; a.ckpt_chunks = states ? ckpt_chunks : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = (a.bf16 && prefill_tc_supported(dk, dv)) ? prefill_tc_launch(a, s) : prefill_cc_launch(a, s);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
+}  // namespace
 
-KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* g,
-                                   const float* beta, float* state_pool, const int32_t* slot_idx, void* out,
-                                   int N, int H, int dk, int dv, int num_slots, kda_dtype dtype,
-                                   kda_dtype out_dtype, const kda_epilogue* epi, void* stream) {
-  if (N < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
+KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, const float* h0, const int32_t* cu_seqlens, void* out,
+                                 float* hT, int B, int64_t T, int H, int dk, int dv, int C, kda_dtype dtype,
+                                 kda_dtype out_dtype, const kda_epilogue* epi, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  return chunk_fwd_common(q, k, v, g, beta, h0, cu_seqlens, out, hT, nullptr, 0, B, T, H, dk, dv, C, dtype,
+                          out_dtype, epi, workspace, workspace_bytes, stream);
+}
+
+KDA_API kda_status kda_chunk_fwd_checkpoints(const void* q, const void* k, const void* v, const float* g,
+                                             const float* beta, const float* h0, const int32_t* cu_seqlens,
+                                             void* out, float* hT, float* states, int64_t ckpt_chunks, int B,
+                                             int64_t T, int H, int dk, int dv, int C, kda_dtype dtype,
+                                             kda_dtype out_dtype, const kda_epilogue* epi, void* workspace,
+                                             size_t workspace_bytes, void* stream) {
+  if (!states) return KDA_ERR_INVALID_ARG;
+  return chunk_fwd_common(q, k, v, g, beta, h0, cu_seqlens, out, hT, states, ckpt_chunks, B, T, H, dk, dv, C, dtype,
+                          out_dtype, epi, workspace, workspace_bytes, stream);
+}
+
+namespace {
+kda_status decode_common(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         float* state_pool, const int32_t* slot_idx, const int32_t* ntok_per_req, void* out, int N,
+                         int n_tok, int H, int dk, int dv, int num_slots, bool commit, kda_dtype dtype,
+                         kda_dtype out_dtype, const kda_epilogue* epi, void* stream) {
+  if (N < 0 || n_tok < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
   if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_FP32) return KDA_ERR_UNSUPPORTED;
   if (out_dtype != KDA_DTYPE_BF16 && out_dtype != KDA_DTYPE_FP32) return KDA_ERR_UNSUPPORTED;
   if (!dims_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
-  if (N > 0 && (!q || !k || !v || !g || !beta || !state_pool || !slot_idx || !out)) return KDA_ERR_INVALID_ARG;
-  if (epi && N > 0 && !epi->gate_logits) return KDA_ERR_INVALID_ARG;
+  const bool work = N > 0 && n_tok > 0;
+  if (work && (!q || !k || !v || !g || !beta || !state_pool || !slot_idx || !out)) return KDA_ERR_INVALID_ARG;
+  if (epi && work && !epi->gate_logits) return KDA_ERR_INVALID_ARG;
   if (epi && !(epi->eps >= 0.f)) return KDA_ERR_INVALID_ARG;
-  if ((int64_t)N * H > 0x7fffffff) return KDA_ERR_UNSUPPORTED;
+  if ((int64_t)N * H > 0x7fffffff || (int64_t)N * n_tok * H > 0x7fffffff) return KDA_ERR_UNSUPPORTED;
   if (!aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
   unsigned int* err = nullptr;
   int major = 0, minor = 0;
   kda_status st = device_state(&err, &major, &minor);
   if (st != KDA_OK) return st;
   if (major != 10 || minor != 3) return KDA_ERR_UNSUPPORTED;
+  if (!work) return KDA_OK;
   DecodeArgs a{};
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state_pool = state_pool; a.slot_idx = slot_idx;
   a.out = out; a.N = N; a.H = H; a.dk = dk; a.dv = dv; a.num_slots = num_slots;
+  a.n_tok = n_tok; a.ntok_per_req = ntok_per_req; a.commit = commit;
   a.bf16 = (dtype == KDA_DTYPE_BF16);
   a.out_bf16 = (out_dtype == KDA_DTYPE_BF16);
   a.epi.gate = epi ? epi->gate_logits : nullptr;
@@ -150,6 +178,24 @@ KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, 
   a.err = err;
   cudaError_t e = decode_launch(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+}  // namespace
+
+KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* g,
+                                   const float* beta, float* state_pool, const int32_t* slot_idx, void* out,
+                                   int N, int H, int dk, int dv, int num_slots, kda_dtype dtype,
+                                   kda_dtype out_dtype, const kda_epilogue* epi, void* stream) {
+  return decode_common(q, k, v, g, beta, state_pool, slot_idx, nullptr, out, N, 1, H, dk, dv, num_slots, true, dtype,
+                       out_dtype, epi, stream);
+}
+
+KDA_API kda_status kda_decode_multi(const void* q, const void* k, const void* v, const float* g,
+                                    const float* beta, float* state_pool, const int32_t* slot_idx,
+                                    const int32_t* ntok_per_req, void* out, int N, int n_tok, int H, int dk, int dv,
+                                    int num_slots, int commit, kda_dtype dtype, kda_dtype out_dtype,
+                                    const kda_epilogue* epi, void* stream) {
+  return decode_common(q, k, v, g, beta, state_pool, slot_idx, ntok_per_req, out, N, n_tok, H, dk, dv, num_slots,
+                       commit != 0, dtype, out_dtype, epi, stream);
 }
 
 KDA_API kda_status kda_get_device_error(void* stream, uint32_t* flags) {

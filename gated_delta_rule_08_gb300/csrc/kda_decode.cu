@@ -1,4 +1,4 @@
-// KDA single-token decode over a pool of fp32 states (in place).
+// KDA recurrent decode over a pool of fp32 states (in place), one or several tokens per request.
 //
 // Kimi K3 report walk-through (kimi-k3-paper.pages.dev): section 2.2 Eq. 1 (the
 // per-token update), section 2.4 Eq. 3 (read-out), section 3.3 Eq. 6 (RMSNorm then
@@ -12,6 +12,13 @@
 //   delta = beta (v - a)
 //   S_new = S' + k delta^T                       (== (I - beta k k^T) S' + beta k v^T)
 //   o     = S_new^T q = b + (k . q) delta
+//
+// Multi-token form (section 13.4, the state problem of speculative decoding: an in-place update
+// cannot be rolled back, so the verify pass must not overwrite the pooled state): a request may
+// carry several tokens, applied in order to the state held in registers; the state is written
+// back only when asked (commit), after exactly the request's own token count.  Verify = all
+// draft tokens, no write-back; accept = the accepted prefix recomputed from the cached inputs,
+// with write-back.  One token with write-back is the plain decode step.
 //
 // The kernel is bound by HBM bandwidth: it streams the 64 KB state in and out once.
 // One CTA per (n, h); each thread owns 4 contiguous value columns (one float4) of
@@ -31,16 +38,16 @@ template <int DK, int DV, typename Tin, typename Tout>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
               const float* __restrict__ g, const float* __restrict__ beta, float* __restrict__ pool,
-              const int32_t* __restrict__ slot_idx, Tout* __restrict__ out, int H, int num_slots,
-              const Tin* __restrict__ gate, const float* __restrict__ norm_w, float eps,
-              unsigned int* __restrict__ err) {
+              const int32_t* __restrict__ slot_idx, Tout* __restrict__ out, int H, int num_slots, int n_tok,
+              const int32_t* __restrict__ ntok_per_req, int commit, const Tin* __restrict__ gate,
+              const float* __restrict__ norm_w, float eps, unsigned int* __restrict__ err) {
   constexpr int TPR = DV / 4;               // threads per state row
   constexpr int NG = kDecodeThreads / TPR;  // row groups
   constexpr int RPG = DK / NG;              // rows per thread
   static_assert(DK % NG == 0, "rows must split evenly");
 
-  const int row = blockIdx.x;  // n * H + h
-  const int n = row / H, h = row - (row / H) * H;
+  const int nh = blockIdx.x;  // n * H + h
+  const int n = nh / H, h = nh - (nh / H) * H;
   const int tid = threadIdx.x;
   const int cg = tid % TPR, rg = tid / TPR;
 
@@ -49,6 +56,15 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     if (tid == 0 && h == 0) atomicOr(err, KDA_DEVERR_BAD_SLOT);
     return;
   }
+  int count = n_tok;
+  if (ntok_per_req != nullptr) {
+    count = ntok_per_req[n];
+    if (count < 0 || count > n_tok) {
+      if (tid == 0 && h == 0) atomicOr(err, KDA_DEVERR_BAD_COUNT);
+      return;
+    }
+  }
+  if (count == 0) return;  // nothing to apply: outputs and state untouched
   float* S = pool + ((size_t)slot * H + h) * (size_t)(DK * DV);
 
   // Issue the state loads first: they are the only long-latency traffic.
@@ -63,76 +79,82 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   __shared__ float red[kDecodeThreads / 32];
   __shared__ float s_kq;
 
-  const size_t rk = (size_t)row * DK, rv = (size_t)row * DV;
-  for (int i = tid; i < DK; i += kDecodeThreads) {
-    sk[i] = to_f32(k[rk + i]);
-    sq[i] = to_f32(q[rk + i]);
-    salpha[i] = __expf(g[rk + i]);
-  }
-  for (int j = tid; j < DV; j += kDecodeThreads) sv[j] = to_f32(v[rv + j]);
-  const float b_r = beta[row];
-  __syncthreads();
-
-  if (tid < 32) {  // k . q
-    float acc = 0.f;
-    for (int i = tid; i < DK; i += 32) acc = fmaf(sk[i], sq[i], acc);
-    acc = warp_sum(acc);
-    if (tid == 0) s_kq = acc;
-  }
-
-  float4 pa = make_float4(0.f, 0.f, 0.f, 0.f), pb = pa;
-#pragma unroll
-  for (int i = 0; i < RPG; ++i) {
-    const int r = rg + i * NG;
-    const float al = salpha[r];
-    s[i].x *= al; s[i].y *= al; s[i].z *= al; s[i].w *= al;
-    pa = f4_fma(sk[r], s[i], pa);
-    pb = f4_fma(sq[r], s[i], pb);
-  }
-  part_a[rg][cg] = pa;
-  part_b[rg][cg] = pb;
-  __syncthreads();
-
-  if (tid < DV) {
-    const int c4 = tid >> 2, e = tid & 3;
-    float a = 0.f, b = 0.f;
-#pragma unroll
-    for (int gi = 0; gi < NG; ++gi) {
-      a += reinterpret_cast<const float*>(&part_a[gi][c4])[e];
-      b += reinterpret_cast<const float*>(&part_b[gi][c4])[e];
+  for (int t = 0; t < count; ++t) {
+    const size_t row = ((size_t)n * n_tok + t) * H + h;  // token row of [N, n_tok, H]
+    const size_t rk = row * DK, rv = row * DV;
+    for (int i = tid; i < DK; i += kDecodeThreads) {
+      sk[i] = to_f32(k[rk + i]);
+      sq[i] = to_f32(q[rk + i]);
+      salpha[i] = __expf(g[rk + i]);
     }
-    const float d = b_r * (sv[tid] - a);
-    sdelta[tid] = d;
-    so[tid] = fmaf(s_kq, d, b);
-  }
-  __syncthreads();
-
-  const float4 d4 = reinterpret_cast<const float4*>(sdelta)[cg];
-#pragma unroll
-  for (int i = 0; i < RPG; ++i) {
-    const int r = rg + i * NG;
-    s[i] = f4_fma(sk[r], d4, s[i]);
-    __stcs(reinterpret_cast<float4*>(S + (size_t)r * DV) + cg, s[i]);
-  }
-
-  // Read-out (+ optional RMSNorm over dv and sigmoid gate).
-  float o = 0.f;
-  if (tid < DV) o = so[tid];
-  if (gate != nullptr) {
-    float sq_sum = (tid < DV) ? o * o : 0.f;
-    sq_sum = warp_sum(sq_sum);
-    if ((tid & 31) == 0) red[tid >> 5] = sq_sum;
+    for (int j = tid; j < DV; j += kDecodeThreads) sv[j] = to_f32(v[rv + j]);
+    const float b_r = beta[row];
     __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < (DV + 31) / 32; ++w) tot += red[w];
-    if (tid < DV) {
-      const float inv = rsqrtf(tot / (float)DV + eps);
-      const float wj = norm_w ? norm_w[tid] : 1.f;
-      o = o * inv * wj * sigmoidf_(to_f32(gate[rv + tid]));
+
+    if (tid < 32) {  // k . q
+      float acc = 0.f;
+      for (int i = tid; i < DK; i += 32) acc = fmaf(sk[i], sq[i], acc);
+      acc = warp_sum(acc);
+      if (tid == 0) s_kq = acc;
     }
+
+    float4 pa = make_float4(0.f, 0.f, 0.f, 0.f), pb = pa;
+#pragma unroll
+    for (int i = 0; i < RPG; ++i) {
+      const int r = rg + i * NG;
+      const float al = salpha[r];
+      s[i].x *= al; s[i].y *= al; s[i].z *= al; s[i].w *= al;
+      pa = f4_fma(sk[r], s[i], pa);
+      pb = f4_fma(sq[r], s[i], pb);
+    }
+    part_a[rg][cg] = pa;
+    part_b[rg][cg] = pb;
+    __syncthreads();
+
+    if (tid < DV) {
+      const int c4 = tid >> 2, e = tid & 3;
+      float a = 0.f, b = 0.f;
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) {
+        a += reinterpret_cast<const float*>(&part_a[gi][c4])[e];
+        b += reinterpret_cast<const float*>(&part_b[gi][c4])[e];
+      }
+      const float d = b_r * (sv[tid] - a);
+      sdelta[tid] = d;
+      so[tid] = fmaf(s_kq, d, b);
+    }
+    __syncthreads();
+
+    const float4 d4 = reinterpret_cast<const float4*>(sdelta)[cg];
+#pragma unroll
+    for (int i = 0; i < RPG; ++i) s[i] = f4_fma(sk[rg + i * NG], d4, s[i]);
+
+    // Read-out (+ optional RMSNorm over dv and sigmoid gate).
+    float o = 0.f;
+    if (tid < DV) o = so[tid];
+    if (gate != nullptr) {
+      float sq_sum = (tid < DV) ? o * o : 0.f;
+      sq_sum = warp_sum(sq_sum);
+      if ((tid & 31) == 0) red[tid >> 5] = sq_sum;
+      __syncthreads();
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < (DV + 31) / 32; ++w) tot += red[w];
+      if (tid < DV) {
+        const float inv = rsqrtf(tot / (float)DV + eps);
+        const float wj = norm_w ? norm_w[tid] : 1.f;
+        o = o * inv * wj * sigmoidf_(to_f32(gate[rv + tid]));
+      }
+    }
+    if (tid < DV) out[rv + tid] = from_f32<Tout>(o);
+    if (t + 1 < count) __syncthreads();  // shared inputs of the next token
   }
-  if (tid < DV) out[rv + tid] = from_f32<Tout>(o);
+
+  if (commit) {
+#pragma unroll
+    for (int i = 0; i < RPG; ++i)
+      __stcs(reinterpret_cast<float4*>(S + (size_t)(rg + i * NG) * DV) + cg, s[i]);
+  }
 }
 
 template <int DK, int DV, typename Tin, typename Tout>
@@ -142,8 +164,8 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
   TraceScope ts("kda_decode", st);
   decode_kernel<DK, DV, Tin, Tout><<<rows, kDecodeThreads, 0, st>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g,
-      a.beta, a.state_pool, a.slot_idx, static_cast<Tout*>(a.out), a.H, a.num_slots,
-      static_cast<const Tin*>(a.epi.gate), a.epi.norm_weight, a.epi.eps, a.err);
+      a.beta, a.state_pool, a.slot_idx, static_cast<Tout*>(a.out), a.H, a.num_slots, a.n_tok, a.ntok_per_req,
+      a.commit ? 1 : 0, static_cast<const Tin*>(a.epi.gate), a.epi.norm_weight, a.epi.eps, a.err);
   return cudaGetLastError();
 }
 

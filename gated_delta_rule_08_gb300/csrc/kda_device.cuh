@@ -8,6 +8,7 @@
 #define KDA_DEVERR_BAD_SLOT 0x1u
 #define KDA_DEVERR_BAD_SEQLENS 0x2u
 #define KDA_DEVERR_WAIT_TIMEOUT 0x4u
+#define KDA_DEVERR_BAD_COUNT 0x8u
 
 namespace kda {
 
@@ -82,6 +83,16 @@ __device__ __forceinline__ int64_t sequence_chunks(int b, const int32_t* plan, c
   t_begin = cu[b];
   len = (int64_t)cu[b + 1] - cu[b];
   return (int64_t)plan[b + 1] - plan[b];
+}
+
+// Index of the first state checkpoint of sequence b when every sequence stores one after each
+// `span` of its tokens (span = 64 x checkpoint interval in chunks): the checkpoints of the
+// sequences before b, floor(len / span) each.
+__device__ __forceinline__ int64_t checkpoint_base(int b, const int32_t* cu, int64_t T, int64_t span) {
+  if (cu == nullptr) return (int64_t)b * (T / span);
+  int64_t s = 0;
+  for (int i = 0; i < b; ++i) s += ((int64_t)cu[i + 1] - cu[i]) / span;
+  return s;
 }
 
 }  // namespace kda

@@ -37,6 +37,8 @@ struct PrefillArgs {
   void* workspace;
   size_t workspace_bytes;
   unsigned int* err;          // device error word
+  float* ckpt;                // state checkpoints [n][H][dk][dv] fp32, or null
+  int64_t ckpt_chunks;        // a checkpoint after every ckpt_chunks full chunks of a sequence
 };
 
 struct DecodeArgs {
@@ -49,6 +51,9 @@ struct DecodeArgs {
   const int32_t* slot_idx;
   void* out;
   int N, H, dk, dv, num_slots;
+  int n_tok;                     // tokens per request in the input arrays ([N, n_tok, H, ..])
+  const int32_t* ntok_per_req;   // device [N] tokens to apply per request, or null (= n_tok)
+  bool commit;                   // write the state back after the request's tokens
   bool bf16;
   bool out_bf16;
   Epilogue epi;

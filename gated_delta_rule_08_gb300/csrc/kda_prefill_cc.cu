@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ plan,
               const int32_t* __restrict__ cu, int B, int64_t T, int H, const float* __restrict__ h0,
               float* __restrict__ hT, Tout* __restrict__ out, const Tin* __restrict__ gate,
-              const float* __restrict__ norm_w, float eps) {
+              const float* __restrict__ norm_w, float eps, float* __restrict__ ckpt, int64_t ckpt_chunks) {
   using L = CcBlob<DK, DV>;
   constexpr int PSV = DV + 4, PSK = DK + 4, JB = DV / 64, SI = DK / 16;
   extern __shared__ float4 smem4[];
@@ -257,6 +257,7 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
   const int64_t nchunks = sequence_chunks(b, plan, cu, B, T, first_chunk, t_begin, len);
 
   const size_t soff = ((size_t)b * H + h) * DK * DV;
+  const int64_t ck_base = ckpt != nullptr ? checkpoint_base(b, cu, T, 64 * ckpt_chunks) : 0;
   for (int idx = tid; idx < DK * DV; idx += kThreads) {
     const int r = idx / DV, j = idx % DV;
     sS[r * PSV + j] = h0 ? h0[soff + idx] : 0.f;
@@ -425,6 +426,12 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
           *reinterpret_cast<float4*>(&sS[(rr + 16 * i) * PSV + cc + 64 * jb]) = acc[i][jb];
     }
     __syncthreads();
+    // state checkpoint after every ckpt_chunks full chunks (sS is next written by step g of a
+    // later chunk, after further barriers)
+    if (ckpt != nullptr && (c + 1) % ckpt_chunks == 0 && (c + 1) * 64 <= len) {
+      float* dst = ckpt + ((size_t)(ck_base + (c + 1) / ckpt_chunks - 1) * H + h) * DK * DV;
+      for (int idx = tid; idx < DK * DV; idx += kThreads) dst[idx] = sS[(idx / DV) * PSV + idx % DV];
+    }
   }
 
   if (hT != nullptr)
@@ -510,7 +517,7 @@ cudaError_t launch_cc(const PrefillArgs& a, cudaStream_t st) {
   TraceScope ts("kda_chunk_scan_cc", st);
   chunk_scan_cc<DK, DV, Tin, Tout><<<grid2, kThreads, scan_smem, st>>>(
       blob, plan, a.cu_seqlens, a.B, a.T, a.H, a.h0, a.hT, static_cast<Tout*>(a.out),
-      static_cast<const Tin*>(a.epi.gate), a.epi.norm_weight, a.epi.eps);
+      static_cast<const Tin*>(a.epi.gate), a.epi.norm_weight, a.epi.eps, a.ckpt, a.ckpt_chunks);
   return cudaGetLastError();
 }
 

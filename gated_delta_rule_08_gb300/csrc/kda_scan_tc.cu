@@ -72,6 +72,8 @@ struct ScanParams {
   int nseg;
   int64_t seg_len;  // chunks per segment
   float* cp;        // [B][H][nseg][3][128][128]: P_p, b_p, S_in(p)
+  float* ckpt;      // state checkpoints [n][H][128][128] fp32, or null (read-out pass only)
+  int64_t ckpt_chunks;
 };
 
 __device__ __forceinline__ void tmem_ld64b(uint32_t taddr, float* v) {
@@ -104,7 +106,7 @@ __device__ __forceinline__ void tmem_st64h(uint32_t taddr, const float* v) {
   tmem_st32u(taddr, a);
 }
 
-template <typename Tout, int MODE>
+template <typename Tout, int MODE, bool CKPT>
 __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -217,6 +219,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
   } else if (warp < 8) {
     // ======================== state warps: TMEM lane quadrant warp & 3, column half hc
     const int hc = warp >> 2;
+    // state checkpoints (CKPT): after every ckpt_chunks full chunks of the sequence
+    const int64_t ck_base = CKPT ? checkpoint_base(b, p.cu, p.T, 64 * p.ckpt_chunks) : 0;
+    int64_t ck_next = CKPT ? (c_begin / p.ckpt_chunks + 1) * p.ckpt_chunks : 0;  // next boundary (chunks done)
     bool ok = true;
     {
       const float* init = nullptr;
@@ -288,21 +293,38 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
       ok = wait_or_abort(bar_s, (uint32_t)(c & 1), abort_flag);
       if (!ok) break;
       tc_fence_after();
-      if (c + 1 < ncs) {
+      bool ckpt_now = false;
+      if constexpr (CKPT) {
+        const int64_t cg1 = c_begin + c + 1;  // chunks of the sequence done
+        if (cg1 == ck_next) {
+          ckpt_now = cg1 * 64 <= len;  // full chunks only
+          ck_next += p.ckpt_chunks;
+        }
+      }
+      if (c + 1 < ncs || ckpt_now) {
         float s[64];
         tmem_ld64b(tl + T_S + 64 * hc, s);
-        tmem_st64h(tl + T_S16 + 32 * hc, s);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(s16_ready);
-        const int st1 = (int)((c + 1) % kStages);
-        ok = wait_or_abort(&full[st1], (uint32_t)(((c + 1) / kStages) & 1), abort_flag);
-        if (!ok) break;
-        const float* gc = reinterpret_cast<const float*>(sm + st1 * kStage + kRecGC) + 64 * hc;
+        if (c + 1 < ncs) {
+          tmem_st64h(tl + T_S16 + 32 * hc, s);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(s16_ready);
+        }
+        if (ckpt_now) {
+          float* dst = p.ckpt + ((size_t)(ck_base + (ck_next - p.ckpt_chunks) / p.ckpt_chunks - 1) * H + h) * kCpMat;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) s[j] *= gc[j];
-        tmem_st64f(tl + T_S + 64 * hc, s);
-        tmem_wait_st();
+          for (int j = 0; j < 64; ++j) dst[(size_t)(64 * hc + j) * 128 + row] = s[j];
+        }
+        if (c + 1 < ncs) {
+          const int st1 = (int)((c + 1) % kStages);
+          ok = wait_or_abort(&full[st1], (uint32_t)(((c + 1) / kStages) & 1), abort_flag);
+          if (!ok) break;
+          const float* gc = reinterpret_cast<const float*>(sm + st1 * kStage + kRecGC) + 64 * hc;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) s[j] *= gc[j];
+          tmem_st64f(tl + T_S + 64 * hc, s);
+          tmem_wait_st();
+        }
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) uh[j] = uh_next[j];
@@ -439,10 +461,12 @@ cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int3
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout, 0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kScanSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+    e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout, 0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
@@ -451,10 +475,11 @@ cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int3
   p.h0 = a.h0; p.hT = a.hT; p.out = a.out; p.gate = static_cast<const __nv_bfloat16*>(a.epi.gate);
   p.norm_w = a.epi.norm_weight; p.eps = a.epi.eps; p.err = a.err;
   p.nseg = nseg; p.seg_len = seg_len; p.cp = cp;
+  p.ckpt = a.ckpt; p.ckpt_chunks = a.ckpt_chunks;
   if (nseg > 1) {
     {
       TraceScope ts("kda_tc_chunk_scan_transition", st);
-      kda_tc_chunk_scan<Tout, 1><<<dim3((unsigned)a.B, (unsigned)a.H, (unsigned)(2 * (nseg - 1))), kScanThreads,
+      kda_tc_chunk_scan<Tout, 1, false><<<dim3((unsigned)a.B, (unsigned)a.H, (unsigned)(2 * (nseg - 1))), kScanThreads,
                                    kScanSmem, st>>>(p);
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
@@ -467,7 +492,9 @@ cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int3
     }
   }
   TraceScope ts("kda_tc_chunk_scan", st);
-  kda_tc_chunk_scan<Tout, 0><<<dim3((unsigned)a.B, (unsigned)a.H, (unsigned)nseg), kScanThreads, kScanSmem, st>>>(p);
+  const dim3 grid((unsigned)a.B, (unsigned)a.H, (unsigned)nseg);
+  if (a.ckpt != nullptr) kda_tc_chunk_scan<Tout, 0, true><<<grid, kScanThreads, kScanSmem, st>>>(p);
+  else kda_tc_chunk_scan<Tout, 0, false><<<grid, kScanThreads, kScanSmem, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -63,6 +63,7 @@ class DecodeConfig:
     state_std: float = 0.1
     epilogue: bool = True
     seed: int = 4
+    n_tok: int = 1  # tokens per request (> 1: the multi-token layout [N, n_tok, H, ..])
 
 
 # The hot path's workloads.
@@ -154,12 +155,13 @@ def decode_inputs(cfg: DecodeConfig, device="cpu") -> dict:
     gen = _gen(cfg.seed, device)
     dt = _TORCH_DTYPE[cfg.dtype]
     f32 = dict(device=device, dtype=torch.float32)
-    q = _unit(torch.randn(cfg.N, cfg.H, cfg.dk, generator=gen, **f32)).to(dt)
-    k = _unit(torch.randn(cfg.N, cfg.H, cfg.dk, generator=gen, **f32)).to(dt)
-    v = torch.randn(cfg.N, cfg.H, cfg.dv, generator=gen, **f32).to(dt)
-    beta = torch.sigmoid(torch.randn(cfg.N, cfg.H, generator=gen, **f32))
-    g = -5.0 * torch.sigmoid(torch.randn(cfg.N, cfg.H, cfg.dk, generator=gen, **f32) + cfg.z_mean)
-    gate = torch.randn(cfg.N, cfg.H, cfg.dv, generator=gen, **f32).to(dt) if cfg.epilogue else None
+    lead = (cfg.N, cfg.H) if cfg.n_tok == 1 else (cfg.N, cfg.n_tok, cfg.H)
+    q = _unit(torch.randn(*lead, cfg.dk, generator=gen, **f32)).to(dt)
+    k = _unit(torch.randn(*lead, cfg.dk, generator=gen, **f32)).to(dt)
+    v = torch.randn(*lead, cfg.dv, generator=gen, **f32).to(dt)
+    beta = torch.sigmoid(torch.randn(*lead, generator=gen, **f32))
+    g = -5.0 * torch.sigmoid(torch.randn(*lead, cfg.dk, generator=gen, **f32) + cfg.z_mean)
+    gate = torch.randn(*lead, cfg.dv, generator=gen, **f32).to(dt) if cfg.epilogue else None
     pool = torch.empty(cfg.num_slots, cfg.H, cfg.dk, cfg.dv, **f32)
     for s0 in range(0, cfg.num_slots, 64):  # bounded temporaries
         s1 = min(cfg.num_slots, s0 + 64)

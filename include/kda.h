@@ -55,6 +55,7 @@ typedef enum {
 #define KDA_DEVERR_BAD_SLOT     0x1u  /* decode: slot_idx[n] outside [0, num_slots)        */
 #define KDA_DEVERR_BAD_SEQLENS  0x2u  /* prefill: cu_seqlens not non-decreasing in [0, T]  */
 #define KDA_DEVERR_WAIT_TIMEOUT 0x4u  /* a bounded device-side wait gave up                */
+#define KDA_DEVERR_BAD_COUNT    0x8u  /* decode_multi: ntok_per_req[n] outside [0, n_tok]   */
 
 /* Optional fused epilogue (section 3.3, Eq. 6): RMSNorm over dv per (token, head), then
  * the sigmoid output gate.  The norm is taken on the fp32 read-out before rounding.
@@ -99,6 +100,24 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const floa
                          kda_dtype dtype, kda_dtype out_dtype, const kda_epilogue* epi,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/* kda_chunk_fwd that also stores intermediate states for a prefix cache (section 13.9: the KDA
+ * path of the prefix cache can only resume at checkpoints stored at the 512-token hash-block
+ * endpoints, i.e. ckpt_chunks = 8).  Sequence b stores its fp32 state after each
+ * span = 64 * ckpt_chunks of its tokens: after tokens span, 2 span, ..., floor(len_b / span) span
+ * (a checkpoint at the sequence end equals hT).
+ *   states      : [n_ckpt, H, dk, dv] fp32 device, 16-byte aligned, written (not read), where
+ *                 n_ckpt = sum_b floor(len_b / span); sequence b's checkpoints start at index
+ *                 sum_{b' < b} floor(len_b' / span), in token order
+ *   ckpt_chunks : >= 1
+ * Every other argument, result and error is that of kda_chunk_fwd (states == NULL or
+ * ckpt_chunks < 1: KDA_ERR_INVALID_ARG). */
+kda_status kda_chunk_fwd_checkpoints(const void* q, const void* k, const void* v, const float* g,
+                                     const float* beta, const float* h0, const int32_t* cu_seqlens,
+                                     void* out, float* hT, float* states, int64_t ckpt_chunks, int B,
+                                     int64_t T, int H, int dk, int dv, int C, kda_dtype dtype,
+                                     kda_dtype out_dtype, const kda_epilogue* epi, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
 /* One recurrent decode step for N requests, one token each, on a pool of fp32 states
  * updated in place (section 13.9 prefix cache: one fixed-size state per request in a
  * pooled layout; section 13.10: state update and read-out in a single fused kernel).
@@ -116,6 +135,30 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const fl
                            void* out, int N, int H, int dk, int dv, int num_slots,
                            kda_dtype dtype, kda_dtype out_dtype, const kda_epilogue* epi,
                            void* stream);
+
+/* Several tokens per request on the pooled states: the verify and accept steps of speculative
+ * decoding (section 13.4: an in-place update cannot be rolled back once a draft token is
+ * rejected, so verification must leave the pooled state untouched and the accepted tokens are
+ * applied afterwards from their cached inputs).
+ *   q, k       : [N, n_tok, H, dk] (dtype);  v : [N, n_tok, H, dv] (dtype)
+ *   g          : [N, n_tok, H, dk] fp32;     beta : [N, n_tok, H] fp32
+ *   gate (epi) : [N, n_tok, H, dv] (dtype)
+ *   state_pool, slot_idx : as for kda_decode_step
+ *   ntok_per_req : device int32 [N], tokens to apply to request n (its first ntok_per_req[n]
+ *                tokens, in order), or NULL meaning all n_tok.  A value outside [0, n_tok] sets
+ *                KDA_DEVERR_BAD_COUNT and that request is skipped (out and state untouched).
+ *   out        : [N, n_tok, H, dv] (out_dtype); rows of tokens not applied are not written
+ *   commit     : 0 = verify: the pool is only read; 1 = accept: the state of each request after
+ *                its applied tokens is written back to its slot (a request with 0 tokens keeps
+ *                its state).  Token t of a request sees exactly the state after its tokens < t,
+ *                so outputs of a verify call and of the accepting call agree on the tokens both
+ *                apply.
+ * kda_decode_step(...) is kda_decode_multi(..., ntok_per_req = NULL, N, n_tok = 1, ..., commit = 1). */
+kda_status kda_decode_multi(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, float* state_pool, const int32_t* slot_idx,
+                            const int32_t* ntok_per_req, void* out, int N, int n_tok, int H, int dk,
+                            int dv, int num_slots, int commit, kda_dtype dtype, kda_dtype out_dtype,
+                            const kda_epilogue* epi, void* stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error word into
  * *flags (KDA_DEVERR_* bits).  Returns KDA_OK, or KDA_ERR_CUDA if the sync failed. */

@@ -91,3 +91,21 @@ def test_bad_arguments_rejected_without_launch(lib):
                                None) == 1
     assert lib.kda_decode_step(fake, fake, fake, fake, fake, fake, fake, fake, -4, 2, 128, 128, 8, 0, 0, None,
                                None) == 1
+
+
+def test_multi_token_and_checkpoint_arguments_rejected_without_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    # decode_multi: negative token count, null values, unsupported dims
+    assert lib.kda_decode_multi(fake, fake, fake, fake, fake, fake, fake, None, fake, 4, -1, 2, 128, 128, 8, 1, 0, 0,
+                                None, None) == 1
+    assert lib.kda_decode_multi(fake, fake, None, fake, fake, fake, fake, None, fake, 4, 3, 2, 128, 128, 8, 0, 0, 0,
+                                None, None) == 1
+    assert lib.kda_decode_multi(fake, fake, fake, fake, fake, fake, fake, None, fake, 4, 3, 2, 128, 96, 8, 0, 0, 0,
+                                None, None) == 2
+    # checkpoints: no state buffer, interval < 1, misaligned buffer
+    args = (fake, fake, fake, fake, fake, None, None, P(0x2000), None)
+    tail = (1, 64, 1, 128, 128, 64, 0, 0, None, fake, 1 << 20, None)
+    assert lib.kda_chunk_fwd_checkpoints(*args, None, 8, *tail) == 1
+    assert lib.kda_chunk_fwd_checkpoints(*args, P(0x4000), 0, *tail) == 1
+    assert lib.kda_chunk_fwd_checkpoints(*args, P(0x4004), 8, *tail) == 1

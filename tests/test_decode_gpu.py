@@ -89,3 +89,97 @@ def test_decode_zero_requests_is_a_no_op():
                                   torch.empty(0, dtype=torch.int32, device="cuda"))
     assert out.shape == (0, 2, 64)
     assert_no_device_error()
+
+
+# ------------------------------------------------------------------ several tokens per request
+def _multi(cfg, n_tok):
+    return inputs.decode_inputs(dataclasses.replace(cfg, n_tok=n_tok), device="cuda")
+
+
+def _oracle_multi(inp, counts, epilogue, pool_before):
+    """The single-step oracle applied token by token to the touched states of `pool_before`:
+    request n takes its first counts[n] tokens.  Returns (out [N, n_tok, H, dv] with NaN where no
+    token applied, final touched states [N, H, dk, dv])."""
+    N, n_tok = inp["q"].shape[:2]
+    pool = pool_before[inp["slot_idx"].long()].clone()
+    outs = np.full((N, n_tok) + tuple(inp["v"].shape[2:]), np.nan)
+    for t in range(n_tok):
+        slots = np.array([n if counts[n] > t else -1 for n in range(N)])
+        tok = {x: inp[x][:, t] for x in ("q", "k", "v", "g", "beta")}
+        gate = inp["gate"][:, t] if epilogue else None
+        nw = inp["norm_weight"] if epilogue else None
+        o, pool, _ = oracle_kda_decode(tok["q"], tok["k"], tok["v"], tok["g"], tok["beta"], pool, slots, gate=gate,
+                                       norm_weight=nw)
+        live = slots >= 0
+        outs[live, t] = o[live]
+    return outs, pool
+
+
+@pytest.mark.parametrize("dk,dv,dtype", [(128, 128, "bf16"), (64, 128, "fp32"), (128, 64, "bf16")])
+def test_decode_multi_verify_leaves_the_pool_untouched(dk, dv, dtype):
+    """Speculative-decode verify: every draft token of every request is applied in order to a
+    private copy of the state; outputs match the oracle, the pool is byte-identical."""
+    cfg = dataclasses.replace(inputs.DECODE, N=6, H=3, dk=dk, dv=dv, num_slots=11, dtype=dtype, seed=90 + dk + dv)
+    inp = _multi(cfg, 4)
+    before = inp["state_pool"].clone()
+    out = binding.kda_decode_multi(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state_pool"],
+                                   inp["slot_idx"], commit=False, gate=inp["gate"], norm_weight=inp["norm_weight"])
+    assert_no_device_error()
+    assert torch.equal(inp["state_pool"], before)
+    ref_out, _ = _oracle_multi(inp, [4] * cfg.N, True, before)
+    assert parity_err(out, ref_out) <= TOL[inputs.torch_dtype(dtype)]
+
+
+def test_decode_multi_accept_commits_exactly_the_accepted_prefix():
+    """Accept: request n re-applies its first accept[n] tokens and writes that state back; its
+    outputs equal the verify outputs bit for bit; rows of rejected tokens are not written."""
+    cfg = dataclasses.replace(inputs.DECODE, N=6, H=4, num_slots=13, seed=95)
+    inp = _multi(cfg, 4)
+    before = inp["state_pool"].clone()
+    kw = dict(gate=inp["gate"], norm_weight=inp["norm_weight"])
+    verify = binding.kda_decode_multi(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state_pool"],
+                                      inp["slot_idx"], commit=False, **kw)
+    accept = [0, 1, 2, 3, 4, 2]
+    counts = torch.tensor(accept, dtype=torch.int32, device="cuda")
+    out = torch.full_like(verify, 5.0)
+    binding.kda_decode_multi(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state_pool"], inp["slot_idx"],
+                             counts, out=out, commit=True, **kw)
+    assert_no_device_error()
+    for n, a in enumerate(accept):
+        assert torch.equal(out[n, :a], verify[n, :a])
+        assert torch.all(out[n, a:] == 5.0)
+    ref_out, ref_states = _oracle_multi(inp, accept, True, before)
+    slots = inp["slot_idx"].long()
+    assert rel_err(inp["state_pool"][slots], ref_states) <= 1e-5
+    assert torch.equal(inp["state_pool"][slots[0]], before[slots[0]])  # nothing accepted: state kept
+    untouched = torch.ones(cfg.num_slots, dtype=torch.bool, device="cuda")
+    untouched[slots] = False
+    assert torch.equal(inp["state_pool"][untouched], before[untouched])
+
+
+def test_decode_multi_one_token_is_the_decode_step():
+    cfg = dataclasses.replace(inputs.DECODE, N=9, H=2, num_slots=20, seed=97)
+    a = inputs.decode_inputs(cfg, device="cuda")
+    b = inputs.decode_inputs(cfg, device="cuda")
+    kw_a = dict(gate=a["gate"], norm_weight=a["norm_weight"])
+    oa = binding.kda_decode_step(a["q"], a["k"], a["v"], a["g"], a["beta"], a["state_pool"], a["slot_idx"], **kw_a)
+    ob = binding.kda_decode_multi(b["q"][:, None], b["k"][:, None], b["v"][:, None], b["g"][:, None],
+                                  b["beta"][:, None], b["state_pool"], b["slot_idx"], commit=True,
+                                  gate=b["gate"][:, None], norm_weight=b["norm_weight"])
+    assert torch.equal(oa, ob[:, 0]) and torch.equal(a["state_pool"], b["state_pool"])
+
+
+def test_decode_multi_bad_count_sets_flag_and_skips_request():
+    cfg = dataclasses.replace(inputs.DECODE, N=3, H=2, num_slots=5, seed=98)
+    inp = _multi(cfg, 2)
+    before = inp["state_pool"].clone()
+    counts = torch.tensor([1, 3, -1], dtype=torch.int32, device="cuda")
+    out = torch.full((3, 2, 2, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    binding.kda_decode_multi(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state_pool"], inp["slot_idx"],
+                             counts, out=out, commit=True)
+    assert binding.kda_get_device_error() & binding.DEVERR_BAD_COUNT
+    slots = inp["slot_idx"].long()
+    assert torch.all(out[1] == 7.0) and torch.all(out[2] == 7.0) and torch.all(out[0, 1] == 7.0)
+    assert torch.equal(inp["state_pool"][slots[1]], before[slots[1]])
+    assert torch.equal(inp["state_pool"][slots[2]], before[slots[2]])
+    assert not torch.equal(inp["state_pool"][slots[0]], before[slots[0]])

@@ -220,3 +220,42 @@ def test_sequence_split_across_sms_matches_oracle(lengths, H, epilogue, z_mean):
     cfg = inputs.PrefillConfig("cp", H=H, dk=128, dv=128, dtype="bf16", lengths=lengths, B=len(lengths),
                                h0_std=0.1, epilogue=epilogue, z_mean=z_mean, seed=309)
     _check(cfg, epilogue=epilogue, device_gen=True)
+
+
+# ------------------------------------------------------------------ prefix-cache checkpoints
+@pytest.mark.parametrize("lengths,H,dk,dtype,ckpt_chunks,z_mean", [
+    ((700, 1300, 64, 2000), 2, 128, "bf16", 4, 0.0),   # tensor-core path, varlen
+    ((700, 1300, 64, 2000), 2, 64, "fp32", 4, 0.0),    # CUDA-core path
+    ((8192,), 4, 128, "bf16", 8, -8.0),                # split into segments, slow decay
+])
+def test_checkpoints_match_the_oracle_on_each_prefix(lengths, H, dk, dtype, ckpt_chunks, z_mean):
+    """Each stored state equals the oracle's final state on the sequence's prefix of
+    j * 64 * ckpt_chunks tokens (from h0); out and hT are unchanged by storing them."""
+    cfg = inputs.PrefillConfig("ckpt", H=H, dk=dk, dv=dk, dtype=dtype, lengths=lengths, B=len(lengths), h0_std=0.1,
+                               z_mean=z_mean, seed=321)
+    inp = inputs.prefill_inputs(cfg, device="cuda")
+    kw = dict(h0=inp["h0"], cu_seqlens=inp["cu_seqlens"], B=len(lengths))
+    out0, hT0 = binding.kda_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], **kw)
+    out, hT, states = binding.kda_chunk_fwd_checkpoints(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                                        ckpt_chunks=ckpt_chunks, **kw)
+    assert_no_device_error()
+    assert torch.equal(out, out0) and torch.equal(hT, hT0)
+    span = 64 * ckpt_chunks
+    # the checkpoint prefixes as one packed batch for the oracle
+    starts = inp["cu_seqlens"].to("cpu").tolist()
+    pieces, h0s = [], []
+    for b, L in enumerate(lengths):
+        for j in range(1, L // span + 1):
+            pieces.append((starts[b], starts[b] + j * span))
+            h0s.append(inp["h0"][b])
+    assert states.shape[0] == len(pieces)
+    sl = lambda x: torch.cat([inp[x][a:e] for a, e in pieces])
+    cu = torch.tensor([0] + list(np.cumsum([e - a for a, e in pieces])), dtype=torch.int64)
+    _, ref = oracle_kda_prefill(sl("q"), sl("k"), sl("v"), sl("g"), sl("beta"), h0=torch.stack(h0s), cu_seqlens=cu)
+    assert rel_err(states, ref) <= TOL[inputs.torch_dtype(dtype)]
+    # a checkpoint at a sequence's end is its final state
+    idx = 0
+    for b, L in enumerate(lengths):
+        idx += L // span
+        if L % span == 0 and L // span > 0:
+            assert torch.equal(states[idx - 1], hT[b])
