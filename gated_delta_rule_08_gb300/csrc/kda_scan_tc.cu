@@ -26,7 +26,7 @@
 //    MODE 0 (read-out): warps 8-11 drain D_O through a staging buffer and run the optional
 //      RMSNorm + gate epilogue, off the serial path;
 //    MODE 1 (transition): z = 2 p + kind; kind 0 runs b_p, kind 1 runs P_p; no read-out.
-//  kda_cp_merge (grid = sequences x heads x 8 column slices): the sequential segment merge in fp32.
+//  kda_cp_merge (grid = sequences x heads x 4 column slices): the sequential segment merge in fp32.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -165,11 +165,23 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
     if (lane == 0) {
       int64_t last_load = -1, consumed = -1;
       bool ok = true;
-      for (int64_t c = 0; c < 2 && c < ncs; ++c) {
-        mbar_arrive_expect_tx(&full[c], kRecStage);
-        bulk_g2s(sm + c * kStage, rec0 + (size_t)c * rec_stride, kRecStage, &full[c]);
+      // the read-out pass stages the whole operand part of a record; the transitions use only
+      // W^T, K_bar^T and e^{G_C}
+      auto stage_record = [&](int64_t c) {
+        const int s2 = (int)(c % kStages);
+        const uint8_t* src = rec0 + (size_t)c * rec_stride;
+        uint8_t* dst = sm + s2 * kStage;
+        if (MODE == 0) {
+          mbar_arrive_expect_tx(&full[s2], kRecStage);
+          bulk_g2s(dst, src, kRecStage, &full[s2]);
+        } else {
+          mbar_arrive_expect_tx(&full[s2], (kRecQT - kRecWT) + (kRecStage - kRecKT));
+          bulk_g2s(dst + kRecWT, src + kRecWT, kRecQT - kRecWT, &full[s2]);
+          bulk_g2s(dst + kRecKT, src + kRecKT, kRecStage - kRecKT, &full[s2]);
+        }
         last_load = c;
-      }
+      };
+      for (int64_t c = 0; c < 2 && c < ncs; ++c) stage_record(c);
       const uint32_t id1 = MODE == 0 ? idesc_f16(128, 128, false, true) : idesc_f16(128, 64, false, true);
       const uint32_t id2 = MODE == 0 ? idesc_f16(128, 192, false, false) : idesc_f16(128, 128, false, false);
       for (int64_t c = 0; c < ncs && ok; ++c) {
@@ -179,10 +191,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
           // chunk c+2 goes where chunk c-1 was: free once that chunk's products are done
           if (c >= 1) ok = wait_or_abort(bar_s, (uint32_t)((c - 1) & 1), abort_flag);
           if (!ok) break;
-          const int s2 = (int)((c + 2) % kStages);
-          mbar_arrive_expect_tx(&full[s2], kRecStage);
-          bulk_g2s(sm + s2 * kStage, rec0 + (size_t)(c + 2) * rec_stride, kRecStage, &full[s2]);
-          last_load = c + 2;
+          stage_record(c + 2);
         }
         ok = wait_or_abort(&full[st], (uint32_t)((c / kStages) & 1), abort_flag);
         if (ok) consumed = c;
@@ -402,55 +411,82 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// Segment merge: S_in(p+1) = P_p S_in(p) + b_p for p < p_last, fp32, on a 16-column slice.
+// Segment merge: S_in(p+1) = P_p S_in(p) + b_p for p < p_last, fp32, on a 32-column slice of the
+// state per CTA.  P_p (64 KB) is staged into shared memory by bulk copies one step ahead; warp w
+// computes rows 16 w .. 16 w + 15 of the slice, lane = column, so P is read as broadcast float4s
+// and the state slice column-wise without bank conflicts.
 constexpr int kMergeThreads = 256;
-__global__ void __launch_bounds__(kMergeThreads) kda_cp_merge(const ScanParams p) {
-  __shared__ __align__(16) float sS[128][16];
-  const int b = blockIdx.x, h = blockIdx.y, j0 = 16 * blockIdx.z, tid = threadIdx.x;
+constexpr int kMergeCols = 32;
+constexpr uint32_t kMergeSmem = 2 * 65536 + 128 * kMergeCols * 4 + 64;
+__global__ void __launch_bounds__(kMergeThreads, 1) kda_cp_merge(const ScanParams p) {
+  extern __shared__ __align__(128) uint8_t msm[];
+  float* sP = reinterpret_cast<float*>(msm);                        // [2][128][128]
+  float* sS = reinterpret_cast<float*>(msm + 2 * 65536);            // [128][kMergeCols]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(msm + 2 * 65536 + 128 * kMergeCols * 4);  // [2]
+  const int b = blockIdx.x, h = blockIdx.y, j0 = kMergeCols * blockIdx.z, tid = threadIdx.x;
+  const int lane = tid & 31, rg = tid >> 5;
   if (p.cu != nullptr && p.plan[p.B + 1] == 0) return;
   int64_t first_chunk, t_begin, len;
   const int64_t nchunks = sequence_chunks(b, p.plan, p.cu, p.B, p.T, first_chunk, t_begin, len);
   const int64_t p_last = nchunks > 0 ? (nchunks - 1) / p.seg_len : 0;
+  if (p_last == 0) return;
   const size_t soff = ((size_t)b * p.H + h) * kCpMat;
   float* cp = p.cp + (size_t)(b * p.H + h) * p.nseg * 3 * kCpMat;
-  for (int i = tid; i < 128 * 16; i += kMergeThreads) {
-    const int r = i >> 4, c = i & 15;
-    sS[r][c] = p.h0 ? p.h0[soff + (size_t)r * 128 + j0 + c] : 0.f;
+  int64_t issued = 0;
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    mbar_fence_init();
+    for (; issued < 2 && issued < p_last; ++issued) {
+      mbar_arrive_expect_tx(&bar[issued], 65536);
+      bulk_g2s(sP + issued * 16384, cp + (size_t)issued * 3 * kCpMat, 65536, &bar[issued]);
+    }
+  }
+  for (int i = tid; i < 128 * kMergeCols; i += kMergeThreads) {
+    const int r = i / kMergeCols, c = i % kMergeCols;
+    sS[i] = p.h0 ? p.h0[soff + (size_t)r * 128 + j0 + c] : 0.f;
   }
   __syncthreads();
-  const int r = tid >> 1, cb = (tid & 1) * 8;  // this thread: row r, columns cb..cb+7 of the slice
+  bool ok = true;
   for (int64_t s = 0; s < p_last; ++s) {
-    const float* P = cp + (size_t)s * 3 * kCpMat;
-    const float* bo = P + kCpMat;
-    float acc[8];
+    const int buf = (int)(s & 1);
+    ok = __syncthreads_and(mbar_wait(&bar[buf], (uint32_t)((s >> 1) & 1))) != 0;
+    if (!ok) break;
+    const float* P = sP + buf * 16384 + (rg * 16) * 128;
+    const float* bo = cp + (size_t)s * 3 * kCpMat + kCpMat;
+    float acc[16];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = bo[(size_t)r * 128 + j0 + cb + e];
-    for (int k0 = 0; k0 < 128; k0 += 32) {
-      // P row r, columns k0..k0+31 (each row is read by the two threads of that row)
-      float prow[32];
+    for (int j = 0; j < 16; ++j) acc[j] = bo[(size_t)(rg * 16 + j) * 128 + j0 + lane];
+#pragma unroll 2
+    for (int k = 0; k < 128; k += 4) {
+      const float s0 = sS[k * kMergeCols + lane], s1 = sS[(k + 1) * kMergeCols + lane];
+      const float s2 = sS[(k + 2) * kMergeCols + lane], s3 = sS[(k + 3) * kMergeCols + lane];
 #pragma unroll
-      for (int kk = 0; kk < 32; kk += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(P + (size_t)r * 128 + k0 + kk);
-        prow[kk] = v.x; prow[kk + 1] = v.y; prow[kk + 2] = v.z; prow[kk + 3] = v.w;
-      }
-#pragma unroll
-      for (int kk = 0; kk < 32; ++kk) {
-        const float4 s0 = *reinterpret_cast<const float4*>(&sS[k0 + kk][cb]);
-        const float4 s1 = *reinterpret_cast<const float4*>(&sS[k0 + kk][cb + 4]);
-        acc[0] = fmaf(prow[kk], s0.x, acc[0]); acc[1] = fmaf(prow[kk], s0.y, acc[1]);
-        acc[2] = fmaf(prow[kk], s0.z, acc[2]); acc[3] = fmaf(prow[kk], s0.w, acc[3]);
-        acc[4] = fmaf(prow[kk], s1.x, acc[4]); acc[5] = fmaf(prow[kk], s1.y, acc[5]);
-        acc[6] = fmaf(prow[kk], s1.z, acc[6]); acc[7] = fmaf(prow[kk], s1.w, acc[7]);
+      for (int j = 0; j < 16; ++j) {
+        const float4 pv = *reinterpret_cast<const float4*>(P + j * 128 + k);
+        acc[j] = fmaf(pv.x, s0, fmaf(pv.y, s1, fmaf(pv.z, s2, fmaf(pv.w, s3, acc[j]))));
       }
     }
+    fence_proxy_async_smem();  // reads of this P buffer precede the next bulk copy into it
     __syncthreads();
+    if (tid == 0 && issued < p_last) {
+      mbar_arrive_expect_tx(&bar[buf], 65536);
+      bulk_g2s(sP + buf * 16384, cp + (size_t)issued * 3 * kCpMat, 65536, &bar[buf]);
+      ++issued;
+    }
     float* sin_next = cp + ((size_t)(s + 1) * 3 + 2) * kCpMat;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      sS[r][cb + e] = acc[e];
-      sin_next[(size_t)r * 128 + j0 + cb + e] = acc[e];
+    for (int j = 0; j < 16; ++j) {
+      const int r = rg * 16 + j;
+      sS[r * kMergeCols + lane] = acc[j];
+      sin_next[(size_t)r * 128 + j0 + lane] = acc[j];
     }
     __syncthreads();
+  }
+  if (!ok && tid == 0) {
+    atomicOr(p.err, KDA_DEVERR_WAIT_TIMEOUT);
+    // let the copies in flight land (bounded) before the CTA's shared memory is released
+    for (int64_t s = 0; s < issued; ++s) mbar_wait(&bar[s & 1], (uint32_t)((s >> 1) & 1), 1u << 16);
   }
 }
 
@@ -467,6 +503,8 @@ cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int3
     e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout, 0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kda_cp_merge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMergeSmem);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
@@ -486,7 +524,7 @@ cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int3
     }
     {
       TraceScope ts("kda_cp_merge", st);
-      kda_cp_merge<<<dim3((unsigned)a.B, (unsigned)a.H, 8), kMergeThreads, 0, st>>>(p);
+      kda_cp_merge<<<dim3((unsigned)a.B, (unsigned)a.H, 128 / kMergeCols), kMergeThreads, kMergeSmem, st>>>(p);
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
