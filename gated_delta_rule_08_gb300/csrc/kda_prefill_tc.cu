@@ -59,6 +59,8 @@ constexpr uint32_t O_SA = 0;             // fp32 A [64][65]
 constexpr uint32_t O_SX = 16640;         // fp32 X = (I + A)^-1 [64][65]
 constexpr uint32_t O_SY = 33280;         // fp32 scratch: three warps x [16][17]
 constexpr uint32_t O_TT = 37888;         // fp16 T [64 r][64 s] row format (1024-aligned)
+constexpr uint32_t O_MST = 47104;        // M staged for its bulk copy to the record (8 KB)
+// after the W / U_hat MMAs: W^T at 0 and U_hat^T at 16384 staged for their bulk copies
 constexpr uint32_t P_MISC = P_OPS + O_BYTES;
 constexpr uint32_t M_BETA = 0;           // fp32 [2 tasks][64]
 constexpr uint32_t M_TOT = 512;          // float2 [2][16 row groups][16 channel pairs]: group decay sums
@@ -312,6 +314,8 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
       int nh = 0, nn = 0;
       int64_t nt0 = 0, nchunk = 0;
       const int64_t ntask_idx = next_task(task + stride, ntask, stride, plan, cu, B, T, H, nh, nt0, nn, nchunk);
+      // the previous task's bulk copies out of the operand region have read it
+      if (tid == 0) bulk_wait_read_all();
       // every break decision of the compute warps is made together (named barriers follow)
       ok = group_and(1, kCompute, wait_or_abort(full, it & 1, abort_flag));
       if (!ok) break;
@@ -463,13 +467,18 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
           } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) val[j] = (s0 + j <= r) ? val[j] : 0.f;
-            *reinterpret_cast<uint4*>(rec + kRecMM + row_chunk(r, s0 >> 3)) = pack8_h(val);
-            *reinterpret_cast<uint4*>(rec + kRecMM + row_chunk(r, (s0 >> 3) + 1)) = pack8_h(val + 8);
+            *reinterpret_cast<uint4*>(ops + O_MST + row_chunk(r, s0 >> 3)) = pack8_h(val);
+            *reinterpret_cast<uint4*>(ops + O_MST + row_chunk(r, (s0 >> 3) + 1)) = pack8_h(val + 8);
           }
         }
       }
+      fence_proxy_async_smem();
       tc_fence_before();
       group_sync(1, kCompute);
+      if (tid == 0) {  // M to the record in one bulk copy
+        bulk_s2g(rec + kRecMM, ops + O_MST, 8192);
+        bulk_commit();
+      }
 
       // ---- T = (I + A)^-1 Diag(beta), blocked 16 x 16
       {
@@ -554,9 +563,10 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
       if (!ok) break;
       tc_fence_after();
       {
+        // staged in the operand region (free now), then two bulk copies to the record
         const int row = (warp & 3) * 32 + lane;  // dk row (W^T, warps 0-3) or dv row (U_hat^T, warps 4-7)
         const uint32_t ta = tmem_lane(tmem + (warp < 4 ? T_W : T_U), warp);
-        uint8_t* dst = rec + (warp < 4 ? kRecWT : kRecUT);
+        uint8_t* dst = ops + (warp < 4 ? 0 : 16384);
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
           float v[32];
@@ -567,12 +577,20 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
             *reinterpret_cast<uint4*>(dst + row_chunk(row, 4 * part + j)) = pack8_h(v + 8 * j);
         }
       }
+      fence_proxy_async_smem();
       tc_fence_before();
+      group_sync(1, kCompute);
+      if (tid == 0) {
+        bulk_s2g(rec + kRecWT, ops, 16384);
+        bulk_s2g(rec + kRecUT, ops + 16384, 16384);
+        bulk_commit();
+      }
       task = ntask_idx;
       h = nh; n = nn; t0 = nt0; chunk = nchunk;
       ++it;
     }
     if (!ok) *abort_flag = 1;
+    if (tid == 0) bulk_wait_all();  // record bulk copies complete before the CTA exits
   }
 
   tc_fence_before();
