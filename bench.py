@@ -53,6 +53,33 @@ def _peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def source_digest() -> str:
+    """sha256 over the CUDA sources of libkda (names and contents, sorted by name)."""
+    import hashlib
+    d = os.path.join(ROOT, "gated_delta_rule_08_gb300", "csrc")
+    hsh = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            hsh.update(name.encode())
+            with open(os.path.join(d, name), "rb") as f:
+                hsh.update(f.read())
+    return hsh.hexdigest()
+
+
+def measured_traffic() -> dict:
+    """Per-kernel DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
+    committed ncu capture, or {} when the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "kda_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return {}
+    if rec.get("source_sha256") != source_digest():
+        return {}
+    return {k: v["dram_bytes_per_launch"] for k, v in rec.get("kernels", {}).items()}
+
+
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
 
@@ -208,6 +235,7 @@ def run_ours(args, world, rank, local):
     dec_achieved = dec_bytes / (dec_ms_k * 1e-3) / 1e9
     pre_flops = PREFILL_FLOPS_PER_TOKEN_HEAD * T * H
     launches = sum(v[0] for v in trace.values())
+    traffic = measured_traffic()
 
     # end to end through the public API with host buffers: pinned H2D of this step's inputs,
     # the call, D2H of the outputs, every step
@@ -261,10 +289,10 @@ def run_ours(args, world, rank, local):
                    "tokens_per_s": round(dec_steps_per_s * dcfg.N, 1),
                    "ms_per_step": round(dec_s * 1e3 / args.steps, 4),
                    "roofline": {"bound": "hbm", "achieved": round(dec_achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
-                                "frac": round(dec_achieved / hbm_gbs, 4), "traffic": None,
+                                "frac": round(dec_achieved / hbm_gbs, 4), "traffic": traffic.get("kda_decode"),
                                 "kernel": "kda_decode", "peak_kind": peak_kind}},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": round(achieved / hbm_gbs, 4), "traffic": None, "kernel": dom[0],
+                     "frac": round(achieved / hbm_gbs, 4), "traffic": traffic.get(dom[0]), "kernel": dom[0],
                      "kernel_ms": round(dom_ms, 4), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": alg_bytes},
         "prefill_tensor": {"flops_per_step": pre_flops,
