@@ -292,6 +292,27 @@ def run_ours(args, world, rank, local):
     # the pipelined calls computed what the resident-input calls did
     assert torch.equal(out_h[(args.steps - 1) % nb], out.cpu()) and torch.equal(hT_h[(args.steps - 1) % nb], hT.cpu())
 
+    # backward of the prefill recurrence (no epilogue) on the same workload: a first, CUDA-core
+    # version; timed beside the step, not part of the metric
+    gen = torch.Generator(device=dev).manual_seed(11)
+    dout = torch.randn(out.shape, generator=gen, device=dev).to(out.dtype)
+    bws = torch.empty(binding.kda_chunk_bwd_workspace_size(1, T, H, pcfg.dk, pcfg.dv), device=dev, dtype=torch.uint8)
+
+    def backward():
+        return binding.kda_chunk_bwd(P["q"], P["k"], P["v"], P["g"], P["beta"], dout, workspace=bws)
+
+    backward()
+    torch.cuda.synchronize()
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nb_calls = 2
+    b0.record(stream)
+    for _ in range(nb_calls):
+        backward()
+    b1.record(stream)
+    torch.cuda.synchronize()
+    bwd_ms = dist_max(b0.elapsed_time(b1) / nb_calls, world)
+    assert binding.kda_get_device_error(dev) == 0
+
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -325,6 +346,8 @@ def run_ours(args, world, rank, local):
                            "frac": round(pre_flops / (pre_s / args.steps) / 1e12 / bf16_tflops, 4)},
         "kernels": {k: {"launches": v[0], "total_ms": round(v[1], 4)} for k, v in trace.items()},
         "gpu_launches": launches,
+        "backward": {"ms_per_call": round(bwd_ms, 3), "tokens_per_s": round(aggregate(T, world, bwd_ms / 1e3), 1),
+                     "kernel": "kda_bwd_token (fp32 CUDA cores, per-token reverse sweep)"},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),

@@ -6,6 +6,7 @@ the same entry-point names, and the seeded synthetic-input generators.
 """
 from .binding import (  # noqa: F401
     KdaError,
+    kda_chunk_bwd,
     kda_chunk_fwd,
     kda_chunk_fwd_checkpoints,
     kda_chunk_fwd_workspace_size,

@@ -29,7 +29,7 @@ DEVERR_BAD_COUNT = 0x8
 
 # Exported symbols, as declared in include/kda.h.
 EXPORTS = ("kda_chunk_fwd_workspace_size", "kda_chunk_fwd", "kda_decode_step", "kda_decode_multi",
-           "kda_chunk_fwd_checkpoints", "kda_get_device_error",
+           "kda_chunk_fwd_checkpoints", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size", "kda_get_device_error",
            "kda_status_string", "kda_trace_enable", "kda_trace_collect", "kda_chunk_fwd_noalloc",
            "kda_noalloc_scratch_bytes")
 
@@ -70,6 +70,10 @@ def load_library(path: Optional[str] = None):
         lib.kda_chunk_fwd_checkpoints.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I, I64, I, I, I, I, I, I, P, P,
                                                   SZ, P]
         lib.kda_chunk_fwd_checkpoints.restype = I
+        lib.kda_chunk_bwd_workspace_size.argtypes = [I, I64, I, I, I]
+        lib.kda_chunk_bwd_workspace_size.restype = SZ
+        lib.kda_chunk_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, P, SZ, P]
+        lib.kda_chunk_bwd.restype = I
         lib.kda_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
         lib.kda_get_device_error.restype = I
         lib.kda_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, I, I, P, P]
@@ -249,6 +253,53 @@ def kda_decode_step(q, k, v, g, beta, state_pool, slot_idx, out=None, *, gate=No
     if st != 0:
         raise KdaError("kda_decode_step", st)
     return out
+
+
+def kda_chunk_bwd_workspace_size(B: int, T: int, H: int, dk: int, dv: int) -> int:
+    return int(load_library().kda_chunk_bwd_workspace_size(B, T, H, dk, dv))
+
+
+def kda_chunk_bwd(q, k, v, g, beta, dout, h0=None, cu_seqlens=None, dhT=None, *, B: Optional[int] = None,
+                  need_dh0: bool = True, workspace=None):
+    """Gradients of sum <dout, out> + <dhT, hT> for the prefill recurrence (no epilogue).
+    Returns (dq, dk, dv, dg, dbeta, dh0 or None), all fp32."""
+    lib = load_library()
+    dev = q.device
+    T_tot, H, dk = q.shape
+    dv = v.shape[2]
+    dt = q.dtype
+    code = _dtype_code(q)
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, device=dev)
+        B = cu_seqlens.numel() - 1
+        T_arg = T_tot
+    else:
+        B = 1 if B is None else B
+        if T_tot % B:
+            raise ValueError("without cu_seqlens, T_tot must be a multiple of B")
+        T_arg = T_tot // B
+    for name, t, d, shape in (("q", q, dt, (T_tot, H, dk)), ("k", k, dt, (T_tot, H, dk)), ("v", v, dt, (T_tot, H, dv)),
+                              ("g", g, torch.float32, (T_tot, H, dk)), ("beta", beta, torch.float32, (T_tot, H)),
+                              ("dout", dout, dt, (T_tot, H, dv))):
+        _check(t, name, d, shape, dev)
+    _check(h0, "h0", torch.float32, (B, H, dk, dv), dev)
+    _check(dhT, "dhT", torch.float32, (B, H, dk, dv), dev)
+    f32 = dict(device=dev, dtype=torch.float32)
+    dq, dk_, dg = (torch.empty(T_tot, H, dk, **f32) for _ in range(3))
+    dv_ = torch.empty(T_tot, H, dv, **f32)
+    dbeta = torch.empty(T_tot, H, **f32)
+    dh0 = torch.empty(B, H, dk, dv, **f32) if need_dh0 else None
+    need = int(lib.kda_chunk_bwd_workspace_size(B, T_arg, H, dk, dv))
+    if need == 0:
+        raise KdaError("kda_chunk_bwd_workspace_size", 2)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    st = lib.kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_seqlens), _ptr(dout),
+                           _ptr(dhT), _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dg), _ptr(dbeta), _ptr(dh0), B, T_arg, H, dk,
+                           dv, code, _ptr(workspace), workspace.numel(), _stream(dev))
+    if st != 0:
+        raise KdaError("kda_chunk_bwd", st)
+    return dq, dk_, dv_, dg, dbeta, dh0
 
 
 def kda_decode_multi(q, k, v, g, beta, state_pool, slot_idx, ntok_per_req=None, out=None, *, commit: bool,

@@ -145,6 +145,51 @@ KDA_API kda_status kda_chunk_fwd_checkpoints(const void* q, const void* k, const
                           out_dtype, epi, workspace, workspace_bytes, stream);
 }
 
+KDA_API size_t kda_chunk_bwd_workspace_size(int B, int64_t T, int H, int dk, int dv) {
+  if (B <= 0 || T < 0 || H <= 0 || !dims_ok(dk, dv)) return 0;
+  // sized for the larger of the two chunk bounds (with and without cu_seqlens)
+  const size_t a = backward_scratch_bytes(B, T, H, dk, dv, true), b = backward_scratch_bytes(B, T, H, dk, dv, false);
+  return plan_bytes(B) + (a > b ? a : b);
+}
+
+KDA_API kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                 const float* h0, const int32_t* cu_seqlens, const void* dout, const float* dhT,
+                                 float* dq, float* dk_, float* dv_, float* dg, float* dbeta, float* dh0, int B,
+                                 int64_t T, int H, int dk, int dv, kda_dtype dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (B <= 0 || T < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_FP32) return KDA_ERR_UNSUPPORTED;
+  if (!dims_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+  const int64_t T_tot = cu_seqlens ? T : (int64_t)B * T;
+  if (T_tot > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk_ || !dv_ || !dg || !dbeta))
+    return KDA_ERR_INVALID_ARG;
+  if (T_tot > ((int64_t)1 << 31) * 64 / H) return KDA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(dout) || !aligned16(h0) ||
+      !aligned16(dhT) || !aligned16(dq) || !aligned16(dk_) || !aligned16(dv_) || !aligned16(dg) || !aligned16(dh0))
+    return KDA_ERR_INVALID_ARG;
+  const size_t need = kda_chunk_bwd_workspace_size(B, T, H, dk, dv);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return KDA_ERR_WORKSPACE;
+  unsigned int* err = nullptr;
+  int major = 0, minor = 0;
+  kda_status st = device_state(&err, &major, &minor);
+  if (st != KDA_OK) return st;
+  if (major != 10 || minor != 3) return KDA_ERR_UNSUPPORTED;
+  if (T_tot == 0 && dh0 == nullptr) return KDA_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* plan = static_cast<int32_t*>(workspace);
+  if (cu_seqlens) {
+    TraceScope ts("kda_plan", s);
+    if (plan_launch(cu_seqlens, B, T_tot, plan, err, s) != cudaSuccess) return KDA_ERR_CUDA;
+  }
+  BackwardArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu_seqlens = cu_seqlens; a.plan = plan;
+  a.dout = dout; a.dhT = dhT; a.dq = dq; a.dk = dk_; a.dv = dv_; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
+  a.B = B; a.T = T; a.H = H; a.dim_k = dk; a.dim_v = dv; a.bf16 = (dtype == KDA_DTYPE_BF16);
+  a.workspace = workspace;
+  return backward_launch(a, s) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 namespace {
 kda_status decode_common(const void* q, const void* k, const void* v, const float* g, const float* beta,
                          float* state_pool, const int32_t* slot_idx, const int32_t* ntok_per_req, void* out, int N,

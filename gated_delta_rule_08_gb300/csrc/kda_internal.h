@@ -60,6 +60,33 @@ struct DecodeArgs {
   unsigned int* err;
 };
 
+// Backward (kda_backward.cu): gradients of sum_t <dout_t, o_t> + <dhT, hT>.
+struct BackwardArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  const float* h0;            // may be null
+  const int32_t* cu_seqlens;  // may be null
+  const int32_t* plan;        // chunk offsets (written by plan_launch when cu_seqlens is given)
+  const void* dout;           // [T_tot, H, dv] (input dtype)
+  const float* dhT;           // [B, H, dk, dv] or null
+  float* dq;                  // [T_tot, H, dk] fp32
+  float* dk;                  // [T_tot, H, dk] fp32
+  float* dv;                  // [T_tot, H, dv] fp32
+  float* dg;                  // [T_tot, H, dk] fp32
+  float* dbeta;               // [T_tot, H] fp32
+  float* dh0;                 // [B, H, dk, dv] fp32 or null
+  int B;
+  int64_t T;                  // per-sequence length if cu_seqlens == null, else T_tot
+  int H, dim_k, dim_v;
+  bool bf16;
+  void* workspace;            // plan region, then the backward scratch
+};
+size_t backward_scratch_bytes(int B, int64_t T, int H, int dk, int dv, bool has_cu);
+cudaError_t backward_launch(const BackwardArgs& a, cudaStream_t stream);
+
 // Upper bound on the number of 64-token chunks of a packed batch:
 // sum_b ceil(len_b / 64) <= ceil(T_tot / 64) + B.
 inline int64_t max_chunks(int B, int64_t T, bool has_cu) {

@@ -160,6 +160,27 @@ kda_status kda_decode_multi(const void* q, const void* k, const void* v, const f
                             int dv, int num_slots, int commit, kda_dtype dtype, kda_dtype out_dtype,
                             const kda_epilogue* epi, void* stream);
 
+/* Backward of the prefill recurrence (no epilogue): the gradients of
+ *   L = sum_t <dout_t, o_t> + <dhT, hT>
+ * with respect to q, k, v, g, beta and h0 (section 2.2 Eq. 1, section 2.4 Eq. 3; section 5.1 names
+ * a KDA training kernel).  Computed per (sequence, head) by a reverse-time sweep over the tokens in
+ * fp32, with the state recomputed from per-chunk checkpoints; this is a correct baseline, not a
+ * tensor-core kernel.
+ *   q, k, v, g, beta, h0, cu_seqlens, B, T, H, dk, dv, dtype : as for kda_chunk_fwd
+ *   dout       : [T_tot, H, dv] (dtype)
+ *   dhT        : [B, H, dk, dv] fp32 or NULL (zero)
+ *   dq, dk_, dg: [T_tot, H, dk] fp32;  dv_ : [T_tot, H, dv] fp32;  dbeta : [T_tot, H] fp32
+ *   dh0        : [B, H, dk, dv] fp32 or NULL (not written)
+ *   workspace  : at least kda_chunk_bwd_workspace_size(B, T, H, dk, dv) bytes, 256-byte aligned
+ * Every pointer 16-byte aligned (beta, dbeta exempt).  Errors as for kda_chunk_fwd. */
+size_t kda_chunk_bwd_workspace_size(int B, int64_t T, int H, int dk, int dv);
+kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* h0, const int32_t* cu_seqlens,
+                         const void* dout, const float* dhT, float* dq, float* dk_, float* dv_,
+                         float* dg, float* dbeta, float* dh0, int B, int64_t T, int H, int dk,
+                         int dv, kda_dtype dtype, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error word into
  * *flags (KDA_DEVERR_* bits).  Returns KDA_OK, or KDA_ERR_CUDA if the sync failed. */
 kda_status kda_get_device_error(void* stream, uint32_t* flags);

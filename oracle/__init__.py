@@ -12,6 +12,9 @@ Contents:
   - ``chunkwise_bruteforce.py``: a numpy fp64 evaluation of the chunkwise
     (Eq. 4) form with explicit pairwise decays and an explicit matrix inverse;
     used only to pin the recurrence and the chunk derivation against each other.
+  - ``gradients.py``: the same recurrence restated in fp64 PyTorch and differentiated
+    by autograd (gradients of the backward pass), pinned to ``kda_oracle.c`` and to
+    finite differences.
 """
 from .recurrence import (  # noqa: F401
     build_oracle,
@@ -19,3 +22,4 @@ from .recurrence import (  # noqa: F401
     oracle_kda_decode,
     oracle_threads,
 )
+from .gradients import oracle_kda_backward, recurrence_torch  # noqa: F401
