@@ -14,8 +14,12 @@
 // (section 5.1 names a training kernel for KDA; this one is a plain, exact-arithmetic-faithful
 // fp32 form, not a chunkwise one).
 //
-//  kda_bwd_token<DK, DV, Tin> (one CTA per (sequence, head), 256 threads): the state lives in
-//  registers as in the decode kernel (thread = 4 value columns x DK/NG rows).  A forward sweep
+//  kda_bwd_token<DK, DV, NSL, Tin> (one CTA per (sequence, head, value-column slice), 256
+//  threads): the recurrence is separable in the value columns of the state, so NSL CTAs each take
+//  DV / NSL columns; their contributions to dq, dk, dg, dbeta (sums over the columns) meet by
+//  atomic adds onto zeroed outputs — with NSL <= 2 that sum is order-independent, so the result
+//  is deterministic.  The state slice lives in registers as in the decode kernel (thread = 4
+//  value columns x DK/NG rows).  A forward sweep
 //  stores the state at every chunk start; then, chunk by chunk from the end, the 64 token states
 //  of the chunk are recomputed into scratch and the chunk's tokens are walked backwards.  Column
 //  sums go through shared memory, row sums through a segmented butterfly of warp shuffles.
@@ -73,7 +77,7 @@ struct BwdShared {
   float dbeta[kBwdThreads / 32];
 };
 
-template <int DK, int DV, typename Tin>
+template <int DK, int DV, int NSL, typename Tin>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
               const float* __restrict__ g, const float* __restrict__ beta, const float* __restrict__ h0,
@@ -81,28 +85,35 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
               const Tin* __restrict__ dout, const float* __restrict__ dhT, float* __restrict__ dq,
               float* __restrict__ dk, float* __restrict__ dv, float* __restrict__ dg, float* __restrict__ dbeta,
               float* __restrict__ dh0, float* __restrict__ ckpt, float* __restrict__ tokbuf) {
-  using SH = BwdShared<DK, DV>;
+  constexpr int DVS = DV / NSL;  // value columns of this CTA's slice
+  using SH = BwdShared<DK, DVS>;
   constexpr int TPR = SH::TPR, NG = SH::NG, RPG = DK / NG;
+  static_assert(NSL == 1 || NSL == 2, "two addends at most keep the column sums order-independent");
   static_assert(DK % NG == 0 && RPG <= TPR, "layout");
   __shared__ SH sh;
-  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x, h = blockIdx.y, slice = blockIdx.z, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int j0 = slice * DVS;
   const int cg = tid % TPR, rg = tid / TPR;
   const int seg_lane = lane % TPR;  // lane within this row's lane segment
   if (cu != nullptr && plan[B + 1] == 0) return;  // invalid cu_seqlens: sequence skipped
   int64_t first_chunk, t_begin, len;
   const int64_t nch = sequence_chunks(b, plan, cu, B, T, first_chunk, t_begin, len);
-  constexpr size_t MAT = (size_t)DK * DV;
-  const size_t soff = ((size_t)b * H + h) * MAT;
-  float* tb = tokbuf + ((size_t)b * H + h) * 64 * MAT;
-  auto ck = [&](int64_t c) { return ckpt + ((size_t)(first_chunk + c) * H + h) * MAT; };
-  // this thread's elements: rows rg + i NG, columns 4 cg .. 4 cg + 3
-  auto ld_state = [&](const float* src, float4 (&s)[RPG]) {
+  constexpr size_t MAT = (size_t)DK * DVS;  // one state slice in scratch
+  const size_t soff = ((size_t)b * H + h) * DK * DV + j0;  // this slice in [B, H, DK, DV] states
+  float* tb = tokbuf + (((size_t)b * H + h) * NSL + slice) * 64 * MAT;
+  auto ck = [&](int64_t c) { return ckpt + (((size_t)(first_chunk + c) * H + h) * NSL + slice) * MAT; };
+  // this thread's elements: rows rg + i NG, columns 4 cg .. 4 cg + 3 of the slice (row stride ld)
+  auto ld_state = [&](const float* src, float4 (&s)[RPG], int ld) {
 #pragma unroll
-    for (int i = 0; i < RPG; ++i) s[i] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(rg + i * NG) * DV) + cg);
+    for (int i = 0; i < RPG; ++i) s[i] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(rg + i * NG) * ld) + cg);
   };
-  auto st_state = [&](float* dst, const float4 (&s)[RPG]) {
+  auto st_state = [&](float* dst, const float4 (&s)[RPG], int ld) {
 #pragma unroll
-    for (int i = 0; i < RPG; ++i) __stcg(reinterpret_cast<float4*>(dst + (size_t)(rg + i * NG) * DV) + cg, s[i]);
+    for (int i = 0; i < RPG; ++i) __stcg(reinterpret_cast<float4*>(dst + (size_t)(rg + i * NG) * ld) + cg, s[i]);
+  };
+  auto out_row = [&](float* dst, float x) {  // one column slice's share of a row gradient
+    if (NSL == 1) *dst = x;
+    else atomicAdd(dst, x);
   };
   // token vectors into shared memory (rows past the sequence end never occur here)
   auto load_token = [&](int64_t t, bool with_q) {
@@ -112,9 +123,9 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       sh.al[i] = __expf(g[row * DK + i]);
       if (with_q) sh.q[i] = to_f32(q[row * DK + i]);
     }
-    for (int j = tid; j < DV; j += kBwdThreads) {
-      sh.v[j] = to_f32(v[row * DV + j]);
-      if (with_q) sh.dout[j] = to_f32(dout[row * DV + j]);
+    for (int j = tid; j < DVS; j += kBwdThreads) {
+      sh.v[j] = to_f32(v[row * DV + j0 + j]);
+      if (with_q) sh.dout[j] = to_f32(dout[row * DV + j0 + j]);
     }
     if (tid == 0) sh.beta = beta[row];
   };
@@ -147,12 +158,12 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   // ---- forward sweep: the state at every chunk start
   {
     float4 s[RPG];
-    if (h0 != nullptr) ld_state(h0 + soff, s);
+    if (h0 != nullptr) ld_state(h0 + soff, s, DV);
     else
 #pragma unroll
       for (int i = 0; i < RPG; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int64_t c = 0; c < nch; ++c) {
-      st_state(ck(c), s);
+      st_state(ck(c), s, DVS);
       const int64_t t0 = t_begin + 64 * c, n = len - 64 * c < 64 ? len - 64 * c : 64;
       for (int64_t t = t0; t < t0 + n; ++t) fwd_step(t, s);
     }
@@ -160,7 +171,7 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
 
   // ---- backward sweep, chunk by chunk from the end
   float4 ds[RPG];
-  if (dhT != nullptr) ld_state(dhT + soff, ds);
+  if (dhT != nullptr) ld_state(dhT + soff, ds, DV);
   else
 #pragma unroll
     for (int i = 0; i < RPG; ++i) ds[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -168,9 +179,9 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     const int64_t t0 = t_begin + 64 * c, n = len - 64 * c < 64 ? len - 64 * c : 64;
     {  // the chunk's token states S_{t-1}, recomputed from its start
       float4 s[RPG];
-      ld_state(ck(c), s);
+      ld_state(ck(c), s, DVS);
       for (int64_t j = 0; j < n; ++j) {
-        st_state(tb + (size_t)j * MAT, s);
+        st_state(tb + (size_t)j * MAT, s, DVS);
         if (j + 1 < n) fwd_step(t0 + j, s);
       }
     }
@@ -178,7 +189,7 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       const int64_t t = t0 + j;
       const size_t row = (size_t)t * H + h;
       float4 sp[RPG];  // S_{t-1}
-      ld_state(tb + (size_t)j * MAT, sp);
+      ld_state(tb + (size_t)j * MAT, sp, DVS);
       load_token(t, true);
       __syncthreads();
       const float bt = sh.beta;
@@ -216,7 +227,7 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       bool owner;
       const float dq_row = seg_row_reduce<RPG, TPR>(rq, seg_lane, rrow, owner);
       const int my_row = rg + rrow * NG;
-      if (owner) dq[row * DK + my_row] = dq_row;
+      if (owner) out_row(&dq[row * DK + my_row], dq_row);
       const float w_row = seg_row_reduce<RPG, TPR>(rw, seg_lane, rrow, owner);
       __syncthreads();
       float4 du4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -226,7 +237,7 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
         du4.x += x.x; du4.y += x.y; du4.z += x.z; du4.w += x.w;
       }
       du4 = f4_scale(bt, du4);
-      if (rg == 0) reinterpret_cast<float4*>(dv + row * DV)[cg] = du4;
+      if (rg == 0) reinterpret_cast<float4*>(dv + row * DV + j0)[cg] = du4;
       // row sums P du and (dP (.) S_{t-1}); dS <- Diag(alpha) dP
       float rp[RPG], ra[RPG];
 #pragma unroll
@@ -241,8 +252,8 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       const float da_row = seg_row_reduce<RPG, TPR>(ra, seg_lane, rrow, owner);
       float kw = 0.f;
       if (owner) {
-        dk[row * DK + my_row] = bt * w_row - pdu_row;
-        dg[row * DK + my_row] = sh.al[my_row] * da_row;
+        out_row(&dk[row * DK + my_row], bt * w_row - pdu_row);
+        out_row(&dg[row * DK + my_row], sh.al[my_row] * da_row);
         kw = sh.k[my_row] * w_row;
       }
       kw = warp_sum(kw);
@@ -252,18 +263,38 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
         float s = 0.f;
 #pragma unroll
         for (int w = 0; w < kBwdThreads / 32; ++w) s += sh.dbeta[w];
-        dbeta[row] = s;
+        out_row(&dbeta[row], s);
       }
       __syncthreads();  // shared token vectors and partials are rewritten by the next token
     }
   }
-  if (dh0 != nullptr) st_state(dh0 + soff, ds);
+  if (dh0 != nullptr) st_state(dh0 + soff, ds, DV);
 }
 
 template <int DK, int DV, typename Tin>
 cudaError_t launch_bwd_typed(const BackwardArgs& a, float* ckpt, float* tokbuf, cudaStream_t st) {
+  // two value-column slices per chain when the chains leave at least half of the SMs idle
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidDevice;
+  const bool split = (int64_t)a.B * a.H * 2 <= sms;
+  const int64_t T_tot = a.cu_seqlens ? a.T : (int64_t)a.B * a.T;
+  if (split) {  // the slices' contributions are added onto zeros
+    const size_t rows = (size_t)T_tot * a.H;
+    cudaError_t e = cudaMemsetAsync(a.dq, 0, rows * DK * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.dk, 0, rows * DK * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.dg, 0, rows * DK * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.dbeta, 0, rows * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
   TraceScope ts("kda_bwd_token", st);
-  kda_bwd_token<DK, DV, Tin><<<dim3((unsigned)a.B, (unsigned)a.H), kBwdThreads, 0, st>>>(
+  if (split)
+    kda_bwd_token<DK, DV, 2, Tin><<<dim3((unsigned)a.B, (unsigned)a.H, 2), kBwdThreads, 0, st>>>(
+      static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.h0,
+      a.plan, a.cu_seqlens, a.B, a.T, a.H, static_cast<const Tin*>(a.dout), a.dhT, a.dq, a.dk, a.dv, a.dg, a.dbeta,
+      a.dh0, ckpt, tokbuf);
+  else
+    kda_bwd_token<DK, DV, 1, Tin><<<dim3((unsigned)a.B, (unsigned)a.H, 1), kBwdThreads, 0, st>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.h0,
       a.plan, a.cu_seqlens, a.B, a.T, a.H, static_cast<const Tin*>(a.dout), a.dhT, a.dq, a.dk, a.dv, a.dg, a.dbeta,
       a.dh0, ckpt, tokbuf);
