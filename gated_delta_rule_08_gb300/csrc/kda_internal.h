@@ -109,9 +109,6 @@ bool prefill_tc_supported(int dk, int dv);
 cudaError_t prefill_tc_launch(const PrefillArgs& a, cudaStream_t stream);
 // Intra-device context parallelism: sequence segments of the state pass (1 = none), chosen
 // from the problem shape and the current device's SM count, and the scratch it needs.
-constexpr int64_t kCpMinChunks = 96;       // sequences shorter than this are never split
-constexpr int64_t kCpMinSegChunks = 32;    // smallest segment
-constexpr int64_t kCpLongChunks = 2048;    // from this length on, transitions may take two waves
 int prefill_tc_cp_segments(int B, int64_t T, int H);
 size_t prefill_tc_cp_bytes(int B, int64_t T, int H);
 cudaError_t scan_tc_launch(const PrefillArgs& a, const uint8_t* records, const int32_t* plan, float* cp, int nseg,

@@ -679,6 +679,10 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
 
 }  // namespace
 
+constexpr int64_t kCpMinChunks = 96;       // sequences shorter than this are never split
+constexpr int64_t kCpMinSegChunks = 32;    // smallest segment
+constexpr int64_t kCpLongChunks = 2048;    // from this length on, transitions may take two waves
+
 int prefill_tc_cp_segments(int B, int64_t T, int H) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
