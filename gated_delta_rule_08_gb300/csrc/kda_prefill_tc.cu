@@ -25,8 +25,9 @@
 //      (p & 1) of every 128-byte operand row, so it only waits for the MMAs of pass p - 2;
 //    - the passes also emit Q_hat^T and K_bar^T (channel-major) and e^{G_C} into the record, and
 //      K_hat and V (fp16) in place of the raw tiles;
-//    - T = (I + A)^-1 Diag(beta): 16 x 16 diagonal blocks by forward substitution (fp32), the
-//      off-diagonal blocks by warp-level tf32 MMAs with a three-term split (~fp32), one block per warp;
+//    - T = (I + A)^-1 Diag(beta): 16 x 16 diagonal blocks by forward substitution (fp32), then two
+//      levels of block merges (16 -> 32 -> 64 rows) by warp-level tf32 MMAs with a three-term split
+//      (~fp32), one 16 x 16 tile per warp;
 //    - fp16 MMAs W^T = K_hat^T T^T and U_hat^T = V^T T^T (M = 128, N = 64, K = 64), then W^T, M
 //      and U_hat^T into the record.
 //
@@ -55,11 +56,12 @@ constexpr uint32_t R_K = 0, R_Q = 16384, R_V = 32768, R_BYTES = 49152;
 constexpr uint32_t P_OPS = R_BYTES;      // 56 KB: one 64-channel K block of split-bf16 operands
 constexpr uint32_t O_XH = 0, O_XL = 16384, O_YH = 32768, O_YL = 45056, O_BYTES = 57344;
 // after the A/M product the operand region holds the solve:
-constexpr uint32_t O_SA = 0;             // fp32 A [64][65]
-constexpr uint32_t O_SX = 16640;         // fp32 X = (I + A)^-1 [64][65]
-constexpr uint32_t O_SY = 33280;         // fp32 scratch: three warps x [16][17]
-constexpr uint32_t O_TT = 37888;         // fp16 T [64 r][64 s] row format (1024-aligned)
-constexpr uint32_t O_MST = 47104;        // M staged for its bulk copy to the record (8 KB)
+constexpr uint32_t O_SA = 0;             // fp32 A [64][68]
+constexpr uint32_t O_SX = 17408;         // fp32 X = (I + A)^-1 [64][64], columns permuted per row (swx)
+constexpr uint32_t O_SY = 33792;         // fp32 scratch: four 16 x 16 tiles, row stride 24
+constexpr uint32_t O_TT = 40960;         // fp16 T [64 r][64 s] row format (1024-aligned)
+constexpr uint32_t O_MST = 49152;        // M staged for its bulk copy to the record (8 KB)
+static_assert(O_SY + 4 * 16 * 24 * 4 <= O_TT && O_MST + 8192 <= O_BYTES, "solve region");
 // after the W / U_hat MMAs: W^T at 0 and U_hat^T at 16384 staged for their bulk copies
 constexpr uint32_t P_MISC = P_OPS + O_BYTES;
 constexpr uint32_t M_BETA = 0;           // fp32 [2 tasks][64]
@@ -96,16 +98,39 @@ __device__ __forceinline__ void mma_tf32_m16n8k8(float (&c)[4], const uint32_t (
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// acc[term][n-tile] += M1 (16 x 16, row-major, stride ld1) * M2 (16 x 16 as k rows x n columns, stride
-// ld2), with each operand split as x = hi + lo (both tf32): the terms hi*hi, hi*lo, lo*hi accumulate
-// separately (independent MMA chains) and sum to ~fp32 accuracy with fp32 range.
-__device__ __forceinline__ void warp_gemm16_acc(float (&acc)[3][2][4], const float* M1, int ld1, const float* M2,
-                                                int ld2, int lane) {
+// Shared-memory layouts of the solve, chosen so that the fragment loads below are free of bank
+// conflicts: A (fragment rows g, columns t) at row stride 68; X with its columns XOR-permuted per
+// row (swx), which serves both fragment shapes (rows g / columns t and rows t / columns g); the
+// 16 x 16 scratch tiles, read as k x n operands only, at row stride 24.
+constexpr int kLdA = 68, kLdY = 24;
+__device__ __forceinline__ int swx(int r) {
+  const int x = r & 7;
+  return (((x & 3) << 1) | (x >> 2)) << 2;
+}
+struct LayA {
+  const float* p;
+  __device__ __forceinline__ float operator()(int r, int c) const { return p[r * kLdA + c]; }
+};
+struct LayX {
+  float* p;
+  __device__ __forceinline__ float& operator()(int r, int c) const { return p[r * 64 + (c ^ swx(r))]; }
+};
+struct LayY {
+  float* p;
+  __device__ __forceinline__ float& operator()(int r, int c) const { return p[r * kLdY + c]; }
+};
+
+// acc[term][n-tile] += M1[r1.., c1..] (16 x 16) * M2[r2.., c2..] (16 x 16, k rows x n columns), with
+// each operand split as x = hi + lo (both tf32): the terms hi*hi, hi*lo, lo*hi accumulate separately
+// (independent MMA chains) and sum to ~fp32 accuracy with fp32 range.
+template <class L1, class L2>
+__device__ __forceinline__ void warp_gemm16_acc(float (&acc)[3][2][4], const L1& m1, int r1, int c1, const L2& m2,
+                                                int r2, int c2, int lane) {
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
-    const float af[4] = {M1[g * ld1 + 8 * ks + t], M1[(g + 8) * ld1 + 8 * ks + t], M1[g * ld1 + 8 * ks + t + 4],
-                         M1[(g + 8) * ld1 + 8 * ks + t + 4]};
+    const int ca = c1 + 8 * ks + t, rb = r2 + 8 * ks + t;
+    const float af[4] = {m1(r1 + g, ca), m1(r1 + g + 8, ca), m1(r1 + g, ca + 4), m1(r1 + g + 8, ca + 4)};
     uint32_t ah[4], al[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -114,7 +139,7 @@ __device__ __forceinline__ void warp_gemm16_acc(float (&acc)[3][2][4], const flo
     }
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      const float b0 = M2[(8 * ks + t) * ld2 + 8 * nt + g], b1 = M2[(8 * ks + t + 4) * ld2 + 8 * nt + g];
+      const float b0 = m2(rb, c2 + 8 * nt + g), b1 = m2(rb + 4, c2 + 8 * nt + g);
       const uint32_t bh0 = tf32_bits(b0), bh1 = tf32_bits(b1);
       const uint32_t bl0 = tf32_bits(b0 - __uint_as_float(bh0)), bl1 = tf32_bits(b1 - __uint_as_float(bh1));
       mma_tf32_m16n8k8(acc[0][nt], ah, bh0, bh1);
@@ -126,6 +151,19 @@ __device__ __forceinline__ void warp_gemm16_acc(float (&acc)[3][2][4], const flo
 // (acc[0] + (acc[1] + acc[2])) of one n-tile element
 __device__ __forceinline__ float acc_sum(const float (&acc)[3][2][4], int nt, int e) {
   return acc[0][nt][e] + (acc[1][nt][e] + acc[2][nt][e]);
+}
+// s * (the 16 x 16 accumulator) into dst[r0.., c0..] (float pairs; every layout keeps columns 2j, 2j+1
+// adjacent).
+template <class L>
+__device__ __forceinline__ void store_acc16(const float (&acc)[3][2][4], float s, const L& dst, int r0, int c0,
+                                            int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const int c = c0 + 8 * nt + 2 * t;
+    *reinterpret_cast<float2*>(&dst(r0 + g, c)) = make_float2(s * acc_sum(acc, nt, 0), s * acc_sum(acc, nt, 1));
+    *reinterpret_cast<float2*>(&dst(r0 + g + 8, c)) = make_float2(s * acc_sum(acc, nt, 2), s * acc_sum(acc, nt, 3));
+  }
 }
 
 struct PrepMaps {
@@ -463,7 +501,14 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
           if (lrow < 64) {
             const float br = sBeta[r];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) sA[r * 65 + s0 + j] = (s0 + j < r) ? br * val[j] : 0.f;  // select, not mask-multiply
+            for (int j = 0; j < 16; j += 4) {  // select, not mask-multiply
+              float4 w;
+              w.x = (s0 + j < r) ? br * val[j] : 0.f;
+              w.y = (s0 + j + 1 < r) ? br * val[j + 1] : 0.f;
+              w.z = (s0 + j + 2 < r) ? br * val[j + 2] : 0.f;
+              w.w = (s0 + j + 3 < r) ? br * val[j + 3] : 0.f;
+              *reinterpret_cast<float4*>(sA + r * kLdA + s0 + j) = w;
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) val[j] = (s0 + j <= r) ? val[j] : 0.f;
@@ -480,9 +525,10 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
         bulk_commit();
       }
 
-      // ---- T = (I + A)^-1 Diag(beta), blocked 16 x 16
+      // ---- T = (I + A)^-1 Diag(beta): 16 x 16 diagonal blocks, then two levels of block merges
       {
-        float* sX = reinterpret_cast<float*>(ops + O_SX);
+        const LayA la{sA};
+        const LayX lx{reinterpret_cast<float*>(ops + O_SX)};
         float* sY = reinterpret_cast<float*>(ops + O_SY);
         // diagonal blocks: one thread per column, substitution inside its 16 x 16 block
         if (tid < 64) {
@@ -494,62 +540,62 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
             float acc0 = 0.f, acc1 = 0.f;  // two independent chains
 #pragma unroll
             for (int j = 0; j < i; j += 2) {
-              acc0 = fmaf(sA[r * 65 + r0 + j], x[j], acc0);
-              if (j + 1 < i) acc1 = fmaf(sA[r * 65 + r0 + j + 1], x[j + 1], acc1);
+              acc0 = fmaf(la(r, r0 + j), x[j], acc0);
+              if (j + 1 < i) acc1 = fmaf(la(r, r0 + j + 1), x[j + 1], acc1);
             }
             x[i] = (r == s_) ? 1.f : ((r < s_) ? 0.f : -(acc0 + acc1));
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) sX[(r0 + i) * 65 + s_] = x[i];
+          for (int i = 0; i < 16; ++i) lx(r0 + i, s_) = x[i];
         }
         group_sync(1, kCompute);
-        // off-diagonal blocks by their distance d from the diagonal, one block per warp:
-        // X_ij = -X_ii * sum_{m=j}^{i-1} A_im X_mj  (i = j + d), warp-level tf32 MMAs
-        {
-          const int g = lane >> 2, t = lane & 3;
-          float* sYw = sY + warp * (16 * 17);  // per-warp 16 x 16 scratch (stride 17)
-#pragma unroll 1
-          for (int d = 1; d < 4; ++d) {
-            if (warp < 4 - d) {
-              const int j = warp, i = j + d;
-              float acc[3][2][4] = {};
-#pragma unroll 1
-              for (int m = j; m < i; ++m)
-                warp_gemm16_acc(acc, sA + (16 * i) * 65 + 16 * m, 65, sX + (16 * m) * 65 + 16 * j, 65, lane);
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt) {
-                sYw[g * 17 + 8 * nt + 2 * t] = acc_sum(acc, nt, 0);
-                sYw[g * 17 + 8 * nt + 2 * t + 1] = acc_sum(acc, nt, 1);
-                sYw[(g + 8) * 17 + 8 * nt + 2 * t] = acc_sum(acc, nt, 2);
-                sYw[(g + 8) * 17 + 8 * nt + 2 * t + 1] = acc_sum(acc, nt, 3);
-              }
-              __syncwarp();
-              float z[3][2][4] = {};
-              warp_gemm16_acc(z, sX + (16 * i) * 65 + 16 * i, 65, sYw, 17, lane);
-              float* xo = sX + (16 * i) * 65 + 16 * j;
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt) {
-                xo[g * 65 + 8 * nt + 2 * t] = -acc_sum(z, nt, 0);
-                xo[g * 65 + 8 * nt + 2 * t + 1] = -acc_sum(z, nt, 1);
-                xo[(g + 8) * 65 + 8 * nt + 2 * t] = -acc_sum(z, nt, 2);
-                xo[(g + 8) * 65 + 8 * nt + 2 * t + 1] = -acc_sum(z, nt, 3);
-              }
-              __syncwarp();
-            }
-            group_sync(1, kCompute);
-          }
+        // With X_[ii] the inverses of two adjacent diagonal blocks of (I + A), the block below them is
+        //   X_[10] = -X_[11] A_[10] X_[00].
+        // Level 1 merges the 16 x 16 pairs (0, 1) and (2, 3) (warps 0 and 1); level 2 merges the two
+        // 32 x 32 halves, first Y = A[32:64, 0:32] X[0:32, 0:32], then X[32:64, 0:32] = -X[32:64, 32:64] Y,
+        // one 16 x 16 tile per warp (warps 0-3).  Warp-level tf32 MMAs with the three-term split.
+        if (warp < 2) {
+          const int b = 32 * warp;
+          const LayY ly{sY + warp * 16 * kLdY};
+          float acc[3][2][4] = {};
+          warp_gemm16_acc(acc, la, b + 16, b, lx, b, b, lane);
+          store_acc16(acc, 1.f, ly, 0, 0, lane);
+          __syncwarp();
+          float z[3][2][4] = {};
+          warp_gemm16_acc(z, lx, b + 16, b + 16, ly, 0, 0, lane);
+          store_acc16(z, -1.f, lx, b + 16, b, lane);
         }
+        group_sync(1, kCompute);
+        if (warp < 4) {
+          const int ti = warp >> 1, tj = warp & 1;
+          float acc[3][2][4] = {};
+          if (tj == 0) warp_gemm16_acc(acc, la, 32 + 16 * ti, 0, lx, 0, 0, lane);
+          warp_gemm16_acc(acc, la, 32 + 16 * ti, 16, lx, 16, 16 * tj, lane);
+          store_acc16(acc, 1.f, LayY{sY + (2 * ti + tj) * 16 * kLdY}, 0, 0, lane);
+        }
+        group_sync(1, kCompute);
+        if (warp < 4) {
+          const int ti = warp >> 1, tj = warp & 1;
+          float acc[3][2][4] = {};
+          if (ti == 1) warp_gemm16_acc(acc, lx, 48, 32, LayY{sY + tj * 16 * kLdY}, 0, 0, lane);
+          warp_gemm16_acc(acc, lx, 32 + 16 * ti, 32 + 16 * ti, LayY{sY + (2 * ti + tj) * 16 * kLdY}, 0, 0, lane);
+          store_acc16(acc, -1.f, lx, 32 + 16 * ti, 16 * tj, lane);
+        }
+        group_sync(1, kCompute);
         // T = X Diag(beta) -> fp16 row format [r][s] (zero above the diagonal)
         {
           const int r = tid >> 2, j0 = (tid & 3) * 2;  // two 8-column chunks per thread
 #pragma unroll
           for (int jj = 0; jj < 2; ++jj) {
             const int j = j0 + jj;
+            const float4 xa = *reinterpret_cast<const float4*>(&lx(r, 8 * j));
+            const float4 xb = *reinterpret_cast<const float4*>(&lx(r, 8 * j + 4));
+            const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
             float v[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int s_ = 8 * j + e;
-              v[e] = (s_ <= r) ? sX[r * 65 + s_] * sBeta[s_] : 0.f;
+              v[e] = (s_ <= r) ? xv[e] * sBeta[s_] : 0.f;
             }
             *reinterpret_cast<uint4*>(ops + O_TT + row_chunk(r, j)) = pack8_h(v);
           }
