@@ -27,7 +27,7 @@
 //      K_hat and V (fp16) in place of the raw tiles;
 //    - T = (I + A)^-1 Diag(beta): 16 x 16 diagonal blocks by forward substitution (fp32), then two
 //      levels of block merges (16 -> 32 -> 64 rows) by warp-level tf32 MMAs with a three-term split
-//      (~fp32), one 16 x 16 tile per warp;
+//      (~fp32), one 16 x 8 half-tile per warp;
 //    - fp16 MMAs W^T = K_hat^T T^T and U_hat^T = V^T T^T (M = 128, N = 64, K = 64), then W^T, M
 //      and U_hat^T into the record.
 //
@@ -65,7 +65,7 @@ static_assert(O_SY + 4 * 16 * 24 * 4 <= O_TT && O_MST + 8192 <= O_BYTES, "solve 
 // after the W / U_hat MMAs: W^T at 0 and U_hat^T at 16384 staged for their bulk copies
 constexpr uint32_t P_MISC = P_OPS + O_BYTES;
 constexpr uint32_t M_BETA = 0;           // fp32 [2 tasks][64]
-constexpr uint32_t M_TOT = 512;          // float2 [2][16 row groups][16 channel pairs]: group decay sums
+constexpr uint32_t M_TOT = 512;          // float2 [2][8 warps][16 channel pairs]: decay sums of row-group pairs
 constexpr uint32_t M_BAR = 4608;         // barriers, tmem slot, abort flag
 constexpr uint32_t M_END = 4736;
 constexpr uint32_t kPrepSmem = P_MISC + M_END + 1024;
@@ -120,50 +120,42 @@ struct LayY {
   __device__ __forceinline__ float& operator()(int r, int c) const { return p[r * kLdY + c]; }
 };
 
-// acc[term][n-tile] += M1[r1.., c1..] (16 x 16) * M2[r2.., c2..] (16 x 16, k rows x n columns), with
-// each operand split as x = hi + lo (both tf32): the terms hi*hi, hi*lo, lo*hi accumulate separately
+// acc[term] += M1[r1.., c1..] (16 x 16) * M2[r2.., c2..] (16 x 8, k rows x n columns), with each
+// operand split as x = hi + lo (both tf32): the terms hi*hi, hi*lo, lo*hi accumulate separately
 // (independent MMA chains) and sum to ~fp32 accuracy with fp32 range.
 template <class L1, class L2>
-__device__ __forceinline__ void warp_gemm16_acc(float (&acc)[3][2][4], const L1& m1, int r1, int c1, const L2& m2,
-                                                int r2, int c2, int lane) {
+__device__ __forceinline__ void warp_gemm16x8_acc(float (&acc)[3][4], const L1& m1, int r1, int c1, const L2& m2,
+                                                  int r2, int c2, int lane) {
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
     const int ca = c1 + 8 * ks + t, rb = r2 + 8 * ks + t;
     const float af[4] = {m1(r1 + g, ca), m1(r1 + g + 8, ca), m1(r1 + g, ca + 4), m1(r1 + g + 8, ca + 4)};
+    const float b0 = m2(rb, c2 + g), b1 = m2(rb + 4, c2 + g);
     uint32_t ah[4], al[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       ah[i] = tf32_bits(af[i]);
       al[i] = tf32_bits(af[i] - __uint_as_float(ah[i]));
     }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const float b0 = m2(rb, c2 + 8 * nt + g), b1 = m2(rb + 4, c2 + 8 * nt + g);
-      const uint32_t bh0 = tf32_bits(b0), bh1 = tf32_bits(b1);
-      const uint32_t bl0 = tf32_bits(b0 - __uint_as_float(bh0)), bl1 = tf32_bits(b1 - __uint_as_float(bh1));
-      mma_tf32_m16n8k8(acc[0][nt], ah, bh0, bh1);
-      mma_tf32_m16n8k8(acc[1][nt], ah, bl0, bl1);
-      mma_tf32_m16n8k8(acc[2][nt], al, bh0, bh1);
-    }
+    const uint32_t bh0 = tf32_bits(b0), bh1 = tf32_bits(b1);
+    const uint32_t bl0 = tf32_bits(b0 - __uint_as_float(bh0)), bl1 = tf32_bits(b1 - __uint_as_float(bh1));
+    mma_tf32_m16n8k8(acc[0], ah, bh0, bh1);
+    mma_tf32_m16n8k8(acc[1], ah, bl0, bl1);
+    mma_tf32_m16n8k8(acc[2], al, bh0, bh1);
   }
 }
-// (acc[0] + (acc[1] + acc[2])) of one n-tile element
-__device__ __forceinline__ float acc_sum(const float (&acc)[3][2][4], int nt, int e) {
-  return acc[0][nt][e] + (acc[1][nt][e] + acc[2][nt][e]);
-}
-// s * (the 16 x 16 accumulator) into dst[r0.., c0..] (float pairs; every layout keeps columns 2j, 2j+1
-// adjacent).
+// s * (acc[0] + (acc[1] + acc[2])) into dst[r0.., c0..] (16 x 8; every layout keeps columns 2j, 2j + 1
+// adjacent)
 template <class L>
-__device__ __forceinline__ void store_acc16(const float (&acc)[3][2][4], float s, const L& dst, int r0, int c0,
-                                            int lane) {
+__device__ __forceinline__ void store_acc16x8(const float (&acc)[3][4], float s, const L& dst, int r0, int c0,
+                                              int lane) {
   const int g = lane >> 2, t = lane & 3;
+  float v[4];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    const int c = c0 + 8 * nt + 2 * t;
-    *reinterpret_cast<float2*>(&dst(r0 + g, c)) = make_float2(s * acc_sum(acc, nt, 0), s * acc_sum(acc, nt, 1));
-    *reinterpret_cast<float2*>(&dst(r0 + g + 8, c)) = make_float2(s * acc_sum(acc, nt, 2), s * acc_sum(acc, nt, 3));
-  }
+  for (int e = 0; e < 4; ++e) v[e] = s * (acc[0][e] + (acc[1][e] + acc[2][e]));
+  *reinterpret_cast<float2*>(&dst(r0 + g, c0 + 2 * t)) = make_float2(v[0], v[1]);
+  *reinterpret_cast<float2*>(&dst(r0 + g + 8, c0 + 2 * t)) = make_float2(v[2], v[3]);
 }
 
 struct PrepMaps {
@@ -184,14 +176,24 @@ __device__ __forceinline__ int64_t next_task(int64_t t, int64_t ntask, int64_t s
   return -1;
 }
 
-// g of this thread's 4 rows x 2 channels for one pass (rows past the sequence end read as 0).
+// 2^x (the decays below are carried in log2 units: e^G = 2^(G log2 e))
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
+// g of this thread's 4 rows x 2 channels for one pass (rows past the sequence end read as 0).  Only
+// the next pass consumes these registers, so the loads stay in flight through the current one.
 __device__ __forceinline__ void load_g(float2 (&gv)[4], const float* __restrict__ g, int64_t t0, int n, int H, int h,
                                        int c, int rg) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = 4 * rg + i;
-    gv[i] = r < n ? __ldg(reinterpret_cast<const float2*>(g + ((size_t)(t0 + r) * H + h) * 128 + c))
-                  : make_float2(0.f, 0.f);
+    const float2 x = r < n ? __ldg(reinterpret_cast<const float2*>(g + ((size_t)(t0 + r) * H + h) * 128 + c))
+                           : make_float2(0.f, 0.f);
+    gv[i] = x;
   }
 }
 
@@ -226,7 +228,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
   uint8_t* ops = sm + P_OPS;
   uint8_t* misc = sm + P_MISC;
   float* sBetaAll = reinterpret_cast<float*>(misc + M_BETA);
-  float2* sTot = reinterpret_cast<float2*>(misc + M_TOT);      // [2][16][16]
+  float2* sTot = reinterpret_cast<float2*>(misc + M_TOT);      // [2][8][16]
   uint64_t* full = reinterpret_cast<uint64_t*>(misc + M_BAR);  // raw tiles landed + beta staged
   uint64_t* ops_ready = full + 1;                              // [2] pass operands written (256 arrivals)
   uint64_t* bar_ops = full + 3;                                // [2] pass MMAs done
@@ -365,37 +367,43 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
         float2 gnext[4];
         if (pass < 3) load_g(gnext, g, t0, n, H, h, c + 32, rg);
         else if (ntask_idx >= 0) load_g(gnext, g, nt0, nn, H, nh, cl, rg);
-        float2 L[4];
+        float2 L[4], prev;
         {
           float2 run = make_float2(0.f, 0.f);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            run.x += gcur[i].x;
-            run.y += gcur[i].y;
+            run.x = fmaf(gcur[i].x, kLog2e, run.x);  // log2 units
+            run.y = fmaf(gcur[i].y, kLog2e, run.y);
             L[i] = run;
           }
-          sTot[(pass & 1) * 256 + rg * 16 + cp] = run;
+          // row groups 2w and 2w + 1 sit in lanes cp and cp + 16 of warp w: one exchange gives
+          // the pair's total and, for the odd group, the sum of the group above it
+          prev = make_float2(__shfl_xor_sync(0xffffffffu, run.x, 16), __shfl_xor_sync(0xffffffffu, run.y, 16));
+          if (lane < 16) sTot[(pass & 1) * 128 + warp * 16 + cp] = make_float2(run.x + prev.x, run.y + prev.y);
         }
         if (pass >= 2) ok = wait_or_abort(&bar_ops[pass & 1], 0, abort_flag);
         ok = group_and(1, kCompute, ok);
         if (!ok) break;
-        float2 off = make_float2(0.f, 0.f), cum = make_float2(0.f, 0.f), G15, G47, G63;
+        float2 off = lane < 16 ? make_float2(0.f, 0.f) : prev, cum = make_float2(0.f, 0.f), G15, G47, G63;
 #pragma unroll
-        for (int gi = 0; gi < 16; ++gi) {
-          const float2 t = sTot[(pass & 1) * 256 + gi * 16 + cp];
-          if (gi == rg) off = cum;
+        for (int wi = 0; wi < 8; ++wi) {
+          const float2 t = sTot[(pass & 1) * 128 + wi * 16 + cp];
+          if (wi < warp) {
+            off.x += t.x;
+            off.y += t.y;
+          }
           cum.x += t.x;
           cum.y += t.y;
-          if (gi == 3) G15 = cum;
-          if (gi == 11) G47 = cum;
+          if (wi == 1) G15 = cum;
+          if (wi == 5) G47 = cum;
         }
         G63 = cum;
         const bool first = rg < 8;  // rows < 32: reference row 15, else 47
         const float2 R = first ? G15 : G47;
-        const float eR0 = __expf(R.x), eR1 = __expf(R.y);
-        const float c30 = __expf(G63.x - G47.x), c31 = __expf(G63.y - G47.y);
+        const float eR0 = ex2(R.x), eR1 = ex2(R.y);
+        const float c30 = ex2(G63.x - G47.x), c31 = ex2(G63.y - G47.y);
         if (rg == 0)
-          *reinterpret_cast<float2*>(rec + kRecGC + c * 4) = make_float2(__expf(G63.x), __expf(G63.y));
+          *reinterpret_cast<float2*>(rec + kRecGC + c * 4) = make_float2(ex2(G63.x), ex2(G63.y));
         uint32_t qh2[4], kb2[4];
         const uint32_t kbyte = (uint32_t)(c & 63) * 2u;  // byte of channel c within its 128-byte row
 #pragma unroll
@@ -414,8 +422,8 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
             q2 = k2;
             v2 = k2;
           }
-          const float e10 = __expf(G0 - R.x), e11 = __expf(G1 - R.y);
-          const float e20 = __expf(R.x - G0), e21 = __expf(R.y - G1);
+          const float e10 = ex2(G0 - R.x), e11 = ex2(G1 - R.y);
+          const float e20 = ex2(R.x - G0), e21 = ex2(R.y - G1);
           uint32_t hi, lo;
           const uint32_t ob64 = ob + 64u * 128u;  // row 64 + r (same swizzle phase)
           split_bf16x2(k2.x * e10, k2.y * e11, hi, lo);
@@ -431,11 +439,11 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
           if (first) {
             // rows < 32: k e^{G_47 - G} and k e^{G_C - G} from one exponential each (a factored
             // form can underflow while the product it feeds is O(1))
-            split_bf16x2(k2.x * __expf(G47.x - G0), k2.y * __expf(G47.y - G1), hi, lo);
+            split_bf16x2(k2.x * ex2(G47.x - G0), k2.y * ex2(G47.y - G1), hi, lo);
             *reinterpret_cast<uint32_t*>(ops + O_YH + ob64) = hi;
             *reinterpret_cast<uint32_t*>(ops + O_YL + ob64) = lo;
-            kb0 = k2.x * __expf(G63.x - G0);
-            kb1 = k2.y * __expf(G63.y - G1);
+            kb0 = k2.x * ex2(G63.x - G0);
+            kb1 = k2.y * ex2(G63.y - G1);
           } else {
             kb0 = k2.x * e20 * c30;  // e^{G_C - G_47} >= e^{-80}: no underflow
             kb1 = k2.y * e21 * c31;
@@ -551,35 +559,36 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
         group_sync(1, kCompute);
         // With X_[ii] the inverses of two adjacent diagonal blocks of (I + A), the block below them is
         //   X_[10] = -X_[11] A_[10] X_[00].
-        // Level 1 merges the 16 x 16 pairs (0, 1) and (2, 3) (warps 0 and 1); level 2 merges the two
-        // 32 x 32 halves, first Y = A[32:64, 0:32] X[0:32, 0:32], then X[32:64, 0:32] = -X[32:64, 32:64] Y,
-        // one 16 x 16 tile per warp (warps 0-3).  Warp-level tf32 MMAs with the three-term split.
-        if (warp < 2) {
-          const int b = 32 * warp;
-          const LayY ly{sY + warp * 16 * kLdY};
-          float acc[3][2][4] = {};
-          warp_gemm16_acc(acc, la, b + 16, b, lx, b, b, lane);
-          store_acc16(acc, 1.f, ly, 0, 0, lane);
+        // Level 1 merges the 16 x 16 pairs (0, 1) and (2, 3) (warps 0-3); level 2 merges the two
+        // 32 x 32 halves, first Y = A[32:64, 0:32] X[0:32, 0:32], then X[32:64, 0:32] = -X[32:64, 32:64] Y
+        // (warps 0-7).  Each warp computes one 8-column half of a 16 x 16 tile with warp-level tf32
+        // MMAs and the three-term split.
+        if (warp < 4) {
+          const int b = 32 * (warp & 1), hn = 8 * (warp >> 1);
+          const LayY ly{sY + (warp & 1) * 16 * kLdY};
+          float acc[3][4] = {};
+          warp_gemm16x8_acc(acc, la, b + 16, b, lx, b, b + hn, lane);
+          store_acc16x8(acc, 1.f, ly, 0, hn, lane);
           __syncwarp();
-          float z[3][2][4] = {};
-          warp_gemm16_acc(z, lx, b + 16, b + 16, ly, 0, 0, lane);
-          store_acc16(z, -1.f, lx, b + 16, b, lane);
+          float z[3][4] = {};
+          warp_gemm16x8_acc(z, lx, b + 16, b + 16, ly, 0, hn, lane);
+          store_acc16x8(z, -1.f, lx, b + 16, b + hn, lane);
         }
         group_sync(1, kCompute);
-        if (warp < 4) {
-          const int ti = warp >> 1, tj = warp & 1;
-          float acc[3][2][4] = {};
-          if (tj == 0) warp_gemm16_acc(acc, la, 32 + 16 * ti, 0, lx, 0, 0, lane);
-          warp_gemm16_acc(acc, la, 32 + 16 * ti, 16, lx, 16, 16 * tj, lane);
-          store_acc16(acc, 1.f, LayY{sY + (2 * ti + tj) * 16 * kLdY}, 0, 0, lane);
+        {
+          const int tile = warp & 3, ti = tile >> 1, tj = tile & 1, hn = 8 * (warp >> 2);
+          float acc[3][4] = {};
+          if (tj == 0) warp_gemm16x8_acc(acc, la, 32 + 16 * ti, 0, lx, 0, hn, lane);
+          warp_gemm16x8_acc(acc, la, 32 + 16 * ti, 16, lx, 16, 16 * tj + hn, lane);
+          store_acc16x8(acc, 1.f, LayY{sY + tile * 16 * kLdY}, 0, hn, lane);
         }
         group_sync(1, kCompute);
-        if (warp < 4) {
-          const int ti = warp >> 1, tj = warp & 1;
-          float acc[3][2][4] = {};
-          if (ti == 1) warp_gemm16_acc(acc, lx, 48, 32, LayY{sY + tj * 16 * kLdY}, 0, 0, lane);
-          warp_gemm16_acc(acc, lx, 32 + 16 * ti, 32 + 16 * ti, LayY{sY + (2 * ti + tj) * 16 * kLdY}, 0, 0, lane);
-          store_acc16(acc, -1.f, lx, 32 + 16 * ti, 16 * tj, lane);
+        {
+          const int tile = warp & 3, ti = tile >> 1, tj = tile & 1, hn = 8 * (warp >> 2);
+          float acc[3][4] = {};
+          if (ti == 1) warp_gemm16x8_acc(acc, lx, 48, 32, LayY{sY + tj * 16 * kLdY}, 0, hn, lane);
+          warp_gemm16x8_acc(acc, lx, 32 + 16 * ti, 32 + 16 * ti, LayY{sY + tile * 16 * kLdY}, 0, hn, lane);
+          store_acc16x8(acc, -1.f, lx, 32 + 16 * ti, 16 * tj + hn, lane);
         }
         group_sync(1, kCompute);
         // T = X Diag(beta) -> fp16 row format [r][s] (zero above the diagonal)
