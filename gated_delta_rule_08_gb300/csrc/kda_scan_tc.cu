@@ -23,8 +23,9 @@
 //    warp 12 (one lane) stages the records with bulk copies and issues every MMA;
 //    warps 0-7 (two per TMEM lane quadrant, each owning half of the columns) convert
 //      D_U -> U^T and the updated state -> its fp16 copy, and apply the decay;
-//    MODE 0 (read-out): warps 8-11 drain D_O through a staging buffer and run the optional
-//      RMSNorm + gate epilogue, off the serial path;
+//    MODE 0 (read-out): warps 8-11 drain D_O off the serial path: a full chunk without the
+//      epilogue straight from registers (each store writes 32 consecutive dv of a token), else
+//      through a staging buffer with the optional RMSNorm + gate epilogue;
 //    MODE 1 (transition): z = 2 p + kind; kind 0 runs b_p, kind 1 runs P_p; no read-out.
 //  kda_cp_merge (grid = sequences x heads x 4 column slices): the sequential segment merge in fp32.
 #include <cuda_bf16.h>
@@ -365,13 +366,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
       tc_fence_before();
       group_sync(2, 128);
       if (ow == 0 && lane == 0) mbar_arrive(do_free);
-#pragma unroll
-      for (int r = 0; r < 64; ++r) ost[r * 128 + row] = o[r];
-      group_sync(2, 128);
       const int64_t cg = c_begin + c;
       const int64_t rem = len - 64 * cg;
       const int n = (int)(rem < 64 ? rem : 64);
       const int64_t t0 = t_begin + 64 * cg;
+      if (n == 64 && p.gate == nullptr && sizeof(Tout) == 2) {
+        // full chunk, plain bf16 output: each warp instruction writes 32 consecutive dv of a token
+        __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(out) + (size_t)t0 * H * 128 + (size_t)h * 128 + row;
+#pragma unroll
+        for (int r = 0; r < 64; ++r) ob[(size_t)r * H * 128] = __float2bfloat16_rn(o[r]);
+        continue;
+      }
+#pragma unroll
+      for (int r = 0; r < 64; ++r) ost[r * 128 + row] = o[r];
+      group_sync(2, 128);
       for (int r = ow; r < n; r += 4) {
         float4 y = *reinterpret_cast<const float4*>(ost + r * 128 + 4 * lane);
         const size_t orow = ((size_t)(t0 + r) * H + h) * 128 + 4 * lane;
