@@ -24,12 +24,12 @@
 //      references 15 and 47, plus the off-diagonal block with reference 47).  Pass p fills half
 //      (p & 1) of every 128-byte operand row, so it only waits for the MMAs of pass p - 2;
 //    - the passes also emit Q_hat^T and K_bar^T (channel-major) and e^{G_C} into the record, and
-//      K_hat and V (fp16) in place of the raw tiles;
-//    - T = (I + A)^-1 Diag(beta): 16 x 16 diagonal blocks by forward substitution (fp32), then two
+//      Diag(beta) K_hat and Diag(beta) V (fp16) in place of the raw tiles;
+//    - X = (I + A)^-1: 16 x 16 diagonal blocks by forward substitution (fp32), then two
 //      levels of block merges (16 -> 32 -> 64 rows) by warp-level tf32 MMAs with a three-term split
 //      (~fp32), one 16 x 8 half-tile per warp;
-//    - fp16 MMAs W^T = K_hat^T T^T and U_hat^T = V^T T^T (M = 128, N = 64, K = 64), then W^T, M
-//      and U_hat^T into the record.
+//    - fp16 MMAs W^T = (Diag(beta) K_hat)^T X^T and U_hat^T = (Diag(beta) V)^T X^T with
+//      X = (I + A)^-1 (M = 128, N = 64, K = 64), then W^T, M and U_hat^T into the record.
 //
 // Precision: bf16 operands cannot meet the parity bound on these workloads; fp16 has the bf16
 // MMA rate with 3 more significand bits, and every fp16 operand here is bounded (decayed
@@ -59,7 +59,7 @@ constexpr uint32_t O_XH = 0, O_XL = 16384, O_YH = 32768, O_YL = 45056, O_BYTES =
 constexpr uint32_t O_SA = 0;             // fp32 A [64][68]
 constexpr uint32_t O_SX = 17408;         // fp32 X = (I + A)^-1 [64][64], columns permuted per row (swx)
 constexpr uint32_t O_SY = 33792;         // fp32 scratch: four 16 x 16 tiles, row stride 24
-constexpr uint32_t O_TT = 40960;         // fp16 T [64 r][64 s] row format (1024-aligned)
+constexpr uint32_t O_TT = 40960;         // fp16 X [64 r][64 s] row format (1024-aligned)
 constexpr uint32_t O_MST = 49152;        // M staged for its bulk copy to the record (8 KB)
 static_assert(O_SY + 4 * 16 * 24 * 4 <= O_TT && O_MST + 8192 <= O_BYTES, "solve region");
 // after the W / U_hat MMAs: W^T at 0 and U_hat^T at 16384 staged for their bulk copies
@@ -232,7 +232,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
   uint64_t* full = reinterpret_cast<uint64_t*>(misc + M_BAR);  // raw tiles landed + beta staged
   uint64_t* ops_ready = full + 1;                              // [2] pass operands written (256 arrivals)
   uint64_t* bar_ops = full + 3;                                // [2] pass MMAs done
-  uint64_t* tt_ready = full + 5;                               // T written, A/M read (256 arrivals)
+  uint64_t* tt_ready = full + 5;                               // X written, A/M read (256 arrivals)
   uint64_t* bar_wu = full + 6;                                 // W / U_hat MMAs done
   uint64_t* bar_fin = full + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + M_BAR + 80);
@@ -450,8 +450,11 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
           }
           qh2[i] = pack_h2(q2.x * e10 * eR0, q2.y * e11 * eR1);  // q e^{G}
           kb2[i] = pack_h2(kb0, kb1);
-          *pk = pack_h2(k2.x * e10 * eR0, k2.y * e11 * eR1);     // K_hat = k e^{G}, in place
-          *pv = pack_h2(v2.x, v2.y);                              // V as fp16, in place
+          // Diag(beta) K_hat and Diag(beta) V as fp16, in place (T = X Diag(beta) is applied
+          // through its right factor, so the solve's X is used as is)
+          const float br = sBeta[r];
+          *pk = pack_h2(k2.x * e10 * eR0 * br, k2.y * e11 * eR1 * br);
+          *pv = pack_h2(v2.x * br, v2.y * br);
         }
         // Q_hat^T / K_bar^T rows (channel-major): lanes l and l ^ 16 hold rows 8w..8w+3 and
         // 8w+4..8w+7 of the same two channels; after one exchange each writes a full 16-byte
@@ -533,7 +536,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
         bulk_commit();
       }
 
-      // ---- T = (I + A)^-1 Diag(beta): 16 x 16 diagonal blocks, then two levels of block merges
+      // ---- X = (I + A)^-1: 16 x 16 diagonal blocks, then two levels of block merges
       {
         const LayA la{sA};
         const LayX lx{reinterpret_cast<float*>(ops + O_SX)};
@@ -591,7 +594,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
           store_acc16x8(acc, -1.f, lx, 32 + 16 * ti, 16 * tj + hn, lane);
         }
         group_sync(1, kCompute);
-        // T = X Diag(beta) -> fp16 row format [r][s] (zero above the diagonal)
+        // X -> fp16 row format [r][s] (zero above the diagonal)
         {
           const int r = tid >> 2, j0 = (tid & 3) * 2;  // two 8-column chunks per thread
 #pragma unroll
@@ -604,7 +607,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int s_ = 8 * j + e;
-              v[e] = (s_ <= r) ? xv[e] * sBeta[s_] : 0.f;
+              v[e] = (s_ <= r) ? xv[e] : 0.f;
             }
             *reinterpret_cast<uint4*>(ops + O_TT + row_chunk(r, j)) = pack8_h(v);
           }

@@ -374,7 +374,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
         // full chunk, plain bf16 output: each warp instruction writes 32 consecutive dv of a token
         __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(out) + (size_t)t0 * H * 128 + (size_t)h * 128 + row;
 #pragma unroll
-        for (int r = 0; r < 64; ++r) ob[(size_t)r * H * 128] = __float2bfloat16_rn(o[r]);
+        for (int r = 0; r < 64; ++r) {
+          ob[(size_t)r * H * 128] = __float2bfloat16_rn(o[r]);
+          if ((r & 7) == 7) __nanosleep(64);  // spread the stores over the chunk period
+        }
         continue;
       }
 #pragma unroll
