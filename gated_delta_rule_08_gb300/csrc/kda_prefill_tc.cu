@@ -242,6 +242,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
   const int64_t stride = gridDim.x;
   int h, n;
   int64_t t0, chunk;
+  griddep_launch_dependents();  // the state pass may be scheduled on SMs this grid leaves
   int64_t task = next_task(blockIdx.x, ntask, stride, plan, cu, B, T, H, h, t0, n, chunk);
   if (task < 0) return;
 

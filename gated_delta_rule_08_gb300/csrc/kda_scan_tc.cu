@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
 
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
+  griddep_launch_dependents();
   if (p.cu != nullptr && p.plan[p.B + 1] == 0) return;  // invalid cu_seqlens: sequence skipped
   int64_t first_chunk, t_begin, len;
   const int64_t nchunks = sequence_chunks(b, p.plan, p.cu, p.B, p.T, first_chunk, t_begin, len);
@@ -155,6 +156,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything above overlaps the predecessor's tail; its records and segment states are read below
+  griddep_wait();
   const uint32_t tl = tmem_lane(tmem, warp);
   const int row = (warp & 3) * 32 + lane;  // TMEM lane = state column (dv for S, dk for P)
   const size_t soff = ((size_t)b * H + h) * kCpMat;
@@ -436,6 +439,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1) kda_cp_merge(const ScanParam
   uint64_t* bar = reinterpret_cast<uint64_t*>(msm + 2 * 65536 + 128 * kMergeCols * 4);  // [2]
   const int b = blockIdx.x, h = blockIdx.y, j0 = kMergeCols * blockIdx.z, tid = threadIdx.x;
   const int lane = tid & 31, rg = tid >> 5;
+  griddep_launch_dependents();
   if (p.cu != nullptr && p.plan[p.B + 1] == 0) return;
   int64_t first_chunk, t_begin, len;
   const int64_t nchunks = sequence_chunks(b, p.plan, p.cu, p.B, p.T, first_chunk, t_begin, len);
@@ -444,6 +448,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1) kda_cp_merge(const ScanParam
   const size_t soff = ((size_t)b * p.H + h) * kCpMat;
   float* cp = p.cp + (size_t)(b * p.H + h) * p.nseg * 3 * kCpMat;
   int64_t issued = 0;
+  griddep_wait();  // the transitions' P and b
   if (tid == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
@@ -501,6 +506,24 @@ __global__ void __launch_bounds__(kMergeThreads, 1) kda_cp_merge(const ScanParam
   }
 }
 
+// Launch with programmatic stream serialization: the kernel may start while its predecessor on
+// the stream drains (it calls griddep_wait() before reading that predecessor's results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, int threads, size_t smem, cudaStream_t st,
+                         Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <typename Tout>
 cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int32_t* plan, float* cp, int nseg,
                         int64_t seg_len, cudaStream_t st) {
@@ -528,23 +551,22 @@ cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int3
   if (nseg > 1) {
     {
       TraceScope ts("kda_tc_chunk_scan_transition", st);
-      kda_tc_chunk_scan<Tout, 1, false><<<dim3((unsigned)a.B, (unsigned)a.H, (unsigned)(2 * (nseg - 1))), kScanThreads,
-                                   kScanSmem, st>>>(p);
-      cudaError_t e = cudaGetLastError();
+      cudaError_t e = launch_after(kda_tc_chunk_scan<Tout, 1, false>,
+                                   dim3((unsigned)a.B, (unsigned)a.H, (unsigned)(2 * (nseg - 1))), kScanThreads,
+                                   kScanSmem, st, p);
       if (e != cudaSuccess) return e;
     }
     {
       TraceScope ts("kda_cp_merge", st);
-      kda_cp_merge<<<dim3((unsigned)a.B, (unsigned)a.H, 128 / kMergeCols), kMergeThreads, kMergeSmem, st>>>(p);
-      cudaError_t e = cudaGetLastError();
+      cudaError_t e = launch_after(kda_cp_merge, dim3((unsigned)a.B, (unsigned)a.H, 128 / kMergeCols), kMergeThreads,
+                                   kMergeSmem, st, p);
       if (e != cudaSuccess) return e;
     }
   }
   TraceScope ts("kda_tc_chunk_scan", st);
   const dim3 grid((unsigned)a.B, (unsigned)a.H, (unsigned)nseg);
-  if (a.ckpt != nullptr) kda_tc_chunk_scan<Tout, 0, true><<<grid, kScanThreads, kScanSmem, st>>>(p);
-  else kda_tc_chunk_scan<Tout, 0, false><<<grid, kScanThreads, kScanSmem, st>>>(p);
-  return cudaGetLastError();
+  if (a.ckpt != nullptr) return launch_after(kda_tc_chunk_scan<Tout, 0, true>, grid, kScanThreads, kScanSmem, st, p);
+  return launch_after(kda_tc_chunk_scan<Tout, 0, false>, grid, kScanThreads, kScanSmem, st, p);
 }
 
 }  // namespace

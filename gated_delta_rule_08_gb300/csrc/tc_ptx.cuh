@@ -50,6 +50,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 }
 
 // ------------------------------------------------------------------ fences
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may
+// start while its predecessor drains; griddep_wait() blocks until the predecessor grid has
+// completed and its memory is visible, and must precede every read of what it produced.
+// griddep_launch_dependents() lets the successor be scheduled once every CTA of this grid has
+// issued it or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
