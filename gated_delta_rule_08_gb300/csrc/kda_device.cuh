@@ -33,8 +33,16 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// plan (built on the device from cu_seqlens): plan[0..B] exclusive chunk offsets (plan[B] = all
+// chunks), plan[B+1] = 1 if cu_seqlens was valid, plan[B+2+r] = the sequence of rank r by
+// decreasing length (ties by index; the identity for large B).
+// Sequence of rank r in the serial pass's launch order: the longest chains start first.
+constexpr int kOrderMaxB = 512;  // beyond this many sequences the order is the identity
+__device__ __forceinline__ int sequence_of_rank(int r, const int32_t* plan, const int32_t* cu, int B) {
+  return cu == nullptr ? r : plan[B + 2 + r];
+}
+
 // Resolve a global chunk index into (sequence b, token start t0, valid rows n).
-// plan: [B+1] exclusive chunk offsets + plan[B+1] = 1 if cu_seqlens was valid.
 // Without cu_seqlens: B sequences of T tokens each.  Returns false for a chunk
 // index beyond the last chunk (grid over-provisioning) or an invalid plan.
 __device__ __forceinline__ bool resolve_chunk(int64_t chunk, const int32_t* plan,

@@ -97,7 +97,9 @@ inline int64_t max_chunks(int B, int64_t T, bool has_cu) {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Plan region at the start of the workspace: int32 chunk offsets [B+1] + one valid flag.
-inline size_t plan_bytes(int B) { return align_up((size_t)(B + 2) * sizeof(int32_t), 256); }
+// plan: [B] exclusive chunk offsets, [B] total chunks, [B+1] cu_seqlens valid, [B+2 .. 2B+1] the
+// sequences by decreasing length (see kda_device.cuh)
+inline size_t plan_bytes(int B) { return align_up((size_t)(2 * B + 2) * sizeof(int32_t), 256); }
 
 // fp32 CUDA-core path (kda_prefill_cc.cu)
 size_t prefill_cc_blob_bytes(int dk, int dv);

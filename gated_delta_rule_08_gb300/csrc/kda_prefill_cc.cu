@@ -475,6 +475,26 @@ __global__ void plan_kernel(const int32_t* __restrict__ cu, int B, int64_t T_tot
     const int64_t a = cu[b], e = cu[b + 1];
     if (a >= 0 && e >= a) acc += (e - a + 63) / 64;
   }
+  // the sequences by decreasing length (ties by index), so that the serial pass starts its
+  // longest chains first; O(B^2) rank count, the identity for large B
+  __shared__ int32_t scu[kOrderMaxB + 1];
+  const bool order = B <= kOrderMaxB;
+  if (order)
+    for (int i = tid; i <= B; i += nt) scu[i] = cu[i];
+  __syncthreads();
+  if (bad) return;  // the kernels that read the order return before it
+  for (int b = b0; b < b1; ++b) {
+    int r = b;
+    if (order) {
+      const int32_t lb = scu[b + 1] - scu[b];
+      r = 0;
+      for (int j = 0; j < B; ++j) {
+        const int32_t lj = scu[j + 1] - scu[j];
+        r += (lj > lb || (lj == lb && j < b)) ? 1 : 0;
+      }
+    }
+    plan[B + 2 + r] = b;
+  }
 }
 
 template <int DK, int DV, typename Tin, typename Tout>

@@ -121,10 +121,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S_BAR + 80);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S_BAR + 84);
 
-  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
   griddep_launch_dependents();
   if (p.cu != nullptr && p.plan[p.B + 1] == 0) return;  // invalid cu_seqlens: sequence skipped
+  // blockIdx.x = rank x H + head: all heads of the longest sequence are dispatched first
+  const int h = (int)(blockIdx.x % (unsigned)H);
+  const int b = sequence_of_rank((int)(blockIdx.x / (unsigned)H), p.plan, p.cu, p.B);
   int64_t first_chunk, t_begin, len;
   const int64_t nchunks = sequence_chunks(b, p.plan, p.cu, p.B, p.T, first_chunk, t_begin, len);
   const int64_t p_last = nchunks > 0 ? (nchunks - 1) / p.seg_len : 0;
@@ -552,7 +555,7 @@ cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int3
     {
       TraceScope ts("kda_tc_chunk_scan_transition", st);
       cudaError_t e = launch_after(kda_tc_chunk_scan<Tout, 1, false>,
-                                   dim3((unsigned)a.B, (unsigned)a.H, (unsigned)(2 * (nseg - 1))), kScanThreads,
+                                   dim3((unsigned)(a.B * a.H), 1, (unsigned)(2 * (nseg - 1))), kScanThreads,
                                    kScanSmem, st, p);
       if (e != cudaSuccess) return e;
     }
@@ -564,7 +567,7 @@ cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int3
     }
   }
   TraceScope ts("kda_tc_chunk_scan", st);
-  const dim3 grid((unsigned)a.B, (unsigned)a.H, (unsigned)nseg);
+  const dim3 grid((unsigned)(a.B * a.H), 1, (unsigned)nseg);
   if (a.ckpt != nullptr) return launch_after(kda_tc_chunk_scan<Tout, 0, true>, grid, kScanThreads, kScanSmem, st, p);
   return launch_after(kda_tc_chunk_scan<Tout, 0, false>, grid, kScanThreads, kScanSmem, st, p);
 }
