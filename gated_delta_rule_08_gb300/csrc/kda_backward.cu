@@ -29,7 +29,8 @@
 namespace kda {
 namespace {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 256;  // one or two value-column slices per chain
+constexpr int kBwdThreads4 = 128;  // four slices per chain: each thread keeps the same share of its slice
 
 // Sums, over the L lanes of a lane segment, R per-row partials per lane (R <= L, powers of two).
 // Afterwards vals[0] holds the full sum of local row `row_of(lane)`; the lanes that share a row all
@@ -68,27 +69,30 @@ __device__ __forceinline__ float4 f4_axpy(float a, float4 x, float4 y) {  // a x
 __device__ __forceinline__ float4 f4_scale(float a, float4 x) { return make_float4(a * x.x, a * x.y, a * x.z, a * x.w); }
 __device__ __forceinline__ float4 f4_sub(float4 a, float4 b) { return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
 
-template <int DK, int DV>
+template <int DK, int DV, int THREADS>
 struct BwdShared {
-  static constexpr int TPR = DV / 4, NG = kBwdThreads / TPR;
+  static constexpr int TPR = DV / 4, NG = THREADS / TPR;
   float k[DK], q[DK], al[DK], v[DV], dout[DV];
   float beta;
   float4 partA[NG][TPR], partB[NG][TPR];
-  float dbeta[kBwdThreads / 32];
+  float dbeta[THREADS / 32];
 };
 
-template <int DK, int DV, int NSL, typename Tin>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+template <int DK, int DV, int NSL, typename Tin, int THREADS = NSL == 4 ? kBwdThreads4 : kBwdThreads>
+__global__ void __launch_bounds__(THREADS, 1)
 kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
               const float* __restrict__ g, const float* __restrict__ beta, const float* __restrict__ h0,
               const int32_t* __restrict__ plan, const int32_t* __restrict__ cu, int B, int64_t T, int H,
               const Tin* __restrict__ dout, const float* __restrict__ dhT, float* __restrict__ dq,
               float* __restrict__ dk, float* __restrict__ dv, float* __restrict__ dg, float* __restrict__ dbeta,
-              float* __restrict__ dh0, float* __restrict__ ckpt, float* __restrict__ tokbuf) {
+              float* __restrict__ dh0, float* __restrict__ ckpt, float* __restrict__ tokbuf,
+              float* __restrict__ side) {
   constexpr int DVS = DV / NSL;  // value columns of this CTA's slice
-  using SH = BwdShared<DK, DVS>;
+  using SH = BwdShared<DK, DVS, THREADS>;
   constexpr int TPR = SH::TPR, NG = SH::NG, RPG = DK / NG;
-  static_assert(NSL == 1 || NSL == 2, "two addends at most keep the column sums order-independent");
+  // each output element receives at most two addends onto zero (order-independent); with four
+  // slices, slices 2 and 3 add into `side` (dq, dk, dg, dbeta in the same layout), summed after
+  static_assert(NSL == 1 || NSL == 2 || NSL == 4, "slices");
   static_assert(DK % NG == 0 && RPG <= TPR, "layout");
   __shared__ SH sh;
   const int b = blockIdx.x, h = blockIdx.y, slice = blockIdx.z, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -111,19 +115,23 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
 #pragma unroll
     for (int i = 0; i < RPG; ++i) __stcg(reinterpret_cast<float4*>(dst + (size_t)(rg + i * NG) * ld) + cg, s[i]);
   };
-  auto out_row = [&](float* dst, float x) {  // one column slice's share of a row gradient
+  const size_t rows_tot = (size_t)(cu != nullptr ? T : (int64_t)B * T) * H;
+  // one column slice's share of a row gradient; `dst` points into dq, dk or dg ([rows][DK]) or
+  // dbeta ([rows]), whose copies in `side` follow each other: dq, dk, dg, dbeta
+  auto out_row = [&](float* dst, size_t side_off, float x) {
     if (NSL == 1) *dst = x;
-    else atomicAdd(dst, x);
+    else if (NSL == 2 || slice < 2) atomicAdd(dst, x);
+    else atomicAdd(side + side_off, x);
   };
   // token vectors into shared memory (rows past the sequence end never occur here)
   auto load_token = [&](int64_t t, bool with_q) {
     const size_t row = (size_t)t * H + h;
-    for (int i = tid; i < DK; i += kBwdThreads) {
+    for (int i = tid; i < DK; i += THREADS) {
       sh.k[i] = to_f32(k[row * DK + i]);
       sh.al[i] = __expf(g[row * DK + i]);
       if (with_q) sh.q[i] = to_f32(q[row * DK + i]);
     }
-    for (int j = tid; j < DVS; j += kBwdThreads) {
+    for (int j = tid; j < DVS; j += THREADS) {
       sh.v[j] = to_f32(v[row * DV + j0 + j]);
       if (with_q) sh.dout[j] = to_f32(dout[row * DV + j0 + j]);
     }
@@ -227,7 +235,7 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       bool owner;
       const float dq_row = seg_row_reduce<RPG, TPR>(rq, seg_lane, rrow, owner);
       const int my_row = rg + rrow * NG;
-      if (owner) out_row(&dq[row * DK + my_row], dq_row);
+      if (owner) out_row(&dq[row * DK + my_row], row * DK + my_row, dq_row);
       const float w_row = seg_row_reduce<RPG, TPR>(rw, seg_lane, rrow, owner);
       __syncthreads();
       float4 du4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -252,8 +260,8 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       const float da_row = seg_row_reduce<RPG, TPR>(ra, seg_lane, rrow, owner);
       float kw = 0.f;
       if (owner) {
-        out_row(&dk[row * DK + my_row], bt * w_row - pdu_row);
-        out_row(&dg[row * DK + my_row], sh.al[my_row] * da_row);
+        out_row(&dk[row * DK + my_row], rows_tot * DK + row * DK + my_row, bt * w_row - pdu_row);
+        out_row(&dg[row * DK + my_row], 2 * rows_tot * DK + row * DK + my_row, sh.al[my_row] * da_row);
         kw = sh.k[my_row] * w_row;
       }
       kw = warp_sum(kw);
@@ -262,8 +270,8 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       if (tid == 0) {
         float s = 0.f;
 #pragma unroll
-        for (int w = 0; w < kBwdThreads / 32; ++w) s += sh.dbeta[w];
-        out_row(&dbeta[row], s);
+        for (int w = 0; w < THREADS / 32; ++w) s += sh.dbeta[w];
+        out_row(&dbeta[row], 3 * rows_tot * DK + row, s);
       }
       __syncthreads();  // shared token vectors and partials are rewritten by the next token
     }
@@ -271,59 +279,93 @@ kda_bwd_token(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   if (dh0 != nullptr) st_state(dh0 + soff, ds, DV);
 }
 
+// out += side for the four slices' second pair of addends (dq, dk, dg: n = rows x DK each; dbeta: rows)
+__global__ void bwd_add_side(float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dg,
+                             float* __restrict__ dbeta, const float* __restrict__ side, size_t n, size_t rows) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    dq[i] += side[i];
+    dk[i] += side[n + i];
+    dg[i] += side[2 * n + i];
+  }
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < rows; i += stride) dbeta[i] += side[3 * n + i];
+}
+
 template <int DK, int DV, typename Tin>
-cudaError_t launch_bwd_typed(const BackwardArgs& a, float* ckpt, float* tokbuf, cudaStream_t st) {
-  // two value-column slices per chain when the chains leave at least half of the SMs idle
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return cudaErrorInvalidDevice;
-  const bool split = (int64_t)a.B * a.H * 2 <= sms;
+cudaError_t launch_bwd_typed(const BackwardArgs& a, float* ckpt, float* tokbuf, float* side, cudaStream_t st) {
+  const int nsl = backward_slices(a.B, a.H, a.dim_v);
   const int64_t T_tot = a.cu_seqlens ? a.T : (int64_t)a.B * a.T;
-  if (split) {  // the slices' contributions are added onto zeros
-    const size_t rows = (size_t)T_tot * a.H;
+  const size_t rows = (size_t)T_tot * a.H;
+  if (nsl > 1) {  // the slices' contributions are added onto zeros
     cudaError_t e = cudaMemsetAsync(a.dq, 0, rows * DK * sizeof(float), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(a.dk, 0, rows * DK * sizeof(float), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(a.dg, 0, rows * DK * sizeof(float), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(a.dbeta, 0, rows * sizeof(float), st);
+    if (e == cudaSuccess && nsl == 4) e = cudaMemsetAsync(side, 0, (3 * rows * DK + rows) * sizeof(float), st);
     if (e != cudaSuccess) return e;
   }
   TraceScope ts("kda_bwd_token", st);
-  if (split)
-    kda_bwd_token<DK, DV, 2, Tin><<<dim3((unsigned)a.B, (unsigned)a.H, 2), kBwdThreads, 0, st>>>(
-      static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.h0,
-      a.plan, a.cu_seqlens, a.B, a.T, a.H, static_cast<const Tin*>(a.dout), a.dhT, a.dq, a.dk, a.dv, a.dg, a.dbeta,
-      a.dh0, ckpt, tokbuf);
-  else
-    kda_bwd_token<DK, DV, 1, Tin><<<dim3((unsigned)a.B, (unsigned)a.H, 1), kBwdThreads, 0, st>>>(
-      static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.h0,
-      a.plan, a.cu_seqlens, a.B, a.T, a.H, static_cast<const Tin*>(a.dout), a.dhT, a.dq, a.dk, a.dv, a.dg, a.dbeta,
-      a.dh0, ckpt, tokbuf);
+  const dim3 grid((unsigned)a.B, (unsigned)a.H, (unsigned)nsl);
+#define KDA_BWD_ARGS                                                                                               \
+  static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.h0,     \
+      a.plan, a.cu_seqlens, a.B, a.T, a.H, static_cast<const Tin*>(a.dout), a.dhT, a.dq, a.dk, a.dv, a.dg, a.dbeta, \
+      a.dh0, ckpt, tokbuf, side
+  if (nsl == 4) {
+    kda_bwd_token<DK, DV, 4, Tin><<<grid, kBwdThreads4, 0, st>>>(KDA_BWD_ARGS);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_add_side<<<1024, 256, 0, st>>>(a.dq, a.dk, a.dg, a.dbeta, side, rows * DK, rows);
+  } else if (nsl == 2) {
+    kda_bwd_token<DK, DV, 2, Tin><<<grid, kBwdThreads, 0, st>>>(KDA_BWD_ARGS);
+  } else {
+    kda_bwd_token<DK, DV, 1, Tin><<<grid, kBwdThreads, 0, st>>>(KDA_BWD_ARGS);
+  }
+#undef KDA_BWD_ARGS
   return cudaGetLastError();
 }
 
 template <typename Tin>
-cudaError_t launch_bwd_dims(const BackwardArgs& a, float* ckpt, float* tokbuf, cudaStream_t st) {
-  if (a.dim_k == 128 && a.dim_v == 128) return launch_bwd_typed<128, 128, Tin>(a, ckpt, tokbuf, st);
-  if (a.dim_k == 64 && a.dim_v == 64) return launch_bwd_typed<64, 64, Tin>(a, ckpt, tokbuf, st);
-  if (a.dim_k == 128 && a.dim_v == 64) return launch_bwd_typed<128, 64, Tin>(a, ckpt, tokbuf, st);
-  if (a.dim_k == 64 && a.dim_v == 128) return launch_bwd_typed<64, 128, Tin>(a, ckpt, tokbuf, st);
+cudaError_t launch_bwd_dims(const BackwardArgs& a, float* ckpt, float* tokbuf, float* side, cudaStream_t st) {
+  if (a.dim_k == 128 && a.dim_v == 128) return launch_bwd_typed<128, 128, Tin>(a, ckpt, tokbuf, side, st);
+  if (a.dim_k == 64 && a.dim_v == 64) return launch_bwd_typed<64, 64, Tin>(a, ckpt, tokbuf, side, st);
+  if (a.dim_k == 128 && a.dim_v == 64) return launch_bwd_typed<128, 64, Tin>(a, ckpt, tokbuf, side, st);
+  if (a.dim_k == 64 && a.dim_v == 128) return launch_bwd_typed<64, 128, Tin>(a, ckpt, tokbuf, side, st);
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
+// Value-column slices per chain: as many (1, 2 or 4) as keep one CTA per chain slice within one
+// wave of the device's SMs.
+int backward_slices(int B, int H, int dv) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  const int64_t chains = (int64_t)B * H;
+  if (chains * 4 <= sms && dv % 64 == 0) return 4;
+  if (chains * 2 <= sms) return 2;
+  return 1;
+}
+
 size_t backward_scratch_bytes(int B, int64_t T, int H, int dk, int dv, bool has_cu) {
   const size_t mat = (size_t)dk * dv * sizeof(float);
-  return align_up((size_t)max_chunks(B, T, has_cu) * H * mat, 256) + (size_t)B * H * 64 * mat;
+  size_t bytes = align_up((size_t)max_chunks(B, T, has_cu) * H * mat, 256) + align_up((size_t)B * H * 64 * mat, 256);
+  if (backward_slices(B, H, dv) == 4) {  // the second pair of addends of dq, dk, dg, dbeta
+    const size_t rows = (size_t)(has_cu ? T : (int64_t)B * T) * H;
+    bytes += (3 * rows * dk + rows) * sizeof(float);
+  }
+  return bytes;
 }
 
 cudaError_t backward_launch(const BackwardArgs& a, cudaStream_t st) {
   uint8_t* ws = static_cast<uint8_t*>(a.workspace) + plan_bytes(a.B);
   const size_t mat = (size_t)a.dim_k * a.dim_v * sizeof(float);
+  const size_t ck_bytes = align_up((size_t)max_chunks(a.B, a.T, a.cu_seqlens != nullptr) * a.H * mat, 256);
   float* ckpt = reinterpret_cast<float*>(ws);
-  float* tokbuf = reinterpret_cast<float*>(ws + align_up((size_t)max_chunks(a.B, a.T, a.cu_seqlens != nullptr) *
-                                                             a.H * mat, 256));
-  return a.bf16 ? launch_bwd_dims<__nv_bfloat16>(a, ckpt, tokbuf, st) : launch_bwd_dims<float>(a, ckpt, tokbuf, st);
+  float* tokbuf = reinterpret_cast<float*>(ws + ck_bytes);
+  float* side = reinterpret_cast<float*>(ws + ck_bytes + align_up((size_t)a.B * a.H * 64 * mat, 256));
+  return a.bf16 ? launch_bwd_dims<__nv_bfloat16>(a, ckpt, tokbuf, side, st)
+                : launch_bwd_dims<float>(a, ckpt, tokbuf, side, st);
 }
 
 }  // namespace kda

@@ -84,6 +84,7 @@ struct BackwardArgs {
   bool bf16;
   void* workspace;            // plan region, then the backward scratch
 };
+int backward_slices(int B, int H, int dv);  // value-column slices per chain (1, 2 or 4)
 size_t backward_scratch_bytes(int B, int64_t T, int H, int dk, int dv, bool has_cu);
 cudaError_t backward_launch(const BackwardArgs& a, cudaStream_t stream);
 

@@ -444,7 +444,7 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
 __global__ void plan_kernel(const int32_t* __restrict__ cu, int B, int64_t T_tot, int32_t* __restrict__ plan,
                             unsigned int* __restrict__ err) {
   // One block of 1024 threads: each thread owns a contiguous range of sequences.
-  __shared__ int64_t part[1024];
+  __shared__ int64_t part[32];
   __shared__ int bad;
   const int tid = threadIdx.x, nt = blockDim.x;
   if (tid == 0) bad = (cu[0] != 0);
@@ -459,17 +459,33 @@ __global__ void plan_kernel(const int32_t* __restrict__ cu, int B, int64_t T_tot
     else local += (e - a + 63) / 64;
   }
   if (lbad) atomicOr(&bad, 1);
-  part[tid] = local;
+  // exclusive scan of the per-thread chunk counts: within each warp by shuffles, then over the
+  // warp totals
+  const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
+  int64_t incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) part[wid] = incl;
   __syncthreads();
-  if (tid == 0) {  // exclusive scan over thread ranges (1024 entries: cheap)
-    int64_t acc = 0;
-    for (int i = 0; i < nt; ++i) { const int64_t x = part[i]; part[i] = acc; acc += x; }
-    plan[B] = (int32_t)acc;
+  if (wid == 0) {
+    int64_t w = lane < nw ? part[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nw) part[lane] = w;  // inclusive totals of warps 0..lane
+  }
+  __syncthreads();
+  if (tid == 0) {
+    plan[B] = (int32_t)part[nw - 1];
     plan[B + 1] = bad ? 0 : 1;
     if (bad) atomicOr(err, KDA_DEVERR_BAD_SEQLENS);
   }
-  __syncthreads();
-  int64_t acc = part[tid];
+  int64_t acc = incl - local + (wid > 0 ? part[wid - 1] : 0);
   for (int b = b0; b < b1; ++b) {
     plan[b] = (int32_t)acc;
     const int64_t a = cu[b], e = cu[b + 1];
