@@ -68,6 +68,22 @@ def test_varlen_with_empty_and_short_sequences():
     assert torch.equal(hT[0], inp["h0"][0]) and torch.equal(hT[5], inp["h0"][5])
 
 
+def test_many_sequences_beyond_the_length_ordering_limit():
+    # more sequences than the plan sorts by length (512): the serial pass keeps their given order
+    rng = np.random.default_rng(320)
+    lengths = tuple(int(x) for x in rng.integers(0, 131, size=600))
+    cfg = inputs.PrefillConfig("many", H=1, dk=128, dv=128, dtype="bf16", lengths=lengths, B=600, h0_std=0.1,
+                               seed=320)
+    _check(cfg, out_dtypes=(torch.bfloat16,))
+
+
+def test_length_ordering_with_ties_matches_oracle():
+    # equal lengths among unequal ones: the rank order breaks ties by index
+    cfg = inputs.PrefillConfig("ties", H=2, dk=128, dv=128, dtype="bf16", lengths=(200, 65, 200, 1, 65, 300, 200),
+                               B=7, h0_std=0.1, seed=321)
+    _check(cfg, out_dtypes=(torch.bfloat16,))
+
+
 def test_equal_lengths_without_cu_seqlens():
     cfg = inputs.PrefillConfig("equal", H=2, dk=128, dv=128, dtype="bf16", B=3, T=100, h0_std=0.1, seed=301)
     inp = inputs.prefill_inputs(cfg, device="cuda")
