@@ -347,7 +347,17 @@ int backward_slices(int B, int H, int dv) {
   return 1;
 }
 
+// The chunkwise backward keeps about 0.6 MB of fp32 scratch per (chunk, head) (dk = dv = 128); up to
+// this much scratch it is used, beyond it the token sweep below (whose scratch is per chain).
+constexpr size_t kChunkedMaxBytes = size_t(48) << 30;
+
+bool use_chunked(int B, int64_t T, int H, int dk, int dv) {
+  return backward_chunked_bytes(B, T, H, dk, dv, true) <= kChunkedMaxBytes &&
+         backward_chunked_bytes(B, T, H, dk, dv, false) <= kChunkedMaxBytes;
+}
+
 size_t backward_scratch_bytes(int B, int64_t T, int H, int dk, int dv, bool has_cu) {
+  if (use_chunked(B, T, H, dk, dv)) return backward_chunked_bytes(B, T, H, dk, dv, has_cu);
   const size_t mat = (size_t)dk * dv * sizeof(float);
   size_t bytes = align_up((size_t)max_chunks(B, T, has_cu) * H * mat, 256) + align_up((size_t)B * H * 64 * mat, 256);
   if (backward_slices(B, H, dv) == 4) {  // the second pair of addends of dq, dk, dg, dbeta
@@ -359,6 +369,7 @@ size_t backward_scratch_bytes(int B, int64_t T, int H, int dk, int dv, bool has_
 
 cudaError_t backward_launch(const BackwardArgs& a, cudaStream_t st) {
   uint8_t* ws = static_cast<uint8_t*>(a.workspace) + plan_bytes(a.B);
+  if (use_chunked(a.B, a.T, a.H, a.dim_k, a.dim_v)) return backward_chunked_launch(a, reinterpret_cast<float*>(ws), st);
   const size_t mat = (size_t)a.dim_k * a.dim_v * sizeof(float);
   const size_t ck_bytes = align_up((size_t)max_chunks(a.B, a.T, a.cu_seqlens != nullptr) * a.H * mat, 256);
   float* ckpt = reinterpret_cast<float*>(ws);

@@ -1,0 +1,880 @@
+// KDA backward, chunkwise (fp32 CUDA cores): gradients of L = sum_t <dout_t, o_t> + <dhT, hT> with
+// respect to q, k, v, g, beta and h0, for the prefill recurrence without epilogue.
+//
+// Kimi K3: Open Frontier Intelligence (kimi-k3-paper.pages.dev), section 2.5 / Eq. 4 gives the
+// chunk form of the forward: with chunk-start state S0, G the chunk's inclusive cumulative decay,
+//   A_rs = beta_r sum_c k_rc k_sc e^{G_rc - G_sc} (s < r),  M_rs = sum_c q_rc k_sc e^{G_rc - G_sc} (s <= r)
+//   X = (I + A)^-1,  T = X Diag(beta),  W = T K_hat,  U_hat = T V,  U = U_hat - W S0
+//   O = Q_hat S0 + M U,  S_C = Diag(e^{G_C}) S0 + K_bar^T U
+// (K_hat = K e^{G}, Q_hat = Q e^{G}, K_bar = K e^{G_C - G}).  Its reverse mode, per chunk, given
+// dO and dS_C (dL/dS at the chunk end):
+//   dU = M^T dO + K_bar dS_C,   dS0 = Q_hat^T dO + Diag(e^{G_C}) dS_C - W^T dU   (the serial pass)
+//   dQ_hat = dO S0^T, dM = dO U^T, dK_bar = U dS_C^T, dW = -dU S0^T,
+//   dT = dU V^T + dW K_hat^T, dK_hat = T^T dW, dV = T^T dU,
+//   dX = dT Diag(beta), dbeta += colsum(X (.) dT), dA = -X^T dX X^T (strict lower),
+//   dbeta += rowsum(dA (.) A_tilde) (A_tilde: A without beta), P = Diag(beta) dA,
+//   and the A / M terms reach dq, dk and dG through e^{G_r - G_s} with the same reference points as
+//   the forward; dg is the reverse cumulative sum of dG over the chunk.
+//
+// Kernels (all fp32):
+//   bwd_rec    per (chunk, head): the chunk's records (T, X, A_tilde, M, W, W^T, U_hat, K_bar,
+//              K_bar^T, Q_hat, e^{G_C});
+//   bwd_fwd    per (sequence, head, value-column slice), serial over chunks: S0 and U per chunk;
+//   bwd_rev    the same, reverse: dS_C and dU per chunk, dh0;
+//   bwd_grads  per (chunk, head): the parameter gradients.
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kC = 64;         // chunk length
+constexpr int kThreads = 256;  // every kernel here
+
+// acc[i][j] += sum_{k < K} At[k * lda + m0 + i] * B[k * ldb + n0 + j]: a register tile of a product
+// whose operands are both stored k-major (At: the left factor transposed).  MI and NJ are multiples
+// of 4; lda, ldb, m0 and n0 are multiples of 4 (16-byte vector loads); At and B may be in shared or
+// global memory.
+template <int MI, int NJ>
+__device__ __forceinline__ void kgemm(float (&acc)[MI][NJ], const float* At, int lda, int m0, const float* B, int ldb,
+                                      int n0, int K) {
+#pragma unroll 2
+  for (int k = 0; k < K; ++k) {
+    float a[MI], b[NJ];
+#pragma unroll
+    for (int i = 0; i < MI; i += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(At + (size_t)k * lda + m0 + i);
+      a[i] = x.x; a[i + 1] = x.y; a[i + 2] = x.z; a[i + 3] = x.w;
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; j += 4) {
+      const float4 y = *reinterpret_cast<const float4*>(B + (size_t)k * ldb + n0 + j);
+      b[j] = y.x; b[j + 1] = y.y; b[j + 2] = y.z; b[j + 3] = y.w;
+    }
+#pragma unroll
+    for (int i = 0; i < MI; ++i)
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+  }
+}
+template <int MI, int NJ>
+__device__ __forceinline__ void zero(float (&acc)[MI][NJ]) {
+#pragma unroll
+  for (int i = 0; i < MI; ++i)
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) acc[i][j] = 0.f;
+}
+
+// Per-(chunk, head) record layout in the workspace (floats).
+struct RecLayout {
+  int D, E;
+  __host__ __device__ size_t T() const { return 0; }                     // [C][C]
+  __host__ __device__ size_t X() const { return (size_t)kC * kC; }       // [C][C]
+  __host__ __device__ size_t At() const { return 2 * (size_t)kC * kC; }  // [C][C] A without beta, strict lower
+  __host__ __device__ size_t M() const { return 3 * (size_t)kC * kC; }   // [C][C] lower incl. diagonal
+  __host__ __device__ size_t W() const { return 4 * (size_t)kC * kC; }   // [C][D]
+  __host__ __device__ size_t WT() const { return W() + (size_t)kC * D; }  // [D][C]
+  __host__ __device__ size_t Uh() const { return WT() + (size_t)kC * D; }  // [C][E]
+  __host__ __device__ size_t Kb() const { return Uh() + (size_t)kC * E; }  // [C][D]
+  __host__ __device__ size_t KbT() const { return Kb() + (size_t)kC * D; }  // [D][C]
+  __host__ __device__ size_t Qh() const { return KbT() + (size_t)kC * D; }  // [C][D]
+  __host__ __device__ size_t GC() const { return Qh() + (size_t)kC * D; }   // [D]
+  __host__ __device__ size_t size() const { return GC() + (size_t)D; }
+};
+// Per-(chunk, head) states of the two serial passes (floats): S0^T and dS_C^T [E][D], U^T and dU^T [E][C].
+struct StateLayout {
+  int D, E;
+  __host__ __device__ size_t S0T() const { return 0; }
+  __host__ __device__ size_t UT() const { return (size_t)E * D; }
+  __host__ __device__ size_t dST() const { return UT() + (size_t)E * kC; }
+  __host__ __device__ size_t dUT() const { return dST() + (size_t)E * D; }
+  __host__ __device__ size_t size() const { return dUT() + (size_t)E * kC; }
+};
+
+// ---------------------------------------------------------------- per-chunk records
+// Shared floats of bwd_rec: k, q, G [C][D+4]; scratch (A/M operands, later V and T^T); A_tilde, M, X
+// [C][C+4]; beta [C].
+template <int D, int E>
+struct RecSmem {
+  static constexpr int LD = D + 4, LE = E + 4, LC = kC + 4, L32 = 32 + 4;
+  static constexpr int SC0 = 3 * D * L32, SC1 = kC * LE + kC * LC;
+  static constexpr int SC = SC0 > SC1 ? SC0 : SC1;
+  static constexpr int floats = 3 * kC * LD + SC + 3 * kC * LC + kC;
+};
+
+template <int D, int E, typename Tin>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v, const float* __restrict__ g,
+        const float* __restrict__ beta, const int32_t* __restrict__ plan, const int32_t* __restrict__ cu, int B,
+        int64_t T, int H, int64_t ntask, float* __restrict__ recs) {
+  using SM = RecSmem<D, E>;
+  constexpr int LD = SM::LD, LE = SM::LE, LC = SM::LC, L32 = SM::L32;
+  extern __shared__ __align__(16) float sm[];
+  float* kS = sm;                 // k, later K_hat
+  float* qS = kS + kC * LD;
+  float* gS = qS + kC * LD;       // g, then G
+  float* sc = gS + kC * LD;
+  float* AtS = sc + SM::SC;
+  float* MS = AtS + kC * LC;
+  float* XS = MS + kC * LC;
+  float* bS = XS + kC * LC;
+  const int tid = threadIdx.x;
+  const RecLayout L{D, E};
+  for (int64_t task = blockIdx.x; task < ntask; task += gridDim.x) {
+    const int64_t chunk = task / H;
+    const int h = (int)(task - chunk * H);
+    int b, n;
+    int64_t t0, cseq;
+    if (!resolve_chunk(chunk, plan, cu, B, T, b, t0, n, cseq)) continue;  // same for the whole CTA
+    float* rec = recs + (size_t)task * L.size();
+    // inputs of the chunk (rows past the sequence end: k = q = 0, g = 0, beta = 0)
+    for (int i = tid; i < kC * D; i += kThreads) {
+      const int r = i / D, c = i % D;
+      const bool ok = r < n;
+      const size_t src = ((size_t)(t0 + r) * H + h) * D + c;
+      kS[r * LD + c] = ok ? to_f32(k[src]) : 0.f;
+      qS[r * LD + c] = ok ? to_f32(q[src]) : 0.f;
+      gS[r * LD + c] = ok ? g[src] : 0.f;
+    }
+    if (tid < kC) bS[tid] = tid < n ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    for (int i = tid; i < kC * LC; i += kThreads) {
+      AtS[i] = 0.f;
+      MS[i] = 0.f;
+    }
+    __syncthreads();
+    if (tid < D) {  // G: inclusive cumulative decay over the chunk
+      float run = 0.f;
+      for (int r = 0; r < kC; ++r) {
+        run += gS[r * LD + tid];
+        gS[r * LD + tid] = run;
+      }
+    }
+    __syncthreads();
+    // e^{G_C}, K_bar = k e^{G_C - G} (and transposed), Q_hat = q e^{G}
+    for (int i = tid; i < kC * D; i += kThreads) {
+      const int r = i / D, c = i % D;
+      const float G = gS[r * LD + c], Gc = gS[(kC - 1) * LD + c];
+      const float kb = kS[r * LD + c] * __expf(Gc - G);
+      rec[L.Kb() + (size_t)r * D + c] = kb;
+      rec[L.KbT() + (size_t)c * kC + r] = kb;
+      rec[L.Qh() + (size_t)r * D + c] = qS[r * LD + c] * __expf(G);
+      if (r == 0) rec[L.GC() + c] = __expf(Gc);
+    }
+    // A_tilde (strict lower) and M (lower incl. diagonal) by 32 x 32 blocks, each with a reference
+    // point R that keeps every factor within e^{+-80} (g > -5): the diagonal blocks use the centred
+    // rows 15 and 47, the block below the diagonal row 47 (its key-side factor is then <= 1)
+    for (int blk = 0; blk < 3; ++blk) {
+      const int ra = blk == 0 ? 0 : 32, sb = blk == 1 ? 32 : 0, ref = blk == 0 ? 15 : 47;
+      float* XkT = sc;
+      float* XqT = sc + D * L32;
+      float* YT = sc + 2 * D * L32;
+      for (int i = tid; i < D * 32; i += kThreads) {
+        const int c = i / 32, r = i % 32;
+        const float R = gS[ref * LD + c];
+        const float er = __expf(gS[(ra + r) * LD + c] - R);
+        XkT[c * L32 + r] = kS[(ra + r) * LD + c] * er;
+        XqT[c * L32 + r] = qS[(ra + r) * LD + c] * er;
+        YT[c * L32 + r] = kS[(sb + r) * LD + c] * __expf(R - gS[(sb + r) * LD + c]);
+      }
+      __syncthreads();
+      if (tid < 128) {
+        const bool isM = tid >= 64;
+        const int t = tid & 63, r0 = 4 * (t >> 3), s0 = 4 * (t & 7);
+        float acc[4][4];
+        zero(acc);
+        kgemm<4, 4>(acc, isM ? XqT : XkT, L32, r0, YT, L32, s0, D);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = ra + r0 + i, s = sb + s0 + j;
+            if (isM) MS[r * LC + s] = r >= s ? acc[i][j] : 0.f;  // select, not mask-multiply
+            else AtS[r * LC + s] = r > s ? acc[i][j] : 0.f;
+          }
+      }
+      __syncthreads();
+    }
+    // X = (I + Diag(beta) A_tilde)^-1: forward substitution, one thread per column
+    if (tid < kC) {
+      const int s = tid;
+      for (int r = 0; r < kC; ++r) {
+        float x = r == s ? 1.f : 0.f;
+        if (r > s) {
+          float acc = 0.f;
+          for (int j = s; j < r; ++j) acc = fmaf(AtS[r * LC + j], XS[j * LC + s], acc);
+          x = -bS[r] * acc;
+        }
+        XS[r * LC + s] = x;
+      }
+    }
+    __syncthreads();
+    // T = X Diag(beta) (also transposed for the products below); records T, X, A_tilde, M
+    float* vS = sc;               // [C][LE]
+    float* TT = sc + kC * LE;     // [C][LC]
+    for (int i = tid; i < kC * kC; i += kThreads) {
+      const int r = i / kC, s = i % kC;
+      const float x = XS[r * LC + s], t = x * bS[s];
+      rec[L.T() + i] = t;
+      rec[L.X() + i] = x;
+      rec[L.At() + i] = AtS[r * LC + s];
+      rec[L.M() + i] = MS[r * LC + s];
+      TT[s * LC + r] = t;
+    }
+    for (int i = tid; i < kC * D; i += kThreads) {  // K_hat = k e^{G}, in place
+      const int r = i / D, c = i % D;
+      kS[r * LD + c] *= __expf(gS[r * LD + c]);
+    }
+    for (int i = tid; i < kC * E; i += kThreads) {
+      const int r = i / E, j = i % E;
+      vS[r * LE + j] = r < n ? to_f32(v[((size_t)(t0 + r) * H + h) * E + j]) : 0.f;
+    }
+    __syncthreads();
+    {  // W = T K_hat (and W^T)
+      const int m0 = 4 * (tid >> 4), n0 = (D / 16) * (tid & 15);
+      float acc[4][D / 16];
+      zero(acc);
+      kgemm<4, D / 16>(acc, TT, LC, m0, kS, LD, n0, kC);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+          rec[L.W() + (size_t)(m0 + i) * D + n0 + j] = acc[i][j];
+          rec[L.WT() + (size_t)(n0 + j) * kC + m0 + i] = acc[i][j];
+        }
+    }
+    {  // U_hat = T V
+      const int m0 = 4 * (tid >> 4), n0 = (E / 16) * (tid & 15);
+      float acc[4][E / 16];
+      zero(acc);
+      kgemm<4, E / 16>(acc, TT, LC, m0, vS, LE, n0, kC);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < E / 16; ++j) rec[L.Uh() + (size_t)(m0 + i) * E + n0 + j] = acc[i][j];
+    }
+    __syncthreads();  // shared memory is rewritten by the next task
+  }
+}
+
+// ---------------------------------------------------------------- the two serial passes
+// Each CTA: one (sequence, head) chain and ES of its value columns (the recurrence is separable in
+// the columns of the state).  Per chunk, 64 x ES and D x ES products with 4 x 4 register tiles.
+template <int D, int ES>
+__device__ __forceinline__ void tile_of(int idx, int& m0, int& n0) {  // idx < (rows / 4) x (ES / 4)
+  m0 = 4 * (idx / (ES / 4));
+  n0 = 4 * (idx % (ES / 4));
+}
+
+template <int D, int E, int ES>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int32_t* __restrict__ plan,
+        const int32_t* __restrict__ cu, int B, int64_t T, int H, float* __restrict__ states) {
+  __shared__ __align__(16) float S[D * ES];   // [D][ES]
+  __shared__ __align__(16) float U[kC * ES];  // [C][ES]
+  const int b = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * ES, tid = threadIdx.x;
+  if (cu != nullptr && plan[B + 1] == 0) return;
+  int64_t first_chunk, t_begin, len;
+  const int64_t nch = sequence_chunks(b, plan, cu, B, T, first_chunk, t_begin, len);
+  const RecLayout L{D, E};
+  const StateLayout SL{D, E};
+  for (int i = tid; i < D * ES; i += kThreads) {
+    const int c = i / ES, j = i % ES;
+    S[i] = h0 != nullptr ? h0[(((size_t)b * H + h) * D + c) * E + j0 + j] : 0.f;
+  }
+  __syncthreads();
+  for (int64_t ci = 0; ci < nch; ++ci) {
+    const size_t task = (size_t)(first_chunk + ci) * H + h;
+    const float* rec = recs + task * L.size();
+    float* st = states + task * SL.size();
+    for (int i = tid; i < D * ES; i += kThreads) {  // S0^T
+      const int c = i / ES, j = i % ES;
+      st[SL.S0T() + (size_t)(j0 + j) * D + c] = S[i];
+    }
+    for (int idx = tid; idx < (kC / 4) * (ES / 4); idx += kThreads) {  // U = U_hat - W S
+      int m0, n0;
+      tile_of<D, ES>(idx, m0, n0);
+      float acc[4][4];
+      zero(acc);
+      kgemm<4, 4>(acc, rec + L.WT(), kC, m0, S, ES, n0, D);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          U[(m0 + i) * ES + n0 + j] = rec[L.Uh() + (size_t)(m0 + i) * E + j0 + n0 + j] - acc[i][j];
+    }
+    __syncthreads();
+    for (int i = tid; i < kC * ES; i += kThreads) {  // U^T
+      const int r = i / ES, j = i % ES;
+      st[SL.UT() + (size_t)(j0 + j) * kC + r] = U[i];
+    }
+    for (int idx = tid; idx < (D / 4) * (ES / 4); idx += kThreads) {  // S <- Diag(e^{G_C}) S + K_bar^T U
+      int m0, n0;
+      tile_of<D, ES>(idx, m0, n0);
+      float acc[4][4];
+      zero(acc);
+      kgemm<4, 4>(acc, rec + L.Kb(), D, m0, U, ES, n0, kC);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float& s = S[(m0 + i) * ES + n0 + j];
+          s = fmaf(rec[L.GC() + m0 + i], s, acc[i][j]);
+        }
+    }
+    __syncthreads();
+  }
+}
+
+template <int D, int E, int ES, typename Tin>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const float* __restrict__ dhT,
+        const int32_t* __restrict__ plan, const int32_t* __restrict__ cu, int B, int64_t T, int H,
+        float* __restrict__ states, float* __restrict__ dh0) {
+  __shared__ __align__(16) float dS[D * ES];   // [D][ES]
+  __shared__ __align__(16) float dO[kC * ES];  // [C][ES]
+  __shared__ __align__(16) float dU[kC * ES];  // [C][ES]
+  const int b = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * ES, tid = threadIdx.x;
+  if (cu != nullptr && plan[B + 1] == 0) return;
+  int64_t first_chunk, t_begin, len;
+  const int64_t nch = sequence_chunks(b, plan, cu, B, T, first_chunk, t_begin, len);
+  const RecLayout L{D, E};
+  const StateLayout SL{D, E};
+  for (int i = tid; i < D * ES; i += kThreads) {
+    const int c = i / ES, j = i % ES;
+    dS[i] = dhT != nullptr ? dhT[(((size_t)b * H + h) * D + c) * E + j0 + j] : 0.f;
+  }
+  __syncthreads();
+  for (int64_t ci = nch - 1; ci >= 0; --ci) {
+    const size_t task = (size_t)(first_chunk + ci) * H + h;
+    const float* rec = recs + task * L.size();
+    float* st = states + task * SL.size();
+    const int64_t t0 = t_begin + 64 * ci;
+    const int n = (int)(len - 64 * ci < 64 ? len - 64 * ci : 64);
+    for (int i = tid; i < D * ES; i += kThreads) {  // dS_C^T
+      const int c = i / ES, j = i % ES;
+      st[SL.dST() + (size_t)(j0 + j) * D + c] = dS[i];
+    }
+    for (int i = tid; i < kC * ES; i += kThreads) {
+      const int r = i / ES, j = i % ES;
+      dO[i] = r < n ? to_f32(dout[((size_t)(t0 + r) * H + h) * E + j0 + j]) : 0.f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < (kC / 4) * (ES / 4); idx += kThreads) {  // dU = M^T dO + K_bar dS
+      int m0, n0;
+      tile_of<D, ES>(idx, m0, n0);
+      float acc[4][4];
+      zero(acc);
+      kgemm<4, 4>(acc, rec + L.M(), kC, m0, dO, ES, n0, kC);
+      kgemm<4, 4>(acc, rec + L.KbT(), kC, m0, dS, ES, n0, D);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dU[(m0 + i) * ES + n0 + j] = acc[i][j];
+    }
+    __syncthreads();
+    for (int i = tid; i < kC * ES; i += kThreads) {  // dU^T
+      const int r = i / ES, j = i % ES;
+      st[SL.dUT() + (size_t)(j0 + j) * kC + r] = dU[i];
+    }
+    for (int idx = tid; idx < (D / 4) * (ES / 4); idx += kThreads) {  // dS <- Q_hat^T dO + Diag(e^{G_C}) dS - W^T dU
+      int m0, n0;
+      tile_of<D, ES>(idx, m0, n0);
+      float a1[4][4], a2[4][4];
+      zero(a1);
+      zero(a2);
+      kgemm<4, 4>(a1, rec + L.Qh(), D, m0, dO, ES, n0, kC);
+      kgemm<4, 4>(a2, rec + L.W(), D, m0, dU, ES, n0, kC);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float& s = dS[(m0 + i) * ES + n0 + j];
+          s = fmaf(rec[L.GC() + m0 + i], s, a1[i][j] - a2[i][j]);
+        }
+    }
+    __syncthreads();
+  }
+  if (dh0 != nullptr)
+    for (int i = tid; i < D * ES; i += kThreads) {
+      const int c = i / ES, j = i % ES;
+      dh0[(((size_t)b * H + h) * D + c) * E + j0 + j] = dS[i];
+    }
+}
+
+// ---------------------------------------------------------------- gradients, part 1: sums over dv
+// Per (chunk, head) scratch written here and read by bwd_grads (floats).
+struct GradLayout {
+  int D;
+  __host__ __device__ size_t dQh() const { return 0; }                       // [C][D]
+  __host__ __device__ size_t dW() const { return (size_t)kC * D; }           // [C][D]
+  __host__ __device__ size_t dWT() const { return 2 * (size_t)kC * D; }      // [D][C]
+  __host__ __device__ size_t dKb() const { return 3 * (size_t)kC * D; }      // [C][D]
+  __host__ __device__ size_t dM() const { return 4 * (size_t)kC * D; }       // [C][C] (on M's support)
+  __host__ __device__ size_t dT1() const { return dM() + (size_t)kC * kC; }  // [C][C]: dU V^T
+  __host__ __device__ size_t dGam() const { return dT1() + (size_t)kC * kC; }  // [D]: rowsum(dS_C (.) S0)
+  __host__ __device__ size_t size() const { return dGam() + (size_t)D; }
+};
+
+template <int D, int E>
+struct DvSmem {
+  static constexpr int LC = kC + 4, LE = E + 4;
+  static constexpr int floats = 2 * E * LC + kC * LE;
+};
+
+// dQ_hat = dO S0^T, dW = -dU S0^T, dK_bar = U dS_C^T, dM = dO U^T, dU V^T, rowsum(dS_C (.) S0) into
+// the scratch; dv = T^T dU into the output.
+template <int D, int E, typename Tin>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_t* __restrict__ plan,
+           const int32_t* __restrict__ cu, int B, int64_t T, int H, int64_t ntask, const float* __restrict__ recs,
+           const float* __restrict__ states, float* __restrict__ grads, float* __restrict__ dv) {
+  using SM = DvSmem<D, E>;
+  constexpr int LC = SM::LC, LE = SM::LE;
+  extern __shared__ __align__(16) float sm[];
+  float* dOT = sm;           // [E][LC]
+  float* VT = dOT + E * LC;  // [E][LC]
+  float* dUr = VT + E * LC;  // [C][LE]
+  const int tid = threadIdx.x;
+  const RecLayout L{D, E};
+  const StateLayout SL{D, E};
+  const GradLayout GL{D};
+  for (int64_t task = blockIdx.x; task < ntask; task += gridDim.x) {
+    const int64_t chunk = task / H;
+    const int h = (int)(task - chunk * H);
+    int b, n;
+    int64_t t0, cseq;
+    if (!resolve_chunk(chunk, plan, cu, B, T, b, t0, n, cseq)) continue;
+    const float* rec = recs + (size_t)task * L.size();
+    const float* st = states + (size_t)task * SL.size();
+    float* gr = grads + (size_t)task * GL.size();
+    for (int i = tid; i < kC * E; i += kThreads) {
+      const int r = i / E, j = i % E;
+      const size_t src = ((size_t)(t0 + r) * H + h) * E + j;
+      dOT[j * LC + r] = r < n ? to_f32(dout[src]) : 0.f;
+      VT[j * LC + r] = r < n ? to_f32(v[src]) : 0.f;
+    }
+    for (int i = tid; i < kC * E; i += kThreads) {
+      const int j = i / kC, r = i % kC;
+      dUr[r * LE + j] = st[SL.dUT() + i];
+    }
+    __syncthreads();
+    {
+      const int m0 = 4 * (tid >> 4), n0 = (D / 16) * (tid & 15);
+      float a1[4][D / 16], a2[4][D / 16];
+      zero(a1);
+      zero(a2);
+      kgemm<4, D / 16>(a1, dOT, LC, m0, st + SL.S0T(), D, n0, E);         // dO S0^T
+      kgemm<4, D / 16>(a2, st + SL.dUT(), kC, m0, st + SL.S0T(), D, n0, E);  // dU S0^T
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+          gr[GL.dQh() + (size_t)(m0 + i) * D + n0 + j] = a1[i][j];
+          gr[GL.dW() + (size_t)(m0 + i) * D + n0 + j] = -a2[i][j];
+          gr[GL.dWT() + (size_t)(n0 + j) * kC + m0 + i] = -a2[i][j];
+        }
+      zero(a1);
+      kgemm<4, D / 16>(a1, st + SL.UT(), kC, m0, st + SL.dST(), D, n0, E);  // U dS_C^T
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) gr[GL.dKb() + (size_t)(m0 + i) * D + n0 + j] = a1[i][j];
+    }
+    {
+      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
+      float a1[4][4], a2[4][4];
+      zero(a1);
+      zero(a2);
+      kgemm<4, 4>(a1, dOT, LC, m0, st + SL.UT(), kC, n0, E);  // dO U^T
+      kgemm<4, 4>(a2, st + SL.dUT(), kC, m0, VT, LC, n0, E);  // dU V^T
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = m0 + i, s = n0 + j;
+          gr[GL.dM() + (size_t)r * kC + s] = r >= s ? a1[i][j] : 0.f;
+          gr[GL.dT1() + (size_t)r * kC + s] = a2[i][j];
+        }
+    }
+    {  // dv = T^T dU (rows of the sequence only)
+      const int m0 = 4 * (tid >> 4), n0 = (E / 16) * (tid & 15);
+      float acc[4][E / 16];
+      zero(acc);
+      kgemm<4, E / 16>(acc, rec + L.T(), kC, m0, dUr, LE, n0, kC);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (m0 + i < n)
+#pragma unroll
+          for (int j = 0; j < E / 16; ++j) dv[((size_t)(t0 + m0 + i) * H + h) * E + n0 + j] = acc[i][j];
+    }
+    if (tid < D) {
+      float s = 0.f;
+      for (int j = 0; j < E; ++j) s = fmaf(st[SL.dST() + (size_t)j * D + tid], st[SL.S0T() + (size_t)j * D + tid], s);
+      gr[GL.dGam() + tid] = s;
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- gradients, part 2
+template <int D>
+struct GradSmem {
+  static constexpr int LD = D + 4, LC = kC + 4;
+  static constexpr int base = 3 * kC * LD;  // k, q, G
+  static constexpr int R1 = 3 * kC * LC;    // P, P^T, dA / dM^T (and dT, dX^T before them)
+  static constexpr int R2a = 3 * 32 * LD, R2b = D * LC, R2c = 2 * kC * LC;
+  static constexpr int R2 = R2a > R2b ? (R2a > R2c ? R2a : R2c) : (R2b > R2c ? R2b : R2c);
+  static constexpr int floats = base + R1 + R2 + kC;
+};
+
+template <int D, int E, typename Tin>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_grads(const Tin* __restrict__ q, const Tin* __restrict__ k, const float* __restrict__ g,
+          const float* __restrict__ beta, const int32_t* __restrict__ plan, const int32_t* __restrict__ cu, int B,
+          int64_t T, int H, int64_t ntask, const float* __restrict__ recs, const float* __restrict__ grads,
+          float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dg, float* __restrict__ dbeta) {
+  using SM = GradSmem<D>;
+  constexpr int LD = SM::LD, LC = SM::LC;
+  extern __shared__ __align__(16) float sm[];
+  float* kS = sm;
+  float* qS = kS + kC * LD;  // q; rows of a finished half then hold that half's dG
+  float* gS = qS + kC * LD;  // G
+  float* s0 = gS + kC * LD;  // R1: three [C][LC]
+  float* s1 = s0 + kC * LC;
+  float* s2 = s1 + kC * LC;
+  float* r2 = s0 + SM::R1;   // R2
+  float* dbS = r2 + SM::R2;  // dbeta of the chunk's rows
+  const int tid = threadIdx.x;
+  const RecLayout L{D, E};
+  const GradLayout GL{D};
+  for (int64_t task = blockIdx.x; task < ntask; task += gridDim.x) {
+    const int64_t chunk = task / H;
+    const int h = (int)(task - chunk * H);
+    int b, n;
+    int64_t t0, cseq;
+    if (!resolve_chunk(chunk, plan, cu, B, T, b, t0, n, cseq)) continue;
+    const float* rec = recs + (size_t)task * L.size();
+    const float* gr = grads + (size_t)task * GL.size();
+    for (int i = tid; i < kC * D; i += kThreads) {
+      const int r = i / D, c = i % D;
+      const bool ok = r < n;
+      const size_t src = ((size_t)(t0 + r) * H + h) * D + c;
+      kS[r * LD + c] = ok ? to_f32(k[src]) : 0.f;
+      qS[r * LD + c] = ok ? to_f32(q[src]) : 0.f;
+      gS[r * LD + c] = ok ? g[src] : 0.f;
+    }
+    if (tid < kC) dbS[tid] = 0.f;
+    __syncthreads();
+    if (tid < D) {
+      float run = 0.f;
+      for (int r = 0; r < kC; ++r) {
+        run += gS[r * LD + tid];
+        gS[r * LD + tid] = run;
+      }
+    }
+    __syncthreads();
+    // ---- dT = dU V^T + dW K_hat^T
+    float* KhT = r2;  // [D][LC]
+    for (int i = tid; i < kC * D; i += kThreads) {
+      const int s = i / D, c = i % D;
+      KhT[c * LC + s] = kS[s * LD + c] * __expf(gS[s * LD + c]);
+    }
+    __syncthreads();
+    float* dTS = s0;
+    {
+      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
+      float acc[4][4];
+      zero(acc);
+      kgemm<4, 4>(acc, gr + GL.dWT(), kC, m0, KhT, LC, n0, D);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dTS[(m0 + i) * LC + n0 + j] = acc[i][j] + gr[GL.dT1() + (size_t)(m0 + i) * kC + n0 + j];
+    }
+    __syncthreads();
+    // ---- T = X Diag(beta): dbeta_s += sum_r X_rs dT_rs; dX = dT Diag(beta) (stored transposed); X^T
+    float* dXT = s1;
+    float* XT = r2;           // [C][LC] (K_hat^T is no longer needed)
+    float* YS = r2 + kC * LC;  // [C][LC]
+    if (tid < kC) {
+      const int s = tid;
+      const float bs = s < n ? beta[(size_t)(t0 + s) * H + h] : 0.f;
+      float acc = 0.f;
+      for (int r = 0; r < kC; ++r) {
+        const float dt = dTS[r * LC + s];
+        acc = fmaf(rec[L.X() + (size_t)r * kC + s], dt, acc);
+        dXT[s * LC + r] = dt * bs;
+      }
+      dbS[s] = acc;
+    }
+    for (int i = tid; i < kC * kC; i += kThreads) {
+      const int s = i / kC, j = i % kC;
+      XT[j * LC + s] = rec[L.X() + i];
+    }
+    __syncthreads();
+    // ---- dA = -X^T dX X^T on the strict lower triangle (Y = dX X^T first)
+    {
+      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
+      float acc[4][4];
+      zero(acc);
+      kgemm<4, 4>(acc, dXT, LC, m0, XT, LC, n0, kC);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) YS[(m0 + i) * LC + n0 + j] = acc[i][j];
+    }
+    __syncthreads();
+    float* PS = s0;   // P = Diag(beta) dA
+    float* PT = s1;   // P^T
+    float* dAS = s2;  // dA, then dM^T
+    {
+      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
+      float acc[4][4];
+      zero(acc);
+      kgemm<4, 4>(acc, rec + L.X(), kC, m0, YS, LC, n0, kC);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = m0 + i;
+        const float br = r < n ? beta[(size_t)(t0 + r) * H + h] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int s = n0 + j;
+          const float da = r > s ? -acc[i][j] : 0.f;
+          dAS[r * LC + s] = da;
+          PS[r * LC + s] = br * da;
+          PT[s * LC + r] = br * da;
+        }
+      }
+    }
+    __syncthreads();
+    if (tid < kC) {  // dbeta_r += sum_s dA_rs A_tilde_rs
+      const int r = tid;
+      float acc = 0.f;
+      for (int s = 0; s < r; ++s) acc = fmaf(dAS[r * LC + s], rec[L.At() + (size_t)r * kC + s], acc);
+      dbS[r] += acc;
+    }
+    __syncthreads();
+    float* dMT = s2;
+    for (int i = tid; i < kC * kC; i += kThreads) {
+      const int r = i / kC, s = i % kC;
+      dMT[s * LC + r] = gr[GL.dM() + i];
+    }
+    __syncthreads();
+    // ---- the A / M terms and the elementwise terms, one 32-row output half at a time; each thread
+    // owns a 4 x 4 tile of the half's dq, dk and dG
+    float* Xk = r2;               // [32][LD] k e^{G - R} of the block's row half
+    float* Xq = r2 + 32 * LD;     // [32][LD] q e^{G - R}
+    float* Yk = r2 + 64 * LD;     // [32][LD] k e^{R - G} of the block's column half
+    constexpr int TILES = 8 * (D / 4);  // 4 x 4 tiles of a 32 x D half
+    const bool own = tid < TILES;
+    const int tm = own ? 4 * (tid / (D / 4)) : 0, tn = own ? 4 * (tid % (D / 4)) : 0;
+    for (int ho = 0; ho < 2; ++ho) {
+      float aq[4][4], ak[4][4], aG[4][4];
+      zero(aq);
+      zero(ak);
+      zero(aG);
+      for (int blk = 0; blk < 3; ++blk) {
+        const int a = blk == 0 ? 0 : 1, bb = blk == 1 ? 1 : 0, ref = blk == 0 ? 15 : 47;
+        const bool rows_side = a == ho, cols_side = bb == ho;
+        if (!rows_side && !cols_side) continue;  // same for every thread
+        for (int i = tid; i < 32 * D; i += kThreads) {
+          const int r = i / D, c = i % D;
+          const float R = gS[ref * LD + c];
+          const float er = __expf(gS[(32 * a + r) * LD + c] - R);
+          Xk[r * LD + c] = kS[(32 * a + r) * LD + c] * er;
+          Xq[r * LD + c] = qS[(32 * a + r) * LD + c] * er;
+          Yk[r * LD + c] = kS[(32 * bb + r) * LD + c] * __expf(R - gS[(32 * bb + r) * LD + c]);
+        }
+        __syncthreads();
+        if (own) {
+          if (rows_side) {  // rows r of half a: sum_s P_rs k_s e^{G_r - G_s}, sum_s dM_rs k_s e^{G_r - G_s}
+            float t1[4][4], t2[4][4];
+            zero(t1);
+            zero(t2);
+            kgemm<4, 4>(t1, PT + 32 * bb * LC, LC, 32 * a + tm, Yk, LD, tn, 32);
+            kgemm<4, 4>(t2, dMT + 32 * bb * LC, LC, 32 * a + tm, Yk, LD, tn, 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int r = 32 * a + tm + i, c = tn + j;
+                const float f = __expf(gS[r * LD + c] - gS[ref * LD + c]);
+                const float pa = f * t1[i][j], pm = f * t2[i][j];
+                ak[i][j] += pa;
+                aq[i][j] += pm;
+                aG[i][j] += kS[r * LD + c] * pa + qS[r * LD + c] * pm;
+              }
+          }
+          if (cols_side) {  // rows s of half bb: sum_r P_rs k_r e^{G_r - G_s}, sum_r dM_rs q_r e^{G_r - G_s}
+            float t3[4][4], t4[4][4];
+            zero(t3);
+            zero(t4);
+            kgemm<4, 4>(t3, PS + 32 * a * LC, LC, 32 * bb + tm, Xk, LD, tn, 32);
+            kgemm<4, 4>(t4, gr + GL.dM() + (size_t)32 * a * kC, kC, 32 * bb + tm, Xq, LD, tn, 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int s = 32 * bb + tm + i, c = tn + j;
+                const float f = __expf(gS[ref * LD + c] - gS[s * LD + c]);
+                const float pa = f * t3[i][j], pm = f * t4[i][j];
+                ak[i][j] += pa + pm;
+                aG[i][j] -= kS[s * LD + c] * (pa + pm);
+              }
+          }
+        }
+        __syncthreads();
+      }
+      if (own) {
+        // dK_hat = T^T dW, and the terms through Q_hat, K_hat and K_bar
+        float t5[4][4];
+        zero(t5);
+        kgemm<4, 4>(t5, rec + L.T(), kC, 32 * ho + tm, gr + GL.dW(), D, tn, kC);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 32 * ho + tm + i;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = tn + j;
+            const float G = gS[r * LD + c], Gc = gS[(kC - 1) * LD + c];
+            const float gam = __expf(G), eb = __expf(Gc - G), kv = kS[r * LD + c], qv = qS[r * LD + c];
+            const float dqh = gr[GL.dQh() + (size_t)r * D + c], dkb = gr[GL.dKb() + (size_t)r * D + c];
+            aq[i][j] += dqh * gam;
+            ak[i][j] += t5[i][j] * gam + dkb * eb;
+            aG[i][j] += dqh * qv * gam + t5[i][j] * kv * gam - dkb * kv * eb;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 32 * ho + tm + i;
+          if (r < n) {
+            const size_t o = ((size_t)(t0 + r) * H + h) * D + tn;
+            *reinterpret_cast<float4*>(dq + o) = make_float4(aq[i][0], aq[i][1], aq[i][2], aq[i][3]);
+            *reinterpret_cast<float4*>(dk + o) = make_float4(ak[i][0], ak[i][1], ak[i][2], ak[i][3]);
+          }
+        }
+      }
+      __syncthreads();  // q rows of this half are no longer read: they receive its dG
+      if (own)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) qS[(32 * ho + tm + i) * LD + tn + j] = aG[i][j];
+      __syncthreads();
+    }
+    // ---- dg: reverse cumulative sum of dG, with G_C's terms on the last row
+    if (tid < D) {
+      const int c = tid;
+      const float Gc = gS[(kC - 1) * LD + c];
+      float last = gr[GL.dGam() + c] * __expf(Gc);
+      for (int r = 0; r < kC; ++r)
+        last = fmaf(gr[GL.dKb() + (size_t)r * D + c], kS[r * LD + c] * __expf(Gc - gS[r * LD + c]), last);
+      float run = last;
+      for (int r = kC - 1; r >= 0; --r) {
+        run += qS[r * LD + c];
+        if (r < n) dg[((size_t)(t0 + r) * H + h) * D + c] = run;
+      }
+    }
+    if (tid < n) dbeta[(size_t)(t0 + tid) * H + h] = dbS[tid];
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- host side
+int serial_slices(int B, int H, int E) {  // value-column slices of the two serial passes
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  const int64_t chains = (int64_t)B * H;
+  for (int n = 8; n > 1; n /= 2)
+    if (chains * n <= 2 * (int64_t)sms && E / n >= 16) return n;
+  return 1;
+}
+
+template <int D, int E, int ES, typename Tin>
+cudaError_t launch_serial(const BackwardArgs& a, const float* recs, float* states, cudaStream_t st) {
+  const dim3 grid((unsigned)a.B, (unsigned)a.H, (unsigned)(E / ES));
+  bwd_fwd<D, E, ES><<<grid, kThreads, 0, st>>>(recs, a.h0, a.plan, a.cu_seqlens, a.B, a.T, a.H, states);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_rev<D, E, ES, Tin><<<grid, kThreads, 0, st>>>(recs, static_cast<const Tin*>(a.dout), a.dhT, a.plan,
+                                                      a.cu_seqlens, a.B, a.T, a.H, states, a.dh0);
+  return cudaGetLastError();
+}
+
+template <int D, int E, typename Tin>
+cudaError_t launch_chunked(const BackwardArgs& a, float* ws, cudaStream_t st) {
+  static bool attr_done[64] = {};
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  constexpr size_t rec_smem = RecSmem<D, E>::floats * sizeof(float);
+  constexpr size_t dv_smem = DvSmem<D, E>::floats * sizeof(float);
+  constexpr size_t gr_smem = GradSmem<D>::floats * sizeof(float);
+  if (!attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_rec<D, E, Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rec_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bwd_dvsums<D, E, Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dv_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bwd_grads<D, E, Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gr_smem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const int64_t ntask = max_chunks(a.B, a.T, a.cu_seqlens != nullptr) * a.H;
+  if (ntask == 0) return cudaSuccess;
+  float* recs = ws;
+  float* states = recs + (size_t)ntask * RecLayout{D, E}.size();
+  float* grads = states + (size_t)ntask * StateLayout{D, E}.size();
+  const int grid = (int)(ntask < sms ? ntask : sms);
+  const Tin* q = static_cast<const Tin*>(a.q);
+  const Tin* k = static_cast<const Tin*>(a.k);
+  const Tin* v = static_cast<const Tin*>(a.v);
+  {
+    TraceScope ts("kda_bwd_records", st);
+    bwd_rec<D, E, Tin><<<grid, kThreads, rec_smem, st>>>(q, k, v, a.g, a.beta, a.plan, a.cu_seqlens, a.B, a.T, a.H,
+                                                          ntask, recs);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    TraceScope ts("kda_bwd_state_passes", st);
+    const int nsl = serial_slices(a.B, a.H, E);
+    cudaError_t e = nsl == 8   ? launch_serial<D, E, E / 8, Tin>(a, recs, states, st)
+                    : nsl == 4 ? launch_serial<D, E, E / 4, Tin>(a, recs, states, st)
+                    : nsl == 2 ? launch_serial<D, E, E / 2, Tin>(a, recs, states, st)
+                               : launch_serial<D, E, E, Tin>(a, recs, states, st);
+    if (e != cudaSuccess) return e;
+  }
+  TraceScope ts("kda_bwd_chunk_grads", st);
+  bwd_dvsums<D, E, Tin><<<grid, kThreads, dv_smem, st>>>(v, static_cast<const Tin*>(a.dout), a.plan, a.cu_seqlens, a.B,
+                                                          a.T, a.H, ntask, recs, states, grads, a.dv);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_grads<D, E, Tin><<<grid, kThreads, gr_smem, st>>>(q, k, a.g, a.beta, a.plan, a.cu_seqlens, a.B, a.T, a.H, ntask,
+                                                         recs, grads, a.dq, a.dk, a.dg, a.dbeta);
+  return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_chunked_dims(const BackwardArgs& a, float* ws, cudaStream_t st) {
+  if (a.dim_k == 128 && a.dim_v == 128) return launch_chunked<128, 128, Tin>(a, ws, st);
+  if (a.dim_k == 64 && a.dim_v == 64) return launch_chunked<64, 64, Tin>(a, ws, st);
+  if (a.dim_k == 128 && a.dim_v == 64) return launch_chunked<128, 64, Tin>(a, ws, st);
+  if (a.dim_k == 64 && a.dim_v == 128) return launch_chunked<64, 128, Tin>(a, ws, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+size_t backward_chunked_bytes(int B, int64_t T, int H, int dk, int dv, bool has_cu) {
+  const int64_t ntask = max_chunks(B, T, has_cu) * H;
+  const size_t per = RecLayout{dk, dv}.size() + StateLayout{dk, dv}.size() + GradLayout{dk}.size();
+  return (size_t)ntask * per * sizeof(float);
+}
+
+cudaError_t backward_chunked_launch(const BackwardArgs& a, float* ws, cudaStream_t st) {
+  return a.bf16 ? launch_chunked_dims<__nv_bfloat16>(a, ws, st) : launch_chunked_dims<float>(a, ws, st);
+}
+
+}  // namespace kda

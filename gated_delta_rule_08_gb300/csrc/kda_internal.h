@@ -86,6 +86,9 @@ struct BackwardArgs {
 };
 int backward_slices(int B, int H, int dv);  // value-column slices per chain (1, 2 or 4)
 size_t backward_scratch_bytes(int B, int64_t T, int H, int dk, int dv, bool has_cu);
+// chunkwise backward (kda_backward_chunk.cu): per-chunk records, states and gradient scratch
+size_t backward_chunked_bytes(int B, int64_t T, int H, int dk, int dv, bool has_cu);
+cudaError_t backward_chunked_launch(const BackwardArgs& a, float* workspace, cudaStream_t stream);
 cudaError_t backward_launch(const BackwardArgs& a, cudaStream_t stream);
 
 // Upper bound on the number of 64-token chunks of a packed batch:
