@@ -309,8 +309,8 @@ def run_ours(args, world, rank, local):
     # the pipelined calls computed what the resident-input calls did
     assert torch.equal(out_h[(args.steps - 1) % nb], out.cpu()) and torch.equal(hT_h[(args.steps - 1) % nb], hT.cpu())
 
-    # backward of the prefill recurrence (no epilogue) on the same workload: a first, CUDA-core
-    # version; timed beside the step, not part of the metric
+    # backward of the prefill recurrence (no epilogue) on the same workload, fp32 on the CUDA cores;
+    # timed beside the step, not part of the metric
     gen = torch.Generator(device=dev).manual_seed(11)
     dout = torch.randn(out.shape, generator=gen, device=dev).to(out.dtype)
     bws = torch.empty(binding.kda_chunk_bwd_workspace_size(1, T, H, pcfg.dk, pcfg.dv), device=dev, dtype=torch.uint8)
@@ -365,7 +365,8 @@ def run_ours(args, world, rank, local):
         "kernels": {k: {"launches": v[0], "total_ms": round(v[1], 4)} for k, v in trace.items()},
         "gpu_launches": launches,
         "backward": {"ms_per_call": round(bwd_ms, 3), "tokens_per_s": round(aggregate(T, world, bwd_ms / 1e3), 1),
-                     "kernel": "kda_bwd_token (fp32 CUDA cores, per-token reverse sweep)"},
+                     "kernel": "chunkwise, fp32 CUDA cores: per-chunk records, serial state passes over "
+                               "chunks, per-chunk gradients"},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),

@@ -30,6 +30,7 @@ namespace {
 
 constexpr int kC = 64;         // chunk length
 constexpr int kThreads = 256;  // every kernel here
+static_assert(kThreads == 4 * kC, "the diagonal inverses in bwd_rec give each column four lanes");
 
 // acc[i][j] += sum_{k < K} At[k * lda + m0 + i] * B[k * ldb + n0 + j]: a register tile of a product
 // whose operands are both stored k-major (At: the left factor transposed).  MI and NJ are multiples
@@ -38,7 +39,7 @@ constexpr int kThreads = 256;  // every kernel here
 template <int MI, int NJ>
 __device__ __forceinline__ void kgemm(float (&acc)[MI][NJ], const float* At, int lda, int m0, const float* B, int ldb,
                                       int n0, int K) {
-#pragma unroll 2
+#pragma unroll 8  // K is a multiple of 8: eight k-steps of loads in flight
   for (int k = 0; k < K; ++k) {
     float a[MI], b[NJ];
 #pragma unroll
@@ -63,6 +64,48 @@ __device__ __forceinline__ void zero(float (&acc)[MI][NJ]) {
   for (int i = 0; i < MI; ++i)
 #pragma unroll
     for (int j = 0; j < NJ; ++j) acc[i][j] = 0.f;
+}
+
+// for (i = tid; i < n; i += kThreads) put(i, get(i)), with eight loads in flight per thread before
+// their stores (the gets are global loads, the puts shared-memory stores)
+template <class Get, class Put>
+__device__ __forceinline__ void batched(int n, int tid, Get get, Put put) {
+  for (int base = tid; base < n; base += 8 * kThreads) {
+    decltype(get(0)) x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + u * kThreads;
+      if (i < n) x[u] = get(i);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + u * kThreads;
+      if (i < n) put(i, x[u]);
+    }
+  }
+}
+
+// bytes (a multiple of 16) from a 16-byte aligned global address into L2, without waiting
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// the D (or E) values of rows t0 .. t0+n-1 of head h of a [T][H][D] array into L2, thread tid0 + r
+// taking row r (rows are 16-byte aligned: D * sizeof(T) is a multiple of 16)
+template <typename Tp>
+__device__ __forceinline__ void prefetch_rows_l2(const Tp* x, int64_t t0, int n, int H, int h, int D, int tid, int tid0) {
+  const int r = tid - tid0;
+  if (r >= 0 && r < n) prefetch_l2(x + ((size_t)(t0 + r) * H + h) * D, (uint32_t)(D * sizeof(Tp)));
+}
+
+// The (chunk, head) task that this CTA takes next: true with its rows when it exists.
+__device__ __forceinline__ bool next_task(int64_t task, int64_t ntask, int H, const int32_t* plan, const int32_t* cu,
+                                          int B, int64_t T, int& h, int64_t& t0, int& n) {
+  const int64_t nt = task + gridDim.x;
+  int b;
+  int64_t cseq;
+  if (nt >= ntask || !resolve_chunk(nt / H, plan, cu, B, T, b, t0, n, cseq)) return false;
+  h = (int)(nt % H);
+  return true;
 }
 
 // Per-(chunk, head) record layout in the workspace (floats).
@@ -102,6 +145,49 @@ struct RecSmem {
   static constexpr int floats = 3 * kC * LD + SC + 3 * kC * LC + kC;
 };
 
+// 16-byte pieces (16 / sizeof(Tp) values) of a [C][D] tile of head h, rows n.. reading as zero, widened
+// to fp32 in shared memory (row stride ld, a multiple of 4)
+template <int D, typename Tp>
+struct TileLoad {
+  static constexpr int V = 16 / sizeof(Tp), PER_ROW = D / V, PIECES = kC * PER_ROW;
+  static_assert(PIECES % kThreads == 0, "whole pieces per thread");
+  static constexpr int N = PIECES / kThreads;
+  uint4 x[N];
+  __device__ __forceinline__ void load(const Tp* a, int64_t t0, int n, int H, int h, int tid) {
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+      const int i = tid + u * kThreads, r = i / PER_ROW;
+      x[u] = r < n ? *reinterpret_cast<const uint4*>(a + ((size_t)(t0 + r) * H + h) * D + V * (i % PER_ROW))
+                   : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  __device__ __forceinline__ void store(float* dst, int ld, int tid) const {
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+      const int i = tid + u * kThreads;
+      float* o = dst + (i / PER_ROW) * ld + V * (i % PER_ROW);
+      const Tp* e = reinterpret_cast<const Tp*>(&x[u]);
+#pragma unroll
+      for (int w = 0; w < V; w += 4)
+        *reinterpret_cast<float4*>(o + w) = make_float4(to_f32(e[w]), to_f32(e[w + 1]), to_f32(e[w + 2]), to_f32(e[w + 3]));
+    }
+  }
+};
+// k, q and g of one chunk into shared memory (row stride ld); rows n..C-1 are zero.  Every load is
+// issued before the first store.
+template <int D, typename Tin>
+__device__ __forceinline__ void load_kqg(const Tin* k, const Tin* q, const float* g, int64_t t0, int n, int H, int h,
+                                         float* kS, float* qS, float* gS, int ld, int tid) {
+  TileLoad<D, Tin> tk, tq;
+  TileLoad<D, float> tg;
+  tk.load(k, t0, n, H, h, tid);
+  tq.load(q, t0, n, H, h, tid);
+  tg.load(g, t0, n, H, h, tid);
+  tk.store(kS, ld, tid);
+  tq.store(qS, ld, tid);
+  tg.store(gS, ld, tid);
+}
+
 template <int D, int E, typename Tin>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v, const float* __restrict__ g,
@@ -127,15 +213,18 @@ bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restr
     int64_t t0, cseq;
     if (!resolve_chunk(chunk, plan, cu, B, T, b, t0, n, cseq)) continue;  // same for the whole CTA
     float* rec = recs + (size_t)task * L.size();
-    // inputs of the chunk (rows past the sequence end: k = q = 0, g = 0, beta = 0)
-    for (int i = tid; i < kC * D; i += kThreads) {
-      const int r = i / D, c = i % D;
-      const bool ok = r < n;
-      const size_t src = ((size_t)(t0 + r) * H + h) * D + c;
-      kS[r * LD + c] = ok ? to_f32(k[src]) : 0.f;
-      qS[r * LD + c] = ok ? to_f32(q[src]) : 0.f;
-      gS[r * LD + c] = ok ? g[src] : 0.f;
+    {  // the next task's inputs into L2 while this one runs
+      int h2, n2;
+      int64_t t2;
+      if (next_task(task, ntask, H, plan, cu, B, T, h2, t2, n2)) {
+        prefetch_rows_l2(k, t2, n2, H, h2, D, tid, 0);
+        prefetch_rows_l2(q, t2, n2, H, h2, D, tid, 64);
+        prefetch_rows_l2(g, t2, n2, H, h2, D, tid, 128);
+        prefetch_rows_l2(v, t2, n2, H, h2, E, tid, 192);
+      }
     }
+    // inputs of the chunk (rows past the sequence end: k = q = 0, g = 0, beta = 0)
+    load_kqg<D>(k, q, g, t0, n, H, h, kS, qS, gS, LD, tid);
     if (tid < kC) bS[tid] = tid < n ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
     for (int i = tid; i < kC * LC; i += kThreads) {
       AtS[i] = 0.f;
@@ -194,20 +283,46 @@ bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restr
       }
       __syncthreads();
     }
-    // X = (I + Diag(beta) A_tilde)^-1: forward substitution, one thread per column
-    if (tid < kC) {
-      const int s = tid;
-      for (int r = 0; r < kC; ++r) {
-        float x = r == s ? 1.f : 0.f;
-        if (r > s) {
-          float acc = 0.f;
-          for (int j = s; j < r; ++j) acc = fmaf(AtS[r * LC + j], XS[j * LC + s], acc);
-          x = -bS[r] * acc;
-        }
-        XS[r * LC + s] = x;
+    // X = (I + A)^-1 with A = Diag(beta) A_tilde strictly lower, by blocks.  First the four diagonal
+    // 16 x 16 inverses by forward substitution, X_rs = -beta_r sum_{s <= j < r} A_tilde_rj X_js: each
+    // column is owned by four adjacent lanes, lane p summing the terms j = s + p (mod 4).
+    {
+      const int o = 16 * (tid >> 6), s = (tid >> 2) & 15, p = tid & 3;
+      for (int r = 0; r < 16; ++r) {
+        float part = 0.f;
+        for (int j = s + p; j < r; j += 4) part = fmaf(AtS[(o + r) * LC + o + j], XS[(o + j) * LC + o + s], part);
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        if (p == 0) XS[(o + r) * LC + o + s] = r > s ? -bS[o + r] * part : (r == s ? 1.f : 0.f);
+        __syncwarp();  // column s of the block is read back only by its own four lanes
       }
+      for (int i = tid; i < kC * kC; i += kThreads)  // the blocks above the diagonal
+        if ((i / kC) >> 4 < (i % kC) >> 4) XS[(i / kC) * LC + i % kC] = 0.f;
     }
     __syncthreads();
+    // Then pairs of diagonal blocks of size m are merged into blocks of size 2m: with
+    // [[X11, 0], [X21, X22]] the inverse of [[I + A11, 0], [A21, I + A22]], X21 = -X22 A21 X11.
+    for (int m = 16; m < kC; m *= 2) {
+      constexpr int LY = 32 + 4;
+      float* Y = sc;  // [kC / 2][LY]: A21 X11 of every merged block, stacked
+      const int outs = (kC / 2) * m;
+      for (int i = tid; i < outs; i += kThreads) {
+        const int bi = i / (m * m), rr = (i / m) % m, cc = i % m, o = 2 * m * bi;
+        float acc = 0.f;
+        for (int j = cc; j < m; ++j)  // X11 is lower triangular
+          acc = fmaf(AtS[(o + m + rr) * LC + o + j], XS[(o + j) * LC + o + cc], acc);
+        Y[(bi * m + rr) * LY + cc] = bS[o + m + rr] * acc;
+      }
+      __syncthreads();
+      for (int i = tid; i < outs; i += kThreads) {
+        const int bi = i / (m * m), rr = (i / m) % m, cc = i % m, o = 2 * m * bi;
+        float acc = 0.f;
+        for (int j = 0; j <= rr; ++j)  // X22 is lower triangular
+          acc = fmaf(XS[(o + m + rr) * LC + o + m + j], Y[(bi * m + j) * LY + cc], acc);
+        XS[(o + m + rr) * LC + o + cc] = -acc;
+      }
+      __syncthreads();
+    }
     // T = X Diag(beta) (also transposed for the products below); records T, X, A_tilde, M
     float* vS = sc;               // [C][LE]
     float* TT = sc + kC * LE;     // [C][LC]
@@ -224,10 +339,8 @@ bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restr
       const int r = i / D, c = i % D;
       kS[r * LD + c] *= __expf(gS[r * LD + c]);
     }
-    for (int i = tid; i < kC * E; i += kThreads) {
-      const int r = i / E, j = i % E;
-      vS[r * LE + j] = r < n ? to_f32(v[((size_t)(t0 + r) * H + h) * E + j]) : 0.f;
-    }
+    batched(kC * E, tid, [&](int i) { const int r = i / E; return r < n ? to_f32(v[((size_t)(t0 + r) * H + h) * E + i % E]) : 0.f; },
+            [&](int i, float x) { vS[(i / E) * LE + i % E] = x; });
     __syncthreads();
     {  // W = T K_hat (and W^T)
       const int m0 = 4 * (tid >> 4), n0 = (D / 16) * (tid & 15);
@@ -265,12 +378,33 @@ __device__ __forceinline__ void tile_of(int idx, int& m0, int& n0) {  // idx < (
   n0 = 4 * (idx % (ES / 4));
 }
 
+// rows x cols floats from global (row stride gld) into shared memory (row stride sld), 16-byte copies
+__device__ __forceinline__ void stage(float* dst, int sld, const float* src, size_t gld, int rows, int cols, int tid) {
+  const int q = cols / 4;
+  batched(rows * q, tid,
+          [&](int i) { return *reinterpret_cast<const float4*>(src + (size_t)(i / q) * gld + 4 * (i % q)); },
+          [&](int i, float4 x) { *reinterpret_cast<float4*>(dst + (i / q) * sld + 4 * (i % q)) = x; });
+}
+
+template <int D, int E, int ES>
+struct FwdSmem {
+  static constexpr int LC = kC + 4, LD = D + 4, LS = ES + 4;
+  static constexpr int floats = D * LC + kC * LD + kC * LS + D + D * ES + kC * ES;
+};
+
 template <int D, int E, int ES>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int32_t* __restrict__ plan,
         const int32_t* __restrict__ cu, int B, int64_t T, int H, float* __restrict__ states) {
-  __shared__ __align__(16) float S[D * ES];   // [D][ES]
-  __shared__ __align__(16) float U[kC * ES];  // [C][ES]
+  using SM = FwdSmem<D, E, ES>;
+  constexpr int LC = SM::LC, LD = SM::LD, LS = SM::LS;
+  extern __shared__ __align__(16) float sm[];
+  float* WTs = sm;              // W^T [D][LC]
+  float* Kbs = WTs + D * LC;    // K_bar [C][LD]
+  float* Uhs = Kbs + kC * LD;   // U_hat slice [C][LS]
+  float* GCs = Uhs + kC * LS;   // e^{G_C} [D]
+  float* S = GCs + D;           // [D][ES]
+  float* U = S + D * ES;        // [C][ES]
   const int b = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * ES, tid = threadIdx.x;
   if (cu != nullptr && plan[B + 1] == 0) return;
   int64_t first_chunk, t_begin, len;
@@ -281,11 +415,20 @@ bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int3
     const int c = i / ES, j = i % ES;
     S[i] = h0 != nullptr ? h0[(((size_t)b * H + h) * D + c) * E + j0 + j] : 0.f;
   }
-  __syncthreads();
   for (int64_t ci = 0; ci < nch; ++ci) {
     const size_t task = (size_t)(first_chunk + ci) * H + h;
     const float* rec = recs + task * L.size();
     float* st = states + task * SL.size();
+    if (tid == 0 && ci + 1 < nch) {  // the next chunk's records: W^T, U_hat, K_bar (adjacent) and e^{G_C}
+      const float* nx = rec + (size_t)H * L.size();
+      prefetch_l2(nx + L.WT(), (uint32_t)((L.Kb() + (size_t)kC * D - L.WT()) * 4));
+      prefetch_l2(nx + L.GC(), D * 4);
+    }
+    stage(WTs, LC, rec + L.WT(), kC, D, kC, tid);
+    stage(Kbs, LD, rec + L.Kb(), D, kC, D, tid);
+    stage(Uhs, LS, rec + L.Uh() + j0, E, kC, ES, tid);
+    stage(GCs, D, rec + L.GC(), D, 1, D, tid);
+    __syncthreads();
     for (int i = tid; i < D * ES; i += kThreads) {  // S0^T
       const int c = i / ES, j = i % ES;
       st[SL.S0T() + (size_t)(j0 + j) * D + c] = S[i];
@@ -295,12 +438,11 @@ bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int3
       tile_of<D, ES>(idx, m0, n0);
       float acc[4][4];
       zero(acc);
-      kgemm<4, 4>(acc, rec + L.WT(), kC, m0, S, ES, n0, D);
+      kgemm<4, 4>(acc, WTs, LC, m0, S, ES, n0, D);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          U[(m0 + i) * ES + n0 + j] = rec[L.Uh() + (size_t)(m0 + i) * E + j0 + n0 + j] - acc[i][j];
+        for (int j = 0; j < 4; ++j) U[(m0 + i) * ES + n0 + j] = Uhs[(m0 + i) * LS + n0 + j] - acc[i][j];
     }
     __syncthreads();
     for (int i = tid; i < kC * ES; i += kThreads) {  // U^T
@@ -312,27 +454,41 @@ bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int3
       tile_of<D, ES>(idx, m0, n0);
       float acc[4][4];
       zero(acc);
-      kgemm<4, 4>(acc, rec + L.Kb(), D, m0, U, ES, n0, kC);
+      kgemm<4, 4>(acc, Kbs, LD, m0, U, ES, n0, kC);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          float& s = S[(m0 + i) * ES + n0 + j];
-          s = fmaf(rec[L.GC() + m0 + i], s, acc[i][j]);
+          float& sv = S[(m0 + i) * ES + n0 + j];
+          sv = fmaf(GCs[m0 + i], sv, acc[i][j]);
         }
     }
     __syncthreads();
   }
 }
 
+template <int D, int E, int ES>
+struct RevSmem {
+  static constexpr int LC = kC + 4, LD = D + 4;
+  static constexpr int floats = kC * LC + D * LC + 2 * kC * LD + D + D * ES + 2 * kC * ES;
+};
+
 template <int D, int E, int ES, typename Tin>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const float* __restrict__ dhT,
         const int32_t* __restrict__ plan, const int32_t* __restrict__ cu, int B, int64_t T, int H,
         float* __restrict__ states, float* __restrict__ dh0) {
-  __shared__ __align__(16) float dS[D * ES];   // [D][ES]
-  __shared__ __align__(16) float dO[kC * ES];  // [C][ES]
-  __shared__ __align__(16) float dU[kC * ES];  // [C][ES]
+  using SM = RevSmem<D, E, ES>;
+  constexpr int LC = SM::LC, LD = SM::LD;
+  extern __shared__ __align__(16) float sm[];
+  float* Ms = sm;               // M [C][LC]
+  float* KbTs = Ms + kC * LC;   // K_bar^T [D][LC]
+  float* Qhs = KbTs + D * LC;   // Q_hat [C][LD]
+  float* Ws = Qhs + kC * LD;    // W [C][LD]
+  float* GCs = Ws + kC * LD;    // [D]
+  float* dS = GCs + D;          // [D][ES]
+  float* dO = dS + D * ES;      // [C][ES]
+  float* dU = dO + kC * ES;     // [C][ES]
   const int b = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * ES, tid = threadIdx.x;
   if (cu != nullptr && plan[B + 1] == 0) return;
   int64_t first_chunk, t_begin, len;
@@ -343,29 +499,45 @@ bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const floa
     const int c = i / ES, j = i % ES;
     dS[i] = dhT != nullptr ? dhT[(((size_t)b * H + h) * D + c) * E + j0 + j] : 0.f;
   }
-  __syncthreads();
   for (int64_t ci = nch - 1; ci >= 0; --ci) {
     const size_t task = (size_t)(first_chunk + ci) * H + h;
     const float* rec = recs + task * L.size();
     float* st = states + task * SL.size();
     const int64_t t0 = t_begin + 64 * ci;
     const int n = (int)(len - 64 * ci < 64 ? len - 64 * ci : 64);
-    for (int i = tid; i < D * ES; i += kThreads) {  // dS_C^T
-      const int c = i / ES, j = i % ES;
-      st[SL.dST() + (size_t)(j0 + j) * D + c] = dS[i];
+    if (ci > 0) {  // the previous chunk's records (M, W, K_bar^T and Q_hat, e^{G_C}) and dout rows
+      const float* nx = rec - (size_t)H * L.size();
+      if (tid == 0) {
+        prefetch_l2(nx + L.M(), kC * kC * 4);
+        prefetch_l2(nx + L.W(), kC * D * 4);
+        prefetch_l2(nx + L.KbT(), 2 * kC * D * 4);
+        prefetch_l2(nx + L.GC(), D * 4);
+      } else if (tid >= 64 && tid < 64 + kC) {
+        const Tin* row = dout + ((size_t)(t0 - 64 + tid - 64) * H + h) * E + j0;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row) : "memory");
+      }
     }
+    stage(Ms, LC, rec + L.M(), kC, kC, kC, tid);
+    stage(KbTs, LC, rec + L.KbT(), kC, D, kC, tid);
+    stage(Qhs, LD, rec + L.Qh(), D, kC, D, tid);
+    stage(Ws, LD, rec + L.W(), D, kC, D, tid);
+    stage(GCs, D, rec + L.GC(), D, 1, D, tid);
     for (int i = tid; i < kC * ES; i += kThreads) {
       const int r = i / ES, j = i % ES;
       dO[i] = r < n ? to_f32(dout[((size_t)(t0 + r) * H + h) * E + j0 + j]) : 0.f;
     }
     __syncthreads();
+    for (int i = tid; i < D * ES; i += kThreads) {  // dS_C^T
+      const int c = i / ES, j = i % ES;
+      st[SL.dST() + (size_t)(j0 + j) * D + c] = dS[i];
+    }
     for (int idx = tid; idx < (kC / 4) * (ES / 4); idx += kThreads) {  // dU = M^T dO + K_bar dS
       int m0, n0;
       tile_of<D, ES>(idx, m0, n0);
       float acc[4][4];
       zero(acc);
-      kgemm<4, 4>(acc, rec + L.M(), kC, m0, dO, ES, n0, kC);
-      kgemm<4, 4>(acc, rec + L.KbT(), kC, m0, dS, ES, n0, D);
+      kgemm<4, 4>(acc, Ms, LC, m0, dO, ES, n0, kC);
+      kgemm<4, 4>(acc, KbTs, LC, m0, dS, ES, n0, D);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -382,14 +554,14 @@ bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const floa
       float a1[4][4], a2[4][4];
       zero(a1);
       zero(a2);
-      kgemm<4, 4>(a1, rec + L.Qh(), D, m0, dO, ES, n0, kC);
-      kgemm<4, 4>(a2, rec + L.W(), D, m0, dU, ES, n0, kC);
+      kgemm<4, 4>(a1, Qhs, LD, m0, dO, ES, n0, kC);
+      kgemm<4, 4>(a2, Ws, LD, m0, dU, ES, n0, kC);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          float& s = dS[(m0 + i) * ES + n0 + j];
-          s = fmaf(rec[L.GC() + m0 + i], s, a1[i][j] - a2[i][j]);
+          float& sv = dS[(m0 + i) * ES + n0 + j];
+          sv = fmaf(GCs[m0 + i], sv, a1[i][j] - a2[i][j]);
         }
     }
     __syncthreads();
@@ -415,25 +587,58 @@ struct GradLayout {
   __host__ __device__ size_t size() const { return dGam() + (size_t)D; }
 };
 
+// Shared floats of bwd_dvsums: dO^T, V^T and dU^T [E][C+4]; S0^T, later dS_C^T [E][D+4]; dU
+// [C][E+4], later U^T [E][C+4]; T [C][C+4].
 template <int D, int E>
 struct DvSmem {
-  static constexpr int LC = kC + 4, LE = E + 4;
-  static constexpr int floats = 2 * E * LC + kC * LE;
+  static constexpr int LC = kC + 4, LE = E + 4, LD = D + 4;
+  static constexpr int CT = E * LC, UR = kC * LE > CT ? kC * LE : CT;
+  static constexpr int floats = 3 * CT + E * LD + UR + kC * LC;
+};
+
+// 16-byte pieces of a [C][E] tile of head h (rows n.. reading as zero), widened to fp32 and stored
+// transposed, [E][ld]; consecutive threads take consecutive rows so that the stores do not conflict
+template <int E, typename Tp>
+struct TileLoadT {
+  static constexpr int V = 16 / sizeof(Tp), PIECES = kC * (E / V);
+  static_assert(PIECES % kThreads == 0, "whole pieces per thread");
+  static constexpr int N = PIECES / kThreads;
+  uint4 x[N];
+  __device__ __forceinline__ void load(const Tp* a, int64_t t0, int n, int H, int h, int tid) {
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+      const int i = tid + u * kThreads, r = i % kC;
+      x[u] = r < n ? *reinterpret_cast<const uint4*>(a + ((size_t)(t0 + r) * H + h) * E + V * (i / kC))
+                   : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  __device__ __forceinline__ void store(float* dst, int ld, int tid) const {
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+      const int i = tid + u * kThreads, r = i % kC, c = V * (i / kC);
+      const Tp* e = reinterpret_cast<const Tp*>(&x[u]);
+#pragma unroll
+      for (int w = 0; w < V; ++w) dst[(c + w) * ld + r] = to_f32(e[w]);
+    }
+  }
 };
 
 // dQ_hat = dO S0^T, dW = -dU S0^T, dK_bar = U dS_C^T, dM = dO U^T, dU V^T, rowsum(dS_C (.) S0) into
-// the scratch; dv = T^T dU into the output.
+// the scratch; dv = T^T dU into the output.  Every product reads both operands from shared memory.
 template <int D, int E, typename Tin>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_t* __restrict__ plan,
            const int32_t* __restrict__ cu, int B, int64_t T, int H, int64_t ntask, const float* __restrict__ recs,
            const float* __restrict__ states, float* __restrict__ grads, float* __restrict__ dv) {
   using SM = DvSmem<D, E>;
-  constexpr int LC = SM::LC, LE = SM::LE;
+  constexpr int LC = SM::LC, LE = SM::LE, LD = SM::LD;
   extern __shared__ __align__(16) float sm[];
-  float* dOT = sm;           // [E][LC]
-  float* VT = dOT + E * LC;  // [E][LC]
-  float* dUr = VT + E * LC;  // [C][LE]
+  float* dOT = sm;              // [E][LC]
+  float* VT = dOT + SM::CT;     // [E][LC]
+  float* dUT = VT + SM::CT;     // [E][LC]
+  float* S0T = dUT + SM::CT;    // [E][LD]: S0^T, then dS_C^T
+  float* dUr = S0T + E * LD;    // [C][LE]: dU, then U^T [E][LC]
+  float* TS = dUr + SM::UR;     // [C][LC]
   const int tid = threadIdx.x;
   const RecLayout L{D, E};
   const StateLayout SL{D, E};
@@ -447,24 +652,37 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
     const float* rec = recs + (size_t)task * L.size();
     const float* st = states + (size_t)task * SL.size();
     float* gr = grads + (size_t)task * GL.size();
-    for (int i = tid; i < kC * E; i += kThreads) {
-      const int r = i / E, j = i % E;
-      const size_t src = ((size_t)(t0 + r) * H + h) * E + j;
-      dOT[j * LC + r] = r < n ? to_f32(dout[src]) : 0.f;
-      VT[j * LC + r] = r < n ? to_f32(v[src]) : 0.f;
+    {  // the next task's operands into L2 while this one runs
+      int h2, n2;
+      int64_t t2;
+      if (next_task(task, ntask, H, plan, cu, B, T, h2, t2, n2)) {
+        const size_t nt = (size_t)task + gridDim.x;
+        if (tid == 0) prefetch_l2(states + nt * SL.size(), (uint32_t)(SL.size() * 4));
+        if (tid == 1) prefetch_l2(recs + nt * L.size() + L.T(), kC * kC * 4);
+        prefetch_rows_l2(v, t2, n2, H, h2, E, tid, 64);
+        prefetch_rows_l2(dout, t2, n2, H, h2, E, tid, 128);
+      }
     }
-    for (int i = tid; i < kC * E; i += kThreads) {
-      const int j = i / kC, r = i % kC;
-      dUr[r * LE + j] = st[SL.dUT() + i];
+    {
+      TileLoadT<E, Tin> tdo, tv;
+      tdo.load(dout, t0, n, H, h, tid);
+      tv.load(v, t0, n, H, h, tid);
+      stage(dUT, LC, st + SL.dUT(), kC, E, kC, tid);
+      stage(S0T, LD, st + SL.S0T(), D, E, D, tid);
+      stage(TS, LC, rec + L.T(), kC, kC, kC, tid);
+      tdo.store(dOT, LC, tid);
+      tv.store(VT, LC, tid);
     }
+    __syncthreads();
+    for (int i = tid; i < kC * E; i += kThreads) dUr[(i % kC) * LE + i / kC] = dUT[(i / kC) * LC + i % kC];
     __syncthreads();
     {
       const int m0 = 4 * (tid >> 4), n0 = (D / 16) * (tid & 15);
       float a1[4][D / 16], a2[4][D / 16];
       zero(a1);
       zero(a2);
-      kgemm<4, D / 16>(a1, dOT, LC, m0, st + SL.S0T(), D, n0, E);         // dO S0^T
-      kgemm<4, D / 16>(a2, st + SL.dUT(), kC, m0, st + SL.S0T(), D, n0, E);  // dU S0^T
+      kgemm<4, D / 16>(a1, dOT, LC, m0, S0T, LD, n0, E);  // dO S0^T
+      kgemm<4, D / 16>(a2, dUT, LC, m0, S0T, LD, n0, E);  // dU S0^T
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -473,8 +691,36 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
           gr[GL.dW() + (size_t)(m0 + i) * D + n0 + j] = -a2[i][j];
           gr[GL.dWT() + (size_t)(n0 + j) * kC + m0 + i] = -a2[i][j];
         }
+    }
+    {  // dv = T^T dU (rows of the sequence only)
+      const int m0 = 4 * (tid >> 4), n0 = (E / 16) * (tid & 15);
+      float acc[4][E / 16];
+      zero(acc);
+      kgemm<4, E / 16>(acc, TS, LC, m0, dUr, LE, n0, kC);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (m0 + i < n)
+#pragma unroll
+          for (int j = 0; j < E / 16; ++j) dv[((size_t)(t0 + m0 + i) * H + h) * E + n0 + j] = acc[i][j];
+    }
+    if (tid < D) {  // rowsum(dS_C (.) S0), dS_C^T from global
+      float s0 = 0.f, s1 = 0.f;
+      for (int j = 0; j < E; j += 2) {
+        s0 = fmaf(st[SL.dST() + (size_t)j * D + tid], S0T[j * LD + tid], s0);
+        s1 = fmaf(st[SL.dST() + (size_t)(j + 1) * D + tid], S0T[(j + 1) * LD + tid], s1);
+      }
+      gr[GL.dGam() + tid] = s0 + s1;
+    }
+    __syncthreads();  // S0^T and dU are no longer read
+    float* UT = dUr;
+    stage(S0T, LD, st + SL.dST(), D, E, D, tid);
+    stage(UT, LC, st + SL.UT(), kC, E, kC, tid);
+    __syncthreads();
+    {
+      const int m0 = 4 * (tid >> 4), n0 = (D / 16) * (tid & 15);
+      float a1[4][D / 16];
       zero(a1);
-      kgemm<4, D / 16>(a1, st + SL.UT(), kC, m0, st + SL.dST(), D, n0, E);  // U dS_C^T
+      kgemm<4, D / 16>(a1, UT, LC, m0, S0T, LD, n0, E);  // U dS_C^T
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -485,8 +731,8 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
       float a1[4][4], a2[4][4];
       zero(a1);
       zero(a2);
-      kgemm<4, 4>(a1, dOT, LC, m0, st + SL.UT(), kC, n0, E);  // dO U^T
-      kgemm<4, 4>(a2, st + SL.dUT(), kC, m0, VT, LC, n0, E);  // dU V^T
+      kgemm<4, 4>(a1, dOT, LC, m0, UT, LC, n0, E);   // dO U^T
+      kgemm<4, 4>(a2, dUT, LC, m0, VT, LC, n0, E);   // dU V^T
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -495,22 +741,6 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
           gr[GL.dM() + (size_t)r * kC + s] = r >= s ? a1[i][j] : 0.f;
           gr[GL.dT1() + (size_t)r * kC + s] = a2[i][j];
         }
-    }
-    {  // dv = T^T dU (rows of the sequence only)
-      const int m0 = 4 * (tid >> 4), n0 = (E / 16) * (tid & 15);
-      float acc[4][E / 16];
-      zero(acc);
-      kgemm<4, E / 16>(acc, rec + L.T(), kC, m0, dUr, LE, n0, kC);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (m0 + i < n)
-#pragma unroll
-          for (int j = 0; j < E / 16; ++j) dv[((size_t)(t0 + m0 + i) * H + h) * E + n0 + j] = acc[i][j];
-    }
-    if (tid < D) {
-      float s = 0.f;
-      for (int j = 0; j < E; ++j) s = fmaf(st[SL.dST() + (size_t)j * D + tid], st[SL.S0T() + (size_t)j * D + tid], s);
-      gr[GL.dGam() + tid] = s;
     }
     __syncthreads();
   }
@@ -555,14 +785,19 @@ bwd_grads(const Tin* __restrict__ q, const Tin* __restrict__ k, const float* __r
     if (!resolve_chunk(chunk, plan, cu, B, T, b, t0, n, cseq)) continue;
     const float* rec = recs + (size_t)task * L.size();
     const float* gr = grads + (size_t)task * GL.size();
-    for (int i = tid; i < kC * D; i += kThreads) {
-      const int r = i / D, c = i % D;
-      const bool ok = r < n;
-      const size_t src = ((size_t)(t0 + r) * H + h) * D + c;
-      kS[r * LD + c] = ok ? to_f32(k[src]) : 0.f;
-      qS[r * LD + c] = ok ? to_f32(q[src]) : 0.f;
-      gS[r * LD + c] = ok ? g[src] : 0.f;
+    {  // the next task's operands into L2 while this one runs
+      int h2, n2;
+      int64_t t2;
+      if (next_task(task, ntask, H, plan, cu, B, T, h2, t2, n2)) {
+        const size_t nt = (size_t)task + gridDim.x;
+        if (tid == 0) prefetch_l2(grads + nt * GL.size(), (uint32_t)(GL.size() * 4));
+        if (tid == 1) prefetch_l2(recs + nt * L.size() + L.T(), 3 * kC * kC * 4);  // T, X, A_tilde
+        prefetch_rows_l2(k, t2, n2, H, h2, D, tid, 64);
+        prefetch_rows_l2(q, t2, n2, H, h2, D, tid, 128);
+        prefetch_rows_l2(g, t2, n2, H, h2, D, tid, 192);
+      }
     }
+    load_kqg<D>(k, q, g, t0, n, H, h, kS, qS, gS, LD, tid);
     if (tid < kC) dbS[tid] = 0.f;
     __syncthreads();
     if (tid < D) {
@@ -788,18 +1023,23 @@ int serial_slices(int B, int H, int E) {  // value-column slices of the two seri
     return 1;
   const int64_t chains = (int64_t)B * H;
   for (int n = 8; n > 1; n /= 2)
-    if (chains * n <= 2 * (int64_t)sms && E / n >= 16) return n;
-  return 1;
+    if (chains * n <= (int64_t)sms && E / n >= 16) return n;
+  return E > 64 ? 2 : 1;  // at most 64 columns per slice (shared memory)
 }
 
 template <int D, int E, int ES, typename Tin>
 cudaError_t launch_serial(const BackwardArgs& a, const float* recs, float* states, cudaStream_t st) {
-  const dim3 grid((unsigned)a.B, (unsigned)a.H, (unsigned)(E / ES));
-  bwd_fwd<D, E, ES><<<grid, kThreads, 0, st>>>(recs, a.h0, a.plan, a.cu_seqlens, a.B, a.T, a.H, states);
-  cudaError_t e = cudaGetLastError();
+  constexpr size_t fs = FwdSmem<D, E, ES>::floats * sizeof(float), rs = RevSmem<D, E, ES>::floats * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(bwd_fwd<D, E, ES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fs);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_rev<D, E, ES, Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rs);
   if (e != cudaSuccess) return e;
-  bwd_rev<D, E, ES, Tin><<<grid, kThreads, 0, st>>>(recs, static_cast<const Tin*>(a.dout), a.dhT, a.plan,
-                                                      a.cu_seqlens, a.B, a.T, a.H, states, a.dh0);
+  const dim3 grid((unsigned)a.B, (unsigned)a.H, (unsigned)(E / ES));
+  bwd_fwd<D, E, ES><<<grid, kThreads, fs, st>>>(recs, a.h0, a.plan, a.cu_seqlens, a.B, a.T, a.H, states);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_rev<D, E, ES, Tin><<<grid, kThreads, rs, st>>>(recs, static_cast<const Tin*>(a.dout), a.dhT, a.plan,
+                                                       a.cu_seqlens, a.B, a.T, a.H, states, a.dh0);
   return cudaGetLastError();
 }
 
@@ -843,7 +1083,7 @@ cudaError_t launch_chunked(const BackwardArgs& a, float* ws, cudaStream_t st) {
     cudaError_t e = nsl == 8   ? launch_serial<D, E, E / 8, Tin>(a, recs, states, st)
                     : nsl == 4 ? launch_serial<D, E, E / 4, Tin>(a, recs, states, st)
                     : nsl == 2 ? launch_serial<D, E, E / 2, Tin>(a, recs, states, st)
-                               : launch_serial<D, E, E, Tin>(a, recs, states, st);
+                               : launch_serial<D, E, (E > 64 ? 64 : E), Tin>(a, recs, states, st);
     if (e != cudaSuccess) return e;
   }
   TraceScope ts("kda_bwd_chunk_grads", st);
