@@ -20,6 +20,7 @@ ranks and value aggregates all ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -35,6 +36,12 @@ METRIC = "KDA prefill tokens/s (bf16, H=32, dk=dv=128) + decode steps/s, % of ro
 PREFILL_BYTES_PER_TOKEN_HEAD = 3 * 2 * 128 + 4 * 128 + 4 + 2 * 128        # q,k,v bf16 + g fp32 + beta + out bf16
 PREFILL_FLOPS_PER_TOKEN_HEAD = 2 * (5 * 64 * 128 + 3 * 128 * 128)          # method's flop count at C=64, d=128
 DECODE_STATE_BYTES = 2 * 128 * 128 * 4                                    # read + write of one fp32 state
+DECODE_IO_BYTES_PER_TOKEN_HEAD = 3 * 2 * 128 + 4 * 128 + 4 + 2 * 128 + 2 * 128  # q,k,v,g,beta,gate,out
+# chunkwise backward, per (chunk, head) at C=64, d=128: 14 C x C x d products (records A, M, W, U_hat;
+# M^T dO; dM, dU V^T, T^T dU; dW K_hat^T, T^T dW and the four A/M-term products), 8 C x d x d
+# (U, the state update, K_bar dS, Q_hat^T dO, W^T dU, dQ_hat, dW, dK_bar) and 2 C^3 (X^T dX X^T)
+BWD_FLOPS_PER_CHUNK_HEAD = 2 * (14 * 64 * 64 * 128 + 8 * 64 * 128 * 128 + 2 * 64 ** 3)
+FP32_LANES_PER_SM = 128                                                   # FP32 FMA lanes per SM (4 x 32)
 
 
 def _env_int(name, default):
@@ -309,26 +316,49 @@ def run_ours(args, world, rank, local):
     # the pipelined calls computed what the resident-input calls did
     assert torch.equal(out_h[(args.steps - 1) % nb], out.cpu()) and torch.equal(hT_h[(args.steps - 1) % nb], hT.cpu())
 
-    # backward of the prefill recurrence (no epilogue) on the same workload, fp32 on the CUDA cores;
-    # timed beside the step, not part of the metric
+    # the next rows, each timed beside the step (not part of the metric) against its own roofline
+    def time_calls(fn, calls):
+        fn()
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(calls):
+            fn()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        assert binding.kda_get_device_error(dev) == 0
+        return dist_max(c0.elapsed_time(c1) / calls, world)
+
+    # prefill with the prefix-cache checkpoints (the state every 512 tokens)
+    ckpt_chunks = 8
+    n_ckpt = T // (64 * ckpt_chunks)
+    states = torch.empty(n_ckpt, H, pcfg.dk, pcfg.dv, device=dev, dtype=torch.float32)
+    ckpt_ms = time_calls(lambda: binding.kda_chunk_fwd_checkpoints(
+        P["q"], P["k"], P["v"], P["g"], P["beta"], out=out, hT=hT, states=states, ckpt_chunks=ckpt_chunks,
+        workspace=ws), max(3, args.steps))
+    ckpt_bytes = alg_bytes + states.numel() * 4
+    # speculative-decode verify: 4 draft tokens per request, the pool read once and not written
+    vcfg = dataclasses.replace(dcfg, n_tok=4)
+    V = inputs.decode_inputs(vcfg, device=dev)
+    vout = torch.empty(vcfg.N, vcfg.n_tok, vcfg.H, vcfg.dv, device=dev, dtype=torch.bfloat16)
+    ver_ms = time_calls(lambda: binding.kda_decode_multi(
+        V["q"], V["k"], V["v"], V["g"], V["beta"], V["state_pool"], V["slot_idx"], out=vout, commit=False,
+        gate=V["gate"], norm_weight=V["norm_weight"]), max(3, args.steps))
+    ver_bytes = vcfg.N * vcfg.H * DECODE_STATE_BYTES // 2 + \
+        vcfg.N * vcfg.n_tok * vcfg.H * DECODE_IO_BYTES_PER_TOKEN_HEAD
+    del V
+    # backward of the prefill recurrence (no epilogue) on the same workload, fp32 on the CUDA cores
     gen = torch.Generator(device=dev).manual_seed(11)
     dout = torch.randn(out.shape, generator=gen, device=dev).to(out.dtype)
     bws = torch.empty(binding.kda_chunk_bwd_workspace_size(1, T, H, pcfg.dk, pcfg.dv), device=dev, dtype=torch.uint8)
-
-    def backward():
-        return binding.kda_chunk_bwd(P["q"], P["k"], P["v"], P["g"], P["beta"], dout, workspace=bws)
-
-    backward()
-    torch.cuda.synchronize()
-    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    nb_calls = 2
-    b0.record(stream)
-    for _ in range(nb_calls):
-        backward()
-    b1.record(stream)
-    torch.cuda.synchronize()
-    bwd_ms = dist_max(b0.elapsed_time(b1) / nb_calls, world)
-    assert binding.kda_get_device_error(dev) == 0
+    bwd_ms = time_calls(lambda: binding.kda_chunk_bwd(P["q"], P["k"], P["v"], P["g"], P["beta"], dout,
+                                                      workspace=bws), 2)
+    del bws
+    bwd_flops = BWD_FLOPS_PER_CHUNK_HEAD * (T // 64) * H
+    csum = clocks.summary() or {}
+    sm_max_mhz = csum.get("sm_max_mhz") or 2070.0
+    fp32_tflops = torch.cuda.get_device_properties(dev).multi_processor_count * FP32_LANES_PER_SM * 2 * \
+        sm_max_mhz * 1e6 / 1e12
 
     line = {
         "metric": METRIC,
@@ -364,12 +394,32 @@ def run_ours(args, world, rank, local):
                            "frac": round(pre_flops / (pre_s / args.steps) / 1e12 / bf16_tflops, 4)},
         "kernels": {k: {"launches": v[0], "total_ms": round(v[1], 4)} for k, v in trace.items()},
         "gpu_launches": launches,
+        "checkpoints": {"workload": f"the prefill workload, state stored every {64 * ckpt_chunks} tokens "
+                                    f"({n_ckpt} x {H} fp32 states)",
+                        "ms_per_call": round(ckpt_ms, 4), "tokens_per_s": round(aggregate(T, world, ckpt_ms / 1e3), 1),
+                        "roofline": {"bound": "hbm", "achieved": round(ckpt_bytes / (ckpt_ms * 1e-3) / 1e9, 1),
+                                     "peak": hbm_gbs, "unit": "GB/s", "peak_kind": peak_kind,
+                                     "frac": round(ckpt_bytes / (ckpt_ms * 1e-3) / 1e9 / hbm_gbs, 4),
+                                     "algorithmic_bytes_per_call": ckpt_bytes, "scope": "whole call"}},
+        "verify": {"workload": f"decode N={vcfg.N} requests x {vcfg.n_tok} draft tokens, H={vcfg.H}, pool not "
+                               "written (commit=0), RMSNorm+gate",
+                   "ms_per_call": round(ver_ms, 4),
+                   "tokens_per_s": round(aggregate(vcfg.N * vcfg.n_tok, world, ver_ms / 1e3), 1),
+                   "roofline": {"bound": "hbm", "achieved": round(ver_bytes / (ver_ms * 1e-3) / 1e9, 1),
+                                "peak": hbm_gbs, "unit": "GB/s", "peak_kind": peak_kind,
+                                "frac": round(ver_bytes / (ver_ms * 1e-3) / 1e9 / hbm_gbs, 4),
+                                "algorithmic_bytes_per_call": ver_bytes, "scope": "whole call"}},
         "backward": {"ms_per_call": round(bwd_ms, 3), "tokens_per_s": round(aggregate(T, world, bwd_ms / 1e3), 1),
                      "kernel": "chunkwise, fp32 CUDA cores: per-chunk records, serial state passes over "
-                               "chunks, per-chunk gradients"},
+                               "chunks, per-chunk gradients",
+                     "roofline": {"bound": "alu", "achieved": round(bwd_flops / (bwd_ms * 1e-3) / 1e12, 2),
+                                  "peak": round(fp32_tflops, 1), "unit": "TFLOP/s",
+                                  "peak_kind": f"fp32 FMA: SMs x {FP32_LANES_PER_SM} lanes x 2 x {sm_max_mhz:.0f} MHz",
+                                  "frac": round(bwd_flops / (bwd_ms * 1e-3) / 1e12 / fp32_tflops, 4),
+                                  "algorithmic_flops_per_call": bwd_flops, "scope": "whole call"}},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "clocks": clocks.summary(),
+        "clocks": csum or None,
         "wall_s": round(t_wall, 3),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

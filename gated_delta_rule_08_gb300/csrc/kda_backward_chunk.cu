@@ -85,10 +85,6 @@ __device__ __forceinline__ void batched(int n, int tid, Get get, Put put) {
   }
 }
 
-// bytes (a multiple of 16) from a 16-byte aligned global address into L2, without waiting
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 // the D (or E) values of rows t0 .. t0+n-1 of head h of a [T][H][D] array into L2, thread tid0 + r
 // taking row r (rows are 16-byte aligned: D * sizeof(T) is a multiple of 16)
 template <typename Tp>

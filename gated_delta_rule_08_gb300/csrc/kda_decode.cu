@@ -33,8 +33,9 @@ namespace kda {
 namespace {
 
 constexpr int kDecodeThreads = 256;
+constexpr int kStageTok = 4;  // tokens whose inputs are staged in shared memory together (multi-token calls)
 
-template <int DK, int DV, typename Tin, typename Tout>
+template <int DK, int DV, int NST, typename Tin, typename Tout>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
               const float* __restrict__ g, const float* __restrict__ beta, float* __restrict__ pool,
@@ -67,33 +68,59 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   if (count == 0) return;  // nothing to apply: outputs and state untouched
   float* S = pool + ((size_t)slot * H + h) * (size_t)(DK * DV);
 
-  // Issue the state loads first: they are the only long-latency traffic.
+  // Issue the state loads first: they are the longest-latency traffic.
   float4 s[RPG];
 #pragma unroll
   for (int i = 0; i < RPG; ++i)
     s[i] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(rg + i * NG) * DV) + cg);
 
-  __shared__ float sk[DK], sq[DK], salpha[DK], sv[DV];
+  // the inputs of up to NST tokens, loaded together so that their latency is paid once
+  __shared__ float sk[NST][DK], sq[NST][DK], salpha[NST][DK], sv[NST][DV];
+  __shared__ float sgate[NST > 1 ? NST : 1][NST > 1 ? DV : 1], sbeta[NST];
   __shared__ float4 part_a[NG][TPR], part_b[NG][TPR];
-  __shared__ float sdelta[DV], so[DV];
+  __shared__ float sdelta[DV], so[NST][DV];
   __shared__ float red[kDecodeThreads / 32];
   __shared__ float s_kq;
 
   for (int t = 0; t < count; ++t) {
+    const int u = t % NST;
     const size_t row = ((size_t)n * n_tok + t) * H + h;  // token row of [N, n_tok, H]
-    const size_t rk = row * DK, rv = row * DV;
-    for (int i = tid; i < DK; i += kDecodeThreads) {
-      sk[i] = to_f32(k[rk + i]);
-      sq[i] = to_f32(q[rk + i]);
-      salpha[i] = __expf(g[rk + i]);
+    const size_t rv = row * DV;
+    float b_r;
+    if constexpr (NST == 1) {  // one token per request (the launch for n_tok = 1)
+      const size_t rk = row * DK;
+      for (int i = tid; i < DK; i += kDecodeThreads) {
+        sk[0][i] = to_f32(k[rk + i]);
+        sq[0][i] = to_f32(q[rk + i]);
+        salpha[0][i] = __expf(g[rk + i]);
+      }
+      for (int j = tid; j < DV; j += kDecodeThreads) sv[0][j] = to_f32(v[rv + j]);
+      b_r = beta[row];
+      __syncthreads();
+    } else if (u == 0) {
+      if (t > 0) __syncthreads();  // the previous stage is no longer read
+      const int nst = count - t < NST ? count - t : NST;
+      for (int i = tid; i < nst * DK; i += kDecodeThreads) {
+        const int w = i / DK, c = i - w * DK;
+        const size_t rk = (row + (size_t)w * H) * DK + c;
+        sk[w][c] = to_f32(k[rk]);
+        sq[w][c] = to_f32(q[rk]);
+        salpha[w][c] = __expf(g[rk]);
+      }
+      for (int i = tid; i < nst * DV; i += kDecodeThreads) {
+        const int w = i / DV, c = i - w * DV;
+        const size_t rw = (row + (size_t)w * H) * DV + c;
+        sv[w][c] = to_f32(v[rw]);
+        if (NST > 1 && gate != nullptr) sgate[w][c] = to_f32(gate[rw]);  // (one-token calls: read where used)
+      }
+      if (tid < nst) sbeta[tid] = beta[row + (size_t)tid * H];
+      __syncthreads();
     }
-    for (int j = tid; j < DV; j += kDecodeThreads) sv[j] = to_f32(v[rv + j]);
-    const float b_r = beta[row];
-    __syncthreads();
+    if constexpr (NST > 1) b_r = sbeta[u];
 
     if (tid < 32) {  // k . q
       float acc = 0.f;
-      for (int i = tid; i < DK; i += 32) acc = fmaf(sk[i], sq[i], acc);
+      for (int i = tid; i < DK; i += 32) acc = fmaf(sk[u][i], sq[u][i], acc);
       acc = warp_sum(acc);
       if (tid == 0) s_kq = acc;
     }
@@ -102,10 +129,10 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
 #pragma unroll
     for (int i = 0; i < RPG; ++i) {
       const int r = rg + i * NG;
-      const float al = salpha[r];
+      const float al = salpha[u][r];
       s[i].x *= al; s[i].y *= al; s[i].z *= al; s[i].w *= al;
-      pa = f4_fma(sk[r], s[i], pa);
-      pb = f4_fma(sq[r], s[i], pb);
+      pa = f4_fma(sk[u][r], s[i], pa);
+      pb = f4_fma(sq[u][r], s[i], pb);
     }
     part_a[rg][cg] = pa;
     part_b[rg][cg] = pb;
@@ -119,35 +146,60 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
         a += reinterpret_cast<const float*>(&part_a[gi][c4])[e];
         b += reinterpret_cast<const float*>(&part_b[gi][c4])[e];
       }
-      const float d = b_r * (sv[tid] - a);
+      const float d = b_r * (sv[u][tid] - a);
       sdelta[tid] = d;
-      so[tid] = fmaf(s_kq, d, b);
+      so[u][tid] = fmaf(s_kq, d, b);
     }
     __syncthreads();
 
     const float4 d4 = reinterpret_cast<const float4*>(sdelta)[cg];
 #pragma unroll
-    for (int i = 0; i < RPG; ++i) s[i] = f4_fma(sk[rg + i * NG], d4, s[i]);
+    for (int i = 0; i < RPG; ++i) s[i] = f4_fma(sk[u][rg + i * NG], d4, s[i]);
 
     // Read-out (+ optional RMSNorm over dv and sigmoid gate).
-    float o = 0.f;
-    if (tid < DV) o = so[tid];
-    if (gate != nullptr) {
-      float sq_sum = (tid < DV) ? o * o : 0.f;
-      sq_sum = warp_sum(sq_sum);
-      if ((tid & 31) == 0) red[tid >> 5] = sq_sum;
-      __syncthreads();
-      float tot = 0.f;
+    if constexpr (NST == 1) {
+      float o = 0.f;
+      if (tid < DV) o = so[0][tid];
+      if (gate != nullptr) {
+        float sq_sum = (tid < DV) ? o * o : 0.f;
+        sq_sum = warp_sum(sq_sum);
+        if ((tid & 31) == 0) red[tid >> 5] = sq_sum;
+        __syncthreads();
+        float tot = 0.f;
 #pragma unroll
-      for (int w = 0; w < (DV + 31) / 32; ++w) tot += red[w];
-      if (tid < DV) {
-        const float inv = rsqrtf(tot / (float)DV + eps);
-        const float wj = norm_w ? norm_w[tid] : 1.f;
-        o = o * inv * wj * sigmoidf_(to_f32(gate[rv + tid]));
+        for (int w = 0; w < (DV + 31) / 32; ++w) tot += red[w];
+        if (tid < DV) {
+          const float inv = rsqrtf(tot / (float)DV + eps);
+          const float wj = norm_w ? norm_w[tid] : 1.f;
+          o = o * inv * wj * sigmoidf_(to_f32(gate[rv + tid]));
+        }
+      }
+      if (tid < DV) out[rv + tid] = from_f32<Tout>(o);
+    } else if (u == NST - 1 || t + 1 == count) {
+      // the stage's read-outs together, one warp per token: no barrier per token for the norm
+      __syncthreads();
+      const int w = tid >> 5, lane = tid & 31;
+      if (w <= u) {
+        float ov[DV / 32], ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < DV / 32; ++j) {
+          ov[j] = so[w][lane + 32 * j];
+          ss = fmaf(ov[j], ov[j], ss);
+        }
+        const float inv = gate != nullptr ? rsqrtf(warp_sum(ss) / (float)DV + eps) : 1.f;
+        const size_t rw = (((size_t)n * n_tok + (t - u + w)) * H + h) * DV;
+#pragma unroll
+        for (int j = 0; j < DV / 32; ++j) {
+          const int c = lane + 32 * j;
+          float o = ov[j];
+          if (gate != nullptr) o = o * inv * (norm_w ? norm_w[c] : 1.f) * sigmoidf_(sgate[w][c]);
+          out[rw + c] = from_f32<Tout>(o);
+        }
       }
     }
-    if (tid < DV) out[rv + tid] = from_f32<Tout>(o);
-    if (t + 1 < count) __syncthreads();  // shared inputs of the next token
+    // no barrier between tokens: what a token writes to shared memory before its first barrier was
+    // last read before the previous token's second barrier (and red, written after the second,
+    // was last read before this point)
   }
 
   if (commit) {
@@ -162,7 +214,8 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
   const int rows = a.N * a.H;
   if (rows == 0) return cudaSuccess;
   TraceScope ts("kda_decode", st);
-  decode_kernel<DK, DV, Tin, Tout><<<rows, kDecodeThreads, 0, st>>>(
+  auto kern = a.n_tok == 1 ? decode_kernel<DK, DV, 1, Tin, Tout> : decode_kernel<DK, DV, kStageTok, Tin, Tout>;
+  kern<<<rows, kDecodeThreads, 0, st>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g,
       a.beta, a.state_pool, a.slot_idx, static_cast<Tout*>(a.out), a.H, a.num_slots, a.n_tok, a.ntok_per_req,
       a.commit ? 1 : 0, static_cast<const Tin*>(a.epi.gate), a.epi.norm_weight, a.epi.eps, a.err);

@@ -37,6 +37,11 @@ __device__ __forceinline__ float warp_sum(float x) {
 // chunks), plan[B+1] = 1 if cu_seqlens was valid, plan[B+2+r] = the sequence of rank r by
 // decreasing length (ties by index; the identity for large B).
 // Sequence of rank r in the serial pass's launch order: the longest chains start first.
+// bytes (a multiple of 16) from a 16-byte aligned global address into L2, without waiting
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 constexpr int kOrderMaxB = 512;  // beyond this many sequences the order is the identity
 __device__ __forceinline__ int sequence_of_rank(int r, const int32_t* plan, const int32_t* cu, int B) {
   return cu == nullptr ? r : plan[B + 2 + r];
