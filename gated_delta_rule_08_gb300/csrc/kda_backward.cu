@@ -23,6 +23,9 @@
 //  stores the state at every chunk start; then, chunk by chunk from the end, the 64 token states
 //  of the chunk are recomputed into scratch and the chunk's tokens are walked backwards.  Column
 //  sums go through shared memory, row sums through a segmented butterfly of warp shuffles.
+#include <cstdlib>
+#include <cstring>
+
 #include "kda_device.cuh"
 #include "kda_internal.h"
 
@@ -351,7 +354,12 @@ int backward_slices(int B, int H, int dv) {
 // this much scratch it is used, beyond it the token sweep below (whose scratch is per chain).
 constexpr size_t kChunkedMaxBytes = size_t(48) << 30;
 
+// KDA_BACKWARD_PATH=token or =chunked in the environment forces one path (read at every call, so
+// the workspace size and the call agree while it is unchanged).
 bool use_chunked(int B, int64_t T, int H, int dk, int dv) {
+  const char* forced = std::getenv("KDA_BACKWARD_PATH");
+  if (forced != nullptr && std::strcmp(forced, "token") == 0) return false;
+  if (forced != nullptr && std::strcmp(forced, "chunked") == 0) return true;
   return backward_chunked_bytes(B, T, H, dk, dv, true) <= kChunkedMaxBytes &&
          backward_chunked_bytes(B, T, H, dk, dv, false) <= kChunkedMaxBytes;
 }

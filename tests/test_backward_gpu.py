@@ -8,6 +8,13 @@ from oracle import oracle_kda_backward
 
 pytestmark = pytest.mark.gpu
 
+
+@pytest.fixture(params=["chunked", "token"])
+def path(request, monkeypatch):
+    """Both backward paths (the library picks the token sweep only beyond 48 GB of chunkwise scratch)."""
+    monkeypatch.setenv("KDA_BACKWARD_PATH", request.param)
+    return request.param
+
 # the backward runs in fp32 on the given inputs whatever their dtype: the fp32 bound applies
 TOL = 1e-3
 
@@ -34,20 +41,20 @@ def _case(lengths, H, dk, dv, dtype, h0, dhT, seed):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-def test_backward_single_sequence_ragged_tail(dtype):
+def test_backward_single_sequence_ragged_tail(dtype, path):
     _case((200,), 2, 128, 128, dtype, h0=True, dhT=True, seed=501)
 
 
-def test_backward_varlen_with_short_sequences():
+def test_backward_varlen_with_short_sequences(path):
     _case((70, 1, 130), 2, 64, 64, "fp32", h0=False, dhT=False, seed=502)
 
 
 @pytest.mark.parametrize("dk,dv", [(128, 64), (64, 128)])
-def test_backward_rectangular_state(dk, dv):
+def test_backward_rectangular_state(dk, dv, path):
     _case((96, 33), 1, dk, dv, "bf16", h0=True, dhT=True, seed=503 + dk)
 
 
-def test_backward_gradients_are_deterministic():
+def test_backward_gradients_are_deterministic(path):
     cfg = inputs.PrefillConfig("bwd", H=2, dk=128, dv=128, dtype="bf16", lengths=(150,), B=1, seed=510)
     inp = inputs.prefill_inputs(cfg, device="cuda")
     dout = torch.ones(150, 2, 128, device="cuda", dtype=torch.bfloat16)
