@@ -367,12 +367,8 @@ bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restr
 
 // ---------------------------------------------------------------- the two serial passes
 // Each CTA: one (sequence, head) chain and ES of its value columns (the recurrence is separable in
-// the columns of the state).  Per chunk, 64 x ES and D x ES products with 4 x 4 register tiles.
-template <int D, int ES>
-__device__ __forceinline__ void tile_of(int idx, int& m0, int& n0) {  // idx < (rows / 4) x (ES / 4)
-  m0 = 4 * (idx / (ES / 4));
-  n0 = 4 * (idx % (ES / 4));
-}
+// the columns of the state).  Per chunk, 64 x ES and D x ES products with 4 x 4 register tiles;
+// when a product has fewer tiles than threads, its k range is split over KS thread groups.
 
 // rows x cols floats from global (row stride gld) into shared memory (row stride sld), 16-byte copies
 __device__ __forceinline__ void stage(float* dst, int sld, const float* src, size_t gld, int rows, int cols, int tid) {
@@ -382,10 +378,47 @@ __device__ __forceinline__ void stage(float* dst, int sld, const float* src, siz
           [&](int i, float4 x) { *reinterpret_cast<float4*>(dst + (i / q) * sld + 4 * (i % q)) = x; });
 }
 
+// Tiles of a ROWS x ES product: thread tid owns tile tid % TILES (if any) and the k part tid / TILES.
+template <int ROWS, int ES>
+struct SerialTiles {
+  static constexpr int TILES = (ROWS / 4) * (ES / 4);
+  static constexpr int KS = TILES >= kThreads ? 1 : kThreads / TILES;  // k parts
+  static constexpr int ROUNDS = TILES >= kThreads ? TILES / kThreads : 1;
+  static_assert(TILES % kThreads == 0 || kThreads % TILES == 0, "tiles and threads must divide");
+  static_assert(KS == 1 || KS == 2 || KS == 4, "k split");
+  __device__ static void at(int tid, int round, int& m0, int& n0, int& part) {
+    const int idx = KS == 1 ? tid + round * kThreads : tid % TILES;
+    part = KS == 1 ? 0 : tid / TILES;
+    m0 = 4 * (idx / (ES / 4));
+    n0 = 4 * (idx % (ES / 4));
+  }
+};
+// After each part has its partial 4 x 4 sums: parts > 0 leave them in red (KS - 1 planes of
+// ROWS x ld floats), and after the barrier part 0 holds the total.  Every thread calls this.
+template <int KS>
+__device__ __forceinline__ void combine_parts(float (&acc)[4][4], int part, float* red, int plane, int ld, int m0,
+                                              int n0) {
+  if (KS == 1) return;
+  if (part > 0)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(red + (part - 1) * plane + (m0 + i) * ld + n0) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+  __syncthreads();
+  if (part == 0)
+    for (int p = 1; p < KS; ++p)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 x = *reinterpret_cast<const float4*>(red + (p - 1) * plane + (m0 + i) * ld + n0);
+        acc[i][0] += x.x; acc[i][1] += x.y; acc[i][2] += x.z; acc[i][3] += x.w;
+      }
+}
+
 template <int D, int E, int ES>
 struct FwdSmem {
   static constexpr int LC = kC + 4, LD = D + 4, LS = ES + 4;
-  static constexpr int floats = D * LC + kC * LD + kC * LS + D + D * ES + kC * ES;
+  static constexpr int RU = (SerialTiles<kC, ES>::KS - 1) * kC * LS, RS = (SerialTiles<D, ES>::KS - 1) * D * LS;
+  static constexpr int floats = D * LC + kC * LD + kC * LS + D + D * LS + kC * LS + (RU > RS ? RU : RS);
 };
 
 template <int D, int E, int ES>
@@ -393,14 +426,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int32_t* __restrict__ plan,
         const int32_t* __restrict__ cu, int B, int64_t T, int H, float* __restrict__ states) {
   using SM = FwdSmem<D, E, ES>;
+  using TU = SerialTiles<kC, ES>;
+  using TS = SerialTiles<D, ES>;
+  static_assert(TU::ROUNDS == 1, "one U tile (or k part) per thread");
   constexpr int LC = SM::LC, LD = SM::LD, LS = SM::LS;
   extern __shared__ __align__(16) float sm[];
   float* WTs = sm;              // W^T [D][LC]
   float* Kbs = WTs + D * LC;    // K_bar [C][LD]
   float* Uhs = Kbs + kC * LD;   // U_hat slice [C][LS]
   float* GCs = Uhs + kC * LS;   // e^{G_C} [D]
-  float* S = GCs + D;           // [D][ES]
-  float* U = S + D * ES;        // [C][ES]
+  float* S = GCs + D;           // [D][LS]
+  float* U = S + D * LS;        // [C][LS]
+  float* red = U + kC * LS;     // k-part sums
   const int b = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * ES, tid = threadIdx.x;
   if (cu != nullptr && plan[B + 1] == 0) return;
   int64_t first_chunk, t_begin, len;
@@ -409,7 +446,7 @@ bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int3
   const StateLayout SL{D, E};
   for (int i = tid; i < D * ES; i += kThreads) {
     const int c = i / ES, j = i % ES;
-    S[i] = h0 != nullptr ? h0[(((size_t)b * H + h) * D + c) * E + j0 + j] : 0.f;
+    S[c * LS + j] = h0 != nullptr ? h0[(((size_t)b * H + h) * D + c) * E + j0 + j] : 0.f;
   }
   for (int64_t ci = 0; ci < nch; ++ci) {
     const size_t task = (size_t)(first_chunk + ci) * H + h;
@@ -425,39 +462,45 @@ bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int3
     stage(Uhs, LS, rec + L.Uh() + j0, E, kC, ES, tid);
     stage(GCs, D, rec + L.GC(), D, 1, D, tid);
     __syncthreads();
-    for (int i = tid; i < D * ES; i += kThreads) {  // S0^T
-      const int c = i / ES, j = i % ES;
-      st[SL.S0T() + (size_t)(j0 + j) * D + c] = S[i];
+    for (int i = tid; i < D * ES; i += kThreads) {  // S0^T, coalesced along dk
+      const int j = i / D, c = i % D;
+      st[SL.S0T() + (size_t)(j0 + j) * D + c] = S[c * LS + j];
     }
-    for (int idx = tid; idx < (kC / 4) * (ES / 4); idx += kThreads) {  // U = U_hat - W S
-      int m0, n0;
-      tile_of<D, ES>(idx, m0, n0);
+    {  // U = U_hat - W S
+      int m0, n0, part;
+      TU::at(tid, 0, m0, n0, part);
+      constexpr int KP = D / TU::KS;
       float acc[4][4];
       zero(acc);
-      kgemm<4, 4>(acc, WTs, LC, m0, S, ES, n0, D);
+      kgemm<4, 4>(acc, WTs + part * KP * LC, LC, m0, S + part * KP * LS, LS, n0, KP);
+      combine_parts<TU::KS>(acc, part, red, kC * LS, LS, m0, n0);
+      if (part == 0)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) U[(m0 + i) * ES + n0 + j] = Uhs[(m0 + i) * LS + n0 + j] - acc[i][j];
+          for (int j = 0; j < 4; ++j) U[(m0 + i) * LS + n0 + j] = Uhs[(m0 + i) * LS + n0 + j] - acc[i][j];
     }
     __syncthreads();
-    for (int i = tid; i < kC * ES; i += kThreads) {  // U^T
-      const int r = i / ES, j = i % ES;
-      st[SL.UT() + (size_t)(j0 + j) * kC + r] = U[i];
+    for (int i = tid; i < kC * ES; i += kThreads) {  // U^T, coalesced along the chunk
+      const int j = i / kC, r = i % kC;
+      st[SL.UT() + (size_t)(j0 + j) * kC + r] = U[r * LS + j];
     }
-    for (int idx = tid; idx < (D / 4) * (ES / 4); idx += kThreads) {  // S <- Diag(e^{G_C}) S + K_bar^T U
-      int m0, n0;
-      tile_of<D, ES>(idx, m0, n0);
+    for (int rd = 0; rd < TS::ROUNDS; ++rd) {  // S <- Diag(e^{G_C}) S + K_bar^T U
+      int m0, n0, part;
+      TS::at(tid, rd, m0, n0, part);
+      constexpr int KP = kC / TS::KS;
       float acc[4][4];
       zero(acc);
-      kgemm<4, 4>(acc, Kbs, LD, m0, U, ES, n0, kC);
+      kgemm<4, 4>(acc, Kbs + part * KP * LD, LD, m0, U + part * KP * LS, LS, n0, KP);
+      combine_parts<TS::KS>(acc, part, red, D * LS, LS, m0, n0);
+      if (part == 0)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float& sv = S[(m0 + i) * ES + n0 + j];
-          sv = fmaf(GCs[m0 + i], sv, acc[i][j]);
-        }
+          for (int j = 0; j < 4; ++j) {
+            float& sv = S[(m0 + i) * LS + n0 + j];
+            sv = fmaf(GCs[m0 + i], sv, acc[i][j]);
+          }
     }
     __syncthreads();
   }
@@ -465,8 +508,9 @@ bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int3
 
 template <int D, int E, int ES>
 struct RevSmem {
-  static constexpr int LC = kC + 4, LD = D + 4;
-  static constexpr int floats = kC * LC + D * LC + 2 * kC * LD + D + D * ES + 2 * kC * ES;
+  static constexpr int LC = kC + 4, LD = D + 4, LS = ES + 4;
+  static constexpr int RU = (SerialTiles<kC, ES>::KS - 1) * kC * LS, RS = (SerialTiles<D, ES>::KS - 1) * D * LS;
+  static constexpr int floats = kC * LC + D * LC + 2 * kC * LD + D + D * LS + 2 * kC * LS + (RU > RS ? RU : RS);
 };
 
 template <int D, int E, int ES, typename Tin>
@@ -475,16 +519,20 @@ bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const floa
         const int32_t* __restrict__ plan, const int32_t* __restrict__ cu, int B, int64_t T, int H,
         float* __restrict__ states, float* __restrict__ dh0) {
   using SM = RevSmem<D, E, ES>;
-  constexpr int LC = SM::LC, LD = SM::LD;
+  using TU = SerialTiles<kC, ES>;
+  using TS = SerialTiles<D, ES>;
+  static_assert(TU::ROUNDS == 1, "one dU tile (or k part) per thread");
+  constexpr int LC = SM::LC, LD = SM::LD, LS = SM::LS;
   extern __shared__ __align__(16) float sm[];
   float* Ms = sm;               // M [C][LC]
   float* KbTs = Ms + kC * LC;   // K_bar^T [D][LC]
   float* Qhs = KbTs + D * LC;   // Q_hat [C][LD]
   float* Ws = Qhs + kC * LD;    // W [C][LD]
   float* GCs = Ws + kC * LD;    // [D]
-  float* dS = GCs + D;          // [D][ES]
-  float* dO = dS + D * ES;      // [C][ES]
-  float* dU = dO + kC * ES;     // [C][ES]
+  float* dS = GCs + D;          // [D][LS]
+  float* dO = dS + D * LS;      // [C][LS]
+  float* dU = dO + kC * LS;     // [C][LS]
+  float* red = dU + kC * LS;    // k-part sums
   const int b = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * ES, tid = threadIdx.x;
   if (cu != nullptr && plan[B + 1] == 0) return;
   int64_t first_chunk, t_begin, len;
@@ -493,7 +541,7 @@ bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const floa
   const StateLayout SL{D, E};
   for (int i = tid; i < D * ES; i += kThreads) {
     const int c = i / ES, j = i % ES;
-    dS[i] = dhT != nullptr ? dhT[(((size_t)b * H + h) * D + c) * E + j0 + j] : 0.f;
+    dS[c * LS + j] = dhT != nullptr ? dhT[(((size_t)b * H + h) * D + c) * E + j0 + j] : 0.f;
   }
   for (int64_t ci = nch - 1; ci >= 0; --ci) {
     const size_t task = (size_t)(first_chunk + ci) * H + h;
@@ -518,54 +566,62 @@ bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const floa
     stage(Qhs, LD, rec + L.Qh(), D, kC, D, tid);
     stage(Ws, LD, rec + L.W(), D, kC, D, tid);
     stage(GCs, D, rec + L.GC(), D, 1, D, tid);
-    for (int i = tid; i < kC * ES; i += kThreads) {
-      const int r = i / ES, j = i % ES;
-      dO[i] = r < n ? to_f32(dout[((size_t)(t0 + r) * H + h) * E + j0 + j]) : 0.f;
-    }
+    batched(kC * ES, tid,
+            [&](int i) { return i / ES < n ? to_f32(dout[((size_t)(t0 + i / ES) * H + h) * E + j0 + i % ES]) : 0.f; },
+            [&](int i, float x) { dO[(i / ES) * LS + i % ES] = x; });
     __syncthreads();
-    for (int i = tid; i < D * ES; i += kThreads) {  // dS_C^T
-      const int c = i / ES, j = i % ES;
-      st[SL.dST() + (size_t)(j0 + j) * D + c] = dS[i];
+    for (int i = tid; i < D * ES; i += kThreads) {  // dS_C^T, coalesced along dk
+      const int j = i / D, c = i % D;
+      st[SL.dST() + (size_t)(j0 + j) * D + c] = dS[c * LS + j];
     }
-    for (int idx = tid; idx < (kC / 4) * (ES / 4); idx += kThreads) {  // dU = M^T dO + K_bar dS
-      int m0, n0;
-      tile_of<D, ES>(idx, m0, n0);
+    {  // dU = M^T dO + K_bar dS
+      int m0, n0, part;
+      TU::at(tid, 0, m0, n0, part);
+      constexpr int K1 = kC / TU::KS, K2 = D / TU::KS;
       float acc[4][4];
       zero(acc);
-      kgemm<4, 4>(acc, Ms, LC, m0, dO, ES, n0, kC);
-      kgemm<4, 4>(acc, KbTs, LC, m0, dS, ES, n0, D);
+      kgemm<4, 4>(acc, Ms + part * K1 * LC, LC, m0, dO + part * K1 * LS, LS, n0, K1);
+      kgemm<4, 4>(acc, KbTs + part * K2 * LC, LC, m0, dS + part * K2 * LS, LS, n0, K2);
+      combine_parts<TU::KS>(acc, part, red, kC * LS, LS, m0, n0);
+      if (part == 0)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) dU[(m0 + i) * ES + n0 + j] = acc[i][j];
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<float4*>(dU + (m0 + i) * LS + n0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
     }
     __syncthreads();
-    for (int i = tid; i < kC * ES; i += kThreads) {  // dU^T
-      const int r = i / ES, j = i % ES;
-      st[SL.dUT() + (size_t)(j0 + j) * kC + r] = dU[i];
+    for (int i = tid; i < kC * ES; i += kThreads) {  // dU^T, coalesced along the chunk
+      const int j = i / kC, r = i % kC;
+      st[SL.dUT() + (size_t)(j0 + j) * kC + r] = dU[r * LS + j];
     }
-    for (int idx = tid; idx < (D / 4) * (ES / 4); idx += kThreads) {  // dS <- Q_hat^T dO + Diag(e^{G_C}) dS - W^T dU
-      int m0, n0;
-      tile_of<D, ES>(idx, m0, n0);
+    for (int rd = 0; rd < TS::ROUNDS; ++rd) {  // dS <- Q_hat^T dO + Diag(e^{G_C}) dS - W^T dU
+      int m0, n0, part;
+      TS::at(tid, rd, m0, n0, part);
+      constexpr int KP = kC / TS::KS;
       float a1[4][4], a2[4][4];
       zero(a1);
       zero(a2);
-      kgemm<4, 4>(a1, Qhs, LD, m0, dO, ES, n0, kC);
-      kgemm<4, 4>(a2, Ws, LD, m0, dU, ES, n0, kC);
+      kgemm<4, 4>(a1, Qhs + part * KP * LD, LD, m0, dO + part * KP * LS, LS, n0, KP);
+      kgemm<4, 4>(a2, Ws + part * KP * LD, LD, m0, dU + part * KP * LS, LS, n0, KP);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float& sv = dS[(m0 + i) * ES + n0 + j];
-          sv = fmaf(GCs[m0 + i], sv, a1[i][j] - a2[i][j]);
-        }
+        for (int j = 0; j < 4; ++j) a1[i][j] -= a2[i][j];
+      combine_parts<TS::KS>(a1, part, red, D * LS, LS, m0, n0);
+      if (part == 0)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float& sv = dS[(m0 + i) * LS + n0 + j];
+            sv = fmaf(GCs[m0 + i], sv, a1[i][j]);
+          }
     }
     __syncthreads();
   }
   if (dh0 != nullptr)
     for (int i = tid; i < D * ES; i += kThreads) {
       const int c = i / ES, j = i % ES;
-      dh0[(((size_t)b * H + h) * D + c) * E + j0 + j] = dS[i];
+      dh0[(((size_t)b * H + h) * D + c) * E + j0 + j] = dS[c * LS + j];
     }
 }
 
@@ -1076,7 +1132,8 @@ cudaError_t launch_chunked(const BackwardArgs& a, float* ws, cudaStream_t st) {
   {
     TraceScope ts("kda_bwd_state_passes", st);
     const int nsl = serial_slices(a.B, a.H, E);
-    cudaError_t e = nsl == 8   ? launch_serial<D, E, E / 8, Tin>(a, recs, states, st)
+    // (serial_slices keeps every slice at 16 columns or more)
+    cudaError_t e = nsl == 8   ? launch_serial<D, E, (E / 8 < 16 ? 16 : E / 8), Tin>(a, recs, states, st)
                     : nsl == 4 ? launch_serial<D, E, E / 4, Tin>(a, recs, states, st)
                     : nsl == 2 ? launch_serial<D, E, E / 2, Tin>(a, recs, states, st)
                                : launch_serial<D, E, (E > 64 ? 64 : E), Tin>(a, recs, states, st);
