@@ -21,7 +21,9 @@
 //              K_bar^T, Q_hat, e^{G_C});
 //   bwd_fwd    per (sequence, head, value-column slice), serial over chunks: S0 and U per chunk;
 //   bwd_rev    the same, reverse: dS_C and dU per chunk, dh0;
+//   bwd_dvsums per (chunk, head): the products summed over the value columns, and dv;
 //   bwd_grads  per (chunk, head): the parameter gradients.
+// Global memory is written row by row: a transposed copy is assembled in shared memory first.
 #include "kda_device.cuh"
 #include "kda_internal.h"
 
@@ -32,11 +34,11 @@ constexpr int kC = 64;         // chunk length
 constexpr int kThreads = 256;  // every kernel here
 static_assert(kThreads == 4 * kC, "the diagonal inverses in bwd_rec give each column four lanes");
 
-// acc[i][j] += sum_{k < K} At[k * lda + m0 + i] * B[k * ldb + n0 + j]: a register tile of a product
-// whose operands are both stored k-major (At: the left factor transposed).  MI and NJ are multiples
-// of 4; lda, ldb, m0 and n0 are multiples of 4 (16-byte vector loads); At and B may be in shared or
-// global memory.
-template <int MI, int NJ>
+// acc[i][j] += sum_{k < K} At[k * lda + m0 + i] * B[k * ldb + n0 + (j / 4) * GS + j % 4]: a register
+// tile of a product whose operands are both stored k-major (At: the left factor transposed).  MI and
+// NJ are multiples of 4; lda, ldb, m0, n0 and GS are multiples of 4 (16-byte vector loads).  With
+// GS = 64 and n0 = 4 x (thread mod 16), sixteen threads read 256 contiguous bytes of B per load.
+template <int MI, int NJ, int GS = 4>
 __device__ __forceinline__ void kgemm(float (&acc)[MI][NJ], const float* At, int lda, int m0, const float* B, int ldb,
                                       int n0, int K) {
 #pragma unroll 8  // K is a multiple of 8: eight k-steps of loads in flight
@@ -49,7 +51,7 @@ __device__ __forceinline__ void kgemm(float (&acc)[MI][NJ], const float* At, int
     }
 #pragma unroll
     for (int j = 0; j < NJ; j += 4) {
-      const float4 y = *reinterpret_cast<const float4*>(B + (size_t)k * ldb + n0 + j);
+      const float4 y = *reinterpret_cast<const float4*>(B + (size_t)k * ldb + n0 + (j / 4) * GS);
       b[j] = y.x; b[j + 1] = y.y; b[j + 2] = y.z; b[j + 3] = y.w;
     }
 #pragma unroll
@@ -58,6 +60,8 @@ __device__ __forceinline__ void kgemm(float (&acc)[MI][NJ], const float* At, int
       for (int j = 0; j < NJ; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
   }
 }
+// column of element j of a tile loaded with group stride 64 (the j-th value of kgemm<.., NJ, 64>)
+__device__ __forceinline__ constexpr int wide_col(int j) { return 64 * (j >> 2) + (j & 3); }
 template <int MI, int NJ>
 __device__ __forceinline__ void zero(float (&acc)[MI][NJ]) {
 #pragma unroll
@@ -129,6 +133,15 @@ struct StateLayout {
   __host__ __device__ size_t dUT() const { return dST() + (size_t)E * D; }
   __host__ __device__ size_t size() const { return dUT() + (size_t)E * kC; }
 };
+
+// rows x C floats from shared memory (row stride sld) to a dense [rows][C] block of global memory,
+// 16-byte coalesced stores
+__device__ __forceinline__ void copy_out(float* dst, const float* src, int sld, int rows, int tid) {
+  for (int i = tid; i < rows * (kC / 4); i += kThreads) {
+    const int r = i / (kC / 4), c = 4 * (i % (kC / 4));
+    *reinterpret_cast<float4*>(dst + (size_t)r * kC + c) = *reinterpret_cast<const float4*>(src + r * sld + c);
+  }
+}
 
 // ---------------------------------------------------------------- per-chunk records
 // Shared floats of bwd_rec: k, q, G [C][D+4]; scratch (A/M operands, later V and T^T); A_tilde, M, X
@@ -235,16 +248,19 @@ bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restr
       }
     }
     __syncthreads();
-    // e^{G_C}, K_bar = k e^{G_C - G} (and transposed), Q_hat = q e^{G}
+    // e^{G_C}, K_bar = k e^{G_C - G} (and its transpose, through the scratch), Q_hat = q e^{G}
     for (int i = tid; i < kC * D; i += kThreads) {
       const int r = i / D, c = i % D;
       const float G = gS[r * LD + c], Gc = gS[(kC - 1) * LD + c];
       const float kb = kS[r * LD + c] * __expf(Gc - G);
       rec[L.Kb() + (size_t)r * D + c] = kb;
-      rec[L.KbT() + (size_t)c * kC + r] = kb;
+      sc[c * LC + r] = kb;
       rec[L.Qh() + (size_t)r * D + c] = qS[r * LD + c] * __expf(G);
       if (r == 0) rec[L.GC() + c] = __expf(Gc);
     }
+    __syncthreads();
+    copy_out(rec + L.KbT(), sc, LC, D, tid);
+    __syncthreads();
     // A_tilde (strict lower) and M (lower incl. diagonal) by 32 x 32 blocks, each with a reference
     // point R that keeps every factor within e^{+-80} (g > -5): the diagonal blocks use the centred
     // rows 15 and 47, the block below the diagonal row 47 (its key-side factor is then <= 1)
@@ -338,29 +354,34 @@ bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restr
     batched(kC * E, tid, [&](int i) { const int r = i / E; return r < n ? to_f32(v[((size_t)(t0 + r) * H + h) * E + i % E]) : 0.f; },
             [&](int i, float x) { vS[(i / E) * LE + i % E] = x; });
     __syncthreads();
-    {  // W = T K_hat (and W^T)
-      const int m0 = 4 * (tid >> 4), n0 = (D / 16) * (tid & 15);
+    float* WTs = qS;  // [D][LC] over q and G (free now)
+    static_assert(D * LC <= 2 * kC * LD, "W^T fits over q and G");
+    {  // W = T K_hat (and its transpose, through shared memory)
+      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
       float acc[4][D / 16];
       zero(acc);
-      kgemm<4, D / 16>(acc, TT, LC, m0, kS, LD, n0, kC);
+      kgemm<4, D / 16, 64>(acc, TT, LC, m0, kS, LD, n0, kC);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < D / 16; ++j) {
-          rec[L.W() + (size_t)(m0 + i) * D + n0 + j] = acc[i][j];
-          rec[L.WT() + (size_t)(n0 + j) * kC + m0 + i] = acc[i][j];
-        }
+        for (int j = 0; j < D / 16; ++j) rec[L.W() + (size_t)(m0 + i) * D + n0 + wide_col(j)] = acc[i][j];
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j)
+        *reinterpret_cast<float4*>(WTs + (n0 + wide_col(j)) * LC + m0) =
+            make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
     }
     {  // U_hat = T V
-      const int m0 = 4 * (tid >> 4), n0 = (E / 16) * (tid & 15);
+      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
       float acc[4][E / 16];
       zero(acc);
-      kgemm<4, E / 16>(acc, TT, LC, m0, vS, LE, n0, kC);
+      kgemm<4, E / 16, 64>(acc, TT, LC, m0, vS, LE, n0, kC);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < E / 16; ++j) rec[L.Uh() + (size_t)(m0 + i) * E + n0 + j] = acc[i][j];
+        for (int j = 0; j < E / 16; ++j) rec[L.Uh() + (size_t)(m0 + i) * E + n0 + wide_col(j)] = acc[i][j];
     }
+    __syncthreads();
+    copy_out(rec + L.WT(), WTs, LC, D, tid);
     __syncthreads();  // shared memory is rewritten by the next task
   }
 }
@@ -376,6 +397,25 @@ __device__ __forceinline__ void stage(float* dst, int sld, const float* src, siz
   batched(rows * q, tid,
           [&](int i) { return *reinterpret_cast<const float4*>(src + (size_t)(i / q) * gld + 4 * (i % q)); },
           [&](int i, float4 x) { *reinterpret_cast<float4*>(dst + (i / q) * sld + 4 * (i % q)) = x; });
+}
+
+// The transpose of a rows x cols block of global memory (row stride gld; rows a multiple of 8, cols
+// of 16) into shared memory, dst[c * sld + r] (sld = 4 mod 32).  Each warp moves 8 rows x 16
+// columns: 64 contiguous bytes of each row, and shared stores at most two-way conflicted.
+__device__ __forceinline__ void stage_t(float* dst, int sld, const float* src, size_t gld, int rows, int cols,
+                                        int tid) {
+  const int rb = rows / 8;
+  const auto row = [&](int i) { return 8 * ((i >> 5) % rb) + (i & 7); };
+  const auto grp = [&](int i) { return 4 * ((i >> 5) / rb) + ((i & 31) >> 3); };  // 4-column group
+  batched(rows * (cols / 4), tid,
+          [&](int i) { return *reinterpret_cast<const float4*>(src + (size_t)row(i) * gld + 4 * grp(i)); },
+          [&](int i, float4 x) {
+            float* o = dst + 4 * grp(i) * sld + row(i);
+            o[0] = x.x;
+            o[sld] = x.y;
+            o[2 * sld] = x.z;
+            o[3 * sld] = x.w;
+          });
 }
 
 // Tiles of a ROWS x ES product: thread tid owns tile tid % TILES (if any) and the k part tid / TILES.
@@ -549,13 +589,11 @@ bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const floa
     float* st = states + task * SL.size();
     const int64_t t0 = t_begin + 64 * ci;
     const int n = (int)(len - 64 * ci < 64 ? len - 64 * ci : 64);
-    if (ci > 0) {  // the previous chunk's records (M, W, K_bar^T and Q_hat, e^{G_C}) and dout rows
+    if (ci > 0) {  // the previous chunk's records (M and W; K_bar^T, Q_hat and e^{G_C}) and dout rows
       const float* nx = rec - (size_t)H * L.size();
       if (tid == 0) {
-        prefetch_l2(nx + L.M(), kC * kC * 4);
-        prefetch_l2(nx + L.W(), kC * D * 4);
-        prefetch_l2(nx + L.KbT(), 2 * kC * D * 4);
-        prefetch_l2(nx + L.GC(), D * 4);
+        prefetch_l2(nx + L.M(), (uint32_t)((L.W() + (size_t)kC * D - L.M()) * 4));
+        prefetch_l2(nx + L.KbT(), (uint32_t)((L.size() - L.KbT()) * 4));
       } else if (tid >= 64 && tid < 64 + kC) {
         const Tin* row = dout + ((size_t)(t0 - 64 + tid - 64) * H + h) * E + j0;
         asm volatile("prefetch.global.L2 [%0];" ::"l"(row) : "memory");
@@ -631,9 +669,8 @@ struct GradLayout {
   int D;
   __host__ __device__ size_t dQh() const { return 0; }                       // [C][D]
   __host__ __device__ size_t dW() const { return (size_t)kC * D; }           // [C][D]
-  __host__ __device__ size_t dWT() const { return 2 * (size_t)kC * D; }      // [D][C]
-  __host__ __device__ size_t dKb() const { return 3 * (size_t)kC * D; }      // [C][D]
-  __host__ __device__ size_t dM() const { return 4 * (size_t)kC * D; }       // [C][C] (on M's support)
+  __host__ __device__ size_t dKb() const { return 2 * (size_t)kC * D; }      // [C][D]
+  __host__ __device__ size_t dM() const { return 3 * (size_t)kC * D; }       // [C][C] (on M's support)
   __host__ __device__ size_t dT1() const { return dM() + (size_t)kC * kC; }  // [C][C]: dU V^T
   __host__ __device__ size_t dGam() const { return dT1() + (size_t)kC * kC; }  // [D]: rowsum(dS_C (.) S0)
   __host__ __device__ size_t size() const { return dGam() + (size_t)D; }
@@ -729,31 +766,30 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
     for (int i = tid; i < kC * E; i += kThreads) dUr[(i % kC) * LE + i / kC] = dUT[(i / kC) * LC + i % kC];
     __syncthreads();
     {
-      const int m0 = 4 * (tid >> 4), n0 = (D / 16) * (tid & 15);
+      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
       float a1[4][D / 16], a2[4][D / 16];
       zero(a1);
       zero(a2);
-      kgemm<4, D / 16>(a1, dOT, LC, m0, S0T, LD, n0, E);  // dO S0^T
-      kgemm<4, D / 16>(a2, dUT, LC, m0, S0T, LD, n0, E);  // dU S0^T
+      kgemm<4, D / 16, 64>(a1, dOT, LC, m0, S0T, LD, n0, E);  // dO S0^T
+      kgemm<4, D / 16, 64>(a2, dUT, LC, m0, S0T, LD, n0, E);  // dU S0^T
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
-          gr[GL.dQh() + (size_t)(m0 + i) * D + n0 + j] = a1[i][j];
-          gr[GL.dW() + (size_t)(m0 + i) * D + n0 + j] = -a2[i][j];
-          gr[GL.dWT() + (size_t)(n0 + j) * kC + m0 + i] = -a2[i][j];
+          gr[GL.dQh() + (size_t)(m0 + i) * D + n0 + wide_col(j)] = a1[i][j];
+          gr[GL.dW() + (size_t)(m0 + i) * D + n0 + wide_col(j)] = -a2[i][j];
         }
     }
     {  // dv = T^T dU (rows of the sequence only)
-      const int m0 = 4 * (tid >> 4), n0 = (E / 16) * (tid & 15);
+      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
       float acc[4][E / 16];
       zero(acc);
-      kgemm<4, E / 16>(acc, TS, LC, m0, dUr, LE, n0, kC);
+      kgemm<4, E / 16, 64>(acc, TS, LC, m0, dUr, LE, n0, kC);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         if (m0 + i < n)
 #pragma unroll
-          for (int j = 0; j < E / 16; ++j) dv[((size_t)(t0 + m0 + i) * H + h) * E + n0 + j] = acc[i][j];
+          for (int j = 0; j < E / 16; ++j) dv[((size_t)(t0 + m0 + i) * H + h) * E + n0 + wide_col(j)] = acc[i][j];
     }
     if (tid < D) {  // rowsum(dS_C (.) S0), dS_C^T from global
       float s0 = 0.f, s1 = 0.f;
@@ -769,14 +805,14 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
     stage(UT, LC, st + SL.UT(), kC, E, kC, tid);
     __syncthreads();
     {
-      const int m0 = 4 * (tid >> 4), n0 = (D / 16) * (tid & 15);
+      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
       float a1[4][D / 16];
       zero(a1);
-      kgemm<4, D / 16>(a1, UT, LC, m0, S0T, LD, n0, E);  // U dS_C^T
+      kgemm<4, D / 16, 64>(a1, UT, LC, m0, S0T, LD, n0, E);  // U dS_C^T
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < D / 16; ++j) gr[GL.dKb() + (size_t)(m0 + i) * D + n0 + j] = a1[i][j];
+        for (int j = 0; j < D / 16; ++j) gr[GL.dKb() + (size_t)(m0 + i) * D + n0 + wide_col(j)] = a1[i][j];
     }
     {
       const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
@@ -862,6 +898,9 @@ bwd_grads(const Tin* __restrict__ q, const Tin* __restrict__ k, const float* __r
     __syncthreads();
     // ---- dT = dU V^T + dW K_hat^T
     float* KhT = r2;  // [D][LC]
+    float* dWT = s1;  // [D][LC] over s1 and s2 (free until dX)
+    static_assert(D * LC <= 2 * kC * LC, "dW^T fits in two C x C tiles");
+    stage_t(dWT, LC, gr + GL.dW(), D, kC, D, tid);
     for (int i = tid; i < kC * D; i += kThreads) {
       const int s = i / D, c = i % D;
       KhT[c * LC + s] = kS[s * LD + c] * __expf(gS[s * LD + c]);
@@ -872,7 +911,7 @@ bwd_grads(const Tin* __restrict__ q, const Tin* __restrict__ k, const float* __r
       const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
       float acc[4][4];
       zero(acc);
-      kgemm<4, 4>(acc, gr + GL.dWT(), kC, m0, KhT, LC, n0, D);
+      kgemm<4, 4>(acc, dWT, LC, m0, KhT, LC, n0, D);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
