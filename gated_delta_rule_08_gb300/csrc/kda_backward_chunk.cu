@@ -391,13 +391,27 @@ bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restr
 // the columns of the state).  Per chunk, 64 x ES and D x ES products with 4 x 4 register tiles;
 // when a product has fewer tiles than threads, its k range is split over KS thread groups.
 
-// rows x cols floats from global (row stride gld) into shared memory (row stride sld), 16-byte copies
+// rows x cols floats from global (row stride gld) into shared memory (row stride sld), 16-byte
+// copies through registers, eight per thread in flight (measured faster than the asynchronous
+// copies below for the serial passes' L2-resident records)
 __device__ __forceinline__ void stage(float* dst, int sld, const float* src, size_t gld, int rows, int cols, int tid) {
   const int q = cols / 4;
   batched(rows * q, tid,
           [&](int i) { return *reinterpret_cast<const float4*>(src + (size_t)(i / q) * gld + 4 * (i % q)); },
           [&](int i, float4 x) { *reinterpret_cast<float4*>(dst + (i / q) * sld + 4 * (i % q)) = x; });
 }
+// the same as asynchronous 16-byte copies, all in flight at once; stage_wait() before the barrier
+// that publishes them
+__device__ __forceinline__ void stage_async(float* dst, int sld, const float* src, size_t gld, int rows, int cols,
+                                            int tid) {
+  const int q = cols / 4;
+  for (int i = tid; i < rows * q; i += kThreads) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst + (i / q) * sld + 4 * (i % q)));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src + (size_t)(i / q) * gld + 4 * (i % q))
+                 : "memory");
+  }
+}
+__device__ __forceinline__ void stage_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // The transpose of a rows x cols block of global memory (row stride gld; rows a multiple of 8, cols
 // of 16) into shared memory, dst[c * sld + r] (sld = 4 mod 32).  Each warp moves 8 rows x 16
@@ -753,15 +767,16 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
       }
     }
     {
+      stage_async(dUT, LC, st + SL.dUT(), kC, E, kC, tid);
+      stage_async(S0T, LD, st + SL.S0T(), D, E, D, tid);
+      stage_async(TS, LC, rec + L.T(), kC, kC, kC, tid);
       TileLoadT<E, Tin> tdo, tv;
       tdo.load(dout, t0, n, H, h, tid);
       tv.load(v, t0, n, H, h, tid);
-      stage(dUT, LC, st + SL.dUT(), kC, E, kC, tid);
-      stage(S0T, LD, st + SL.S0T(), D, E, D, tid);
-      stage(TS, LC, rec + L.T(), kC, kC, kC, tid);
       tdo.store(dOT, LC, tid);
       tv.store(VT, LC, tid);
     }
+    stage_wait();
     __syncthreads();
     for (int i = tid; i < kC * E; i += kThreads) dUr[(i % kC) * LE + i / kC] = dUT[(i / kC) * LC + i % kC];
     __syncthreads();
@@ -801,8 +816,9 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
     }
     __syncthreads();  // S0^T and dU are no longer read
     float* UT = dUr;
-    stage(S0T, LD, st + SL.dST(), D, E, D, tid);
-    stage(UT, LC, st + SL.UT(), kC, E, kC, tid);
+    stage_async(S0T, LD, st + SL.dST(), D, E, D, tid);
+    stage_async(UT, LC, st + SL.UT(), kC, E, kC, tid);
+    stage_wait();
     __syncthreads();
     {
       const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
