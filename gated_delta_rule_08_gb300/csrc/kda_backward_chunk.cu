@@ -70,6 +70,65 @@ __device__ __forceinline__ void zero(float (&acc)[MI][NJ]) {
     for (int j = 0; j < NJ; ++j) acc[i][j] = 0.f;
 }
 
+// ---- warp-level tensor-core products (mma.sync m16n8k8, tf32) with a three-term split: each operand
+// x = hi + lo with hi = x truncated to tf32 (its low 13 mantissa bits cleared) and lo = x - hi (exact
+// in fp32), and hi*hi + hi*lo + lo*hi accumulated in fp32.  The tensor core reads only the tf32 part
+// of lo, so the dropped terms are about 2^-20 of each product: fp32-level results for the backward's
+// tolerance, with two integer/float instructions per element instead of conversions.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = __float_as_uint(x) & 0xffffe000u;
+  lo = __float_as_uint(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// acc (a 16 x 8 NT tile at rows m0.., columns n0..) += sum_{k < K} At[k * lda + m] B[k * ldb + n] for one
+// warp; both operands k-major in shared memory, K a multiple of 8.  The three terms accumulate
+// separately (no MMA waits on the one before it in the same k step) and are added at the end.
+// Lane (g = lane / 4, t = lane % 4) holds acc[nt][0..1] at row m0 + g, columns n0 + 8 nt + 2t, +1,
+// and acc[nt][2..3] eight rows below.
+template <int NT>
+__device__ __forceinline__ void warp_mma(float (&acc)[NT][4], const float* At, int lda, int m0, const float* B,
+                                         int ldb, int n0, int K, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  float hl[NT][4] = {}, lh[NT][4] = {};
+#pragma unroll 4
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint32_t ah[4], al[4];
+    split_tf32(At[(k0 + t) * lda + m0 + g], ah[0], al[0]);
+    split_tf32(At[(k0 + t) * lda + m0 + g + 8], ah[1], al[1]);
+    split_tf32(At[(k0 + t + 4) * lda + m0 + g], ah[2], al[2]);
+    split_tf32(At[(k0 + t + 4) * lda + m0 + g + 8], ah[3], al[3]);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      uint32_t bh0, bl0, bh1, bl1;
+      split_tf32(B[(k0 + t) * ldb + n0 + 8 * nt + g], bh0, bl0);
+      split_tf32(B[(k0 + t + 4) * ldb + n0 + 8 * nt + g], bh1, bl1);
+      mma_tf32(acc[nt], ah, bh0, bh1);
+      mma_tf32(hl[nt], ah, bl0, bl1);
+      mma_tf32(lh[nt], al, bh0, bh1);
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] += hl[nt][e] + lh[nt][e];
+}
+// Warp tiling of a ROWS x ES product over the eight warps: warp w takes the 16-row tile w mod
+// (ROWS / 16) and NT eight-column tiles starting at column n0.
+template <int ROWS, int ES>
+struct WarpTiles {
+  static constexpr int MT = ROWS / 16, WPM = 8 / MT, NT = ES / 8 / WPM;
+  static_assert(8 % MT == 0 && NT >= 1, "tiling");
+  __device__ static void at(int warp, int& m0, int& n0) {
+    m0 = 16 * (warp % MT);
+    n0 = (warp / MT) * (ES / WPM);
+  }
+};
+
 // for (i = tid; i < n; i += kThreads) put(i, get(i)), with eight loads in flight per thread before
 // their stores (the gets are global loads, the puts shared-memory stores)
 template <class Get, class Put>
@@ -388,8 +447,8 @@ bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restr
 
 // ---------------------------------------------------------------- the two serial passes
 // Each CTA: one (sequence, head) chain and ES of its value columns (the recurrence is separable in
-// the columns of the state).  Per chunk, 64 x ES and D x ES products with 4 x 4 register tiles;
-// when a product has fewer tiles than threads, its k range is split over KS thread groups.
+// the columns of the state).  Per chunk, 64 x ES and D x ES products on the tensor cores (warp_mma,
+// three-term tf32), each warp owning whole tiles of the result.
 
 // rows x cols floats from global (row stride gld) into shared memory (row stride sld), 16-byte
 // copies through registers, eight per thread in flight (measured faster than the asynchronous
@@ -432,57 +491,23 @@ __device__ __forceinline__ void stage_t(float* dst, int sld, const float* src, s
           });
 }
 
-// Tiles of a ROWS x ES product: thread tid owns tile tid % TILES (if any) and the k part tid / TILES.
-template <int ROWS, int ES>
-struct SerialTiles {
-  static constexpr int TILES = (ROWS / 4) * (ES / 4);
-  static constexpr int KS = TILES >= kThreads ? 1 : kThreads / TILES;  // k parts
-  static constexpr int ROUNDS = TILES >= kThreads ? TILES / kThreads : 1;
-  static_assert(TILES % kThreads == 0 || kThreads % TILES == 0, "tiles and threads must divide");
-  static_assert(KS == 1 || KS == 2 || KS == 4, "k split");
-  __device__ static void at(int tid, int round, int& m0, int& n0, int& part) {
-    const int idx = KS == 1 ? tid + round * kThreads : tid % TILES;
-    part = KS == 1 ? 0 : tid / TILES;
-    m0 = 4 * (idx / (ES / 4));
-    n0 = 4 * (idx % (ES / 4));
-  }
-};
-// After each part has its partial 4 x 4 sums: parts > 0 leave them in red (KS - 1 planes of
-// ROWS x ld floats), and after the barrier part 0 holds the total.  Every thread calls this.
-template <int KS>
-__device__ __forceinline__ void combine_parts(float (&acc)[4][4], int part, float* red, int plane, int ld, int m0,
-                                              int n0) {
-  if (KS == 1) return;
-  if (part > 0)
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      *reinterpret_cast<float4*>(red + (part - 1) * plane + (m0 + i) * ld + n0) =
-          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-  __syncthreads();
-  if (part == 0)
-    for (int p = 1; p < KS; ++p)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 x = *reinterpret_cast<const float4*>(red + (p - 1) * plane + (m0 + i) * ld + n0);
-        acc[i][0] += x.x; acc[i][1] += x.y; acc[i][2] += x.z; acc[i][3] += x.w;
-      }
-}
-
 template <int D, int E, int ES>
 struct FwdSmem {
   static constexpr int LC = kC + 4, LD = D + 4, LS = ES + 4;
-  static constexpr int RU = (SerialTiles<kC, ES>::KS - 1) * kC * LS, RS = (SerialTiles<D, ES>::KS - 1) * D * LS;
-  static constexpr int floats = D * LC + kC * LD + kC * LS + D + D * LS + kC * LS + (RU > RS ? RU : RS);
+  static constexpr int floats = D * LC + kC * LD + kC * LS + D + D * LS + kC * LS;
 };
+
+// the fragment element e of tile nt of a warp_mma accumulator: its row and column
+__device__ __forceinline__ int frag_row(int m0, int lane, int e) { return m0 + (lane >> 2) + 8 * (e >> 1); }
+__device__ __forceinline__ int frag_col(int n0, int lane, int nt, int e) { return n0 + 8 * nt + 2 * (lane & 3) + (e & 1); }
 
 template <int D, int E, int ES>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int32_t* __restrict__ plan,
         const int32_t* __restrict__ cu, int B, int64_t T, int H, float* __restrict__ states) {
   using SM = FwdSmem<D, E, ES>;
-  using TU = SerialTiles<kC, ES>;
-  using TS = SerialTiles<D, ES>;
-  static_assert(TU::ROUNDS == 1, "one U tile (or k part) per thread");
+  using TU = WarpTiles<kC, ES>;
+  using TS = WarpTiles<D, ES>;
   constexpr int LC = SM::LC, LD = SM::LD, LS = SM::LS;
   extern __shared__ __align__(16) float sm[];
   float* WTs = sm;              // W^T [D][LC]
@@ -491,8 +516,8 @@ bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int3
   float* GCs = Uhs + kC * LS;   // e^{G_C} [D]
   float* S = GCs + D;           // [D][LS]
   float* U = S + D * LS;        // [C][LS]
-  float* red = U + kC * LS;     // k-part sums
   const int b = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * ES, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   if (cu != nullptr && plan[B + 1] == 0) return;
   int64_t first_chunk, t_begin, len;
   const int64_t nch = sequence_chunks(b, plan, cu, B, T, first_chunk, t_begin, len);
@@ -521,40 +546,36 @@ bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int3
       st[SL.S0T() + (size_t)(j0 + j) * D + c] = S[c * LS + j];
     }
     {  // U = U_hat - W S
-      int m0, n0, part;
-      TU::at(tid, 0, m0, n0, part);
-      constexpr int KP = D / TU::KS;
-      float acc[4][4];
-      zero(acc);
-      kgemm<4, 4>(acc, WTs + part * KP * LC, LC, m0, S + part * KP * LS, LS, n0, KP);
-      combine_parts<TU::KS>(acc, part, red, kC * LS, LS, m0, n0);
-      if (part == 0)
+      int m0, n0;
+      TU::at(warp, m0, n0);
+      float acc[TU::NT][4] = {};
+      warp_mma<TU::NT>(acc, WTs, LC, m0, S, LS, n0, D, lane);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+      for (int nt = 0; nt < TU::NT; ++nt)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) U[(m0 + i) * LS + n0 + j] = Uhs[(m0 + i) * LS + n0 + j] - acc[i][j];
+        for (int e = 0; e < 4; ++e) {
+          const int r = frag_row(m0, lane, e), c = frag_col(n0, lane, nt, e);
+          U[r * LS + c] = Uhs[r * LS + c] - acc[nt][e];
+        }
     }
     __syncthreads();
     for (int i = tid; i < kC * ES; i += kThreads) {  // U^T, coalesced along the chunk
       const int j = i / kC, r = i % kC;
       st[SL.UT() + (size_t)(j0 + j) * kC + r] = U[r * LS + j];
     }
-    for (int rd = 0; rd < TS::ROUNDS; ++rd) {  // S <- Diag(e^{G_C}) S + K_bar^T U
-      int m0, n0, part;
-      TS::at(tid, rd, m0, n0, part);
-      constexpr int KP = kC / TS::KS;
-      float acc[4][4];
-      zero(acc);
-      kgemm<4, 4>(acc, Kbs + part * KP * LD, LD, m0, U + part * KP * LS, LS, n0, KP);
-      combine_parts<TS::KS>(acc, part, red, D * LS, LS, m0, n0);
-      if (part == 0)
+    {  // S <- Diag(e^{G_C}) S + K_bar^T U (each warp reads and writes only its own tile of S)
+      int m0, n0;
+      TS::at(warp, m0, n0);
+      float acc[TS::NT][4] = {};
+      warp_mma<TS::NT>(acc, Kbs, LD, m0, U, LS, n0, kC, lane);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+      for (int nt = 0; nt < TS::NT; ++nt)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float& sv = S[(m0 + i) * LS + n0 + j];
-            sv = fmaf(GCs[m0 + i], sv, acc[i][j]);
-          }
+        for (int e = 0; e < 4; ++e) {
+          const int r = frag_row(m0, lane, e), c = frag_col(n0, lane, nt, e);
+          float& sv = S[r * LS + c];
+          sv = fmaf(GCs[r], sv, acc[nt][e]);
+        }
     }
     __syncthreads();
   }
@@ -563,8 +584,7 @@ bwd_fwd(const float* __restrict__ recs, const float* __restrict__ h0, const int3
 template <int D, int E, int ES>
 struct RevSmem {
   static constexpr int LC = kC + 4, LD = D + 4, LS = ES + 4;
-  static constexpr int RU = (SerialTiles<kC, ES>::KS - 1) * kC * LS, RS = (SerialTiles<D, ES>::KS - 1) * D * LS;
-  static constexpr int floats = kC * LC + D * LC + 2 * kC * LD + D + D * LS + 2 * kC * LS + (RU > RS ? RU : RS);
+  static constexpr int floats = kC * LC + D * LC + 2 * kC * LD + D + D * LS + 2 * kC * LS;
 };
 
 template <int D, int E, int ES, typename Tin>
@@ -573,9 +593,8 @@ bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const floa
         const int32_t* __restrict__ plan, const int32_t* __restrict__ cu, int B, int64_t T, int H,
         float* __restrict__ states, float* __restrict__ dh0) {
   using SM = RevSmem<D, E, ES>;
-  using TU = SerialTiles<kC, ES>;
-  using TS = SerialTiles<D, ES>;
-  static_assert(TU::ROUNDS == 1, "one dU tile (or k part) per thread");
+  using TU = WarpTiles<kC, ES>;
+  using TS = WarpTiles<D, ES>;
   constexpr int LC = SM::LC, LD = SM::LD, LS = SM::LS;
   extern __shared__ __align__(16) float sm[];
   float* Ms = sm;               // M [C][LC]
@@ -586,8 +605,8 @@ bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const floa
   float* dS = GCs + D;          // [D][LS]
   float* dO = dS + D * LS;      // [C][LS]
   float* dU = dO + kC * LS;     // [C][LS]
-  float* red = dU + kC * LS;    // k-part sums
   const int b = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * ES, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   if (cu != nullptr && plan[B + 1] == 0) return;
   int64_t first_chunk, t_begin, len;
   const int64_t nch = sequence_chunks(b, plan, cu, B, T, first_chunk, t_begin, len);
@@ -627,46 +646,35 @@ bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const floa
       st[SL.dST() + (size_t)(j0 + j) * D + c] = dS[c * LS + j];
     }
     {  // dU = M^T dO + K_bar dS
-      int m0, n0, part;
-      TU::at(tid, 0, m0, n0, part);
-      constexpr int K1 = kC / TU::KS, K2 = D / TU::KS;
-      float acc[4][4];
-      zero(acc);
-      kgemm<4, 4>(acc, Ms + part * K1 * LC, LC, m0, dO + part * K1 * LS, LS, n0, K1);
-      kgemm<4, 4>(acc, KbTs + part * K2 * LC, LC, m0, dS + part * K2 * LS, LS, n0, K2);
-      combine_parts<TU::KS>(acc, part, red, kC * LS, LS, m0, n0);
-      if (part == 0)
+      int m0, n0;
+      TU::at(warp, m0, n0);
+      float acc[TU::NT][4] = {};
+      warp_mma<TU::NT>(acc, Ms, LC, m0, dO, LS, n0, kC, lane);
+      warp_mma<TU::NT>(acc, KbTs, LC, m0, dS, LS, n0, D, lane);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<float4*>(dU + (m0 + i) * LS + n0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      for (int nt = 0; nt < TU::NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dU[frag_row(m0, lane, e) * LS + frag_col(n0, lane, nt, e)] = acc[nt][e];
     }
     __syncthreads();
     for (int i = tid; i < kC * ES; i += kThreads) {  // dU^T, coalesced along the chunk
       const int j = i / kC, r = i % kC;
       st[SL.dUT() + (size_t)(j0 + j) * kC + r] = dU[r * LS + j];
     }
-    for (int rd = 0; rd < TS::ROUNDS; ++rd) {  // dS <- Q_hat^T dO + Diag(e^{G_C}) dS - W^T dU
-      int m0, n0, part;
-      TS::at(tid, rd, m0, n0, part);
-      constexpr int KP = kC / TS::KS;
-      float a1[4][4], a2[4][4];
-      zero(a1);
-      zero(a2);
-      kgemm<4, 4>(a1, Qhs + part * KP * LD, LD, m0, dO + part * KP * LS, LS, n0, KP);
-      kgemm<4, 4>(a2, Ws + part * KP * LD, LD, m0, dU + part * KP * LS, LS, n0, KP);
+    {  // dS <- Q_hat^T dO + Diag(e^{G_C}) dS - W^T dU (each warp reads and writes only its own tile of dS)
+      int m0, n0;
+      TS::at(warp, m0, n0);
+      float a1[TS::NT][4] = {}, a2[TS::NT][4] = {};
+      warp_mma<TS::NT>(a1, Qhs, LD, m0, dO, LS, n0, kC, lane);
+      warp_mma<TS::NT>(a2, Ws, LD, m0, dU, LS, n0, kC, lane);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int nt = 0; nt < TS::NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) a1[i][j] -= a2[i][j];
-      combine_parts<TS::KS>(a1, part, red, D * LS, LS, m0, n0);
-      if (part == 0)
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float& sv = dS[(m0 + i) * LS + n0 + j];
-            sv = fmaf(GCs[m0 + i], sv, a1[i][j]);
-          }
+        for (int e = 0; e < 4; ++e) {
+          const int r = frag_row(m0, lane, e), c = frag_col(n0, lane, nt, e);
+          float& sv = dS[r * LS + c];
+          sv = fmaf(GCs[r], sv, a1[nt][e] - a2[nt][e]);
+        }
     }
     __syncthreads();
   }
