@@ -117,6 +117,24 @@ __device__ __forceinline__ void warp_mma(float (&acc)[NT][4], const float* At, i
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[nt][e] += hl[nt][e] + lh[nt][e];
 }
+// the fragment element e of tile nt of a warp_mma accumulator: its row and column
+__device__ __forceinline__ int frag_row(int m0, int lane, int e) { return m0 + (lane >> 2) + 8 * (e >> 1); }
+__device__ __forceinline__ int frag_col(int n0, int lane, int nt, int e) { return n0 + 8 * nt + 2 * (lane & 3) + (e & 1); }
+// rows r < rmax of a warp_mma result, times scale, into a row-major array (row stride ld)
+template <int NT>
+__device__ __forceinline__ void frag_store(float* dst, size_t ld, const float (&acc)[NT][4], int m0, int n0, int lane,
+                                           float scale, int rmax = kC) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int r = m0 + g + 8 * hf;
+      if (r < rmax)
+        *reinterpret_cast<float2*>(dst + (size_t)r * ld + n0 + 8 * nt + 2 * t) =
+            make_float2(scale * acc[nt][2 * hf], scale * acc[nt][2 * hf + 1]);
+    }
+}
 // Warp tiling of a ROWS x ES product over the eight warps: warp w takes the 16-row tile w mod
 // (ROWS / 16) and NT eight-column tiles starting at column n0.
 template <int ROWS, int ES>
@@ -337,19 +355,19 @@ bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restr
         YT[c * L32 + r] = kS[(sb + r) * LD + c] * __expf(R - gS[(sb + r) * LD + c]);
       }
       __syncthreads();
-      if (tid < 128) {
-        const bool isM = tid >= 64;
-        const int t = tid & 63, r0 = 4 * (t >> 3), s0 = 4 * (t & 7);
-        float acc[4][4];
-        zero(acc);
-        kgemm<4, 4>(acc, isM ? XqT : XkT, L32, r0, YT, L32, s0, D);
+      {  // warp w: the A (w < 4) or M block, rows 16 ((w >> 1) & 1).., columns 16 (w & 1)..
+        const int warp = tid >> 5, lane = tid & 31;
+        const bool isM = warp >= 4;
+        const int m0 = 16 * ((warp >> 1) & 1), n0 = 16 * (warp & 1);
+        float acc[2][4] = {};
+        warp_mma<2>(acc, isM ? XqT : XkT, L32, m0, YT, L32, n0, D, lane);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int r = ra + r0 + i, s = sb + s0 + j;
-            if (isM) MS[r * LC + s] = r >= s ? acc[i][j] : 0.f;  // select, not mask-multiply
-            else AtS[r * LC + s] = r > s ? acc[i][j] : 0.f;
+          for (int e = 0; e < 4; ++e) {
+            const int r = ra + frag_row(m0, lane, e), s = sb + frag_col(n0, lane, nt, e);
+            if (isM) MS[r * LC + s] = r >= s ? acc[nt][e] : 0.f;  // select, not mask-multiply
+            else AtS[r * LC + s] = r > s ? acc[nt][e] : 0.f;
           }
       }
       __syncthreads();
@@ -416,28 +434,26 @@ bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restr
     float* WTs = qS;  // [D][LC] over q and G (free now)
     static_assert(D * LC <= 2 * kC * LD, "W^T fits over q and G");
     {  // W = T K_hat (and its transpose, through shared memory)
-      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
-      float acc[4][D / 16];
-      zero(acc);
-      kgemm<4, D / 16, 64>(acc, TT, LC, m0, kS, LD, n0, kC);
+      using TD = WarpTiles<kC, D>;
+      const int warp = tid >> 5, lane = tid & 31;
+      int m0, n0;
+      TD::at(warp, m0, n0);
+      float acc[TD::NT][4] = {};
+      warp_mma<TD::NT>(acc, TT, LC, m0, kS, LD, n0, kC, lane);
+      frag_store<TD::NT>(rec + L.W(), D, acc, m0, n0, lane, 1.f);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int nt = 0; nt < TD::NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < D / 16; ++j) rec[L.W() + (size_t)(m0 + i) * D + n0 + wide_col(j)] = acc[i][j];
-#pragma unroll
-      for (int j = 0; j < D / 16; ++j)
-        *reinterpret_cast<float4*>(WTs + (n0 + wide_col(j)) * LC + m0) =
-            make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
+        for (int e = 0; e < 4; ++e) WTs[frag_col(n0, lane, nt, e) * LC + frag_row(m0, lane, e)] = acc[nt][e];
     }
     {  // U_hat = T V
-      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
-      float acc[4][E / 16];
-      zero(acc);
-      kgemm<4, E / 16, 64>(acc, TT, LC, m0, vS, LE, n0, kC);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < E / 16; ++j) rec[L.Uh() + (size_t)(m0 + i) * E + n0 + wide_col(j)] = acc[i][j];
+      using TE = WarpTiles<kC, E>;
+      const int warp = tid >> 5, lane = tid & 31;
+      int m0, n0;
+      TE::at(warp, m0, n0);
+      float acc[TE::NT][4] = {};
+      warp_mma<TE::NT>(acc, TT, LC, m0, vS, LE, n0, kC, lane);
+      frag_store<TE::NT>(rec + L.Uh(), E, acc, m0, n0, lane, 1.f);
     }
     __syncthreads();
     copy_out(rec + L.WT(), WTs, LC, D, tid);
@@ -497,9 +513,6 @@ struct FwdSmem {
   static constexpr int floats = D * LC + kC * LD + kC * LS + D + D * LS + kC * LS;
 };
 
-// the fragment element e of tile nt of a warp_mma accumulator: its row and column
-__device__ __forceinline__ int frag_row(int m0, int lane, int e) { return m0 + (lane >> 2) + 8 * (e >> 1); }
-__device__ __forceinline__ int frag_col(int n0, int lane, int nt, int e) { return n0 + 8 * nt + 2 * (lane & 3) + (e & 1); }
 
 template <int D, int E, int ES>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -788,31 +801,26 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
     __syncthreads();
     for (int i = tid; i < kC * E; i += kThreads) dUr[(i % kC) * LE + i / kC] = dUT[(i / kC) * LC + i % kC];
     __syncthreads();
+    using TD = WarpTiles<kC, D>;
+    using TE = WarpTiles<kC, E>;
+    using TC = WarpTiles<kC, kC>;
+    const int warp = tid >> 5, lane = tid & 31;
     {
-      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
-      float a1[4][D / 16], a2[4][D / 16];
-      zero(a1);
-      zero(a2);
-      kgemm<4, D / 16, 64>(a1, dOT, LC, m0, S0T, LD, n0, E);  // dO S0^T
-      kgemm<4, D / 16, 64>(a2, dUT, LC, m0, S0T, LD, n0, E);  // dU S0^T
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < D / 16; ++j) {
-          gr[GL.dQh() + (size_t)(m0 + i) * D + n0 + wide_col(j)] = a1[i][j];
-          gr[GL.dW() + (size_t)(m0 + i) * D + n0 + wide_col(j)] = -a2[i][j];
-        }
+      int m0, n0;
+      TD::at(warp, m0, n0);
+      float acc[TD::NT][4] = {};
+      warp_mma<TD::NT>(acc, dOT, LC, m0, S0T, LD, n0, E, lane);  // dO S0^T
+      frag_store<TD::NT>(gr + GL.dQh(), D, acc, m0, n0, lane, 1.f);
+      float acc2[TD::NT][4] = {};
+      warp_mma<TD::NT>(acc2, dUT, LC, m0, S0T, LD, n0, E, lane);  // dU S0^T
+      frag_store<TD::NT>(gr + GL.dW(), D, acc2, m0, n0, lane, -1.f);
     }
     {  // dv = T^T dU (rows of the sequence only)
-      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
-      float acc[4][E / 16];
-      zero(acc);
-      kgemm<4, E / 16, 64>(acc, TS, LC, m0, dUr, LE, n0, kC);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (m0 + i < n)
-#pragma unroll
-          for (int j = 0; j < E / 16; ++j) dv[((size_t)(t0 + m0 + i) * H + h) * E + n0 + wide_col(j)] = acc[i][j];
+      int m0, n0;
+      TE::at(warp, m0, n0);
+      float acc[TE::NT][4] = {};
+      warp_mma<TE::NT>(acc, TS, LC, m0, dUr, LE, n0, kC, lane);
+      frag_store<TE::NT>(dv + ((size_t)t0 * H + h) * E, (size_t)H * E, acc, m0, n0, lane, 1.f, n);
     }
     if (tid < D) {  // rowsum(dS_C (.) S0), dS_C^T from global
       float s0 = 0.f, s1 = 0.f;
@@ -829,30 +837,26 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
     stage_wait();
     __syncthreads();
     {
-      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
-      float a1[4][D / 16];
-      zero(a1);
-      kgemm<4, D / 16, 64>(a1, UT, LC, m0, S0T, LD, n0, E);  // U dS_C^T
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < D / 16; ++j) gr[GL.dKb() + (size_t)(m0 + i) * D + n0 + wide_col(j)] = a1[i][j];
+      int m0, n0;
+      TD::at(warp, m0, n0);
+      float acc[TD::NT][4] = {};
+      warp_mma<TD::NT>(acc, UT, LC, m0, S0T, LD, n0, E, lane);  // U dS_C^T
+      frag_store<TD::NT>(gr + GL.dKb(), D, acc, m0, n0, lane, 1.f);
     }
     {
-      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
-      float a1[4][4], a2[4][4];
-      zero(a1);
-      zero(a2);
-      kgemm<4, 4>(a1, dOT, LC, m0, UT, LC, n0, E);   // dO U^T
-      kgemm<4, 4>(a2, dUT, LC, m0, VT, LC, n0, E);   // dU V^T
+      int m0, n0;
+      TC::at(warp, m0, n0);
+      float acc[TC::NT][4] = {};
+      warp_mma<TC::NT>(acc, dOT, LC, m0, UT, LC, n0, E, lane);  // dO U^T, kept on M's support (s <= r)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int nt = 0; nt < TC::NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = m0 + i, s = n0 + j;
-          gr[GL.dM() + (size_t)r * kC + s] = r >= s ? a1[i][j] : 0.f;
-          gr[GL.dT1() + (size_t)r * kC + s] = a2[i][j];
-        }
+        for (int e = 0; e < 4; ++e)
+          if (frag_row(m0, lane, e) < frag_col(n0, lane, nt, e)) acc[nt][e] = 0.f;
+      frag_store<TC::NT>(gr + GL.dM(), kC, acc, m0, n0, lane, 1.f);
+      float acc2[TC::NT][4] = {};
+      warp_mma<TC::NT>(acc2, dUT, LC, m0, VT, LC, n0, E, lane);  // dU V^T
+      frag_store<TC::NT>(gr + GL.dT1(), kC, acc2, m0, n0, lane, 1.f);
     }
     __syncthreads();
   }
