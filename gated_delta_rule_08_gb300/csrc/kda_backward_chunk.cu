@@ -90,18 +90,20 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
 // separately (no MMA waits on the one before it in the same k step) and are added at the end.
 // Lane (g = lane / 4, t = lane % 4) holds acc[nt][0..1] at row m0 + g, columns n0 + 8 nt + 2t, +1,
 // and acc[nt][2..3] eight rows below.
-template <int NT>
+// With AT = false the left operand is given row-major instead (A[m * lda + k]).
+template <int NT, bool AT = true>
 __device__ __forceinline__ void warp_mma(float (&acc)[NT][4], const float* At, int lda, int m0, const float* B,
                                          int ldb, int n0, int K, int lane) {
   const int g = lane >> 2, t = lane & 3;
+  const auto a = [&](int m, int k) { return AT ? At[k * lda + m] : At[m * lda + k]; };
   float hl[NT][4] = {}, lh[NT][4] = {};
 #pragma unroll 4
   for (int k0 = 0; k0 < K; k0 += 8) {
     uint32_t ah[4], al[4];
-    split_tf32(At[(k0 + t) * lda + m0 + g], ah[0], al[0]);
-    split_tf32(At[(k0 + t) * lda + m0 + g + 8], ah[1], al[1]);
-    split_tf32(At[(k0 + t + 4) * lda + m0 + g], ah[2], al[2]);
-    split_tf32(At[(k0 + t + 4) * lda + m0 + g + 8], ah[3], al[3]);
+    split_tf32(a(m0 + g, k0 + t), ah[0], al[0]);
+    split_tf32(a(m0 + g + 8, k0 + t), ah[1], al[1]);
+    split_tf32(a(m0 + g, k0 + t + 4), ah[2], al[2]);
+    split_tf32(a(m0 + g + 8, k0 + t + 4), ah[3], al[3]);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       uint32_t bh0, bl0, bh1, bl1;
@@ -870,7 +872,7 @@ struct GradSmem {
   static constexpr int R1 = 3 * kC * LC;    // P, P^T, dA / dM^T (and dT, dX^T before them)
   static constexpr int R2a = 3 * 32 * LD, R2b = D * LC, R2c = 2 * kC * LC;
   static constexpr int R2 = R2a > R2b ? (R2a > R2c ? R2a : R2c) : (R2b > R2c ? R2b : R2c);
-  static constexpr int floats = base + R1 + R2 + kC;
+  static constexpr int floats = base + R1 + R2 + kC * LC + 2 * kC;  // + dM [C][LC], dbeta, beta
 };
 
 template <int D, int E, typename Tin>
@@ -889,8 +891,10 @@ bwd_grads(const Tin* __restrict__ q, const Tin* __restrict__ k, const float* __r
   float* s1 = s0 + kC * LC;
   float* s2 = s1 + kC * LC;
   float* r2 = s0 + SM::R1;   // R2
-  float* dbS = r2 + SM::R2;  // dbeta of the chunk's rows
-  const int tid = threadIdx.x;
+  float* dMs = r2 + SM::R2;  // dM [C][LC]
+  float* dbS = dMs + kC * LC;  // dbeta of the chunk's rows
+  float* bS = dbS + kC;        // beta of the chunk's rows
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const RecLayout L{D, E};
   const GradLayout GL{D};
   for (int64_t task = blockIdx.x; task < ntask; task += gridDim.x) {
@@ -914,7 +918,10 @@ bwd_grads(const Tin* __restrict__ q, const Tin* __restrict__ k, const float* __r
       }
     }
     load_kqg<D>(k, q, g, t0, n, H, h, kS, qS, gS, LD, tid);
-    if (tid < kC) dbS[tid] = 0.f;
+    if (tid < kC) {
+      dbS[tid] = 0.f;
+      bS[tid] = tid < n ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    }
     __syncthreads();
     if (tid < D) {
       float run = 0.f;
@@ -935,71 +942,69 @@ bwd_grads(const Tin* __restrict__ q, const Tin* __restrict__ k, const float* __r
     }
     __syncthreads();
     float* dTS = s0;
+    using TC = WarpTiles<kC, kC>;
     {
-      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
-      float acc[4][4];
-      zero(acc);
-      kgemm<4, 4>(acc, dWT, LC, m0, KhT, LC, n0, D);
+      int m0, n0;
+      TC::at(warp, m0, n0);
+      float acc[TC::NT][4] = {};
+      warp_mma<TC::NT>(acc, dWT, LC, m0, KhT, LC, n0, D, lane);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int nt = 0; nt < TC::NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          dTS[(m0 + i) * LC + n0 + j] = acc[i][j] + gr[GL.dT1() + (size_t)(m0 + i) * kC + n0 + j];
+        for (int e = 0; e < 4; ++e) {
+          const int r = frag_row(m0, lane, e), c = frag_col(n0, lane, nt, e);
+          dTS[r * LC + c] = acc[nt][e] + gr[GL.dT1() + (size_t)r * kC + c];
+        }
     }
     __syncthreads();
     // ---- T = X Diag(beta): dbeta_s += sum_r X_rs dT_rs; dX = dT Diag(beta) (stored transposed); X^T
     float* dXT = s1;
     float* XT = r2;           // [C][LC] (K_hat^T is no longer needed)
     float* YS = r2 + kC * LC;  // [C][LC]
-    if (tid < kC) {
-      const int s = tid;
-      const float bs = s < n ? beta[(size_t)(t0 + s) * H + h] : 0.f;
-      float acc = 0.f;
-      for (int r = 0; r < kC; ++r) {
-        const float dt = dTS[r * LC + s];
-        acc = fmaf(rec[L.X() + (size_t)r * kC + s], dt, acc);
-        dXT[s * LC + r] = dt * bs;
-      }
-      dbS[s] = acc;
-    }
     for (int i = tid; i < kC * kC; i += kThreads) {
       const int s = i / kC, j = i % kC;
       XT[j * LC + s] = rec[L.X() + i];
+      dXT[j * LC + s] = dTS[s * LC + j] * bS[j];
     }
     __syncthreads();
+    {  // four lanes per column s, lane p summing the rows r = p (mod 4)
+      const int s = tid >> 2, p = tid & 3;
+      float acc = 0.f;
+      for (int r = p; r < kC; r += 4) acc = fmaf(XT[s * LC + r], dTS[r * LC + s], acc);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      if (p == 0) dbS[s] = acc;
+    }
     // ---- dA = -X^T dX X^T on the strict lower triangle (Y = dX X^T first)
     {
-      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
-      float acc[4][4];
-      zero(acc);
-      kgemm<4, 4>(acc, dXT, LC, m0, XT, LC, n0, kC);
+      int m0, n0;
+      TC::at(warp, m0, n0);
+      float acc[TC::NT][4] = {};
+      warp_mma<TC::NT>(acc, dXT, LC, m0, XT, LC, n0, kC, lane);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int nt = 0; nt < TC::NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) YS[(m0 + i) * LC + n0 + j] = acc[i][j];
+        for (int e = 0; e < 4; ++e) YS[frag_row(m0, lane, e) * LC + frag_col(n0, lane, nt, e)] = acc[nt][e];
     }
     __syncthreads();
     float* PS = s0;   // P = Diag(beta) dA
     float* PT = s1;   // P^T
     float* dAS = s2;  // dA, then dM^T
     {
-      const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
-      float acc[4][4];
-      zero(acc);
-      kgemm<4, 4>(acc, rec + L.X(), kC, m0, YS, LC, n0, kC);
+      int m0, n0;
+      TC::at(warp, m0, n0);
+      float acc[TC::NT][4] = {};
+      warp_mma<TC::NT, false>(acc, XT, LC, m0, YS, LC, n0, kC, lane);  // X^T Y: XT read row-major
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = m0 + i;
-        const float br = r < n ? beta[(size_t)(t0 + r) * H + h] : 0.f;
+      for (int nt = 0; nt < TC::NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int s = n0 + j;
-          const float da = r > s ? -acc[i][j] : 0.f;
+        for (int e = 0; e < 4; ++e) {
+          const int r = frag_row(m0, lane, e), s = frag_col(n0, lane, nt, e);
+          const float da = r > s ? -acc[nt][e] : 0.f;
           dAS[r * LC + s] = da;
-          PS[r * LC + s] = br * da;
-          PT[s * LC + r] = br * da;
+          PS[r * LC + s] = bS[r] * da;
+          PT[s * LC + r] = bS[r] * da;
         }
-      }
     }
     __syncthreads();
     if (tid < kC) {  // dbeta_r += sum_s dA_rs A_tilde_rs
@@ -1012,22 +1017,22 @@ bwd_grads(const Tin* __restrict__ q, const Tin* __restrict__ k, const float* __r
     float* dMT = s2;
     for (int i = tid; i < kC * kC; i += kThreads) {
       const int r = i / kC, s = i % kC;
-      dMT[s * LC + r] = gr[GL.dM() + i];
+      const float x = gr[GL.dM() + i];
+      dMT[s * LC + r] = x;
+      dMs[r * LC + s] = x;
     }
     __syncthreads();
-    // ---- the A / M terms and the elementwise terms, one 32-row output half at a time; each thread
-    // owns a 4 x 4 tile of the half's dq, dk and dG
+    // ---- the A / M terms and the elementwise terms, one 32-row output half at a time; warp w owns
+    // 16-row tile w mod 2 and columns (w / 2) D/4.. of the half's dq, dk and dG (warp_mma fragments)
     float* Xk = r2;               // [32][LD] k e^{G - R} of the block's row half
     float* Xq = r2 + 32 * LD;     // [32][LD] q e^{G - R}
     float* Yk = r2 + 64 * LD;     // [32][LD] k e^{R - G} of the block's column half
-    constexpr int TILES = 8 * (D / 4);  // 4 x 4 tiles of a 32 x D half
-    const bool own = tid < TILES;
-    const int tm = own ? 4 * (tid / (D / 4)) : 0, tn = own ? 4 * (tid % (D / 4)) : 0;
+    using TH = WarpTiles<32, D>;
+    constexpr int NT = TH::NT;
+    int hm0, hn0;
+    TH::at(warp, hm0, hn0);
     for (int ho = 0; ho < 2; ++ho) {
-      float aq[4][4], ak[4][4], aG[4][4];
-      zero(aq);
-      zero(ak);
-      zero(aG);
+      float aq[NT][4] = {}, ak[NT][4] = {}, aG[NT][4] = {};
       for (int blk = 0; blk < 3; ++blk) {
         const int a = blk == 0 ? 0 : 1, bb = blk == 1 ? 1 : 0, ref = blk == 0 ? 15 : 47;
         const bool rows_side = a == ho, cols_side = bb == ho;
@@ -1041,80 +1046,73 @@ bwd_grads(const Tin* __restrict__ q, const Tin* __restrict__ k, const float* __r
           Yk[r * LD + c] = kS[(32 * bb + r) * LD + c] * __expf(R - gS[(32 * bb + r) * LD + c]);
         }
         __syncthreads();
-        if (own) {
-          if (rows_side) {  // rows r of half a: sum_s P_rs k_s e^{G_r - G_s}, sum_s dM_rs k_s e^{G_r - G_s}
-            float t1[4][4], t2[4][4];
-            zero(t1);
-            zero(t2);
-            kgemm<4, 4>(t1, PT + 32 * bb * LC, LC, 32 * a + tm, Yk, LD, tn, 32);
-            kgemm<4, 4>(t2, dMT + 32 * bb * LC, LC, 32 * a + tm, Yk, LD, tn, 32);
+        if (rows_side) {  // rows r of half a: sum_s P_rs k_s e^{G_r - G_s}, sum_s dM_rs k_s e^{G_r - G_s}
+          float t1[NT][4] = {}, t2[NT][4] = {};
+          warp_mma<NT>(t1, PT + 32 * bb * LC, LC, 32 * a + hm0, Yk, LD, hn0, 32, lane);
+          warp_mma<NT>(t2, dMT + 32 * bb * LC, LC, 32 * a + hm0, Yk, LD, hn0, 32, lane);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int r = 32 * a + tm + i, c = tn + j;
-                const float f = __expf(gS[r * LD + c] - gS[ref * LD + c]);
-                const float pa = f * t1[i][j], pm = f * t2[i][j];
-                ak[i][j] += pa;
-                aq[i][j] += pm;
-                aG[i][j] += kS[r * LD + c] * pa + qS[r * LD + c] * pm;
-              }
-          }
-          if (cols_side) {  // rows s of half bb: sum_r P_rs k_r e^{G_r - G_s}, sum_r dM_rs q_r e^{G_r - G_s}
-            float t3[4][4], t4[4][4];
-            zero(t3);
-            zero(t4);
-            kgemm<4, 4>(t3, PS + 32 * a * LC, LC, 32 * bb + tm, Xk, LD, tn, 32);
-            kgemm<4, 4>(t4, gr + GL.dM() + (size_t)32 * a * kC, kC, 32 * bb + tm, Xq, LD, tn, 32);
+            for (int e = 0; e < 4; ++e) {
+              const int r = 32 * a + frag_row(hm0, lane, e), c = frag_col(hn0, lane, nt, e);
+              const float f = __expf(gS[r * LD + c] - gS[ref * LD + c]);
+              const float pa = f * t1[nt][e], pm = f * t2[nt][e];
+              ak[nt][e] += pa;
+              aq[nt][e] += pm;
+              aG[nt][e] += kS[r * LD + c] * pa + qS[r * LD + c] * pm;
+            }
+        }
+        if (cols_side) {  // rows s of half bb: sum_r P_rs k_r e^{G_r - G_s}, sum_r dM_rs q_r e^{G_r - G_s}
+          float t3[NT][4] = {}, t4[NT][4] = {};
+          warp_mma<NT>(t3, PS + 32 * a * LC, LC, 32 * bb + hm0, Xk, LD, hn0, 32, lane);
+          warp_mma<NT>(t4, dMs + 32 * a * LC, LC, 32 * bb + hm0, Xq, LD, hn0, 32, lane);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int s = 32 * bb + tm + i, c = tn + j;
-                const float f = __expf(gS[ref * LD + c] - gS[s * LD + c]);
-                const float pa = f * t3[i][j], pm = f * t4[i][j];
-                ak[i][j] += pa + pm;
-                aG[i][j] -= kS[s * LD + c] * (pa + pm);
-              }
-          }
+            for (int e = 0; e < 4; ++e) {
+              const int s_ = 32 * bb + frag_row(hm0, lane, e), c = frag_col(hn0, lane, nt, e);
+              const float f = __expf(gS[ref * LD + c] - gS[s_ * LD + c]);
+              const float pa = f * t3[nt][e], pm = f * t4[nt][e];
+              ak[nt][e] += pa + pm;
+              aG[nt][e] -= kS[s_ * LD + c] * (pa + pm);
+            }
         }
         __syncthreads();
       }
-      if (own) {
-        // dK_hat = T^T dW, and the terms through Q_hat, K_hat and K_bar
-        float t5[4][4];
-        zero(t5);
-        kgemm<4, 4>(t5, rec + L.T(), kC, 32 * ho + tm, gr + GL.dW(), D, tn, kC);
+      // dK_hat = T^T dW (columns 32 ho.. of T and all of dW staged over the operand tiles), and the
+      // terms through Q_hat, K_hat and K_bar
+      constexpr int L36 = 32 + 4;
+      float* Tsl = r2;            // [C][36]: T[k][32 ho + m]
+      float* dWs = r2 + kC * L36;  // [C][LD]
+      static_assert(kC * L36 + kC * LD <= SM::R2, "T slab and dW fit over the operand tiles");
+      stage_async(Tsl, L36, rec + L.T() + 32 * ho, kC, kC, 32, tid);
+      stage_async(dWs, LD, gr + GL.dW(), D, kC, D, tid);
+      stage_wait();
+      __syncthreads();
+      {
+        float t5[NT][4] = {};
+        warp_mma<NT>(t5, Tsl, L36, hm0, dWs, LD, hn0, kC, lane);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 32 * ho + tm + i;
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int c = tn + j;
+          for (int e = 0; e < 4; ++e) {
+            const int r = 32 * ho + frag_row(hm0, lane, e), c = frag_col(hn0, lane, nt, e);
             const float G = gS[r * LD + c], Gc = gS[(kC - 1) * LD + c];
             const float gam = __expf(G), eb = __expf(Gc - G), kv = kS[r * LD + c], qv = qS[r * LD + c];
             const float dqh = gr[GL.dQh() + (size_t)r * D + c], dkb = gr[GL.dKb() + (size_t)r * D + c];
-            aq[i][j] += dqh * gam;
-            ak[i][j] += t5[i][j] * gam + dkb * eb;
-            aG[i][j] += dqh * qv * gam + t5[i][j] * kv * gam - dkb * kv * eb;
+            aq[nt][e] += dqh * gam;
+            ak[nt][e] += t5[nt][e] * gam + dkb * eb;
+            aG[nt][e] += dqh * qv * gam + t5[nt][e] * kv * gam - dkb * kv * eb;
           }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 32 * ho + tm + i;
-          if (r < n) {
-            const size_t o = ((size_t)(t0 + r) * H + h) * D + tn;
-            *reinterpret_cast<float4*>(dq + o) = make_float4(aq[i][0], aq[i][1], aq[i][2], aq[i][3]);
-            *reinterpret_cast<float4*>(dk + o) = make_float4(ak[i][0], ak[i][1], ak[i][2], ak[i][3]);
-          }
-        }
       }
-      __syncthreads();  // q rows of this half are no longer read: they receive its dG
-      if (own)
+      frag_store<NT>(dq + ((size_t)(t0 + 32 * ho) * H + h) * D, (size_t)H * D, aq, hm0, hn0, lane, 1.f, n - 32 * ho);
+      frag_store<NT>(dk + ((size_t)(t0 + 32 * ho) * H + h) * D, (size_t)H * D, ak, hm0, hn0, lane, 1.f, n - 32 * ho);
+      __syncthreads();  // q rows of this half and the staged tiles are no longer read
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) qS[(32 * ho + tm + i) * LD + tn + j] = aG[i][j];
+        for (int e = 0; e < 4; ++e)
+          qS[(32 * ho + frag_row(hm0, lane, e)) * LD + frag_col(hn0, lane, nt, e)] = aG[nt][e];
       __syncthreads();
     }
     // ---- dg: reverse cumulative sum of dG, with G_C's terms on the last row
