@@ -163,11 +163,12 @@ kda_status kda_decode_multi(const void* q, const void* k, const void* v, const f
 /* Backward of the prefill recurrence (no epilogue): the gradients of
  *   L = sum_t <dout_t, o_t> + <dhT, hT>
  * with respect to q, k, v, g, beta and h0 (section 2.2 Eq. 1, section 2.4 Eq. 3; section 5.1 names
- * a KDA training kernel), in fp32 on the CUDA cores.  Two paths give the same gradients within
- * rounding: the chunkwise reverse mode of the section 2.5 / Eq. 4 chunk form (per-chunk records,
- * serial state passes over chunks, per-chunk gradients; used while its scratch, about 0.6 MB per
- * (chunk, head) at dk = dv = 128, stays within 48 GB), else a reverse-time sweep over the tokens
- * with the state recomputed from per-chunk checkpoints.  The environment variable
+ * a KDA training kernel), to fp32 accuracy.  Two paths give the same gradients within rounding:
+ * the chunkwise reverse mode of the section 2.5 / Eq. 4 chunk form (per-chunk records, serial
+ * state passes over chunks, per-chunk gradients, its products as tensor-core MMAs with a
+ * three-term tf32 split; used while its scratch, about 0.6 MB per (chunk, head) at dk = dv = 128,
+ * stays within 48 GB), else an fp32 reverse-time sweep over the tokens with the state recomputed
+ * from per-chunk checkpoints.  The environment variable
  * KDA_BACKWARD_PATH=token or =chunked forces one of them; it is read at every call, including by
  * kda_chunk_bwd_workspace_size, so query the size under the same setting.
  *   q, k, v, g, beta, h0, cu_seqlens, B, T, H, dk, dv, dtype : as for kda_chunk_fwd
