@@ -94,7 +94,9 @@ def measured_traffic() -> dict:
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+    """Samples SM clocks and throttle reasons with nvidia-smi while the GPU works.  It is entered
+    before the warm-up steps and waits for nvidia-smi's first sample, so that the timed steps and
+    the traced pass after them are sampled in full (a few tens of milliseconds of GPU time)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -111,6 +113,15 @@ class ClockSampler:
                  "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
+            return self
+        import threading
+        self._lines = []
+        self._reader = threading.Thread(target=lambda: self._lines.extend(iter(self.proc.stdout.readline, "")),
+                                        daemon=True)
+        self._reader.start()
+        t_end = time.monotonic() + 5.0
+        while not self._lines and time.monotonic() < t_end and self.proc.poll() is None:
+            time.sleep(0.01)
         return self
 
     def __exit__(self, *exc):
@@ -118,11 +129,12 @@ class ClockSampler:
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+                self.proc.wait()
+            self._reader.join(timeout=5)
+            self.lines = [ln for ln in self._lines if ln.strip()]
 
     def summary(self):
         if not getattr(self, "lines", None):
@@ -143,7 +155,8 @@ class ClockSampler:
                     reasons.add(nm)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "window": "warm-up steps, timed steps and the traced pass"}
 
 
 def _dist():
@@ -201,6 +214,7 @@ def run_ours(args, world, rank, local):
         binding.kda_decode_step(D["q"], D["k"], D["v"], D["g"], D["beta"], D["state_pool"], D["slot_idx"], out=dout,
                                 gate=D["gate"], norm_weight=D["norm_weight"])
 
+    clocks = ClockSampler(local).__enter__()  # sampling from the warm-up through the traced pass
     for _ in range(args.warmup):
         prefill()
         decode()
@@ -224,11 +238,10 @@ def run_ours(args, world, rank, local):
     # start while their predecessor drains)
     _barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        t_wall = time.perf_counter()
-        ev = timed_steps()
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
+    t_wall = time.perf_counter()
+    ev = timed_steps()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
     _barrier(world)
     # the same K steps again with every kernel bracketed by CUDA events on its stream: per-kernel
     # durations for the roofline (the events cost the overlap above, so this pass is not the value)
@@ -239,6 +252,7 @@ def run_ours(args, world, rank, local):
     _barrier(world)
     trace = binding.kda_trace_collect()
     binding.kda_trace_enable(False)
+    clocks.__exit__(None, None, None)
     pre_ms = [a.elapsed_time(b) for a, b, _ in ev]
     dec_ms = [b.elapsed_time(c) for _, b, c in ev]
     pre_s = dist_max(sum(pre_ms) / 1e3, world)

@@ -749,11 +749,12 @@ int prefill_tc_cp_segments(int B, int64_t T, int H) {
   const int64_t maxc = (T + kChunk - 1) / kChunk;
   const int64_t chains = (int64_t)B * H;
   // Worth it only when the chains leave at least half of the SMs idle and the sequences span
-  // several minimum-size segments.  Each extra segment costs two transition runs (P and b) of
-  // segment length; for moderate lengths keep them to one wave of CTAs, for very long sequences
-  // a second wave is repaid by the shorter read-out pass.
+  // several minimum-size segments.  n segments cost 2 n - 3 transition runs of segment length per
+  // chain (one run of segment 0 from h0, then P and b of every later segment but the last); for
+  // moderate lengths keep them to one wave of CTAs, for very long sequences a second wave is
+  // repaid by the shorter read-out pass.
   if (maxc < kCpMinChunks || chains * 2 > sms) return 1;
-  int64_t n = maxc >= kCpLongChunks ? sms / chains : 1 + sms / (2 * chains);
+  int64_t n = maxc >= kCpLongChunks ? sms / chains : (sms / chains + 3) / 2;
   if (n > maxc / kCpMinSegChunks) n = maxc / kCpMinSegChunks;
   return n < 1 ? 1 : (int)n;
 }

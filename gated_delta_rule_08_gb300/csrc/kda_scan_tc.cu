@@ -10,8 +10,10 @@
 // so a segment of chunks maps S_in to S_out = P S_in + b with
 //   b = the segment's final state from S_in = 0,
 //   P = the segment's final state from S_in = I with U_hat = 0 (a dk x dk state);
-// both are ordinary runs of the same state pass.  The merge then walks the segments,
-// S_in(p+1) = P_p S_in(p) + b_p, and a last pass re-runs every segment from its S_in with outputs.
+// both are ordinary runs of the same state pass.  The first segment's input is known (h0), so it
+// needs neither: one run from h0 gives S_in(1) itself.  The merge then walks the remaining
+// segments, S_in(p+1) = P_p S_in(p) + b_p for p >= 1, and a last pass re-runs every segment from
+// its S_in with outputs.
 //
 //  kda_tc_chunk_scan<Tout, MODE> (grid = sequences x heads x segments, 13 warps):
 //    the state^T (dv x dk, fp32) lives in TMEM for the whole segment, next to an fp16 copy that
@@ -26,7 +28,8 @@
 //    MODE 0 (read-out): warps 8-11 drain D_O off the serial path: a full chunk without the
 //      epilogue straight from registers (each store writes 32 consecutive dv of a token), else
 //      through a staging buffer with the optional RMSNorm + gate epilogue;
-//    MODE 1 (transition): z = 2 p + kind; kind 0 runs b_p, kind 1 runs P_p; no read-out.
+//    MODE 1 (transition): z = 0 runs segment 0 from h0 (its final state is S_in(1)); for p >= 1,
+//      z = 2 p - 1 + kind, kind 0 runs b_p and kind 1 runs P_p; no read-out.
 //  kda_cp_merge (grid = sequences x heads x 4 column slices): the sequential segment merge in fp32.
 #include <cuda_bf16.h>
 
@@ -124,17 +127,26 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
   griddep_launch_dependents();
-  if (p.cu != nullptr && p.plan[p.B + 1] == 0) return;  // invalid cu_seqlens: sequence skipped
+  // A CTA that has nothing to do still waits for the predecessor grid before it exits, so that
+  // no grid of the chain completes before the one it follows (a successor's griddep_wait covers
+  // only its immediate predecessor).
+  if (p.cu != nullptr && p.plan[p.B + 1] == 0) {  // invalid cu_seqlens: sequence skipped
+    griddep_wait();
+    return;
+  }
   // blockIdx.x = rank x H + head: all heads of the longest sequence are dispatched first
   const int h = (int)(blockIdx.x % (unsigned)H);
   const int b = sequence_of_rank((int)(blockIdx.x / (unsigned)H), p.plan, p.cu, p.B);
   int64_t first_chunk, t_begin, len;
   const int64_t nchunks = sequence_chunks(b, p.plan, p.cu, p.B, p.T, first_chunk, t_begin, len);
   const int64_t p_last = nchunks > 0 ? (nchunks - 1) / p.seg_len : 0;
-  const int seg = MODE == 0 ? (int)blockIdx.z : (int)(blockIdx.z >> 1);
-  const int kind = MODE == 0 ? 0 : (int)(blockIdx.z & 1);  // MODE 1: 0 = offset b, 1 = transition P
-  if (MODE == 0 && seg > p_last) return;
-  if (MODE == 1 && seg >= p_last) return;
+  // MODE 1: kind 0 = offset b (from h0 for segment 0), 1 = transition P
+  const int seg = MODE == 0 || blockIdx.z == 0 ? (int)blockIdx.z : (int)((blockIdx.z + 1) >> 1);
+  const int kind = MODE == 0 || blockIdx.z == 0 ? 0 : (int)((blockIdx.z + 1) & 1);
+  if ((MODE == 0 && seg > p_last) || (MODE == 1 && seg >= p_last)) {
+    griddep_wait();
+    return;
+  }
   const int64_t c_begin = (int64_t)seg * p.seg_len;
   const int64_t c_end = nchunks < c_begin + p.seg_len ? nchunks : c_begin + p.seg_len;
   const int64_t ncs = c_end > c_begin ? c_end - c_begin : 0;
@@ -240,13 +252,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
     int64_t ck_next = CKPT ? (c_begin / p.ckpt_chunks + 1) * p.ckpt_chunks : 0;  // next boundary (chunks done)
     bool ok = true;
     {
+      // segment 0 starts from h0 in both modes; the read-out of a later segment from S_in(seg)
+      const bool from_state = MODE == 0 || seg == 0;
       const float* init = nullptr;
-      if (MODE == 0) init = seg == 0 ? (p.h0 ? p.h0 + soff : nullptr) : cpb + 2 * kCpMat;
+      if (from_state) init = seg == 0 ? (p.h0 ? p.h0 + soff : nullptr) : cpb + 2 * kCpMat;
       float s[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const int col = 64 * hc + c;
-        if (MODE == 0) s[c] = init ? init[(size_t)col * 128 + row] : 0.f;
+        if (from_state) s[c] = init ? init[(size_t)col * 128 + row] : 0.f;
         else s[c] = (kind == 1 && col == row) ? 1.f : 0.f;
       }
       tmem_st64h(tl + T_S16 + 32 * hc, s);
@@ -348,7 +362,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
     // final state of this (sequence, head, segment)
     float* dst = nullptr;
     if (MODE == 0 && seg == p_last) dst = p.hT ? p.hT + soff : nullptr;
-    if (MODE == 1) dst = cpb + (kind == 1 ? 0 : kCpMat);
+    if (MODE == 1) dst = seg == 0 ? cpb + (3 + 2) * kCpMat : cpb + (kind == 1 ? 0 : kCpMat);  // S_in(1), or P_p / b_p
     if (ok && !*abort_flag && dst != nullptr) {
       tc_fence_after();
       float s[64];
@@ -428,8 +442,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// Segment merge: S_in(p+1) = P_p S_in(p) + b_p for p < p_last, fp32, on a 32-column slice of the
-// state per CTA.  P_p (64 KB) is staged into shared memory by bulk copies one step ahead; warp w
+// Segment merge: S_in(p+1) = P_p S_in(p) + b_p for 1 <= p < p_last (S_in(1) comes from the
+// transitions), fp32, on a 32-column slice of the state per CTA.  P_p (64 KB) is staged into shared memory by bulk copies one step ahead; warp w
 // computes rows 16 w .. 16 w + 15 of the slice, lane = column, so P is read as broadcast float4s
 // and the state slice column-wise without bank conflicts.
 constexpr int kMergeThreads = 256;
@@ -443,39 +457,48 @@ __global__ void __launch_bounds__(kMergeThreads, 1) kda_cp_merge(const ScanParam
   const int b = blockIdx.x, h = blockIdx.y, j0 = kMergeCols * blockIdx.z, tid = threadIdx.x;
   const int lane = tid & 31, rg = tid >> 5;
   griddep_launch_dependents();
+  griddep_wait();  // the transitions' P, b and S_in(1); every CTA waits (see the state pass)
   if (p.cu != nullptr && p.plan[p.B + 1] == 0) return;
   int64_t first_chunk, t_begin, len;
   const int64_t nchunks = sequence_chunks(b, p.plan, p.cu, p.B, p.T, first_chunk, t_begin, len);
   const int64_t p_last = nchunks > 0 ? (nchunks - 1) / p.seg_len : 0;
-  if (p_last == 0) return;
-  const size_t soff = ((size_t)b * p.H + h) * kCpMat;
+  const int64_t nsteps = p_last - 1;  // step i composes segment i + 1
+  if (nsteps <= 0) return;
   float* cp = p.cp + (size_t)(b * p.H + h) * p.nseg * 3 * kCpMat;
   int64_t issued = 0;
-  griddep_wait();  // the transitions' P and b
   if (tid == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
     mbar_fence_init();
-    for (; issued < 2 && issued < p_last; ++issued) {
+    for (; issued < 2 && issued < nsteps; ++issued) {
       mbar_arrive_expect_tx(&bar[issued], 65536);
-      bulk_g2s(sP + issued * 16384, cp + (size_t)issued * 3 * kCpMat, 65536, &bar[issued]);
+      bulk_g2s(sP + issued * 16384, cp + (size_t)(issued + 1) * 3 * kCpMat, 65536, &bar[issued]);
     }
   }
-  for (int i = tid; i < 128 * kMergeCols; i += kMergeThreads) {
-    const int r = i / kMergeCols, c = i % kMergeCols;
-    sS[i] = p.h0 ? p.h0[soff + (size_t)r * 128 + j0 + c] : 0.f;
+  // S_in(1) slice and the first b slice: all loads in flight before any is used
+  constexpr int kPer = 128 * kMergeCols / kMergeThreads;
+  {
+    const float* sin1 = cp + (size_t)(3 + 2) * kCpMat;
+    float x[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + i * kMergeThreads;
+      x[i] = sin1[(size_t)(e / kMergeCols) * 128 + j0 + e % kMergeCols];
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) sS[tid + i * kMergeThreads] = x[i];
   }
+  float acc[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j] = cp[(size_t)(3 + 1) * kCpMat + (size_t)(rg * 16 + j) * 128 + j0 + lane];
   __syncthreads();
   bool ok = true;
-  for (int64_t s = 0; s < p_last; ++s) {
-    const int buf = (int)(s & 1);
-    ok = __syncthreads_and(mbar_wait(&bar[buf], (uint32_t)((s >> 1) & 1))) != 0;
+  for (int64_t step = 0; step < nsteps; ++step) {
+    const int64_t s = step + 1;
+    const int buf = (int)(step & 1);
+    ok = __syncthreads_and(mbar_wait(&bar[buf], (uint32_t)((step >> 1) & 1))) != 0;
     if (!ok) break;
     const float* P = sP + buf * 16384 + (rg * 16) * 128;
-    const float* bo = cp + (size_t)s * 3 * kCpMat + kCpMat;
-    float acc[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = bo[(size_t)(rg * 16 + j) * 128 + j0 + lane];
 #pragma unroll 2
     for (int k = 0; k < 128; k += 4) {
       const float s0 = sS[k * kMergeCols + lane], s1 = sS[(k + 1) * kMergeCols + lane];
@@ -488,9 +511,9 @@ __global__ void __launch_bounds__(kMergeThreads, 1) kda_cp_merge(const ScanParam
     }
     fence_proxy_async_smem();  // reads of this P buffer precede the next bulk copy into it
     __syncthreads();
-    if (tid == 0 && issued < p_last) {
+    if (tid == 0 && issued < nsteps) {
       mbar_arrive_expect_tx(&bar[buf], 65536);
-      bulk_g2s(sP + buf * 16384, cp + (size_t)issued * 3 * kCpMat, 65536, &bar[buf]);
+      bulk_g2s(sP + buf * 16384, cp + (size_t)(issued + 1) * 3 * kCpMat, 65536, &bar[buf]);
       ++issued;
     }
     float* sin_next = cp + ((size_t)(s + 1) * 3 + 2) * kCpMat;
@@ -499,6 +522,11 @@ __global__ void __launch_bounds__(kMergeThreads, 1) kda_cp_merge(const ScanParam
       const int r = rg * 16 + j;
       sS[r * kMergeCols + lane] = acc[j];
       sin_next[(size_t)r * 128 + j0 + lane] = acc[j];
+    }
+    if (step + 1 < nsteps) {  // the next step's b slice
+      const float* bo = cp + ((size_t)(s + 1) * 3 + 1) * kCpMat;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = bo[(size_t)(rg * 16 + j) * 128 + j0 + lane];
     }
     __syncthreads();
   }
@@ -553,13 +581,14 @@ cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int3
   p.ckpt = a.ckpt; p.ckpt_chunks = a.ckpt_chunks;
   if (nseg > 1) {
     {
+      // segment 0 from h0, then b_p and P_p for 1 <= p <= nseg - 2
       TraceScope ts("kda_tc_chunk_scan_transition", st);
       cudaError_t e = launch_after(kda_tc_chunk_scan<Tout, 1, false>,
-                                   dim3((unsigned)(a.B * a.H), 1, (unsigned)(2 * (nseg - 1))), kScanThreads,
+                                   dim3((unsigned)(a.B * a.H), 1, (unsigned)(2 * nseg - 3)), kScanThreads,
                                    kScanSmem, st, p);
       if (e != cudaSuccess) return e;
     }
-    {
+    if (nseg > 2) {
       TraceScope ts("kda_cp_merge", st);
       cudaError_t e = launch_after(kda_cp_merge, dim3((unsigned)a.B, (unsigned)a.H, 128 / kMergeCols), kMergeThreads,
                                    kMergeSmem, st, p);

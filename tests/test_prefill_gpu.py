@@ -226,13 +226,21 @@ def test_strong_decay_inside_chunk_with_weak_decay_across_the_half_boundary(dtyp
     assert rel_err(out, ref_out) <= tol and rel_err(hT, ref_hT) <= tol
 
 
-@pytest.mark.parametrize("lengths,H,epilogue,z_mean", [((16384,), 4, False, 0.0), ((20000, 300), 2, True, 0.0),
-                                                      ((8192,), 4, False, -8.0)])
+@pytest.mark.parametrize("lengths,H,epilogue,z_mean", [
+    ((16384,), 4, False, 0.0),
+    ((20000, 300), 2, True, 0.0),
+    ((8192,), 4, False, -8.0),
+    ((6400,), 64, False, -8.0),             # two segments: the run of segment 0 from h0 is S_in(1), no merge
+    ((4096, 4096), 16, False, -8.0),        # three segments planned, every sequence ends in segment 1
+    ((2730, 2730, 2730), 16, False, -8.0),  # two segments planned, every sequence fits in segment 0
+])
 def test_sequence_split_across_sms_matches_oracle(lengths, H, epilogue, z_mean):
     """Few (sequence, head) chains with long sequences: the state pass is split into segments
     whose transitions are merged (intra-device context parallelism); results must not change.
     z_mean = -8 gives g close to 0 (decay ~e^-0.002 per token), so each segment's initial state,
-    recovered by the merge, still shapes the segment's outputs and final state."""
+    recovered by the merge, still shapes the segment's outputs and final state.  The segment
+    counts in the comments are those of a 152-SM GPU; the last two cases leave every merge CTA,
+    and in the last case every transition CTA, with nothing to do."""
     cfg = inputs.PrefillConfig("cp", H=H, dk=128, dv=128, dtype="bf16", lengths=lengths, B=len(lengths),
                                h0_std=0.1, epilogue=epilogue, z_mean=z_mean, seed=309)
     _check(cfg, epilogue=epilogue, device_gen=True)
