@@ -10,9 +10,9 @@
 // Section 3.2 / Eq. 5 (g > -5) bounds every reference-scaled factor used below by e^{+-80}.
 //
 //  kda_tc_chunk_prep (persistent, two CTAs per SM, each looping over (chunk, head) tasks)
-//    warp 8 stages the raw q, k, v tiles by TMA (128-byte swizzle; q of the next task as soon as
-//      the current one has been read, k and v once its last MMAs are done) and beta by plain
-//      loads, and issues every MMA;
+//    warp 8 stages the raw q, k, v tiles by TMA (128-byte swizzle; the next task's tiles once the
+//      current task's last MMAs have read k and v, which the passes overwrite in place) and beta by
+//      plain loads, and issues every MMA;
 //    warps 0-7, per task:
 //    - four 32-channel passes; thread = (channel pair, 4 rows): the cumulative log-decay is a
 //      running sum over the thread's rows plus the sums of the row groups above it (exchanged in
@@ -87,10 +87,12 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
 // ---- warp-level tf32 MMA (mma.sync m16n8k8) for the 16 x 16 blocks of the triangular solve.
 // Fragments: A (16 x 8) a0 (g, t), a1 (g+8, t), a2 (g, t+4), a3 (g+8, t+4); B (8 x 8, k x n) b0 (t, g),
 // b1 (t+4, g); C (16 x 8) c0 (g, 2t), c1 (g, 2t+1), c2 (g+8, 2t), c3 (g+8, 2t+1); g = lane / 4, t = lane % 4.
-__device__ __forceinline__ uint32_t tf32_bits(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
+// x = hi + lo with hi = x with its low 13 mantissa bits cleared (exact in tf32) and lo = x - hi
+// (exact in fp32); the MMA reads lo's top 19 bits, so lo carries about 10 more significant bits
+// and hi*hi + hi*lo + lo*hi is ~2^-20 relative, with fp32 range.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = __float_as_uint(x) & 0xFFFFE000u;
+  lo = __float_as_uint(x - __uint_as_float(hi));
 }
 __device__ __forceinline__ void mma_tf32_m16n8k8(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -132,14 +134,11 @@ __device__ __forceinline__ void warp_gemm16x8_acc(float (&acc)[3][4], const L1& 
     const int ca = c1 + 8 * ks + t, rb = r2 + 8 * ks + t;
     const float af[4] = {m1(r1 + g, ca), m1(r1 + g + 8, ca), m1(r1 + g, ca + 4), m1(r1 + g + 8, ca + 4)};
     const float b0 = m2(rb, c2 + g), b1 = m2(rb + 4, c2 + g);
-    uint32_t ah[4], al[4];
+    uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      ah[i] = tf32_bits(af[i]);
-      al[i] = tf32_bits(af[i] - __uint_as_float(ah[i]));
-    }
-    const uint32_t bh0 = tf32_bits(b0), bh1 = tf32_bits(b1);
-    const uint32_t bl0 = tf32_bits(b0 - __uint_as_float(bh0)), bl1 = tf32_bits(b1 - __uint_as_float(bh1));
+    for (int i = 0; i < 4; ++i) split_tf32(af[i], ah[i], al[i]);
+    split_tf32(b0, bh0, bl0);
+    split_tf32(b1, bh1, bl1);
     mma_tf32_m16n8k8(acc[0], ah, bh0, bh1);
     mma_tf32_m16n8k8(acc[1], ah, bl0, bl1);
     mma_tf32_m16n8k8(acc[2], al, bh0, bh1);
@@ -162,13 +161,31 @@ struct PrepMaps {
   CUtensorMap k, q, v;
 };
 
-// Next valid task index >= t (tasks: chunk-major, head-minor), or -1.
+// Next valid task index >= t (tasks: chunk-major, head-minor), or -1.  Task and chunk indices and
+// sequence lengths below 2^31 (every practical problem) take 32-bit divisions.
 __device__ __forceinline__ int64_t next_task(int64_t t, int64_t ntask, int64_t stride, const int32_t* plan,
                                              const int32_t* cu, int B, int64_t T, int H, int& h, int64_t& t0,
                                              int& n, int64_t& chunk) {
+  const bool narrow = ntask < (int64_t(1) << 31) && T < (int64_t(1) << 31);
   for (; t < ntask; t += stride) {
-    chunk = t / H;
-    h = (int)(t - chunk * H);
+    if (narrow) {
+      const uint32_t c32 = (uint32_t)t / (uint32_t)H;
+      chunk = c32;
+      h = (int)((uint32_t)t - c32 * (uint32_t)H);
+      if (cu == nullptr) {
+        const uint32_t nc = (uint32_t)((T + 63) / 64);
+        if (nc == 0) continue;
+        const uint32_t b = c32 / nc, cs = c32 - b * nc;
+        if ((int)b >= B) continue;
+        t0 = (int64_t)b * T + (int64_t)cs * 64;
+        const int64_t rem = T - (int64_t)cs * 64;
+        n = (int)(rem < 64 ? rem : 64);
+        return t;
+      }
+    } else {
+      chunk = t / H;
+      h = (int)(t - chunk * H);
+    }
     int b;
     int64_t cseq;
     if (resolve_chunk(chunk, plan, cu, B, T, b, t0, n, cseq)) return t;
@@ -360,6 +377,17 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
       // every break decision of the compute warps is made together (named barriers follow)
       ok = group_and(1, kCompute, wait_or_abort(full, it & 1, abort_flag));
       if (!ok) break;
+      if (n < 64) {
+        // a tail chunk: rows n..63 of the raw tiles (the next sequence's tokens, or the tensor's
+        // zero fill) become zeros once, so that the passes need no per-row test
+        const int nz = (64 - n) * 6 * 8;  // 16-byte pieces: rows x (k, q, v) x (two blocks) x 8
+        for (int i = tid; i < nz; i += kCompute) {
+          const int piece = i & 7, tile = (i >> 3) % 6, r = n + (i >> 3) / 6;
+          *reinterpret_cast<uint4*>(raw + (uint32_t)tile * 8192u + (uint32_t)r * 128u + (uint32_t)piece * 16u) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        group_sync(1, kCompute);
+      }
 
       // ---- four 32-channel passes
 #pragma unroll 1
@@ -410,19 +438,13 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = 4 * rg + i;
-          const bool valid = r < n;
           const float G0 = off.x + L[i].x, G1 = off.y + L[i].y;
           const uint32_t ob = (uint32_t)r * 128u + ((((kbyte >> 4) ^ (uint32_t)r) & 7u) << 4) + (kbyte & 15u);
           const uint32_t toff = (uint32_t)(c >> 6) * 8192u + ob;
           uint32_t* pk = reinterpret_cast<uint32_t*>(raw + R_K + toff);
           uint32_t* pq = reinterpret_cast<uint32_t*>(raw + R_Q + toff);
           uint32_t* pv = reinterpret_cast<uint32_t*>(raw + R_V + toff);
-          float2 k2 = unpack_bf2(*pk), q2 = unpack_bf2(*pq), v2 = unpack_bf2(*pv);
-          if (!valid) {
-            k2 = make_float2(0.f, 0.f);
-            q2 = k2;
-            v2 = k2;
-          }
+          const float2 k2 = unpack_bf2(*pk), q2 = unpack_bf2(*pq), v2 = unpack_bf2(*pv);
           const float e10 = ex2(G0 - R.x), e11 = ex2(G1 - R.y);
           const float e20 = ex2(R.x - G0), e21 = ex2(R.y - G1);
           uint32_t hi, lo;
