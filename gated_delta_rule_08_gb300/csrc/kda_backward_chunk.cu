@@ -1,4 +1,5 @@
-// KDA backward, chunkwise (fp32 CUDA cores): gradients of L = sum_t <dout_t, o_t> + <dhT, hT> with
+// KDA backward, chunkwise (products on the tensor cores as three-term tf32 warp MMAs, everything else
+// in fp32): gradients of L = sum_t <dout_t, o_t> + <dhT, hT> with
 // respect to q, k, v, g, beta and h0, for the prefill recurrence without epilogue.
 //
 // Kimi K3: Open Frontier Intelligence (kimi-k3-paper.pages.dev), section 2.5 / Eq. 4 gives the
@@ -16,7 +17,7 @@
 //   and the A / M terms reach dq, dk and dG through e^{G_r - G_s} with the same reference points as
 //   the forward; dg is the reverse cumulative sum of dG over the chunk.
 //
-// Kernels (all fp32):
+// Kernels (fp32 data; the products by warp_mma below):
 //   bwd_rec    per (chunk, head): the chunk's records (T, X, A_tilde, M, W, W^T, U_hat, K_bar,
 //              K_bar^T, Q_hat, e^{G_C});
 //   bwd_fwd    per (sequence, head, value-column slice), serial over chunks: S0 and U per chunk;
