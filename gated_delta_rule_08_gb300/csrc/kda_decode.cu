@@ -80,7 +80,7 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   __shared__ float4 part_a[NG][TPR], part_b[NG][TPR];
   __shared__ float sdelta[DV], so[NST][DV];
   __shared__ float red[kDecodeThreads / 32];
-  __shared__ float s_kq;
+  __shared__ float s_kq, s_kq_st[NST];
 
   for (int t = 0; t < count; ++t) {
     const int u = t % NST;
@@ -115,10 +115,18 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       }
       if (tid < nst) sbeta[tid] = beta[row + (size_t)tid * H];
       __syncthreads();
+      // k . q of every staged token, one warp each, read after the token's first barrier
+      if (tid < 32 * nst) {
+        const int w = tid >> 5;
+        float acc = 0.f;
+        for (int i = tid & 31; i < DK; i += 32) acc = fmaf(sk[w][i], sq[w][i], acc);
+        acc = warp_sum(acc);
+        if ((tid & 31) == 0) s_kq_st[w] = acc;
+      }
     }
     if constexpr (NST > 1) b_r = sbeta[u];
 
-    if (tid < 32) {  // k . q
+    if (NST == 1 && tid < 32) {  // k . q
       float acc = 0.f;
       for (int i = tid; i < DK; i += 32) acc = fmaf(sk[u][i], sq[u][i], acc);
       acc = warp_sum(acc);
@@ -148,7 +156,7 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       }
       const float d = b_r * (sv[u][tid] - a);
       sdelta[tid] = d;
-      so[u][tid] = fmaf(s_kq, d, b);
+      so[u][tid] = fmaf(NST == 1 ? s_kq : s_kq_st[u], d, b);
     }
     __syncthreads();
 

@@ -183,3 +183,55 @@ def test_decode_multi_bad_count_sets_flag_and_skips_request():
     assert torch.equal(inp["state_pool"][slots[1]], before[slots[1]])
     assert torch.equal(inp["state_pool"][slots[2]], before[slots[2]])
     assert not torch.equal(inp["state_pool"][slots[0]], before[slots[0]])
+
+
+def test_decode_multi_many_items_per_cta():
+    """More (request, head) items than the persistent multi-token grid has CTAs, so each CTA runs
+    several items and copies the next one's state while it computes: verify (no write-back) and
+    accept with per-request counts from 0 to 4 against the oracle."""
+    cfg = dataclasses.replace(inputs.DECODE, N=160, H=8, num_slots=400, seed=99)
+    inp = _multi(cfg, 4)
+    before = inp["state_pool"].clone()
+    kw = dict(gate=inp["gate"], norm_weight=inp["norm_weight"])
+    verify = binding.kda_decode_multi(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state_pool"],
+                                      inp["slot_idx"], commit=False, **kw)
+    assert_no_device_error()
+    assert torch.equal(inp["state_pool"], before)
+    ref_out, _ = _oracle_multi(inp, [4] * cfg.N, True, before)
+    assert parity_err(verify, ref_out) <= TOL[torch.bfloat16]
+    accept = [(7 * n) % 5 for n in range(cfg.N)]  # 0..4, every value many times
+    counts = torch.tensor(accept, dtype=torch.int32, device="cuda")
+    out = torch.full_like(verify, 5.0)
+    binding.kda_decode_multi(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state_pool"], inp["slot_idx"],
+                             counts, out=out, commit=True, **kw)
+    assert_no_device_error()
+    for n, a in enumerate(accept):
+        assert torch.equal(out[n, :a], verify[n, :a])
+        assert torch.all(out[n, a:] == 5.0)
+    _, ref_states = _oracle_multi(inp, accept, True, before)
+    slots = inp["slot_idx"].long()
+    assert rel_err(inp["state_pool"][slots], ref_states) <= 1e-5
+    untouched = torch.ones(cfg.num_slots, dtype=torch.bool, device="cuda")
+    untouched[slots] = False
+    assert torch.equal(inp["state_pool"][untouched], before[untouched])
+
+
+def test_decode_multi_bad_slot_among_many_items():
+    """A request with an out-of-range slot is skipped by the persistent multi-token grid (flag
+    set, its outputs untouched) and every other request is still served."""
+    cfg = dataclasses.replace(inputs.DECODE, N=100, H=8, num_slots=300, seed=101)
+    inp = _multi(cfg, 3)
+    good = inp["slot_idx"].clone()
+    ref = binding.kda_decode_multi(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state_pool"], good,
+                                   commit=False)
+    assert_no_device_error()
+    bad = good.clone()
+    bad[37] = cfg.num_slots + 5
+    out = torch.full_like(ref, 3.0)
+    binding.kda_decode_multi(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state_pool"], bad, out=out,
+                             commit=False)
+    assert binding.kda_get_device_error() & binding.DEVERR_BAD_SLOT
+    assert torch.all(out[37] == 3.0)
+    keep = torch.ones(cfg.N, dtype=torch.bool, device="cuda")
+    keep[37] = False
+    assert torch.equal(out[keep], ref[keep])
