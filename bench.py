@@ -61,18 +61,24 @@ def _peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-# the files that define the profiled kernels and their launch shapes; the host API, the other
-# paths and the backward do not change what these kernels move
-TRAFFIC_SOURCES = ("kda_prefill_tc.cu", "kda_scan_tc.cu", "kda_decode.cu", "kda_tc_common.cuh",
-                   "tc_ptx.cuh", "kda_device.cuh")
+# the files that define each profiled kernel and its launch shape; a kernel's recorded traffic
+# stands only while these hash to the digest recorded with it
+_TC_HEADERS = ("kda_tc_common.cuh", "tc_ptx.cuh", "kda_device.cuh", "kda_internal.h")
+KERNEL_SOURCES = {
+    "kda_tc_chunk_prep": ("kda_prefill_tc.cu",) + _TC_HEADERS,
+    "kda_tc_chunk_scan_transition": ("kda_scan_tc.cu",) + _TC_HEADERS,
+    "kda_cp_merge": ("kda_scan_tc.cu",) + _TC_HEADERS,
+    "kda_tc_chunk_scan": ("kda_scan_tc.cu",) + _TC_HEADERS,
+    "kda_decode": ("kda_decode.cu", "kda_device.cuh", "kda_internal.h"),
+}
 
 
-def source_digest() -> str:
-    """sha256 over the sources of the profiled kernels (names and contents, in a fixed order)."""
+def source_digest(names) -> str:
+    """sha256 over the named sources (names and contents, in the given order)."""
     import hashlib
     d = os.path.join(ROOT, "gated_delta_rule_08_gb300", "csrc")
     hsh = hashlib.sha256()
-    for name in TRAFFIC_SOURCES:
+    for name in names:
         hsh.update(name.encode())
         with open(os.path.join(d, name), "rb") as f:
             hsh.update(f.read())
@@ -81,16 +87,18 @@ def source_digest() -> str:
 
 def measured_traffic() -> dict:
     """Per-kernel DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
-    committed ncu capture, or {} when the kernel sources changed since it was taken."""
+    committed ncu capture, for the kernels whose sources are unchanged since it was taken."""
     path = os.path.join(ROOT, "profiles", "kda_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return {}
-    if rec.get("source_sha256") != source_digest():
-        return {}
-    return {k: v["dram_bytes_per_launch"] for k, v in rec.get("kernels", {}).items()}
+    out = {}
+    for k, v in rec.get("kernels", {}).items():
+        if k in KERNEL_SOURCES and v.get("source_sha256") == source_digest(KERNEL_SOURCES[k]):
+            out[k] = v["dram_bytes_per_launch"]
+    return out
 
 
 class ClockSampler:
