@@ -22,7 +22,8 @@
 //
 // The kernel is bound by HBM bandwidth: it streams the 64 KB state in and out once.
 // One CTA per (n, h); each thread owns 4 contiguous value columns (one float4) of
-// DK / NG rows, so a warp reads/writes whole 512-byte rows with 128-bit accesses;
+// DK / NG consecutive rows (so its rows' k, q and decay come four per 16-byte shared load),
+// and a warp reads/writes whole 512-byte rows with 128-bit accesses;
 // the whole state slice lives in registers between the load and the store.  The
 // column reductions over dk are a register partial sum per thread followed by one
 // shared-memory pass across the row groups.
@@ -45,7 +46,7 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   constexpr int TPR = DV / 4;               // threads per state row
   constexpr int NG = kDecodeThreads / TPR;  // row groups
   constexpr int RPG = DK / NG;              // rows per thread
-  static_assert(DK % NG == 0, "rows must split evenly");
+  static_assert(DK % NG == 0 && (DK / NG) % 4 == 0, "rows must split evenly, four per thread at least");
 
   const int nh = blockIdx.x;  // n * H + h
   const int n = nh / H, h = nh - (nh / H) * H;
@@ -72,10 +73,10 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   float4 s[RPG];
 #pragma unroll
   for (int i = 0; i < RPG; ++i)
-    s[i] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(rg + i * NG) * DV) + cg);
+    s[i] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(rg * RPG + i) * DV) + cg);
 
   // the inputs of up to NST tokens, loaded together so that their latency is paid once
-  __shared__ float sk[NST][DK], sq[NST][DK], salpha[NST][DK], sv[NST][DV];
+  __shared__ __align__(16) float sk[NST][DK], sq[NST][DK], salpha[NST][DK], sv[NST][DV];
   __shared__ float sgate[NST > 1 ? NST : 1][NST > 1 ? DV : 1], sbeta[NST];
   __shared__ float4 part_a[NG][TPR], part_b[NG][TPR];
   __shared__ float sdelta[DV], so[NST][DV];
@@ -135,12 +136,19 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
 
     float4 pa = make_float4(0.f, 0.f, 0.f, 0.f), pb = pa;
 #pragma unroll
-    for (int i = 0; i < RPG; ++i) {
-      const int r = rg + i * NG;
-      const float al = salpha[u][r];
-      s[i].x *= al; s[i].y *= al; s[i].z *= al; s[i].w *= al;
-      pa = f4_fma(sk[u][r], s[i], pa);
-      pb = f4_fma(sq[u][r], s[i], pb);
+    for (int i4 = 0; i4 < RPG; i4 += 4) {  // this thread's rows rg RPG + i: four per 16-byte load
+      const float4 al4 = *reinterpret_cast<const float4*>(&salpha[u][rg * RPG + i4]);
+      const float4 k4 = *reinterpret_cast<const float4*>(&sk[u][rg * RPG + i4]);
+      const float4 q4 = *reinterpret_cast<const float4*>(&sq[u][rg * RPG + i4]);
+      const float al[4] = {al4.x, al4.y, al4.z, al4.w}, kk[4] = {k4.x, k4.y, k4.z, k4.w},
+                  qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float4& x = s[i4 + e];
+        x.x *= al[e]; x.y *= al[e]; x.z *= al[e]; x.w *= al[e];
+        pa = f4_fma(kk[e], x, pa);
+        pb = f4_fma(qq[e], x, pb);
+      }
     }
     part_a[rg][cg] = pa;
     part_b[rg][cg] = pb;
@@ -162,7 +170,13 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
 
     const float4 d4 = reinterpret_cast<const float4*>(sdelta)[cg];
 #pragma unroll
-    for (int i = 0; i < RPG; ++i) s[i] = f4_fma(sk[u][rg + i * NG], d4, s[i]);
+    for (int i4 = 0; i4 < RPG; i4 += 4) {
+      const float4 k4 = *reinterpret_cast<const float4*>(&sk[u][rg * RPG + i4]);
+      s[i4] = f4_fma(k4.x, d4, s[i4]);
+      s[i4 + 1] = f4_fma(k4.y, d4, s[i4 + 1]);
+      s[i4 + 2] = f4_fma(k4.z, d4, s[i4 + 2]);
+      s[i4 + 3] = f4_fma(k4.w, d4, s[i4 + 3]);
+    }
 
     // Read-out (+ optional RMSNorm over dv and sigmoid gate).
     if constexpr (NST == 1) {
@@ -213,7 +227,7 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   if (commit) {
 #pragma unroll
     for (int i = 0; i < RPG; ++i)
-      __stcs(reinterpret_cast<float4*>(S + (size_t)(rg + i * NG) * DV) + cg, s[i]);
+      __stcs(reinterpret_cast<float4*>(S + (size_t)(rg * RPG + i) * DV) + cg, s[i]);
   }
 }
 
