@@ -133,16 +133,18 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                self.proc.wait()
-            self._reader.join(timeout=5)
-            self.lines = [ln for ln in self._lines if ln.strip()]
+        if self.proc is None:  # never started, or already stopped
+            self.lines = getattr(self, "lines", [])
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        self._reader.join(timeout=5)
+        self.lines = [ln for ln in self._lines if ln.strip()]
+        self.proc = None
 
     def summary(self):
         if not getattr(self, "lines", None):
@@ -223,44 +225,46 @@ def run_ours(args, world, rank, local):
                                 gate=D["gate"], norm_weight=D["norm_weight"])
 
     clocks = ClockSampler(local).__enter__()  # sampling from the warm-up through the traced pass
-    for _ in range(args.warmup):
-        prefill()
-        decode()
-    torch.cuda.synchronize()
-    assert binding.kda_get_device_error(dev) == 0
-
-    stream = torch.cuda.current_stream(dev)
-
-    def timed_steps():
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-               torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        for i in range(args.steps):
-            ev[i][0].record(stream)
+    try:
+        for _ in range(args.warmup):
             prefill()
-            ev[i][1].record(stream)
             decode()
-            ev[i][2].record(stream)
-        return ev
+        torch.cuda.synchronize()
+        assert binding.kda_get_device_error(dev) == 0
 
-    # the headline: K steps with nothing between the kernels of a call (the state-pass kernels
-    # start while their predecessor drains)
-    _barrier(world)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter()
-    ev = timed_steps()
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
-    _barrier(world)
-    # the same K steps again with every kernel bracketed by CUDA events on its stream: per-kernel
-    # durations for the roofline (the events cost the overlap above, so this pass is not the value)
-    binding.kda_trace_enable(True)
-    binding.kda_trace_collect()  # drop anything recorded before this pass
-    ev_traced = timed_steps()
-    torch.cuda.synchronize()
-    _barrier(world)
-    trace = binding.kda_trace_collect()
-    binding.kda_trace_enable(False)
-    clocks.__exit__(None, None, None)
+        stream = torch.cuda.current_stream(dev)
+
+        def timed_steps():
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                   torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+            for i in range(args.steps):
+                ev[i][0].record(stream)
+                prefill()
+                ev[i][1].record(stream)
+                decode()
+                ev[i][2].record(stream)
+            return ev
+
+        # the headline: K steps with nothing between the kernels of a call (the state-pass kernels
+        # start while their predecessor drains)
+        _barrier(world)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        ev = timed_steps()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        _barrier(world)
+        # the same K steps again with every kernel bracketed by CUDA events on its stream: per-kernel
+        # durations for the roofline (the events cost the overlap above, so this pass is not the value)
+        binding.kda_trace_enable(True)
+        binding.kda_trace_collect()  # drop anything recorded before this pass
+        ev_traced = timed_steps()
+        torch.cuda.synchronize()
+        _barrier(world)
+        trace = binding.kda_trace_collect()
+        binding.kda_trace_enable(False)
+    finally:
+        clocks.__exit__(None, None, None)
     pre_ms = [a.elapsed_time(b) for a, b, _ in ev]
     dec_ms = [b.elapsed_time(c) for _, b, c in ev]
     pre_s = dist_max(sum(pre_ms) / 1e3, world)
