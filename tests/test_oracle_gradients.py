@@ -55,3 +55,20 @@ def test_gradient_of_the_read_out_alone_is_the_state():
     dq = oracle_kda_backward(q, k, v, g, beta, dout, h0=h0)[0]
     expect = torch.einsum("hij,thj->thi", h0[0], dout).numpy()
     assert np.abs(dq - expect).max() < 1e-12
+
+
+def test_no_write_gradients_in_closed_form():
+    """With beta = 0 the state is S_t = Diag(prod_{s<=t} exp g_s) h0, so k and v get no gradient
+    and dL/dh0 = sum_t Diag(prod_{s<=t} exp g_s) q_t dout_t^T + Diag(prod_all exp g) dhT; dL/dbeta
+    is the only path through k and v, and is not zero."""
+    q, k, v, g, beta, h0 = _inputs(6, 2, 3, 4, seed=5)
+    beta = torch.zeros_like(beta)
+    gen = torch.Generator().manual_seed(6)
+    dout = torch.randn(6, 2, 4, generator=gen, dtype=torch.float64)
+    dhT = torch.randn(1, 2, 3, 4, generator=gen, dtype=torch.float64)
+    dq, dk, dv, dg, dbeta, dh0 = oracle_kda_backward(q, k, v, g, beta, dout, h0=h0, dhT=dhT)
+    assert np.abs(dk).max() == 0.0 and np.abs(dv).max() == 0.0
+    assert np.abs(dbeta).max() > 1e-6
+    cum = torch.exp(torch.cumsum(g, dim=0))  # [T, H, dk]: prod_{s<=t} exp g_s, per key channel
+    expect = torch.einsum("thi,thi,thj->hij", cum, q, dout) + cum[-1][:, :, None] * dhT[0]
+    assert np.abs(dh0[0] - expect.numpy()).max() < 1e-12
