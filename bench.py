@@ -35,6 +35,8 @@ if ROOT not in sys.path:
 METRIC = "KDA prefill tokens/s (bf16, H=32, dk=dv=128) + decode steps/s, % of roofline"
 PREFILL_BYTES_PER_TOKEN_HEAD = 3 * 2 * 128 + 4 * 128 + 4 + 2 * 128        # q,k,v bf16 + g fp32 + beta + out bf16
 PREFILL_FLOPS_PER_TOKEN_HEAD = 2 * (5 * 64 * 128 + 3 * 128 * 128)          # method's flop count at C=64, d=128
+PREP_BYTES_PER_TOKEN_HEAD = 3 * 2 * 128 + 4 * 128 + 4                      # the chunk-parallel kernel's inputs
+STATE_BYTES = 128 * 128 * 4                                                # one fp32 state (h0 or hT)
 DECODE_STATE_BYTES = 2 * 128 * 128 * 4                                    # read + write of one fp32 state
 DECODE_IO_BYTES_PER_TOKEN_HEAD = 3 * 2 * 128 + 4 * 128 + 4 + 2 * 128 + 2 * 128  # q,k,v,g,beta,gate,out
 # chunkwise backward, per (chunk, head) at C=64, d=128: 14 C x C x d products (records A, M, W, U_hat;
@@ -99,6 +101,15 @@ def measured_traffic() -> dict:
         if k in KERNEL_SOURCES and v.get("source_sha256") == source_digest(KERNEL_SOURCES[k]):
             out[k] = v["dram_bytes_per_launch"]
     return out
+
+
+def call_traffic(traffic: dict, kernels: dict):
+    """DRAM bytes of one prefill call: the sum over its kernels of the captured bytes per launch, or
+    None unless every kernel of the call has a capture that matches its current sources."""
+    if not kernels or any(k not in traffic for k in kernels):
+        return None
+    calls = min(v[0] for v in kernels.values())
+    return int(sum(traffic[k] * v[0] / calls for k, v in kernels.items()))
 
 
 class ClockSampler:
@@ -274,12 +285,15 @@ def run_ours(args, world, rank, local):
     value = aggregate(T * args.steps, world, pre_s)
     dec_steps_per_s = aggregate(args.steps, world, dec_s)
 
-    # dominant prefill kernel: largest summed time among the prefill-side kernels
+    # the whole prefill call against the HBM roofline (the headline), and its dominant kernel on its
+    # own inputs (the largest summed time among the prefill-side kernels)
     pre_k = {k: v for k, v in trace.items() if k != "kda_decode"}
     dom = max(pre_k.items(), key=lambda kv: kv[1][1])
     dom_ms = dom[1][1] / dom[1][0]
     alg_bytes = PREFILL_BYTES_PER_TOKEN_HEAD * T * H
-    achieved = alg_bytes / (dom_ms * 1e-3) / 1e9
+    call_ms = pre_s * 1e3 / args.steps
+    achieved = alg_bytes / (call_ms * 1e-3) / 1e9
+    dom_bytes = PREP_BYTES_PER_TOKEN_HEAD * T * H if dom[0] == "kda_tc_chunk_prep" else None
     dec_launch = trace.get("kda_decode", (1, float("nan")))
     dec_ms_k = dec_launch[1] / dec_launch[0]
     dec_bytes = DECODE_STATE_BYTES * dcfg.N * dcfg.H + dcfg.N * dcfg.H * (3 * 2 * 128 + 4 * 128 + 4 + 2 * 128 + 2 * 128)
@@ -382,6 +396,14 @@ def run_ours(args, world, rank, local):
                                                       workspace=bws), 2)
     del bws
     bwd_flops = BWD_FLOPS_PER_CHUNK_HEAD * (T // 64) * H
+    del P, D, ws
+    torch.cuda.empty_cache()
+    # the other prefill workloads, each timed on its own with its whole-call HBM roofline
+    others = {}
+    if not args.skip_other_workloads:
+        others["varlen"] = prefill_workload(inputs.VARLEN, max(3, args.steps), dev, hbm_gbs, peak_kind, world,
+                                            time_calls)
+        others["long"] = prefill_workload(inputs.LONG, 3, dev, hbm_gbs, peak_kind, world, time_calls)
     csum = clocks.summary() or {}
     sm_max_mhz = csum.get("sm_max_mhz") or 2070.0
     fp32_tflops = torch.cuda.get_device_properties(dev).multi_processor_count * FP32_LANES_PER_SM * 2 * \
@@ -414,9 +436,17 @@ def run_ours(args, world, rank, local):
                                 "frac": round(dec_achieved / hbm_gbs, 4), "traffic": traffic.get("kda_decode"),
                                 "kernel": "kda_decode", "peak_kind": peak_kind}},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": round(achieved / hbm_gbs, 4), "traffic": traffic.get(dom[0]), "kernel": dom[0],
-                     "kernel_ms": round(dom_ms, 4), "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": alg_bytes},
+                     "frac": round(achieved / hbm_gbs, 4), "traffic": call_traffic(traffic, pre_k),
+                     "kernel": "kda_chunk_fwd (whole call: " + ", ".join(sorted(pre_k)) + ")",
+                     "scope": "whole call", "call_ms": round(call_ms, 4), "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_call": alg_bytes,
+                     "dominant_kernel": {
+                         "kernel": dom[0], "kernel_ms": round(dom_ms, 4), "traffic": traffic.get(dom[0]),
+                         "algorithmic_bytes_per_launch": dom_bytes,
+                         "achieved": round(dom_bytes / (dom_ms * 1e-3) / 1e9, 1) if dom_bytes else None,
+                         "frac": round(dom_bytes / (dom_ms * 1e-3) / 1e9 / hbm_gbs, 4) if dom_bytes else None,
+                         "bytes": "its inputs q, k, v, g, beta (1284 B per token and head); the records it "
+                                  "writes are not algorithmic bytes"}},
         "prefill_tensor": {"flops_per_step": pre_flops,
                            "achieved_tflops": round(pre_flops / (pre_s / args.steps) / 1e12, 2),
                            "peak_tflops": bf16_tflops,
@@ -447,6 +477,7 @@ def run_ours(args, world, rank, local):
                                   "frac": round(bwd_tflops / tf32_tflops, 4),
                                   "frac_of_fp32_fma": round(bwd_tflops / fp32_tflops, 4),
                                   "algorithmic_flops_per_call": bwd_flops, "scope": "whole call"}},
+        **others,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": csum or None,
@@ -454,7 +485,37 @@ def run_ours(args, world, rank, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
+        if "long" in line:
+            line["long"]["cpu_baseline"] = cpu_baseline_long(args)
     return line
+
+
+def prefill_workload(cfg, calls, dev, hbm_gbs, peak_kind, world, time_calls):
+    """ms per kda_chunk_fwd call on a prefill workload (inputs resident in HBM), its tokens/s and
+    its whole-call HBM roofline (q, k, v, g, beta in, out written, plus h0 read and hT written)."""
+    import torch
+
+    from gated_delta_rule_08_gb300 import binding, inputs
+
+    P = inputs.prefill_inputs(cfg, device=dev)
+    T_tot, H, B = P["T_tot"], cfg.H, len(P["lengths"])
+    varlen = cfg.len_range is not None or cfg.lengths is not None
+    kw = {"cu_seqlens": P["cu_seqlens"]} if varlen else {"B": B}
+    out = torch.empty(T_tot, H, cfg.dv, device=dev, dtype=torch.bfloat16)
+    hT = torch.empty(B, H, cfg.dk, cfg.dv, device=dev, dtype=torch.float32)
+    ws = torch.empty(binding.kda_chunk_fwd_workspace_size(B, T_tot if varlen else T_tot // B, H, cfg.dk, cfg.dv),
+                     device=dev, dtype=torch.uint8)
+    ms = time_calls(lambda: binding.kda_chunk_fwd(P["q"], P["k"], P["v"], P["g"], P["beta"], h0=P["h0"], out=out,
+                                                  hT=hT, workspace=ws, **kw), calls)
+    nbytes = PREFILL_BYTES_PER_TOKEN_HEAD * T_tot * H + B * H * STATE_BYTES * (2 if P["h0"] is not None else 1)
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    del P, out, hT, ws
+    torch.cuda.empty_cache()
+    return {"workload": cfg.name + f" ({T_tot} tokens)", "ms_per_call": round(ms, 4),
+            "tokens_per_s": round(aggregate(T_tot, world, ms / 1e3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": round(achieved / hbm_gbs, 4), "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_call": nbytes, "scope": "whole call"}}
 
 
 def _oracle_prefill_sample(tokens: int):
@@ -477,6 +538,24 @@ def cpu_baseline(args):
     return {"value": round(tokens / secs, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"fp64 token-by-token oracle on the first {tokens} of the 8192 prefill tokens, all 32 heads "
                       f"(OpenMP over heads; {secs:.2f} s wall)"}
+
+
+def cpu_baseline_long(args):
+    """The oracle on the 65,536-token prefix of the long-context workload (H = 16)."""
+    import dataclasses
+
+    from gated_delta_rule_08_gb300 import inputs
+    from oracle import oracle_kda_prefill, oracle_threads
+
+    tokens = args.cpu_tokens_long
+    P = inputs.prefill_inputs(dataclasses.replace(inputs.LONG, T=tokens), device="cpu")
+    t0 = time.perf_counter()
+    oracle_kda_prefill(P["q"], P["k"], P["v"], P["g"], P["beta"])
+    secs = time.perf_counter() - t0
+    return {"value": round(tokens / secs, 1), "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"fp64 token-by-token oracle on the first {tokens} tokens of the long-context workload, "
+                      f"all 16 heads ({secs:.2f} s wall); a 1,048,576-token call would take about "
+                      f"{secs * (1 << 20) / tokens:.0f} s (extrapolated)"}
 
 
 def run_reference(args, world, rank):
@@ -508,15 +587,28 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-tokens", type=int, default=8192)
+    ap.add_argument("--cpu-tokens-long", type=int, default=65536)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-other-workloads", action="store_true",
+                    help="time only the prefill + decode step (no varlen / long-context lines)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world, rank, local = _dist()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: relaunch this command under torch.distributed.run
+        port = str(_env_int("MASTER_PORT", 29511))
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", port, os.path.abspath(__file__)] + \
+            (list(argv) if argv is not None else sys.argv[1:])
+        return subprocess.call(cmd)
+    if world != args.gpus:
+        sys.stderr.write(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch one process per GPU\n")
+        return 2
     if args.impl == "reference":
         line = run_reference(args, world, rank)
         if line is not None:
