@@ -26,12 +26,14 @@ DEVERR_BAD_SLOT = 0x1
 DEVERR_BAD_SEQLENS = 0x2
 DEVERR_WAIT_TIMEOUT = 0x4
 DEVERR_BAD_COUNT = 0x8
+DEVERR_NONFINITE = 0x10
+DEVERR_PRECONDITION = 0x20
 
 # Exported symbols, as declared in include/kda.h.
 EXPORTS = ("kda_chunk_fwd_workspace_size", "kda_chunk_fwd", "kda_decode_step", "kda_decode_multi",
            "kda_chunk_fwd_checkpoints", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size", "kda_get_device_error",
            "kda_status_string", "kda_trace_enable", "kda_trace_collect", "kda_chunk_fwd_noalloc",
-           "kda_noalloc_scratch_bytes")
+           "kda_noalloc_scratch_bytes", "kda_chunk_fwd_segment_map", "kda_state_compose")
 
 
 class KdaError(RuntimeError):
@@ -78,6 +80,10 @@ def load_library(path: Optional[str] = None):
         lib.kda_get_device_error.restype = I
         lib.kda_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, I, I, P, P]
         lib.kda_chunk_fwd_noalloc.restype = I
+        lib.kda_chunk_fwd_segment_map.argtypes = [P, P, P, P, P, P, I64, I, I, I, I, I, P, SZ, P]
+        lib.kda_chunk_fwd_segment_map.restype = I
+        lib.kda_state_compose.argtypes = [P, P, P, P, I, I, I, I, P]
+        lib.kda_state_compose.restype = I
         lib.kda_noalloc_scratch_bytes.argtypes = []
         lib.kda_noalloc_scratch_bytes.restype = SZ
         lib.kda_trace_enable.argtypes = [I]
@@ -424,3 +430,55 @@ def kda_chunk_fwd_noalloc(q, k, v, g, beta, h0=None, cu_seqlens=None, out=None, 
     if st != 0:
         raise KdaError("kda_chunk_fwd_noalloc", st)
     return out, hT
+
+
+def kda_chunk_fwd_segment_map(k, v, g, beta, *, C: int = 64, P=None, b=None, workspace=None):
+    """The affine map of one token range's state pass (context parallelism across devices):
+    S_out = P S_in + b.  k: [T, H, dk]; v: [T, H, dv]; g: [T, H, dk] fp32; beta: [T, H] fp32.
+    Returns (P [H, dk, dk], b [H, dk, dv]), both fp32."""
+    lib = load_library()
+    dev = k.device
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    dt = k.dtype
+    code = _dtype_code(k)
+    _check(k, "k", dt, (T, H, dk), dev)
+    _check(v, "v", dt, (T, H, dv), dev)
+    _check(g, "g", torch.float32, (T, H, dk), dev)
+    _check(beta, "beta", torch.float32, (T, H), dev)
+    if P is None:
+        P = torch.empty(H, dk, dk, device=dev, dtype=torch.float32)
+    if b is None:
+        b = torch.empty(H, dk, dv, device=dev, dtype=torch.float32)
+    _check(P, "P", torch.float32, (H, dk, dk), dev)
+    _check(b, "b", torch.float32, (H, dk, dv), dev)
+    need = int(lib.kda_chunk_fwd_workspace_size(1, T, H, dk, dv, C, code))
+    if need == 0:
+        raise KdaError("kda_chunk_fwd_workspace_size", 2)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    st = lib.kda_chunk_fwd_segment_map(_ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(P), _ptr(b), T, H, dk, dv, C,
+                                       code, _ptr(workspace), workspace.numel(), _stream(dev))
+    if st != 0:
+        raise KdaError("kda_chunk_fwd_segment_map", st)
+    return P, b
+
+
+def kda_state_compose(P, b, S0=None, out=None):
+    """Fold n range maps into an initial state: S = P[n-1](...(P[0] S0 + b[0])...) + b[n-1].
+    P: [n, H, dk, dk] fp32; b: [n, H, dk, dv] fp32; S0: [H, dk, dv] fp32 or None (zero).
+    Returns S [H, dk, dv] fp32 (`out` if given; it may be S0)."""
+    lib = load_library()
+    n, H, dk, _ = P.shape
+    dv = b.shape[3]
+    dev = P.device
+    _check(P, "P", torch.float32, (n, H, dk, dk), dev)
+    _check(b, "b", torch.float32, (n, H, dk, dv), dev)
+    _check(S0, "S0", torch.float32, (H, dk, dv), dev)
+    if out is None:
+        out = torch.empty(H, dk, dv, device=dev, dtype=torch.float32)
+    _check(out, "out", torch.float32, (H, dk, dv), dev)
+    st = lib.kda_state_compose(_ptr(P), _ptr(b), _ptr(S0), _ptr(out), n, H, dk, dv, _stream(dev))
+    if st != 0:
+        raise KdaError("kda_state_compose", st)
+    return out

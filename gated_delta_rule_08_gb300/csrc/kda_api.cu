@@ -1,6 +1,8 @@
 // C-ABI entry points of libkda: argument validation, dispatch, device error word.
 // The public contract is include/kda.h.
 #include <cuda_runtime.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -16,7 +18,6 @@ namespace {
 // Host code only uses its address, obtained per device with cudaGetSymbolAddress.
 __device__ unsigned int g_device_error = 0u;
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned int* g_err_ptr[kMaxDevices] = {};
 int g_cc_major[kMaxDevices] = {}, g_cc_minor[kMaxDevices] = {};
@@ -43,6 +44,52 @@ kda_status device_state(unsigned int** err, int* major, int* minor) {
 
 bool dims_ok(int dk, int dv) { return (dk == 64 || dk == 128) && (dv == 64 || dv == 128); }
 
+// ---- precondition checks (KDA_DEBUG_CHECKS): one pass over the inputs, flag on the device
+__global__ void check_decay_beta(const float4* __restrict__ g, int64_t n_g4, const float* __restrict__ beta,
+                                 int64_t n_beta, unsigned int* err) {
+  bool bad = false;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_g4; i += stride) {
+    const float4 x = g[i];
+    bad |= !(x.x > -5.f && x.x <= 0.f) || !(x.y > -5.f && x.y <= 0.f) || !(x.z > -5.f && x.z <= 0.f) ||
+           !(x.w > -5.f && x.w <= 0.f);
+  }
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_beta; i += stride) {
+    const float x = beta[i];
+    bad |= !(x >= 0.f && x <= 1.f);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err, KDA_DEVERR_PRECONDITION);
+}
+// distinct decode slots: every in-range slot index compared with the ones after it (O(N^2) work,
+// spread over the grid; a debugging aid)
+__global__ void check_distinct_slots(const int32_t* __restrict__ slot, int N, int num_slots, unsigned int* err) {
+  bool bad = false;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < N; i += gridDim.x * blockDim.x) {
+    const int si = slot[i];
+    if (si < 0 || si >= num_slots) continue;  // reported by the decode kernel itself
+    for (int j = i + 1; j < N; ++j) bad |= slot[j] == si;
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err, KDA_DEVERR_PRECONDITION);
+}
+
+cudaError_t launch_checks(const float* g, int64_t n_g, const float* beta, int64_t n_beta, const int32_t* slot, int N,
+                          int num_slots, unsigned int* err, cudaStream_t st) {
+  TraceScope ts("kda_debug_checks", st);
+  if (n_g > 0 || n_beta > 0) {
+    const int64_t work = (n_g / 4 > n_beta ? n_g / 4 : n_beta);
+    const int grid = (int)((work + 255) / 256 < 1184 ? (work + 255) / 256 : 1184);
+    check_decay_beta<<<grid > 0 ? grid : 1, 256, 0, st>>>(reinterpret_cast<const float4*>(g), n_g / 4, beta,
+                                                          n_beta, err);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (slot != nullptr && N > 1) {
+    check_distinct_slots<<<(N + 255) / 256, 256, 0, st>>>(slot, N, num_slots, err);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t blob_bytes(kda_dtype dtype, int dk, int dv) {
@@ -51,6 +98,16 @@ size_t blob_bytes(kda_dtype dtype, int dk, int dv) {
 }
 
 }  // namespace
+
+bool test_wait_timeout() {
+  const char* e = getenv("KDA_TEST_WAIT_TIMEOUT");
+  return e != nullptr && *e != '\0' && strcmp(e, "0") != 0;
+}
+
+bool debug_checks() {
+  const char* e = getenv("KDA_DEBUG_CHECKS");
+  return e != nullptr && *e != '\0' && strcmp(e, "0") != 0;
+}
 }  // namespace kda
 
 using namespace kda;
@@ -119,7 +176,11 @@ kda_status chunk_fwd_common(const void* q, const void* k, const void* v, const f
   a.epi.eps = epi ? epi->eps : 0.f;
   a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.err = err;
   a.ckpt = states; a.ckpt_chunks = states ? ckpt_chunks : 0;
+  a.give_up = test_wait_timeout();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (debug_checks() &&
+      launch_checks(g, T_tot * H * dk, beta, T_tot * H, nullptr, 0, 0, err, s) != cudaSuccess)
+    return KDA_ERR_CUDA;
   cudaError_t e = (a.bf16 && prefill_tc_supported(dk, dv)) ? prefill_tc_launch(a, s) : prefill_cc_launch(a, s);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -143,6 +204,53 @@ KDA_API kda_status kda_chunk_fwd_checkpoints(const void* q, const void* k, const
   if (!states) return KDA_ERR_INVALID_ARG;
   return chunk_fwd_common(q, k, v, g, beta, h0, cu_seqlens, out, hT, states, ckpt_chunks, B, T, H, dk, dv, C, dtype,
                           out_dtype, epi, workspace, workspace_bytes, stream);
+}
+
+KDA_API kda_status kda_chunk_fwd_segment_map(const void* k, const void* v, const float* g, const float* beta,
+                                             float* P, float* b, int64_t T, int H, int dk, int dv, int C,
+                                             kda_dtype dtype, void* workspace, size_t workspace_bytes,
+                                             void* stream) {
+  if (T < 0 || H <= 0 || !P || !b) return KDA_ERR_INVALID_ARG;
+  if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_FP32) return KDA_ERR_UNSUPPORTED;
+  if (C != kChunk || !dims_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+  if (dtype != KDA_DTYPE_BF16 || !prefill_tc_supported(dk, dv)) return KDA_ERR_UNSUPPORTED;
+  if (T > 0 && (!k || !v || !g || !beta)) return KDA_ERR_INVALID_ARG;
+  if (T > ((int64_t)1 << 31) * 64 / H) return KDA_ERR_UNSUPPORTED;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(P) || !aligned16(b)) return KDA_ERR_INVALID_ARG;
+  const size_t need = kda_chunk_fwd_workspace_size(1, T, H, dk, dv, C, dtype);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return KDA_ERR_WORKSPACE;
+  unsigned int* err = nullptr;
+  int major = 0, minor = 0;
+  kda_status st = device_state(&err, &major, &minor);
+  if (st != KDA_OK) return st;
+  if (major != 10 || minor != 3) return KDA_ERR_UNSUPPORTED;
+  PrefillArgs a{};
+  a.q = k; a.k = k; a.v = v; a.g = g; a.beta = beta;  // the read-out operands are not used
+  a.B = 1; a.T = T; a.T_tot = T; a.H = H; a.dk = dk; a.dv = dv;
+  a.bf16 = true; a.out_bf16 = true;
+  a.workspace = workspace; a.workspace_bytes = workspace_bytes; a.err = err;
+  a.give_up = test_wait_timeout();
+  a.seg_P = P; a.seg_b = b;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (debug_checks() && launch_checks(g, T * H * dk, beta, T * H, nullptr, 0, 0, err, s) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  return prefill_tc_launch(a, s) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+KDA_API kda_status kda_state_compose(const float* P, const float* b, const float* S0, float* S_out, int n, int H,
+                                     int dk, int dv, void* stream) {
+  if (n < 0 || H <= 0 || !S_out || (n > 0 && (!P || !b))) return KDA_ERR_INVALID_ARG;
+  if (!dims_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+  if (!aligned16(P) || !aligned16(b) || !aligned16(S0) || !aligned16(S_out)) return KDA_ERR_INVALID_ARG;
+  unsigned int* err = nullptr;
+  int major = 0, minor = 0;
+  kda_status st = device_state(&err, &major, &minor);
+  if (st != KDA_OK) return st;
+  if (major != 10 || minor != 3) return KDA_ERR_UNSUPPORTED;
+  return state_compose_launch(P, b, S0, S_out, n, H, dk, dv, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KDA_OK
+             : KDA_ERR_CUDA;
 }
 
 KDA_API size_t kda_chunk_bwd_workspace_size(int B, int64_t T, int H, int dk, int dv) {
@@ -221,7 +329,11 @@ kda_status decode_common(const void* q, const void* k, const void* v, const floa
   a.epi.norm_weight = epi ? epi->norm_weight : nullptr;
   a.epi.eps = epi ? epi->eps : 0.f;
   a.err = err;
-  cudaError_t e = decode_launch(a, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t rows = (int64_t)N * n_tok * H;
+  if (debug_checks() && launch_checks(g, rows * dk, beta, rows, slot_idx, N, num_slots, err, s) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  cudaError_t e = decode_launch(a, s);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 }  // namespace

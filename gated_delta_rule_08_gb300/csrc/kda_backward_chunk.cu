@@ -1163,22 +1163,22 @@ cudaError_t launch_serial(const BackwardArgs& a, const float* recs, float* state
 
 template <int D, int E, typename Tin>
 cudaError_t launch_chunked(const BackwardArgs& a, float* ws, cudaStream_t st) {
-  static bool attr_done[64] = {};
+  static DeviceOnce once;
   int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return cudaErrorInvalidDevice;
   constexpr size_t rec_smem = RecSmem<D, E>::floats * sizeof(float);
   constexpr size_t dv_smem = DvSmem<D, E>::floats * sizeof(float);
   constexpr size_t gr_smem = GradSmem<D>::floats * sizeof(float);
-  if (!attr_done[dev]) {
+  const cudaError_t e0 = once.run(dev, [] {
     cudaError_t e = cudaFuncSetAttribute(bwd_rec<D, E, Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rec_smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(bwd_dvsums<D, E, Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dv_smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(bwd_grads<D, E, Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gr_smem);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+    return e;
+  });
+  if (e0 != cudaSuccess) return e0;
   const int64_t ntask = max_chunks(a.B, a.T, a.cu_seqlens != nullptr) * a.H;
   if (ntask == 0) return cudaSuccess;
   float* recs = ws;

@@ -9,6 +9,8 @@
 #define KDA_DEVERR_BAD_SEQLENS 0x2u
 #define KDA_DEVERR_WAIT_TIMEOUT 0x4u
 #define KDA_DEVERR_BAD_COUNT 0x8u
+#define KDA_DEVERR_NONFINITE 0x10u
+#define KDA_DEVERR_PRECONDITION 0x20u
 
 namespace kda {
 

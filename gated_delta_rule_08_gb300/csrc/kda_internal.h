@@ -6,9 +6,42 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace kda {
 
 constexpr int kChunk = 64;  // tokens per chunk (C)
+constexpr int kMaxDevices = 64;
+
+// One-time per-device set-up (kernel attributes, device properties), safe to call from several
+// host threads: `init` runs under a lock until it has succeeded once on the device, and whatever it
+// wrote is visible to every caller that returns cudaSuccess.
+struct DeviceOnce {
+  std::mutex mu;
+  bool done[kMaxDevices] = {};
+  template <class F>
+  cudaError_t run(int dev, F&& init) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done[dev]) return cudaSuccess;
+    const cudaError_t e = init();
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
+  }
+};
+
+// The tensor-core kernels' bounded waits on work of their own CTA (mbarrier phases of copies, MMAs
+// and hand-overs between warps) give up after ~2e7 polls.  With the environment variable
+// KDA_TEST_WAIT_TIMEOUT set (any value but "" or "0"; read at every call) the launches use kernel
+// variants whose waits give up at once, so that a test can make them run out on purpose and check
+// that the kernels report KDA_DEVERR_WAIT_TIMEOUT and leave the device usable.  Waits for a CTA's own
+// copies and MMAs to drain before it exits keep their bound in both variants.
+bool test_wait_timeout();
+
+// KDA_DEBUG_CHECKS (environment variable, read at every call; any value but "" or "0" enables it):
+// before the hot-path kernels, a check kernel tests the documented preconditions on the device
+// (g in (-5, 0], beta in [0, 1], distinct decode slots) and sets KDA_DEVERR_PRECONDITION.
+bool debug_checks();
 
 // Epilogue arguments as the kernels see them (gate == nullptr: no epilogue).
 struct Epilogue {
@@ -39,6 +72,11 @@ struct PrefillArgs {
   unsigned int* err;          // device error word
   float* ckpt;                // state checkpoints [n][H][dk][dv] fp32, or null
   int64_t ckpt_chunks;        // a checkpoint after every ckpt_chunks full chunks of a sequence
+  bool give_up;               // launch the kernel variants whose waits give up at once (tests)
+  // segment map (context parallelism across devices): instead of out / hT, the transition P
+  // [H][dk][dk] and the offset b [H][dk][dv] of the whole token range (B == 1, no cu_seqlens)
+  float* seg_P;
+  float* seg_b;
 };
 
 struct DecodeArgs {
@@ -119,6 +157,10 @@ int prefill_tc_cp_segments(int B, int64_t T, int H);
 size_t prefill_tc_cp_bytes(int B, int64_t T, int H);
 cudaError_t scan_tc_launch(const PrefillArgs& a, const uint8_t* records, const int32_t* plan, float* cp, int nseg,
                            int64_t seg_len, cudaStream_t stream);
+
+// context parallelism across devices (kda_kcp.cu): S_out = P[n-1](... (P[0] S0 + b[0]) ...) + b[n-1]
+cudaError_t state_compose_launch(const float* P, const float* b, const float* S0, float* S_out, int n, int H, int dk,
+                                 int dv, cudaStream_t stream);
 
 // plan kernel (kda_prefill_cc.cu): chunk offsets per sequence + cu_seqlens validation
 cudaError_t plan_launch(const int32_t* cu_seqlens, int B, int64_t T_tot, int32_t* plan,

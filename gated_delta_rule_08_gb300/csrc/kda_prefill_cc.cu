@@ -518,18 +518,17 @@ cudaError_t launch_cc(const PrefillArgs& a, cudaStream_t st) {
   using L = CcBlob<DK, DV>;
   const size_t prep_smem = prep_smem_floats<DK, DV>() * sizeof(float);
   const size_t scan_smem = scan_smem_floats<DK, DV>() * sizeof(float);
-  static bool attr_done[64] = {};  // per instantiation and device; idempotent if raced
+  static DeviceOnce once;  // per instantiation
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const cudaError_t e0 = once.run(dev, [prep_smem, scan_smem] {
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_cc<DK, DV, Tin>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chunk_scan_cc<DK, DV, Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)scan_smem);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+    return cudaFuncSetAttribute(chunk_scan_cc<DK, DV, Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)scan_smem);
+  });
+  if (e0 != cudaSuccess) return e0;
   const bool has_cu = a.cu_seqlens != nullptr;
   const int64_t nchunks = max_chunks(a.B, a.T, has_cu);
   int32_t* plan = static_cast<int32_t*>(a.workspace);

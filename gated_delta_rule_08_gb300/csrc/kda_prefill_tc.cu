@@ -33,8 +33,11 @@
 //
 // Precision: bf16 operands cannot meet the parity bound on these workloads; fp16 has the bf16
 // MMA rate with 3 more significand bits, and every fp16 operand here is bounded (decayed
-// keys/queries <= 1, values well inside the fp16 range).  The reference-scaled A/M operands
-// need fp32 range and ~16 significant bits (M feeds the read-out directly): hence the split.
+// keys/queries <= 1) except those that scale with the values (Diag(beta) V, U_hat) and the
+// inverse X; one of those past 65504 becomes inf, which the state pass meets in what it writes
+// (KDA_DEVERR_NONFINITE).  The reference-scaled A/M operands need fp32 range and ~16 significant
+// bits (M feeds the read-out directly, and a head-wise RMSNorm amplifies its error on rows of small
+// norm: a single tf32 product measured 0.031 max|err|/RMS there): hence the split.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -235,6 +238,7 @@ __device__ __forceinline__ void stage_beta(const float* beta, float* sbeta, uint
   if (lane == 0) mbar_arrive(bar);
 }
 
+template <bool GIVEUP>
 __global__ void __launch_bounds__(kPrepThreads, 2)
 kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict__ g, const float* __restrict__ beta,
                   const int32_t* __restrict__ plan, const int32_t* __restrict__ cu, int B, int64_t T, int H,
@@ -310,7 +314,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
       const int64_t ntask_idx = next_task(task + stride, ntask, stride, plan, cu, B, T, H, nh, nt0, nn, nchunk);
       if (lane == 0) {
         for (int pass = 0; pass < 4 && ok; ++pass) {
-          ok = wait_or_abort(&ops_ready[pass & 1], (uint32_t)((pass >> 1) & 1), abort_flag);
+          ok = wait_or_abort_t<GIVEUP>(&ops_ready[pass & 1], (uint32_t)((pass >> 1) & 1), abort_flag);
           if (!ok) break;
           if (pass == 0) load_pending = false;  // the compute warps have consumed this task's tiles
           tc_fence_after();
@@ -327,7 +331,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
       if (!ok) break;
       if (ntask_idx >= 0) stage_beta(beta, sBetaAll + 64 * ((it + 1) & 1), full, nh, nt0, nn, H, lane);
       if (lane == 0) {
-        ok = wait_or_abort(tt_ready, it & 1, abort_flag);
+        ok = wait_or_abort_t<GIVEUP>(tt_ready, it & 1, abort_flag);
         if (ok) {
           tc_fence_after();
 #pragma unroll
@@ -338,7 +342,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
           mma_commit(bar_wu);
           if (ntask_idx >= 0) {
             // the next task's tiles once these MMAs have read the current k and v
-            ok = wait_or_abort(bar_wu, it & 1, abort_flag);
+            ok = wait_or_abort_t<GIVEUP>(bar_wu, it & 1, abort_flag);
             if (ok) {
               tma_qkv(maps, raw, full, nh, nt0);
               load_pending = true;
@@ -375,7 +379,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
       // the previous task's bulk copies out of the operand region have read it
       if (tid == 0) bulk_wait_read_all();
       // every break decision of the compute warps is made together (named barriers follow)
-      ok = group_and(1, kCompute, wait_or_abort(full, it & 1, abort_flag));
+      ok = group_and(1, kCompute, wait_or_abort_t<GIVEUP>(full, it & 1, abort_flag));
       if (!ok) break;
       if (n < 64) {
         // a tail chunk: rows n..63 of the raw tiles (the next sequence's tokens, or the tensor's
@@ -410,7 +414,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
           prev = make_float2(__shfl_xor_sync(0xffffffffu, run.x, 16), __shfl_xor_sync(0xffffffffu, run.y, 16));
           if (lane < 16) sTot[(pass & 1) * 128 + warp * 16 + cp] = make_float2(run.x + prev.x, run.y + prev.y);
         }
-        if (pass >= 2) ok = wait_or_abort(&bar_ops[pass & 1], 0, abort_flag);
+        if (pass >= 2) ok = wait_or_abort_t<GIVEUP>(&bar_ops[pass & 1], 0, abort_flag);
         ok = group_and(1, kCompute, ok);
         if (!ok) break;
         float2 off = lane < 16 ? make_float2(0.f, 0.f) : prev, cum = make_float2(0.f, 0.f), G15, G47, G63;
@@ -503,7 +507,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
         for (int i = 0; i < 4; ++i) gcur[i] = gnext[i];
       }
       if (!ok) break;
-      ok = group_and(1, kCompute, wait_or_abort(&bar_ops[1], 1, abort_flag));  // pass 3 (and all before) done
+      ok = group_and(1, kCompute, wait_or_abort_t<GIVEUP>(&bar_ops[1], 1, abort_flag));  // pass 3 (and all before) done
       if (!ok) break;
       tc_fence_after();
 
@@ -640,7 +644,7 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
       mbar_arrive(tt_ready);
 
       // ---- W^T = K_hat^T T^T, U_hat^T = V^T T^T (issued by the issuer warp) -> the record
-      ok = group_and(1, kCompute, wait_or_abort(bar_wu, it & 1, abort_flag));
+      ok = group_and(1, kCompute, wait_or_abort_t<GIVEUP>(bar_wu, it & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       {
@@ -714,18 +718,19 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
 
 template <typename Tout>
 cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
-  static bool attr_done[64] = {};
-  static int sm_count[64] = {};
+  static DeviceOnce once;
+  static int sm_count[kMaxDevices] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kda_tc_chunk_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  cudaError_t e0 = once.run(dev, [dev] {
+    cudaError_t e = cudaFuncSetAttribute(kda_tc_chunk_prep<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kPrepSmem);
     if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    e = cudaFuncSetAttribute(kda_tc_chunk_prep<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+    return cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+  });
+  if (e0 != cudaSuccess) return e0;
   const bool has_cu = a.cu_seqlens != nullptr;
   const int64_t nchunks = max_chunks(a.B, a.T, has_cu);
   int32_t* plan = static_cast<int32_t*>(a.workspace);
@@ -745,13 +750,15 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t st) {
     const int64_t slots = 2 * (int64_t)sm_count[dev];  // two CTAs per SM
     const int grid = (int)(ntask < slots ? ntask : slots);
     TraceScope ts("kda_tc_chunk_prep", st);
-    kda_tc_chunk_prep<<<grid, kPrepThreads, kPrepSmem, st>>>(maps, a.g, a.beta, plan, a.cu_seqlens, a.B, a.T, a.H,
-                                                            ntask, records, a.err);
+    auto* kernel = a.give_up ? kda_tc_chunk_prep<true> : kda_tc_chunk_prep<false>;
+    kernel<<<grid, kPrepThreads, kPrepSmem, st>>>(maps, a.g, a.beta, plan, a.cu_seqlens, a.B, a.T, a.H, ntask, records,
+                                                  a.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  // state pass, split into sequence segments when there are too few (sequence, head) chains
-  const int nseg = prefill_tc_cp_segments(a.B, a.T, a.H);
+  // state pass, split into sequence segments when there are too few (sequence, head) chains (a
+  // segment map runs its range as one segment)
+  const int nseg = a.seg_P != nullptr ? 1 : prefill_tc_cp_segments(a.B, a.T, a.H);
   const int64_t maxc = (a.T + kChunk - 1) / kChunk;  // chunks of the longest possible sequence
   const int64_t seg_len = (maxc + nseg - 1) / nseg;
   float* cp = reinterpret_cast<float*>(records + align_up((size_t)nchunks * a.H * kRecBytes, 256));

@@ -30,7 +30,16 @@
 //      through a staging buffer with the optional RMSNorm + gate epilogue;
 //    MODE 1 (transition): z = 0 runs segment 0 from h0 (its final state is S_in(1)); for p >= 1,
 //      z = 2 p - 1 + kind, kind 0 runs b_p and kind 1 runs P_p; no read-out.
+//    segment map (context parallelism across devices, section 13.3.2): MODE 1 over one token range
+//      with z = 2 p + kind for every segment p, both runs starting from 0 (kind 0, with U_hat) or I
+//      (kind 1, U_hat = 0); with one segment the runs' final states are the range's b and P.
 //  kda_cp_merge (grid = sequences x heads x 4 column slices): the sequential segment merge in fp32.
+//
+//  Non-finite results: an fp16 operand past 65504 (a value, an intra-chunk term or the state copy)
+//  becomes inf and reaches the state (through U = U_hat - W S and S += K_bar^T U) as well as the
+//  outputs, so the state warps test every run's final state (written or not) and the checkpoints
+//  they write (a sum is finite exactly when its terms are) and set KDA_DEVERR_NONFINITE; nothing on
+//  the serial path or in the output warps is checked.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -78,6 +87,8 @@ struct ScanParams {
   float* cp;        // [B][H][nseg][3][128][128]: P_p, b_p, S_in(p)
   float* ckpt;      // state checkpoints [n][H][128][128] fp32, or null (read-out pass only)
   int64_t ckpt_chunks;
+  float* seg_P;         // segment map: the range's transition [H][128][128] (MODE 1), or null
+  float* seg_b;         // segment map: the range's offset [H][128][128] (MODE 1)
 };
 
 __device__ __forceinline__ void tmem_ld64b(uint32_t taddr, float* v) {
@@ -110,7 +121,7 @@ __device__ __forceinline__ void tmem_st64h(uint32_t taddr, const float* v) {
   tmem_st32u(taddr, a);
 }
 
-template <typename Tout, int MODE, bool CKPT>
+template <typename Tout, int MODE, bool CKPT, bool GIVEUP = false>
 __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -140,10 +151,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
   int64_t first_chunk, t_begin, len;
   const int64_t nchunks = sequence_chunks(b, p.plan, p.cu, p.B, p.T, first_chunk, t_begin, len);
   const int64_t p_last = nchunks > 0 ? (nchunks - 1) / p.seg_len : 0;
-  // MODE 1: kind 0 = offset b (from h0 for segment 0), 1 = transition P
-  const int seg = MODE == 0 || blockIdx.z == 0 ? (int)blockIdx.z : (int)((blockIdx.z + 1) >> 1);
-  const int kind = MODE == 0 || blockIdx.z == 0 ? 0 : (int)((blockIdx.z + 1) & 1);
-  if ((MODE == 0 && seg > p_last) || (MODE == 1 && seg >= p_last)) {
+  // MODE 1: kind 0 = offset b (from h0 for segment 0), 1 = transition P; a segment map runs both
+  // kinds for every segment, from 0 and from I
+  const bool segmap = MODE == 1 && p.seg_P != nullptr;
+  const uint32_t z = blockIdx.z;
+  const int seg = segmap ? (int)(z >> 1) : (MODE == 0 || z == 0 ? (int)z : (int)((z + 1) >> 1));
+  const int kind = segmap ? (int)(z & 1) : (MODE == 0 || z == 0 ? 0 : (int)((z + 1) & 1));
+  if ((MODE == 0 && seg > p_last) || (MODE == 1 && !segmap && seg >= p_last) || (segmap && seg > p_last)) {
     griddep_wait();
     return;
   }
@@ -208,14 +222,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
         uint8_t* stage = sm + st * kStage;
         if (c + 2 < ncs) {
           // chunk c+2 goes where chunk c-1 was: free once that chunk's products are done
-          if (c >= 1) ok = wait_or_abort(bar_s, (uint32_t)((c - 1) & 1), abort_flag);
+          if (c >= 1) ok = wait_or_abort_t<GIVEUP>(bar_s, (uint32_t)((c - 1) & 1), abort_flag);
           if (!ok) break;
           stage_record(c + 2);
         }
-        ok = wait_or_abort(&full[st], (uint32_t)((c / kStages) & 1), abort_flag);
+        ok = wait_or_abort_t<GIVEUP>(&full[st], (uint32_t)((c / kStages) & 1), abort_flag);
         if (ok) consumed = c;
-        ok = ok && wait_or_abort(s16_ready, (uint32_t)(c & 1), abort_flag);
-        if (MODE == 0 && ok && c >= 1) ok = wait_or_abort(do_free, (uint32_t)((c - 1) & 1), abort_flag);
+        ok = ok && wait_or_abort_t<GIVEUP>(s16_ready, (uint32_t)(c & 1), abort_flag);
+        if (MODE == 0 && ok && c >= 1) ok = wait_or_abort_t<GIVEUP>(do_free, (uint32_t)((c - 1) & 1), abort_flag);
         if (!ok) break;
         tc_fence_after();
         {
@@ -225,7 +239,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
             mma_f16_ts(tmem + T_DU, tmem + T_S16 + 8 * ks, desc_add(db, ks * 2048), id1, ks > 0);
           mma_commit(bar_u);
         }
-        ok = wait_or_abort(u16_ready, (uint32_t)(c & 1), abort_flag);
+        ok = wait_or_abort_t<GIVEUP>(u16_ready, (uint32_t)(c & 1), abort_flag);
         if (!ok) break;
         tc_fence_after();
         {
@@ -251,9 +265,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
     const int64_t ck_base = CKPT ? checkpoint_base(b, p.cu, p.T, 64 * p.ckpt_chunks) : 0;
     int64_t ck_next = CKPT ? (c_begin / p.ckpt_chunks + 1) * p.ckpt_chunks : 0;  // next boundary (chunks done)
     bool ok = true;
+    float fsum = 0.f;  // sum over this run's final state and its checkpoints (finite iff each entry is)
     {
-      // segment 0 starts from h0 in both modes; the read-out of a later segment from S_in(seg)
-      const bool from_state = MODE == 0 || seg == 0;
+      // segment 0 starts from h0 in both modes (a segment map's from 0); the read-out of a later
+      // segment from S_in(seg)
+      const bool from_state = MODE == 0 || (seg == 0 && !segmap);
       const float* init = nullptr;
       if (from_state) init = seg == 0 ? (p.h0 ? p.h0 + soff : nullptr) : cpb + 2 * kCpMat;
       float s[64];
@@ -268,7 +284,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
       tc_fence_before();
       mbar_arrive(s16_ready);
       if (ncs > 0) {
-        ok = wait_or_abort(&full[0], 0, abort_flag);
+        ok = wait_or_abort_t<GIVEUP>(&full[0], 0, abort_flag);
         if (ok) {
           const float* gc = reinterpret_cast<const float*>(sm + kRecGC) + 64 * hc;
 #pragma unroll
@@ -297,7 +313,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
         for (int j = 0; j < 4; ++j) uh_next[j] = *reinterpret_cast<const uint4*>(ut + row_chunk(row, 4 * hc + j));
       }
       // U^T = U_hat^T - D_U on this thread's 32 columns
-      ok = wait_or_abort(bar_u, (uint32_t)(c & 1), abort_flag);
+      ok = wait_or_abort_t<GIVEUP>(bar_u, (uint32_t)(c & 1), abort_flag);
       if (!ok) break;
       tc_fence_after();
       {
@@ -320,7 +336,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
       tc_fence_before();
       mbar_arrive(u16_ready);
       // updated state -> fp16 copy (next chunk's A operand), then the next chunk's decay in place
-      ok = wait_or_abort(bar_s, (uint32_t)(c & 1), abort_flag);
+      ok = wait_or_abort_t<GIVEUP>(bar_s, (uint32_t)(c & 1), abort_flag);
       if (!ok) break;
       tc_fence_after();
       bool ckpt_now = false;
@@ -343,11 +359,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
         if (ckpt_now) {
           float* dst = p.ckpt + ((size_t)(ck_base + (ck_next - p.ckpt_chunks) / p.ckpt_chunks - 1) * H + h) * kCpMat;
 #pragma unroll
-          for (int j = 0; j < 64; ++j) dst[(size_t)(64 * hc + j) * 128 + row] = s[j];
+          for (int j = 0; j < 64; ++j) {
+            dst[(size_t)(64 * hc + j) * 128 + row] = s[j];
+            fsum += s[j];
+          }
         }
         if (c + 1 < ncs) {
           const int st1 = (int)((c + 1) % kStages);
-          ok = wait_or_abort(&full[st1], (uint32_t)(((c + 1) / kStages) & 1), abort_flag);
+          ok = wait_or_abort_t<GIVEUP>(&full[st1], (uint32_t)(((c + 1) / kStages) & 1), abort_flag);
           if (!ok) break;
           const float* gc = reinterpret_cast<const float*>(sm + st1 * kStage + kRecGC) + 64 * hc;
 #pragma unroll
@@ -363,14 +382,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
     float* dst = nullptr;
     if (MODE == 0 && seg == p_last) dst = p.hT ? p.hT + soff : nullptr;
     if (MODE == 1) dst = seg == 0 ? cpb + (3 + 2) * kCpMat : cpb + (kind == 1 ? 0 : kCpMat);  // S_in(1), or P_p / b_p
-    if (ok && !*abort_flag && dst != nullptr) {
+    if (segmap) dst = p.nseg == 1 ? (kind == 1 ? p.seg_P : p.seg_b) + (size_t)h * kCpMat : cpb + (kind == 1 ? 0 : kCpMat);
+    if (ok && !*abort_flag) {
       tc_fence_after();
       float s[64];
       tmem_ld64b(tl + T_S + 64 * hc, s);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) dst[(size_t)(64 * hc + c) * 128 + row] = s[c];
+      for (int c = 0; c < 64; ++c) fsum += s[c];
+      if (dst != nullptr) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) dst[(size_t)(64 * hc + c) * 128 + row] = s[c];
+      }
     }
     if (!ok) *abort_flag = 1;
+    if (!isfinite(fsum)) atomicOr(p.err, KDA_DEVERR_NONFINITE);
   } else if (MODE == 0) {
     // ======================== output warps: D_O -> staging -> epilogue -> global
     float* ost = reinterpret_cast<float*>(sm + S_OUT);
@@ -378,7 +403,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
     const int ow = warp - 8;
     bool ok = true;
     for (int64_t c = 0; c < ncs; ++c) {
-      ok = group_and(2, 128, wait_or_abort(bar_s, (uint32_t)(c & 1), abort_flag));
+      ok = group_and(2, 128, wait_or_abort_t<GIVEUP>(bar_s, (uint32_t)(c & 1), abort_flag));
       if (!ok) break;
       tc_fence_after();
       float o[64];
@@ -532,8 +557,9 @@ __global__ void __launch_bounds__(kMergeThreads, 1) kda_cp_merge(const ScanParam
   }
   if (!ok && tid == 0) {
     atomicOr(p.err, KDA_DEVERR_WAIT_TIMEOUT);
-    // let the copies in flight land (bounded) before the CTA's shared memory is released
-    for (int64_t s = 0; s < issued; ++s) mbar_wait(&bar[s & 1], (uint32_t)((s >> 1) & 1), 1u << 16);
+    // let the copies in flight land before the CTA's shared memory is released (each completes on
+    // its own; the wait keeps the default bound)
+    for (int64_t s = 0; s < issued; ++s) mbar_wait(&bar[s & 1], (uint32_t)((s >> 1) & 1));
   }
 }
 
@@ -558,33 +584,41 @@ cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, int threads, size_
 template <typename Tout>
 cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int32_t* plan, float* cp, int nseg,
                         int64_t seg_len, cudaStream_t st) {
-  static bool attr_done[64] = {};
+  static DeviceOnce once;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout, 0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kScanSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kda_tc_chunk_scan<Tout, 0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kda_cp_merge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMergeSmem);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  cudaError_t e0 = once.run(dev, [] {
+    void (*kernels[])(const ScanParams) = {kda_tc_chunk_scan<Tout, 0, false>, kda_tc_chunk_scan<Tout, 1, false>,
+                                           kda_tc_chunk_scan<Tout, 0, true>, kda_tc_chunk_scan<Tout, 0, false, true>,
+                                           kda_tc_chunk_scan<Tout, 1, false, true>};
+    for (auto* k : kernels) {
+      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaFuncSetAttribute(kda_cp_merge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMergeSmem);
+  });
+  if (e0 != cudaSuccess) return e0;
+  // the variants whose waits give up at once (abort-path tests) are used when asked for; the
+  // checkpointing pass has none
+  auto* mode0 = a.give_up ? kda_tc_chunk_scan<Tout, 0, false, true> : kda_tc_chunk_scan<Tout, 0, false>;
+  auto* mode1 = a.give_up ? kda_tc_chunk_scan<Tout, 1, false, true> : kda_tc_chunk_scan<Tout, 1, false>;
   ScanParams p;
   p.records = records; p.plan = plan; p.cu = a.cu_seqlens; p.B = a.B; p.T = a.T; p.H = a.H;
   p.h0 = a.h0; p.hT = a.hT; p.out = a.out; p.gate = static_cast<const __nv_bfloat16*>(a.epi.gate);
   p.norm_w = a.epi.norm_weight; p.eps = a.epi.eps; p.err = a.err;
   p.nseg = nseg; p.seg_len = seg_len; p.cp = cp;
   p.ckpt = a.ckpt; p.ckpt_chunks = a.ckpt_chunks;
+  p.seg_P = a.seg_P; p.seg_b = a.seg_b;
+  if (a.seg_P != nullptr) {
+    // segment map of one token range: both runs of every segment (one segment: P and b directly)
+    TraceScope ts("kda_tc_chunk_scan_segmap", st);
+    return launch_after(mode1, dim3((unsigned)a.H, 1, (unsigned)(2 * nseg)), kScanThreads, kScanSmem, st, p);
+  }
   if (nseg > 1) {
     {
       // segment 0 from h0, then b_p and P_p for 1 <= p <= nseg - 2
       TraceScope ts("kda_tc_chunk_scan_transition", st);
-      cudaError_t e = launch_after(kda_tc_chunk_scan<Tout, 1, false>,
-                                   dim3((unsigned)(a.B * a.H), 1, (unsigned)(2 * nseg - 3)), kScanThreads,
+      cudaError_t e = launch_after(mode1, dim3((unsigned)(a.B * a.H), 1, (unsigned)(2 * nseg - 3)), kScanThreads,
                                    kScanSmem, st, p);
       if (e != cudaSuccess) return e;
     }
@@ -598,7 +632,7 @@ cudaError_t launch_scan(const PrefillArgs& a, const uint8_t* records, const int3
   TraceScope ts("kda_tc_chunk_scan", st);
   const dim3 grid((unsigned)(a.B * a.H), 1, (unsigned)nseg);
   if (a.ckpt != nullptr) return launch_after(kda_tc_chunk_scan<Tout, 0, true>, grid, kScanThreads, kScanSmem, st, p);
-  return launch_after(kda_tc_chunk_scan<Tout, 0, false>, grid, kScanThreads, kScanSmem, st, p);
+  return launch_after(mode0, grid, kScanThreads, kScanSmem, st, p);
 }
 
 }  // namespace

@@ -123,6 +123,17 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   *abort_flag = 1;
   return false;
 }
+// The same wait in a kernel variant built to test the abort path: with kGiveUp it gives up at
+// once (raises the abort flag without polling), which is what a wait that runs out does.
+template <bool kGiveUp>
+__device__ __forceinline__ bool wait_or_abort_t(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if constexpr (kGiveUp) {
+    *abort_flag = 1;
+    return false;
+  } else {
+    return wait_or_abort(bar, parity, abort_flag);
+  }
+}
 
 }  // namespace tcx
 }  // namespace kda

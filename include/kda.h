@@ -26,6 +26,25 @@
  *     (either may be bf16 or fp32).  bf16 inputs run on the tensor-core path; fp32 inputs
  *     run on an fp32 CUDA-core path (slower, ~1e-6 relative error).  The read-out is
  *     computed in fp32 and rounded once when stored in out_dtype.
+ *   - Value range of the bf16 tensor-core path (prefill with dk = dv = 128): the values, the
+ *     intra-chunk terms built from them (beta v, U_hat = T V, U = U_hat - W S) and the running
+ *     state (h0 included) enter fp16 tensor-core operands, so each of |beta v|, |h0| and the
+ *     state's entries must stay below 65504 (keep them below ~1e4 for margin; accumulation is
+ *     fp32).  Past it the operand becomes inf, which reaches out and the state; the state pass
+ *     tests every final state it reaches (and each checkpoint) and sets KDA_DEVERR_NONFINITE (the
+ *     results are not valid; nothing traps).  Non-finite inputs set it too.  Values far below 1 (under ~6e-5 relative to the state) lose precision as fp16
+ *     subnormals.  The recurrence is linear in (v, h0) jointly, so a caller with larger or tiny
+ *     values can scale v and h0 by one factor and divide out and hT by it.  Keys and queries
+ *     (unit norm) and the decays need no such care.  The fp32 paths have fp32 range.
+ *   - Debugging: with the environment variable KDA_DEBUG_CHECKS set (any value but "" or "0";
+ *     read at every call), kda_chunk_fwd*, kda_chunk_fwd_segment_map and kda_decode_* first run
+ *     a check kernel over the inputs and set KDA_DEVERR_PRECONDITION when g is outside (-5, 0],
+ *     beta outside [0, 1], or (decode) two requests name the same slot.  The check reads every
+ *     g and beta once (decode: O(N^2) slot comparisons); it is off by default.
+ *   - Testing: with the environment variable KDA_TEST_WAIT_TIMEOUT set (any value but "" or "0";
+ *     read at every call) the prefill launches kernel variants whose bounded waits on work of
+ *     their own CTA give up at once, so that a test can make them run out and see
+ *     KDA_DEVERR_WAIT_TIMEOUT reported with the device left usable.  Not for production use.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -56,6 +75,8 @@ typedef enum {
 #define KDA_DEVERR_BAD_SEQLENS  0x2u  /* prefill: cu_seqlens not non-decreasing in [0, T]  */
 #define KDA_DEVERR_WAIT_TIMEOUT 0x4u  /* a bounded device-side wait gave up                */
 #define KDA_DEVERR_BAD_COUNT    0x8u  /* decode_multi: ntok_per_req[n] outside [0, n_tok]   */
+#define KDA_DEVERR_NONFINITE   0x10u /* tensor-core path wrote a non-finite out / state value */
+#define KDA_DEVERR_PRECONDITION 0x20u /* KDA_DEBUG_CHECKS: g, beta or slot_idx broke a precondition */
 
 /* Optional fused epilogue (section 3.3, Eq. 6): RMSNorm over dv per (token, head), then
  * the sigmoid output gate.  The norm is taken on the fp32 read-out before rounding.
@@ -185,6 +206,39 @@ kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, const floa
                          float* dg, float* dbeta, float* dh0, int B, int64_t T, int H, int dk,
                          int dv, kda_dtype dtype, void* workspace, size_t workspace_bytes,
                          void* stream);
+
+/* Context parallelism across devices (section 13.3.2, KCP; open-day article section 5.2).  A long
+ * sequence is split into consecutive token ranges, one per device.  Over a range the state pass is
+ * affine in the range's initial state: S_out = P S_in + b, with P the range's accumulated transition
+ * and b its final state from a zero initial state.  Each device computes the map of its range, the
+ * devices exchange these fixed-size maps (an all-gather of H * (dk*dk + dk*dv) fp32 values each),
+ * each folds the maps of the ranges before its own into its initial state with kda_state_compose,
+ * then runs kda_chunk_fwd on its range from that state.
+ *
+ * kda_chunk_fwd_segment_map: the map (P, b) of one token range of one sequence, all H heads.
+ *   k, v, g, beta : the range's tokens: [T, H, dk], [T, H, dv] (dtype), [T, H, dk] fp32, [T, H] fp32
+ *                   (no q: the map does not depend on it)
+ *   P             : [H, dk, dk] fp32, written: S_out = P S_in + b for every initial state S_in
+ *   b             : [H, dk, dv] fp32, written: the range's final state from S_in = 0
+ *   workspace     : at least kda_chunk_fwd_workspace_size(1, T, H, dk, dv, C, dtype) bytes, 256-byte
+ *                   aligned
+ * T = 0 gives P = I and b = 0.  Supported: bf16 inputs with dk = dv = 128 (else KDA_ERR_UNSUPPORTED).
+ * The range runs as one serial pass per head (two runs: from 0 and, for P, from I).
+ * Other errors as for kda_chunk_fwd. */
+kda_status kda_chunk_fwd_segment_map(const void* k, const void* v, const float* g, const float* beta,
+                                     float* P, float* b, int64_t T, int H, int dk, int dv, int C,
+                                     kda_dtype dtype, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/* kda_state_compose: the initial state of the range that follows n ranges with maps (P[i], b[i]),
+ *   S_out = P[n-1] ( ... (P[0] S0 + b[0]) ... ) + b[n-1],
+ * in fp32 on the device.
+ *   P     : [n, H, dk, dk] fp32;  b : [n, H, dk, dv] fp32   (maps in token order)
+ *   S0    : [H, dk, dv] fp32, or NULL for a zero state;  S_out : [H, dk, dv] fp32, may alias S0
+ * n = 0 copies S0 (or writes zeros).  dk, dv in {64, 128}; all pointers 16-byte aligned device
+ * memory (KDA_ERR_INVALID_ARG otherwise). */
+kda_status kda_state_compose(const float* P, const float* b, const float* S0, float* S_out, int n, int H,
+                             int dk, int dv, void* stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error word into
  * *flags (KDA_DEVERR_* bits).  Returns KDA_OK, or KDA_ERR_CUDA if the sync failed. */
