@@ -23,28 +23,38 @@
 // Two kernels:
 //   chunk_prep_cc : one CTA per (chunk, head), fully parallel; writes the chunk's
 //                   W, U_hat, Q_hat, K_bar, M and exp(G_last) into the workspace.
-//   chunk_scan_cc : one CTA per (sequence, head); walks the chunks in order keeping
-//                   the dk x dv state in shared memory; writes outputs (with the
-//                   optional RMSNorm + sigmoid gate epilogue) and the final state.
+//   chunk_scan_cc : one cluster of dv / 16 CTAs per (sequence, head), each walking the
+//                   chunks in order with 16 value columns of the state in shared memory;
+//                   writes outputs (with the optional RMSNorm + sigmoid gate epilogue) and
+//                   the final state.
 #include <algorithm>
 
 #include "kda_device.cuh"
 #include "kda_internal.h"
+#include "tc_ptx.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
 
+// One (chunk, head) record of the chunkwise operands in the workspace, laid out as the serial
+// pass's shared-memory image: row pitches of 4 floats past a multiple of 32 keep that pass's
+// row-parallel float4 reads free of bank conflicts, and one bulk copy moves W .. Gamma while a
+// second moves the CTA's 16-column slice of U_hat (stored slice-major).
 template <int DK, int DV>
-struct CcBlob {  // fp32 offsets inside one (chunk, head) record
-  static constexpr size_t W = 0;
-  static constexpr size_t UH = W + 64 * DK;
-  static constexpr size_t QH = UH + 64 * DV;
-  static constexpr size_t KB = QH + 64 * DK;
-  static constexpr size_t M = KB + 64 * DK;
-  static constexpr size_t GC = M + 64 * 64;
-  static constexpr size_t FLOATS = (GC + DK + 63) / 64 * 64;
+struct CcBlob {
+  static constexpr int NC = 16, NS = DV / NC;             // value-column slices of the serial pass
+  static constexpr int PK = DK + 4, PR = 68, PC = NC + 4;  // row pitches in floats (16-byte multiples)
+  static constexpr int W = 0;                              // [64][PK]
+  static constexpr int QH = W + 64 * PK;                   // [64][PK]
+  static constexpr int KBT = QH + 64 * PK;                 // K_bar transposed: [DK][PR]
+  static constexpr int M = KBT + DK * PR;                  // [64][PR], lower triangular
+  static constexpr int GC = M + 64 * PR;                   // exp(G_last): [DK]
+  static constexpr int HEAD = GC + DK;                     // floats of the first bulk copy
+  static constexpr int UH = HEAD;                          // [NS][64][PC]
+  static constexpr int SLICE = 64 * PC;
+  static constexpr int FLOATS = (UH + NS * SLICE + 63) / 64 * 64;
 };
 
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
@@ -54,9 +64,10 @@ __device__ __forceinline__ float comp(const float4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
-// C[64][N] (global, row-major) = T[64][64] (smem, pitch 65) x Bm[64][N] (smem, pitch PB)
-template <int N>
-__device__ __forceinline__ void tmul_store(const float* sT, const float* sB, int PB, float* outg) {
+// C[64][N] = T[64][64] (smem, pitch 65) x Bm[64][N] (smem, pitch PB), element (r, j) of C stored
+// at outg[at(r, j)] (j a multiple of 4: four consecutive floats)
+template <int N, typename At>
+__device__ __forceinline__ void tmul_store(const float* sT, const float* sB, int PB, float* outg, At at) {
   const int rr = threadIdx.x / 16, cc = (threadIdx.x % 16) * 4;
   constexpr int JB = N / 64;
   float4 acc[4][JB];
@@ -79,13 +90,33 @@ __device__ __forceinline__ void tmul_store(const float* sT, const float* sB, int
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int jb = 0; jb < JB; ++jb)
-      *reinterpret_cast<float4*>(&outg[(size_t)(rr + 16 * i) * N + cc + 64 * jb]) = acc[i][jb];
+      *reinterpret_cast<float4*>(&outg[at(rr + 16 * i, cc + 64 * jb)]) = acc[i][jb];
 }
 
 template <int DK, int DV>
 constexpr int prep_smem_floats() {
   constexpr int PM = (DK > DV ? DK : DV) + 4;
-  return 64 * PM * 4 + 32 * PM + 64 * 65 + 64;
+  return 64 * PM * 4 + 32 * PM + 64 * 65 + 3 * DK + 64;
+}
+
+// 2^x: the decays are carried in log2 units (e^G = 2^(G log2 e)), so every factor is one ex2
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 16 bytes of raw input elements -> fp32 in shared memory
+__device__ __forceinline__ void store_f32(float* dst, const uint4& raw, float) {
+  *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(&raw);
+}
+__device__ __forceinline__ void store_f32(float* dst, const uint4& raw, __nv_bfloat16) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&raw);
+  const float2 a = __bfloat1622float2(p[0]), b = __bfloat1622float2(p[1]);
+  const float2 c = __bfloat1622float2(p[2]), d = __bfloat1622float2(p[3]);
+  *reinterpret_cast<float4*>(dst) = make_float4(a.x, a.y, b.x, b.y);
+  *reinterpret_cast<float4*>(dst + 4) = make_float4(c.x, c.y, d.x, d.y);
 }
 
 template <int DK, int DV, typename Tin>
@@ -96,14 +127,19 @@ chunk_prep_cc(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
               int H, float* __restrict__ blob_base) {
   using L = CcBlob<DK, DV>;
   constexpr int PM = (DK > DV ? DK : DV) + 4;
+  constexpr int VE = 16 / (int)sizeof(Tin);          // input elements per 16-byte load
+  constexpr int NLK = 64 * DK / VE / kThreads;       // loads of k (and of q) per thread
+  constexpr int NLV = 64 * DV / VE / kThreads;
+  constexpr int NLG = 64 * DK / 4 / kThreads;
   extern __shared__ float4 smem4[];
-  float* sG = reinterpret_cast<float*>(smem4);  // [64][PM] cumulative log-decay
-  float* sKL = sG + 64 * PM;                     // [64][PM] k * exp(G - R(r)); later K_hat
-  float* sQL = sKL + 64 * PM;                    // [64][PM] q * exp(G - R(r)); later V
-  float* sKR = sQL + 64 * PM;                    // [64][PM] k * exp(R(s) - G); later T
-  float* sKX = sKR + 64 * PM;                    // [32][PM] k * exp(G_47 - G), s < 32
-  float* sA = sKX + 32 * PM;                     // [64][65]
-  float* sBeta = sA + 64 * 65;                   // [64]
+  float* sG = reinterpret_cast<float*>(smem4);  // [64][PM] g, then G (log2 units), then K_hat
+  float* sK = sG + 64 * PM;                      // [64][PM] k, then k * 2^(G - R(r))
+  float* sQ = sK + 64 * PM;                      // [64][PM] q, then q * 2^(G - R(r)), then V
+  float* sKR = sQ + 64 * PM;                     // [64][PM] k * 2^(R(s) - G), then T (pitch 65)
+  float* sKX = sKR + 64 * PM;                    // [32][PM] k * 2^(G_47 - G), s < 32
+  float* sA = sKX + 32 * PM;                     // [64][65]; first the cumulative sums' part totals
+  float* sRef = sA + 64 * 65;                    // [3][DK] G at rows 15, 47, 63
+  float* sBeta = sRef + 3 * DK;                  // [64]
 
   const int64_t chunk = blockIdx.x;
   const int h = blockIdx.y;
@@ -113,35 +149,96 @@ chunk_prep_cc(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   float* blob = blob_base + ((size_t)chunk * H + h) * L::FLOATS;
   const int tid = threadIdx.x;
 
-  // 1. cumulative log-decay per key channel (padding rows: g = 0, so G stays flat)
-  for (int c = tid; c < DK; c += kThreads) {
-    float acc = 0.f;
-    for (int r = 0; r < 64; ++r) {
-      const float gv = (r < n) ? g[((size_t)(t0 + r) * H + h) * DK + c] : 0.f;
-      acc += gv;
-      sG[r * PM + c] = acc;
-    }
+  // 1. the raw tiles (rows n..63 zero; g = 0 there keeps G flat), every load issued before use;
+  //    v stays in registers until its shared-memory buffer is free
+  float4 rg[NLG];
+  uint4 rk[NLK], rq[NLK], rv[NLV];
+#pragma unroll
+  for (int j = 0; j < NLG; ++j) {
+    const int i = tid + j * kThreads, r = i / (DK / 4), c4 = (i % (DK / 4)) * 4;
+    rg[j] = r < n ? __ldg(reinterpret_cast<const float4*>(g + ((size_t)(t0 + r) * H + h) * DK + c4))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int j = 0; j < NLK; ++j) {
+    const int i = tid + j * kThreads, r = i / (DK / VE), e0 = (i % (DK / VE)) * VE;
+    const size_t gi = ((size_t)(t0 + r) * H + h) * DK + e0;
+    rk[j] = r < n ? __ldg(reinterpret_cast<const uint4*>(k + gi)) : make_uint4(0u, 0u, 0u, 0u);
+    rq[j] = r < n ? __ldg(reinterpret_cast<const uint4*>(q + gi)) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int j = 0; j < NLV; ++j) {
+    const int i = tid + j * kThreads, r = i / (DV / VE), e0 = (i % (DV / VE)) * VE;
+    rv[j] = r < n ? __ldg(reinterpret_cast<const uint4*>(v + ((size_t)(t0 + r) * H + h) * DV + e0))
+                  : make_uint4(0u, 0u, 0u, 0u);
   }
   if (tid < 64) sBeta[tid] = (tid < n) ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
-  __syncthreads();
-
-  // 2. reference-scaled operands for A and M
-  for (int idx = tid; idx < 64 * DK; idx += kThreads) {
-    const int r = idx / DK, c = idx % DK;
-    const size_t gi = ((size_t)(t0 + r) * H + h) * DK + c;
-    const float kv = (r < n) ? to_f32(k[gi]) : 0.f;
-    const float qv = (r < n) ? to_f32(q[gi]) : 0.f;
-    const float G = sG[r * PM + c];
-    const float R = sG[(r < 32 ? 15 : 47) * PM + c];
-    const float ef = expf(G - R), eb = expf(R - G);
-    sKL[r * PM + c] = kv * ef;
-    sQL[r * PM + c] = qv * ef;
-    sKR[r * PM + c] = kv * eb;
-    if (r < 32) sKX[r * PM + c] = kv * expf(sG[47 * PM + c] - G);
+#pragma unroll
+  for (int j = 0; j < NLG; ++j) {
+    const int i = tid + j * kThreads, r = i / (DK / 4), c4 = (i % (DK / 4)) * 4;
+    *reinterpret_cast<float4*>(&sG[r * PM + c4]) =
+        make_float4(rg[j].x * kLog2e, rg[j].y * kLog2e, rg[j].z * kLog2e, rg[j].w * kLog2e);
+  }
+#pragma unroll
+  for (int j = 0; j < NLK; ++j) {
+    const int i = tid + j * kThreads, r = i / (DK / VE), e0 = (i % (DK / VE)) * VE;
+    store_f32(&sK[r * PM + e0], rk[j], Tin());
+    store_f32(&sQ[r * PM + e0], rq[j], Tin());
   }
   __syncthreads();
 
-  // 3. A (strict lower, row-scaled by beta) and M (lower incl. diagonal)
+  // 2. cumulative log-decay per channel: each of the 256 / DK parts of a channel's rows sums its
+  //    own rows, then adds the totals of the parts above it
+  {
+    constexpr int P = kThreads / DK, RP = 64 / P;
+    const int c = tid % DK, part = tid / DK;
+    float run = 0.f;
+#pragma unroll
+    for (int i = 0; i < RP; ++i) {
+      float& x = sG[(part * RP + i) * PM + c];
+      run += x;
+      x = run;
+    }
+    sA[part * DK + c] = run;
+    __syncthreads();
+    float off = 0.f;
+    for (int p = 0; p < part; ++p) off += sA[p * DK + c];
+    if (part > 0)
+#pragma unroll
+      for (int i = 0; i < RP; ++i) sG[(part * RP + i) * PM + c] += off;
+    __syncthreads();
+    if (tid < DK) {
+      sRef[tid] = sG[15 * PM + tid];
+      sRef[DK + tid] = sG[47 * PM + tid];
+      sRef[2 * DK + tid] = sG[63 * PM + tid];
+    }
+    __syncthreads();
+  }
+
+  // 3. K_bar^T = (k * 2^(G_63 - G))^T into the record (rows fastest, for coalesced stores) and
+  //    exp(G_last); then the reference-scaled operands of A and M, K_hat and Q_hat, each element
+  //    in place by the one thread that owns it
+  for (int idx = tid; idx < 64 * DK; idx += kThreads) {
+    const int r = idx % 64, c = idx / 64;
+    blob[L::KBT + c * L::PR + r] = sK[r * PM + c] * ex2(sRef[2 * DK + c] - sG[r * PM + c]);
+  }
+  if (tid < DK) blob[L::GC + tid] = ex2(sRef[2 * DK + tid]);
+  __syncthreads();
+  for (int idx = tid; idx < 64 * DK; idx += kThreads) {
+    const int r = idx / DK, c = idx % DK;
+    const float G = sG[r * PM + c], R = sRef[(r < 32 ? 0 : DK) + c];
+    const float kv = sK[r * PM + c], qv = sQ[r * PM + c];
+    const float ef = ex2(G - R), eG = ex2(G);
+    sK[r * PM + c] = kv * ef;
+    sQ[r * PM + c] = qv * ef;
+    sKR[r * PM + c] = kv * ex2(R - G);
+    if (r < 32) sKX[r * PM + c] = kv * ex2(sRef[DK + c] - G);
+    sG[r * PM + c] = kv * eG;
+    blob[L::QH + r * L::PK + c] = qv * eG;
+  }
+  __syncthreads();
+
+  // 4. A (strict lower, row-scaled by beta) and M (lower incl. diagonal)
   {
     const int rr = tid / 16, ss = tid % 16;
     float accA[4][4], accM[4][4];
@@ -153,8 +250,8 @@ chunk_prep_cc(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       float4 kl[4], ql[4], kr[4], kx[2];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        kl[i] = *reinterpret_cast<const float4*>(&sKL[(rr + 16 * i) * PM + c]);
-        ql[i] = *reinterpret_cast<const float4*>(&sQL[(rr + 16 * i) * PM + c]);
+        kl[i] = *reinterpret_cast<const float4*>(&sK[(rr + 16 * i) * PM + c]);
+        ql[i] = *reinterpret_cast<const float4*>(&sQ[(rr + 16 * i) * PM + c]);
         kr[i] = *reinterpret_cast<const float4*>(&sKR[(ss + 16 * i) * PM + c]);
       }
 #pragma unroll
@@ -175,32 +272,19 @@ chunk_prep_cc(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       for (int j = 0; j < 4; ++j) {
         const int r = rr + 16 * i, s = ss + 16 * j;
         sA[r * 65 + s] = (s < r) ? sBeta[r] * accA[i][j] : 0.f;
-        blob[L::M + r * 64 + s] = (s <= r) ? accM[i][j] : 0.f;
+        blob[L::M + r * L::PR + s] = (s <= r) ? accM[i][j] : 0.f;
       }
   }
   __syncthreads();
 
-  // 4. K_hat and V into shared memory; Q_hat, K_bar, exp(G_last) into the blob
-  float* sKH = sKL;
-  float* sV = sQL;
-  for (int idx = tid; idx < 64 * DK; idx += kThreads) {
-    const int r = idx / DK, c = idx % DK;
-    const size_t gi = ((size_t)(t0 + r) * H + h) * DK + c;
-    const float kv = (r < n) ? to_f32(k[gi]) : 0.f;
-    const float qv = (r < n) ? to_f32(q[gi]) : 0.f;
-    const float G = sG[r * PM + c];
-    const float eG = expf(G);
-    sKH[r * PM + c] = kv * eG;
-    blob[L::QH + r * DK + c] = qv * eG;
-    blob[L::KB + r * DK + c] = kv * expf(sG[63 * PM + c] - G);
+  // 5. V into shared memory (over q * 2^(G - R)); T = (I + A)^-1 Diag(beta) by forward
+  //    substitution, 4 threads per column s (over k * 2^(R - G))
+  float* sV = sQ;
+#pragma unroll
+  for (int j = 0; j < NLV; ++j) {
+    const int i = tid + j * kThreads, r = i / (DV / VE), e0 = (i % (DV / VE)) * VE;
+    store_f32(&sV[r * PM + e0], rv[j], Tin());
   }
-  for (int idx = tid; idx < 64 * DV; idx += kThreads) {
-    const int r = idx / DV, j = idx % DV;
-    sV[r * PM + j] = (r < n) ? to_f32(v[((size_t)(t0 + r) * H + h) * DV + j]) : 0.f;
-  }
-  for (int c = tid; c < DK; c += kThreads) blob[L::GC + c] = expf(sG[63 * PM + c]);
-
-  // 5. T = (I + A)^-1 Diag(beta): forward substitution, 4 threads per column s
   float* sT = sKR;
   {
     const int s = tid >> 2, part = tid & 3;
@@ -227,13 +311,76 @@ chunk_prep_cc(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   __syncthreads();
 
   // 6. W = T K_hat, U_hat = T V
-  tmul_store<DK>(sT, sKH, PM, blob + L::W);
-  tmul_store<DV>(sT, sV, PM, blob + L::UH);
+  tmul_store<DK>(sT, sG, PM, blob, [](int r, int j) { return L::W + r * L::PK + j; });
+  tmul_store<DV>(sT, sV, PM, blob,
+                 [](int r, int j) { return L::UH + (j / L::NC) * L::SLICE + r * L::PC + j % L::NC; });
 }
 
+// ------------------------------------------------------------------ serial state pass
+// The recurrence is separable in the value columns: column j of U, O and S involves only column
+// j of U_hat and of S.  A chain therefore runs as a thread-block cluster of NS = dv / 16 CTAs,
+// each owning 16 value columns of the state; every CTA reads the chunk's W, Q_hat, K_bar^T and M
+// (the repeats hit L2).  The one exchange is the RMSNorm's sum of squares over a token's dv
+// outputs (gate epilogue only): each CTA stores its 16-column partial sums into every CTA of the
+// cluster (distributed shared memory) with a remote mbarrier arrival, and normalises a chunk's
+// outputs one chunk later, so that the exchange overlaps the next chunk's products.  The next
+// chunk's record arrives by bulk copy while the current one is used (two stages where shared
+// memory allows).
 template <int DK, int DV>
-constexpr int scan_smem_floats() {
-  return DK * (DV + 4) + 64 * (DV + 4) + 64 * (DK + 4) + 64 * 68 + DK;
+struct CcScan {
+  using L = CcBlob<DK, DV>;
+  static constexpr int NSLOT = 4;   // partial-sum slots in flight (a peer runs at most 2 chunks ahead)
+  static constexpr int PST = DK + 4, PUT = 68;        // pitches of the transposed state and U
+  static constexpr int STAGE = L::HEAD + L::SLICE;    // record image + this CTA's U_hat slice
+  static constexpr int EXTRA = L::NC * PST + L::NC * PUT + 4 * 64 + NSLOT * L::NS * 64;
+  static constexpr size_t bytes(int stages) {
+    return ((size_t)stages * STAGE + EXTRA) * sizeof(float) + (2 + NSLOT) * sizeof(uint64_t);
+  }
+  static constexpr int STAGES = bytes(2) <= 227 * 1024 ? 2 : 1;
+  static constexpr size_t SMEM = bytes(STAGES);
+};
+
+// d = a * b + c on two fp32 lanes at once (one packed instruction, each lane rounded as fmaf)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 lo2(const float4& v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(const float4& v) { return make_float2(v.z, v.w); }
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// the address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(tc::smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 template <int DK, int DV, typename Tin, typename Tout>
@@ -241,204 +388,251 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ plan,
               const int32_t* __restrict__ cu, int B, int64_t T, int H, const float* __restrict__ h0,
               float* __restrict__ hT, Tout* __restrict__ out, const Tin* __restrict__ gate,
-              const float* __restrict__ norm_w, float eps, float* __restrict__ ckpt, int64_t ckpt_chunks) {
+              const float* __restrict__ norm_w, float eps, float* __restrict__ ckpt, int64_t ckpt_chunks,
+              unsigned int* __restrict__ err) {
   using L = CcBlob<DK, DV>;
-  constexpr int PSV = DV + 4, PSK = DK + 4, JB = DV / 64, SI = DK / 16;
+  using Sc = CcScan<DK, DV>;
+  constexpr int NC = L::NC, NS = L::NS, PK = L::PK, PR = L::PR, PC = L::PC, KR = DK / 64;
+  constexpr int PST = Sc::PST, PUT = Sc::PUT, NSLOT = Sc::NSLOT, STAGES = Sc::STAGES;
   extern __shared__ float4 smem4[];
-  float* sS = reinterpret_cast<float*>(smem4);  // [DK][PSV] state
-  float* sU = sS + DK * PSV;                     // [64][PSV] U_hat, then U
-  float* sX = sU + 64 * PSV;                     // [64][PSK] W, then Q_hat, then K_bar
-  float* sM = sX + 64 * PSK;                     // [64][68]
-  float* sGam = sM + 64 * 68;                    // [DK]
+  float* stages = reinterpret_cast<float*>(smem4);
+  float* sST = stages + STAGES * Sc::STAGE;  // [NC][PST] this CTA's 16 state columns, transposed
+  float* sUT = sST + NC * PST;               // [NC][PUT] U, transposed
+  float* sPart = sUT + NC * PUT;             // [4][64] sums of squares of each 4-column group
+  float* sSlot = sPart + 4 * 64;             // [NSLOT][NS][64] 16-column sums from each CTA
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSlot + NSLOT * NS * 64);  // [2] stage landed
+  uint64_t* slot_bar = full + 2;                                         // [NSLOT] slot filled
 
-  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
-  if (cu != nullptr && plan[B + 1] == 0) return;  // invalid cu_seqlens: sequence skipped
+  const int tid = threadIdx.x;
+  if (cu != nullptr && plan[B + 1] == 0) return;  // invalid cu_seqlens: every CTA returns
+  const int slice = (int)cluster_ctarank();       // = blockIdx.x % NS
+  const int h = blockIdx.y;
+  const int b = sequence_of_rank(blockIdx.x / NS, plan, cu, B);
   int64_t first_chunk, t_begin, len;
   const int64_t nchunks = sequence_chunks(b, plan, cu, B, T, first_chunk, t_begin, len);
+  const bool epi = gate != nullptr;
+  const int col0 = slice * NC;
 
-  const size_t soff = ((size_t)b * H + h) * DK * DV;
-  const int64_t ck_base = ckpt != nullptr ? checkpoint_base(b, cu, T, 64 * ckpt_chunks) : 0;
-  for (int idx = tid; idx < DK * DV; idx += kThreads) {
-    const int r = idx / DV, j = idx % DV;
-    sS[r * PSV + j] = h0 ? h0[soff + idx] : 0.f;
+  if (tid == 0) {
+    tc::mbar_init(&full[0], 1);
+    tc::mbar_init(&full[1], 1);
+    for (int i = 0; i < NSLOT; ++i) tc::mbar_init(&slot_bar[i], 64 * NS);
+    tc::mbar_fence_init();
   }
-  __syncthreads();
+  if (epi) cluster_sync_all();  // every CTA's barriers exist before the first remote arrival
+  else __syncthreads();
 
-  const int rr = tid / 16, cc = (tid % 16) * 4;
-  for (int64_t c = 0; c < nchunks; ++c) {
+  // thread = (row r, columns c4..c4+3 of the slice); a warp holds 32 rows of one column group,
+  // so its reads of the state and of U are broadcasts.  State rows r + 64 i.
+  const int cg = tid >> 6, r = (tid & 31) + 32 * ((tid >> 5) & 1), c4 = cg * 4;
+  const size_t soff = ((size_t)b * H + h) * DK * DV;
+  float4 sreg[KR];
+#pragma unroll
+  for (int i = 0; i < KR; ++i) {
+    const size_t o = soff + (size_t)(r + 64 * i) * DV + col0 + c4;
+    sreg[i] = h0 ? make_float4(h0[o], h0[o + 1], h0[o + 2], h0[o + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sST[(c4 + j) * PST + r + 64 * i] = comp(sreg[i], j);
+  }
+  const int64_t ck_base = ckpt != nullptr ? checkpoint_base(b, cu, T, 64 * ckpt_chunks) : 0;
+  float nw[4] = {1.f, 1.f, 1.f, 1.f};
+  if (epi && norm_w != nullptr)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) nw[j] = norm_w[col0 + c4 + j];
+
+  // one thread stages chunk c's record image and U_hat slice
+  auto issue = [&](int64_t c) {
+    const int st = STAGES == 2 ? (int)(c & 1) : 0;
     const float* blob = blob_base + ((size_t)(first_chunk + c) * H + h) * L::FLOATS;
+    float* d = stages + st * Sc::STAGE;
+    tc::fence_proxy_async_smem();
+    tc::mbar_arrive_expect_tx(&full[st], Sc::STAGE * sizeof(float));
+    tc::bulk_g2s(d, blob, L::HEAD * sizeof(float), &full[st]);
+    tc::bulk_g2s(d + L::HEAD, blob + L::UH + slice * L::SLICE, L::SLICE * sizeof(float), &full[st]);
+  };
+
+  bool waits_ok = true;
+  auto wait_bar = [&](uint64_t* bar, uint32_t parity, bool cluster_scope) {
+    if (!waits_ok) return;
+    bool ok = false;
+    for (uint32_t i = 0; i < 20000000u && !ok; ++i)
+      ok = cluster_scope ? mbar_try_wait_cluster(bar, parity) : tc::mbar_try_wait(bar, parity);
+    if (!ok) {
+      atomicOr(err, KDA_DEVERR_WAIT_TIMEOUT);
+      waits_ok = false;
+    }
+  };
+  auto rows_of = [&](int64_t c) {
     const int64_t rem = len - 64 * c;
-    const int n = (int)(rem < 64 ? rem : 64);
-    const int64_t t0 = t_begin + 64 * c;
-
-    // a. W -> sX, U_hat -> sU, exp(G_last) -> sGam
-    for (int idx = tid; idx < 64 * DK / 4; idx += kThreads) {
-      const int r = idx / (DK / 4), c4 = (idx % (DK / 4)) * 4;
-      *reinterpret_cast<float4*>(&sX[r * PSK + c4]) = *reinterpret_cast<const float4*>(&blob[L::W + r * DK + c4]);
+    return (int)(rem < 64 ? rem : 64);
+  };
+  // epilogue: the 16-column sum of squares of chunk c's row r (from the four column groups) into
+  // slot c % NSLOT of every CTA of the cluster; one thread per row
+  auto send = [&](int64_t c) {
+    const float ss = sPart[r] + sPart[64 + r] + sPart[128 + r] + sPart[192 + r];
+    const int sl = (int)(c % NSLOT);
+    const uint32_t slot = tc::smem_u32(&sSlot[(sl * NS + slice) * 64 + r]);
+    const uint32_t bar = tc::smem_u32(&slot_bar[sl]);
+#pragma unroll
+    for (int p = 0; p < NS; ++p) st_cluster_f32(cluster_map(slot, (uint32_t)p), ss);
+#pragma unroll
+    for (int p = 0; p < NS; ++p) mbar_arrive_cluster(cluster_map(bar, (uint32_t)p));
+  };
+  auto store = [&](int64_t c, const float (&o)[4], const float (&gv)[4]) {
+    float scale = 1.f;
+    if (epi) {
+      const int sl = (int)(c % NSLOT);
+      wait_bar(&slot_bar[sl], (uint32_t)((c / NSLOT) & 1), true);
+      float tot = 0.f;
+#pragma unroll
+      for (int p = 0; p < NS; ++p) tot += sSlot[(sl * NS + p) * 64 + r];
+      scale = rsqrtf(tot / (float)DV + eps);
     }
-    for (int idx = tid; idx < 64 * DV / 4; idx += kThreads) {
-      const int r = idx / (DV / 4), c4 = (idx % (DV / 4)) * 4;
-      *reinterpret_cast<float4*>(&sU[r * PSV + c4]) = *reinterpret_cast<const float4*>(&blob[L::UH + r * DV + c4]);
-    }
-    for (int i = tid; i < DK; i += kThreads) sGam[i] = blob[L::GC + i];
-    __syncthreads();
-
-    // b. U = U_hat - W S
-    {
-      float4 acc[4][JB];
+    if (r < rows_of(c)) {
+      const size_t orow = ((size_t)(t_begin + 64 * c + r) * H + h) * DV + col0 + c4;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int jb = 0; jb < JB; ++jb)
-          acc[i][jb] = *reinterpret_cast<const float4*>(&sU[(rr + 16 * i) * PSV + cc + 64 * jb]);
-      for (int c4 = 0; c4 < DK; c4 += 4) {
-        float4 w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const float4*>(&sX[(rr + 16 * i) * PSK + c4]);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int jb = 0; jb < JB; ++jb) {
-            const float4 sv = *reinterpret_cast<const float4*>(&sS[(c4 + u) * PSV + cc + 64 * jb]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i][jb] = f4_fma(-comp(w[i], u), sv, acc[i][jb]);
-          }
+      for (int j = 0; j < 4; ++j) {
+        float y = o[j];
+        if (epi) y = y * scale * nw[j] * sigmoidf_(gv[j]);
+        out[orow + j] = from_f32<Tout>(y);
       }
-      __syncthreads();  // all reads of sX (W) done
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int jb = 0; jb < JB; ++jb)
-          *reinterpret_cast<float4*>(&sU[(rr + 16 * i) * PSV + cc + 64 * jb]) = acc[i][jb];
     }
-    // c. Q_hat -> sX, M -> sM
-    for (int idx = tid; idx < 64 * DK / 4; idx += kThreads) {
-      const int r = idx / (DK / 4), c4 = (idx % (DK / 4)) * 4;
-      *reinterpret_cast<float4*>(&sX[r * PSK + c4]) = *reinterpret_cast<const float4*>(&blob[L::QH + r * DK + c4]);
-    }
-    for (int idx = tid; idx < 64 * 16; idx += kThreads) {
-      const int r = idx / 16, c4 = (idx % 16) * 4;
-      *reinterpret_cast<float4*>(&sM[r * 68 + c4]) = *reinterpret_cast<const float4*>(&blob[L::M + r * 64 + c4]);
-    }
-    __syncthreads();
+  };
 
-    // d. O = Q_hat S + M U
-    float4 o[4][JB];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int jb = 0; jb < JB; ++jb) o[i][jb] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c4 = 0; c4 < DK; c4 += 4) {
-      float4 qq[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) qq[i] = *reinterpret_cast<const float4*>(&sX[(rr + 16 * i) * PSK + c4]);
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int jb = 0; jb < JB; ++jb) {
-          const float4 sv = *reinterpret_cast<const float4*>(&sS[(c4 + u) * PSV + cc + 64 * jb]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) o[i][jb] = f4_fma(comp(qq[i], u), sv, o[i][jb]);
-        }
+  if (tid == 0 && nchunks > 0) issue(0);
+  float o_prev[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int64_t c = 0; c < nchunks; ++c) {
+    const int st = STAGES == 2 ? (int)(c & 1) : 0;
+    const float* d = stages + st * Sc::STAGE;
+    __syncthreads();  // chunk c - 1 is done with the state, U, the partial sums and (one stage) the record
+    if (tid == 0) {
+      if (STAGES == 2 && c + 1 < nchunks) issue(c + 1);
+      if (STAGES == 1 && c > 0) issue(c);
     }
+    float gv[4] = {0.f, 0.f, 0.f, 0.f};  // gate of chunk c - 1, whose outputs leave at the end of chunk c
+    if (epi && c > 0) {
+      if (cg == 0) send(c - 1);
+      if (r < rows_of(c - 1)) {
+        const size_t orow = ((size_t)(t_begin + 64 * (c - 1) + r) * H + h) * DV + col0 + c4;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) gv[j] = to_f32(gate[orow + j]);
+      }
+    }
+    wait_bar(&full[st], (uint32_t)((c / STAGES) & 1), false);
+
+    // W S and Q_hat S in one pass over the state rows, pairing k and k + 1
+    float2 ws[4], os[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ws[j] = os[j] = make_float2(0.f, 0.f);
+#pragma unroll 2
+    for (int k4 = 0; k4 < DK; k4 += 4) {
+      const float4 w = *reinterpret_cast<const float4*>(&d[L::W + r * PK + k4]);
+      const float4 q = *reinterpret_cast<const float4*>(&d[L::QH + r * PK + k4]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 sv = *reinterpret_cast<const float4*>(&sST[(c4 + j) * PST + k4]);
+        ws[j] = ffma2(lo2(w), lo2(sv), ws[j]);
+        ws[j] = ffma2(hi2(w), hi2(sv), ws[j]);
+        os[j] = ffma2(lo2(q), lo2(sv), os[j]);
+        os[j] = ffma2(hi2(q), hi2(sv), os[j]);
+      }
+    }
+    {
+      const float4 uh = *reinterpret_cast<const float4*>(&d[L::HEAD + r * PC + c4]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sUT[(c4 + j) * PUT + r] = comp(uh, j) - (ws[j].x + ws[j].y);  // U = U_hat - W S
+    }
+    __syncthreads();  // U complete; every read of the state done
+
+    // O += M U (M lower triangular: rows 0..31 stop at column 31) and
+    // S = Diag(exp G_last) S + K_bar^T U, in one pass over the rows of U, pairing s and s + 1
+    float2 acc[KR][4];
+#pragma unroll
+    for (int i = 0; i < KR; ++i) {
+      const float gm = d[L::GC + r + 64 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(comp(sreg[i], j) * gm, 0.f);
+    }
+    const int s_end = r < 32 ? 32 : 64;  // warp-uniform
+#pragma unroll 2
     for (int s4 = 0; s4 < 64; s4 += 4) {
-      float4 mm[4];
+      float4 ut[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) mm[i] = *reinterpret_cast<const float4*>(&sM[(rr + 16 * i) * 68 + s4]);
+      for (int j = 0; j < 4; ++j) ut[j] = *reinterpret_cast<const float4*>(&sUT[(c4 + j) * PUT + s4]);
+      if (s4 < s_end) {
+        const float4 m = *reinterpret_cast<const float4*>(&d[L::M + r * PR + s4]);
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int jb = 0; jb < JB; ++jb) {
-          const float4 uv = *reinterpret_cast<const float4*>(&sU[(s4 + u) * PSV + cc + 64 * jb]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) o[i][jb] = f4_fma(comp(mm[i], u), uv, o[i][jb]);
-        }
-    }
-
-    // e. optional epilogue, store valid rows
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = rr + 16 * i;
-      const size_t orow = ((size_t)(t0 + r) * H + h) * DV;
-      float scale = 1.f;
-      if (gate != nullptr) {
-        float ss = 0.f;
-#pragma unroll
-        for (int jb = 0; jb < JB; ++jb) ss += dot4(o[i][jb], o[i][jb]);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-        scale = rsqrtf(ss / (float)DV + eps);
-      }
-      if (r < n) {
-#pragma unroll
-        for (int jb = 0; jb < JB; ++jb)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int col = cc + 64 * jb + e;
-            float y = comp(o[i][jb], e);
-            if (gate != nullptr) {
-              const float wj = norm_w ? norm_w[col] : 1.f;
-              y = y * scale * wj * sigmoidf_(to_f32(gate[orow + col]));
-            }
-            out[orow + col] = from_f32<Tout>(y);
-          }
-      }
-    }
-    __syncthreads();  // all reads of sX (Q_hat) done
-
-    // f. K_bar -> sX
-    for (int idx = tid; idx < 64 * DK / 4; idx += kThreads) {
-      const int r = idx / (DK / 4), c4 = (idx % (DK / 4)) * 4;
-      *reinterpret_cast<float4*>(&sX[r * PSK + c4]) = *reinterpret_cast<const float4*>(&blob[L::KB + r * DK + c4]);
-    }
-    __syncthreads();
-
-    // g. S = Diag(exp G_last) S + K_bar^T U
-    {
-      float4 acc[SI][JB];
-#pragma unroll
-      for (int i = 0; i < SI; ++i) {
-        const float gm = sGam[rr + 16 * i];
-#pragma unroll
-        for (int jb = 0; jb < JB; ++jb) {
-          float4 sv = *reinterpret_cast<const float4*>(&sS[(rr + 16 * i) * PSV + cc + 64 * jb]);
-          sv.x *= gm; sv.y *= gm; sv.z *= gm; sv.w *= gm;
-          acc[i][jb] = sv;
-        }
-      }
-      for (int r = 0; r < 64; ++r) {
-        float4 uv[JB];
-#pragma unroll
-        for (int jb = 0; jb < JB; ++jb) uv[jb] = *reinterpret_cast<const float4*>(&sU[r * PSV + cc + 64 * jb]);
-#pragma unroll
-        for (int i = 0; i < SI; ++i) {
-          const float kb = sX[r * PSK + rr + 16 * i];
-#pragma unroll
-          for (int jb = 0; jb < JB; ++jb) acc[i][jb] = f4_fma(kb, uv[jb], acc[i][jb]);
+        for (int j = 0; j < 4; ++j) {
+          os[j] = ffma2(lo2(m), lo2(ut[j]), os[j]);
+          os[j] = ffma2(hi2(m), hi2(ut[j]), os[j]);
         }
       }
 #pragma unroll
-      for (int i = 0; i < SI; ++i)
+      for (int i = 0; i < KR; ++i) {
+        const float4 kb = *reinterpret_cast<const float4*>(&d[L::KBT + (r + 64 * i) * PR + s4]);
 #pragma unroll
-        for (int jb = 0; jb < JB; ++jb)
-          *reinterpret_cast<float4*>(&sS[(rr + 16 * i) * PSV + cc + 64 * jb]) = acc[i][jb];
+        for (int j = 0; j < 4; ++j) {
+          acc[i][j] = ffma2(lo2(kb), lo2(ut[j]), acc[i][j]);
+          acc[i][j] = ffma2(hi2(kb), hi2(ut[j]), acc[i][j]);
+        }
+      }
     }
-    __syncthreads();
-    // state checkpoint after every ckpt_chunks full chunks (sS is next written by step g of a
-    // later chunk, after further barriers)
+#pragma unroll
+    for (int i = 0; i < KR; ++i) {
+      sreg[i] = make_float4(acc[i][0].x + acc[i][0].y, acc[i][1].x + acc[i][1].y, acc[i][2].x + acc[i][2].y,
+                            acc[i][3].x + acc[i][3].y);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sST[(c4 + j) * PST + r + 64 * i] = comp(sreg[i], j);
+    }
+    float o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = os[j].x + os[j].y;
+
+    // state checkpoint after every ckpt_chunks full chunks (this thread's own elements)
     if (ckpt != nullptr && (c + 1) % ckpt_chunks == 0 && (c + 1) * 64 <= len) {
       float* dst = ckpt + ((size_t)(ck_base + (c + 1) / ckpt_chunks - 1) * H + h) * DK * DV;
-      for (int idx = tid; idx < DK * DV; idx += kThreads) dst[idx] = sS[(idx / DV) * PSV + idx % DV];
+#pragma unroll
+      for (int i = 0; i < KR; ++i) {
+        float* po = dst + (size_t)(r + 64 * i) * DV + col0 + c4;
+        po[0] = sreg[i].x;
+        po[1] = sreg[i].y;
+        po[2] = sreg[i].z;
+        po[3] = sreg[i].w;
+      }
     }
+
+    if (epi) {
+      sPart[cg * 64 + r] = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
+      if (c > 0) store(c - 1, o_prev, gv);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o_prev[j] = o[j];
+    } else {
+      store(c, o, gv);
+    }
+  }
+  if (epi && nchunks > 0) {
+    float gv[4] = {0.f, 0.f, 0.f, 0.f};
+    const int64_t c = nchunks - 1;
+    if (r < rows_of(c)) {
+      const size_t orow = ((size_t)(t_begin + 64 * c + r) * H + h) * DV + col0 + c4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) gv[j] = to_f32(gate[orow + j]);
+    }
+    __syncthreads();  // every column group's partial sums of the last chunk are in place
+    if (cg == 0) send(c);
+    store(c, o_prev, gv);
   }
 
   if (hT != nullptr)
-    for (int idx = tid; idx < DK * DV; idx += kThreads) {
-      const int r = idx / DV, j = idx % DV;
-      hT[soff + idx] = sS[r * PSV + j];
+#pragma unroll
+    for (int i = 0; i < KR; ++i) {
+      const size_t o = soff + (size_t)(r + 64 * i) * DV + col0 + c4;
+      hT[o] = sreg[i].x;
+      hT[o + 1] = sreg[i].y;
+      hT[o + 2] = sreg[i].z;
+      hT[o + 3] = sreg[i].w;
     }
+  if (epi) cluster_sync_all();  // no CTA leaves while a peer may still write into its shared memory
 }
 
 __global__ void plan_kernel(const int32_t* __restrict__ cu, int B, int64_t T_tot, int32_t* __restrict__ plan,
@@ -515,25 +709,23 @@ __global__ void plan_kernel(const int32_t* __restrict__ cu, int B, int64_t T_tot
 
 template <int DK, int DV, typename Tin, typename Tout>
 cudaError_t launch_cc(const PrefillArgs& a, cudaStream_t st) {
-  using L = CcBlob<DK, DV>;
+  using Sc = CcScan<DK, DV>;
   const size_t prep_smem = prep_smem_floats<DK, DV>() * sizeof(float);
-  const size_t scan_smem = scan_smem_floats<DK, DV>() * sizeof(float);
   static DeviceOnce once;  // per instantiation
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  const cudaError_t e0 = once.run(dev, [prep_smem, scan_smem] {
+  const cudaError_t e0 = once.run(dev, [prep_smem] {
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_cc<DK, DV, Tin>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(chunk_scan_cc<DK, DV, Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)scan_smem);
+                                (int)Sc::SMEM);
   });
   if (e0 != cudaSuccess) return e0;
   const bool has_cu = a.cu_seqlens != nullptr;
   const int64_t nchunks = max_chunks(a.B, a.T, has_cu);
   int32_t* plan = static_cast<int32_t*>(a.workspace);
   float* blob = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + plan_bytes(a.B));
-  (void)L::FLOATS;
   if (has_cu) {
     TraceScope ts("kda_plan", st);
     cudaError_t e = plan_launch(a.cu_seqlens, a.B, a.T_tot, plan, a.err, st);
@@ -548,12 +740,24 @@ cudaError_t launch_cc(const PrefillArgs& a, cudaStream_t st) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  dim3 grid2((unsigned)a.B, (unsigned)a.H);
+  // one cluster of NS CTAs (the value-column slices) per (sequence, head)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(CcBlob<DK, DV>::NS * a.B), (unsigned)a.H, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Sc::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CcBlob<DK, DV>::NS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   TraceScope ts("kda_chunk_scan_cc", st);
-  chunk_scan_cc<DK, DV, Tin, Tout><<<grid2, kThreads, scan_smem, st>>>(
-      blob, plan, a.cu_seqlens, a.B, a.T, a.H, a.h0, a.hT, static_cast<Tout*>(a.out),
-      static_cast<const Tin*>(a.epi.gate), a.epi.norm_weight, a.epi.eps, a.ckpt, a.ckpt_chunks);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, chunk_scan_cc<DK, DV, Tin, Tout>, static_cast<const float*>(blob),
+                            static_cast<const int32_t*>(plan), a.cu_seqlens, a.B, a.T, a.H, a.h0, a.hT,
+                            static_cast<Tout*>(a.out), static_cast<const Tin*>(a.epi.gate), a.epi.norm_weight,
+                            a.epi.eps, a.ckpt, a.ckpt_chunks, a.err);
 }
 
 template <typename Tin, typename Tout>
@@ -573,7 +777,11 @@ cudaError_t launch_cc_out(const PrefillArgs& a, cudaStream_t st) {
 }  // namespace
 
 size_t prefill_cc_blob_bytes(int dk, int dv) {
-  return (((size_t)64 * (3 * dk + dv) + 64 * 64 + dk + 63) / 64 * 64) * sizeof(float);
+  if (dk == 128 && dv == 128) return CcBlob<128, 128>::FLOATS * sizeof(float);
+  if (dk == 64 && dv == 64) return CcBlob<64, 64>::FLOATS * sizeof(float);
+  if (dk == 128 && dv == 64) return CcBlob<128, 64>::FLOATS * sizeof(float);
+  if (dk == 64 && dv == 128) return CcBlob<64, 128>::FLOATS * sizeof(float);
+  return 0;
 }
 
 cudaError_t plan_launch(const int32_t* cu_seqlens, int B, int64_t T_tot, int32_t* plan, unsigned int* err,
