@@ -37,6 +37,11 @@ PREFILL_BYTES_PER_TOKEN_HEAD = 3 * 2 * 128 + 4 * 128 + 4 + 2 * 128        # q,k,
 PREFILL_FLOPS_PER_TOKEN_HEAD = 2 * (5 * 64 * 128 + 3 * 128 * 128)          # method's flop count at C=64, d=128
 PREP_BYTES_PER_TOKEN_HEAD = 3 * 2 * 128 + 4 * 128 + 4                      # the chunk-parallel kernel's inputs
 STATE_BYTES = 128 * 128 * 4                                                # one fp32 state (h0 or hT)
+
+
+def prefill_bytes_per_token_head(dk: int, dv: int) -> int:
+    """q, k (bf16, dk each), v (bf16, dv), g (fp32, dk), beta (fp32), out (bf16, dv)."""
+    return 2 * (2 * dk + dv) + 4 * dk + 4 + 2 * dv
 DECODE_STATE_BYTES = 2 * 128 * 128 * 4                                    # read + write of one fp32 state
 DECODE_IO_BYTES_PER_TOKEN_HEAD = 3 * 2 * 128 + 4 * 128 + 4 + 2 * 128 + 2 * 128  # q,k,v,g,beta,gate,out
 # chunkwise backward, per (chunk, head) at C=64, d=128: 14 C x C x d products (records A, M, W, U_hat;
@@ -404,6 +409,10 @@ def run_ours(args, world, rank, local):
         others["varlen"] = prefill_workload(inputs.VARLEN, max(3, args.steps), dev, hbm_gbs, peak_kind, world,
                                             time_calls)
         others["long"] = prefill_workload(inputs.LONG, 3, dev, hbm_gbs, peak_kind, world, time_calls)
+        # 64-dim heads: the same shape as the prefill workload, carried by the CUDA-core prefill
+        others["prefill_d64"] = prefill_workload(
+            dataclasses.replace(inputs.PREFILL, dk=64, dv=64, name="prefill B=1 H=32 T=8192 dk=dv=64 bf16"),
+            max(3, args.steps), dev, hbm_gbs, peak_kind, world, time_calls)
     csum = clocks.summary() or {}
     sm_max_mhz = csum.get("sm_max_mhz") or 2070.0
     fp32_tflops = torch.cuda.get_device_properties(dev).multi_processor_count * FP32_LANES_PER_SM * 2 * \
@@ -507,7 +516,8 @@ def prefill_workload(cfg, calls, dev, hbm_gbs, peak_kind, world, time_calls):
                      device=dev, dtype=torch.uint8)
     ms = time_calls(lambda: binding.kda_chunk_fwd(P["q"], P["k"], P["v"], P["g"], P["beta"], h0=P["h0"], out=out,
                                                   hT=hT, workspace=ws, **kw), calls)
-    nbytes = PREFILL_BYTES_PER_TOKEN_HEAD * T_tot * H + B * H * STATE_BYTES * (2 if P["h0"] is not None else 1)
+    nbytes = prefill_bytes_per_token_head(cfg.dk, cfg.dv) * T_tot * H + \
+        B * H * cfg.dk * cfg.dv * 4 * (2 if P["h0"] is not None else 1)
     achieved = nbytes / (ms * 1e-3) / 1e9
     del P, out, hT, ws
     torch.cuda.empty_cache()

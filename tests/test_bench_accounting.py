@@ -21,6 +21,15 @@ def test_prefill_bytes_and_flops_per_token_head():
     assert bench.PREFILL_BYTES_PER_TOKEN_HEAD * 8192 * 32 == 403701760  # the bench's prefill workload
 
 
+def test_prefill_bytes_for_other_head_sizes():
+    # the same operands at dk = dv = d; the 128-dim figure is the constant above
+    for d in (64, 128):
+        assert bench.prefill_bytes_per_token_head(d, d) == 3 * d * BF16 + d * FP32 + FP32 + d * BF16
+    assert bench.prefill_bytes_per_token_head(128, 128) == bench.PREFILL_BYTES_PER_TOKEN_HEAD
+    assert bench.prefill_bytes_per_token_head(64, 64) == 772
+    assert bench.prefill_bytes_per_token_head(64, 64) * 8192 * 32 + 32 * 64 * 64 * FP32 == 202899456  # with hT
+
+
 def test_decode_and_verify_bytes():
     state = D * D * FP32
     assert bench.DECODE_STATE_BYTES == 2 * state  # read and written once
