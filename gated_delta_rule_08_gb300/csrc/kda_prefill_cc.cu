@@ -277,8 +277,12 @@ chunk_prep_cc(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   }
   __syncthreads();
 
-  // 5. V into shared memory (over q * 2^(G - R)); T = (I + A)^-1 Diag(beta) by forward
-  //    substitution, 4 threads per column s (over k * 2^(R - G))
+  // 5. V into shared memory (over q * 2^(G - R)), and T = (I + A)^-1 Diag(beta) by blocks:
+  //    X = (I + A)^-1 is unit lower triangular; its four 16 x 16 diagonal blocks come from forward
+  //    substitution, and each off-diagonal block from the two above it on the diagonal,
+  //    X_10 = -X_11 A_10 X_00, first for the 16-row pairs (0, 1) and (2, 3), then for the 32-row
+  //    halves.  X and then T sit over k * 2^(R - G) (pitch 65); the products' intermediate
+  //    Y = A_10 X_00 over k * 2^(G_47 - G) (pitch 33).
   float* sV = sQ;
 #pragma unroll
   for (int j = 0; j < NLV; ++j) {
@@ -286,27 +290,87 @@ chunk_prep_cc(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     store_f32(&sV[r * PM + e0], rv[j], Tin());
   }
   float* sT = sKR;
+  float* sY = sKX;
   {
-    const int s = tid >> 2, part = tid & 3;
-    float x[16];  // x[jj] = X[4 jj + part][s]
+    // diagonal blocks: thread = (block bi, column s, part p); X[b + r][b + s] for the rows r of the
+    // block, the sum over j split four ways (j = 4 p .. 4 p + 3) and combined by two shuffles
+    const int p = tid & 3, s = (tid >> 2) & 15, bi = tid >> 6, b = 16 * bi;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};  // x[jj] = X[b + 4 p + jj][b + s]
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) x[jj] = 0.f;
-#pragma unroll
-    for (int r = 0; r < 64; ++r) {
+    for (int r = 0; r < 16; ++r) {
       float acc = 0.f;
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int j = 4 * jj + part;
-        if (j < r) acc = fmaf(sA[r * 65 + j], x[jj], acc);
-      }
+      for (int jj = 0; jj < 4; ++jj)
+        if (4 * p + jj < r) acc = fmaf(sA[(b + r) * 65 + b + 4 * p + jj], x[jj], acc);
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       acc += __shfl_xor_sync(0xffffffffu, acc, 2);
       const float xv = (r == s) ? 1.f : ((r < s) ? 0.f : -acc);
-      if (part == (r & 3)) x[r >> 2] = xv;
+      if (p == (r >> 2)) x[r & 3] = xv;
     }
-    const float bs = sBeta[s];
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) sT[(4 * jj + part) * 65 + s] = x[jj] * bs;
+    for (int jj = 0; jj < 4; ++jj) sT[(b + 4 * p + jj) * 65 + b + s] = x[jj];
+    // the blocks above the diagonal are zero
+    for (int i = tid; i < 64 * 64; i += kThreads) {
+      const int r = i >> 6, c = i & 63;
+      if ((c >> 4) > (r >> 4)) sT[r * 65 + c] = 0.f;
+    }
+  }
+  __syncthreads();
+  {
+    // 16-row pairs q = 0, 1 (blocks 2q, 2q + 1): Y_q = A[16(2q+1) + r][16(2q) + k] X[16(2q) + k][16(2q) + c]
+    const int q = tid >> 7, r = tid & 15, c2 = ((tid >> 4) & 7) * 2;
+    const int r0 = 16 * (2 * q + 1), c0 = 16 * (2 * q);
+    float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float a = sA[(r0 + r) * 65 + c0 + k];
+      y0 = fmaf(a, sT[(c0 + k) * 65 + c0 + c2], y0);
+      y1 = fmaf(a, sT[(c0 + k) * 65 + c0 + c2 + 1], y1);
+    }
+    sY[q * 16 * 33 + r * 33 + c2] = y0;
+    sY[q * 16 * 33 + r * 33 + c2 + 1] = y1;
+    __syncthreads();
+    // X[16(2q+1) + r][16(2q) + c] = -X[16(2q+1) + r][16(2q+1) + k] Y_q[k][c]
+    float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float xr = sT[(r0 + r) * 65 + r0 + k];
+      z0 = fmaf(xr, sY[q * 16 * 33 + k * 33 + c2], z0);
+      z1 = fmaf(xr, sY[q * 16 * 33 + k * 33 + c2 + 1], z1);
+    }
+    sT[(r0 + r) * 65 + c0 + c2] = -z0;
+    sT[(r0 + r) * 65 + c0 + c2 + 1] = -z1;
+  }
+  __syncthreads();
+  {
+    // 32-row halves: Y = A[32 + r][k] X[k][c] (k, c < 32), then X[32 + r][c] = -X[32 + r][32 + k] Y[k][c];
+    // thread = (row r = lane, four columns of a warp-uniform group)
+    const int r = tid & 31, c4 = (tid >> 5) * 4;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float a = sA[(32 + r) * 65 + k];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) y[e] = fmaf(a, sT[k * 65 + c4 + e], y[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sY[r * 33 + c4 + e] = y[e];
+    __syncthreads();
+    float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float xr = sT[(32 + r) * 65 + 32 + k];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) z[e] = fmaf(xr, sY[k * 33 + c4 + e], z[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sT[(32 + r) * 65 + c4 + e] = -z[e];
+  }
+  __syncthreads();
+  // T = X Diag(beta)
+  for (int i = tid; i < 64 * 64; i += kThreads) {
+    const int r = i >> 6, c = i & 63;
+    sT[r * 65 + c] *= sBeta[c];
   }
   __syncthreads();
 
