@@ -386,7 +386,8 @@ chunk_prep_cc(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
 // each owning 16 value columns of the state; every CTA reads the chunk's W, Q_hat, K_bar^T and M
 // (the repeats hit L2).  The one exchange is the RMSNorm's sum of squares over a token's dv
 // outputs (gate epilogue only): each CTA stores its 16-column partial sums into every CTA of the
-// cluster (distributed shared memory) with a remote mbarrier arrival, and normalises a chunk's
+// cluster (distributed shared memory) by st.async, whose bytes complete the peer's mbarrier
+// phase, and normalises a chunk's
 // outputs one chunk later, so that the exchange overlaps the next chunk's products.  The next
 // chunk's record arrives by bulk copy while the current one is used (two stages where shared
 // memory allows).
@@ -427,11 +428,12 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+// an asynchronous 4-byte store into a peer's shared memory that, once it lands, counts its bytes
+// against the peer's mbarrier (both addresses in the peer CTA); the sender does not wait for it
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr), "f"(v),
+               "r"(bar)
+               : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -480,7 +482,7 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
   if (tid == 0) {
     tc::mbar_init(&full[0], 1);
     tc::mbar_init(&full[1], 1);
-    for (int i = 0; i < NSLOT; ++i) tc::mbar_init(&slot_bar[i], 64 * NS);
+    for (int i = 0; i < NSLOT; ++i) tc::mbar_init(&slot_bar[i], 1);  // armed per chunk, filled by st.async
     tc::mbar_fence_init();
   }
   if (epi) cluster_sync_all();  // every CTA's barriers exist before the first remote arrival
@@ -538,9 +540,7 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
     const uint32_t slot = tc::smem_u32(&sSlot[(sl * NS + slice) * 64 + r]);
     const uint32_t bar = tc::smem_u32(&slot_bar[sl]);
 #pragma unroll
-    for (int p = 0; p < NS; ++p) st_cluster_f32(cluster_map(slot, (uint32_t)p), ss);
-#pragma unroll
-    for (int p = 0; p < NS; ++p) mbar_arrive_cluster(cluster_map(bar, (uint32_t)p));
+    for (int p = 0; p < NS; ++p) st_async_f32(cluster_map(slot, (uint32_t)p), ss, cluster_map(bar, (uint32_t)p));
   };
   auto store = [&](int64_t c, const float (&o)[4], const float (&gv)[4]) {
     float scale = 1.f;
@@ -575,6 +575,8 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
     }
     float gv[4] = {0.f, 0.f, 0.f, 0.f};  // gate of chunk c - 1, whose outputs leave at the end of chunk c
     if (epi && c > 0) {
+      // slot (c - 1) % NSLOT expects 64 rows from each of the NS CTAs (bytes counted on arrival)
+      if (tid == 0) tc::mbar_arrive_expect_tx(&slot_bar[(c - 1) % NSLOT], 64 * NS * (uint32_t)sizeof(float));
       if (cg == 0) send(c - 1);
       if (r < rows_of(c - 1)) {
         const size_t orow = ((size_t)(t_begin + 64 * (c - 1) + r) * H + h) * DV + col0 + c4;
@@ -585,10 +587,10 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
     wait_bar(&full[st], (uint32_t)((c / STAGES) & 1), false);
 
     // W S and Q_hat S in one pass over the state rows, pairing k and k + 1
-    float2 ws[4], os[4];
+    float2 ws[4], os[4], ws2[4], os2[4];  // two accumulators per sum: shorter dependency chains
 #pragma unroll
-    for (int j = 0; j < 4; ++j) ws[j] = os[j] = make_float2(0.f, 0.f);
-#pragma unroll 2
+    for (int j = 0; j < 4; ++j) ws[j] = os[j] = ws2[j] = os2[j] = make_float2(0.f, 0.f);
+#pragma unroll 4
     for (int k4 = 0; k4 < DK; k4 += 4) {
       const float4 w = *reinterpret_cast<const float4*>(&d[L::W + r * PK + k4]);
       const float4 q = *reinterpret_cast<const float4*>(&d[L::QH + r * PK + k4]);
@@ -596,10 +598,15 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
       for (int j = 0; j < 4; ++j) {
         const float4 sv = *reinterpret_cast<const float4*>(&sST[(c4 + j) * PST + k4]);
         ws[j] = ffma2(lo2(w), lo2(sv), ws[j]);
-        ws[j] = ffma2(hi2(w), hi2(sv), ws[j]);
+        ws2[j] = ffma2(hi2(w), hi2(sv), ws2[j]);
         os[j] = ffma2(lo2(q), lo2(sv), os[j]);
-        os[j] = ffma2(hi2(q), hi2(sv), os[j]);
+        os2[j] = ffma2(hi2(q), hi2(sv), os2[j]);
       }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      ws[j] = make_float2(ws[j].x + ws2[j].x, ws[j].y + ws2[j].y);
+      os[j] = make_float2(os[j].x + os2[j].x, os[j].y + os2[j].y);
     }
     {
       const float4 uh = *reinterpret_cast<const float4*>(&d[L::HEAD + r * PC + c4]);
@@ -610,15 +617,20 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
 
     // O += M U (M lower triangular: rows 0..31 stop at column 31) and
     // S = Diag(exp G_last) S + K_bar^T U, in one pass over the rows of U, pairing s and s + 1
-    float2 acc[KR][4];
+    float2 acc[KR][4], acc2[KR][4];
 #pragma unroll
     for (int i = 0; i < KR; ++i) {
       const float gm = d[L::GC + r + 64 * i];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(comp(sreg[i], j) * gm, 0.f);
+      for (int j = 0; j < 4; ++j) {
+        acc[i][j] = make_float2(comp(sreg[i], j) * gm, 0.f);
+        acc2[i][j] = make_float2(0.f, 0.f);
+      }
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) os2[j] = make_float2(0.f, 0.f);
     const int s_end = r < 32 ? 32 : 64;  // warp-uniform
-#pragma unroll 2
+#pragma unroll 4
     for (int s4 = 0; s4 < 64; s4 += 4) {
       float4 ut[4];
 #pragma unroll
@@ -628,7 +640,7 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           os[j] = ffma2(lo2(m), lo2(ut[j]), os[j]);
-          os[j] = ffma2(hi2(m), hi2(ut[j]), os[j]);
+          os2[j] = ffma2(hi2(m), hi2(ut[j]), os2[j]);
         }
       }
 #pragma unroll
@@ -637,12 +649,16 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           acc[i][j] = ffma2(lo2(kb), lo2(ut[j]), acc[i][j]);
-          acc[i][j] = ffma2(hi2(kb), hi2(ut[j]), acc[i][j]);
+          acc2[i][j] = ffma2(hi2(kb), hi2(ut[j]), acc2[i][j]);
         }
       }
     }
 #pragma unroll
+    for (int j = 0; j < 4; ++j) os[j] = make_float2(os[j].x + os2[j].x, os[j].y + os2[j].y);
+#pragma unroll
     for (int i = 0; i < KR; ++i) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(acc[i][j].x + acc2[i][j].x, acc[i][j].y + acc2[i][j].y);
       sreg[i] = make_float4(acc[i][0].x + acc[i][0].y, acc[i][1].x + acc[i][1].y, acc[i][2].x + acc[i][2].y,
                             acc[i][3].x + acc[i][3].y);
 #pragma unroll
@@ -683,6 +699,7 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
       for (int j = 0; j < 4; ++j) gv[j] = to_f32(gate[orow + j]);
     }
     __syncthreads();  // every column group's partial sums of the last chunk are in place
+    if (tid == 0) tc::mbar_arrive_expect_tx(&slot_bar[c % NSLOT], 64 * NS * (uint32_t)sizeof(float));
     if (cg == 0) send(c);
     store(c, o_prev, gv);
   }

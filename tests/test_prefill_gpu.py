@@ -60,6 +60,16 @@ def test_dims_and_epilogue(dk, dv, epilogue):
     _check(cfg, epilogue=epilogue)
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128)])
+def test_fp32_inputs_with_the_epilogue(dk, dv):
+    """fp32 inputs take the CUDA-core path: its serial pass runs each chain as a cluster of dv/16
+    CTAs that exchange the RMSNorm's partial sums through distributed shared memory (one stage of
+    records at dk = 128, two at dk = 64)."""
+    cfg = inputs.PrefillConfig("fp32 epi", H=3, dk=dk, dv=dv, dtype="fp32", lengths=(200, 64, 1, 333), B=4,
+                               h0_std=0.1, epilogue=True, seed=240 + dk + dv)
+    _check(cfg, epilogue=True)
+
+
 def test_varlen_with_empty_and_short_sequences():
     cfg = inputs.PrefillConfig("varlen edge", H=4, dk=128, dv=128, dtype="bf16",
                                lengths=(0, 1, 63, 64, 65, 0, 129, 3), B=8, h0_std=0.1, epilogue=True, seed=300)
@@ -250,6 +260,7 @@ def test_sequence_split_across_sms_matches_oracle(lengths, H, epilogue, z_mean):
 @pytest.mark.parametrize("lengths,H,dk,dtype,ckpt_chunks,z_mean", [
     ((700, 1300, 64, 2000), 2, 128, "bf16", 4, 0.0),   # tensor-core path, varlen
     ((700, 1300, 64, 2000), 2, 64, "fp32", 4, 0.0),    # CUDA-core path
+    ((700, 1300, 64, 2000), 2, 128, "fp32", 2, 0.0),   # CUDA-core path, one record stage, 8-CTA clusters
     ((8192,), 4, 128, "bf16", 8, -8.0),                # split into segments, slow decay
 ])
 def test_checkpoints_match_the_oracle_on_each_prefix(lengths, H, dk, dtype, ckpt_chunks, z_mean):
