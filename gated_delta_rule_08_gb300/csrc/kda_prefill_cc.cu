@@ -397,7 +397,8 @@ struct CcScan {
   static constexpr int NSLOT = 4;   // partial-sum slots in flight (a peer runs at most 2 chunks ahead)
   static constexpr int PST = DK + 4, PUT = 68;        // pitches of the transposed state and U
   static constexpr int STAGE = L::HEAD + L::SLICE;    // record image + this CTA's U_hat slice
-  static constexpr int EXTRA = L::NC * PST + L::NC * PUT + 4 * 64 + NSLOT * L::NS * 64;
+  // state, U, partial sums, slots, and the gate tiles of two chunks (room for fp32 gates)
+  static constexpr int EXTRA = L::NC * PST + L::NC * PUT + 4 * 64 + NSLOT * L::NS * 64 + 2 * 64 * L::NC;
   static constexpr size_t bytes(int stages) {
     return ((size_t)stages * STAGE + EXTRA) * sizeof(float) + (2 + NSLOT) * sizeof(uint64_t);
   }
@@ -417,6 +418,14 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 __device__ __forceinline__ float2 lo2(const float4& v) { return make_float2(v.x, v.y); }
 __device__ __forceinline__ float2 hi2(const float4& v) { return make_float2(v.z, v.w); }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -466,7 +475,8 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
   float* sUT = sST + NC * PST;               // [NC][PUT] U, transposed
   float* sPart = sUT + NC * PUT;             // [4][64] sums of squares of each 4-column group
   float* sSlot = sPart + 4 * 64;             // [NSLOT][NS][64] 16-column sums from each CTA
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSlot + NSLOT * NS * 64);  // [2] stage landed
+  Tin* sGate = reinterpret_cast<Tin*>(sSlot + NSLOT * NS * 64);          // [2][64][NC] gate tiles
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSlot + NSLOT * NS * 64 + 2 * 64 * NC);  // [2] stage landed
   uint64_t* slot_bar = full + 2;                                         // [NSLOT] slot filled
 
   const int tid = threadIdx.x;
@@ -542,7 +552,19 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
 #pragma unroll
     for (int p = 0; p < NS; ++p) st_async_f32(cluster_map(slot, (uint32_t)p), ss, cluster_map(bar, (uint32_t)p));
   };
-  auto store = [&](int64_t c, const float (&o)[4], const float (&gv)[4]) {
+  // epilogue: chunk c's gate tile (this CTA's 16 columns) into slot c & 1, by cp.async
+  constexpr int PPR = NC * (int)sizeof(Tin) / 16;  // 16-byte pieces per row
+  auto stage_gate = [&](int64_t c) {
+    if (tid < 64 * PPR) {
+      const int rr = tid / PPR, pc = tid % PPR;
+      if (rr < rows_of(c))
+        cp_async16(reinterpret_cast<char*>(sGate + ((int)(c & 1) * 64 + rr) * NC) + pc * 16,
+                   reinterpret_cast<const char*>(gate + ((size_t)(t_begin + 64 * c + rr) * H + h) * DV + col0) +
+                       pc * 16);
+    }
+    cp_async_commit();
+  };
+  auto store = [&](int64_t c, const float (&o)[4]) {
     float scale = 1.f;
     if (epi) {
       const int sl = (int)(c % NSLOT);
@@ -557,7 +579,7 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         float y = o[j];
-        if (epi) y = y * scale * nw[j] * sigmoidf_(gv[j]);
+        if (epi) y = y * scale * nw[j] * sigmoidf_(to_f32(sGate[((int)(c & 1) * 64 + r) * NC + c4 + j]));
         out[orow + j] = from_f32<Tout>(y);
       }
     }
@@ -573,15 +595,12 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
       if (STAGES == 2 && c + 1 < nchunks) issue(c + 1);
       if (STAGES == 1 && c > 0) issue(c);
     }
-    float gv[4] = {0.f, 0.f, 0.f, 0.f};  // gate of chunk c - 1, whose outputs leave at the end of chunk c
-    if (epi && c > 0) {
-      // slot (c - 1) % NSLOT expects 64 rows from each of the NS CTAs (bytes counted on arrival)
-      if (tid == 0) tc::mbar_arrive_expect_tx(&slot_bar[(c - 1) % NSLOT], 64 * NS * (uint32_t)sizeof(float));
-      if (cg == 0) send(c - 1);
-      if (r < rows_of(c - 1)) {
-        const size_t orow = ((size_t)(t_begin + 64 * (c - 1) + r) * H + h) * DV + col0 + c4;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) gv[j] = to_f32(gate[orow + j]);
+    if (epi) {
+      stage_gate(c);  // read when chunk c's outputs leave, at the end of chunk c + 1
+      if (c > 0) {
+        // slot (c - 1) % NSLOT expects 64 rows from each of the NS CTAs (bytes counted on arrival)
+        if (tid == 0) tc::mbar_arrive_expect_tx(&slot_bar[(c - 1) % NSLOT], 64 * NS * (uint32_t)sizeof(float));
+        if (cg == 0) send(c - 1);
       }
     }
     wait_bar(&full[st], (uint32_t)((c / STAGES) & 1), false);
@@ -613,7 +632,8 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
 #pragma unroll
       for (int j = 0; j < 4; ++j) sUT[(c4 + j) * PUT + r] = comp(uh, j) - (ws[j].x + ws[j].y);  // U = U_hat - W S
     }
-    __syncthreads();  // U complete; every read of the state done
+    if (epi) cp_async_wait<1>();  // this thread's copies of chunk c - 1's gate have landed
+    __syncthreads();  // U complete; every read of the state done; the gate of chunk c - 1 in place
 
     // O += M U (M lower triangular: rows 0..31 stop at column 31) and
     // S = Diag(exp G_last) S + K_bar^T U, in one pass over the rows of U, pairing s and s + 1
@@ -683,25 +703,20 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
 
     if (epi) {
       sPart[cg * 64 + r] = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
-      if (c > 0) store(c - 1, o_prev, gv);
+      if (c > 0) store(c - 1, o_prev);
 #pragma unroll
       for (int j = 0; j < 4; ++j) o_prev[j] = o[j];
     } else {
-      store(c, o, gv);
+      store(c, o);
     }
   }
   if (epi && nchunks > 0) {
-    float gv[4] = {0.f, 0.f, 0.f, 0.f};
     const int64_t c = nchunks - 1;
-    if (r < rows_of(c)) {
-      const size_t orow = ((size_t)(t_begin + 64 * c + r) * H + h) * DV + col0 + c4;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) gv[j] = to_f32(gate[orow + j]);
-    }
-    __syncthreads();  // every column group's partial sums of the last chunk are in place
+    cp_async_wait<0>();
+    __syncthreads();  // every column group's partial sums and the gate of the last chunk are in place
     if (tid == 0) tc::mbar_arrive_expect_tx(&slot_bar[c % NSLOT], 64 * NS * (uint32_t)sizeof(float));
     if (cg == 0) send(c);
-    store(c, o_prev, gv);
+    store(c, o_prev);
   }
 
   if (hT != nullptr)
