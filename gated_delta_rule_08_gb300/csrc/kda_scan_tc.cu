@@ -42,6 +42,8 @@
 //  the serial path or in the output warps is checked.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "kda_internal.h"
 #include "kda_tc_common.cuh"
 
@@ -56,7 +58,8 @@ constexpr int kIssuerWarp = 12;
 constexpr int kStages = 3;                       // records staged up to two chunks ahead
 constexpr uint32_t kStage = 59392;               // staged record bytes, 1024-aligned
 constexpr uint32_t S_OUT = kStages * kStage;     // fp32 read-out staging [64 r][128 dv]
-constexpr uint32_t S_BAR = S_OUT + 32768;        // barriers + tmem slot + abort flag
+constexpr uint32_t S_GATE = S_OUT + 32768;       // gate logits of a chunk: [4 warps][16 rows][32 lanes] x 8 B
+constexpr uint32_t S_BAR = S_GATE + 16384;       // barriers + tmem slot + abort flag
 constexpr uint32_t S_END = S_BAR + 128;
 constexpr uint32_t kScanSmem = S_END + 1024;
 
@@ -90,6 +93,23 @@ struct ScanParams {
   float* seg_P;         // segment map: the range's transition [H][128][128] (MODE 1), or null
   float* seg_b;         // segment map: the range's offset [H][128][128] (MODE 1)
 };
+
+// 8 bytes global -> shared without registers (completion: cp_async_wait_all by the same thread)
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// four consecutive outputs (16-byte fp32 or 8-byte bf16 store)
+__device__ __forceinline__ void store_row(float* dst, const float4& y) { *reinterpret_cast<float4*>(dst) = y; }
+__device__ __forceinline__ void store_row(__nv_bfloat16* dst, const float4& y) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(y.x, y.y), b = __floats2bfloat162_rn(y.z, y.w);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t*>(&a);
+  pk.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(dst) = pk;
+}
 
 __device__ __forceinline__ void tmem_ld64b(uint32_t taddr, float* v) {
   float a[32], b[32];
@@ -398,65 +418,92 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
     if (!isfinite(fsum)) atomicOr(p.err, KDA_DEVERR_NONFINITE);
   } else if (MODE == 0) {
     // ======================== output warps: D_O -> staging -> epilogue -> global
+    // (two specialisations: without the epilogue, and with it; the gate's global loads of the
+    // latter are copied into shared memory while D_O is produced)
     float* ost = reinterpret_cast<float*>(sm + S_OUT);
-    Tout* out = static_cast<Tout*>(p.out);
     const int ow = warp - 8;
+    Tout* out = static_cast<Tout*>(p.out);
     bool ok = true;
-    for (int64_t c = 0; c < ncs; ++c) {
-      ok = group_and(2, 128, wait_or_abort_t<GIVEUP>(bar_s, (uint32_t)(c & 1), abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      float o[64];
-      tmem_ld64b(tl + T_DO, o);
-      tc_fence_before();
-      group_sync(2, 128);
-      if (ow == 0 && lane == 0) mbar_arrive(do_free);
-      const int64_t cg = c_begin + c;
-      const int64_t rem = len - 64 * cg;
-      const int n = (int)(rem < 64 ? rem : 64);
-      const int64_t t0 = t_begin + 64 * cg;
-      if (n == 64 && p.gate == nullptr && sizeof(Tout) == 2) {
-        // full chunk, plain bf16 output: each warp instruction writes 32 consecutive dv of a token
-        __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(out) + (size_t)t0 * H * 128 + (size_t)h * 128 + row;
-#pragma unroll
-        for (int r = 0; r < 64; ++r) {
-          ob[(size_t)r * H * 128] = __float2bfloat16_rn(o[r]);
-          if ((r & 7) == 7) __nanosleep(64);  // spread the stores over the chunk period
+    auto readout = [&](auto epi_tag) {
+      constexpr bool EPI = decltype(epi_tag)::value;
+      uint2* sgate = reinterpret_cast<uint2*>(sm + S_GATE) + ow * 16 * 32 + lane;  // this warp's [16 rows] x 32 lanes
+      float4 wv = make_float4(1.f, 1.f, 1.f, 1.f);  // RMSNorm weight of this lane's four dv
+      if (EPI && p.norm_w != nullptr)
+        wv = make_float4(p.norm_w[4 * lane], p.norm_w[4 * lane + 1], p.norm_w[4 * lane + 2], p.norm_w[4 * lane + 3]);
+      for (int64_t c = 0; c < ncs; ++c) {
+        const int64_t cg = c_begin + c;
+        const int64_t rem = len - 64 * cg;
+        const int n = (int)(rem < 64 ? rem : 64);
+        const int64_t t0 = t_begin + 64 * cg;
+        if constexpr (EPI) {
+          // the gate logits of this warp's rows, each lane its own 8 bytes
+#pragma unroll 1
+          for (int r = ow, i = 0; r < n; r += 4, ++i)
+            cp_async8(sgate + i * 32, p.gate + ((size_t)(t0 + r) * H + h) * 128 + 4 * lane);
+          cp_async_commit();
         }
-        continue;
-      }
+        ok = group_and(2, 128, wait_or_abort_t<GIVEUP>(bar_s, (uint32_t)(c & 1), abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        float o[64];
+        tmem_ld64b(tl + T_DO, o);
+        tc_fence_before();
+        group_sync(2, 128);
+        if (ow == 0 && lane == 0) mbar_arrive(do_free);
+        if (!EPI && n == 64 && sizeof(Tout) == 2) {
+          // full chunk, plain bf16 output: each warp instruction writes 32 consecutive dv of a token
+          __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(out) + (size_t)t0 * H * 128 + (size_t)h * 128 + row;
 #pragma unroll
-      for (int r = 0; r < 64; ++r) ost[r * 128 + row] = o[r];
-      group_sync(2, 128);
-      for (int r = ow; r < n; r += 4) {
-        float4 y = *reinterpret_cast<const float4*>(ost + r * 128 + 4 * lane);
-        const size_t orow = ((size_t)(t0 + r) * H + h) * 128 + 4 * lane;
-        if (p.gate != nullptr) {
-          float ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
-          ss = warp_sum(ss);
-          const float inv = rsqrtf(ss * (1.f / 128.f) + p.eps);
-          const uint2 gw = *reinterpret_cast<const uint2*>(p.gate + orow);
-          const float2 g01 = unpack_bf2(gw.x), g23 = unpack_bf2(gw.y);
-          float4 wv = make_float4(1.f, 1.f, 1.f, 1.f);
-          if (p.norm_w)
-            wv = make_float4(p.norm_w[4 * lane], p.norm_w[4 * lane + 1], p.norm_w[4 * lane + 2], p.norm_w[4 * lane + 3]);
-          y.x = y.x * inv * wv.x * sigmoidf_(g01.x);
-          y.y = y.y * inv * wv.y * sigmoidf_(g01.y);
-          y.z = y.z * inv * wv.z * sigmoidf_(g23.x);
-          y.w = y.w * inv * wv.w * sigmoidf_(g23.y);
+          for (int r = 0; r < 64; ++r) {
+            ob[(size_t)r * H * 128] = __float2bfloat16_rn(o[r]);
+            if ((r & 7) == 7) __nanosleep(64);  // spread the stores over the chunk period
+          }
+          continue;
         }
-        if constexpr (sizeof(Tout) == 4) {
-          *reinterpret_cast<float4*>(out + orow) = y;
+#pragma unroll
+        for (int r = 0; r < 64; ++r) ost[r * 128 + row] = o[r];
+        if constexpr (EPI) cp_async_wait_all();  // this lane's gate copies
+        group_sync(2, 128);
+        if constexpr (EPI) {
+          // the sums of squares of this warp's 16 rows first, reduced together (16 independent chains)
+          float ss[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int r = ow + 4 * i;
+            const float4 y = r < n ? *reinterpret_cast<const float4*>(ost + r * 128 + 4 * lane)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            ss[i] = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+          }
+#pragma unroll
+          for (int m = 16; m > 0; m >>= 1)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], m);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int r = ow + 4 * i;
+            if (r >= n) break;
+            float4 y = *reinterpret_cast<const float4*>(ost + r * 128 + 4 * lane);
+            const size_t orow = ((size_t)(t0 + r) * H + h) * 128 + 4 * lane;
+            const float inv = rsqrtf(ss[i] * (1.f / 128.f) + p.eps);
+            const uint2 gw = sgate[i * 32];
+            const float2 g01 = unpack_bf2(gw.x), g23 = unpack_bf2(gw.y);
+            y.x = y.x * inv * wv.x * sigmoidf_(g01.x);
+            y.y = y.y * inv * wv.y * sigmoidf_(g01.y);
+            y.z = y.z * inv * wv.z * sigmoidf_(g23.x);
+            y.w = y.w * inv * wv.w * sigmoidf_(g23.y);
+            store_row(out + orow, y);
+          }
         } else {
-          __nv_bfloat162 a = __floats2bfloat162_rn(y.x, y.y), b2 = __floats2bfloat162_rn(y.z, y.w);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t*>(&a);
-          pk.y = *reinterpret_cast<uint32_t*>(&b2);
-          *reinterpret_cast<uint2*>(out + orow) = pk;
+          for (int r = ow; r < n; r += 4) {
+            const float4 y = *reinterpret_cast<const float4*>(ost + r * 128 + 4 * lane);
+            store_row(out + ((size_t)(t0 + r) * H + h) * 128 + 4 * lane, y);
+          }
         }
+        group_sync(2, 128);  // staging buffer free for the next chunk
       }
-      group_sync(2, 128);  // staging buffer free for the next chunk
-    }
+    };
+    if (p.gate != nullptr) readout(std::true_type{});
+    else readout(std::false_type{});
     if (!ok) *abort_flag = 1;
   }
 
