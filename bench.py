@@ -409,6 +409,11 @@ def run_ours(args, world, rank, local):
         others["varlen"] = prefill_workload(inputs.VARLEN, max(3, args.steps), dev, hbm_gbs, peak_kind, world,
                                             time_calls)
         others["long"] = prefill_workload(inputs.LONG, 3, dev, hbm_gbs, peak_kind, world, time_calls)
+        # the prefill workload with the fused RMSNorm + sigmoid-gate epilogue
+        others["prefill_epilogue"] = prefill_workload(
+            dataclasses.replace(inputs.PREFILL, epilogue=True, name="prefill B=1 H=32 T=8192 dk=dv=128 bf16 "
+                                                                  "+ RMSNorm + gate"),
+            max(3, args.steps), dev, hbm_gbs, peak_kind, world, time_calls)
         # 64-dim heads: the same shape as the prefill workload, carried by the CUDA-core prefill
         others["prefill_d64"] = prefill_workload(
             dataclasses.replace(inputs.PREFILL, dk=64, dv=64, name="prefill B=1 H=32 T=8192 dk=dv=64 bf16"),
@@ -514,10 +519,13 @@ def prefill_workload(cfg, calls, dev, hbm_gbs, peak_kind, world, time_calls):
     hT = torch.empty(B, H, cfg.dk, cfg.dv, device=dev, dtype=torch.float32)
     ws = torch.empty(binding.kda_chunk_fwd_workspace_size(B, T_tot if varlen else T_tot // B, H, cfg.dk, cfg.dv),
                      device=dev, dtype=torch.uint8)
+    if cfg.epilogue:
+        kw.update(gate=P["gate"], norm_weight=P["norm_weight"])
     ms = time_calls(lambda: binding.kda_chunk_fwd(P["q"], P["k"], P["v"], P["g"], P["beta"], h0=P["h0"], out=out,
                                                   hT=hT, workspace=ws, **kw), calls)
     nbytes = prefill_bytes_per_token_head(cfg.dk, cfg.dv) * T_tot * H + \
-        B * H * cfg.dk * cfg.dv * 4 * (2 if P["h0"] is not None else 1)
+        B * H * cfg.dk * cfg.dv * 4 * (2 if P["h0"] is not None else 1) + \
+        (2 * cfg.dv * T_tot * H + 4 * cfg.dv if cfg.epilogue else 0)  # gate logits (bf16) and the norm weight
     achieved = nbytes / (ms * 1e-3) / 1e9
     del P, out, hT, ws
     torch.cuda.empty_cache()
