@@ -34,6 +34,31 @@ namespace kda {
 namespace {
 
 constexpr int kDecodeThreads = 256;
+
+// two fp32 lanes per instruction (each lane rounded as fmaf / a plain product)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
 constexpr int kStageTok = 4;  // tokens whose inputs are staged in shared memory together (multi-token calls)
 
 template <int DK, int DV, int NST, typename Tin, typename Tout>
@@ -69,15 +94,53 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   if (count == 0) return;  // nothing to apply: outputs and state untouched
   float* S = pool + ((size_t)slot * H + h) * (size_t)(DK * DV);
 
-  // Issue the state loads first: they are the longest-latency traffic.
+  // Several tokens per request: the inputs of a stage of up to NST tokens as raw values in
+  // registers (loaded together, converted when stored to shared memory).  The first stage's are
+  // issued before the state, so that they land first and their conversion overlaps the state's
+  // arrival.
+  constexpr int NLK = NST > 1 ? (NST * DK + kDecodeThreads - 1) / kDecodeThreads : 1;
+  constexpr int VPT = 16 / (int)sizeof(Tin);  // elements per 16-byte copy of v or the gate
+  __shared__ __align__(16) Tin sv_raw[NST > 1 ? NST : 1][NST > 1 ? DV : 8], sg_raw[NST > 1 ? NST : 1][NST > 1 ? DV : 8];
+  struct StageRegs {
+    Tin k[NLK], q[NLK];
+    float g[NLK], b;
+  };
+  auto load_stage = [&](int t, StageRegs& R) {
+    const int nst = count - t < NST ? count - t : NST;
+    const size_t row0 = ((size_t)n * n_tok + t) * H + h;
+#pragma unroll
+    for (int j = 0; j < NLK; ++j) {
+      const int i = tid + j * kDecodeThreads;
+      if (i < nst * DK) {
+        const int w = i / DK, c = i - w * DK;
+        const size_t rk = (row0 + (size_t)w * H) * DK + c;
+        R.k[j] = k[rk];
+        R.q[j] = q[rk];
+        R.g[j] = g[rk];
+      }
+    }
+    // v and the gate: raw 16-byte pieces straight into shared memory (converted where used)
+    if (tid < nst * DV / VPT) {
+      const int w = tid / (DV / VPT), c = (tid % (DV / VPT)) * VPT;
+      const size_t rw = (row0 + (size_t)w * H) * DV + c;
+      cp_async16(&sv_raw[w][c], v + rw);
+      if (gate != nullptr) cp_async16(&sg_raw[w][c], gate + rw);
+    }
+    cp_async_commit();
+    R.b = tid < nst ? beta[row0 + (size_t)tid * H] : 0.f;
+  };
+  StageRegs R;
+  if constexpr (NST > 1) load_stage(0, R);
+
+  // Issue the state loads next: they are the longest-latency traffic.
   float4 s[RPG];
 #pragma unroll
   for (int i = 0; i < RPG; ++i)
     s[i] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(rg * RPG + i) * DV) + cg);
 
   // the inputs of up to NST tokens, loaded together so that their latency is paid once
-  __shared__ __align__(16) float sk[NST][DK], sq[NST][DK], salpha[NST][DK], sv[NST][DV];
-  __shared__ float sgate[NST > 1 ? NST : 1][NST > 1 ? DV : 1], sbeta[NST];
+  __shared__ __align__(16) float sk[NST][DK], sq[NST][DK], salpha[NST][DK], sv[1][NST > 1 ? 1 : DV];
+  __shared__ float sbeta[NST];
   __shared__ float4 part_a[NG][TPR], part_b[NG][TPR];
   __shared__ float sdelta[DV], so[NST][DV];
   __shared__ float red[kDecodeThreads / 32];
@@ -99,22 +162,23 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       b_r = beta[row];
       __syncthreads();
     } else if (u == 0) {
-      if (t > 0) __syncthreads();  // the previous stage is no longer read
+      if (t > 0) {
+        __syncthreads();  // the previous stage is no longer read
+        load_stage(t, R);
+      }
       const int nst = count - t < NST ? count - t : NST;
-      for (int i = tid; i < nst * DK; i += kDecodeThreads) {
-        const int w = i / DK, c = i - w * DK;
-        const size_t rk = (row + (size_t)w * H) * DK + c;
-        sk[w][c] = to_f32(k[rk]);
-        sq[w][c] = to_f32(q[rk]);
-        salpha[w][c] = __expf(g[rk]);
+#pragma unroll
+      for (int j = 0; j < NLK; ++j) {
+        const int i = tid + j * kDecodeThreads;
+        if (i < nst * DK) {
+          const int w = i / DK, c = i - w * DK;
+          sk[w][c] = to_f32(R.k[j]);
+          sq[w][c] = to_f32(R.q[j]);
+          salpha[w][c] = __expf(R.g[j]);
+        }
       }
-      for (int i = tid; i < nst * DV; i += kDecodeThreads) {
-        const int w = i / DV, c = i - w * DV;
-        const size_t rw = (row + (size_t)w * H) * DV + c;
-        sv[w][c] = to_f32(v[rw]);
-        if (NST > 1 && gate != nullptr) sgate[w][c] = to_f32(gate[rw]);  // (one-token calls: read where used)
-      }
-      if (tid < nst) sbeta[tid] = beta[row + (size_t)tid * H];
+      if (tid < nst) sbeta[tid] = R.b;
+      cp_async_wait_all();  // this thread's v and gate pieces
       __syncthreads();
       // k . q of every staged token, one warp each, read after the token's first barrier
       if (tid < 32 * nst) {
@@ -134,7 +198,7 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
       if (tid == 0) s_kq = acc;
     }
 
-    float4 pa = make_float4(0.f, 0.f, 0.f, 0.f), pb = pa;
+    float2 pa01 = make_float2(0.f, 0.f), pa23 = pa01, pb01 = pa01, pb23 = pa01;
 #pragma unroll
     for (int i4 = 0; i4 < RPG; i4 += 4) {  // this thread's rows rg RPG + i: four per 16-byte load
       const float4 al4 = *reinterpret_cast<const float4*>(&salpha[u][rg * RPG + i4]);
@@ -145,11 +209,16 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         float4& x = s[i4 + e];
-        x.x *= al[e]; x.y *= al[e]; x.z *= al[e]; x.w *= al[e];
-        pa = f4_fma(kk[e], x, pa);
-        pb = f4_fma(qq[e], x, pb);
+        const float2 a2 = make_float2(al[e], al[e]), k2 = make_float2(kk[e], kk[e]), q2 = make_float2(qq[e], qq[e]);
+        const float2 x01 = fmul2(make_float2(x.x, x.y), a2), x23 = fmul2(make_float2(x.z, x.w), a2);
+        x = make_float4(x01.x, x01.y, x23.x, x23.y);
+        pa01 = ffma2(k2, x01, pa01);
+        pa23 = ffma2(k2, x23, pa23);
+        pb01 = ffma2(q2, x01, pb01);
+        pb23 = ffma2(q2, x23, pb23);
       }
     }
+    const float4 pa = make_float4(pa01.x, pa01.y, pa23.x, pa23.y), pb = make_float4(pb01.x, pb01.y, pb23.x, pb23.y);
     part_a[rg][cg] = pa;
     part_b[rg][cg] = pb;
     __syncthreads();
@@ -162,20 +231,28 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
         a += reinterpret_cast<const float*>(&part_a[gi][c4])[e];
         b += reinterpret_cast<const float*>(&part_b[gi][c4])[e];
       }
-      const float d = b_r * (sv[u][tid] - a);
+      float vv;
+      if constexpr (NST > 1) vv = to_f32(sv_raw[u][tid]);
+      else vv = sv[0][tid];
+      const float d = b_r * (vv - a);
       sdelta[tid] = d;
       so[u][tid] = fmaf(NST == 1 ? s_kq : s_kq_st[u], d, b);
     }
     __syncthreads();
 
     const float4 d4 = reinterpret_cast<const float4*>(sdelta)[cg];
+    const float2 d01 = make_float2(d4.x, d4.y), d23 = make_float2(d4.z, d4.w);
 #pragma unroll
     for (int i4 = 0; i4 < RPG; i4 += 4) {
       const float4 k4 = *reinterpret_cast<const float4*>(&sk[u][rg * RPG + i4]);
-      s[i4] = f4_fma(k4.x, d4, s[i4]);
-      s[i4 + 1] = f4_fma(k4.y, d4, s[i4 + 1]);
-      s[i4 + 2] = f4_fma(k4.z, d4, s[i4 + 2]);
-      s[i4 + 3] = f4_fma(k4.w, d4, s[i4 + 3]);
+      const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float4& x = s[i4 + e];
+        const float2 k2 = make_float2(kk[e], kk[e]);
+        const float2 x01 = ffma2(k2, d01, make_float2(x.x, x.y)), x23 = ffma2(k2, d23, make_float2(x.z, x.w));
+        x = make_float4(x01.x, x01.y, x23.x, x23.y);
+      }
     }
 
     // Read-out (+ optional RMSNorm over dv and sigmoid gate).
@@ -214,7 +291,7 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
         for (int j = 0; j < DV / 32; ++j) {
           const int c = lane + 32 * j;
           float o = ov[j];
-          if (gate != nullptr) o = o * inv * (norm_w ? norm_w[c] : 1.f) * sigmoidf_(sgate[w][c]);
+          if (gate != nullptr) o = o * inv * (norm_w ? norm_w[c] : 1.f) * sigmoidf_(to_f32(sg_raw[w][c]));
           out[rw + c] = from_f32<Tout>(o);
         }
       }
