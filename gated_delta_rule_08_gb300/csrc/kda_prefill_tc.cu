@@ -80,10 +80,26 @@ constexpr uint32_t T_U = 64;    // U_hat^T [128 x 64]  }
 
 // x (2 floats) -> bf16 hi (x with its low 16 bits cleared, exact in bf16) and lo = x - hi
 // rounded to bf16, each as a packed pair.
-__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const uint32_t a = __float_as_uint(x0) & 0xFFFF0000u, b = __float_as_uint(x1) & 0xFFFF0000u;
+// two fp32 lanes per instruction (each lane rounded exactly as the scalar operation)
+#define KDA_F32X2_OP(name, op)                                                                        \
+  __device__ __forceinline__ float2 name(float2 a, float2 b) {                                        \
+    float2 d;                                                                                         \
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n " op            \
+        " rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"                                                       \
+        : "=f"(d.x), "=f"(d.y)                                                                        \
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                                    \
+    return d;                                                                                         \
+  }
+KDA_F32X2_OP(fadd2, "add.rn.f32x2")
+KDA_F32X2_OP(fsub2, "sub.rn.f32x2")
+KDA_F32X2_OP(fmul2, "mul.rn.f32x2")
+#undef KDA_F32X2_OP
+
+__device__ __forceinline__ void split_bf16x2(float2 x, uint32_t& hi, uint32_t& lo) {
+  const uint32_t a = __float_as_uint(x.x) & 0xFFFF0000u, b = __float_as_uint(x.y) & 0xFFFF0000u;
   hi = (a >> 16) | b;
-  const __nv_bfloat162 t = __floats2bfloat162_rn(x0 - __uint_as_float(a), x1 - __uint_as_float(b));
+  const float2 r = fsub2(x, make_float2(__uint_as_float(a), __uint_as_float(b)));
+  const __nv_bfloat162 t = __floats2bfloat162_rn(r.x, r.y);
   lo = *reinterpret_cast<const uint32_t*>(&t);
 }
 
@@ -433,8 +449,8 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
         G63 = cum;
         const bool first = rg < 8;  // rows < 32: reference row 15, else 47
         const float2 R = first ? G15 : G47;
-        const float eR0 = ex2(R.x), eR1 = ex2(R.y);
-        const float c30 = ex2(G63.x - G47.x), c31 = ex2(G63.y - G47.y);
+        const float2 eR = make_float2(ex2(R.x), ex2(R.y));
+        const float2 c3 = make_float2(ex2(G63.x - G47.x), ex2(G63.y - G47.y));
         if (rg == 0)
           *reinterpret_cast<float2*>(rec + kRecGC + c * 4) = make_float2(ex2(G63.x), ex2(G63.y));
         uint32_t qh2[4], kb2[4];
@@ -442,46 +458,49 @@ kda_tc_chunk_prep(const __grid_constant__ PrepMaps maps, const float* __restrict
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = 4 * rg + i;
-          const float G0 = off.x + L[i].x, G1 = off.y + L[i].y;
+          const float2 G = fadd2(off, L[i]);
           const uint32_t ob = (uint32_t)r * 128u + ((((kbyte >> 4) ^ (uint32_t)r) & 7u) << 4) + (kbyte & 15u);
           const uint32_t toff = (uint32_t)(c >> 6) * 8192u + ob;
           uint32_t* pk = reinterpret_cast<uint32_t*>(raw + R_K + toff);
           uint32_t* pq = reinterpret_cast<uint32_t*>(raw + R_Q + toff);
           uint32_t* pv = reinterpret_cast<uint32_t*>(raw + R_V + toff);
           const float2 k2 = unpack_bf2(*pk), q2 = unpack_bf2(*pq), v2 = unpack_bf2(*pv);
-          const float e10 = ex2(G0 - R.x), e11 = ex2(G1 - R.y);
-          const float e20 = ex2(R.x - G0), e21 = ex2(R.y - G1);
+          const float2 d1 = fsub2(G, R), d2 = fsub2(R, G);
+          const float2 e1 = make_float2(ex2(d1.x), ex2(d1.y)), e2 = make_float2(ex2(d2.x), ex2(d2.y));
           uint32_t hi, lo;
           const uint32_t ob64 = ob + 64u * 128u;  // row 64 + r (same swizzle phase)
-          split_bf16x2(k2.x * e10, k2.y * e11, hi, lo);
+          const float2 ke1 = fmul2(k2, e1), qe1 = fmul2(q2, e1), ke2 = fmul2(k2, e2);
+          split_bf16x2(ke1, hi, lo);
           *reinterpret_cast<uint32_t*>(ops + O_XH + ob) = hi;
           *reinterpret_cast<uint32_t*>(ops + O_XL + ob) = lo;
-          split_bf16x2(q2.x * e10, q2.y * e11, hi, lo);
+          split_bf16x2(qe1, hi, lo);
           *reinterpret_cast<uint32_t*>(ops + O_XH + ob64) = hi;
           *reinterpret_cast<uint32_t*>(ops + O_XL + ob64) = lo;
-          split_bf16x2(k2.x * e20, k2.y * e21, hi, lo);
+          split_bf16x2(ke2, hi, lo);
           *reinterpret_cast<uint32_t*>(ops + O_YH + ob) = hi;
           *reinterpret_cast<uint32_t*>(ops + O_YL + ob) = lo;
-          float kb0, kb1;
+          float2 kb;
           if (first) {
             // rows < 32: k e^{G_47 - G} and k e^{G_C - G} from one exponential each (a factored
             // form can underflow while the product it feeds is O(1))
-            split_bf16x2(k2.x * ex2(G47.x - G0), k2.y * ex2(G47.y - G1), hi, lo);
+            const float2 d3 = fsub2(G47, G), d4 = fsub2(G63, G);
+            split_bf16x2(fmul2(k2, make_float2(ex2(d3.x), ex2(d3.y))), hi, lo);
             *reinterpret_cast<uint32_t*>(ops + O_YH + ob64) = hi;
             *reinterpret_cast<uint32_t*>(ops + O_YL + ob64) = lo;
-            kb0 = k2.x * ex2(G63.x - G0);
-            kb1 = k2.y * ex2(G63.y - G1);
+            kb = fmul2(k2, make_float2(ex2(d4.x), ex2(d4.y)));
           } else {
-            kb0 = k2.x * e20 * c30;  // e^{G_C - G_47} >= e^{-80}: no underflow
-            kb1 = k2.y * e21 * c31;
+            kb = fmul2(ke2, c3);  // e^{G_C - G_47} >= e^{-80}: no underflow
           }
-          qh2[i] = pack_h2(q2.x * e10 * eR0, q2.y * e11 * eR1);  // q e^{G}
-          kb2[i] = pack_h2(kb0, kb1);
+          const float2 qh = fmul2(qe1, eR);
+          qh2[i] = pack_h2(qh.x, qh.y);  // q e^{G}
+          kb2[i] = pack_h2(kb.x, kb.y);
           // Diag(beta) K_hat and Diag(beta) V as fp16, in place (T = X Diag(beta) is applied
           // through its right factor, so the solve's X is used as is)
           const float br = sBeta[r];
-          *pk = pack_h2(k2.x * e10 * eR0 * br, k2.y * e11 * eR1 * br);
-          *pv = pack_h2(v2.x * br, v2.y * br);
+          const float2 b2 = make_float2(br, br);
+          const float2 kh = fmul2(fmul2(ke1, eR), b2), vb = fmul2(v2, b2);
+          *pk = pack_h2(kh.x, kh.y);
+          *pv = pack_h2(vb.x, vb.y);
         }
         // Q_hat^T / K_bar^T rows (channel-major): lanes l and l ^ 16 hold rows 8w..8w+3 and
         // 8w+4..8w+7 of the same two channels; after one exchange each writes a full 16-byte
