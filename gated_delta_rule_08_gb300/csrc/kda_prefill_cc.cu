@@ -60,9 +60,6 @@ struct CcBlob {
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
 }
-__device__ __forceinline__ float comp(const float4& v, int i) {
-  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
-}
 
 // C[64][N] = T[64][64] (smem, pitch 65) x Bm[64][N] (smem, pitch PB), element (r, j) of C stored
 // at outg[at(r, j)] (j a multiple of 4: four consecutive floats)
@@ -406,17 +403,6 @@ struct CcScan {
   static constexpr size_t SMEM = bytes(STAGES);
 };
 
-// d = a * b + c on two fp32 lanes at once (one packed instruction, each lane rounded as fmaf)
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-__device__ __forceinline__ float2 lo2(const float4& v) { return make_float2(v.x, v.y); }
-__device__ __forceinline__ float2 hi2(const float4& v) { return make_float2(v.z, v.w); }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
@@ -458,6 +444,34 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// ---- warp-level tf32 MMA (mma.sync m16n8k8).  Fragments (g = lane / 4, t = lane % 4):
+// A (16 x 8) a0 (g, t), a1 (g+8, t), a2 (g, t+4), a3 (g+8, t+4); B (8 x 8, k x n) b0 (t, g), b1 (t+4, g);
+// C (16 x 8) c0 (g, 2t), c1 (g, 2t+1), c2 (g+8, 2t), c3 (g+8, 2t+1).
+__device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// x = hi + lo: hi = x with its low 13 mantissa bits cleared (exact in tf32), lo = x - hi (exact in
+// fp32, of which the MMA reads the top 19 bits): hi*hi + hi*lo + lo*hi is ~2^-20 relative
+struct Tf32x2 {
+  uint32_t hi, lo;
+};
+__device__ __forceinline__ Tf32x2 split_tf32(float x) {
+  const uint32_t h = __float_as_uint(x) & 0xFFFFE000u;
+  return {h, __float_as_uint(x - __uint_as_float(h))};
+}
+// D += A B with A (16 x 8) and B (8 x 8) given by their fp32 fragment values, three-term split
+__device__ __forceinline__ void mma3(float (&c)[4], const float (&a)[4], const float (&bv)[2]) {
+  const Tf32x2 a0 = split_tf32(a[0]), a1 = split_tf32(a[1]), a2 = split_tf32(a[2]), a3 = split_tf32(a[3]);
+  const Tf32x2 b0 = split_tf32(bv[0]), b1 = split_tf32(bv[1]);
+  mma_tf32(c, a0.lo, a1.lo, a2.lo, a3.lo, b0.hi, b1.hi);
+  mma_tf32(c, a0.hi, a1.hi, a2.hi, a3.hi, b0.lo, b1.lo);
+  mma_tf32(c, a0.hi, a1.hi, a2.hi, a3.hi, b0.hi, b1.hi);
+}
+
 template <int DK, int DV, typename Tin, typename Tout>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ plan,
@@ -473,7 +487,7 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
   float* stages = reinterpret_cast<float*>(smem4);
   float* sST = stages + STAGES * Sc::STAGE;  // [NC][PST] this CTA's 16 state columns, transposed
   float* sUT = sST + NC * PST;               // [NC][PUT] U, transposed
-  float* sPart = sUT + NC * PUT;             // [4][64] sums of squares of each 4-column group
+  float* sPart = sUT + NC * PUT;             // [2][64] sums of squares of each 8-column half
   float* sSlot = sPart + 4 * 64;             // [NSLOT][NS][64] 16-column sums from each CTA
   Tin* sGate = reinterpret_cast<Tin*>(sSlot + NSLOT * NS * 64);          // [2][64][NC] gate tiles
   uint64_t* full = reinterpret_cast<uint64_t*>(sSlot + NSLOT * NS * 64 + 2 * 64 * NC);  // [2] stage landed
@@ -498,23 +512,30 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
   if (epi) cluster_sync_all();  // every CTA's barriers exist before the first remote arrival
   else __syncthreads();
 
-  // thread = (row r, columns c4..c4+3 of the slice); a warp holds 32 rows of one column group,
-  // so its reads of the state and of U are broadcasts.  State rows r + 64 i.
-  const int cg = tid >> 6, r = (tid & 31) + 32 * ((tid >> 5) & 1), c4 = cg * 4;
+  // Warp w owns the 16 x 8 output tile (rows 16 m .. 16 m + 15 of the chunk, columns 8 n .. 8 n + 7
+  // of the slice), m = w / 2, n = w % 2, of W S, Q_hat S, M U and U, and the state tiles (rows
+  // 16 (m + 4 j), the same columns) of the update K_bar^T U, j < dk / 64.
+  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int m = warp >> 1, n = warp & 1;
+  const int rA = 16 * m + g, cA = 8 * n + 2 * t;  // this lane's first C element (row, slice column)
   const size_t soff = ((size_t)b * H + h) * DK * DV;
-  float4 sreg[KR];
+  float sreg[KR][4];  // state tiles, C layout
 #pragma unroll
-  for (int i = 0; i < KR; ++i) {
-    const size_t o = soff + (size_t)(r + 64 * i) * DV + col0 + c4;
-    sreg[i] = h0 ? make_float4(h0[o], h0[o + 1], h0[o + 2], h0[o + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < KR; ++j) {
+    const int k0 = 16 * (m + 4 * j) + g;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) sST[(c4 + j) * PST + r + 64 * i] = comp(sreg[i], j);
+    for (int e = 0; e < 4; ++e) {
+      const int k = k0 + 8 * (e >> 1), c = cA + (e & 1);
+      sreg[j][e] = h0 ? h0[soff + (size_t)k * DV + col0 + c] : 0.f;
+      sST[c * PST + k] = sreg[j][e];
+    }
   }
   const int64_t ck_base = ckpt != nullptr ? checkpoint_base(b, cu, T, 64 * ckpt_chunks) : 0;
-  float nw[4] = {1.f, 1.f, 1.f, 1.f};
-  if (epi && norm_w != nullptr)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) nw[j] = norm_w[col0 + c4 + j];
+  float nw[2] = {1.f, 1.f};
+  if (epi && norm_w != nullptr) {
+    nw[0] = norm_w[col0 + cA];
+    nw[1] = norm_w[col0 + cA + 1];
+  }
 
   // one thread stages chunk c's record image and U_hat slice
   auto issue = [&](int64_t c) {
@@ -542,12 +563,12 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
     const int64_t rem = len - 64 * c;
     return (int)(rem < 64 ? rem : 64);
   };
-  // epilogue: the 16-column sum of squares of chunk c's row r (from the four column groups) into
-  // slot c % NSLOT of every CTA of the cluster; one thread per row
+  // epilogue: the 16-column sum of squares of chunk c's row tid (both 8-column halves) into slot
+  // c % NSLOT of every CTA of the cluster; one thread per row
   auto send = [&](int64_t c) {
-    const float ss = sPart[r] + sPart[64 + r] + sPart[128 + r] + sPart[192 + r];
+    const float ss = sPart[tid] + sPart[64 + tid];
     const int sl = (int)(c % NSLOT);
-    const uint32_t slot = tc::smem_u32(&sSlot[(sl * NS + slice) * 64 + r]);
+    const uint32_t slot = tc::smem_u32(&sSlot[(sl * NS + slice) * 64 + tid]);
     const uint32_t bar = tc::smem_u32(&slot_bar[sl]);
 #pragma unroll
     for (int p = 0; p < NS; ++p) st_async_f32(cluster_map(slot, (uint32_t)p), ss, cluster_map(bar, (uint32_t)p));
@@ -564,23 +585,29 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
     }
     cp_async_commit();
   };
+  // chunk c's outputs (this lane's rows rA, rA + 8 and columns cA, cA + 1), normalised with every
+  // CTA's partial sums (epilogue) or as they are
   auto store = [&](int64_t c, const float (&o)[4]) {
-    float scale = 1.f;
-    if (epi) {
-      const int sl = (int)(c % NSLOT);
-      wait_bar(&slot_bar[sl], (uint32_t)((c / NSLOT) & 1), true);
-      float tot = 0.f;
+    const int nrows = rows_of(c);
 #pragma unroll
-      for (int p = 0; p < NS; ++p) tot += sSlot[(sl * NS + p) * 64 + r];
-      scale = rsqrtf(tot / (float)DV + eps);
-    }
-    if (r < rows_of(c)) {
-      const size_t orow = ((size_t)(t_begin + 64 * c + r) * H + h) * DV + col0 + c4;
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = rA + 8 * hr;
+      float y0 = o[2 * hr], y1 = o[2 * hr + 1];
+      if (epi) {
+        const int sl = (int)(c % NSLOT);
+        if (hr == 0) wait_bar(&slot_bar[sl], (uint32_t)((c / NSLOT) & 1), true);
+        float tot = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float y = o[j];
-        if (epi) y = y * scale * nw[j] * sigmoidf_(to_f32(sGate[((int)(c & 1) * 64 + r) * NC + c4 + j]));
-        out[orow + j] = from_f32<Tout>(y);
+        for (int p = 0; p < NS; ++p) tot += sSlot[(sl * NS + p) * 64 + r];
+        const float scale = rsqrtf(tot / (float)DV + eps);
+        const Tin* gr = sGate + ((int)(c & 1) * 64 + r) * NC + cA;
+        y0 = y0 * scale * nw[0] * sigmoidf_(to_f32(gr[0]));
+        y1 = y1 * scale * nw[1] * sigmoidf_(to_f32(gr[1]));
+      }
+      if (r < nrows) {
+        Tout* po = out + ((size_t)(t_begin + 64 * c + r) * H + h) * DV + col0 + cA;
+        po[0] = from_f32<Tout>(y0);
+        po[1] = from_f32<Tout>(y1);
       }
     }
   };
@@ -600,112 +627,95 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
       if (c > 0) {
         // slot (c - 1) % NSLOT expects 64 rows from each of the NS CTAs (bytes counted on arrival)
         if (tid == 0) tc::mbar_arrive_expect_tx(&slot_bar[(c - 1) % NSLOT], 64 * NS * (uint32_t)sizeof(float));
-        if (cg == 0) send(c - 1);
+        if (tid < 64) send(c - 1);
       }
     }
     wait_bar(&full[st], (uint32_t)((c / STAGES) & 1), false);
 
-    // W S and Q_hat S in one pass over the state rows, pairing k and k + 1
-    float2 ws[4], os[4], ws2[4], os2[4];  // two accumulators per sum: shorter dependency chains
-#pragma unroll
-    for (int j = 0; j < 4; ++j) ws[j] = os[j] = ws2[j] = os2[j] = make_float2(0.f, 0.f);
-#pragma unroll 4
-    for (int k4 = 0; k4 < DK; k4 += 4) {
-      const float4 w = *reinterpret_cast<const float4*>(&d[L::W + r * PK + k4]);
-      const float4 q = *reinterpret_cast<const float4*>(&d[L::QH + r * PK + k4]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 sv = *reinterpret_cast<const float4*>(&sST[(c4 + j) * PST + k4]);
-        ws[j] = ffma2(lo2(w), lo2(sv), ws[j]);
-        ws2[j] = ffma2(hi2(w), hi2(sv), ws2[j]);
-        os[j] = ffma2(lo2(q), lo2(sv), os[j]);
-        os2[j] = ffma2(hi2(q), hi2(sv), os2[j]);
-      }
+    // W S and Q_hat S for this warp's tile; B = S (k x slice column) from the transposed state
+    float ws[4] = {0.f, 0.f, 0.f, 0.f}, o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int kk = 0; kk < DK; kk += 8) {
+      const float bv[2] = {sST[(8 * n + g) * PST + kk + t], sST[(8 * n + g) * PST + kk + t + 4]};
+      const float aw[4] = {d[L::W + rA * PK + kk + t], d[L::W + (rA + 8) * PK + kk + t],
+                           d[L::W + rA * PK + kk + t + 4], d[L::W + (rA + 8) * PK + kk + t + 4]};
+      const float aq[4] = {d[L::QH + rA * PK + kk + t], d[L::QH + (rA + 8) * PK + kk + t],
+                           d[L::QH + rA * PK + kk + t + 4], d[L::QH + (rA + 8) * PK + kk + t + 4]};
+      mma3(ws, aw, bv);
+      mma3(o, aq, bv);
     }
+    // U = U_hat - W S, transposed into shared memory
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      ws[j] = make_float2(ws[j].x + ws2[j].x, ws[j].y + ws2[j].y);
-      os[j] = make_float2(os[j].x + os2[j].x, os[j].y + os2[j].y);
-    }
-    {
-      const float4 uh = *reinterpret_cast<const float4*>(&d[L::HEAD + r * PC + c4]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) sUT[(c4 + j) * PUT + r] = comp(uh, j) - (ws[j].x + ws[j].y);  // U = U_hat - W S
+    for (int e = 0; e < 4; ++e) {
+      const int r = rA + 8 * (e >> 1), cl = cA + (e & 1);
+      sUT[cl * PUT + r] = d[L::HEAD + r * PC + cl] - ws[e];
     }
     if (epi) cp_async_wait<1>();  // this thread's copies of chunk c - 1's gate have landed
     __syncthreads();  // U complete; every read of the state done; the gate of chunk c - 1 in place
 
-    // O += M U (M lower triangular: rows 0..31 stop at column 31) and
-    // S = Diag(exp G_last) S + K_bar^T U, in one pass over the rows of U, pairing s and s + 1
-    float2 acc[KR][4], acc2[KR][4];
+    // O += M U (M lower triangular: tile m stops at column 16 m + 15) and
+    // S = Diag(exp G_last) S + K_bar^T U, B = U (s x slice column) from the transposed U
+    float acc[KR][4];
 #pragma unroll
-    for (int i = 0; i < KR; ++i) {
-      const float gm = d[L::GC + r + 64 * i];
+    for (int j = 0; j < KR; ++j) {
+      const int k0 = 16 * (m + 4 * j) + g;
+      const float gm0 = d[L::GC + k0], gm1 = d[L::GC + k0 + 8];
+      acc[j][0] = sreg[j][0] * gm0;
+      acc[j][1] = sreg[j][1] * gm0;
+      acc[j][2] = sreg[j][2] * gm1;
+      acc[j][3] = sreg[j][3] * gm1;
+    }
+#pragma unroll 2
+    for (int kk = 0; kk < 64; kk += 8) {
+      const float bv[2] = {sUT[(8 * n + g) * PUT + kk + t], sUT[(8 * n + g) * PUT + kk + t + 4]};
+      if (kk < 16 * m + 16) {  // warp-uniform
+        const float am[4] = {d[L::M + rA * PR + kk + t], d[L::M + (rA + 8) * PR + kk + t],
+                             d[L::M + rA * PR + kk + t + 4], d[L::M + (rA + 8) * PR + kk + t + 4]};
+        mma3(o, am, bv);
+      }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        acc[i][j] = make_float2(comp(sreg[i], j) * gm, 0.f);
-        acc2[i][j] = make_float2(0.f, 0.f);
+      for (int j = 0; j < KR; ++j) {
+        const int k0 = 16 * (m + 4 * j) + g;
+        const float ak[4] = {d[L::KBT + k0 * PR + kk + t], d[L::KBT + (k0 + 8) * PR + kk + t],
+                             d[L::KBT + k0 * PR + kk + t + 4], d[L::KBT + (k0 + 8) * PR + kk + t + 4]};
+        mma3(acc[j], ak, bv);
       }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) os2[j] = make_float2(0.f, 0.f);
-    const int s_end = r < 32 ? 32 : 64;  // warp-uniform
-#pragma unroll 4
-    for (int s4 = 0; s4 < 64; s4 += 4) {
-      float4 ut[4];
+    for (int j = 0; j < KR; ++j) {
+      const int k0 = 16 * (m + 4 * j) + g;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) ut[j] = *reinterpret_cast<const float4*>(&sUT[(c4 + j) * PUT + s4]);
-      if (s4 < s_end) {
-        const float4 m = *reinterpret_cast<const float4*>(&d[L::M + r * PR + s4]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          os[j] = ffma2(lo2(m), lo2(ut[j]), os[j]);
-          os2[j] = ffma2(hi2(m), hi2(ut[j]), os2[j]);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < KR; ++i) {
-        const float4 kb = *reinterpret_cast<const float4*>(&d[L::KBT + (r + 64 * i) * PR + s4]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[i][j] = ffma2(lo2(kb), lo2(ut[j]), acc[i][j]);
-          acc2[i][j] = ffma2(hi2(kb), hi2(ut[j]), acc2[i][j]);
-        }
+      for (int e = 0; e < 4; ++e) {
+        sreg[j][e] = acc[j][e];
+        sST[(cA + (e & 1)) * PST + k0 + 8 * (e >> 1)] = acc[j][e];
       }
     }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) os[j] = make_float2(os[j].x + os2[j].x, os[j].y + os2[j].y);
-#pragma unroll
-    for (int i = 0; i < KR; ++i) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(acc[i][j].x + acc2[i][j].x, acc[i][j].y + acc2[i][j].y);
-      sreg[i] = make_float4(acc[i][0].x + acc[i][0].y, acc[i][1].x + acc[i][1].y, acc[i][2].x + acc[i][2].y,
-                            acc[i][3].x + acc[i][3].y);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) sST[(c4 + j) * PST + r + 64 * i] = comp(sreg[i], j);
-    }
-    float o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) o[j] = os[j].x + os[j].y;
 
-    // state checkpoint after every ckpt_chunks full chunks (this thread's own elements)
+    // state checkpoint after every ckpt_chunks full chunks (this lane's own elements)
     if (ckpt != nullptr && (c + 1) % ckpt_chunks == 0 && (c + 1) * 64 <= len) {
       float* dst = ckpt + ((size_t)(ck_base + (c + 1) / ckpt_chunks - 1) * H + h) * DK * DV;
 #pragma unroll
-      for (int i = 0; i < KR; ++i) {
-        float* po = dst + (size_t)(r + 64 * i) * DV + col0 + c4;
-        po[0] = sreg[i].x;
-        po[1] = sreg[i].y;
-        po[2] = sreg[i].z;
-        po[3] = sreg[i].w;
+      for (int j = 0; j < KR; ++j) {
+        const int k0 = 16 * (m + 4 * j) + g;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[(size_t)(k0 + 8 * (e >> 1)) * DV + col0 + cA + (e & 1)] = sreg[j][e];
       }
     }
 
     if (epi) {
-      sPart[cg * 64 + r] = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
+      // this tile's 8-column sums of squares of rows rA and rA + 8 (over the four lanes of a row)
+      float s0 = o[0] * o[0] + o[1] * o[1], s1 = o[2] * o[2] + o[3] * o[3];
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+      if (t == 0) {
+        sPart[n * 64 + rA] = s0;
+        sPart[n * 64 + rA + 8] = s1;
+      }
       if (c > 0) store(c - 1, o_prev);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) o_prev[j] = o[j];
+      for (int e = 0; e < 4; ++e) o_prev[e] = o[e];
     } else {
       store(c, o);
     }
@@ -713,20 +723,18 @@ chunk_scan_cc(const float* __restrict__ blob_base, const int32_t* __restrict__ p
   if (epi && nchunks > 0) {
     const int64_t c = nchunks - 1;
     cp_async_wait<0>();
-    __syncthreads();  // every column group's partial sums and the gate of the last chunk are in place
+    __syncthreads();  // every column half's partial sums and the gate of the last chunk are in place
     if (tid == 0) tc::mbar_arrive_expect_tx(&slot_bar[c % NSLOT], 64 * NS * (uint32_t)sizeof(float));
-    if (cg == 0) send(c);
+    if (tid < 64) send(c);
     store(c, o_prev);
   }
 
   if (hT != nullptr)
 #pragma unroll
-    for (int i = 0; i < KR; ++i) {
-      const size_t o = soff + (size_t)(r + 64 * i) * DV + col0 + c4;
-      hT[o] = sreg[i].x;
-      hT[o + 1] = sreg[i].y;
-      hT[o + 2] = sreg[i].z;
-      hT[o + 3] = sreg[i].w;
+    for (int j = 0; j < KR; ++j) {
+      const int k0 = 16 * (m + 4 * j) + g;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) hT[soff + (size_t)(k0 + 8 * (e >> 1)) * DV + col0 + cA + (e & 1)] = sreg[j][e];
     }
   if (epi) cluster_sync_all();  // no CTA leaves while a peer may still write into its shared memory
 }
