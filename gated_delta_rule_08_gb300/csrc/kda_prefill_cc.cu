@@ -57,37 +57,33 @@ struct CcBlob {
   static constexpr int FLOATS = (UH + NS * SLICE + 63) / 64 * 64;
 };
 
-__device__ __forceinline__ float dot4(float4 a, float4 b) {
-  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
-}
 
-// C[64][N] = T[64][64] (smem, pitch 65) x Bm[64][N] (smem, pitch PB), element (r, j) of C stored
-// at outg[at(r, j)] (j a multiple of 4: four consecutive floats)
-template <int N, typename At>
-__device__ __forceinline__ void tmul_store(const float* sT, const float* sB, int PB, float* outg, At at) {
-  const int rr = threadIdx.x / 16, cc = (threadIdx.x % 16) * 4;
-  constexpr int JB = N / 64;
-  float4 acc[4][JB];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int jb = 0; jb < JB; ++jb) acc[i][jb] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < 64; ++s) {
-    float t[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) t[i] = sT[(rr + 16 * i) * 65 + s];
-#pragma unroll
-    for (int jb = 0; jb < JB; ++jb) {
-      const float4 bv = *reinterpret_cast<const float4*>(&sB[s * PB + cc + 64 * jb]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i][jb] = f4_fma(t[i], bv, acc[i][jb]);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int jb = 0; jb < JB; ++jb)
-      *reinterpret_cast<float4*>(&outg[at(rr + 16 * i, cc + 64 * jb)]) = acc[i][jb];
+// ---- warp-level tf32 MMA (mma.sync m16n8k8).  Fragments (g = lane / 4, t = lane % 4):
+// A (16 x 8) a0 (g, t), a1 (g+8, t), a2 (g, t+4), a3 (g+8, t+4); B (8 x 8, k x n) b0 (t, g), b1 (t+4, g);
+// C (16 x 8) c0 (g, 2t), c1 (g, 2t+1), c2 (g+8, 2t), c3 (g+8, 2t+1).
+__device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// x = hi + lo: hi = x with its low 13 mantissa bits cleared (exact in tf32), lo = x - hi (exact in
+// fp32, of which the MMA reads the top 19 bits): hi*hi + hi*lo + lo*hi is ~2^-20 relative
+struct Tf32x2 {
+  uint32_t hi, lo;
+};
+__device__ __forceinline__ Tf32x2 split_tf32(float x) {
+  const uint32_t h = __float_as_uint(x) & 0xFFFFE000u;
+  return {h, __float_as_uint(x - __uint_as_float(h))};
+}
+// D += A B with A (16 x 8) and B (8 x 8) given by their fp32 fragment values, three-term split
+__device__ __forceinline__ void mma3(float (&c)[4], const float (&a)[4], const float (&bv)[2]) {
+  const Tf32x2 a0 = split_tf32(a[0]), a1 = split_tf32(a[1]), a2 = split_tf32(a[2]), a3 = split_tf32(a[3]);
+  const Tf32x2 b0 = split_tf32(bv[0]), b1 = split_tf32(bv[1]);
+  mma_tf32(c, a0.lo, a1.lo, a2.lo, a3.lo, b0.hi, b1.hi);
+  mma_tf32(c, a0.hi, a1.hi, a2.hi, a3.hi, b0.lo, b1.lo);
+  mma_tf32(c, a0.hi, a1.hi, a2.hi, a3.hi, b0.hi, b1.hi);
 }
 
 template <int DK, int DV>
@@ -235,42 +231,35 @@ chunk_prep_cc(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
   }
   __syncthreads();
 
-  // 4. A (strict lower, row-scaled by beta) and M (lower incl. diagonal)
+  // 4. A (strict lower, row-scaled by beta) and M (lower incl. diagonal) as three-term tf32 MMAs:
+  //    A = K_L K_R^T and M = Q_L K_R^T, with K_X in place of K_R for the off-diagonal block (rows
+  //    >= 32, columns < 32); the upper off-diagonal block is masked and neither computed nor read.
+  //    Warps 0-3 take A's 24 tiles of 16 x 8, warps 4-7 M's.
+  const int warp = tid >> 5, lane = tid & 31, fg = lane >> 2, ft = lane & 3;  // MMA fragment row / column
   {
-    const int rr = tid / 16, ss = tid % 16;
-    float accA[4][4], accM[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) accA[i][j] = accM[i][j] = 0.f;
-    for (int c = 0; c < DK; c += 4) {
-      float4 kl[4], ql[4], kr[4], kx[2];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        kl[i] = *reinterpret_cast<const float4*>(&sK[(rr + 16 * i) * PM + c]);
-        ql[i] = *reinterpret_cast<const float4*>(&sQ[(rr + 16 * i) * PM + c]);
-        kr[i] = *reinterpret_cast<const float4*>(&sKR[(ss + 16 * i) * PM + c]);
+    const bool isM = warp >= 4;
+    const float* X = isM ? sQ : sK;
+    for (int q = 0; q < 6; ++q) {
+      const int ti = (warp & 3) + 4 * q;  // tiles 0..7: rows 0-31, columns 0-31; 8..23: rows 32-63
+      const int mi = ti < 8 ? (ti >> 2) : 2 + ((ti - 8) >> 3);
+      const int ni = ti < 8 ? (ti & 3) : ((ti - 8) & 7);
+      const float* Y = (mi >= 2 && ni < 4) ? sKX : sKR;
+      const int ra = 16 * mi + fg, sb = 8 * ni + fg;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int kk = 0; kk < DK; kk += 8) {
+        const float a[4] = {X[ra * PM + kk + ft], X[(ra + 8) * PM + kk + ft], X[ra * PM + kk + ft + 4],
+                            X[(ra + 8) * PM + kk + ft + 4]};
+        const float bv[2] = {Y[sb * PM + kk + ft], Y[sb * PM + kk + ft + 4]};
+        mma3(acc, a, bv);
       }
 #pragma unroll
-      for (int j = 0; j < 2; ++j) kx[j] = *reinterpret_cast<const float4*>(&sKX[(ss + 16 * j) * PM + c]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (i < 2 && j >= 2) continue;  // upper off-diagonal block: always masked
-          const float4 bb = (i >= 2 && j < 2) ? kx[j] : kr[j];
-          accA[i][j] += dot4(kl[i], bb);
-          accM[i][j] += dot4(ql[i], bb);
-        }
+      for (int e = 0; e < 4; ++e) {
+        const int r = ra + 8 * (e >> 1), sc = 8 * ni + 2 * ft + (e & 1);
+        if (isM) blob[L::M + r * L::PR + sc] = (sc <= r) ? acc[e] : 0.f;
+        else sA[r * 65 + sc] = (sc < r) ? sBeta[r] * acc[e] : 0.f;
+      }
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int r = rr + 16 * i, s = ss + 16 * j;
-        sA[r * 65 + s] = (s < r) ? sBeta[r] * accA[i][j] : 0.f;
-        blob[L::M + r * L::PR + s] = (s <= r) ? accM[i][j] : 0.f;
-      }
   }
   __syncthreads();
 
@@ -364,17 +353,40 @@ chunk_prep_cc(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     for (int e = 0; e < 4; ++e) sT[(32 + r) * 65 + c4 + e] = -z[e];
   }
   __syncthreads();
-  // T = X Diag(beta)
+  // T = X Diag(beta), re-laid at row pitch 68 over k * 2^(G - R) (free after the A/M products)
+  float* sT2 = sK;
   for (int i = tid; i < 64 * 64; i += kThreads) {
     const int r = i >> 6, c = i & 63;
-    sT[r * 65 + c] *= sBeta[c];
+    sT2[r * 68 + c] = sT[r * 65 + c] * sBeta[c];
   }
   __syncthreads();
 
-  // 6. W = T K_hat, U_hat = T V
-  tmul_store<DK>(sT, sG, PM, blob, [](int r, int j) { return L::W + r * L::PK + j; });
-  tmul_store<DV>(sT, sV, PM, blob,
-                 [](int r, int j) { return L::UH + (j / L::NC) * L::SLICE + r * L::PC + j % L::NC; });
+  // 6. [W | U_hat] = T [K_hat | V] as three-term tf32 MMAs (T lower triangular: tile row block mi
+  //    stops at column 16 mi + 15); warp w takes every eighth 16 x 8 tile
+  {
+    constexpr int NT = 4 * (DK + DV) / 8;
+    for (int q = 0; q < NT / 8; ++q) {
+      const int ti = warp + 8 * q;
+      const int mi = ti & 3, nj = ti >> 2;
+      const bool isW = nj < DK / 8;
+      const float* Bm = isW ? sG : sV;
+      const int nb = isW ? nj : nj - DK / 8;
+      const int ra = 16 * mi + fg;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kk = 0; kk < 16 * mi + 16; kk += 8) {
+        const float a[4] = {sT2[ra * 68 + kk + ft], sT2[(ra + 8) * 68 + kk + ft], sT2[ra * 68 + kk + ft + 4],
+                            sT2[(ra + 8) * 68 + kk + ft + 4]};
+        const float bv[2] = {Bm[(kk + ft) * PM + 8 * nb + fg], Bm[(kk + ft + 4) * PM + 8 * nb + fg]};
+        mma3(acc, a, bv);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = ra + 8 * (e >> 1), j = 8 * nb + 2 * ft + (e & 1);
+        if (isW) blob[L::W + r * L::PK + j] = acc[e];
+        else blob[L::UH + (j / L::NC) * L::SLICE + r * L::PC + j % L::NC] = acc[e];
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------------ serial state pass
@@ -442,34 +454,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 }
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// ---- warp-level tf32 MMA (mma.sync m16n8k8).  Fragments (g = lane / 4, t = lane % 4):
-// A (16 x 8) a0 (g, t), a1 (g+8, t), a2 (g, t+4), a3 (g+8, t+4); B (8 x 8, k x n) b0 (t, g), b1 (t+4, g);
-// C (16 x 8) c0 (g, 2t), c1 (g, 2t+1), c2 (g+8, 2t), c3 (g+8, 2t+1).
-__device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// x = hi + lo: hi = x with its low 13 mantissa bits cleared (exact in tf32), lo = x - hi (exact in
-// fp32, of which the MMA reads the top 19 bits): hi*hi + hi*lo + lo*hi is ~2^-20 relative
-struct Tf32x2 {
-  uint32_t hi, lo;
-};
-__device__ __forceinline__ Tf32x2 split_tf32(float x) {
-  const uint32_t h = __float_as_uint(x) & 0xFFFFE000u;
-  return {h, __float_as_uint(x - __uint_as_float(h))};
-}
-// D += A B with A (16 x 8) and B (8 x 8) given by their fp32 fragment values, three-term split
-__device__ __forceinline__ void mma3(float (&c)[4], const float (&a)[4], const float (&bv)[2]) {
-  const Tf32x2 a0 = split_tf32(a[0]), a1 = split_tf32(a[1]), a2 = split_tf32(a[2]), a3 = split_tf32(a[3]);
-  const Tf32x2 b0 = split_tf32(bv[0]), b1 = split_tf32(bv[1]);
-  mma_tf32(c, a0.lo, a1.lo, a2.lo, a3.lo, b0.hi, b1.hi);
-  mma_tf32(c, a0.hi, a1.hi, a2.hi, a3.hi, b0.lo, b1.lo);
-  mma_tf32(c, a0.hi, a1.hi, a2.hi, a3.hi, b0.hi, b1.hi);
 }
 
 template <int DK, int DV, typename Tin, typename Tout>
