@@ -40,6 +40,19 @@ def test_prefill_bf16_h32_t8192_d128():
     _check(inputs.PREFILL, device_gen=True)
 
 
+def test_prefill_bf16_h32_t8192_d64():
+    """The prefill workload's shape with 64-dim heads: the CUDA-core path (tensor-core products,
+    value-column clusters) over 128 chunks per chain."""
+    _check(dataclasses.replace(inputs.PREFILL, dk=64, dv=64, h0_std=0.1, name="prefill d64"), device_gen=True)
+
+
+def test_prefill_bf16_h32_t8192_d128_epilogue():
+    """The prefill workload with the fused RMSNorm + sigmoid gate: the tensor-core read-out's
+    epilogue specialisation (staged gate logits, batched row reductions) over the whole sequence."""
+    cfg = dataclasses.replace(inputs.PREFILL, epilogue=True, name="prefill epilogue")
+    _check(cfg, epilogue=True, device_gen=True)
+
+
 def test_varlen_bf16_8seqs_h32_d128_h0():
     _check(inputs.VARLEN, device_gen=True)
 
