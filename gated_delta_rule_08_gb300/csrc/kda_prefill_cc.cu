@@ -1,4 +1,5 @@
-// KDA chunked prefill on CUDA cores in fp32 (the fp32-input path).
+// KDA chunked prefill for fp32 inputs and 64-dim heads: fp32 arithmetic on the CUDA cores, with
+// the chunk products on the warp-level tensor cores as three-term tf32 MMAs (fp32-level accuracy).
 //
 // Kimi K3 report walk-through (kimi-k3-paper.pages.dev), section 2.5 / Eq. 4: the
 // sequence is cut into chunks of C = 64 tokens; a parallel intra-chunk part is
@@ -13,7 +14,7 @@
 //
 // Decay numerics (section 3.1-3.2, Eq. 5: g > -5): a pairwise factor exp(G_r - G_s)
 // is split as exp(G_r - R) exp(R - G_s) around a reference R so that A and M are
-// plain dot products.  One reference per 64-token chunk could need exp(+-320)
+// plain matrix products.  One reference per 64-token chunk could need exp(+-320)
 // (fp32 overflows past exp(88.7)), so the chunk uses two 32-token halves with centred
 // references (positions 15 and 47: every factor within exp(+-80)) for the two
 // diagonal 32x32 blocks, and the reference 47 for the off-diagonal block (its
@@ -24,9 +25,9 @@
 //   chunk_prep_cc : one CTA per (chunk, head), fully parallel; writes the chunk's
 //                   W, U_hat, Q_hat, K_bar, M and exp(G_last) into the workspace.
 //   chunk_scan_cc : one cluster of dv / 16 CTAs per (sequence, head), each walking the
-//                   chunks in order with 16 value columns of the state in shared memory;
-//                   writes outputs (with the optional RMSNorm + sigmoid gate epilogue) and
-//                   the final state.
+//                   chunks in order with 16 value columns of the state (registers, and a
+//                   transposed copy in shared memory); writes outputs (with the optional
+//                   RMSNorm + sigmoid gate epilogue) and the final state.
 #include <algorithm>
 
 #include "kda_device.cuh"
@@ -39,9 +40,9 @@ namespace {
 constexpr int kThreads = 256;
 
 // One (chunk, head) record of the chunkwise operands in the workspace, laid out as the serial
-// pass's shared-memory image: row pitches of 4 floats past a multiple of 32 keep that pass's
-// row-parallel float4 reads free of bank conflicts, and one bulk copy moves W .. Gamma while a
-// second moves the CTA's 16-column slice of U_hat (stored slice-major).
+// pass's shared-memory image: row pitches of 4 floats past a multiple of 32 keep that pass's MMA
+// fragment loads free of bank conflicts, and one bulk copy moves W .. Gamma while a second moves
+// the CTA's 16-column slice of U_hat (stored slice-major).
 template <int DK, int DV>
 struct CcBlob {
   static constexpr int NC = 16, NS = DV / NC;             // value-column slices of the serial pass
@@ -396,10 +397,9 @@ chunk_prep_cc(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
 // (the repeats hit L2).  The one exchange is the RMSNorm's sum of squares over a token's dv
 // outputs (gate epilogue only): each CTA stores its 16-column partial sums into every CTA of the
 // cluster (distributed shared memory) by st.async, whose bytes complete the peer's mbarrier
-// phase, and normalises a chunk's
-// outputs one chunk later, so that the exchange overlaps the next chunk's products.  The next
-// chunk's record arrives by bulk copy while the current one is used (two stages where shared
-// memory allows).
+// phase, and normalises a chunk's outputs one chunk later, so that the exchange overlaps the next
+// chunk's products.  The next chunk's record arrives by bulk copy while the current one is used
+// (two stages where shared memory allows).
 template <int DK, int DV>
 struct CcScan {
   using L = CcBlob<DK, DV>;
