@@ -23,8 +23,10 @@
  *     affected rows are skipped, never trapped on.
  *   - dk, dv must each be 64 or 128 and C must be 64 (KDA_ERR_UNSUPPORTED otherwise).
  *   - `dtype` is the element type of q, k, v and the gate logits; `out_dtype` that of out
- *     (either may be bf16 or fp32).  bf16 inputs run on the tensor-core path; fp32 inputs
- *     run on an fp32 CUDA-core path (slower, ~1e-6 relative error).  The read-out is
+ *     (either may be bf16 or fp32).  bf16 prefill inputs with dk = dv = 128 run on the tcgen05
+ *     tensor-core path.  fp32 inputs, and bf16 inputs with dk or dv = 64, run on a path with
+ *     fp32 arithmetic whose chunk products are three-term tf32 warp MMAs (fp32-level accuracy:
+ *     about 3e-5 max|err|/RMS against an fp64 reference over 8192 tokens).  The read-out is
  *     computed in fp32 and rounded once when stored in out_dtype.
  *   - Value range of the bf16 tensor-core path (prefill with dk = dv = 128): the values, the
  *     intra-chunk terms built from them (beta v, U_hat = T V, U = U_hat - W S) and the running
