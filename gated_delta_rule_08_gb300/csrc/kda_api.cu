@@ -312,7 +312,8 @@ kda_status decode_common(const void* q, const void* k, const void* v, const floa
   if (epi && work && !epi->gate_logits) return KDA_ERR_INVALID_ARG;
   if (epi && !(epi->eps >= 0.f)) return KDA_ERR_INVALID_ARG;
   if ((int64_t)N * H > 0x7fffffff || (int64_t)N * n_tok * H > 0x7fffffff) return KDA_ERR_UNSUPPORTED;
-  if (!aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
+  // v and the gate logits are staged into shared memory by 16-byte asynchronous copies
+  if (!aligned16(state_pool) || !aligned16(v) || (epi && !aligned16(epi->gate_logits))) return KDA_ERR_INVALID_ARG;
   unsigned int* err = nullptr;
   int major = 0, minor = 0;
   kda_status st = device_state(&err, &major, &minor);

@@ -12,7 +12,7 @@
  * General conventions for every entry point:
  *   - All tensor pointers are caller-owned DEVICE memory, dense, row-major, in the
  *     layouts stated per argument, and 16-byte aligned (KDA_ERR_INVALID_ARG otherwise;
- *     for decode only the state pool must be).  The library never allocates device memory and
+ *     for decode only the state pool, v and the gate logits must be).  The library never allocates device memory and
  *     never frees anything it is given.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL means
  *     the legacy default stream).  The call returns after validation and launch.

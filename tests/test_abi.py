@@ -103,6 +103,18 @@ def test_multi_token_and_checkpoint_arguments_rejected_without_launch(lib):
                                 None, None) == 1
     assert lib.kda_decode_multi(fake, fake, fake, fake, fake, fake, fake, None, fake, 4, 3, 2, 128, 96, 8, 0, 0, 0,
                                 None, None) == 2
+    # decode: v and the gate logits must be 16-byte aligned (the state pool too)
+    odd = P(0x1008)
+    assert lib.kda_decode_multi(fake, fake, odd, fake, fake, fake, fake, None, fake, 4, 3, 2, 128, 128, 8, 0, 0, 0,
+                                None, None) == 1
+    assert lib.kda_decode_step(fake, fake, odd, fake, fake, fake, fake, fake, 4, 2, 128, 128, 8, 0, 0, None,
+                               None) == 1
+    assert lib.kda_decode_step(fake, fake, fake, fake, fake, odd, fake, fake, 4, 2, 128, 128, 8, 0, 0, None,
+                               None) == 1
+    from gated_delta_rule_08_gb300.binding import _Epilogue
+    epi = _Epilogue(0x1008, None, 1e-6)
+    assert lib.kda_decode_multi(fake, fake, fake, fake, fake, fake, fake, None, fake, 4, 3, 2, 128, 128, 8, 0, 0, 0,
+                                ctypes.byref(epi), None) == 1
     # checkpoints: no state buffer, interval < 1, misaligned buffer
     args = (fake, fake, fake, fake, fake, None, None, P(0x2000), None)
     tail = (1, 64, 1, 128, 128, 64, 0, 0, None, fake, 1 << 20, None)
