@@ -225,7 +225,7 @@ decode_group_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const 
                     const float* __restrict__ g, const float* __restrict__ beta, float* __restrict__ pool,
                     const int32_t* __restrict__ slot_idx, Tout* __restrict__ out, int H, int num_slots, int n_tok,
                     const int32_t* __restrict__ ntok_per_req, int commit, const Tin* __restrict__ gate,
-                    const float* __restrict__ norm_w, float eps, unsigned int* __restrict__ err) {
+                    const float* __restrict__ norm_w, float eps, unsigned int* __restrict__ err, int pf_lead) {
   constexpr int NST = kStageTok;
   constexpr int TPR = DV / 4;               // threads per state row
   constexpr int NG = kDecodeThreads / TPR;  // row groups
@@ -291,6 +291,38 @@ decode_group_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const 
 #pragma unroll
   for (int i = 0; i < RPG; ++i)
     s[i] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(rg * RPG + i) * DV) + cg);
+
+  // Warm L2 with the state and inputs of the CTA that will take this one's place (pf_lead = the
+  // number of CTAs resident at once), so that HBM keeps streaming while the resident CTAs compute:
+  // the state by four bulk prefetches (the pool is 16-byte aligned), each input row line by line.
+  if (pf_lead > 0 && nh + pf_lead < (int)gridDim.x) {
+    const int nh2 = nh + pf_lead;
+    const int n2 = nh2 / H, h2 = nh2 - (nh2 / H) * H;
+    if (tid >= kDecodeThreads - 4) {
+      const int slot2 = slot_idx[n2];
+      if (slot2 >= 0 && slot2 < num_slots)
+        prefetch_l2(pool + ((size_t)slot2 * H + h2) * (size_t)(DK * DV) + (tid - (kDecodeThreads - 4)) * (DK * DV / 4),
+                    DK * DV);
+    }
+    for (int i = tid; i < 5 * n_tok; i += kDecodeThreads) {
+      const int t = i / 5, a = i - 5 * t;
+      const size_t r2 = ((size_t)n2 * n_tok + t) * H + h2;
+      const char* p = nullptr;
+      int bytes = 0;
+      if (a == 0) {
+        p = reinterpret_cast<const char*>(k + r2 * DK), bytes = DK * (int)sizeof(Tin);
+      } else if (a == 1) {
+        p = reinterpret_cast<const char*>(q + r2 * DK), bytes = DK * (int)sizeof(Tin);
+      } else if (a == 2) {
+        p = reinterpret_cast<const char*>(g + r2 * DK), bytes = DK * 4;
+      } else if (a == 3) {
+        p = reinterpret_cast<const char*>(v + r2 * DV), bytes = DV * (int)sizeof(Tin);
+      } else if (gate != nullptr) {
+        p = reinterpret_cast<const char*>(gate + r2 * DV), bytes = DV * (int)sizeof(Tin);
+      }
+      for (int o = 0; o < bytes; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o));
+    }
+  }
 
   extern __shared__ float4 dsm4[];
   float4* part = dsm4;  // [2 NST][NG][TPR]: per-row-group partial reductions (a_t, then b_t)
@@ -490,17 +522,24 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t st) {
   TraceScope ts("kda_decode", st);
   if (a.n_tok > 1) {  // several tokens per request: the grouped chunk form
     static DeviceOnce once;
+    static int lead[kMaxDevices];  // CTAs resident at once, written under the once-lock
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-    const cudaError_t e = once.run(dev, [] {
-      return cudaFuncSetAttribute(decode_group_kernel<DK, DV, Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)group_smem<DK, DV>());
+    const cudaError_t e = once.run(dev, [dev] {
+      auto kern = decode_group_kernel<DK, DV, Tin, Tout>;
+      cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)group_smem<DK, DV>());
+      int per_sm = 0, sms = 0;
+      if (r == cudaSuccess)
+        r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, group_smem<DK, DV>());
+      if (r == cudaSuccess) r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (r == cudaSuccess) lead[dev] = per_sm * sms;
+      return r;
     });
     if (e != cudaSuccess) return e;
     decode_group_kernel<DK, DV, Tin, Tout><<<rows, kDecodeThreads, group_smem<DK, DV>(), st>>>(
         static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta,
         a.state_pool, a.slot_idx, static_cast<Tout*>(a.out), a.H, a.num_slots, a.n_tok, a.ntok_per_req,
-        a.commit ? 1 : 0, static_cast<const Tin*>(a.epi.gate), a.epi.norm_weight, a.epi.eps, a.err);
+        a.commit ? 1 : 0, static_cast<const Tin*>(a.epi.gate), a.epi.norm_weight, a.epi.eps, a.err, lead[dev]);
     return cudaGetLastError();
   }
   auto kern = decode_kernel<DK, DV, Tin, Tout>;

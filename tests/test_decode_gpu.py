@@ -186,9 +186,9 @@ def test_decode_multi_bad_count_sets_flag_and_skips_request():
 
 
 def test_decode_multi_many_items_per_cta():
-    """More (request, head) items than the persistent multi-token grid has CTAs, so each CTA runs
-    several items and copies the next one's state while it computes: verify (no write-back) and
-    accept with per-request counts from 0 to 4 against the oracle."""
+    """More (request, head) items (1280) than CTAs resident at once, so CTAs warm L2 with the state
+    and inputs of the ones that follow them: verify (no write-back) and accept with per-request
+    counts from 0 to 4 against the oracle."""
     cfg = dataclasses.replace(inputs.DECODE, N=160, H=8, num_slots=400, seed=99)
     inp = _multi(cfg, 4)
     before = inp["state_pool"].clone()
@@ -217,8 +217,9 @@ def test_decode_multi_many_items_per_cta():
 
 
 def test_decode_multi_bad_slot_among_many_items():
-    """A request with an out-of-range slot is skipped by the persistent multi-token grid (flag
-    set, its outputs untouched) and every other request is still served."""
+    """A request with an out-of-range slot is skipped by the multi-token kernel (flag set, its
+    outputs untouched) and every other request is still served.  Its items come late enough in the
+    grid that earlier CTAs try to prefetch its state, which must skip the bad slot too."""
     cfg = dataclasses.replace(inputs.DECODE, N=100, H=8, num_slots=300, seed=101)
     inp = _multi(cfg, 3)
     good = inp["slot_idx"].clone()
@@ -226,12 +227,12 @@ def test_decode_multi_bad_slot_among_many_items():
                                    commit=False)
     assert_no_device_error()
     bad = good.clone()
-    bad[37] = cfg.num_slots + 5
+    bad[77] = cfg.num_slots + 5
     out = torch.full_like(ref, 3.0)
     binding.kda_decode_multi(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state_pool"], bad, out=out,
                              commit=False)
     assert binding.kda_get_device_error() & binding.DEVERR_BAD_SLOT
-    assert torch.all(out[37] == 3.0)
+    assert torch.all(out[77] == 3.0)
     keep = torch.ones(cfg.N, dtype=torch.bool, device="cuda")
-    keep[37] = False
+    keep[77] = False
     assert torch.equal(out[keep], ref[keep])
