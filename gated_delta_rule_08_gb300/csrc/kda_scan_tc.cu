@@ -15,7 +15,7 @@
 // segments, S_in(p+1) = P_p S_in(p) + b_p for p >= 1, and a last pass re-runs every segment from
 // its S_in with outputs.
 //
-//  kda_tc_chunk_scan<Tout, MODE> (grid = sequences x heads x segments, 13 warps):
+//  kda_tc_chunk_scan<Tout, MODE> (grid = sequences x heads x segments, 16 warps):
 //    the state^T (dv x dk, fp32) lives in TMEM for the whole segment, next to an fp16 copy that
 //    is the A operand (read from TMEM) of the first fused product
 //      [D_U | D_O] = S^T [W^T | Q_hat^T]                      (8 MMAs, N = 128)
@@ -27,7 +27,8 @@
 //      D_U -> U^T and the updated state -> its fp16 copy, and apply the decay;
 //    MODE 0 (read-out): warps 8-11 drain D_O off the serial path: a full chunk without the
 //      epilogue straight from registers (each store writes 32 consecutive dv of a token), else
-//      through a staging buffer with the optional RMSNorm + gate epilogue;
+//      through a staging buffer with the optional RMSNorm + gate epilogue, whose rows warps
+//      13-15 share with them (seven warps on a chunk's 64 rows);
 //    MODE 1 (transition): z = 0 runs segment 0 from h0 (its final state is S_in(1)); for p >= 1,
 //      z = 2 p - 1 + kind, kind 0 runs b_p and kind 1 runs P_p; no read-out.
 //    segment map (context parallelism across devices, section 13.3.2): MODE 1 over one token range
@@ -52,13 +53,14 @@ namespace {
 
 using namespace tcx;
 
-constexpr int kScanThreads = 416;
+constexpr int kScanThreads = 512;
+constexpr int kEpiWarps = 7;                     // warps 8-11 and 13-15 (with the epilogue)
 constexpr int kStateThreads = 256;               // warps 0-7
 constexpr int kIssuerWarp = 12;
 constexpr int kStages = 3;                       // records staged up to two chunks ahead
 constexpr uint32_t kStage = 59392;               // staged record bytes, 1024-aligned
 constexpr uint32_t S_OUT = kStages * kStage;     // fp32 read-out staging [64 r][128 dv]
-constexpr uint32_t S_GATE = S_OUT + 32768;       // gate logits of a chunk: [4 warps][16 rows][32 lanes] x 8 B
+constexpr uint32_t S_GATE = S_OUT + 32768;       // gate logits of a chunk: [64 rows][32 lanes] x 8 B
 constexpr uint32_t S_BAR = S_GATE + 16384;       // barriers + tmem slot + abort flag
 constexpr uint32_t S_END = S_BAR + 128;
 constexpr uint32_t kScanSmem = S_END + 1024;
@@ -417,16 +419,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
     if (!ok) *abort_flag = 1;
     if (!isfinite(fsum)) atomicOr(p.err, KDA_DEVERR_NONFINITE);
   } else if (MODE == 0) {
-    // ======================== output warps: D_O -> staging -> epilogue -> global
+    // ======================== output warps 8-11: D_O -> staging -> epilogue -> global; with the
+    // epilogue, warps 13-15 join them on the staged rows (seven warps share a chunk's 64 rows)
     // (two specialisations: without the epilogue, and with it; the gate's global loads of the
     // latter are copied into shared memory while D_O is produced)
     float* ost = reinterpret_cast<float*>(sm + S_OUT);
-    const int ow = warp - 8;
+    const bool tw = warp < kIssuerWarp;       // reads D_O from TMEM lane quadrant warp & 3
+    const int ow = tw ? warp - 8 : warp - 9;  // 0-3 the TMEM warps, 4-6 the epilogue helpers
     Tout* out = static_cast<Tout*>(p.out);
     bool ok = true;
     auto readout = [&](auto epi_tag) {
       constexpr bool EPI = decltype(epi_tag)::value;
-      uint2* sgate = reinterpret_cast<uint2*>(sm + S_GATE) + ow * 16 * 32 + lane;  // this warp's [16 rows] x 32 lanes
+      if (!EPI && !tw) return;
+      constexpr int kEw = kEpiWarps, kRows = (64 + kEpiWarps - 1) / kEpiWarps;
+      uint2* sgate = reinterpret_cast<uint2*>(sm + S_GATE) + lane;  // [64 rows][32 lanes]
       float4 wv = make_float4(1.f, 1.f, 1.f, 1.f);  // RMSNorm weight of this lane's four dv
       if (EPI && p.norm_w != nullptr)
         wv = make_float4(p.norm_w[4 * lane], p.norm_w[4 * lane + 1], p.norm_w[4 * lane + 2], p.norm_w[4 * lane + 3]);
@@ -435,41 +441,64 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
         const int64_t rem = len - 64 * cg;
         const int n = (int)(rem < 64 ? rem : 64);
         const int64_t t0 = t_begin + 64 * cg;
-        if constexpr (EPI) {
-          // the gate logits of this warp's rows, each lane its own 8 bytes
-#pragma unroll 1
-          for (int r = ow, i = 0; r < n; r += 4, ++i)
-            cp_async8(sgate + i * 32, p.gate + ((size_t)(t0 + r) * H + h) * 128 + 4 * lane);
-          cp_async_commit();
-        }
-        ok = group_and(2, 128, wait_or_abort_t<GIVEUP>(bar_s, (uint32_t)(c & 1), abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        float o[64];
-        tmem_ld64b(tl + T_DO, o);
-        tc_fence_before();
-        group_sync(2, 128);
-        if (ow == 0 && lane == 0) mbar_arrive(do_free);
-        if (!EPI && n == 64 && sizeof(Tout) == 2) {
-          // full chunk, plain bf16 output: each warp instruction writes 32 consecutive dv of a token
-          __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(out) + (size_t)t0 * H * 128 + (size_t)h * 128 + row;
+        if constexpr (!EPI) {
+          ok = group_and(2, 128, wait_or_abort_t<GIVEUP>(bar_s, (uint32_t)(c & 1), abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          float o[64];
+          tmem_ld64b(tl + T_DO, o);
+          tc_fence_before();
+          group_sync(2, 128);
+          if (ow == 0 && lane == 0) mbar_arrive(do_free);
+          if (n == 64 && sizeof(Tout) == 2) {
+            // full chunk, plain bf16 output: each warp instruction writes 32 consecutive dv of a token
+            __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(out) + (size_t)t0 * H * 128 + (size_t)h * 128 + row;
 #pragma unroll
-          for (int r = 0; r < 64; ++r) {
-            ob[(size_t)r * H * 128] = __float2bfloat16_rn(o[r]);
-            if ((r & 7) == 7) __nanosleep(64);  // spread the stores over the chunk period
+            for (int r = 0; r < 64; ++r) {
+              ob[(size_t)r * H * 128] = __float2bfloat16_rn(o[r]);
+              if ((r & 7) == 7) __nanosleep(64);  // spread the stores over the chunk period
+            }
+            continue;
           }
-          continue;
-        }
 #pragma unroll
-        for (int r = 0; r < 64; ++r) ost[r * 128 + row] = o[r];
-        if constexpr (EPI) cp_async_wait_all();  // this lane's gate copies
-        group_sync(2, 128);
-        if constexpr (EPI) {
-          // the sums of squares of this warp's 16 rows first, reduced together (16 independent chains)
-          float ss[16];
+          for (int r = 0; r < 64; ++r) ost[r * 128 + row] = o[r];
+          group_sync(2, 128);
+          for (int r = ow; r < n; r += 4) {
+            const float4 y = *reinterpret_cast<const float4*>(ost + r * 128 + 4 * lane);
+            store_row(out + ((size_t)(t0 + r) * H + h) * 128 + 4 * lane, y);
+          }
+          group_sync(2, 128);  // staging buffer free for the next chunk
+        } else {
+          {
+            // the gate logits of this warp's rows, each lane its own 8 bytes
+            const __nv_bfloat16* gp = p.gate + ((size_t)(t0 + ow) * H + h) * 128 + 4 * lane;
+            const size_t gstep = (size_t)kEw * H * 128;
+#pragma unroll 1
+            for (int r = ow, i = 0; r < n; r += kEw, ++i) cp_async8(sgate + r * 32, gp + i * gstep);
+            cp_async_commit();
+          }
+          if (tw) {
+            ok = group_and(2, 128, wait_or_abort_t<GIVEUP>(bar_s, (uint32_t)(c & 1), abort_flag));
+            if (ok) {
+              tc_fence_after();
+              float o[64];
+              tmem_ld64b(tl + T_DO, o);
+              tc_fence_before();
+              group_sync(2, 128);
+              if (ow == 0 && lane == 0) mbar_arrive(do_free);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int r = ow + 4 * i;
+              for (int r = 0; r < 64; ++r) ost[r * 128 + row] = o[r];
+            }
+          }
+          cp_async_wait_all();  // this lane's gate copies
+          // the staged chunk (and every warp's decision to go on) to all seven warps
+          ok = group_and(3, 32 * kEw, ok);
+          if (!ok) break;
+          // the sums of squares of this warp's rows first, reduced together (independent chains)
+          float ss[kRows];
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) {
+            const int r = ow + kEw * i;
             const float4 y = r < n ? *reinterpret_cast<const float4*>(ost + r * 128 + 4 * lane)
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
             ss[i] = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
@@ -477,15 +506,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
 #pragma unroll
           for (int m = 16; m > 0; m >>= 1)
 #pragma unroll
-            for (int i = 0; i < 16; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], m);
+            for (int i = 0; i < kRows; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], m);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int r = ow + 4 * i;
+          for (int i = 0; i < kRows; ++i) {
+            const int r = ow + kEw * i;
             if (r >= n) break;
             float4 y = *reinterpret_cast<const float4*>(ost + r * 128 + 4 * lane);
             const size_t orow = ((size_t)(t0 + r) * H + h) * 128 + 4 * lane;
             const float inv = rsqrtf(ss[i] * (1.f / 128.f) + p.eps);
-            const uint2 gw = sgate[i * 32];
+            const uint2 gw = sgate[r * 32];
             const float2 g01 = unpack_bf2(gw.x), g23 = unpack_bf2(gw.y);
             y.x = y.x * inv * wv.x * sigmoidf_(g01.x);
             y.y = y.y * inv * wv.y * sigmoidf_(g01.y);
@@ -493,13 +522,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
             y.w = y.w * inv * wv.w * sigmoidf_(g23.y);
             store_row(out + orow, y);
           }
-        } else {
-          for (int r = ow; r < n; r += 4) {
-            const float4 y = *reinterpret_cast<const float4*>(ost + r * 128 + 4 * lane);
-            store_row(out + ((size_t)(t0 + r) * H + h) * 128 + 4 * lane, y);
-          }
+          group_sync(3, 32 * kEw);  // staging buffer and gate rows free for the next chunk
         }
-        group_sync(2, 128);  // staging buffer free for the next chunk
       }
     };
     if (p.gate != nullptr) readout(std::true_type{});
