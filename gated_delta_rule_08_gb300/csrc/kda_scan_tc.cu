@@ -53,6 +53,14 @@ namespace {
 
 using namespace tcx;
 
+// sigmoid(x) = (1 + tanh(x / 2)) / 2 with the hardware tanh approximation (relative error about
+// 2^-11): one special-function operation instead of an exponential and a reciprocal
+__device__ __forceinline__ float sigmoid_tanh(float x) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+  return fmaf(0.5f, t, 0.5f);
+}
+
 constexpr int kScanThreads = 512;
 constexpr int kEpiWarps = 7;                     // warps 8-11 and 13-15 (with the epilogue)
 constexpr int kStateThreads = 256;               // warps 0-7
@@ -516,10 +524,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
             const float inv = rsqrtf(ss[i] * (1.f / 128.f) + p.eps);
             const uint2 gw = sgate[r * 32];
             const float2 g01 = unpack_bf2(gw.x), g23 = unpack_bf2(gw.y);
-            y.x = y.x * inv * wv.x * sigmoidf_(g01.x);
-            y.y = y.y * inv * wv.y * sigmoidf_(g01.y);
-            y.z = y.z * inv * wv.z * sigmoidf_(g23.x);
-            y.w = y.w * inv * wv.w * sigmoidf_(g23.y);
+            y.x = y.x * inv * wv.x * sigmoid_tanh(g01.x);
+            y.y = y.y * inv * wv.y * sigmoid_tanh(g01.y);
+            y.z = y.z * inv * wv.z * sigmoid_tanh(g23.x);
+            y.w = y.w * inv * wv.w * sigmoid_tanh(g23.y);
             store_row(out + orow, y);
           }
           group_sync(3, 32 * kEw);  // staging buffer and gate rows free for the next chunk
