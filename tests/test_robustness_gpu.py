@@ -53,16 +53,18 @@ def test_values_beyond_the_fp16_range_set_the_flag(v_scale, h0_scale):
 
 
 # ------------------------------------------------------------------ bounded waits that run out
-@pytest.mark.parametrize("lengths,H", [((300, 70), 2), ((8192,), 4)], ids=["one-pass", "split-into-segments"])
-def test_waits_that_run_out_are_reported_and_the_device_stays_usable(lengths, H, monkeypatch):
+@pytest.mark.parametrize("lengths,H,epilogue", [((300, 70), 2, False), ((8192,), 4, False), ((8192,), 4, True)],
+                         ids=["one-pass", "split-into-segments", "split-with-epilogue"])
+def test_waits_that_run_out_are_reported_and_the_device_stays_usable(lengths, H, epilogue, monkeypatch):
     """KDA_TEST_WAIT_TIMEOUT=1 launches kernel variants whose waits on work of their own CTA give up at
     once, as a wait that runs out does (the drains of in-flight copies and MMAs keep their normal
     bound).  The call reports
     KDA_DEVERR_WAIT_TIMEOUT; the next ordinary call on the same stream matches the oracle, so every
     CTA released its tensor memory and the context is intact.  The second case runs the segment
-    transitions, the merge and the read-out pass (intra-device context parallelism)."""
+    transitions, the merge and the read-out pass (intra-device context parallelism); the third adds
+    the gate epilogue, whose helper warps must leave their loop when a TMEM warp's wait gives up."""
     cfg = inputs.PrefillConfig("timeout", H=H, dk=128, dv=128, dtype="bf16", lengths=lengths, B=len(lengths),
-                               h0_std=0.1, z_mean=-8.0, seed=603)
+                               h0_std=0.1, z_mean=-8.0, seed=603, epilogue=epilogue)
     inp = inputs.prefill_inputs(cfg, device="cuda")
     monkeypatch.setenv("KDA_TEST_WAIT_TIMEOUT", "1")
     run_prefill(inp, out_dtype=torch.float32)
