@@ -1,10 +1,12 @@
 """One workload of the hot path, run alone a few times: a target for a profiler (ncu) that should
 see one kernel family on a small device footprint.
 
-    python -m gated_delta_rule_08_gb300.profile_cases prefill|varlen|decode|verify|backward|prefill_d64|prefill_d64_epi
+    python -m gated_delta_rule_08_gb300.profile_cases prefill|prefill_epi|varlen|decode|verify|backward|prefill_d64|
+        prefill_d64_epi
         [--calls N]
 
 prefill      B=1, H=32, T=8192, dk=dv=128, bf16 (q, k, v, g, beta: 337 MB; records 310 MB)
+prefill_epi  the same with the RMSNorm + sigmoid gate epilogue
 varlen       8 sequences, 27,654 tokens, H=32, dk=dv=128, bf16, h0
 decode       N=256 requests, H=32, 1024-slot fp32 pool (2 GiB), RMSNorm + gate
 verify       the decode workload with 4 draft tokens per request, pool not written
@@ -37,14 +39,14 @@ def _prefill(cfg, calls, dev):
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill", "varlen", "decode", "verify", "backward", "prefill_d64",
+    ap.add_argument("case", choices=["prefill", "prefill_epi", "varlen", "decode", "verify", "backward", "prefill_d64",
                                      "prefill_d64_epi"])
     ap.add_argument("--calls", type=int, default=2)
     args = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if args.case == "prefill":
-        _prefill(inputs.PREFILL, args.calls, dev)
+    if args.case in ("prefill", "prefill_epi"):
+        _prefill(dataclasses.replace(inputs.PREFILL, epilogue=args.case == "prefill_epi"), args.calls, dev)
     elif args.case == "varlen":
         _prefill(inputs.VARLEN, args.calls, dev)
     elif args.case in ("prefill_d64", "prefill_d64_epi"):
