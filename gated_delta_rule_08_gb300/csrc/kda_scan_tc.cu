@@ -484,6 +484,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) kda_tc_chunk_scan(const ScanP
 #pragma unroll 1
             for (int r = ow, i = 0; r < n; r += kEw, ++i) cp_async8(sgate + r * 32, gp + i * gstep);
             cp_async_commit();
+            // the next chunk's rows of this warp into L2, one 128-byte line per lane
+            if (c + 1 < ncs) {
+              const int64_t rem1 = len - 64 * (cg + 1);
+              const int n1 = (int)(rem1 < 64 ? rem1 : 64);
+              const int r1 = ow + kEw * (lane >> 1);
+              if (r1 < n1)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p.gate + ((size_t)(t0 + 64 + r1) * H + h) * 128 + 64 * (lane & 1)));
+            }
           }
           if (tw) {
             ok = group_and(2, 128, wait_or_abort_t<GIVEUP>(bar_s, (uint32_t)(c & 1), abort_flag));
