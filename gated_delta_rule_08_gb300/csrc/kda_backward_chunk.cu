@@ -25,6 +25,8 @@
 //   bwd_dvsums per (chunk, head): the products summed over the value columns, and dv;
 //   bwd_grads  per (chunk, head): the parameter gradients.
 // Global memory is written row by row: a transposed copy is assembled in shared memory first.
+#include <type_traits>
+
 #include "kda_device.cuh"
 #include "kda_internal.h"
 
@@ -34,42 +36,6 @@ namespace {
 constexpr int kC = 64;         // chunk length
 constexpr int kThreads = 256;  // every kernel here
 static_assert(kThreads == 4 * kC, "the diagonal inverses in bwd_rec give each column four lanes");
-
-// acc[i][j] += sum_{k < K} At[k * lda + m0 + i] * B[k * ldb + n0 + (j / 4) * GS + j % 4]: a register
-// tile of a product whose operands are both stored k-major (At: the left factor transposed).  MI and
-// NJ are multiples of 4; lda, ldb, m0, n0 and GS are multiples of 4 (16-byte vector loads).  With
-// GS = 64 and n0 = 4 x (thread mod 16), sixteen threads read 256 contiguous bytes of B per load.
-template <int MI, int NJ, int GS = 4>
-__device__ __forceinline__ void kgemm(float (&acc)[MI][NJ], const float* At, int lda, int m0, const float* B, int ldb,
-                                      int n0, int K) {
-#pragma unroll 8  // K is a multiple of 8: eight k-steps of loads in flight
-  for (int k = 0; k < K; ++k) {
-    float a[MI], b[NJ];
-#pragma unroll
-    for (int i = 0; i < MI; i += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(At + (size_t)k * lda + m0 + i);
-      a[i] = x.x; a[i + 1] = x.y; a[i + 2] = x.z; a[i + 3] = x.w;
-    }
-#pragma unroll
-    for (int j = 0; j < NJ; j += 4) {
-      const float4 y = *reinterpret_cast<const float4*>(B + (size_t)k * ldb + n0 + (j / 4) * GS);
-      b[j] = y.x; b[j + 1] = y.y; b[j + 2] = y.z; b[j + 3] = y.w;
-    }
-#pragma unroll
-    for (int i = 0; i < MI; ++i)
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-  }
-}
-// column of element j of a tile loaded with group stride 64 (the j-th value of kgemm<.., NJ, 64>)
-__device__ __forceinline__ constexpr int wide_col(int j) { return 64 * (j >> 2) + (j & 3); }
-template <int MI, int NJ>
-__device__ __forceinline__ void zero(float (&acc)[MI][NJ]) {
-#pragma unroll
-  for (int i = 0; i < MI; ++i)
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) acc[i][j] = 0.f;
-}
 
 // ---- warp-level tensor-core products (mma.sync m16n8k8, tf32) with a three-term split: each operand
 // x = hi + lo with hi = x truncated to tf32 (its low 13 mantissa bits cleared) and lo = x - hi (exact
@@ -91,8 +57,10 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
 // separately (no MMA waits on the one before it in the same k step) and are added at the end.
 // Lane (g = lane / 4, t = lane % 4) holds acc[nt][0..1] at row m0 + g, columns n0 + 8 nt + 2t, +1,
 // and acc[nt][2..3] eight rows below.
-// With AT = false the left operand is given row-major instead (A[m * lda + k]).
-template <int NT, bool AT = true>
+// With AT = false the left operand is given row-major instead (A[m * lda + k]).  AX (BX) declares every
+// value of the left (right) operand exact in tf32, a widened bf16 input: its low part is zero, so the
+// product term that would multiply it is skipped (the result is bit-identical).
+template <int NT, bool AT = true, bool AX = false, bool BX = false>
 __device__ __forceinline__ void warp_mma(float (&acc)[NT][4], const float* At, int lda, int m0, const float* B,
                                          int ldb, int n0, int K, int lane) {
   const int g = lane >> 2, t = lane & 3;
@@ -111,8 +79,8 @@ __device__ __forceinline__ void warp_mma(float (&acc)[NT][4], const float* At, i
       split_tf32(B[(k0 + t) * ldb + n0 + 8 * nt + g], bh0, bl0);
       split_tf32(B[(k0 + t + 4) * ldb + n0 + 8 * nt + g], bh1, bl1);
       mma_tf32(acc[nt], ah, bh0, bh1);
-      mma_tf32(hl[nt], ah, bl0, bl1);
-      mma_tf32(lh[nt], al, bh0, bh1);
+      if constexpr (!BX) mma_tf32(hl[nt], ah, bl0, bl1);
+      if constexpr (!AX) mma_tf32(lh[nt], al, bh0, bh1);
     }
   }
 #pragma unroll
@@ -120,6 +88,9 @@ __device__ __forceinline__ void warp_mma(float (&acc)[NT][4], const float* At, i
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[nt][e] += hl[nt][e] + lh[nt][e];
 }
+// inputs stored as bf16 (8 significant bits) are exact in tf32 once widened to fp32
+template <typename Tin>
+constexpr bool kExactInput = std::is_same<Tin, __nv_bfloat16>::value;
 // the fragment element e of tile nt of a warp_mma accumulator: its row and column
 __device__ __forceinline__ int frag_row(int m0, int lane, int e) { return m0 + (lane >> 2) + 8 * (e >> 1); }
 __device__ __forceinline__ int frag_col(int n0, int lane, int nt, int e) { return n0 + 8 * nt + 2 * (lane & 3) + (e & 1); }
@@ -455,7 +426,7 @@ bwd_rec(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restr
       int m0, n0;
       TE::at(warp, m0, n0);
       float acc[TE::NT][4] = {};
-      warp_mma<TE::NT>(acc, TT, LC, m0, vS, LE, n0, kC, lane);
+      warp_mma<TE::NT, true, false, kExactInput<Tin>>(acc, TT, LC, m0, vS, LE, n0, kC, lane);
       frag_store<TE::NT>(rec + L.Uh(), E, acc, m0, n0, lane, 1.f);
     }
     __syncthreads();
@@ -665,7 +636,7 @@ bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const floa
       int m0, n0;
       TU::at(warp, m0, n0);
       float acc[TU::NT][4] = {};
-      warp_mma<TU::NT>(acc, Ms, LC, m0, dO, LS, n0, kC, lane);
+      warp_mma<TU::NT, true, false, kExactInput<Tin>>(acc, Ms, LC, m0, dO, LS, n0, kC, lane);
       warp_mma<TU::NT>(acc, KbTs, LC, m0, dS, LS, n0, D, lane);
 #pragma unroll
       for (int nt = 0; nt < TU::NT; ++nt)
@@ -681,7 +652,7 @@ bwd_rev(const float* __restrict__ recs, const Tin* __restrict__ dout, const floa
       int m0, n0;
       TS::at(warp, m0, n0);
       float a1[TS::NT][4] = {}, a2[TS::NT][4] = {};
-      warp_mma<TS::NT>(a1, Qhs, LD, m0, dO, LS, n0, kC, lane);
+      warp_mma<TS::NT, true, false, kExactInput<Tin>>(a1, Qhs, LD, m0, dO, LS, n0, kC, lane);
       warp_mma<TS::NT>(a2, Ws, LD, m0, dU, LS, n0, kC, lane);
 #pragma unroll
       for (int nt = 0; nt < TS::NT; ++nt)
@@ -812,7 +783,7 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
       int m0, n0;
       TD::at(warp, m0, n0);
       float acc[TD::NT][4] = {};
-      warp_mma<TD::NT>(acc, dOT, LC, m0, S0T, LD, n0, E, lane);  // dO S0^T
+      warp_mma<TD::NT, true, kExactInput<Tin>>(acc, dOT, LC, m0, S0T, LD, n0, E, lane);  // dO S0^T
       frag_store<TD::NT>(gr + GL.dQh(), D, acc, m0, n0, lane, 1.f);
       float acc2[TD::NT][4] = {};
       warp_mma<TD::NT>(acc2, dUT, LC, m0, S0T, LD, n0, E, lane);  // dU S0^T
@@ -850,7 +821,7 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
       int m0, n0;
       TC::at(warp, m0, n0);
       float acc[TC::NT][4] = {};
-      warp_mma<TC::NT>(acc, dOT, LC, m0, UT, LC, n0, E, lane);  // dO U^T, kept on M's support (s <= r)
+      warp_mma<TC::NT, true, kExactInput<Tin>>(acc, dOT, LC, m0, UT, LC, n0, E, lane);  // dO U^T, on M's support
 #pragma unroll
       for (int nt = 0; nt < TC::NT; ++nt)
 #pragma unroll
@@ -858,7 +829,7 @@ bwd_dvsums(const Tin* __restrict__ v, const Tin* __restrict__ dout, const int32_
           if (frag_row(m0, lane, e) < frag_col(n0, lane, nt, e)) acc[nt][e] = 0.f;
       frag_store<TC::NT>(gr + GL.dM(), kC, acc, m0, n0, lane, 1.f);
       float acc2[TC::NT][4] = {};
-      warp_mma<TC::NT>(acc2, dUT, LC, m0, VT, LC, n0, E, lane);  // dU V^T
+      warp_mma<TC::NT, true, false, kExactInput<Tin>>(acc2, dUT, LC, m0, VT, LC, n0, E, lane);  // dU V^T
       frag_store<TC::NT>(gr + GL.dT1(), kC, acc2, m0, n0, lane, 1.f);
     }
     __syncthreads();
