@@ -70,3 +70,17 @@ def test_splits_keep_fp32_range():
             hi, lo = split(x)
             assert np.isfinite(hi) and hi != 0 and abs(float(hi) + float(lo) - float(x)) <= 2.0 ** -15 * float(x)
     assert np.finfo(np.float16).max < np.exp(80.0) and np.finfo(np.float16).tiny > np.exp(-80.0)
+
+
+def test_widened_bf16_values_are_exact_in_tf32():
+    """A bf16 input widened to fp32 has its low 16 bits zero, so the tf32 split gives hi = x and
+    lo = 0 exactly.  The backward (and nothing else) relies on it to skip the product term that would
+    multiply such an operand's lo: the term adds exactly zero, and the gradients are bit-identical."""
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal(50000) * np.exp(rng.uniform(-30, 30, 50000))).astype(np.float32)
+    xb = _bf16_round(x)
+    hi, lo = _split_tf32(xb)
+    assert np.array_equal(hi.view(np.uint32), xb.view(np.uint32)) and np.all(lo == 0)
+    # a general fp32 value is not: the split's lo carries its low mantissa bits
+    h2, l2 = _split_tf32(x)
+    assert np.count_nonzero(l2) > 0.99 * x.size
